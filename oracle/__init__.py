@@ -1,0 +1,169 @@
+"""CPU oracle for the quantized decode GEMV path -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library never does, and it
+shares no code with it.
+
+The arithmetic lives in ``oracle.c`` (plain scalar C, -O2 -ffp-contract=off);
+this module compiles it with gcc into ``oracle/_lib/liboracle.so`` and wraps it
+with numpy-array helpers.  Every routine cites the passage it follows in
+``oracle.c``.  The fp64 tolerance scale ``S`` and the exact block sums make the
+comparison rules of the parity tests explicit:
+
+  * quantized activations (q bytes and fp16 scale bits): bit-exact;
+  * per-block integer sums: bit-exact;
+  * fp32 outputs: |y_gpu - y_ref| <= 1e-5 * S elementwise, S = sum_b |d_w d_x isum_b|.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIBDIR = os.path.join(_HERE, "_lib")
+_LIB = os.path.join(_LIBDIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+QK = 32
+Q4_BLOCK = 18
+Q8_BLOCK = 34
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (host arch, no SIMD flags)."""
+    os.makedirs(_LIBDIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           "-std=c11", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = ctypes.CDLL(_LIB)
+            c_i64, c_f, c_p = ctypes.c_int64, ctypes.c_float, ctypes.c_void_p
+            L.orc_f16_to_f32.argtypes = [ctypes.c_uint16]
+            L.orc_f16_to_f32.restype = c_f
+            L.orc_f32_to_f16.argtypes = [c_f]
+            L.orc_f32_to_f16.restype = ctypes.c_uint16
+            L.orc_quantize_q4_0.argtypes = [c_p, c_i64, c_i64, c_p]
+            L.orc_quantize_q4_0.restype = None
+            L.orc_rms_scale.argtypes = [c_p, c_i64, c_f]
+            L.orc_rms_scale.restype = c_f
+            L.orc_quantize_q8_0.argtypes = [c_p, c_i64, c_p, c_f, c_i64, c_i64, c_p]
+            L.orc_quantize_q8_0.restype = None
+            L.orc_block_sums.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p]
+            L.orc_block_sums.restype = None
+            L.orc_matvec.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_i64, c_p, c_p, c_p]
+            L.orc_matvec.restype = None
+            _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def f16_to_f32(h: int) -> float:
+    return float(lib().orc_f16_to_f32(int(h) & 0xFFFF))
+
+
+def f32_to_f16(f: float) -> int:
+    return int(lib().orc_f32_to_f16(float(np.float32(f))))
+
+
+def quantize_q4_0(w: np.ndarray) -> np.ndarray:
+    """fp32 [O][K] -> uint8 [O][K/32*18] (Q4_0 blocks, row-major)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    O, K = w.shape
+    assert K % QK == 0
+    out = np.empty((O, K // QK * Q4_BLOCK), dtype=np.uint8)
+    lib().orc_quantize_q4_0(_ptr(w), O, K, _ptr(out))
+    return out
+
+
+def rms_scale(x: np.ndarray, eps: float) -> float:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return float(lib().orc_rms_scale(_ptr(x), x.shape[-1], float(np.float32(eps))))
+
+
+def quantize_q8_0(x: np.ndarray, gamma: np.ndarray | None, eps: float = 1e-6) -> np.ndarray:
+    """fp32 [N][K] (or [K]) -> uint8 [N][K/32*34] Q8_0 blocks; gamma=None = no norm."""
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
+    N, K = x.shape
+    assert K % QK == 0
+    g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float32)
+    out = np.empty((N, K // QK * Q8_BLOCK), dtype=np.uint8)
+    lib().orc_quantize_q8_0(_ptr(x), K, _ptr(g), float(np.float32(eps)), K, N, _ptr(out))
+    return out
+
+
+def block_sums(Wq: np.ndarray, xq: np.ndarray, K: int) -> np.ndarray:
+    """int32 [N][O][K/32] exact block sums."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    xq = np.ascontiguousarray(np.atleast_2d(xq), dtype=np.uint8)
+    O = Wq.shape[0]
+    N = xq.shape[0]
+    out = np.empty((N, O, K // QK), dtype=np.int32)
+    lib().orc_block_sums(_ptr(Wq), _ptr(xq), O, K, N, _ptr(out))
+    return out
+
+
+def matvec(Wq: np.ndarray, xq: np.ndarray, K: int, rows: np.ndarray | None = None,
+           threads: int = 1):
+    """Reference y for N vectors: returns (y32 [N][R], y64 [N][R], S [N][R]).
+
+    ``rows`` restricts the evaluation to the given row indices of Wq (R of
+    them); otherwise all O rows.  ``threads`` > 1 splits rows over Python
+    threads (the C call releases the GIL); results do not depend on it.
+    """
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    xq = np.ascontiguousarray(np.atleast_2d(xq), dtype=np.uint8)
+    O = Wq.shape[0]
+    N = xq.shape[0]
+    if rows is None:
+        rows = np.arange(O, dtype=np.int64)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    R = rows.shape[0]
+    y32 = np.empty((N, R), dtype=np.float32)
+    y64 = np.empty((N, R), dtype=np.float64)
+    S = np.empty((N, R), dtype=np.float64)
+    L = lib()
+
+    def run(lo, hi):
+        if hi <= lo:
+            return
+        sub = np.ascontiguousarray(rows[lo:hi])
+        a = np.empty((N, hi - lo), dtype=np.float32)
+        b = np.empty((N, hi - lo), dtype=np.float64)
+        c = np.empty((N, hi - lo), dtype=np.float64)
+        L.orc_matvec(_ptr(Wq), _ptr(xq), O, K, N, _ptr(sub), hi - lo, _ptr(a), _ptr(b), _ptr(c))
+        y32[:, lo:hi] = a
+        y64[:, lo:hi] = b
+        S[:, lo:hi] = c
+
+    if threads <= 1 or R < 2 * threads:
+        run(0, R)
+    else:
+        bounds = np.linspace(0, R, threads + 1).astype(np.int64)
+        ts = [threading.Thread(target=run, args=(int(bounds[i]), int(bounds[i + 1])))
+              for i in range(threads)]
+        for t in ts:
+            t.start()
+        for t in ts:
+            t.join()
+    return y32, y64, S

@@ -1,0 +1,303 @@
+/*
+ * oracle.c -- plain scalar CPU oracle for the quantized decode GEMV path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  It shares no code,
+ * header, table or constant with the CUDA library: every routine below is a
+ * direct, slow restatement of what the method computes, in plain loops,
+ * compiled with -O2 -ffp-contract=off so that every fp32 operation rounds
+ * exactly once, where written.
+ *
+ * What the method computes (sources, by page title and section):
+ *  - Decode multiplies a quantized weight matrix by one activation vector
+ *    ("mmvq"), prefill by many ("mmq")  [GGML: Backend abstraction and
+ *    hardware acceleration, section "CUDA: mmvq, mmq, cublas -- three matrix
+ *    paths", shape-dispatch table].
+ *  - The arithmetic convention is Q4 weights x Q8 activations on every
+ *    backend  [same page, sections "Metal and Vulkan" and "How hardware choice
+ *    maps onto the stack"].
+ *  - The activation entering a projection is the output of RMS_NORM followed
+ *    by MUL with a weight vector gamma, a pattern the Metal backend fuses
+ *    [llama.cpp b10909: Metal backend fusion-table refactor, fixes ~5% token
+ *    generation regression, introduction and section "CI and related fixes"].
+ *  - The norm's epsilon sits where GGML puts it: added to the mean square,
+ *    inside the square root  [llama.cpp b10981: OpenVINO backend optimises
+ *    stateful decode and GPU MoE inference, section "NPU cacheless encoder
+ *    models and norm optimisation"].
+ *
+ * Block formats (the library's reading of the Q4/Q8 convention; 32-element
+ * blocks, little-endian):
+ *  Q4_0 block, 18 bytes: fp16 scale d, then 16 bytes; byte j holds element j
+ *       in its low nibble and element j+16 in its high nibble; value of
+ *       element = d * (q - 8), q in 0..15.
+ *  Q8_0 block, 34 bytes: fp16 scale d, then 32 int8 q; value = d * q.
+ *
+ * Parity pins: every function here is checked in tests/test_oracle_pins.py
+ * against values the mathematics fixes (IEEE binary16 encodings from numpy,
+ * closed forms, round-trip bounds, exact rational brute force on tiny
+ * shapes, special blocks).  The bitwise summation order of the RMS statistic
+ * is a convention of this library (fixed below); its value is pinned to the
+ * fp64 definition within a few ulp.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#include <fenv.h>
+
+#define QK 32
+
+/* ---------------------------------------------------------------------- */
+/* IEEE 754 binary16 <-> binary32, from the format's definition.           */
+/* ---------------------------------------------------------------------- */
+
+float orc_f16_to_f32(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 31;
+    int m = h & 1023;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);                 /* subnormal: m * 2^-24 */
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);     /* (1 + m/1024) * 2^(e-15) */
+    return (float)(sign ? -v : v);
+}
+
+/* Round to nearest, ties to even; overflow to infinity. */
+uint16_t orc_f32_to_f16(float f)
+{
+    uint16_t sign = signbit(f) ? 0x8000u : 0u;
+    if (isnan(f))
+        return (uint16_t)(sign | 0x7E00u);
+    double a = fabs((double)f);
+    /* 65520 is the midpoint between the largest finite value 65504 and 2^16;
+       ties go to the even significand, which is the (infinite) 2^16. */
+    if (a >= 65520.0)
+        return (uint16_t)(sign | 0x7C00u);
+    if (a == 0.0)
+        return sign;
+    int e2;
+    frexp(a, &e2);                  /* a = f * 2^e2, f in [0.5, 1) */
+    int ex = e2 - 1;                /* floor(log2 a) */
+    if (ex < -14)
+        ex = -14;                   /* subnormal range has quantum 2^-24 */
+    double quantum = ldexp(1.0, ex - 10);
+    double n = a / quantum;         /* exact: division by a power of two */
+    int old = fegetround();
+    fesetround(FE_TONEAREST);
+    double r = nearbyint(n);        /* ties to even */
+    fesetround(old);
+    long ri = (long)r;
+    if (ex == -14 && ri < 1024)
+        return (uint16_t)(sign | (uint16_t)ri);           /* subnormal (or min normal reached below) */
+    if (ri == 2048) {               /* rounding carried into the next binade */
+        ri = 1024;
+        ex += 1;
+    }
+    if (ex + 15 >= 31)
+        return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (uint16_t)((ex + 15) << 10) | (uint16_t)(ri - 1024));
+}
+
+static uint16_t rd_u16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static void wr_u16(uint8_t* p, uint16_t v) { p[0] = (uint8_t)(v & 0xFF); p[1] = (uint8_t)(v >> 8); }
+
+/* ---------------------------------------------------------------------- */
+/* Q4_0 weight quantization (input preparation).                           */
+/* Per block: m = the element of largest magnitude (first one on ties),     */
+/* d = m / -8 (fp32), q = min(15, floor(w/d + 8.5)), stored d = fp16(d).    */
+/* An all-zero block stores d = 0 and q = 8 everywhere.                     */
+/* ---------------------------------------------------------------------- */
+void orc_quantize_q4_0(const float* w, int64_t rows, int64_t K, uint8_t* out)
+{
+    const int64_t nb = K / QK;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float* v = w + r * K + b * QK;
+            uint8_t* blk = out + (r * nb + b) * 18;
+            float amax = 0.0f, m = 0.0f;
+            for (int j = 0; j < QK; ++j) {
+                if (fabsf(v[j]) > amax) {
+                    amax = fabsf(v[j]);
+                    m = v[j];
+                }
+            }
+            float d = m / -8.0f;
+            int q[QK];
+            for (int j = 0; j < QK; ++j) {
+                if (d == 0.0f) {
+                    q[j] = 8;
+                } else {
+                    float t = v[j] / d;
+                    t = t + 8.5f;
+                    int qi = (int)t;            /* t >= 0.5 here, so this is floor */
+                    q[j] = qi > 15 ? 15 : (qi < 0 ? 0 : qi);
+                }
+            }
+            wr_u16(blk, orc_f32_to_f16(d));
+            for (int j = 0; j < 16; ++j)
+                blk[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+        }
+    }
+}
+
+/* Element j (0..31) of a Q4_0 block, as the code q in 0..15. */
+static int q4_code(const uint8_t* blk, int j)
+{
+    uint8_t byte = blk[2 + (j & 15)];
+    return j < 16 ? (byte & 0x0F) : (byte >> 4);
+}
+
+/* ---------------------------------------------------------------------- */
+/* RMS statistic s = 1 / sqrt(mean(x^2) + eps)  (fp32).                     */
+/*                                                                          */
+/* fp32 sums depend on their order, and bit-exact quantized activations     */
+/* need one fixed order.  This library fixes it as follows:                 */
+/*   partial[j], j = 0..255: x_i^2 accumulated with fused multiply-add over */
+/*     i = j, j+256, j+512, ... in ascending order, starting from 0;        */
+/*   the 256 partials form 8 groups of 32; within a group, five rounds of   */
+/*     pairwise sums t[l] <- t[l] + t[l xor h] for h = 16, 8, 4, 2, 1 leave  */
+/*     the group total in t[0];                                             */
+/*   ss = ((g0+g1)+(g2+g3)) + ((g4+g5)+(g6+g7));                             */
+/*   mean = ss / K, s = 1 / sqrt(mean + eps), each one IEEE fp32 operation. */
+/* ---------------------------------------------------------------------- */
+float orc_rms_scale(const float* x, int64_t K, float eps)
+{
+    float partial[256];
+    for (int j = 0; j < 256; ++j) {
+        float acc = 0.0f;
+        for (int64_t i = j; i < K; i += 256)
+            acc = fmaf(x[i], x[i], acc);
+        partial[j] = acc;
+    }
+    float g[8];
+    for (int grp = 0; grp < 8; ++grp) {
+        float t[32], u[32];
+        for (int l = 0; l < 32; ++l)
+            t[l] = partial[grp * 32 + l];
+        for (int h = 16; h >= 1; h >>= 1) {
+            for (int l = 0; l < 32; ++l)
+                u[l] = t[l] + t[l ^ h];
+            for (int l = 0; l < 32; ++l)
+                t[l] = u[l];
+        }
+        g[grp] = t[0];
+    }
+    float ss = ((g[0] + g[1]) + (g[2] + g[3])) + ((g[4] + g[5]) + (g[6] + g[7]));
+    float mean = ss / (float)K;
+    float denom = sqrtf(mean + eps);
+    return 1.0f / denom;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Activation -> Q8_0, optionally through RMS_NORM then MUL by gamma.       */
+/*  gamma != NULL: v_i = (x_i * s) * gamma_i   (two fp32 products, in that   */
+/*                 order: normalise, then multiply)                         */
+/*  gamma == NULL: v_i = x_i (plain quantization, no norm)                   */
+/* Per block: amax = max |v|, d = amax / 127 (fp32), q = round(v / d) with   */
+/* halves away from zero, clamped to [-127, 127]; d == 0 gives q = 0; the   */
+/* stored scale is fp16(d), round to nearest even.                          */
+/* x is [N][ldx] (row n = one vector); xq is [N][K/32] blocks.              */
+/* ---------------------------------------------------------------------- */
+void orc_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float eps,
+                       int64_t K, int64_t N, uint8_t* xq)
+{
+    const int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; ++n) {
+        const float* xn = x + n * ldx;
+        float s = gamma ? orc_rms_scale(xn, K, eps) : 1.0f;
+        for (int64_t b = 0; b < nb; ++b) {
+            float v[QK];
+            for (int j = 0; j < QK; ++j) {
+                int64_t i = b * QK + j;
+                if (gamma) {
+                    float t = xn[i] * s;
+                    v[j] = t * gamma[i];
+                } else {
+                    v[j] = xn[i];
+                }
+            }
+            float amax = 0.0f;
+            for (int j = 0; j < QK; ++j)
+                if (fabsf(v[j]) > amax)
+                    amax = fabsf(v[j]);
+            float d = amax / 127.0f;
+            uint8_t* blk = xq + (n * nb + b) * 34;
+            wr_u16(blk, orc_f32_to_f16(d));
+            for (int j = 0; j < QK; ++j) {
+                int q = 0;
+                if (d != 0.0f) {
+                    float r = roundf(v[j] / d);
+                    if (r > 127.0f) r = 127.0f;
+                    if (r < -127.0f) r = -127.0f;
+                    q = (int)r;
+                }
+                blk[2 + j] = (uint8_t)(int8_t)q;
+            }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Exact per-block integer sums isum[n][o][b] = sum_j (qw_j - 8) * qx_j.     */
+/* ---------------------------------------------------------------------- */
+void orc_block_sums(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64_t N,
+                    int32_t* isum)
+{
+    const int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t o = 0; o < O; ++o)
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = W + (o * nb + b) * 18;
+                const uint8_t* xb = xq + (n * nb + b) * 34;
+                int32_t acc = 0;
+                for (int j = 0; j < QK; ++j)
+                    acc += (q4_code(wb, j) - 8) * (int32_t)(int8_t)xb[2 + j];
+                isum[(n * O + o) * nb + b] = acc;
+            }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Reference product: dequantize both operands and take the dot product in  */
+/* fp64:  y[n][o] = sum_b sum_j (d_w * (qw_j - 8)) * (d_x * qx_j).           */
+/* Each term is exact in fp64 (11+4 by 11+8 significant bits), so y64 is     */
+/* the exact value up to fp64 summation rounding; y32 = (float)y64.          */
+/* S[n][o] = sum_b |d_w * d_x * isum_b| is the magnitude that scales the     */
+/* output tolerance.                                                        */
+/* rows: optional list of nrows row indices to evaluate (NULL = all O).     */
+/* Outputs are [N][nrows].                                                  */
+/* ---------------------------------------------------------------------- */
+void orc_matvec(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64_t N,
+                const int64_t* rows, int64_t nrows, float* y32, double* y64, double* S)
+{
+    const int64_t nb = K / QK;
+    if (!rows)
+        nrows = O;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t t = 0; t < nrows; ++t) {
+            int64_t o = rows ? rows[t] : t;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = W + (o * nb + b) * 18;
+                const uint8_t* xb = xq + (n * nb + b) * 34;
+                double dw = (double)orc_f16_to_f32(rd_u16(wb));
+                double dx = (double)orc_f16_to_f32(rd_u16(xb));
+                double blk = 0.0;
+                int64_t isum = 0;
+                for (int j = 0; j < QK; ++j) {
+                    double wv = dw * (double)(q4_code(wb, j) - 8);
+                    double xv = dx * (double)(int8_t)xb[2 + j];
+                    blk += wv * xv;
+                    isum += (int64_t)(q4_code(wb, j) - 8) * (int64_t)(int8_t)xb[2 + j];
+                }
+                acc += blk;
+                mag += fabs(dw * dx * (double)isum);
+            }
+            if (y32) y32[n * nrows + t] = (float)acc;
+            if (y64) y64[n * nrows + t] = acc;
+            if (S) S[n * nrows + t] = mag;
+        }
+    }
+}

@@ -1,0 +1,56 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a private copy of oracle.c (on the CPU, in a
+temporary directory), rebuilds it and runs the pin suite against it; the
+suite has to fail.  This shows the pins are not just re-stating the oracle.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    "nibble_order_swapped": ("return j < 16 ? (byte & 0x0F) : (byte >> 4);",
+                             "return j < 16 ? (byte >> 4) : (byte & 0x0F);"),
+    "q4_offset_dropped_in_sums": ("acc += (q4_code(wb, j) - 8) * (int32_t)(int8_t)xb[2 + j];",
+                                  "acc += q4_code(wb, j) * (int32_t)(int8_t)xb[2 + j];"),
+    "eps_outside_sqrt": ("float denom = sqrtf(mean + eps);", "float denom = sqrtf(mean) + eps;"),
+    "gamma_dropped": ("v[j] = t * gamma[i];", "v[j] = t;"),
+    "q8_scale_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
+    "q8_truncation": ("float r = roundf(v[j] / d);", "float r = truncf(v[j] / d);"),
+    "q4_scale_sign": ("float d = m / -8.0f;", "float d = m / 8.0f;"),
+    "activation_column_ignored": ("const uint8_t* xb = xq + (n * nb + b) * 34;\n                double dw",
+                                  "const uint8_t* xb = xq + (b) * 34;\n                double dw"),
+    "f16_truncating": ("double r = nearbyint(n);", "double r = floor(n);"),
+    "mean_over_k_minus_1": ("float mean = ss / (float)K;", "float mean = ss / (float)(K - 1);"),
+    "weight_scale_dropped": ("blk += wv * xv;", "blk += (double)(q4_code(wb, j) - 8) * xv;"),
+}
+
+
+def _mutated_tree(tmp, name):
+    find, repl = MUTATIONS[name]
+    dst = os.path.join(tmp, name)
+    os.makedirs(os.path.join(dst, "oracle"))
+    shutil.copytree(os.path.join(ROOT, "tests"), os.path.join(dst, "tests"),
+                    ignore=shutil.ignore_patterns("__pycache__", "test_oracle_mutations.py"))
+    shutil.copy(os.path.join(ROOT, "oracle", "__init__.py"), os.path.join(dst, "oracle"))
+    src = open(os.path.join(ROOT, "oracle", "oracle.c")).read()
+    assert src.count(find) == 1, name
+    open(os.path.join(dst, "oracle", "oracle.c"), "w").write(src.replace(find, repl))
+    return dst
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(tmp_path, name):
+    dst = _mutated_tree(str(tmp_path), name)
+    env = dict(os.environ)
+    env["PYTHONPATH"] = dst
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(dst, "tests", "test_oracle_pins.py")],
+                       cwd=dst, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0, f"mutation {name} survived the pins:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout

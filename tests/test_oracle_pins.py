@@ -1,0 +1,341 @@
+"""Pins for the CPU oracle: values fixed by mathematics or by hand, not by the oracle.
+
+Each test ties one oracle routine to something independent of it: IEEE
+binary16 encodings (numpy), closed forms, hand-derived blocks in
+tests/golden/, exact rational arithmetic on tiny shapes, round-trip bounds,
+special blocks and symmetry.  A dropped term, wrong sign, wrong nibble order,
+transposed operand or misplaced epsilon fails at least one of them.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_blocks.json")
+
+
+def golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+# ---------------------------------------------------------------- helpers
+def unpack_q4(Wq, K):
+    """Independent vectorised unpack: codes [O][K] in 0..15 and scales [O][K/32]."""
+    O = Wq.shape[0]
+    blk = Wq.reshape(O, K // 32, 18)
+    d = blk[:, :, 0:2].copy().view(np.float16)[:, :, 0].astype(np.float64)
+    qs = blk[:, :, 2:]
+    lo = (qs & 0x0F).astype(np.int64)
+    hi = (qs >> 4).astype(np.int64)
+    codes = np.concatenate([lo, hi], axis=2).reshape(O, K)
+    return codes, d
+
+
+def unpack_q8(xq, K):
+    N = xq.shape[0]
+    blk = xq.reshape(N, K // 32, 34)
+    d = blk[:, :, 0:2].copy().view(np.float16)[:, :, 0].astype(np.float64)
+    q = blk[:, :, 2:].view(np.int8).astype(np.int64).reshape(N, K)
+    return q, d
+
+
+def ulp32(v):
+    return float(np.spacing(np.float32(abs(v))))
+
+
+# ---------------------------------------------------------------- fp16
+def test_f16_to_f32_all_patterns(orc):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([orc.f16_to_f32(int(b)) for b in bits], dtype=np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def test_f32_to_f16_matches_ieee(orc):
+    rng = np.random.default_rng(7)
+    vals = [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.99, 65520.0, 1e9, -1e9,
+            2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0000001, 3 * 2.0 ** -26, 2.0 ** -14,
+            2.0 ** -14 - 2.0 ** -25, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 0.1, 1 / 127]
+    vals += list(rng.standard_normal(3000) * 10.0 ** rng.integers(-9, 6, 3000))
+    # exact ties in the normal and subnormal ranges
+    m = rng.integers(1024, 2048, 500)
+    e = rng.integers(-14, 15, 500)
+    vals += list((m + 0.5) * 2.0 ** (e - 10))
+    vals += list((rng.integers(0, 1024, 200) + 0.5) * 2.0 ** -24)
+    v32 = np.array(vals, dtype=np.float32)
+    ref = v32.astype(np.float16).view(np.uint16)
+    got = np.array([orc.f32_to_f16(float(v)) for v in v32], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+# ---------------------------------------------------------------- Q4_0
+def test_q4_golden_block(orc):
+    g = golden()["q4_weights"]
+    w = np.array(g["w"], dtype=np.float32).reshape(1, 32)
+    out = orc.quantize_q4_0(w)
+    assert list(out[0]) == g["bytes"]
+    codes, d = unpack_q4(out, 32)
+    assert list(codes[0]) == g["q"]
+    assert out[0, :2].view(np.uint16)[0] == g["d_bits"]
+
+
+def test_q4_invariants_random(orc):
+    rng = np.random.default_rng(11)
+    O, K = 64, 256
+    w = (rng.standard_normal((O, K)) * 0.02).astype(np.float32)
+    w[3, 32:64] = 0.0                                  # an all-zero block
+    w[5, 0:32] = 0.01                                  # ties on the max magnitude
+    w[5, 7] = -0.01
+    Wq = orc.quantize_q4_0(w)
+    codes, d16 = unpack_q4(Wq, K)
+    blocks = w.reshape(O, K // 32, 32).astype(np.float64)
+    cb = codes.reshape(O, K // 32, 32)
+    # all-zero block: d = 0, every code 8
+    assert d16[3, 1] == 0.0 and np.all(cb[3, 1] == 8)
+    # ties: the first element of largest magnitude sets the sign of d (w=+0.01 first -> d<0)
+    assert d16[5, 0] < 0 and cb[5, 0, 0] == 0 and cb[5, 0, 7] == 15
+    for o in range(O):
+        for b in range(K // 32):
+            v = blocks[o, b]
+            if not np.any(v):
+                continue
+            i = int(np.argmax(np.abs(v)))               # first on ties
+            m = v[i]
+            d = np.float32(np.float32(m) / np.float32(-8.0))
+            # the extreme element maps to code 0 and d has the opposite sign of m
+            assert cb[o, b, i] == 0
+            assert np.sign(d16[o, b]) == -np.sign(m)
+            assert d16[o, b] == float(np.float16(d))
+            # round trip with the fp32 scale: within d/2 (+ fp32 slop) unless clamped at 15
+            err = np.abs(v - float(d) * (cb[o, b] - 8))
+            clamped = cb[o, b] == 15
+            assert np.all(err[~clamped] <= abs(float(d)) * (0.5 + 2 ** -17))
+            assert np.all(err[clamped] <= abs(float(d)) * (1.0 + 2 ** -17))
+
+
+# ---------------------------------------------------------------- RMS statistic
+@pytest.mark.parametrize("K", [32, 256, 2048, 4096, 14336])
+def test_rms_scale_vs_fp64(orc, K):
+    rng = np.random.default_rng(K)
+    for scale in (1.0, 1e-3, 30.0):
+        x = (rng.standard_normal(K) * scale).astype(np.float32)
+        eps = 1e-6
+        ref = 1.0 / math.sqrt(float(np.mean(x.astype(np.float64) ** 2)) + eps)
+        got = orc.rms_scale(x, eps)
+        bound = (K / 256 + 12) * 2.0 ** -24
+        assert abs(got - ref) <= bound * ref, (scale, got, ref)
+
+
+def test_rms_eps_inside_sqrt(orc):
+    g = golden()["norm_eps_position"]
+    x = np.full(g["K"], g["x_value"], dtype=np.float32)
+    s = orc.rms_scale(x, g["eps"])
+    assert abs(s - g["s"]) <= 2e-6 * g["s"]
+    # the other placement would be far away
+    assert abs(s - 1.0 / (math.sqrt(1e-6) + 1e-6)) > 100
+
+
+# ---------------------------------------------------------------- Q8_0
+def test_q8_golden_plain(orc):
+    g = golden()["q8_plain"]
+    xq = orc.quantize_q8_0(np.array(g["x"], dtype=np.float32), None)
+    q, d = unpack_q8(xq, 32)
+    assert xq[0, :2].view(np.uint16)[0] == g["d_bits"]
+    assert list(q[0]) == g["q"]
+
+
+@pytest.mark.parametrize("case", ["norm_constant", "norm_eps_position"])
+def test_q8_golden_norm(orc, case):
+    g = golden()[case]
+    K = g["K"]
+    x = np.full((1, K), g["x_value"], dtype=np.float32)
+    xq = orc.quantize_q8_0(x, np.ones(K, np.float32), g["eps"])
+    q, d = unpack_q8(xq, K)
+    assert np.all(q == g["q_value"])
+    assert np.all(xq.reshape(1, K // 32, 34)[:, :, :2].copy().view(np.uint16) == g["d_bits"])
+
+
+def test_q8_roundtrip_bound_plain(orc):
+    rng = np.random.default_rng(3)
+    N, K = 4, 1024
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    x[1, 64:96] = 0.0
+    x[2, :] *= 20.0
+    xq = orc.quantize_q8_0(x, None)
+    q, d16 = unpack_q8(xq, K)
+    xb = x.reshape(N, K // 32, 32).astype(np.float64)
+    qb = q.reshape(N, K // 32, 32)
+    amax = np.abs(xb).max(axis=2)
+    d32 = (amax.astype(np.float32) / np.float32(127.0)).astype(np.float64)
+    # stored scale is the fp16 rounding of amax/127
+    assert np.array_equal(d16, d32.astype(np.float16).astype(np.float64))
+    # zero block
+    assert np.all(qb[1, 2] == 0) and d16[1, 2] == 0.0
+    # the extreme element reaches |q| = 127, nothing exceeds it
+    nz = amax > 0
+    assert np.all(np.abs(qb).max(axis=2)[nz] == 127)
+    # round trip |x - d q| <= d/2 with the fp32 scale (plus division rounding)
+    err = np.abs(xb - d32[:, :, None] * qb)
+    assert np.all(err <= d32[:, :, None] * (0.5 + 2 ** -16))
+
+
+def test_q8_norm_scale_equivariance(orc):
+    rng = np.random.default_rng(5)
+    N, K = 3, 4096
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    gam = rng.uniform(0.5, 1.5, K).astype(np.float32)
+    a = orc.quantize_q8_0(x, gam, 1e-6)
+    b = orc.quantize_q8_0(x, gam * np.float32(2.0), 1e-6)
+    qa, da = unpack_q8(a, K)
+    qb, db = unpack_q8(b, K)
+    assert np.array_equal(qa, qb)
+    assert np.array_equal(db, 2.0 * da)
+
+
+def test_q8_norm_matches_definition(orc):
+    """Quantized codes agree with the fp64 definition up to the rounding of v/d."""
+    rng = np.random.default_rng(9)
+    N, K = 2, 4096
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    x[0, rng.choice(K, 40, replace=False)] *= 20.0
+    gam = rng.uniform(0.5, 1.5, K).astype(np.float32)
+    xq = orc.quantize_q8_0(x, gam, 1e-6)
+    q, d16 = unpack_q8(xq, K)
+    x64 = x.astype(np.float64)
+    s = 1.0 / np.sqrt(np.mean(x64 ** 2, axis=1, keepdims=True) + 1e-6)
+    v = (x64 * s * gam).reshape(N, K // 32, 32)
+    d = np.abs(v).max(axis=2) / 127.0
+    ideal = v / d[:, :, None]
+    qb = q.reshape(N, K // 32, 32)
+    assert np.all(np.abs(qb - ideal) <= 0.5 + 1e-4)
+    assert np.allclose(d16, d, rtol=2 ** -11, atol=0)
+
+
+# ---------------------------------------------------------------- block sums / product
+def test_golden_dot(orc):
+    g = golden()
+    W = orc.quantize_q4_0(np.array(g["q4_weights"]["w"], dtype=np.float32).reshape(1, 32))
+    xq = orc.quantize_q8_0(np.array(g["q8_plain"]["x"], dtype=np.float32), None)
+    assert int(orc.block_sums(W, xq, 32)[0, 0, 0]) == g["dot"]["isum"]
+    y32, y64, S = orc.matvec(W, xq, 32)
+    assert y64[0, 0] == g["dot"]["y"] and y32[0, 0] == g["dot"]["y"]
+    assert S[0, 0] == 3.0
+
+
+def random_problem(rng, O, K, N):
+    import oracle
+    w = (rng.standard_normal((O, K)) * 0.02).astype(np.float32)
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    gam = rng.uniform(0.5, 1.5, K).astype(np.float32)
+    return oracle.quantize_q4_0(w), oracle.quantize_q8_0(x, gam, 1e-6)
+
+
+@pytest.mark.parametrize("O,K,N", [(1, 32, 1), (7, 64, 2), (16, 256, 3), (33, 256, 8)])
+def test_block_sums_brute_force(orc, O, K, N):
+    rng = np.random.default_rng(O * 1000 + K + N)
+    Wq, xq = random_problem(rng, O, K, N)
+    codes, _ = unpack_q4(Wq, K)
+    q, _ = unpack_q8(xq, K)
+    ref = np.einsum("obj,nbj->nob", (codes - 8).reshape(O, K // 32, 32),
+                    q.reshape(N, K // 32, 32))
+    got = orc.block_sums(Wq, xq, K)
+    assert got.dtype == np.int32
+    assert np.array_equal(got.astype(np.int64), ref)
+
+
+@pytest.mark.parametrize("O,K,N", [(3, 32, 1), (5, 64, 2), (4, 256, 2)])
+def test_matvec_exact_rational(orc, O, K, N):
+    rng = np.random.default_rng(100 + O + K + N)
+    Wq, xq = random_problem(rng, O, K, N)
+    codes, dw = unpack_q4(Wq, K)
+    q, dx = unpack_q8(xq, K)
+    y32, y64, S = orc.matvec(Wq, xq, K)
+    for n in range(N):
+        for o in range(O):
+            exact = Fraction(0)
+            mag = Fraction(0)
+            for b in range(K // 32):
+                fw = Fraction(float(dw[o, b]))
+                fx = Fraction(float(dx[n, b]))
+                isum = sum(int(codes[o, b * 32 + j] - 8) * int(q[n, b * 32 + j]) for j in range(32))
+                exact += fw * fx * isum
+                mag += abs(fw * fx * isum)
+            assert abs(Fraction(float(y64[n, o])) - exact) <= Fraction(2.0 ** -50) * mag
+            assert abs(float(y32[n, o]) - float(exact)) <= ulp32(float(exact))
+            assert float(S[n, o]) == pytest.approx(float(mag), rel=1e-15)
+
+
+def test_matvec_vs_numpy_dequant(orc):
+    rng = np.random.default_rng(21)
+    O, K, N = 48, 512, 3
+    Wq, xq = random_problem(rng, O, K, N)
+    codes, dw = unpack_q4(Wq, K)
+    q, dx = unpack_q8(xq, K)
+    Wf = (codes - 8).astype(np.float64) * np.repeat(dw, 32, axis=1)
+    Xf = q.astype(np.float64) * np.repeat(dx, 32, axis=1)
+    ref = Xf @ Wf.T                                   # [N][O]
+    y32, y64, S = orc.matvec(Wq, xq, K)
+    assert np.all(np.abs(y64 - ref) <= 1e-12 * S)
+    # row subset and threading give the same numbers
+    rows = np.array([0, 5, 47, 6], dtype=np.int64)
+    a32, a64, aS = orc.matvec(Wq, xq, K, rows=rows, threads=3)
+    assert np.array_equal(a64, y64[:, rows]) and np.array_equal(aS, S[:, rows])
+
+
+def test_special_blocks(orc):
+    """All-zero codes contribute -8 d_w sum(q_x); all-8 contribute 0; all-15 contribute 7 d_w sum(q_x)."""
+    import oracle
+    rng = np.random.default_rng(4)
+    K = 64
+    xq = oracle.quantize_q8_0(rng.standard_normal((1, K)).astype(np.float32), None)
+    q, dx = unpack_q8(xq, K)
+    W = np.zeros((3, K // 32 * 18), dtype=np.uint8)
+    d_bits = np.float16(0.5).view(np.uint16)
+    for r, byte in enumerate((0x00, 0x88, 0xFF)):
+        for b in range(K // 32):
+            W[r, b * 18:b * 18 + 2] = np.array([d_bits], dtype=np.uint16).view(np.uint8)
+            W[r, b * 18 + 2:b * 18 + 18] = byte
+    y32, y64, S = orc.matvec(W, xq, K)
+    sums = q.reshape(K // 32, 32).sum(axis=1)
+    expect = [sum(-8 * 0.5 * dx[0, b] * sums[b] for b in range(K // 32)), 0.0,
+              sum(7 * 0.5 * dx[0, b] * sums[b] for b in range(K // 32))]
+    assert np.allclose(y64[0], expect, rtol=0, atol=1e-12)
+    isum = orc.block_sums(W, xq, K)
+    assert np.array_equal(isum[0, 0], -8 * sums) and np.all(isum[0, 1] == 0)
+    assert np.array_equal(isum[0, 2], 7 * sums)
+
+
+def test_selection_and_permutation(orc):
+    import oracle
+    rng = np.random.default_rng(8)
+    O, K = 6, 256
+    Wq, xq = random_problem(rng, O, K, 1)
+    nb = K // 32
+    isum = orc.block_sums(Wq, xq, K)
+    _, dw = unpack_q4(Wq, K)
+    _, dx = unpack_q8(xq, K)
+    # selection: keep one block per row, neutralise the others with code 8
+    sel = Wq.copy().reshape(O, nb, 18)
+    keep = rng.integers(0, nb, O)
+    for o in range(O):
+        for b in range(nb):
+            if b != keep[o]:
+                sel[o, b, 2:] = 0x88
+    y32, y64, S = orc.matvec(sel.reshape(O, -1), xq, K)
+    for o in range(O):
+        b = keep[o]
+        assert y64[0, o] == dw[o, b] * dx[0, b] * isum[0, o, b]
+    # permutation of K-blocks applied to both operands
+    perm = rng.permutation(nb)
+    Wp = Wq.reshape(O, nb, 18)[:, perm].reshape(O, -1)
+    xp = xq.reshape(1, nb, 34)[:, perm].reshape(1, -1)
+    a = orc.matvec(Wq, xq, K)
+    b = orc.matvec(Wp, xp, K)
+    assert np.all(np.abs(a[1] - b[1]) <= 1e-12 * a[2])
+    assert np.array_equal(orc.block_sums(Wp, xp, K)[0], isum[0][:, perm])
