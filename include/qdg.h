@@ -1,0 +1,185 @@
+/*
+ * qdg.h -- C ABI of the GB300 (sm_103a) quantized decode GEMV library.
+ *
+ * What the library computes.  A decode step multiplies each projection's
+ * quantized weight matrix by one activation vector; prefill multiplies it by
+ * many.  Batch-1 decode goes down the quantized matrix-vector route ("mmvq"),
+ * longer batches down the quantized matrix-matrix route ("mmq")  [GGML:
+ * Backend abstraction and hardware acceleration, section "CUDA: mmvq, mmq,
+ * cublas -- three matrix paths", shape-dispatch table].  Weights are Q4,
+ * activations Q8 on every backend  [same page, sections "Metal and Vulkan"
+ * and "How hardware choice maps onto the stack"].  The activation is first
+ * RMS-normalised and multiplied by gamma (RMS_NORM + MUL), a pair the Metal
+ * backend runs as one fused kernel; losing that fusion cost about 5% of
+ * token-generation speed  [llama.cpp b10909: Metal backend fusion-table
+ * refactor, introduction].  Here the norm, the MUL and the Q8_0 quantization
+ * are one kernel, and the quantized products are three more.
+ *
+ * Formats (32-element blocks, little-endian, packed, no padding):
+ *   Q4_0 block (18 bytes): uint16 fp16 scale d; uint8 qs[16].  Byte j holds
+ *     element j in its low nibble and element j+16 in its high nibble; the
+ *     value of element i is d * (q_i - 8), q_i in 0..15.
+ *   Q8_0 block (34 bytes): uint16 fp16 scale d; int8 q[32]; value d * q_i.
+ *   A Q4_0 matrix of O rows and K columns is row-major: row o holds its K/32
+ *   blocks contiguously (o * K/32 * 18 bytes from the base).  N Q8_0 vectors
+ *   are stored one after another, K/32 blocks each.
+ *
+ * Output.  y[n][o] = sum over blocks b of d_w(o,b) * d_x(n,b) * isum(n,o,b)
+ *   with the exact integer block sum isum = sum_j (q_w - 8) * q_x, computed in
+ *   fp32 from exact products; the result agrees with the exact value within
+ *   1e-5 * sum_b |d_w d_x isum|.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named x, gamma, xq, W, y, w, isum are DEVICE pointers owned by
+ *     the caller; the library never frees or keeps them and allocates no
+ *     device memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  Arguments are validated on the host before anything
+ *     is launched; a rejected call launches nothing and returns a negative
+ *     status.  QDG_ECUDA reports a failed launch (cudaGetLastError).
+ *   - Device-side problems (a bounded wait that gave up, a Q8_0 scale that
+ *     overflowed fp16) set a flag on the device; qdg_device_status() reports
+ *     and clears it.
+ *   - No entry point is thread-safe against concurrent qdg_set_option calls.
+ */
+#ifndef QDG_H
+#define QDG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define QDG_API __attribute__((visibility("default")))
+#else
+#define QDG_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* qdg_stream_t;
+
+enum qdg_status {
+    QDG_OK = 0,
+    QDG_EINVAL = -1,    /* null pointer, non-positive size, N out of range, bad option */
+    QDG_EALIGN = -2,    /* a pointer or a leading dimension breaks the required alignment */
+    QDG_ESHAPE = -3,    /* K not a multiple of 32 (256 for the products) or beyond a stated maximum */
+    QDG_ECUDA = -4,     /* a CUDA runtime call failed */
+    QDG_ETIMEOUT = -5,  /* a bounded device-side wait gave up (from qdg_device_status) */
+    QDG_EOVERFLOW = -6  /* a Q8_0 scale exceeded the fp16 range (from qdg_device_status) */
+};
+
+/*
+ * qnorm_quantize_q8_0 -- fused RMS_NORM + MUL(gamma) + Q8_0 quantization.
+ *   [llama.cpp b10909, introduction and section "CI and related fixes"
+ *   (the RMS_NORM+MUL pattern); llama.cpp b10981, section "NPU cacheless
+ *   encoder models and norm optimisation" (epsilon kept where GGML puts it)]
+ *
+ * x      [N][ldx] fp32, vector n at x + n*ldx (ldx >= K; 4-byte aligned).
+ * gamma  [K] fp32, or NULL for plain quantization (no norm: v = x).
+ * eps    >= 0, added to the mean square inside the square root.
+ * K      multiple of 32, 32 <= K <= 1048576.   N >= 1.
+ * xq     [N][K/32] Q8_0 blocks (2-byte aligned).
+ * With gamma: s = 1/sqrt(sum(x^2)/K + eps), v_i = (x_i*s)*gamma_i, each an
+ * IEEE fp32 operation; the sum of squares uses this library's fixed order
+ * (256 strided fused multiply-add chains, then pairwise trees), so results
+ * are bit-reproducible.  Per block: d = max|v|/127, q = round(v/d) (halves
+ * away from zero), stored d = fp16(d) rounded to nearest even; d = 0 stores
+ * q = 0.  A block whose d exceeds the fp16 range stores an infinite scale
+ * and sets QDG_EOVERFLOW on the device.
+ */
+QDG_API int qnorm_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float eps,
+                        int64_t K, int64_t N, void* xq, qdg_stream_t stream);
+
+/*
+ * q4_0_q8_0_gemv -- y = W * x for one Q8_0 vector (batch-1 decode, the
+ * "mmvq" route)  [GGML: Backend abstraction and hardware acceleration,
+ * section "CUDA: mmvq, mmq, cublas -- three matrix paths"].
+ *
+ * W   [O][K/32] Q4_0, 16-byte aligned.      xq  [K/32] Q8_0, 4-byte aligned.
+ * y   [O] fp32, 4-byte aligned (overwritten).
+ * K   multiple of 256, 256 <= K <= 32768.   1 <= O < 2^31.
+ * W is streamed once from HBM through a shared-memory ring filled by bulk
+ * asynchronous copies; the result is deterministic (fixed reduction order).
+ */
+QDG_API int q4_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K,
+                   qdg_stream_t stream);
+
+/*
+ * q4_0_q8_0_gemm_small_n -- Y = W * X for 1 <= N <= 8 Q8_0 vectors sharing
+ * one pass over W (speculative / parallel decode; the "vector case" of the
+ * mmvq route)  [same page and section].
+ *
+ * W   [O][K/32] Q4_0, 16-byte aligned.   xq  [N][K/32] Q8_0, 16-byte aligned.
+ * y   [N][ldy] fp32: output vector n at y + n*ldy, ldy >= O.
+ * K   multiple of 256, 256 <= K <= 65536.   1 <= N <= 8.
+ */
+QDG_API int q4_0_q8_0_gemm_small_n(const void* W, const void* xq, float* y, int64_t ldy,
+                           int64_t O, int64_t K, int64_t N, qdg_stream_t stream);
+
+/*
+ * quantize_q4_0 -- weight preparation: fp32 [O][ldw] -> Q4_0 [O][K/32].
+ * Per block: m = the element of largest magnitude (the first one on ties),
+ * d = m / -8 in fp32, q = min(15, floor(w/d + 8.5)), stored d = fp16(d); an
+ * all-zero block stores d = 0 and q = 8.  Runs once at load time, not on the
+ * decode path.  K multiple of 32, ldw >= K; Wq 2-byte aligned.
+ */
+QDG_API int quantize_q4_0(const float* w, int64_t ldw, int64_t O, int64_t K, void* Wq,
+                  qdg_stream_t stream);
+
+/*
+ * qdg_device_status -- synchronise `stream`, then read and clear the device
+ * flags of every kernel of this library on the current device.  Returns
+ * QDG_OK, QDG_ETIMEOUT (a bounded wait gave up; that call's output is
+ * incomplete), QDG_EOVERFLOW, or QDG_ECUDA.
+ */
+QDG_API int qdg_device_status(qdg_stream_t stream);
+
+/* Human-readable text for a status code (static storage). */
+QDG_API const char* qdg_status_string(int status);
+
+/*
+ * Options (process-wide).  QDG_OPT_PDL = 1 launches the decode kernels with
+ * programmatic dependent launch: a kernel may start streaming W while the
+ * previous kernel on the stream is still running, and waits for it before
+ * reading activations or writing outputs.  Enable it only when W is not
+ * written by the kernel launched immediately before on the same stream.
+ * Default 0.  Returns QDG_EINVAL for an unknown option.
+ */
+enum qdg_option { QDG_OPT_PDL = 1 };
+QDG_API int qdg_set_option(int option, int64_t value);
+
+/*
+ * qdg_launch_count -- number of kernels this library has launched in this
+ * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
+ * 4 weight quantize, -1 total.  Lets a caller check that the fused kernel
+ * is the one that ran.
+ */
+QDG_API int64_t qdg_launch_count(int which);
+
+/*
+ * qdg_debug_block_sums -- test hook.  Runs the production inner loop of one
+ * product path and writes the exact per-block integer sums
+ * isum[n][o][b] = sum_j (q_w - 8) * q_x  (int32 [N][O][K/32]) instead of y.
+ * path: 0 = gemv (N must be 1), 1 = small-N.
+ * Same argument rules as the corresponding entry point.
+ */
+QDG_API int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum, int64_t O,
+                         int64_t K, int64_t N, int path, qdg_stream_t stream);
+
+/*
+ * qdg_debug_timeout_probe -- test hook for failure detection.  Launches one
+ * kernel that waits on a barrier nothing will complete; its bounded wait
+ * gives up after about two seconds, sets the timeout flag and returns, so a
+ * following qdg_device_status() reports QDG_ETIMEOUT and the context stays
+ * usable.  Faults nothing.
+ */
+QDG_API int qdg_debug_timeout_probe(qdg_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QDG_H */

@@ -1,0 +1,166 @@
+// common.cuh -- shared device helpers of the sm_103a kernels: status flags,
+// hand-written PTX for mbarriers, bulk asynchronous copies and programmatic
+// dependent launch, and the host-side validation helpers of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include <cmath>
+
+#include "../../include/qdg.h"
+
+namespace qdg {
+
+// Device flag bits (per translation unit; qdg_device_status gathers them).
+enum : unsigned { FLAG_TIMEOUT = 1u, FLAG_OVERFLOW = 2u };
+
+// A wait gives up after kWaitNs nanoseconds of the global timer, or after
+// kSpinLimit polls, whichever comes first (legitimate waits take microseconds).
+constexpr uint32_t kSpinLimit = 1u << 24;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the asynchronous (bulk copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait for the phase of `parity` to complete.  False = gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kSpinLimit; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 15u) == 0 && global_ns() - t0 > kWaitNs) return false;
+        if (i >= 32) __nanosleep(128);
+    }
+    return false;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D bulk copy global -> shared (TMA engine), completion counted in bytes
+// on `bar`.  dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Programmatic dependent launch: wait for the preceding grid's memory, and
+// allow the following grid to be scheduled.  No-ops without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
+}
+
+// Bytes 2..5 of the 8-byte little-endian pair (lo, hi).
+__device__ __forceinline__ uint32_t bytes_2_to_5(uint32_t lo, uint32_t hi) { return __byte_perm(lo, hi, 0x5432); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, h));
+    return v;
+}
+
+// ---------------------------------------------------------------- host side
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    size_t smem_optin = 0;
+};
+
+// Per-device properties, cached (one GPU per process in practice).
+DeviceInfo device_info();
+
+bool pdl_enabled();
+void count_launch(int which);
+
+// Launch with the PDL attribute when enabled.
+template <typename Kern, typename... Args>
+cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool allow_pdl,
+                   Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    if (allow_pdl && pdl_enabled()) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Internal launchers shared with the debug hook (dbg != nullptr writes the
+// exact per-block integer sums [N][O][K/32] as the kernel forms them).
+int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
+                int32_t* dbg);
+int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t N,
+                   cudaStream_t stream, int32_t* dbg);
+int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t T,
+                cudaStream_t stream, int32_t* dbg);
+
+// Per-translation-unit device flags: read and clear (synchronises stream).
+unsigned flags_read_clear_quantize(cudaStream_t stream);
+unsigned flags_read_clear_gemv(cudaStream_t stream);
+unsigned flags_read_clear_small_n(cudaStream_t stream);
+unsigned flags_read_clear_gemm(cudaStream_t stream);
+unsigned flags_read_clear_api(cudaStream_t stream);
+
+}  // namespace qdg

@@ -1,0 +1,170 @@
+// quantize.cu -- the fused RMS_NORM + MUL(gamma) -> Q8_0 activation kernel
+// and the load-time fp32 -> Q4_0 weight quantizer.
+//
+// RMS_NORM followed by MUL is the pattern whose fusion the Metal backend
+// lost, costing about 5% of token-generation speed [llama.cpp b10909: Metal
+// backend fusion-table refactor, introduction]; here the two ops and the Q8_0
+// quantization the Q4 x Q8 products need [GGML: Backend abstraction and
+// hardware acceleration, section "Metal and Vulkan"] are a single pass.
+// Epsilon is added to the mean square, inside the square root [llama.cpp
+// b10981, section "NPU cacheless encoder models and norm optimisation"].
+#include "common.cuh"
+
+namespace qdg {
+
+static __device__ unsigned g_flags_quantize;
+
+namespace {
+
+constexpr int kNormThreads = 256;   // the fixed reduction order is defined over 256 lanes
+
+// One CTA per vector.  Thread j sums x_i^2 for i = j (mod 256) with an fma
+// chain in ascending i; warps combine with an xor butterfly (16,8,4,2,1);
+// the 8 warp totals combine as ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).  Then
+// warp w quantizes blocks w, w+8, ... with lane l on element 32b+l.
+__global__ void __launch_bounds__(kNormThreads)
+qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restrict__ gamma, float eps, int K,
+                uint8_t* __restrict__ xq) {
+    pdl_wait();
+    pdl_trigger();
+    const int n = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const float* xn = x + static_cast<int64_t>(n) * ldx;
+    const int nb = K >> 5;
+
+    float s = 1.0f;
+    if (gamma != nullptr) {
+        __shared__ float wsum[kNormThreads / 32];
+        float acc = 0.0f;
+        for (int i = tid; i < K; i += kNormThreads) {
+            const float v = __ldg(xn + i);
+            acc = __fmaf_rn(v, v, acc);
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) wsum[warp] = acc;
+        __syncthreads();
+        const float ss = __fadd_rn(__fadd_rn(__fadd_rn(wsum[0], wsum[1]), __fadd_rn(wsum[2], wsum[3])),
+                                   __fadd_rn(__fadd_rn(wsum[4], wsum[5]), __fadd_rn(wsum[6], wsum[7])));
+        const float mean = __fdiv_rn(ss, static_cast<float>(K));
+        s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+    }
+
+    uint8_t* out = xq + static_cast<int64_t>(n) * nb * 34;
+    for (int b = warp; b < nb; b += kNormThreads / 32) {
+        const int i = (b << 5) + lane;
+        float v = __ldg(xn + i);
+        if (gamma != nullptr) v = __fmul_rn(__fmul_rn(v, s), __ldg(gamma + i));
+        float amax = fabsf(v);
+#pragma unroll
+        for (int h = 16; h >= 1; h >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, h));
+        const float d = __fdiv_rn(amax, 127.0f);
+        int q = 0;
+        if (d != 0.0f) {
+            float r = roundf(__fdiv_rn(v, d));
+            r = fminf(fmaxf(r, -127.0f), 127.0f);
+            q = static_cast<int>(r);
+        }
+        uint8_t* blk = out + static_cast<int64_t>(b) * 34;
+        if (lane == 0) {
+            const __half dh = __float2half_rn(d);
+            *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
+            if (__hisinf(dh)) atomicOr(&g_flags_quantize, FLAG_OVERFLOW);
+        }
+        blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+    }
+}
+
+// One thread per Q4_0 block.
+__global__ void quantize_q4_0_kernel(const float* __restrict__ w, int64_t ldw, int64_t O, int K,
+                                     uint8_t* __restrict__ Wq) {
+    const int nb = K >> 5;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= O * nb) return;
+    const int64_t row = idx / nb;
+    const int b = static_cast<int>(idx - row * nb);
+    const float* v = w + row * ldw + (b << 5);
+    float vals[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) vals[j] = __ldg(v + j);
+    float amax = 0.0f, m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        if (fabsf(vals[j]) > amax) {
+            amax = fabsf(vals[j]);
+            m = vals[j];
+        }
+    }
+    const float d = __fdiv_rn(m, -8.0f);
+    int q[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        if (d == 0.0f) {
+            q[j] = 8;
+        } else {
+            const float t = __fadd_rn(__fdiv_rn(vals[j], d), 8.5f);
+            const int qi = static_cast<int>(t);
+            q[j] = qi > 15 ? 15 : (qi < 0 ? 0 : qi);
+        }
+    }
+    unsigned short* dst = reinterpret_cast<unsigned short*>(Wq + idx * 18);
+    dst[0] = __half_as_ushort(__float2half_rn(d));
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+        const unsigned lo = static_cast<unsigned>(q[j] | (q[j + 16] << 4));
+        const unsigned hi = static_cast<unsigned>(q[j + 1] | (q[j + 17] << 4));
+        dst[1 + j / 2] = static_cast<unsigned short>(lo | (hi << 8));
+    }
+}
+
+}  // namespace
+
+unsigned flags_read_clear_quantize(cudaStream_t stream) {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_flags_quantize, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) !=
+        cudaSuccess)
+        return ~0u;
+    if (cudaMemcpyToSymbolAsync(g_flags_quantize, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+        return ~0u;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ~0u;
+    return v;
+}
+
+}  // namespace qdg
+
+using namespace qdg;
+
+extern "C" int qnorm_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float eps, int64_t K, int64_t N,
+                                   void* xq, qdg_stream_t stream) {
+    if (!x || !xq) return QDG_EINVAL;
+    if (K <= 0 || N <= 0 || ldx < K) return QDG_EINVAL;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
+    if (K % 32 != 0 || K > (1 << 20)) return QDG_ESHAPE;
+    if (N > 0x7fffffff) return QDG_ESHAPE;
+    if (!aligned(x, 4) || !aligned(xq, 2) || (gamma && !aligned(gamma, 4))) return QDG_EALIGN;
+    cudaError_t e = launch(qnorm_q8_kernel, dim3(static_cast<unsigned>(N)), dim3(kNormThreads), 0,
+                           reinterpret_cast<cudaStream_t>(stream), true, x, ldx, gamma, eps, static_cast<int>(K),
+                           static_cast<uint8_t*>(xq));
+    if (e != cudaSuccess) return QDG_ECUDA;
+    count_launch(0);
+    return QDG_OK;
+}
+
+extern "C" int quantize_q4_0(const float* w, int64_t ldw, int64_t O, int64_t K, void* Wq, qdg_stream_t stream) {
+    if (!w || !Wq) return QDG_EINVAL;
+    if (O <= 0 || K <= 0 || ldw < K) return QDG_EINVAL;
+    if (K % 32 != 0 || K > (1 << 20)) return QDG_ESHAPE;
+    if (!aligned(w, 4) || !aligned(Wq, 2)) return QDG_EALIGN;
+    const int64_t blocks = O * (K / 32);
+    const int threads = 256;
+    const int64_t grid = (blocks + threads - 1) / threads;
+    if (grid > 0x7fffffff) return QDG_ESHAPE;
+    cudaError_t e = launch(quantize_q4_0_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0,
+                           reinterpret_cast<cudaStream_t>(stream), false, w, ldw, O, static_cast<int>(K),
+                           static_cast<uint8_t*>(Wq));
+    if (e != cudaSuccess) return QDG_ECUDA;
+    count_launch(4);
+    return QDG_OK;
+}

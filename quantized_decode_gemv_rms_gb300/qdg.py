@@ -1,0 +1,169 @@
+"""Python binding of the C ABI in include/qdg.h (ctypes; argument marshalling only).
+
+Every function here has the name of the C entry point it calls, takes torch
+tensors for the device buffers (PyTorch is only the allocator and the stream
+provider) and raises ``QdgError`` when the library returns a negative status.
+All arithmetic happens in the CUDA kernels of ``libqdg.so``; there is no other
+code path, and importing this module fails loudly if the library cannot be
+built or loaded.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+QK = 32
+Q4_BLOCK = 18
+Q8_BLOCK = 34
+
+QDG_OK = 0
+QDG_EINVAL = -1
+QDG_EALIGN = -2
+QDG_ESHAPE = -3
+QDG_ECUDA = -4
+QDG_ETIMEOUT = -5
+QDG_EOVERFLOW = -6
+QDG_OPT_PDL = 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class QdgError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({status_string(status)})")
+
+
+def lib() -> ctypes.CDLL:
+    """Load libqdg.so (building it in-tree with nvcc when missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            L = ctypes.CDLL(path, mode=ctypes.RTLD_GLOBAL)
+            i64, p, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
+            sig = {
+                "qnorm_quantize_q8_0": ([p, i64, p, f32, i64, i64, p, p], i32),
+                "q4_0_q8_0_gemv": ([p, p, p, i64, i64, p], i32),
+                "q4_0_q8_0_gemm_small_n": ([p, p, p, i64, i64, i64, i64, p], i32),
+                "quantize_q4_0": ([p, i64, i64, i64, p, p], i32),
+                "qdg_device_status": ([p], i32),
+                "qdg_status_string": ([i32], ctypes.c_char_p),
+                "qdg_set_option": ([i32, i64], i32),
+                "qdg_launch_count": ([i32], i64),
+                "qdg_debug_block_sums": ([p, p, p, i64, i64, i64, i32, p], i32),
+                "qdg_debug_timeout_probe": ([p], i32),
+            }
+            if hasattr(L, "q4_0_q8_0_gemm"):
+                sig["q4_0_q8_0_gemm"] = ([p, p, p, i64, i64, i64, i64, p], i32)
+            for name, (args, res) in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().qdg_status_string(int(status)).decode()
+    except OSError:
+        return "unknown"
+
+
+def _check(status: int, what: str) -> None:
+    if status != QDG_OK:
+        raise QdgError(status, what)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def q4_0_nbytes(O: int, K: int) -> int:
+    return O * (K // QK) * Q4_BLOCK
+
+
+def q8_0_nbytes(N: int, K: int) -> int:
+    return N * (K // QK) * Q8_BLOCK
+
+
+# ------------------------------------------------------------------ entry points
+def qnorm_quantize_q8_0(x, gamma, eps: float, xq, K: int | None = None, N: int | None = None,
+                        ldx: int | None = None, stream=None) -> None:
+    """Fused RMSNorm*gamma -> Q8_0 (gamma=None: plain Q8_0).  x fp32 [N][ldx]."""
+    if K is None:
+        K = x.shape[-1]
+    if N is None:
+        N = 1 if x.dim() == 1 else x.shape[0]
+    if ldx is None:
+        ldx = K if x.dim() == 1 else x.stride(0)
+    _check(lib().qnorm_quantize_q8_0(_ptr(x), ldx, _ptr(gamma), float(eps), K, N, _ptr(xq), _stream(stream)),
+           "qnorm_quantize_q8_0")
+
+
+def q4_0_q8_0_gemv(W, xq, y, O: int, K: int, stream=None) -> None:
+    _check(lib().q4_0_q8_0_gemv(_ptr(W), _ptr(xq), _ptr(y), O, K, _stream(stream)), "q4_0_q8_0_gemv")
+
+
+def q4_0_q8_0_gemm_small_n(W, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:
+    _check(lib().q4_0_q8_0_gemm_small_n(_ptr(W), _ptr(xq), _ptr(y), ldy, O, K, N, _stream(stream)),
+           "q4_0_q8_0_gemm_small_n")
+
+
+def q4_0_q8_0_gemm(W, xq, y, ldy: int, O: int, K: int, T: int, stream=None) -> None:
+    L = lib()
+    if not hasattr(L, "q4_0_q8_0_gemm"):
+        raise QdgError(QDG_EINVAL, "q4_0_q8_0_gemm is not in this build of libqdg.so")
+    _check(L.q4_0_q8_0_gemm(_ptr(W), _ptr(xq), _ptr(y), ldy, O, K, T, _stream(stream)), "q4_0_q8_0_gemm")
+
+
+def quantize_q4_0(w, Wq, O: int | None = None, K: int | None = None, ldw: int | None = None,
+                  stream=None) -> None:
+    if O is None:
+        O, K = w.shape
+    if ldw is None:
+        ldw = w.stride(0) if w.dim() == 2 else K
+    _check(lib().quantize_q4_0(_ptr(w), ldw, O, K, _ptr(Wq), _stream(stream)), "quantize_q4_0")
+
+
+def qdg_device_status(stream=None) -> int:
+    return int(lib().qdg_device_status(_stream(stream)))
+
+
+def qdg_set_option(option: int, value: int) -> None:
+    _check(lib().qdg_set_option(option, value), "qdg_set_option")
+
+
+def qdg_launch_count(which: int = -1) -> int:
+    return int(lib().qdg_launch_count(which))
+
+
+def qdg_debug_block_sums(W, xq, isum, O: int, K: int, N: int, path: int, stream=None) -> None:
+    _check(lib().qdg_debug_block_sums(_ptr(W), _ptr(xq), _ptr(isum), O, K, N, path, _stream(stream)),
+           "qdg_debug_block_sums")
+
+
+def qdg_debug_timeout_probe(stream=None) -> None:
+    _check(lib().qdg_debug_timeout_probe(_stream(stream)), "qdg_debug_timeout_probe")

@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+include/qdg.h declares, and rejects bad arguments on the host before any
+CUDA call (no compute call is made here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qdg.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"QDG_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantized_decode_gemv_rms_gb300 import qdg
+    return qdg.lib()
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for must in ("qnorm_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "quantize_q4_0",
+                 "qdg_device_status", "qdg_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), f"libqdg.so does not export {name}"
+
+
+def test_status_strings(L):
+    from quantized_decode_gemv_rms_gb300 import qdg
+    for code in (qdg.QDG_OK, qdg.QDG_EINVAL, qdg.QDG_EALIGN, qdg.QDG_ESHAPE, qdg.QDG_ECUDA,
+                 qdg.QDG_ETIMEOUT, qdg.QDG_EOVERFLOW):
+        assert qdg.status_string(code) not in ("", "unknown status")
+    assert qdg.status_string(12345) == "unknown status"
+
+
+A16 = 0x10000          # fake, 16-byte aligned device addresses: never dereferenced on the host
+A2 = 0x10002           # 2-byte aligned only
+
+
+def test_qnorm_host_validation(L):
+    f = L.qnorm_quantize_q8_0
+    assert f(None, 256, None, 1e-6, 256, 1, A16, None) == -1          # null x
+    assert f(A16, 256, None, 1e-6, 256, 1, None, None) == -1          # null xq
+    assert f(A16, 256, None, 1e-6, 0, 1, A16, None) == -1             # K = 0
+    assert f(A16, 256, None, 1e-6, 256, 0, A16, None) == -1           # N = 0
+    assert f(A16, 100, None, 1e-6, 256, 1, A16, None) == -1           # ldx < K
+    assert f(A16, 256, None, -1.0, 256, 1, A16, None) == -1           # eps < 0
+    assert f(A16, 256, None, float("nan"), 256, 1, A16, None) == -1   # eps NaN
+    assert f(A16, 48, None, 1e-6, 48, 1, A16, None) == -3             # K % 32
+    assert f(A2, 256, None, 1e-6, 256, 1, A16, None) == -2            # x misaligned
+    assert f(A16, 256, A2, 1e-6, 256, 1, A16, None) == -2             # gamma misaligned
+    assert f(A16, 256, None, 1e-6, 256, 1, A16 + 1, None) == -2       # xq misaligned
+
+
+def test_gemv_host_validation(L):
+    f = L.q4_0_q8_0_gemv
+    assert f(None, A16, A16, 8, 256, None) == -1
+    assert f(A16, A16, None, 8, 256, None) == -1
+    assert f(A16, A16, A16, 0, 256, None) == -1
+    assert f(A16, A16, A16, 8, 128, None) == -3       # K % 256
+    assert f(A16, A16, A16, 8, 65536, None) == -3     # K beyond the maximum
+    assert f(A2, A16, A16, 8, 256, None) == -2        # W not 16-byte aligned
+    assert f(A16, A2, A16, 8, 256, None) == -2        # xq not 4-byte aligned
+
+
+def test_small_n_host_validation(L):
+    f = L.q4_0_q8_0_gemm_small_n
+    assert f(A16, A16, A16, 8, 8, 256, 0, None) == -1      # N = 0
+    assert f(A16, A16, A16, 8, 8, 256, 9, None) == -1      # N > 8
+    assert f(A16, A16, A16, 4, 8, 256, 2, None) == -1      # ldy < O
+    assert f(A16, A16, None, 8, 8, 256, 2, None) == -1
+    assert f(A16, A16, A16, 8, 8, 384, 2, None) == -3      # K % 256
+    assert f(A16, A2, A16, 8, 8, 256, 2, None) == -2       # xq must be 16-byte aligned
+
+
+def test_quantize_q4_0_host_validation(L):
+    f = L.quantize_q4_0
+    assert f(None, 32, 1, 32, A16, None) == -1
+    assert f(A16, 16, 1, 32, A16, None) == -1               # ldw < K
+    assert f(A16, 40, 1, 40, A16, None) == -3               # K % 32
+    assert f(A2 + 1, 32, 1, 32, A16, None) == -2
+
+
+def test_options_and_counters(L):
+    assert L.qdg_set_option(99, 1) == -1
+    assert L.qdg_set_option(1, 2) == -1
+    assert L.qdg_set_option(1, 0) == 0
+    assert L.qdg_launch_count(-1) >= 0
+    assert L.qdg_launch_count(7) == -1
+    assert L.qdg_debug_block_sums(A16, A16, None, 8, 256, 1, 0, None) == -1
+    assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 1, 9, None) == -1
+    assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 0, None) == -1   # gemv path needs N == 1
+
+
+def test_binding_names_match_header():
+    from quantized_decode_gemv_rms_gb300 import qdg
+    for name in declared_symbols():
+        if name in ("qdg_status_string",):
+            continue
+        assert hasattr(qdg, name), f"binding lacks {name}"

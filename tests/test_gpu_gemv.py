@@ -1,0 +1,137 @@
+"""GPU parity of the product kernels (batch-1 GEMV and small-N) against the
+CPU oracle: exact per-block integer sums through the test hook, fp32 outputs
+within 1e-5 * sum_b |d_w d_x isum_b|, determinism, PDL on/off."""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_decode_gemv_rms_gb300 import qdg, synth
+from helpers import assert_within_tol, empty_u8, to_dev, to_host, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def problem(seed, O, K, N, norm=True, outliers=0.0):
+    w = synth.weights(seed, "W", O, K)
+    x = synth.activations(seed, "x", N, K, outlier_frac=outliers)
+    gam = synth.gamma(seed, "g", K) if norm else None
+    Wq = oracle.quantize_q4_0(w)
+    xq = oracle.quantize_q8_0(x, gam, 1e-6)
+    return Wq, xq
+
+
+def gpu_gemv(Wq, xq, O, K):
+    torch = torch_cuda()
+    y = torch.empty(O, dtype=torch.float32, device="cuda")
+    qdg.q4_0_q8_0_gemv(to_dev(Wq), to_dev(xq), y, O, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    return to_host(y)
+
+
+def gpu_small_n(Wq, xq, O, K, N, ldy=None):
+    torch = torch_cuda()
+    ldy = O if ldy is None else ldy
+    y = torch.full((N, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    qdg.q4_0_q8_0_gemm_small_n(to_dev(Wq), to_dev(xq), y, ldy, O, K, N)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    out = to_host(y)
+    if ldy > O:
+        assert np.all(np.isnan(out[:, O:])), "wrote past O inside the leading dimension"
+    return out[:, :O]
+
+
+def gpu_block_sums(Wq, xq, O, K, N, path):
+    torch = torch_cuda()
+    isum = torch.full((N, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(to_dev(Wq), to_dev(xq), isum, O, K, N, path)
+    torch.cuda.synchronize()
+    return to_host(isum)
+
+
+GEMV_SHAPES = [(256, 256), (1, 256), (37, 512), (1000, 2048), (152, 4096), (1024, 4096), (153, 4096),
+               (600, 6144), (4096, 14336), (64, 32768), (3000, 768)]
+
+
+@pytest.mark.parametrize("O,K", GEMV_SHAPES)
+def test_gemv_block_sums_exact(O, K):
+    Wq, xq = problem(O * 7 + K, O, K, 1)
+    got = gpu_block_sums(Wq, xq, O, K, 1, 0)
+    assert np.array_equal(got, oracle.block_sums(Wq, xq, K))
+
+
+@pytest.mark.parametrize("O,K", GEMV_SHAPES)
+def test_gemv_output_within_tolerance(O, K):
+    Wq, xq = problem(O * 11 + K, O, K, 1, outliers=0.01)
+    y = gpu_gemv(Wq, xq, O, K)
+    _, y64, S = oracle.matvec(Wq, xq, K, threads=8)
+    assert_within_tol(y[None, :], y64, S)
+
+
+def test_gemv_deterministic_and_pdl_invariant():
+    torch = torch_cuda()
+    O, K = 4096, 4096
+    Wq, xq = problem(77, O, K, 1)
+    Wd, xd = to_dev(Wq), to_dev(xq)
+    outs = []
+    for pdl in (0, 1, 0):
+        qdg.qdg_set_option(qdg.QDG_OPT_PDL, pdl)
+        y = torch.empty(O, dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            qdg.q4_0_q8_0_gemv(Wd, xd, y, O, K)
+        torch.cuda.synchronize()
+        outs.append(to_host(y))
+    qdg.qdg_set_option(qdg.QDG_OPT_PDL, 0)
+    assert all(np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)) for o in outs[1:])
+
+
+def test_gemv_special_blocks():
+    """All-zero codes -> -8 d_w sum(q_x); all-8 -> 0; all-15 -> 7 d_w sum(q_x)."""
+    K = 512
+    O = 3
+    rng = np.random.default_rng(1)
+    xq = oracle.quantize_q8_0(rng.standard_normal((1, K)).astype(np.float32), None)
+    W = np.zeros((O, K // 32 * 18), dtype=np.uint8)
+    d = np.array([np.float16(0.25).view(np.uint16)], dtype=np.uint16).view(np.uint8)
+    for r, byte in enumerate((0x00, 0x88, 0xFF)):
+        for b in range(K // 32):
+            W[r, b * 18:b * 18 + 2] = d
+            W[r, b * 18 + 2:b * 18 + 18] = byte
+    y = gpu_gemv(W, xq, O, K)
+    _, y64, S = oracle.matvec(W, xq, K)
+    assert_within_tol(y[None, :], y64, S)
+    assert y[1] == 0.0
+
+
+SMALLN_SHAPES = [(256, 256), (33, 512), (100, 4096), (1000, 2048), (4096, 14336), (14336, 4096)]
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("O,K", SMALLN_SHAPES)
+def test_small_n_block_sums_exact(O, K, N):
+    if O * K * N > 14336 * 4096 * 2 and N not in (2, 8):
+        pytest.skip("large shapes: N in {2, 8} suffice")
+    Wq, xq = problem(O + K + N, O, K, N)
+    got = gpu_block_sums(Wq, xq, O, K, N, 1)
+    assert np.array_equal(got, oracle.block_sums(Wq, xq, K))
+
+
+@pytest.mark.parametrize("N", [1, 2, 4, 7, 8])
+@pytest.mark.parametrize("O,K", SMALLN_SHAPES)
+def test_small_n_output_within_tolerance(O, K, N):
+    Wq, xq = problem(O * 3 + K + N, O, K, N, outliers=0.01)
+    rows = None if O <= 4096 else synth.sample_indices(O, "rows", O, 2048)
+    y = gpu_small_n(Wq, xq, O, K, N, ldy=O + 5)
+    _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
+    assert_within_tol(y if rows is None else y[:, rows], y64, S)
+
+
+def test_small_n_one_column_matches_gemv_tolerance():
+    O, K = 2048, 4096
+    Wq, xq = problem(5, O, K, 1)
+    a = gpu_gemv(Wq, xq, O, K)
+    b = gpu_small_n(Wq, xq, O, K, 1)[0]
+    _, y64, S = oracle.matvec(Wq, xq, K, threads=8)
+    assert_within_tol(a[None], y64, S)
+    assert_within_tol(b[None], y64, S)
