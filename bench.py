@@ -1,0 +1,538 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark of the Q4_0 x Q8_0 GEMV path with fused RMSNorm -> Q8_0.
+
+One step = one batch-1 decode pass of an 8B-shaped Llama layer stack's
+projections: fused RMSNorm*gamma -> Q8_0 (or plain Q8_0) for each activation,
+then one GEMV per projection (q, k, v, o, gate, up, down, vocab head).  The
+weights (419 MB of Q4_0 per step) exceed the 129 MB L2, so every step streams
+them from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  ``value`` is the step's algorithmic bytes (weights,
+activations, outputs) over device time with inputs resident; ``e2e`` repeats
+the step through the same C-ABI calls with the step's inputs copied from
+pinned host memory and all outputs copied back inside the timed region.  The
+step is replayed from a CUDA graph (one graph per input set).  ``roofline``
+is the GEMV kernel's achieved bandwidth from per-launch CUDA events; the peak
+is the measured copy bandwidth of this GPU model.  ``cpu_baseline`` times the
+CPU oracle on a bounded sample.  ``--impl reference`` times that oracle alone
+as the reference arm.
+
+Multi-GPU: replicas only (each rank runs the whole step on its own GPU; the
+product shards with no exchange); the per-rank time is max-reduced.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_decode_gemv_rms_gb300 import synth, workloads  # noqa: E402
+
+METRIC = "Q4_0×Q8_0 GEMV HBM GB/s (fraction of GB300 peak) and µs/call at batch 1"
+UNIT = "GB/s"
+N_INPUT_SETS = 4
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+# ---------------------------------------------------------------- helpers
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+            "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+def source_hash(*paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_file: str):
+    """Per-launch DRAM bytes of a kernel from the committed ncu summary, or
+    None when the summary is missing or was taken on a different source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_file)
+    if not e or e.get("source_sha") != source_hash(os.path.join("quantized_decode_gemv_rms_gb300", "csrc",
+                                                                 kernel_file)):
+        return None
+    return e
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_id: str):
+        self.dev = device_id
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts))
+            except ValueError:
+                continue
+        win = [r for r in rows if self.t0 is not None and self.t0 - 0.15 <= r[0] <= (self.t1 or r[0]) + 0.15]
+        use = win if win else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in use:
+            for i, n in enumerate(names):
+                if r[3][5 + i].lower().startswith("active"):
+                    reasons.add(n)
+        sm = [r[1] for r in use]
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(r[2] for r in use) if use else None,
+                "reasons": sorted(reasons), "samples": len(use),
+                "window": "timed region" if win else "whole run (no sample fell inside the timed region)"}
+
+
+# ---------------------------------------------------------------- distributed
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int, device=None) -> float:
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- workload bytes
+def step_bytes(wl):
+    """Algorithmic bytes of one decode step: every GEMV's W + xq + y, and every
+    quantization's x (+ gamma) read and xq write."""
+    total = 0
+    for m in wl.matrices:
+        total += workloads.gemv_algorithmic_bytes(m.rows, m.cols)
+    for tag, K in wl.activations.items():
+        norm = any(m.source == f"norm:{tag}" for m in wl.matrices)
+        total += 4 * K + (4 * K if norm else 0) + workloads.q8_0_bytes(1, K)
+    return total
+
+
+def activation_kinds(wl):
+    kinds = {}
+    for m in wl.matrices:
+        kind, tag = m.source.split(":", 1)
+        kinds[tag] = kind
+    return kinds
+
+
+# ---------------------------------------------------------------- CPU oracle leg
+def oracle_decode_sample(wl, row_frac, threads, inputs, Wq_rows):
+    """One oracle pass: quantize every activation, then the sampled rows of
+    every matrix.  Returns the algorithmic bytes it covered."""
+    import oracle
+    kinds = activation_kinds(wl)
+    xq = {}
+    nbytes = 0
+    for tag, K in wl.activations.items():
+        gam = inputs["gamma"].get(tag) if kinds[tag] == "norm" else None
+        xq[tag] = oracle.quantize_q8_0(inputs["x"][tag], gam, wl.eps)
+        nbytes += 4 * K + (4 * K if gam is not None else 0) + workloads.q8_0_bytes(1, K)
+    for m in wl.matrices:
+        tag = m.source.split(":", 1)[1]
+        Wq = Wq_rows[m.name]
+        oracle.matvec(Wq, xq[tag], m.cols, threads=threads)
+        nbytes += Wq.nbytes + workloads.q8_0_bytes(1, m.cols) + 4 * Wq.shape[0]
+    return nbytes
+
+
+def oracle_setup(wl, row_frac):
+    """Sampled rows of every matrix (every 1/row_frac-th row), quantized by the oracle."""
+    import oracle
+    Wq_rows = {}
+    for m in wl.matrices:
+        step = max(1, int(round(1.0 / row_frac)))
+        rows = np.arange(0, m.rows, step)
+        Wq_rows[m.name] = oracle.quantize_q4_0(synth.weight_rows(wl.seed, m.name, m.rows, m.cols, rows))
+    kinds = activation_kinds(wl)
+    inputs = {"x": {}, "gamma": {}}
+    for tag, K in wl.activations.items():
+        inputs["x"][tag] = synth.activations(wl.seed, f"x:{tag}:0", 1, K, outlier_frac=wl.outlier_frac)
+        if kinds[tag] == "norm":
+            inputs["gamma"][tag] = synth.gamma(wl.seed, tag, K)
+    return Wq_rows, inputs
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(wl, budget_s, row_frac, steps=None, warmup=1):
+    cores = cpu_cores()
+    Wq_rows, inputs = oracle_setup(wl, row_frac)
+    for _ in range(max(1, warmup)):
+        oracle_decode_sample(wl, row_frac, cores, inputs, Wq_rows)  # untimed
+    t0 = time.perf_counter()
+    done = 0
+    nbytes = 0
+    while True:
+        nbytes += oracle_decode_sample(wl, row_frac, cores, inputs, Wq_rows)
+        done += 1
+        el = time.perf_counter() - t0
+        if steps is not None and done >= steps:
+            break
+        if steps is None and el >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return nbytes / el / 1e9, cores, done, el, nbytes
+
+
+# ---------------------------------------------------------------- GPU leg
+class DecodeStep:
+    def __init__(self, wl, device):
+        import torch
+        from quantized_decode_gemv_rms_gb300 import qdg
+        self.qdg = qdg
+        self.torch = torch
+        self.wl = wl
+        self.kinds = activation_kinds(wl)
+        self.W = {}
+        for m in wl.matrices:
+            Wq = torch.empty(qdg.q4_0_nbytes(m.rows, m.cols), dtype=torch.uint8, device=device)
+            chunk = 16384
+            for r in range(0, m.rows, chunk):
+                r1 = min(m.rows, r + chunk)
+                w = torch.from_numpy(synth.weights(wl.seed, m.name, m.rows, m.cols, row_begin=r, row_end=r1))
+                wd = w.to(device)
+                qdg.quantize_q4_0(wd, Wq[r * (m.cols // 32) * 18:r1 * (m.cols // 32) * 18], O=r1 - r, K=m.cols)
+                del wd
+            self.W[m.name] = Wq
+        torch.cuda.synchronize()
+        self.gamma = {tag: torch.from_numpy(synth.gamma(wl.seed, tag, K)).to(device)
+                      for tag, K in wl.activations.items() if self.kinds[tag] == "norm"}
+        # input sets: host (pinned) and device copies
+        self.x_host = [{tag: torch.from_numpy(synth.activations(wl.seed, f"x:{tag}:{p}", 1, K,
+                                                                outlier_frac=wl.outlier_frac)[0]).pin_memory()
+                        for tag, K in wl.activations.items()} for p in range(N_INPUT_SETS)]
+        self.x_dev = [{tag: t.to(device) for tag, t in xs.items()} for xs in self.x_host]
+        self.x_stage = {tag: torch.empty(K, dtype=torch.float32, device=device) for tag, K in wl.activations.items()}
+        self.xq = {tag: torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
+                   for tag, K in wl.activations.items()}
+        self.y = {m.name: torch.empty(m.rows, dtype=torch.float32, device=device) for m in wl.matrices}
+        self.y_host = {m.name: torch.empty(m.rows, dtype=torch.float32).pin_memory() for m in wl.matrices}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()      # release the fp32 staging of the weights
+
+    def launches_per_step(self):
+        return len(self.wl.activations) + len(self.wl.matrices)
+
+    def run(self, xs, events=None):
+        qdg = self.qdg
+        i = 0
+        for tag, K in self.wl.activations.items():
+            g = self.gamma.get(tag)
+            if events:
+                events[i].record()
+            qdg.qnorm_quantize_q8_0(xs[tag], g, self.wl.eps, self.xq[tag], K=K, N=1)
+            i += 1
+        for m in self.wl.matrices:
+            tag = m.source.split(":", 1)[1]
+            if events:
+                events[i].record()
+            qdg.q4_0_q8_0_gemv(self.W[m.name], self.xq[tag], self.y[m.name], m.rows, m.cols)
+            i += 1
+        if events:
+            events[i].record()
+
+
+def bench_ours(args, wl, world, rank, local):
+    import torch
+    from quantized_decode_gemv_rms_gb300 import qdg
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    qdg.lib()
+    qdg.qdg_set_option(qdg.QDG_OPT_PDL, 1 if args.pdl else 0)
+    step = DecodeStep(wl, device)
+    stream = torch.cuda.current_stream()
+    nbytes = step_bytes(wl)
+    L = step.launches_per_step()
+
+    # eager warm-up (also sets kernel attributes before capture)
+    for i in range(3):
+        step.run(step.x_dev[i % N_INPUT_SETS])
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+
+    graphs = []
+    if args.graph:
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            for p in range(N_INPUT_SETS):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=side):
+                    step.run(step.x_dev[p])
+                graphs.append(g)
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+
+    def one_step(k):
+        if graphs:
+            graphs[k % N_INPUT_SETS].replay()
+        else:
+            step.run(step.x_dev[k % N_INPUT_SETS])
+
+    try:
+        smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        smi_id = str(local)
+    sampler = ClockSampler(smi_id)
+    sampler.start()
+    # pre-roll so the clock sampler sees the GPU under this load
+    t_end = time.time() + 0.6
+    k = 0
+    while time.time() < t_end:
+        one_step(k)
+        k += 1
+        if k % 200 == 0:
+            torch.cuda.synchronize()
+    for k in range(args.warmup):
+        one_step(k)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = qdg.qdg_launch_count(-1)
+    graph_launches0 = 0
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    sampler.mark("t0")
+    e0.record(stream)
+    for k in range(args.steps):
+        one_step(k)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sampler.mark("t1")
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(ms, world, device)
+    launches = qdg.qdg_launch_count(-1) - launches0
+    gpu_launches = launches if not graphs else L * args.steps
+    status = qdg.qdg_device_status()
+    if status != qdg.QDG_OK:
+        raise RuntimeError(f"device status after timed region: {qdg.status_string(status)}")
+
+    # post-roll for the clock sampler
+    t_end = time.time() + 0.3
+    k = 0
+    while time.time() < t_end:
+        one_step(k)
+        k += 1
+        if k % 200 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+
+    # ---- instrumented pass: per-launch events (eager launches, same kernels)
+    n_inst = max(20, min(args.steps, 200))
+    per = {m.name: [] for m in wl.matrices}
+    qn = []
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(n_inst)]
+    for k in range(n_inst):
+        step.run(step.x_dev[k % N_INPUT_SETS], events=evs[k])
+    torch.cuda.synchronize()
+    for k in range(n_inst):
+        ev = evs[k]
+        na = len(wl.activations)
+        qn.append(sum(ev[i].elapsed_time(ev[i + 1]) for i in range(na)) * 1e3 / na)
+        for j, m in enumerate(wl.matrices):
+            per[m.name].append(ev[na + j].elapsed_time(ev[na + j + 1]) * 1e3)
+    us_per_call = {name: float(np.median(v)) for name, v in per.items()}
+    gemv_bytes = {m.name: workloads.gemv_algorithmic_bytes(m.rows, m.cols) for m in wl.matrices}
+    tot_b = sum(gemv_bytes.values())
+    tot_us = sum(us_per_call.values())
+    achieved = tot_b / (tot_us * 1e-6) / 1e9
+    gbs_per_call = {n: gemv_bytes[n] / (us_per_call[n] * 1e-6) / 1e9 for n in us_per_call}
+
+    # ---- end-to-end pass through the same calls with host buffers
+    n_e2e = max(10, min(args.steps, 500))
+    h2d = sum(t.numel() * 4 for t in step.x_host[0].values())
+    d2h = sum(t.numel() * 4 for t in step.y_host.values())
+    for k in range(3):
+        _e2e_step(step, graphs, k)
+    torch.cuda.synchronize()
+    barrier(world)
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for k in range(n_e2e):
+        _e2e_step(step, graphs, k)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
+
+    peaks, peak_src = measured_peaks()
+    traffic = ncu_traffic("gemv.cu")
+    roof = {"bound": "hbm", "kernel": "gemv_kernel", "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+            "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
+            "traffic_source": (traffic.get("what") if traffic else "no ncu summary for this source"),
+            "algorithmic_bytes_per_step_gemv": tot_b,
+            "frac_of_nominal_8TB": round(achieved / 8000.0, 4)}
+    result = {
+        "metric": METRIC, "value": round(nbytes * world / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "i32 (int4 x int8 block sums) + f32 scaling",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations with 1% x20 outliers)",
+        "config": {"workload": wl.name, "batch": 1, "matrices": {m.name: [m.rows, m.cols] for m in wl.matrices},
+                   "bytes_per_step": nbytes, "l2": "inputs larger than L2 (419 MB of weights per step vs 129 MB L2)",
+                   "launch": ("cuda graph" if graphs else "eager") + (" + PDL" if args.pdl else ""),
+                   "parallelism": f"replicas x{world}"},
+        "us_per_step": round(ms * 1e3, 2),
+        "us_per_call": {k: round(v, 2) for k, v in us_per_call.items()},
+        "gbs_per_call": {k: round(v, 1) for k, v in gbs_per_call.items()},
+        "qnorm_us_per_call": round(float(np.median(qn)), 2),
+        "roofline": roof,
+        "e2e": {"value": round(nbytes * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": UNIT,
+                "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": int(gpu_launches),
+        "clocks": clocks,
+    }
+    return result, step
+
+
+def _e2e_step(step, graphs, k):
+    p = k % N_INPUT_SETS
+    for tag, t in step.x_host[p].items():
+        step.x_dev[p][tag].copy_(t, non_blocking=True)
+    if graphs:
+        graphs[p].replay()
+    else:
+        step.run(step.x_dev[p])
+    for name, t in step.y_host.items():
+        t.copy_(step.y[name], non_blocking=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=workloads.LLAMA_8B.name, choices=sorted(workloads.ALL))
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--pdl", action="store_true", default=True)
+    ap.add_argument("--no-pdl", dest="pdl", action="store_false")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = workloads.ALL[args.workload]
+    world, rank, local = dist_setup(args)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        row_frac = 1.0 / 16
+        rate, cores, done, el, nb = time_oracle(wl, 0, row_frac, steps=args.steps, warmup=args.warmup)
+        line = {"impl": "reference", "metric": METRIC, "value": round(rate, 4), "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / done * 1e3, 3),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64 (oracle: dequantize-then-dot)", "data": "synthetic",
+                "config": {"workload": wl.name, "batch": 1},
+                "cpu_baseline": {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                 "sample": f"every 16th row of each matrix + all activations, {done} steps"},
+                "e2e": {"value": round(rate, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    result, _ = bench_ours(args, wl, world, rank, local)
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        rate, cores, done, el, nb = time_oracle(wl, args.cpu_budget, 1.0 / 16)
+        result["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                                  "sample": f"every 16th row of each matrix + all activations; {done} passes "
+                                            f"in {el:.1f} s ({nb / 1e9:.2f} GB)"}
+    if rank == 0:
+        print(json.dumps(result))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

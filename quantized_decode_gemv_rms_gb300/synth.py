@@ -49,6 +49,22 @@ def weights(seed: int, name: str, rows: int, cols: int, sigma: float = 0.02,
     return out
 
 
+def weight_rows(seed: int, name: str, rows: int, cols: int, index: np.ndarray,
+                sigma: float = 0.02) -> np.ndarray:
+    """fp32 rows ``index`` (sorted) of the matrix ``weights(seed, name, rows, cols)``,
+    drawing only the chunks that contain them."""
+    index = np.asarray(index, dtype=np.int64)
+    out = np.empty((index.shape[0], cols), dtype=np.float32)
+    chunk = 1024
+    for c in np.unique(index // chunk):
+        sel = np.nonzero(index // chunk == c)[0]
+        lo = int(c) * chunk
+        hi = min(rows, lo + chunk)
+        blk = weights(seed, name, rows, cols, sigma=sigma, row_begin=lo, row_end=hi)
+        out[sel] = blk[index[sel] - lo]
+    return out
+
+
 def activations(seed: int, name: str, n: int, cols: int, outlier_frac: float = 0.0,
                 outlier_mult: float = 20.0) -> np.ndarray:
     """fp32 [n][cols] ~ N(0, 1) with optional per-vector outliers."""
