@@ -120,6 +120,23 @@ QDG_API int q4_0_q8_0_gemm_small_n(const void* W, const void* xq, float* y, int6
                            int64_t O, int64_t K, int64_t N, qdg_stream_t stream);
 
 /*
+ * q4_0_q8_0_gemm -- Y = W * X for T tokens (prefill, the "mmq" route)
+ *   [same page and section: quantized matrices other than the vector case go
+ *   to mmq; long prefill batches keep it busy].
+ *
+ * W   [O][K/32] Q4_0, 16-byte aligned.   xq  [T][K/32] Q8_0, 16-byte aligned.
+ * y   [T][ldy] fp32: the output for token t at y + t*ldy, ldy >= O.
+ * K   multiple of 256, 256 <= K <= 65536.   1 <= O, T <= 2^30.
+ * The exact per-block integer sums are formed on the fifth-generation tensor
+ * cores (tcgen05.mma, fp16 operands holding the integer codes exactly, fp32
+ * accumulation in tensor memory) and scaled per block on the CUDA cores.
+ * Needs no workspace; every tile is owned by one CTA, so results are
+ * deterministic.
+ */
+QDG_API int q4_0_q8_0_gemm(const void* W, const void* xq, float* y, int64_t ldy,
+                           int64_t O, int64_t K, int64_t T, qdg_stream_t stream);
+
+/*
  * quantize_q4_0 -- weight preparation: fp32 [O][ldw] -> Q4_0 [O][K/32].
  * Per block: m = the element of largest magnitude (the first one on ties),
  * d = m / -8 in fp32, q = min(15, floor(w/d + 8.5)), stored d = fp16(d); an
@@ -163,7 +180,7 @@ QDG_API int64_t qdg_launch_count(int which);
  * qdg_debug_block_sums -- test hook.  Runs the production inner loop of one
  * product path and writes the exact per-block integer sums
  * isum[n][o][b] = sum_j (q_w - 8) * q_x  (int32 [N][O][K/32]) instead of y.
- * path: 0 = gemv (N must be 1), 1 = small-N.
+ * path: 0 = gemv (N must be 1), 1 = small-N, 2 = prefill gemm (N = T tokens).
  * Same argument rules as the corresponding entry point.
  */
 QDG_API int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum, int64_t O,

@@ -109,7 +109,7 @@ extern "C" int qdg_device_status(qdg_stream_t stream) {
     }
     unsigned f = 0;
     const unsigned parts[] = {flags_read_clear_quantize(s), flags_read_clear_gemv(s), flags_read_clear_small_n(s),
-                              flags_read_clear_api(s)};
+                              flags_read_clear_gemm(s), flags_read_clear_api(s)};
     for (unsigned p : parts) {
         if (p == ~0u) {
             cudaGetLastError();
@@ -132,6 +132,8 @@ extern "C" int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum
             return gemv_launch(W, xq, nullptr, O, K, s, isum);
         case 1:
             return small_n_launch(W, xq, nullptr, O, O, K, N, s, isum);
+        case 2:
+            return gemm_launch(W, xq, nullptr, O, O, K, N, s, isum);
         default:
             return QDG_EINVAL;
     }

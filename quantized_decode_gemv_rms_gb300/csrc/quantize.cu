@@ -16,31 +16,56 @@ static __device__ unsigned g_flags_quantize;
 
 namespace {
 
-constexpr int kNormThreads = 256;   // the fixed reduction order is defined over 256 lanes
+constexpr int kNormThreads = 256;     // the fixed reduction order is defined over 256 lanes
+constexpr int kBlocksPerCta = 32;     // Q8_0 blocks quantized by one CTA (4 per warp)
 
-// One CTA per vector.  Thread j sums x_i^2 for i = j (mod 256) with an fma
-// chain in ascending i; warps combine with an xor butterfly (16,8,4,2,1);
-// the 8 warp totals combine as ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).  Then
-// warp w quantizes blocks w, w+8, ... with lane l on element 32b+l.
+// Grid: (vectors * splits).  Every CTA of a vector recomputes the vector's
+// sum of squares in the library's fixed order (so all CTAs agree bit for
+// bit), then quantizes its own slice of kBlocksPerCta blocks.
+//   Sum of squares: thread j sums x_i^2 for i = j (mod 256) with an fma chain
+//   in ascending i; each warp combines with an xor butterfly (16,8,4,2,1);
+//   the 8 warp totals combine as ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).
+//   Quantization: warp w takes blocks w, w+8, ... of the slice, lane l
+//   element 32b+l.
 __global__ void __launch_bounds__(kNormThreads)
 qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restrict__ gamma, float eps, int K,
-                uint8_t* __restrict__ xq) {
+                int splits, uint8_t* __restrict__ xq) {
     pdl_wait();
     pdl_trigger();
-    const int n = blockIdx.x;
+    const int64_t n = blockIdx.x / splits;
+    const int split = blockIdx.x - static_cast<int>(n * splits);
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const float* xn = x + static_cast<int64_t>(n) * ldx;
+    const float* xn = x + n * ldx;
     const int nb = K >> 5;
+    const int b0 = split * kBlocksPerCta;
+    const int b1 = min(nb, b0 + kBlocksPerCta);
+
+    // Issue this CTA's slice loads first; they overlap the reduction below.
+    constexpr int kPer = kBlocksPerCta / (kNormThreads / 32);
+    float xv[kPer], gv[kPer];
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int b = b0 + warp + u * (kNormThreads / 32);
+        xv[u] = b < b1 ? __ldg(xn + (b << 5) + lane) : 0.0f;
+        gv[u] = (gamma != nullptr && b < b1) ? __ldg(gamma + (b << 5) + lane) : 1.0f;
+    }
 
     float s = 1.0f;
     if (gamma != nullptr) {
         __shared__ float wsum[kNormThreads / 32];
         float acc = 0.0f;
-        for (int i = tid; i < K; i += kNormThreads) {
-            const float v = __ldg(xn + i);
-            acc = __fmaf_rn(v, v, acc);
+        for (int i0 = tid; i0 < K; i0 += kNormThreads * 8) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int i = i0 + u * kNormThreads;
+                v[u] = i < K ? __ldg(xn + i) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (i0 + u * kNormThreads < K) acc = __fmaf_rn(v[u], v[u], acc);
         }
         acc = warp_sum(acc);
         if (lane == 0) wsum[warp] = acc;
@@ -51,11 +76,13 @@ qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restric
         s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
     }
 
-    uint8_t* out = xq + static_cast<int64_t>(n) * nb * 34;
-    for (int b = warp; b < nb; b += kNormThreads / 32) {
-        const int i = (b << 5) + lane;
-        float v = __ldg(xn + i);
-        if (gamma != nullptr) v = __fmul_rn(__fmul_rn(v, s), __ldg(gamma + i));
+    uint8_t* out = xq + n * nb * 34;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+        const int b = b0 + warp + u * (kNormThreads / 32);
+        if (b >= b1) break;
+        float v = xv[u];
+        if (gamma != nullptr) v = __fmul_rn(__fmul_rn(v, s), gv[u]);
         float amax = fabsf(v);
 #pragma unroll
         for (int h = 16; h >= 1; h >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, h));
@@ -142,11 +169,12 @@ extern "C" int qnorm_quantize_q8_0(const float* x, int64_t ldx, const float* gam
     if (K <= 0 || N <= 0 || ldx < K) return QDG_EINVAL;
     if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
     if (K % 32 != 0 || K > (1 << 20)) return QDG_ESHAPE;
-    if (N > 0x7fffffff) return QDG_ESHAPE;
+    const int splits = static_cast<int>((K / 32 + kBlocksPerCta - 1) / kBlocksPerCta);
+    if (N * splits > 0x7fffffff) return QDG_ESHAPE;
     if (!aligned(x, 4) || !aligned(xq, 2) || (gamma && !aligned(gamma, 4))) return QDG_EALIGN;
-    cudaError_t e = launch(qnorm_q8_kernel, dim3(static_cast<unsigned>(N)), dim3(kNormThreads), 0,
+    cudaError_t e = launch(qnorm_q8_kernel, dim3(static_cast<unsigned>(N * splits)), dim3(kNormThreads), 0,
                            reinterpret_cast<cudaStream_t>(stream), true, x, ldx, gamma, eps, static_cast<int>(K),
-                           static_cast<uint8_t*>(xq));
+                           splits, static_cast<uint8_t*>(xq));
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(0);
     return QDG_OK;
