@@ -475,6 +475,73 @@ def bench_ours(args, wl, world, rank, local):
     return result, step
 
 
+def bench_extras(args, device):
+    """Small-N (N = 2, 4, 8) and prefill GEMM timings: CUDA events around each
+    call, after warm-up.  The small-N weights rotate through enough copies to
+    exceed three L2 sizes, so every call reads HBM."""
+    import torch
+    from quantized_decode_gemv_rms_gb300 import qdg
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    peaks, _ = measured_peaks()
+    out = {"small_n": {}, "prefill": {}}
+
+    def timed(fn, reps, warm=5):
+        for i in range(warm):
+            fn(i)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i, (a, b) in enumerate(evs):
+            a.record()
+            fn(i)
+            b.record()
+        torch.cuda.synchronize()
+        return float(np.median([a.elapsed_time(b) for a, b in evs])) * 1e3
+
+    def make_w(seed, name, O, K):
+        Wq = torch.empty(qdg.q4_0_nbytes(O, K), dtype=torch.uint8, device=device)
+        for r in range(0, O, 8192):
+            r1 = min(O, r + 8192)
+            w = torch.from_numpy(synth.weights(seed, name, O, K, row_begin=r, row_end=r1)).to(device)
+            qdg.quantize_q4_0(w, Wq[r * (K // 32) * 18:r1 * (K // 32) * 18], O=r1 - r, K=K)
+        return Wq
+
+    for (O, K) in workloads.SMALL_N_SHAPES:
+        Wq = make_w(workloads.SMALL_N_SEED, f"smalln-{O}x{K}", O, K)
+        copies = max(2, -(-3 * l2 // Wq.numel()))
+        Ws = [Wq] + [Wq.clone() for _ in range(copies - 1)]
+        res = {}
+        for N in workloads.SMALL_N_COLS:
+            x = torch.from_numpy(synth.activations(workloads.SMALL_N_SEED, f"smalln-x-{K}", N, K)).to(device)
+            g = torch.from_numpy(synth.gamma(workloads.SMALL_N_SEED, f"smalln-g-{K}", K)).to(device)
+            xq = torch.empty(qdg.q8_0_nbytes(N, K), dtype=torch.uint8, device=device)
+            qdg.qnorm_quantize_q8_0(x, g, 1e-6, xq)
+            y = torch.empty((N, O), dtype=torch.float32, device=device)
+            us = timed(lambda i: qdg.q4_0_q8_0_gemm_small_n(Ws[i % copies], xq, y, O, O, K, N), 60)
+            nbytes = workloads.gemv_algorithmic_bytes(O, K, N)
+            res[f"N{N}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                            "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+        out["small_n"][f"{O}x{K}"] = dict(res, weight_copies=copies)
+        del Ws, Wq
+        torch.cuda.empty_cache()
+    for (O, K, T) in workloads.PREFILL_SHAPES:
+        Wq = make_w(workloads.PREFILL_SEED, f"prefill-{O}x{K}", O, K)
+        x = torch.from_numpy(synth.activations(workloads.PREFILL_SEED, f"prefill-{O}x{K}-x", T, K)).to(device)
+        xq = torch.empty(qdg.q8_0_nbytes(T, K), dtype=torch.uint8, device=device)
+        qdg.qnorm_quantize_q8_0(x, None, 0.0, xq)
+        y = torch.empty((T, O), dtype=torch.float32, device=device)
+        us = timed(lambda i: qdg.q4_0_q8_0_gemm(Wq, xq, y, O, O, K, T), 30)
+        tflops = 2.0 * O * K * T / (us * 1e-6) / 1e12
+        out["prefill"][f"{O}x{K}x{T}"] = {"us": round(us, 2), "tflops": round(tflops, 1),
+                                          "frac_fp16_peak": round(tflops / peaks["bf16_tflops"], 4)}
+        del Wq, x, xq, y
+        torch.cuda.empty_cache()
+    out["peak_note"] = ("small-N against the measured HBM copy bandwidth; prefill against the measured dense "
+                        "bf16 burst peak (the fp16 tensor rate is the same nominal 2.25 PFLOP/s)")
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    return out
+
+
 def _e2e_step(step, graphs, k):
     p = k % N_INPUT_SETS
     for tag, t in step.x_host[p].items():
@@ -499,6 +566,8 @@ def main():
     ap.add_argument("--no-pdl", dest="pdl", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the small-N and prefill timings")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -521,7 +590,12 @@ def main():
         print(json.dumps(line))
         return
 
-    result, _ = bench_ours(args, wl, world, rank, local)
+    result, step = bench_ours(args, wl, world, rank, local)
+    if args.extras and rank == 0:
+        import torch
+        del step
+        torch.cuda.empty_cache()
+        result["extras"] = bench_extras(args, torch.device("cuda", local))
     if rank == 0 and world == 1 and args.cpu_baseline:
         rate, cores, done, el, nb = time_oracle(wl, args.cpu_budget, 1.0 / 16)
         result["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",

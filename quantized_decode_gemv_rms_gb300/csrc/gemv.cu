@@ -2,54 +2,52 @@
 // batch-1 decode [GGML: Backend abstraction and hardware acceleration,
 // section "CUDA: mmvq, mmq, cublas -- three matrix paths"]).
 //
-// The product is bound by the weight stream: 4.5 bits per weight read once
-// from HBM, against a few integer operations per weight.  Design:
-//   * One persistent CTA per SM owns a contiguous range of rows.  With
-//     K % 256 == 0 a row is a multiple of 16 bytes, so the CTA's share of W is
-//     one contiguous byte range, copied in stages of whole rows by 1-D bulk
-//     asynchronous copies (TMA engine) into a ring of shared-memory buffers
-//     guarded by mbarriers; one producer warp keeps the ring full.
-//   * Consumer warps read W from shared memory in 36-byte block pairs (two
-//     Q4_0 blocks, 4-byte aligned): lane l of segment s owns pair p = 32s + l
-//     of every row, keeps the matching 64 Q8_0 activations in registers for
-//     the whole kernel, unpacks nibbles and forms the exact block sums with
-//     dp4a, then scales by d_w * d_x (exact in fp32) and reduces across the
-//     warp with shuffles.  Rows with more than 32 pairs are split into
-//     segments handled by different warps; the producer warp adds the
-//     segment partials in a fixed order and stores y, so results are
+// The product is bound by the weight stream: 4.5 bits per weight, read once
+// from HBM, against a few integer operations per weight.  Design (chosen by
+// measurement on GB300: plain 16-byte loads with enough bytes in flight
+// stream HBM faster than the bulk-copy engine fed through a barrier ring):
+//   * A row of K weights is split into segments of 32 block pairs (2048
+//     weights, 1152 bytes).  Lane l of a warp owns pair l of its segment and
+//     keeps the matching 64 Q8_0 activations in registers for the whole
+//     kernel.
+//   * Each CTA owns a contiguous range of rows; warp w works on segment
+//     w % nseg of rows slot, slot + nslots, ... (slot = w / nseg).  For every
+//     row-segment the warp reads its 1152 bytes with coalesced 16-byte loads
+//     (L1 bypassed), issued kDepth row-segments ahead of use, so each SM keeps
+//     tens of kilobytes in flight.
+//   * The 18-byte blocks are only 2-byte aligned, so the warp passes the
+//     segment through a private shared-memory buffer: coalesced 16-byte
+//     stores, then each lane reads its 36-byte pair as nine conflict-free
+//     32-bit loads, unpacks the nibbles, forms the exact block sums with dp4a
+//     (minus 8 * sum(q_x)), scales by d_w * d_x (exact in fp32), and the warp
+//     reduces with shuffles.
+//   * Segment partials are combined per row in a fixed order, so results are
 //     deterministic.
-//   * Programmatic dependent launch (optional): W is prefetched before the
-//     kernel waits for the preceding grid; activations are read and y is
-//     written only after the wait.
+//   * Programmatic dependent launch (optional): the first row-segments of W
+//     are requested before the kernel waits for the preceding grid;
+//     activations are read and y is written only after the wait.
 #include "common.cuh"
 
 #include <algorithm>
-#include <mutex>
 
 namespace qdg {
 
-static __device__ unsigned g_flags_gemv;
-
 namespace {
 
-constexpr int kMaxConsumerWarps = 16;
-constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
-constexpr int kStageTarget = 20 * 1024;     // bytes of W per ring stage (whole rows)
-constexpr int kRingBudget = 200 * 1024;     // shared memory for the ring
-constexpr int kMaxStages = 12;
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kDepth = 3;                   // row-segments in flight per warp
+constexpr int kSegBytes = 1152;             // 32 pairs x 36 bytes
+constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
 
 struct Plan {
-    int rowbytes;     // K/32 * 18
-    int nb;           // K/32
-    int P;            // block pairs per row (K/64)
-    int nseg;         // ceil(P / 32)
-    int ncw;          // consumer warps, a multiple of nseg
-    int nslots;       // rows processed concurrently = ncw / nseg
-    int rps;          // rows per stage
-    int stage_bytes;  // rps * rowbytes
-    int stages;       // ring depth
-    size_t smem;      // dynamic shared memory
+    int rowbytes;   // K/32 * 18
+    int nb;         // K/32
+    int P;          // block pairs per row (K/64)
+    int nseg;       // segments per row, ceil(P / 32)
+    int nslots;     // rows in flight per CTA = kWarps / nseg
+    int rch;        // rows per chunk (partial-sum buffer capacity), multiple of nslots
 };
 
 Plan make_plan(int64_t K) {
@@ -58,16 +56,17 @@ Plan make_plan(int64_t K) {
     p.rowbytes = p.nb * 18;
     p.P = static_cast<int>(K / 64);
     p.nseg = (p.P + 31) / 32;
-    p.ncw = p.nseg * (kMaxConsumerWarps / p.nseg);
-    p.nslots = p.ncw / p.nseg;
-    const int m = std::max(1, kStageTarget / (p.nslots * p.rowbytes));
-    p.rps = p.nslots * m;
-    p.stage_bytes = p.rps * p.rowbytes;
-    p.stages = std::max(2, std::min(kMaxStages, kRingBudget / p.stage_bytes));
-    const size_t part = static_cast<size_t>(p.stages) * p.rps * p.nseg * sizeof(float);
-    p.smem = static_cast<size_t>(p.stages) * p.stage_bytes + ((part + 15) / 16) * 16 +
-             2 * static_cast<size_t>(p.stages) * sizeof(uint64_t);
+    p.nslots = kWarps / p.nseg;
+    p.rch = (kPartFloats / p.nseg) / p.nslots * p.nslots;
     return p;
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint8_t* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
 }
 
 __device__ __forceinline__ int block_dot(uint32_t q0, uint32_t q1, uint32_t q2, uint32_t q3, const uint32_t* x) {
@@ -83,104 +82,59 @@ __device__ __forceinline__ int block_dot(uint32_t q0, uint32_t q1, uint32_t q2, 
     return acc;
 }
 
+// The 16-byte chunks of one row-segment held by a lane: indices lane, lane+32, lane+64.
+struct SegRegs {
+    uint4 v[3];
+};
+
 template <bool kDebug>
-__global__ void __launch_bounds__(kMaxThreads, 1)
+__global__ void __launch_bounds__(kThreads, 1)
 gemv_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq, float* __restrict__ y, int64_t O,
             Plan plan, int32_t* __restrict__ dbg) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int S = plan.stages;
-    const int rps = plan.rps;
-    const int nseg = plan.nseg;
-    uint8_t* ring = smem;
-    float* part = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * plan.stage_bytes);
-    const size_t part_bytes = ((static_cast<size_t>(S) * rps * nseg * sizeof(float) + 15) / 16) * 16;
-    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(part) + part_bytes);
-    uint64_t* empty = full + S;
+    __shared__ __align__(16) uint8_t seg_buf[kWarps][kSegBytes];
+    __shared__ float part[kPartFloats];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int nseg = plan.nseg;
+    const int seg = warp % nseg;
+    const int slot = warp / nseg;
+    const bool worker = slot < plan.nslots;   // warps beyond nslots * nseg stay idle
+    const int p = seg * 32 + lane;            // block pair owned by this lane
+    const bool active = worker && p < plan.P;
+    // this warp's segment within a row: byte offset and number of 16-byte chunks
+    const int seg_off = seg * kSegBytes;
+    const int seg_vec = worker ? (min(plan.P, seg * 32 + 32) - seg * 32) * 36 / 16 : 0;
+
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * O / gridDim.x;
     const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * O / gridDim.x;
     const int nrows = static_cast<int>(r1 - r0);
-    const int nst = (nrows + rps - 1) / rps;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], plan.ncw);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
     pdl_trigger();
 
-    if (warp == 0) {
-        // ------------------------------------------------ producer + y writer
-        const uint64_t policy = l2_policy_evict_first();
-        bool ok = true;
-        bool waited = false;
-        int issued = 0;
-        auto store_stage = [&](int k) {
-            const int s = k % S;
-            const int64_t rs = r0 + static_cast<int64_t>(k) * rps;
-            const int rows = static_cast<int>((r1 - rs) < rps ? (r1 - rs) : rps);
-            const float* ps = part + static_cast<size_t>(s) * rps * nseg;
-            for (int i = lane; i < rows; i += 32) {
-                float v = ps[i * nseg];
-                for (int g = 1; g < nseg; ++g) v = __fadd_rn(v, ps[i * nseg + g]);
-                if (!kDebug) y[rs + i] = v;   // the block-sum hook stores no y
-            }
-            __syncwarp();
-        };
-        for (int k = 0; k < nst; ++k) {
-            const int s = k % S;
-            if (k >= S) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ((k / S) - 1) & 1));
-                if (!ok) break;
-                if (!waited) {
-                    pdl_wait();
-                    waited = true;
-                }
-                store_stage(k - S);
-            }
-            if (lane == 0) {
-                const int64_t rs = r0 + static_cast<int64_t>(k) * rps;
-                const int rows = static_cast<int>((r1 - rs) < rps ? (r1 - rs) : rps);
-                const uint32_t bytes = static_cast<uint32_t>(rows) * plan.rowbytes;
-                mbar_arrive_expect_tx(&full[s], bytes);
-                bulk_g2s(ring + static_cast<size_t>(s) * plan.stage_bytes, W + rs * plan.rowbytes, bytes, &full[s],
-                         policy);
-            }
-            __syncwarp();
-            issued = k + 1;
+    SegRegs pipe[kDepth];
+    auto load_seg = [&](int64_t row, SegRegs& s) {
+        const uint8_t* base = W + row * plan.rowbytes + seg_off;
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+            const int idx = lane + 32 * k;
+            if (idx < seg_vec) s.v[k] = ldg_stream(base + idx * 16);
         }
-        if (ok) {
-            for (int k = (issued - S > 0 ? issued - S : 0); k < issued; ++k) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&empty[k % S], (k / S) & 1));
-                if (!ok) break;
-                if (!waited) {
-                    pdl_wait();
-                    waited = true;
-                }
-                store_stage(k);
-            }
+    };
+    auto fill = [&](int64_t c0, int crows) {
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) {
+            const int ri = slot + d * plan.nslots;
+            if (ri < crows) load_seg(c0 + ri, pipe[d]);
         }
-        if (!ok) {
-            if (lane == 0) atomicOr(&g_flags_gemv, FLAG_TIMEOUT);
-            // Do not leave with copies still landing in this CTA's shared memory.
-            for (int k = (issued - S > 0 ? issued - S : 0); k < issued; ++k) mbar_wait(&full[k % S], (k / S) & 1);
-        }
-        return;
-    }
+    };
 
-    // ---------------------------------------------------------- consumers
-    const int cw = warp - 1;
-    const int seg = cw % nseg;
-    const int slot = cw / nseg;
-    const int p = seg * 32 + lane;
-    const bool active = p < plan.P;
+    // ---- the first chunk's leading row-segments (W only) before the wait
+    if (worker) fill(r0, min(nrows, plan.rch));
 
     pdl_wait();
+
+    // ---- activations of this lane's pair, kept in registers
     uint32_t xa[8], xb[8];
     float dxa = 0.0f, dxb = 0.0f;
     int sa = 0, sb = 0;
@@ -205,58 +159,66 @@ gemv_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq, float
         for (int i = 0; i < 8; ++i) xa[i] = xb[i] = 0u;
     }
 
-    for (int k = 0; k < nst; ++k) {
-        const int s = k % S;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (k / S) & 1));
-        if (!ok) {
-            if (lane == 0) atomicOr(&g_flags_gemv, FLAG_TIMEOUT);
-            break;
-        }
-        const int64_t rs = r0 + static_cast<int64_t>(k) * rps;
-        const int rows = static_cast<int>((r1 - rs) < rps ? (r1 - rs) : rps);
-        const uint8_t* st = ring + static_cast<size_t>(s) * plan.stage_bytes;
-        float* ps = part + static_cast<size_t>(s) * rps * nseg;
-        for (int row = slot; row < rows; row += plan.nslots) {
-            float acc = 0.0f;
-            if (active) {
-                const uint32_t* wp =
-                    reinterpret_cast<const uint32_t*>(st + static_cast<size_t>(row) * plan.rowbytes + p * 36);
-                uint32_t w[9];
+    uint8_t* buf = seg_buf[warp];
+    for (int64_t c0 = r0; c0 < r1; c0 += plan.rch) {
+        const int crows = static_cast<int>((r1 - c0) < plan.rch ? (r1 - c0) : plan.rch);
+        if (worker) {
+            if (c0 != r0) fill(c0, crows);
+            int k = 0;   // ring position of the row-segment being consumed
+            for (int ri = slot; ri < crows; ri += plan.nslots) {
+                SegRegs cur;
 #pragma unroll
-                for (int i = 0; i < 9; ++i) w[i] = wp[i];
-                const int ia = block_dot(bytes_2_to_5(w[0], w[1]), bytes_2_to_5(w[1], w[2]),
-                                         bytes_2_to_5(w[2], w[3]), bytes_2_to_5(w[3], w[4]), xa) -
-                               8 * sa;
-                const int ib = block_dot(w[5], w[6], w[7], w[8], xb) - 8 * sb;
-                const float dwa = half_bits_to_float(w[0]);
-                const float dwb = half_bits_to_float(w[4] >> 16);
-                acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
-                acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
-                if (kDebug) {
-                    int32_t* d = dbg + (rs + row) * plan.nb + 2 * p;
-                    d[0] = ia;
-                    d[1] = ib;
+                for (int d = 0; d < kDepth; ++d)
+                    if (d == k) cur = pipe[d];
+                const int ahead = ri + kDepth * plan.nslots;
+                if (ahead < crows) {
+#pragma unroll
+                    for (int d = 0; d < kDepth; ++d)
+                        if (d == k) load_seg(c0 + ahead, pipe[d]);
                 }
+                k = (k + 1 == kDepth) ? 0 : k + 1;
+                // stage through shared memory, then read this lane's 36-byte pair
+#pragma unroll
+                for (int q = 0; q < 3; ++q) {
+                    const int idx = lane + 32 * q;
+                    if (idx < seg_vec) *reinterpret_cast<uint4*>(buf + idx * 16) = cur.v[q];
+                }
+                __syncwarp();
+                float acc = 0.0f;
+                if (active) {
+                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(buf + lane * 36);
+                    uint32_t w[9];
+#pragma unroll
+                    for (int i = 0; i < 9; ++i) w[i] = wp[i];
+                    const int ia = block_dot(bytes_2_to_5(w[0], w[1]), bytes_2_to_5(w[1], w[2]),
+                                             bytes_2_to_5(w[2], w[3]), bytes_2_to_5(w[3], w[4]), xa) -
+                                   8 * sa;
+                    const int ib = block_dot(w[5], w[6], w[7], w[8], xb) - 8 * sb;
+                    const float dwa = half_bits_to_float(w[0]);
+                    const float dwb = half_bits_to_float(w[4] >> 16);
+                    acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
+                    acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
+                    if (kDebug) {
+                        int32_t* d = dbg + (c0 + ri) * plan.nb + 2 * p;
+                        d[0] = ia;
+                        d[1] = ib;
+                    }
+                }
+                __syncwarp();
+                acc = warp_sum(acc);
+                if (lane == 0) part[ri * nseg + seg] = acc;
             }
-            acc = warp_sum(acc);
-            if (lane == 0) ps[row * nseg + seg] = acc;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        __syncthreads();
+        if (!kDebug) {
+            for (int t = threadIdx.x; t < crows; t += kThreads) {
+                float v = part[t * nseg];
+                for (int g = 1; g < nseg; ++g) v = __fadd_rn(v, part[t * nseg + g]);
+                y[c0 + t] = v;
+            }
+        }
+        __syncthreads();
     }
-}
-
-std::mutex g_attr_mutex;
-size_t g_attr_smem[2] = {0, 0};
-
-template <bool kDebug>
-cudaError_t ensure_smem(size_t bytes) {
-    std::lock_guard<std::mutex> lock(g_attr_mutex);
-    if (g_attr_smem[kDebug] >= bytes) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<kDebug>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(bytes));
-    if (e == cudaSuccess) g_attr_smem[kDebug] = bytes;
-    return e;
 }
 
 }  // namespace
@@ -269,36 +231,21 @@ int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, c
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     const Plan plan = make_plan(K);
-    if (plan.smem > dev.smem_optin) return QDG_ESHAPE;
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
     cudaError_t e;
-    if (dbg) {
-        e = ensure_smem<true>(plan.smem);
-        if (e == cudaSuccess)
-            e = launch(gemv_kernel<true>, dim3(grid), dim3(32 * (plan.ncw + 1)), plan.smem, stream, false,
-                       static_cast<const uint8_t*>(W), static_cast<const uint8_t*>(xq), y, O, plan, dbg);
-    } else {
-        e = ensure_smem<false>(plan.smem);
-        if (e == cudaSuccess)
-            e = launch(gemv_kernel<false>, dim3(grid), dim3(32 * (plan.ncw + 1)), plan.smem, stream, true,
-                       static_cast<const uint8_t*>(W), static_cast<const uint8_t*>(xq), y, O, plan,
-                       static_cast<int32_t*>(nullptr));
-    }
+    if (dbg)
+        e = launch(gemv_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, false, static_cast<const uint8_t*>(W),
+                   static_cast<const uint8_t*>(xq), y, O, plan, dbg);
+    else
+        e = launch(gemv_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, true, static_cast<const uint8_t*>(W),
+                   static_cast<const uint8_t*>(xq), y, O, plan, static_cast<int32_t*>(nullptr));
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(1);
     return QDG_OK;
 }
 
-unsigned flags_read_clear_gemv(cudaStream_t stream) {
-    unsigned v = 0, zero = 0;
-    if (cudaMemcpyFromSymbolAsync(&v, g_flags_gemv, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        return ~0u;
-    if (cudaMemcpyToSymbolAsync(g_flags_gemv, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
-        cudaSuccess)
-        return ~0u;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return ~0u;
-    return v;
-}
+// The GEMV has no bounded waits (only __syncthreads), so it never raises a flag.
+unsigned flags_read_clear_gemv(cudaStream_t) { return 0; }
 
 }  // namespace qdg
 
