@@ -505,7 +505,7 @@ def bench_extras(args, device):
             qdg.quantize_q4_0(w, Wq[r * (K // 32) * 18:r1 * (K // 32) * 18], O=r1 - r, K=K)
         return Wq
 
-    for (O, K) in workloads.SMALL_N_SHAPES:
+    for (O, K) in (workloads.SMALL_N_SHAPES if args.only in (None, "small_n") else ()):
         Wq = make_w(workloads.SMALL_N_SEED, f"smalln-{O}x{K}", O, K)
         copies = max(2, -(-3 * l2 // Wq.numel()))
         Ws = [Wq] + [Wq.clone() for _ in range(copies - 1)]
@@ -523,7 +523,7 @@ def bench_extras(args, device):
         out["small_n"][f"{O}x{K}"] = dict(res, weight_copies=copies)
         del Ws, Wq
         torch.cuda.empty_cache()
-    for (O, K, T) in workloads.PREFILL_SHAPES:
+    for (O, K, T) in (workloads.PREFILL_SHAPES if args.only in (None, "prefill") else ()):
         Wq = make_w(workloads.PREFILL_SEED, f"prefill-{O}x{K}", O, K)
         x = torch.from_numpy(synth.activations(workloads.PREFILL_SEED, f"prefill-{O}x{K}-x", T, K)).to(device)
         xq = torch.empty(qdg.q8_0_nbytes(T, K), dtype=torch.uint8, device=device)
@@ -568,6 +568,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the small-N and prefill timings")
+    ap.add_argument("--only", choices=["small_n", "prefill"], default=None,
+                    help="time only that product (one JSON object with its numbers)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -590,6 +592,13 @@ def main():
         print(json.dumps(line))
         return
 
+    if args.only in ("small_n", "prefill"):
+        import torch
+        torch.cuda.set_device(local)
+        ex = bench_extras(args, torch.device("cuda", local))
+        if rank == 0:
+            print(json.dumps({"only": args.only, args.only: ex[args.only]}))
+        return
     result, step = bench_ours(args, wl, world, rank, local)
     if args.extras and rank == 0:
         import torch

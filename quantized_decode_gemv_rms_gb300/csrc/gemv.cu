@@ -36,7 +36,7 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kDepth = 3;                   // row-segments in flight per warp
+constexpr int kDepth = 3;                   // row-segments in flight per warp (the consume loop is unrolled by 3)
 constexpr int kSegBytes = 1152;             // 32 pairs x 36 bytes
 constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
@@ -160,53 +160,56 @@ gemv_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq, float
     }
 
     uint8_t* buf = seg_buf[warp];
+    // One row-segment: stage it through shared memory, refill its ring entry
+    // with the segment kDepth ahead, dot it, reduce it.
+    auto consume = [&](int64_t c0, int crows, int ri, SegRegs& entry) {
+        // Store first (this waits for the entry's loads, issued kDepth steps
+        // ago), then reuse the same registers for the segment kDepth ahead.
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const int idx = lane + 32 * q;
+            if (idx < seg_vec) *reinterpret_cast<uint4*>(buf + idx * 16) = entry.v[q];
+        }
+        const int ahead = ri + kDepth * plan.nslots;
+        if (ahead < crows) load_seg(c0 + ahead, entry);
+        __syncwarp();
+        float acc = 0.0f;
+        if (active) {
+            const uint32_t* wp = reinterpret_cast<const uint32_t*>(buf + lane * 36);
+            uint32_t w[9];
+#pragma unroll
+            for (int i = 0; i < 9; ++i) w[i] = wp[i];
+            const int ia = block_dot(bytes_2_to_5(w[0], w[1]), bytes_2_to_5(w[1], w[2]), bytes_2_to_5(w[2], w[3]),
+                                     bytes_2_to_5(w[3], w[4]), xa) -
+                           8 * sa;
+            const int ib = block_dot(w[5], w[6], w[7], w[8], xb) - 8 * sb;
+            const float dwa = half_bits_to_float(w[0]);
+            const float dwb = half_bits_to_float(w[4] >> 16);
+            acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
+            acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
+            if (kDebug) {
+                int32_t* d = dbg + (c0 + ri) * plan.nb + 2 * p;
+                d[0] = ia;
+                d[1] = ib;
+            }
+        }
+        __syncwarp();
+        acc = warp_sum(acc);
+        if (lane == 0) part[ri * nseg + seg] = acc;
+    };
+
     for (int64_t c0 = r0; c0 < r1; c0 += plan.rch) {
         const int crows = static_cast<int>((r1 - c0) < plan.rch ? (r1 - c0) : plan.rch);
         if (worker) {
             if (c0 != r0) fill(c0, crows);
-            int k = 0;   // ring position of the row-segment being consumed
-            for (int ri = slot; ri < crows; ri += plan.nslots) {
-                SegRegs cur;
-#pragma unroll
-                for (int d = 0; d < kDepth; ++d)
-                    if (d == k) cur = pipe[d];
-                const int ahead = ri + kDepth * plan.nslots;
-                if (ahead < crows) {
-#pragma unroll
-                    for (int d = 0; d < kDepth; ++d)
-                        if (d == k) load_seg(c0 + ahead, pipe[d]);
-                }
-                k = (k + 1 == kDepth) ? 0 : k + 1;
-                // stage through shared memory, then read this lane's 36-byte pair
-#pragma unroll
-                for (int q = 0; q < 3; ++q) {
-                    const int idx = lane + 32 * q;
-                    if (idx < seg_vec) *reinterpret_cast<uint4*>(buf + idx * 16) = cur.v[q];
-                }
-                __syncwarp();
-                float acc = 0.0f;
-                if (active) {
-                    const uint32_t* wp = reinterpret_cast<const uint32_t*>(buf + lane * 36);
-                    uint32_t w[9];
-#pragma unroll
-                    for (int i = 0; i < 9; ++i) w[i] = wp[i];
-                    const int ia = block_dot(bytes_2_to_5(w[0], w[1]), bytes_2_to_5(w[1], w[2]),
-                                             bytes_2_to_5(w[2], w[3]), bytes_2_to_5(w[3], w[4]), xa) -
-                                   8 * sa;
-                    const int ib = block_dot(w[5], w[6], w[7], w[8], xb) - 8 * sb;
-                    const float dwa = half_bits_to_float(w[0]);
-                    const float dwb = half_bits_to_float(w[4] >> 16);
-                    acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
-                    acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
-                    if (kDebug) {
-                        int32_t* d = dbg + (c0 + ri) * plan.nb + 2 * p;
-                        d[0] = ia;
-                        d[1] = ib;
-                    }
-                }
-                __syncwarp();
-                acc = warp_sum(acc);
-                if (lane == 0) part[ri * nseg + seg] = acc;
+            // The ring is consumed in a loop unrolled by its depth so every
+            // access to it uses a compile-time index: each step then waits only
+            // for its own loads, issued kDepth steps earlier.
+            const int step = plan.nslots;
+            for (int ri = slot; ri < crows; ri += kDepth * step) {
+                consume(c0, crows, ri, pipe[0]);
+                if (ri + step < crows) consume(c0, crows, ri + step, pipe[1]);
+                if (ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[2]);
             }
         }
         __syncthreads();
