@@ -14,16 +14,22 @@
 // core works on the next block (two accumulator buffers).
 //
 // Warp roles in one persistent CTA per SM (tile 128 weight rows x 128 tokens):
-//   warp 0      producer: 1-D bulk copies (TMA engine) of raw Q4_0 / Q8_0
-//               bytes, 8 blocks per stage, into a ring of shared memory
+//   warp 0      producer: two 2-D tensor copies (TMA) per stage -- a 128-row
+//               box of raw Q4_0 bytes and a 128-token box of raw Q8_0 bytes,
+//               8 blocks wide -- into a ring of shared memory
 //   warp 1      tensor-memory allocator and MMA issuer (one thread)
-//   warps 2-5   converters: raw blocks -> fp16 operand tiles in the
-//               canonical no-swizzle K-major layout (8x16-byte core
-//               matrices), plus per-block fp32 scales
-//   warps 6-21  drain: tcgen05.ld of the block sums, y += d_w d_x isum
+//   warps 2-5   weight converters, warps 6-9 activation converters: raw
+//               blocks -> fp16 operand tiles in the canonical no-swizzle
+//               K-major layout (8x16-byte core matrices) plus per-block fp32
+//               scales; raw rows are read as 16-byte vectors (conflict-free)
+//   warps 10-25 drain: tcgen05.ld of the block sums, y += d_w d_x isum with
+//               packed fp32x2 arithmetic
 // Every wait is bounded; a timeout sets a flag, the CTA stops working,
 // waits for its copies and MMAs in flight, frees tensor memory and exits.
 #include "common.cuh"
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <mutex>
@@ -46,7 +52,7 @@ constexpr int OPB = BN * 32 * 2;         // fp16 B tile of one block
 constexpr int OP_BYTES = OPA + OPB + (BM + BN) * 4;
 constexpr int OS = 4;                    // operand slots
 constexpr int TMEM_COLS = 2 * BN;        // two accumulator buffers
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = 8;                           // 4 for the weights, 4 for the activations
 constexpr int kDrainWarps = 16;                         // 4 lane quarters x 4 column groups of 32
 constexpr int kWarps = 2 + kConvWarps + kDrainWarps;
 constexpr int kThreads = 32 * kWarps;
@@ -55,7 +61,8 @@ constexpr int OFF_BAR = OFF_OPS + OS * OP_BYTES;         // 176128
 constexpr int NBARS = 2 * RS + 2 * OS + 4;
 constexpr size_t kSmem = OFF_BAR + NBARS * 8 + 16;
 
-static_assert(OFF_OPS % 1024 == 0 && OP_BYTES % 1024 == 0, "operand alignment");
+static_assert(OFF_OPS % 1024 == 0 && OP_BYTES % 1024 == 0 && RAW_W % 1024 == 0 && RAW_BYTES % 1024 == 0,
+              "operand and stage alignment");
 
 // Instruction descriptor, kind::f16: D fp32, A/B fp16, both K-major, N>>3, M>>4.
 constexpr uint32_t kIdesc = (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (static_cast<uint32_t>(BM >> 4) << 24);
@@ -85,14 +92,11 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
-        "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -101,6 +105,42 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
     uint32_t d;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
     return d;
+}
+
+// 2-D tiled tensor copy global -> shared (TMA), completion counted on bar.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// (a0, a1) += (s0, s1) * (v0, v1), one packed fp32x2 fused multiply-add.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float s0, float s1, float v0, float v1) {
+    asm("{\n\t.reg .b64 s, v, a;\n\t"
+        "mov.b64 s, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\tmov.b64 a, {%0, %1};\n\t"
+        "fma.rn.f32x2 a, s, v, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s0), "f"(s1), "f"(v0), "f"(v1));
+}
+
+// (d0, d1) = (a0, a1) * (b0, b1), packed fp32x2.
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// The 4-byte word starting at byte offset `off` (even, compile-time) of w[].
+template <int off>
+__device__ __forceinline__ uint32_t word_at(const uint32_t* w) {
+    if constexpr ((off & 3) == 0)
+        return w[off >> 2];
+    else
+        return bytes_2_to_5(w[off >> 2], w[(off >> 2) + 1]);
 }
 
 // Four bytes (0..255 each) -> two fp16x2 words holding 1024 + byte.
@@ -127,6 +167,8 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, vo
 }
 
 struct Args {
+    CUtensorMap wmap;    // Q4_0 bytes: inner dim = row bytes (uint8), outer = O rows
+    CUtensorMap xmap;    // Q8_0 bytes: inner dim = row bytes / 2 (uint16), outer = T tokens
     const uint8_t* W;
     const uint8_t* xq;
     float* y;
@@ -142,7 +184,7 @@ struct Args {
 };
 
 template <bool kDebug>
-__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
+__global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_constant__ Args a) {
     extern __shared__ __align__(1024) uint8_t smem[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
     uint64_t* raw_full = bars;
@@ -190,28 +232,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
-        const uint64_t policy = l2_policy_evict_first();
         int c = 0;
         for (int tile = blockIdx.x; tile < total_tiles && !*abort_flag; tile += gridDim.x) {
             const int m0 = (tile / a.ntiles) * BM;
             const int n0 = (tile % a.ntiles) * BN;
-            const int vrows = min(BM, a.O - m0);
-            const int vtoks = min(BN, a.T - n0);
             for (int ch = 0; ch < nchunks; ++ch, ++c) {
                 const int s = c % RS;
                 if (c >= RS && !__all_sync(0xffffffffu, wait_or_abort(&raw_empty[s], ((c / RS) - 1) & 1, abort_flag)))
                     break;
-                uint8_t* st = smem + s * RAW_BYTES;
-                if (lane == 0) mbar_arrive_expect_tx(&raw_full[s], vrows * (CHUNK * 18) + vtoks * (CHUNK * 34));
-                __syncwarp();
-                for (int i = lane; i < vrows; i += 32)
-                    bulk_g2s(st + i * (CHUNK * 18),
-                             a.W + static_cast<int64_t>(m0 + i) * a.rowbytes + static_cast<int64_t>(ch) * CHUNK * 18,
-                             CHUNK * 18, &raw_full[s], policy);
-                for (int i = lane; i < vtoks; i += 32)
-                    bulk_g2s(st + RAW_W + i * (CHUNK * 34),
-                             a.xq + static_cast<int64_t>(n0 + i) * a.xrow + static_cast<int64_t>(ch) * CHUNK * 34,
-                             CHUNK * 34, &raw_full[s], policy);
+                if (lane == 0) {
+                    // Rows past O / tokens past T are zero-filled by the copy
+                    // and still count toward the transaction bytes.
+                    uint8_t* st = smem + s * RAW_BYTES;
+                    mbar_arrive_expect_tx(&raw_full[s], RAW_BYTES);
+                    tma_load_2d(st, &a.wmap, ch * (CHUNK * 18), m0, &raw_full[s]);
+                    tma_load_2d(st + RAW_W, &a.xmap, ch * (CHUNK * 34 / 2), n0, &raw_full[s]);
+                }
                 __syncwarp();
             }
         }
@@ -251,117 +287,105 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
         __syncwarp();
     } else if (warp < 2 + kConvWarps) {
         // ------------------------------------------------------------ converters
-        const int t = threadIdx.x - 64;   // 0..127: weight row t and token t of the tile
+        const int role = (warp - 2) >> 2;            // 0: weight rows, 1: activation tokens
+        const int t = (threadIdx.x - 64) & 127;      // row / token within the tile
         int g = 0;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
             const int m0 = (tile / a.ntiles) * BM;
             const int n0 = (tile % a.ntiles) * BN;
-            const bool vrow = m0 + t < a.O;
-            const bool vtok = n0 + t < a.T;
-            bool ok = true;
-            for (int b = 0; b < a.nb; ++b, ++g) {
+            const bool valid = role == 0 ? (m0 + t < a.O) : (n0 + t < a.T);
+            for (int ch = 0; ch < nchunks && ok; ++ch) {
                 const int c = g / CHUNK;
                 const int s = c % RS;
-                const int bl = g % CHUNK;
-                const int o = g % OS;
-                if (bl == 0) ok = __all_sync(0xffffffffu, wait_or_abort(&raw_full[s], (c / RS) & 1, abort_flag));
-                if (ok && g >= OS)
-                    ok = __all_sync(0xffffffffu, wait_or_abort(&op_empty[o], ((g / OS) - 1) & 1, abort_flag));
+                ok = __all_sync(0xffffffffu, wait_or_abort(&raw_full[s], (c / RS) & 1, abort_flag));
                 if (!ok) break;
                 const uint8_t* st = smem + s * RAW_BYTES;
-                uint8_t* op = smem + OFF_OPS + o * OP_BYTES;
-                float* dws = reinterpret_cast<float*>(op + OPA + OPB);
-                float* dxs = dws + BM;
-                // ---- A: weight row t, block bl -> 32 fp16 (q - 8)
-                uint4 av[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                               make_uint4(0, 0, 0, 0)};
-                float dw = 0.0f;
-                if (vrow) {
-                    const uint8_t* p = st + t * (CHUNK * 18) + bl * 18;
-                    uint32_t q[4];
-                    uint32_t dbits;
-                    if ((bl & 1) == 0) {
-                        const uint32_t* pw = reinterpret_cast<const uint32_t*>(p);
-                        uint32_t w[5];
 #pragma unroll
-                        for (int i = 0; i < 5; ++i) w[i] = pw[i];
-                        dbits = w[0];
+                for (int bl = 0; bl < CHUNK; ++bl, ++g) {
+                    const int o = g % OS;
+                    if (g >= OS) {
+                        ok = __all_sync(0xffffffffu, wait_or_abort(&op_empty[o], ((g / OS) - 1) & 1, abort_flag));
+                        if (!ok) break;
+                    }
+                    uint8_t* op = smem + OFF_OPS + o * OP_BYTES;
+                    float* dws = reinterpret_cast<float*>(op + OPA + OPB);
+                    float dsc = 0.0f;
+                    if (role == 0) {
+                        // weight row t, block bl: 18 bytes at bl*18 of a 144-byte row, read as
+                        // two 16-byte vectors (row stride 9 x 16 bytes: conflict-free)
+                        const int off = (bl * 18) & 15;
+                        const uint4* rv = reinterpret_cast<const uint4*>(st + t * (CHUNK * 18)) + ((bl * 18) >> 4);
+                        const uint4 c0v = rv[0], c1v = rv[1];
+                        const uint32_t w[8] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y, c1v.z, c1v.w};
+                        uint32_t q[4] = {0u, 0u, 0u, 0u};
+                        if (valid) {
+                            const uint32_t dbits = (off & 3) == 0 ? w[off >> 2] : (w[off >> 2] >> 16);
+                            dsc = half_bits_to_float(dbits);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) q[i] = bytes_2_to_5(w[i], w[i + 1]);
+                            for (int i = 0; i < 4; ++i) {
+                                const int bo = off + 2 + 4 * i;
+                                q[i] = (bo & 3) == 0 ? w[bo >> 2] : bytes_2_to_5(w[bo >> 2], w[(bo >> 2) + 1]);
+                            }
+                        }
+                        // core matrix j holds elements 8j..8j+7: low nibbles of words
+                        // 2j, 2j+1 for j < 2, high nibbles of words 2(j-2), 2(j-2)+1 after
+                        const uint32_t k1032 = 0x64086408u;
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t wa = q[(2 * j) & 3], wb = q[(2 * j + 1) & 3];
+                            const uint32_t na = j < 2 ? (wa & 0x0F0F0F0Fu) : ((wa >> 4) & 0x0F0F0F0Fu);
+                            const uint32_t nb2 = j < 2 ? (wb & 0x0F0F0F0Fu) : ((wb >> 4) & 0x0F0F0F0Fu);
+                            uint32_t a01, a23, b01, b23;
+                            bytes_to_f16x2(na, a01, a23);
+                            bytes_to_f16x2(nb2, b01, b23);
+                            uint4 v = make_uint4(hsub2(a01, k1032), hsub2(a23, k1032), hsub2(b01, k1032),
+                                                 hsub2(b23, k1032));
+                            if (!valid) v = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4*>(op + ((t >> 3) * 4 + j) * 128 + (t & 7) * 16) = v;
+                        }
+                        dws[t] = dsc;
                     } else {
-                        dbits = *reinterpret_cast<const uint32_t*>(p - 2) >> 16;
-                        const uint32_t* pw = reinterpret_cast<const uint32_t*>(p + 2);
+                        // token t, block bl: 34 bytes at bl*34 of a 272-byte row, three 16-byte vectors
+                        const int off = (bl * 34) & 15;
+                        const uint4* rv =
+                            reinterpret_cast<const uint4*>(st + RAW_W + t * (CHUNK * 34)) + ((bl * 34) >> 4);
+                        const uint4 c0v = rv[0], c1v = rv[1], c2v = rv[2];
+                        const uint32_t w[12] = {c0v.x, c0v.y, c0v.z, c0v.w, c1v.x, c1v.y,
+                                                c1v.z, c1v.w, c2v.x, c2v.y, c2v.z, c2v.w};
+                        if (valid) {
+                            const uint32_t dbits = (off & 3) == 0 ? w[off >> 2] : (w[off >> 2] >> 16);
+                            dsc = half_bits_to_float(dbits);
+                        }
+                        const uint32_t k1152 = 0x64806480u;
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) q[i] = pw[i];
+                        for (int j = 0; j < 4; ++j) {
+                            uint32_t hv[4];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int bo = off + 2 + 4 * (2 * j + u);
+                                const uint32_t q =
+                                    (bo & 3) == 0 ? w[bo >> 2] : bytes_2_to_5(w[bo >> 2], w[(bo >> 2) + 1]);
+                                uint32_t h01, h23;
+                                bytes_to_f16x2(q ^ 0x80808080u, h01, h23);
+                                hv[2 * u] = hsub2(h01, k1152);
+                                hv[2 * u + 1] = hsub2(h23, k1152);
+                            }
+                            uint4 v = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+                            if (!valid) v = make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4*>(op + OPA + ((t >> 3) * 4 + j) * 128 + (t & 7) * 16) = v;
+                        }
+                        dws[BM + t] = dsc;
                     }
-                    dw = half_bits_to_float(dbits);
-                    const uint32_t k1032 = 0x64086408u;
-                    uint32_t h[16];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        uint32_t a01, a23, b01, b23;
-                        bytes_to_f16x2(q[i] & 0x0F0F0F0Fu, a01, a23);
-                        bytes_to_f16x2((q[i] >> 4) & 0x0F0F0F0Fu, b01, b23);
-                        h[2 * i] = hsub2(a01, k1032);          // elements 4i, 4i+1
-                        h[2 * i + 1] = hsub2(a23, k1032);      // 4i+2, 4i+3
-                        h[8 + 2 * i] = hsub2(b01, k1032);      // 16+4i, 16+4i+1
-                        h[8 + 2 * i + 1] = hsub2(b23, k1032);
+                    // generic-proxy writes -> visible to the tensor core (async proxy)
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&op_full[o]);
+                        if (bl == CHUNK - 1) mbar_arrive(&raw_empty[s]);
                     }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) av[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(op + ((t >> 3) * 4 + j) * 128 + (t & 7) * 16) = av[j];
-                dws[t] = dw;
-                // ---- B: token t, block bl -> 32 fp16 q
-                uint4 bv[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
-                               make_uint4(0, 0, 0, 0)};
-                float dx = 0.0f;
-                if (vtok) {
-                    const uint8_t* p = st + RAW_W + t * (CHUNK * 34) + bl * 34;
-                    uint32_t q[8];
-                    uint32_t dbits;
-                    if ((bl & 1) == 0) {
-                        const uint32_t* pw = reinterpret_cast<const uint32_t*>(p);
-                        uint32_t w[9];
-#pragma unroll
-                        for (int i = 0; i < 9; ++i) w[i] = pw[i];
-                        dbits = w[0];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) q[i] = bytes_2_to_5(w[i], w[i + 1]);
-                    } else {
-                        dbits = *reinterpret_cast<const uint32_t*>(p - 2) >> 16;
-                        const uint32_t* pw = reinterpret_cast<const uint32_t*>(p + 2);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) q[i] = pw[i];
-                    }
-                    dx = half_bits_to_float(dbits);
-                    const uint32_t k1152 = 0x64806480u;
-                    uint32_t h[16];
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        uint32_t h01, h23;
-                        bytes_to_f16x2(q[i] ^ 0x80808080u, h01, h23);
-                        h[2 * i] = hsub2(h01, k1152);
-                        h[2 * i + 1] = hsub2(h23, k1152);
-                    }
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) bv[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-                }
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(op + OPA + ((t >> 3) * 4 + j) * 128 + (t & 7) * 16) = bv[j];
-                dxs[t] = dx;
-                // generic-proxy writes -> visible to the tensor core (async proxy)
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&op_full[o]);
-                    if (bl == CHUNK - 1) mbar_arrive(&raw_empty[s]);
                 }
             }
-            if (!ok) break;
         }
     } else {
         // ------------------------------------------------------------ drain
@@ -382,31 +406,42 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
                 ok = __all_sync(0xffffffffu, wait_or_abort(&tm_full[buf], (g / 2) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
-                uint32_t v[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(dq * 32) << 16) + static_cast<uint32_t>(buf * BN + 32 * h), v);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tm_empty[buf]);
+                const uint32_t taddr =
+                    tmem + (static_cast<uint32_t>(dq * 32) << 16) + static_cast<uint32_t>(buf * BN + 32 * h);
                 const uint8_t* op = smem + OFF_OPS + o * OP_BYTES;
                 const float* dws = reinterpret_cast<const float*>(op + OPA + OPB);
                 const float4* dx4 = reinterpret_cast<const float4*>(dws + BM + 32 * h);
                 const float dw = dws[r];
+                // two halves of 16 columns keep the live registers down
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 dx = dx4[j4];
-                    acc[4 * j4 + 0] = __fmaf_rn(__fmul_rn(dw, dx.x), __uint_as_float(v[4 * j4 + 0]), acc[4 * j4 + 0]);
-                    acc[4 * j4 + 1] = __fmaf_rn(__fmul_rn(dw, dx.y), __uint_as_float(v[4 * j4 + 1]), acc[4 * j4 + 1]);
-                    acc[4 * j4 + 2] = __fmaf_rn(__fmul_rn(dw, dx.z), __uint_as_float(v[4 * j4 + 2]), acc[4 * j4 + 2]);
-                    acc[4 * j4 + 3] = __fmaf_rn(__fmul_rn(dw, dx.w), __uint_as_float(v[4 * j4 + 3]), acc[4 * j4 + 3]);
-                }
-                if (kDebug) {
-                    if (m0 + r < a.O) {
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[16];
+                    tmem_ld16(taddr + 16 * half, v);
+                    if (half == 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&tm_empty[buf]);
+                    }
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            const int tok = n0 + 32 * h + j;
-                            if (tok < a.T)
-                                a.dbg[(static_cast<int64_t>(tok) * a.O + m0 + r) * a.nb + b] =
-                                    static_cast<int32_t>(__uint_as_float(v[j]));
+                    for (int j4 = 0; j4 < 4; ++j4) {
+                        const float4 dx = dx4[4 * half + j4];
+                        const int j = 16 * half + 4 * j4;
+                        float s0, s1, s2, s3;
+                        fmul2(s0, s1, dw, dw, dx.x, dx.y);   // per-element scale d_w * d_x
+                        fmul2(s2, s3, dw, dw, dx.z, dx.w);
+                        ffma2(acc[j], acc[j + 1], s0, s1, __uint_as_float(v[4 * j4]), __uint_as_float(v[4 * j4 + 1]));
+                        ffma2(acc[j + 2], acc[j + 3], s2, s3, __uint_as_float(v[4 * j4 + 2]),
+                              __uint_as_float(v[4 * j4 + 3]));
+                    }
+                    if (kDebug) {
+                        if (m0 + r < a.O) {
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) {
+                                const int tok = n0 + 32 * h + 16 * half + jj;
+                                if (tok < a.T)
+                                    a.dbg[(static_cast<int64_t>(tok) * a.O + m0 + r) * a.nb + b] =
+                                        static_cast<int32_t>(__uint_as_float(v[jj]));
+                            }
                         }
                     }
                 }
@@ -434,6 +469,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(Args a) {
 std::mutex g_attr_mutex;
 bool g_attr_done[2] = {false, false};
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        cudaGetLastError();
+    });
+    return fn;
+}
+
+// Rank-2 map over a row-major byte matrix read in boxes of box_bytes x 128 rows.
+bool encode_rows(CUtensorMap* map, const void* base, int64_t row_bytes, int64_t rows, int box_bytes,
+                 bool u16) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int esz = u16 ? 2 : 1;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / esz), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / esz), 128u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, u16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
+               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <bool kDebug>
 cudaError_t ensure_smem() {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
@@ -456,7 +521,7 @@ int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O,
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     if (kSmem > dev.smem_optin) return QDG_ECUDA;
-    Args a;
+    Args a{};
     a.W = static_cast<const uint8_t*>(W);
     a.xq = static_cast<const uint8_t*>(xq);
     a.y = y;
@@ -469,6 +534,9 @@ int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O,
     a.xrow = a.nb * 34;
     a.mtiles = static_cast<int>((O + BM - 1) / BM);
     a.ntiles = static_cast<int>((T + BN - 1) / BN);
+    if (!encode_rows(&a.wmap, W, a.rowbytes, O, CHUNK * 18, false) ||
+        !encode_rows(&a.xmap, xq, a.xrow, T, CHUNK * 34, true))
+        return QDG_ECUDA;
     const int64_t tiles = static_cast<int64_t>(a.mtiles) * a.ntiles;
     if (tiles > (1 << 30)) return QDG_ESHAPE;
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, tiles));
