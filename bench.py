@@ -175,15 +175,23 @@ def barrier(world):
 
 # ---------------------------------------------------------------- workload bytes
 def step_bytes(wl):
-    """Algorithmic bytes of one decode step: every GEMV's W + xq + y, and every
-    quantization's x (+ gamma) read and xq write."""
+    """Algorithmic bytes of one decode step -- what it must move at least once:
+    every projection's Q4_0 weights and fp32 outputs, every fp32 activation
+    vector and every gamma.  The same count serves the fused and the unfused
+    route (the unfused one also writes and reads the Q8_0 vectors, ~0.01%)."""
     total = 0
     for m in wl.matrices:
-        total += workloads.gemv_algorithmic_bytes(m.rows, m.cols)
+        total += workloads.q4_0_bytes(m.rows, m.cols) + 4 * m.rows
     for tag, K in wl.activations.items():
         norm = any(m.source == f"norm:{tag}" for m in wl.matrices)
-        total += 4 * K + (4 * K if norm else 0) + workloads.q8_0_bytes(1, K)
+        total += 4 * K + (4 * K if norm else 0)
     return total
+
+
+def fused_launch_bytes(m):
+    """Algorithmic bytes of one fused norm+GEMV launch: W, x, gamma (if any), y."""
+    norm = m.source.startswith("norm:")
+    return workloads.q4_0_bytes(m.rows, m.cols) + 4 * m.cols * (2 if norm else 1) + 4 * m.rows
 
 
 def activation_kinds(wl):
@@ -286,7 +294,6 @@ class DecodeStep:
                                                                 outlier_frac=wl.outlier_frac)[0]).pin_memory()
                         for tag, K in wl.activations.items()} for p in range(N_INPUT_SETS)]
         self.x_dev = [{tag: t.to(device) for tag, t in xs.items()} for xs in self.x_host]
-        self.x_stage = {tag: torch.empty(K, dtype=torch.float32, device=device) for tag, K in wl.activations.items()}
         self.xq = {tag: torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
                    for tag, K in wl.activations.items()}
         self.y = {m.name: torch.empty(m.rows, dtype=torch.float32, device=device) for m in wl.matrices}
@@ -294,11 +301,22 @@ class DecodeStep:
         torch.cuda.synchronize()
         torch.cuda.empty_cache()      # release the fp32 staging of the weights
 
-    def launches_per_step(self):
-        return len(self.wl.activations) + len(self.wl.matrices)
+    def launches_per_step(self, fused=True):
+        return len(self.wl.matrices) + (0 if fused else len(self.wl.activations))
 
-    def run(self, xs, events=None):
+    def run(self, xs, events=None, fused=True):
         qdg = self.qdg
+        if fused:
+            # one launch per projection: RMSNorm*gamma -> Q8_0 -> GEMV
+            for i, m in enumerate(self.wl.matrices):
+                tag = m.source.split(":", 1)[1]
+                if events:
+                    events[i].record()
+                qdg.q4_0_gemv_rmsnorm(self.W[m.name], xs[tag], self.gamma.get(tag) if self.kinds[tag] == "norm"
+                                      else None, self.wl.eps, self.y[m.name], m.rows, m.cols)
+            if events:
+                events[len(self.wl.matrices)].record()
+            return
         i = 0
         for tag, K in self.wl.activations.items():
             g = self.gamma.get(tag)
@@ -316,6 +334,16 @@ class DecodeStep:
             events[i].record()
 
 
+def capture(fn, side, count=1):
+    """CUDA graph of `count` calls of fn (on the side stream)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        for _ in range(count):
+            fn()
+    return g
+
+
 def bench_ours(args, wl, world, rank, local):
     import torch
     from quantized_decode_gemv_rms_gb300 import qdg
@@ -326,32 +354,41 @@ def bench_ours(args, wl, world, rank, local):
     step = DecodeStep(wl, device)
     stream = torch.cuda.current_stream()
     nbytes = step_bytes(wl)
-    L = step.launches_per_step()
+    fused = not args.unfused
+    L = step.launches_per_step(fused)
 
-    # eager warm-up (also sets kernel attributes before capture)
-    for i in range(3):
-        step.run(step.x_dev[i % N_INPUT_SETS])
+    # eager warm-up of both routes (also sets kernel attributes before capture)
+    for fz in (True, False):
+        for i in range(3):
+            step.run(step.x_dev[i % N_INPUT_SETS], fused=fz)
     torch.cuda.synchronize()
     assert qdg.qdg_device_status() == qdg.QDG_OK
 
-    graphs = []
-    if args.graph:
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            for p in range(N_INPUT_SETS):
-                g = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(g, stream=side):
-                    step.run(step.x_dev[p])
-                graphs.append(g)
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
+    # graphs: one per input set and route; the launch counters, read around the
+    # capture of the timed route, tell which kernels the step consists of
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    graphs = {}
+    counts = {}
+    with torch.cuda.stream(side):
+        for fz in (fused, not fused):
+            before = [qdg.qdg_launch_count(i) for i in range(6)]
+            graphs[fz] = [capture(lambda p=p: step.run(step.x_dev[p], fused=fz), side) for p in range(N_INPUT_SETS)]
+            after = [qdg.qdg_launch_count(i) for i in range(6)]
+            counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(6)]
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    if fused:
+        assert counts[True][5] == len(wl.matrices) and counts[True][0] == 0 and counts[True][1] == 0, counts
+    fusion = {"route": "fused" if fused else "unfused",
+              "per_step_launches": {"fused_norm_gemv": counts[fused][5], "standalone_quantize": counts[fused][0],
+                                    "gemv": counts[fused][1]}}
 
-    def one_step(k):
-        if graphs:
-            graphs[k % N_INPUT_SETS].replay()
+    def one_step(k, fz=fused):
+        if args.graph:
+            graphs[fz][k % N_INPUT_SETS].replay()
         else:
-            step.run(step.x_dev[k % N_INPUT_SETS])
+            step.run(step.x_dev[k % N_INPUT_SETS], fused=fz)
 
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -359,8 +396,7 @@ def bench_ours(args, wl, world, rank, local):
         smi_id = str(local)
     sampler = ClockSampler(smi_id)
     sampler.start()
-    # pre-roll so the clock sampler sees the GPU under this load
-    t_end = time.time() + 0.6
+    t_end = time.time() + 0.6                       # pre-roll: clocks under this load
     k = 0
     while time.time() < t_end:
         one_step(k)
@@ -372,8 +408,6 @@ def bench_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    launches0 = qdg.qdg_launch_count(-1)
-    graph_launches0 = 0
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     sampler.mark("t0")
@@ -385,16 +419,11 @@ def bench_ours(args, wl, world, rank, local):
     sampler.mark("t1")
     barrier(world)
     torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.steps
-    ms = max_over_ranks(ms, world, device)
-    launches = qdg.qdg_launch_count(-1) - launches0
-    gpu_launches = launches if not graphs else L * args.steps
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world, device)
     status = qdg.qdg_device_status()
     if status != qdg.QDG_OK:
         raise RuntimeError(f"device status after timed region: {qdg.status_string(status)}")
-
-    # post-roll for the clock sampler
-    t_end = time.time() + 0.3
+    t_end = time.time() + 0.3                       # post-roll
     k = 0
     while time.time() < t_end:
         one_step(k)
@@ -404,53 +433,79 @@ def bench_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     clocks = sampler.stop()
 
-    # ---- instrumented pass: per-launch events (eager launches, same kernels)
-    n_inst = max(20, min(args.steps, 200))
-    per = {m.name: [] for m in wl.matrices}
-    qn = []
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for _ in range(n_inst)]
-    for k in range(n_inst):
-        step.run(step.x_dev[k % N_INPUT_SETS], events=evs[k])
+    # ---- the other route, same number of steps, for comparison
+    for k in range(args.warmup):
+        one_step(k, not fused)
     torch.cuda.synchronize()
-    for k in range(n_inst):
-        ev = evs[k]
-        na = len(wl.activations)
-        qn.append(sum(ev[i].elapsed_time(ev[i + 1]) for i in range(na)) * 1e3 / na)
-        for j, m in enumerate(wl.matrices):
-            per[m.name].append(ev[na + j].elapsed_time(ev[na + j + 1]) * 1e3)
-    us_per_call = {name: float(np.median(v)) for name, v in per.items()}
-    gemv_bytes = {m.name: workloads.gemv_algorithmic_bytes(m.rows, m.cols) for m in wl.matrices}
-    tot_b = sum(gemv_bytes.values())
-    tot_us = sum(us_per_call.values())
-    achieved = tot_b / (tot_us * 1e-6) / 1e9
-    gbs_per_call = {n: gemv_bytes[n] / (us_per_call[n] * 1e-6) / 1e9 for n in us_per_call}
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for k in range(args.steps):
+        one_step(k, not fused)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ms_other = f0.elapsed_time(f1) / args.steps
 
-    # ---- end-to-end pass through the same calls with host buffers
+    # ---- per-matrix cost: a graph of 20 back-to-back launches of one projection
+    per_call = {}
+    with torch.cuda.stream(side):
+        for m in wl.matrices:
+            tag = m.source.split(":", 1)[1]
+            g = step.gamma.get(tag) if step.kinds[tag] == "norm" else None
+            fn = (lambda m=m, tag=tag, g=g: qdg.q4_0_gemv_rmsnorm(step.W[m.name], step.x_dev[0][tag], g, wl.eps,
+                                                                  step.y[m.name], m.rows, m.cols))
+            gr = capture(fn, side, 20)
+            gr.replay()
+            side.synchronize()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(side)
+            for _ in range(5):
+                gr.replay()
+            a1.record(side)
+            side.synchronize()
+            per_call[m.name] = a0.elapsed_time(a1) * 1e3 / 100
+            del gr
+    torch.cuda.synchronize()
+    launch_bytes = {m.name: fused_launch_bytes(m) for m in wl.matrices}
+    gbs_per_call = {n: launch_bytes[n] / (per_call[n] * 1e-6) / 1e9 for n in per_call}
+
+    # ---- end to end through the same calls, inputs from pinned host memory
     n_e2e = max(10, min(args.steps, 500))
     h2d = sum(t.numel() * 4 for t in step.x_host[0].values())
     d2h = sum(t.numel() * 4 for t in step.y_host.values())
     for k in range(3):
-        _e2e_step(step, graphs, k)
+        _e2e_step(step, graphs[fused] if args.graph else None, k, fused)
     torch.cuda.synchronize()
     barrier(world)
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     for k in range(n_e2e):
-        _e2e_step(step, graphs, k)
+        _e2e_step(step, graphs[fused] if args.graph else None, k, fused)
     f1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
 
     peaks, peak_src = measured_peaks()
-    traffic = ncu_traffic("gemv.cu")
-    roof = {"bound": "hbm", "kernel": "gemv_kernel", "achieved": round(achieved, 1),
-            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)" if peak_src == "measured"
-            else "fallback 6.8 TB/s",
+    if fused:
+        # Every launch of the fused step is the fused GEMV kernel: its average
+        # launch duration is at most the step time over the launches per step.
+        kern_bytes = sum(launch_bytes.values())
+        achieved = kern_bytes / (ms * 1e-3) / 1e9
+        kernel = "gemv_kernel<fused> (q4_0_gemv_rmsnorm)"
+        traffic = ncu_traffic("gemv.cu")
+    else:
+        kern_bytes = sum(workloads.gemv_algorithmic_bytes(m.rows, m.cols) for m in wl.matrices)
+        achieved = kern_bytes / (sum(per_call.values()) * 1e-6) / 1e9
+        kernel = "gemv_kernel (per-matrix graphs)"
+        traffic = None
+    roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)" if peak_src == "measured"
+                            else "fallback 6.8 TB/s"),
             "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
-            "traffic_source": (traffic.get("what") if traffic else "no ncu summary for this source"),
-            "algorithmic_bytes_per_step_gemv": tot_b,
+            "traffic_source": (traffic.get("what") if traffic else "no ncu capture of this source yet"),
+            "algorithmic_bytes_per_launch": round(kern_bytes / len(wl.matrices)),
+            "launches_per_step": len(wl.matrices),
             "frac_of_nominal_8TB": round(achieved / 8000.0, 4)}
     result = {
         "metric": METRIC, "value": round(nbytes * world / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
@@ -460,16 +515,22 @@ def bench_ours(args, wl, world, rank, local):
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations with 1% x20 outliers)",
         "config": {"workload": wl.name, "batch": 1, "matrices": {m.name: [m.rows, m.cols] for m in wl.matrices},
                    "bytes_per_step": nbytes, "l2": "inputs larger than L2 (419 MB of weights per step vs 129 MB L2)",
-                   "launch": ("cuda graph" if graphs else "eager") + (" + PDL" if args.pdl else ""),
+                   "route": "fused RMSNorm->Q8_0->GEMV, one launch per projection" if fused
+                   else "standalone quantize + GEMV",
+                   "launch": ("cuda graph" if args.graph else "eager") + (" + PDL" if args.pdl else ""),
                    "parallelism": f"replicas x{world}"},
         "us_per_step": round(ms * 1e3, 2),
-        "us_per_call": {k: round(v, 2) for k, v in us_per_call.items()},
+        "us_per_call": {k: round(v, 2) for k, v in per_call.items()},
         "gbs_per_call": {k: round(v, 1) for k, v in gbs_per_call.items()},
-        "qnorm_us_per_call": round(float(np.median(qn)), 2),
+        "per_call_note": "fused launch, graph of 20 back-to-back launches of one projection, PDL as configured",
+        "other_route": {"route": "standalone quantize + GEMV" if fused else "fused",
+                        "us_per_step": round(ms_other * 1e3, 2),
+                        "value": round(nbytes / (ms_other * 1e-3) / 1e9, 1)},
+        "fusion_check": fusion,
         "roofline": roof,
         "e2e": {"value": round(nbytes * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": UNIT,
                 "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": int(gpu_launches),
+        "gpu_launches": int(L * args.steps),
         "clocks": clocks,
     }
     return result, step
@@ -542,14 +603,14 @@ def bench_extras(args, device):
     return out
 
 
-def _e2e_step(step, graphs, k):
+def _e2e_step(step, graphs, k, fused=True):
     p = k % N_INPUT_SETS
     for tag, t in step.x_host[p].items():
         step.x_dev[p][tag].copy_(t, non_blocking=True)
     if graphs:
         graphs[p].replay()
     else:
-        step.run(step.x_dev[p])
+        step.run(step.x_dev[p], fused=fused)
     for name, t in step.y_host.items():
         t.copy_(step.y[name], non_blocking=True)
 
@@ -562,6 +623,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.LLAMA_8B.name, choices=sorted(workloads.ALL))
     ap.add_argument("--no-graph", dest="graph", action="store_false")
+    ap.add_argument("--unfused", action="store_true",
+                    help="time the standalone quantize + GEMV route (the fused route is the default)")
     ap.add_argument("--pdl", action="store_true", default=True)
     ap.add_argument("--no-pdl", dest="pdl", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")

@@ -108,6 +108,27 @@ QDG_API int q4_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, i
                    qdg_stream_t stream);
 
 /*
+ * q4_0_gemv_rmsnorm -- the fused decode route: RMS_NORM + MUL(gamma) + Q8_0
+ * quantization + Q4_0 x Q8_0 GEMV in one kernel.  The norm/MUL pair is the
+ * pattern whose fusion the Metal backend lost (about 5% of token generation)
+ *   [llama.cpp b10909, introduction]; here the quantization and the product
+ *   join it, so a decode projection is a single launch.
+ *
+ * W      [O][K/32] Q4_0, 16-byte aligned.
+ * x      [K] fp32, 16-byte aligned.   gamma [K] fp32, 16-byte aligned, or NULL
+ *        for plain quantization.   eps >= 0 (inside the square root).
+ * y      [O] fp32 (overwritten).
+ * xq_out [K/32] Q8_0 or NULL: if given, receives the quantized activations.
+ * K      multiple of 256, 256 <= K <= 32768.
+ * The quantized activations are bit-identical to qnorm_quantize_q8_0's and y
+ * is bit-identical to q4_0_q8_0_gemv on them.  Every CTA recomputes the
+ * norm (the vector is small and L2-resident) while its first weight segments
+ * are already in flight.
+ */
+QDG_API int q4_0_gemv_rmsnorm(const void* W, const float* x, const float* gamma, float eps, float* y,
+                              int64_t O, int64_t K, void* xq_out, qdg_stream_t stream);
+
+/*
  * q4_0_q8_0_gemm_small_n -- Y = W * X for 1 <= N <= 8 Q8_0 vectors sharing
  * one pass over W (speculative / parallel decode; the "vector case" of the
  * mmvq route)  [same page and section].
@@ -171,7 +192,7 @@ QDG_API int qdg_set_option(int option, int64_t value);
 /*
  * qdg_launch_count -- number of kernels this library has launched in this
  * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
- * 4 weight quantize, -1 total.  Lets a caller check that the fused kernel
+ * 4 weight quantize, 5 fused norm+gemv, -1 total.  Lets a caller check that the fused kernel
  * is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);

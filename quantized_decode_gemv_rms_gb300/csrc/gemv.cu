@@ -32,6 +32,8 @@
 
 namespace qdg {
 
+static __device__ unsigned g_flags_gemv;
+
 namespace {
 
 constexpr int kWarps = 16;
@@ -87,12 +89,104 @@ struct SegRegs {
     uint4 v[3];
 };
 
-template <bool kDebug>
-__global__ void __launch_bounds__(kThreads, 1)
-gemv_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq, float* __restrict__ y, int64_t O,
-            Plan plan, int32_t* __restrict__ dbg) {
+struct Args {
+    const uint8_t* W;
+    const uint8_t* xq;      // Q8_0 activations (unfused form)
+    const float* x;         // fp32 activations (fused form)
+    const float* gamma;     // fused form: NULL = plain quantization
+    uint8_t* xq_out;        // fused form: optional copy of the Q8_0 activations (written by CTA 0)
+    float* y;
+    int32_t* dbg;
+    int64_t O;
+    int K;
+    float eps;
+};
+
+// Fused form: RMS_NORM * gamma -> Q8_0 of the two blocks of pair p, computed by
+// the lane that owns the pair, with exactly the arithmetic of the standalone
+// quantize kernel (same s, same products, same IEEE divisions and rounding).
+__device__ __forceinline__ void quantize_pair(const float* __restrict__ x, const float* __restrict__ gamma, float s,
+                                              int p, uint32_t (&xa)[8], uint32_t (&xb)[8], float& dxa, float& dxb,
+                                              int& sa, int& sb, uint32_t (&blk)[17]) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        const float4* xv = reinterpret_cast<const float4*>(x + p * 64 + half * 32);
+        const float4* gv = reinterpret_cast<const float4*>(gamma + p * 64 + half * 32);
+        float v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 a = __ldg(xv + i);
+            v[4 * i] = a.x;
+            v[4 * i + 1] = a.y;
+            v[4 * i + 2] = a.z;
+            v[4 * i + 3] = a.w;
+        }
+        if (gamma != nullptr) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 g = __ldg(gv + i);
+                v[4 * i] = __fmul_rn(__fmul_rn(v[4 * i], s), g.x);
+                v[4 * i + 1] = __fmul_rn(__fmul_rn(v[4 * i + 1], s), g.y);
+                v[4 * i + 2] = __fmul_rn(__fmul_rn(v[4 * i + 2], s), g.z);
+                v[4 * i + 3] = __fmul_rn(__fmul_rn(v[4 * i + 3], s), g.w);
+            }
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const __half dh = __float2half_rn(d);
+        if (__hisinf(dh)) atomicOr(&g_flags_gemv, FLAG_OVERFLOW);
+        uint32_t w[8];
+        int qs = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            uint32_t word = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                int q = 0;
+                if (d != 0.0f) {
+                    float r = roundf(__fdiv_rn(v[4 * i + j], d));
+                    r = fminf(fmaxf(r, -127.0f), 127.0f);
+                    q = static_cast<int>(r);
+                }
+                qs += q;
+                word |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * j);
+            }
+            w[i] = word;
+        }
+        const uint32_t dbits = __half_as_ushort(dh);
+        if (half == 0) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xa[i] = w[i];
+            dxa = __half2float(dh);
+            sa = qs;
+            // Q8_0 block bytes: d (2 bytes) then 32 q, packed into the 68-byte pair
+            blk[0] = dbits | (w[0] << 16);
+#pragma unroll
+            for (int i = 1; i < 8; ++i) blk[i] = (w[i - 1] >> 16) | (w[i] << 16);
+            blk[8] = w[7] >> 16;
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xb[i] = w[i];
+            dxb = __half2float(dh);
+            sb = qs;
+            blk[8] |= dbits << 16;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) blk[9 + i] = w[i];
+        }
+    }
+}
+
+template <bool kFused, bool kDebug>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan plan) {
     __shared__ __align__(16) uint8_t seg_buf[kWarps][kSegBytes];
     __shared__ float part[kPartFloats];
+    __shared__ float norm_part[8];
+    const uint8_t* __restrict__ W = a.W;
+    float* __restrict__ y = a.y;
+    int32_t* __restrict__ dbg = a.dbg;
+    const int64_t O = a.O;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -138,8 +232,48 @@ gemv_kernel(const uint8_t* __restrict__ W, const uint8_t* __restrict__ xq, float
     uint32_t xa[8], xb[8];
     float dxa = 0.0f, dxb = 0.0f;
     int sa = 0, sb = 0;
-    if (active) {
-        const uint32_t* xp = reinterpret_cast<const uint32_t*>(xq + static_cast<size_t>(p) * 68);
+    if (kFused) {
+        // RMS statistic in the library's fixed order: chain j (threads 0..255)
+        // sums x_i^2 over i = j (mod 256) ascending with fma; warp butterflies;
+        // ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).
+        float s = 1.0f;
+        if (a.gamma != nullptr) {
+            if (threadIdx.x < 256) {
+                float acc = 0.0f;
+                for (int i0 = threadIdx.x; i0 < a.K; i0 += 256 * 8) {
+                    float v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int i = i0 + u * 256;
+                        v[u] = i < a.K ? __ldg(a.x + i) : 0.0f;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (i0 + u * 256 < a.K) acc = __fmaf_rn(v[u], v[u], acc);
+                }
+                acc = warp_sum(acc);
+                if (lane == 0) norm_part[warp] = acc;
+            }
+            __syncthreads();
+            const float ss = __fadd_rn(__fadd_rn(__fadd_rn(norm_part[0], norm_part[1]), __fadd_rn(norm_part[2], norm_part[3])),
+                                       __fadd_rn(__fadd_rn(norm_part[4], norm_part[5]), __fadd_rn(norm_part[6], norm_part[7])));
+            const float mean = __fdiv_rn(ss, static_cast<float>(a.K));
+            s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
+        }
+        if (active) {
+            uint32_t blk[17];
+            quantize_pair(a.x, a.gamma, s, p, xa, xb, dxa, dxb, sa, sb, blk);
+            if (a.xq_out != nullptr && blockIdx.x == 0 && slot == 0) {
+                uint32_t* dst = reinterpret_cast<uint32_t*>(a.xq_out + static_cast<size_t>(p) * 68);
+#pragma unroll
+                for (int i = 0; i < 17; ++i) dst[i] = blk[i];
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xa[i] = xb[i] = 0u;
+        }
+    } else if (active) {
+        const uint32_t* xp = reinterpret_cast<const uint32_t*>(a.xq + static_cast<size_t>(p) * 68);
         uint32_t w[17];
 #pragma unroll
         for (int i = 0; i < 17; ++i) w[i] = __ldg(xp + i);
@@ -235,20 +369,61 @@ int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, c
     if (dev.device < 0) return QDG_ECUDA;
     const Plan plan = make_plan(K);
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
+    Args a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.y = y;
+    a.dbg = dbg;
+    a.O = O;
+    a.K = static_cast<int>(K);
     cudaError_t e;
     if (dbg)
-        e = launch(gemv_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, false, static_cast<const uint8_t*>(W),
-                   static_cast<const uint8_t*>(xq), y, O, plan, dbg);
+        e = launch(gemv_kernel<false, true>, dim3(grid), dim3(kThreads), 0, stream, false, a, plan);
     else
-        e = launch(gemv_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, true, static_cast<const uint8_t*>(W),
-                   static_cast<const uint8_t*>(xq), y, O, plan, static_cast<int32_t*>(nullptr));
+        e = launch(gemv_kernel<false, false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(1);
     return QDG_OK;
 }
 
-// The GEMV has no bounded waits (only __syncthreads), so it never raises a flag.
-unsigned flags_read_clear_gemv(cudaStream_t) { return 0; }
+int gemv_rmsnorm_launch(const void* W, const float* x, const float* gamma, float eps, float* y, int64_t O, int64_t K,
+                        void* xq_out, cudaStream_t stream) {
+    if (!W || !x || !y) return QDG_EINVAL;
+    if (O <= 0 || K <= 0) return QDG_EINVAL;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
+    if (K % 256 != 0 || K > 32768 || O >= (int64_t(1) << 31)) return QDG_ESHAPE;
+    if (!aligned(W, 16) || !aligned(x, 16) || (gamma && !aligned(gamma, 16)) || !aligned(y, 4) ||
+        !aligned(xq_out, 4))
+        return QDG_EALIGN;
+    const DeviceInfo dev = device_info();
+    if (dev.device < 0) return QDG_ECUDA;
+    const Plan plan = make_plan(K);
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
+    Args a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.x = x;
+    a.gamma = gamma;
+    a.eps = eps;
+    a.xq_out = static_cast<uint8_t*>(xq_out);
+    a.y = y;
+    a.O = O;
+    a.K = static_cast<int>(K);
+    const cudaError_t e = launch(gemv_kernel<true, false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
+    if (e != cudaSuccess) return QDG_ECUDA;
+    count_launch(5);
+    return QDG_OK;
+}
+
+unsigned flags_read_clear_gemv(cudaStream_t stream) {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_flags_gemv, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return ~0u;
+    if (cudaMemcpyToSymbolAsync(g_flags_gemv, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+        return ~0u;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ~0u;
+    return v;
+}
 
 }  // namespace qdg
 
@@ -256,4 +431,9 @@ extern "C" int q4_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O
                               qdg_stream_t stream) {
     if (!y) return QDG_EINVAL;
     return qdg::gemv_launch(W, xq, y, O, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" int q4_0_gemv_rmsnorm(const void* W, const float* x, const float* gamma, float eps, float* y, int64_t O,
+                                 int64_t K, void* xq_out, qdg_stream_t stream) {
+    return qdg::gemv_rmsnorm_launch(W, x, gamma, eps, y, O, K, xq_out, reinterpret_cast<cudaStream_t>(stream));
 }

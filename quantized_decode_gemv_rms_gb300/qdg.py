@@ -49,6 +49,7 @@ def lib() -> ctypes.CDLL:
             sig = {
                 "qnorm_quantize_q8_0": ([p, i64, p, f32, i64, i64, p, p], i32),
                 "q4_0_q8_0_gemv": ([p, p, p, i64, i64, p], i32),
+                "q4_0_gemv_rmsnorm": ([p, p, p, f32, p, i64, i64, p, p], i32),
                 "q4_0_q8_0_gemm_small_n": ([p, p, p, i64, i64, i64, i64, p], i32),
                 "quantize_q4_0": ([p, i64, i64, i64, p, p], i32),
                 "qdg_device_status": ([p], i32),
@@ -125,6 +126,12 @@ def qnorm_quantize_q8_0(x, gamma, eps: float, xq, K: int | None = None, N: int |
 
 def q4_0_q8_0_gemv(W, xq, y, O: int, K: int, stream=None) -> None:
     _check(lib().q4_0_q8_0_gemv(_ptr(W), _ptr(xq), _ptr(y), O, K, _stream(stream)), "q4_0_q8_0_gemv")
+
+
+def q4_0_gemv_rmsnorm(W, x, gamma, eps: float, y, O: int, K: int, xq_out=None, stream=None) -> None:
+    """Fused RMSNorm*gamma -> Q8_0 -> GEMV (gamma=None: plain quantization)."""
+    _check(lib().q4_0_gemv_rmsnorm(_ptr(W), _ptr(x), _ptr(gamma), float(eps), _ptr(y), O, K, _ptr(xq_out),
+                                   _stream(stream)), "q4_0_gemv_rmsnorm")
 
 
 def q4_0_q8_0_gemm_small_n(W, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:

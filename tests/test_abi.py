@@ -72,6 +72,16 @@ def test_gemv_host_validation(L):
     assert f(A16, A2, A16, 8, 256, None) == -2        # xq not 4-byte aligned
 
 
+def test_fused_host_validation(L):
+    f = L.q4_0_gemv_rmsnorm
+    assert f(A16, None, None, 1e-6, A16, 8, 256, None, None) == -1      # null x
+    assert f(A16, A16, None, -1.0, A16, 8, 256, None, None) == -1       # eps < 0
+    assert f(A16, A16, None, 1e-6, A16, 8, 320, None, None) == -3       # K % 256
+    assert f(A16, A16 + 4, None, 1e-6, A16, 8, 256, None, None) == -2   # x not 16-byte aligned
+    assert f(A16, A16, A16 + 8, 1e-6, A16, 8, 256, None, None) == -2    # gamma not 16-byte aligned
+    assert f(A16, A16, None, 1e-6, A16, 8, 256, A2, None) == -2         # xq_out not 4-byte aligned
+
+
 def test_small_n_host_validation(L):
     f = L.q4_0_q8_0_gemm_small_n
     assert f(A16, A16, A16, 8, 8, 256, 0, None) == -1      # N = 0
@@ -106,6 +116,7 @@ def test_options_and_counters(L):
     assert L.qdg_set_option(1, 0) == 0
     assert L.qdg_launch_count(-1) >= 0
     assert L.qdg_launch_count(7) == -1
+    assert L.qdg_launch_count(5) >= 0
     assert L.qdg_debug_block_sums(A16, A16, None, 8, 256, 1, 0, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 1, 9, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 0, None) == -1   # gemv path needs N == 1

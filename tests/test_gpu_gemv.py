@@ -135,3 +135,67 @@ def test_small_n_one_column_matches_gemv_tolerance():
     _, y64, S = oracle.matvec(Wq, xq, K, threads=8)
     assert_within_tol(a[None], y64, S)
     assert_within_tol(b[None], y64, S)
+
+
+FUSED_SHAPES = [(256, 256), (37, 512), (1000, 2048), (4096, 4096), (153, 6144), (4096, 14336), (64, 32768)]
+
+
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("O,K", FUSED_SHAPES)
+def test_fused_norm_gemv(O, K, norm):
+    """Fused RMSNorm*gamma -> Q8_0 -> GEMV: activations bit-identical to the
+    standalone quantizer and to the oracle, y bit-identical to the unfused GEMV
+    on those activations, and within tolerance of the oracle."""
+    torch = torch_cuda()
+    seed = O + K + int(norm)
+    w = synth.weights(seed, "W", O, K)
+    x = synth.activations(seed, "x", 1, K, outlier_frac=0.01)
+    gam = synth.gamma(seed, "g", K) if norm else None
+    Wd = empty_u8(qdg.q4_0_nbytes(O, K))
+    qdg.quantize_q4_0(to_dev(w), Wd)
+    xd = to_dev(x[0])
+    gd = None if gam is None else to_dev(gam)
+    xq_sep = empty_u8(qdg.q8_0_nbytes(1, K))
+    qdg.qnorm_quantize_q8_0(xd, gd, 1e-6, xq_sep)
+    y_sep = torch.empty(O, dtype=torch.float32, device="cuda")
+    qdg.q4_0_q8_0_gemv(Wd, xq_sep, y_sep, O, K)
+    xq_fused = torch.zeros(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device="cuda")
+    y_fused = torch.empty(O, dtype=torch.float32, device="cuda")
+    before = qdg.qdg_launch_count(5)
+    qdg.q4_0_gemv_rmsnorm(Wd, xd, gd, 1e-6, y_fused, O, K, xq_out=xq_fused)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert qdg.qdg_launch_count(5) == before + 1
+    xq_ref = oracle.quantize_q8_0(x, gam, 1e-6)
+    assert np.array_equal(to_host(xq_fused).reshape(1, -1), xq_ref)
+    assert np.array_equal(to_host(xq_sep).reshape(1, -1), xq_ref)
+    a, b = to_host(y_fused), to_host(y_sep)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+    Wq_ref = oracle.quantize_q4_0(w)
+    assert np.array_equal(to_host(Wd).reshape(O, -1), Wq_ref)
+    _, y64, S = oracle.matvec(Wq_ref, xq_ref, K, threads=8)
+    assert_within_tol(a[None], y64, S)
+
+
+def test_fused_without_xq_out_and_with_pdl():
+    torch = torch_cuda()
+    O, K = 2048, 4096
+    w = synth.weights(3, "W", O, K)
+    x = synth.activations(3, "x", 1, K)
+    gam = synth.gamma(3, "g", K)
+    Wd = empty_u8(qdg.q4_0_nbytes(O, K))
+    qdg.quantize_q4_0(to_dev(w), Wd)
+    torch.cuda.synchronize()
+    outs = []
+    for pdl in (0, 1):
+        qdg.qdg_set_option(qdg.QDG_OPT_PDL, pdl)
+        y = torch.empty(O, dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            qdg.q4_0_gemv_rmsnorm(Wd, to_dev(x[0]), to_dev(gam), 1e-6, y, O, K)
+        torch.cuda.synchronize()
+        outs.append(to_host(y))
+    qdg.qdg_set_option(qdg.QDG_OPT_PDL, 0)
+    assert np.array_equal(outs[0].view(np.uint32), outs[1].view(np.uint32))
+    xq_ref = oracle.quantize_q8_0(x, gam, 1e-6)
+    _, y64, S = oracle.matvec(oracle.quantize_q4_0(w), xq_ref, K, threads=8)
+    assert_within_tol(outs[0][None], y64, S)
