@@ -29,6 +29,7 @@
 #include "common.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace qdg {
 
@@ -41,6 +42,8 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kDepth = 3;                   // row-segments in flight per warp (the consume loop is unrolled by 3)
 constexpr int kSegBytes = 1152;             // 32 pairs x 36 bytes
 constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
+constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
+constexpr int kFusedMaxK = 16384;           // fused form stages x and gamma in shared memory
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
 
 struct Plan {
@@ -102,87 +105,13 @@ struct Args {
     float eps;
 };
 
-// Fused form: RMS_NORM * gamma -> Q8_0 of the two blocks of pair p, computed by
-// the lane that owns the pair, with exactly the arithmetic of the standalone
-// quantize kernel (same s, same products, same IEEE divisions and rounding).
-__device__ __forceinline__ void quantize_pair(const float* __restrict__ x, const float* __restrict__ gamma, float s,
-                                              int p, uint32_t (&xa)[8], uint32_t (&xb)[8], float& dxa, float& dxb,
-                                              int& sa, int& sb, uint32_t (&blk)[17]) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        const float4* xv = reinterpret_cast<const float4*>(x + p * 64 + half * 32);
-        const float4* gv = reinterpret_cast<const float4*>(gamma + p * 64 + half * 32);
-        float v[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const float4 a = __ldg(xv + i);
-            v[4 * i] = a.x;
-            v[4 * i + 1] = a.y;
-            v[4 * i + 2] = a.z;
-            v[4 * i + 3] = a.w;
-        }
-        if (gamma != nullptr) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const float4 g = __ldg(gv + i);
-                v[4 * i] = __fmul_rn(__fmul_rn(v[4 * i], s), g.x);
-                v[4 * i + 1] = __fmul_rn(__fmul_rn(v[4 * i + 1], s), g.y);
-                v[4 * i + 2] = __fmul_rn(__fmul_rn(v[4 * i + 2], s), g.z);
-                v[4 * i + 3] = __fmul_rn(__fmul_rn(v[4 * i + 3], s), g.w);
-            }
-        }
-        float amax = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        const float d = __fdiv_rn(amax, 127.0f);
-        const __half dh = __float2half_rn(d);
-        if (__hisinf(dh)) atomicOr(&g_flags_gemv, FLAG_OVERFLOW);
-        uint32_t w[8];
-        int qs = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            uint32_t word = 0;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                int q = 0;
-                if (d != 0.0f) {
-                    float r = roundf(__fdiv_rn(v[4 * i + j], d));
-                    r = fminf(fmaxf(r, -127.0f), 127.0f);
-                    q = static_cast<int>(r);
-                }
-                qs += q;
-                word |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * j);
-            }
-            w[i] = word;
-        }
-        const uint32_t dbits = __half_as_ushort(dh);
-        if (half == 0) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) xa[i] = w[i];
-            dxa = __half2float(dh);
-            sa = qs;
-            // Q8_0 block bytes: d (2 bytes) then 32 q, packed into the 68-byte pair
-            blk[0] = dbits | (w[0] << 16);
-#pragma unroll
-            for (int i = 1; i < 8; ++i) blk[i] = (w[i - 1] >> 16) | (w[i] << 16);
-            blk[8] = w[7] >> 16;
-        } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) xb[i] = w[i];
-            dxb = __half2float(dh);
-            sb = qs;
-            blk[8] |= dbits << 16;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) blk[9 + i] = w[i];
-        }
-    }
-}
-
 template <bool kFused, bool kDebug>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan plan) {
     __shared__ __align__(16) uint8_t seg_buf[kWarps][kSegBytes];
     __shared__ float part[kPartFloats];
     __shared__ float norm_part[8];
+    // fused form only: x [K] fp32, gamma [K] fp32, Q8_0 activations [K/32 x 34 B]
+    extern __shared__ __align__(16) uint8_t fused_smem[];
     const uint8_t* __restrict__ W = a.W;
     float* __restrict__ y = a.y;
     int32_t* __restrict__ dbg = a.dbg;
@@ -223,8 +152,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
         }
     };
 
-    // ---- the first chunk's leading row-segments (W only) before the wait
+    // ---- the first chunk's leading row-segments (W only) before the wait,
+    // plus an L2 prefetch of the rows after them (up to kL2Prefetch bytes per
+    // CTA) so the weight stream keeps flowing while the prologue runs.
     if (worker) fill(r0, min(nrows, plan.rch));
+    if (threadIdx.x == 0) {
+        const int64_t ahead_rows = static_cast<int64_t>(kDepth) * plan.nslots;
+        if (ahead_rows < nrows) {
+            const int64_t bytes = min(static_cast<int64_t>(kL2Prefetch), (nrows - ahead_rows) * plan.rowbytes);
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + (r0 + ahead_rows) * plan.rowbytes),
+                         "r"(static_cast<uint32_t>(bytes))
+                         : "memory");
+        }
+    }
 
     pdl_wait();
 
@@ -233,40 +173,99 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
     float dxa = 0.0f, dxb = 0.0f;
     int sa = 0, sb = 0;
     if (kFused) {
-        // RMS statistic in the library's fixed order: chain j (threads 0..255)
-        // sums x_i^2 over i = j (mod 256) ascending with fma; warp butterflies;
-        // ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).
+        const int K = a.K;
+        const int nb = K >> 5;
+        float* xs = reinterpret_cast<float*>(fused_smem);
+        float* gs = xs + K;
+        uint8_t* xqs = reinterpret_cast<uint8_t*>(gs + K);
+        // (1) stage x and gamma with one wave of 16-byte loads
+        {
+            const float4* x4 = reinterpret_cast<const float4*>(a.x);
+            const float4* g4 = reinterpret_cast<const float4*>(a.gamma);
+            for (int i = threadIdx.x; i < K / 4; i += kThreads) {
+                reinterpret_cast<float4*>(xs)[i] = __ldg(x4 + i);
+                if (a.gamma != nullptr) reinterpret_cast<float4*>(gs)[i] = __ldg(g4 + i);
+            }
+        }
+        __syncthreads();
+        // (2) RMS statistic in the library's fixed order: chain j (threads
+        // 0..255) sums x_i^2 over i = j (mod 256) ascending with fma; warp
+        // butterflies; ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).
         float s = 1.0f;
         if (a.gamma != nullptr) {
             if (threadIdx.x < 256) {
                 float acc = 0.0f;
-                for (int i0 = threadIdx.x; i0 < a.K; i0 += 256 * 8) {
-                    float v[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int i = i0 + u * 256;
-                        v[u] = i < a.K ? __ldg(a.x + i) : 0.0f;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (i0 + u * 256 < a.K) acc = __fmaf_rn(v[u], v[u], acc);
-                }
+                for (int i = threadIdx.x; i < K; i += 256) acc = __fmaf_rn(xs[i], xs[i], acc);
                 acc = warp_sum(acc);
                 if (lane == 0) norm_part[warp] = acc;
             }
             __syncthreads();
             const float ss = __fadd_rn(__fadd_rn(__fadd_rn(norm_part[0], norm_part[1]), __fadd_rn(norm_part[2], norm_part[3])),
                                        __fadd_rn(__fadd_rn(norm_part[4], norm_part[5]), __fadd_rn(norm_part[6], norm_part[7])));
-            const float mean = __fdiv_rn(ss, static_cast<float>(a.K));
+            const float mean = __fdiv_rn(ss, static_cast<float>(K));
             s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
         }
-        if (active) {
-            uint32_t blk[17];
-            quantize_pair(a.x, a.gamma, s, p, xa, xb, dxa, dxb, sa, sb, blk);
-            if (a.xq_out != nullptr && blockIdx.x == 0 && slot == 0) {
-                uint32_t* dst = reinterpret_cast<uint32_t*>(a.xq_out + static_cast<size_t>(p) * 68);
+        // (3) Q8_0 blocks, one per warp at a time (lane = element), four
+        // independent blocks interleaved; the arithmetic of the standalone
+        // quantize kernel: v = (x*s)*gamma, d = max|v|/127, q = round(v/d).
+        for (int b0 = warp; b0 < nb; b0 += 4 * kWarps) {
+            float v[4], d[4];
 #pragma unroll
-                for (int i = 0; i < 17; ++i) dst[i] = blk[i];
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * kWarps;
+                v[u] = 0.0f;
+                if (b < nb) {
+                    v[u] = xs[(b << 5) + lane];
+                    if (a.gamma != nullptr) v[u] = __fmul_rn(__fmul_rn(v[u], s), gs[(b << 5) + lane]);
+                }
+                d[u] = fabsf(v[u]);
+            }
+#pragma unroll
+            for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) d[u] = fmaxf(d[u], __shfl_xor_sync(0xffffffffu, d[u], h));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * kWarps;
+                if (b >= nb) break;
+                const float dd = __fdiv_rn(d[u], 127.0f);
+                int q = 0;
+                if (dd != 0.0f) {
+                    float r = roundf(__fdiv_rn(v[u], dd));
+                    r = fminf(fmaxf(r, -127.0f), 127.0f);
+                    q = static_cast<int>(r);
+                }
+                uint8_t* blk = xqs + b * 34;
+                if (lane == 0) {
+                    const __half dh = __float2half_rn(dd);
+                    *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
+                    if (__hisinf(dh)) atomicOr(&g_flags_gemv, FLAG_OVERFLOW);
+                }
+                blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+            }
+        }
+        __syncthreads();
+        if (a.xq_out != nullptr && blockIdx.x == 0) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(xqs);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(a.xq_out);
+            for (int i = threadIdx.x; i < nb * 34 / 4; i += kThreads) dst[i] = src[i];
+        }
+        // (4) this lane's pair, from shared memory
+        if (active) {
+            const uint32_t* xp = reinterpret_cast<const uint32_t*>(xqs + static_cast<size_t>(p) * 68);
+            uint32_t w[17];
+#pragma unroll
+            for (int i = 0; i < 17; ++i) w[i] = xp[i];
+            dxa = half_bits_to_float(w[0]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xa[i] = bytes_2_to_5(w[i], w[i + 1]);
+            dxb = half_bits_to_float(w[8] >> 16);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) xb[i] = w[9 + i];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                sa = __dp4a(static_cast<int>(xa[i]), 0x01010101, sa);
+                sb = __dp4a(static_cast<int>(xb[i]), 0x01010101, sb);
             }
         } else {
 #pragma unroll
@@ -391,7 +390,7 @@ int gemv_rmsnorm_launch(const void* W, const float* x, const float* gamma, float
     if (!W || !x || !y) return QDG_EINVAL;
     if (O <= 0 || K <= 0) return QDG_EINVAL;
     if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
-    if (K % 256 != 0 || K > 32768 || O >= (int64_t(1) << 31)) return QDG_ESHAPE;
+    if (K % 256 != 0 || K > kFusedMaxK || O >= (int64_t(1) << 31)) return QDG_ESHAPE;
     if (!aligned(W, 16) || !aligned(x, 16) || (gamma && !aligned(gamma, 16)) || !aligned(y, 4) ||
         !aligned(xq_out, 4))
         return QDG_EALIGN;
@@ -408,7 +407,19 @@ int gemv_rmsnorm_launch(const void* W, const float* x, const float* gamma, float
     a.y = y;
     a.O = O;
     a.K = static_cast<int>(K);
-    const cudaError_t e = launch(gemv_kernel<true, false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
+    const size_t smem = static_cast<size_t>(8) * K + static_cast<size_t>(K / 32) * 34;
+    {
+        static std::mutex mu;
+        static size_t set_bytes = 0;
+        std::lock_guard<std::mutex> lock(mu);
+        if (set_bytes < smem) {
+            if (cudaFuncSetAttribute(gemv_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess)
+                return QDG_ECUDA;
+            set_bytes = smem;
+        }
+    }
+    const cudaError_t e = launch(gemv_kernel<true, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(5);
     return QDG_OK;

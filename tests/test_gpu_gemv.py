@@ -137,7 +137,7 @@ def test_small_n_one_column_matches_gemv_tolerance():
     assert_within_tol(b[None], y64, S)
 
 
-FUSED_SHAPES = [(256, 256), (37, 512), (1000, 2048), (4096, 4096), (153, 6144), (4096, 14336), (64, 32768)]
+FUSED_SHAPES = [(256, 256), (37, 512), (1000, 2048), (4096, 4096), (153, 6144), (4096, 14336), (64, 16384)]
 
 
 @pytest.mark.parametrize("norm", [True, False])
