@@ -298,24 +298,35 @@ class DecodeStep:
                    for tag, K in wl.activations.items()}
         self.y = {m.name: torch.empty(m.rows, dtype=torch.float32, device=device) for m in wl.matrices}
         self.y_host = {m.name: torch.empty(m.rows, dtype=torch.float32).pin_memory() for m in wl.matrices}
+        # consecutive projections with the same input (and K) form one launch
+        self.groups = []
+        for m in wl.matrices:
+            if (self.groups and self.groups[-1][0].source == m.source and self.groups[-1][0].cols == m.cols
+                    and len(self.groups[-1]) < 4):
+                self.groups[-1].append(m)
+            else:
+                self.groups.append([m])
         torch.cuda.synchronize()
         torch.cuda.empty_cache()      # release the fp32 staging of the weights
 
     def launches_per_step(self, fused=True):
-        return len(self.wl.matrices) + (0 if fused else len(self.wl.activations))
+        return len(self.groups) if fused else len(self.wl.activations) + len(self.wl.matrices)
+
+    def run_group(self, grp, xs, Ws=None):
+        """One fused launch for projections that read the same activation."""
+        tag = grp[0].source.split(":", 1)[1]
+        g = self.gamma.get(tag) if self.kinds[tag] == "norm" else None
+        Ws = Ws if Ws is not None else [self.W[m.name] for m in grp]
+        self.qdg.q4_0_gemv_rmsnorm_group(Ws, [self.y[m.name] for m in grp], [m.rows for m in grp], xs[tag], g,
+                                         self.wl.eps, grp[0].cols)
 
     def run(self, xs, events=None, fused=True):
         qdg = self.qdg
         if fused:
-            # one launch per projection: RMSNorm*gamma -> Q8_0 -> GEMV
-            for i, m in enumerate(self.wl.matrices):
-                tag = m.source.split(":", 1)[1]
-                if events:
-                    events[i].record()
-                qdg.q4_0_gemv_rmsnorm(self.W[m.name], xs[tag], self.gamma.get(tag) if self.kinds[tag] == "norm"
-                                      else None, self.wl.eps, self.y[m.name], m.rows, m.cols)
-            if events:
-                events[len(self.wl.matrices)].record()
+            # one launch per group of projections sharing an input:
+            # RMSNorm*gamma -> Q8_0 -> GEMV over all rows of the group
+            for grp in self.groups:
+                self.run_group(grp, xs)
             return
         i = 0
         for tag, K in self.wl.activations.items():
@@ -379,7 +390,7 @@ def bench_ours(args, wl, world, rank, local):
     stream.wait_stream(side)
     torch.cuda.synchronize()
     if fused:
-        assert counts[True][5] == len(wl.matrices) and counts[True][0] == 0 and counts[True][1] == 0, counts
+        assert counts[True][5] == len(step.groups) and counts[True][0] == 0 and counts[True][1] == 0, counts
     fusion = {"route": "fused" if fused else "unfused",
               "per_step_launches": {"fused_norm_gemv": counts[fused][5], "standalone_quantize": counts[fused][0],
                                     "gemv": counts[fused][1]}}
@@ -446,28 +457,37 @@ def bench_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     ms_other = f0.elapsed_time(f1) / args.steps
 
-    # ---- per-matrix cost: a graph of 20 back-to-back launches of one projection
+    # ---- per-launch cost: a graph of C back-to-back launches of one group, each
+    # on its own copy of the weights (C copies exceed three L2 sizes, so every
+    # launch streams its weights from HBM)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
     per_call = {}
-    with torch.cuda.stream(side):
-        for m in wl.matrices:
-            tag = m.source.split(":", 1)[1]
-            g = step.gamma.get(tag) if step.kinds[tag] == "norm" else None
-            fn = (lambda m=m, tag=tag, g=g: qdg.q4_0_gemv_rmsnorm(step.W[m.name], step.x_dev[0][tag], g, wl.eps,
-                                                                  step.y[m.name], m.rows, m.cols))
-            gr = capture(fn, side, 20)
+    launch_bytes = {}
+    for grp in step.groups:
+        name = "+".join(m.name for m in grp)
+        gbytes = sum(workloads.q4_0_bytes(m.rows, m.cols) for m in grp)
+        copies = int(min(160, max(2, -(-3 * l2 // gbytes))))
+        Wc = [[step.W[m.name] for m in grp]] + [[step.W[m.name].clone() for m in grp] for _ in range(copies - 1)]
+        with torch.cuda.stream(side):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=side):
+                for c in range(copies):
+                    step.run_group(grp, step.x_dev[0], Ws=Wc[c])
             gr.replay()
             side.synchronize()
             a0 = torch.cuda.Event(enable_timing=True)
             a1 = torch.cuda.Event(enable_timing=True)
             a0.record(side)
-            for _ in range(5):
+            for _ in range(3):
                 gr.replay()
             a1.record(side)
             side.synchronize()
-            per_call[m.name] = a0.elapsed_time(a1) * 1e3 / 100
-            del gr
+        per_call[name] = a0.elapsed_time(a1) * 1e3 / (3 * copies)
+        launch_bytes[name] = sum(fused_launch_bytes(m) for m in grp) - (
+            4 * grp[0].cols * (2 if grp[0].source.startswith("norm:") else 1) * (len(grp) - 1))
+        del gr, Wc
+        torch.cuda.empty_cache()
     torch.cuda.synchronize()
-    launch_bytes = {m.name: fused_launch_bytes(m) for m in wl.matrices}
     gbs_per_call = {n: launch_bytes[n] / (per_call[n] * 1e-6) / 1e9 for n in per_call}
 
     # ---- end to end through the same calls, inputs from pinned host memory
@@ -491,12 +511,12 @@ def bench_ours(args, wl, world, rank, local):
         # launch duration is at most the step time over the launches per step.
         kern_bytes = sum(launch_bytes.values())
         achieved = kern_bytes / (ms * 1e-3) / 1e9
-        kernel = "gemv_kernel<fused> (q4_0_gemv_rmsnorm)"
+        kernel = "gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)"
         traffic = ncu_traffic("gemv.cu")
     else:
-        kern_bytes = sum(workloads.gemv_algorithmic_bytes(m.rows, m.cols) for m in wl.matrices)
+        kern_bytes = sum(launch_bytes.values())
         achieved = kern_bytes / (sum(per_call.values()) * 1e-6) / 1e9
-        kernel = "gemv_kernel (per-matrix graphs)"
+        kernel = "gemv_kernel<fused> (per-group graphs)"
         traffic = None
     roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -504,8 +524,8 @@ def bench_ours(args, wl, world, rank, local):
                             else "fallback 6.8 TB/s"),
             "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
             "traffic_source": (traffic.get("what") if traffic else "no ncu capture of this source yet"),
-            "algorithmic_bytes_per_launch": round(kern_bytes / len(wl.matrices)),
-            "launches_per_step": len(wl.matrices),
+            "algorithmic_bytes_per_launch": round(kern_bytes / len(step.groups)),
+            "launches_per_step": len(step.groups),
             "frac_of_nominal_8TB": round(achieved / 8000.0, 4)}
     result = {
         "metric": METRIC, "value": round(nbytes * world / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
@@ -522,7 +542,8 @@ def bench_ours(args, wl, world, rank, local):
         "us_per_step": round(ms * 1e3, 2),
         "us_per_call": {k: round(v, 2) for k, v in per_call.items()},
         "gbs_per_call": {k: round(v, 1) for k, v in gbs_per_call.items()},
-        "per_call_note": "fused launch, graph of 20 back-to-back launches of one projection, PDL as configured",
+        "per_call_note": ("one fused launch per group of projections sharing an input; graph of back-to-back "
+                          "launches on distinct weight copies (> 3 x L2), PDL as configured"),
         "other_route": {"route": "standalone quantize + GEMV" if fused else "fused",
                         "us_per_step": round(ms_other * 1e3, 2),
                         "value": round(nbytes / (ms_other * 1e-3) / 1e9, 1)},

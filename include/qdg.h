@@ -130,6 +130,22 @@ QDG_API int q4_0_gemv_rmsnorm(const void* W, const float* x, const float* gamma,
                               int64_t O, int64_t K, void* xq_out, qdg_stream_t stream);
 
 /*
+ * q4_0_gemv_rmsnorm_group -- the fused route for up to 4 projections that
+ * read the same activation (a decode layer's q, k and v; its gate and up):
+ * one launch normalises and quantizes x once per CTA and streams the rows of
+ * all the matrices, y[g] = W[g] * Q8_0(RMSNorm(x) * gamma).
+ *
+ * W, y, O   host arrays of `count` entries (1..4): device pointers W[g]
+ *           ([O[g]][K/32] Q4_0, 16-byte aligned) and y[g] ([O[g]] fp32), and
+ *           row counts O[g] >= 1.  All matrices have the same K.
+ * Other arguments as q4_0_gemv_rmsnorm.  Results are bit-identical to
+ * q4_0_gemv_rmsnorm called once per matrix.
+ */
+QDG_API int q4_0_gemv_rmsnorm_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                    const float* x, const float* gamma, float eps, int64_t K, void* xq_out,
+                                    qdg_stream_t stream);
+
+/*
  * q4_0_q8_0_gemm_small_n -- Y = W * X for 1 <= N <= 8 Q8_0 vectors sharing
  * one pass over W (speculative / parallel decode; the "vector case" of the
  * mmvq route)  [same page and section].

@@ -92,7 +92,15 @@ struct SegRegs {
     uint4 v[3];
 };
 
+constexpr int kMaxGroup = 4;   // matrices sharing one input in a grouped launch
+
 struct Args {
+    // Grouped launch: matrices g = 0..ng-1 (same K, same input) are stacked;
+    // global row r belongs to the last g with start[g] <= r.
+    const uint8_t* Wg[kMaxGroup];
+    float* yg[kMaxGroup];
+    int64_t start[kMaxGroup];
+    int ng;
     const uint8_t* W;
     const uint8_t* xq;      // Q8_0 activations (unfused form)
     const float* x;         // fp32 activations (fused form)
@@ -112,8 +120,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
     __shared__ float norm_part[8];
     // fused form only: x [K] fp32, gamma [K] fp32, Q8_0 activations [K/32 x 34 B]
     extern __shared__ __align__(16) uint8_t fused_smem[];
-    const uint8_t* __restrict__ W = a.W;
-    float* __restrict__ y = a.y;
     int32_t* __restrict__ dbg = a.dbg;
     const int64_t O = a.O;
 
@@ -137,7 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
 
     SegRegs pipe[kDepth];
     auto load_seg = [&](int64_t row, SegRegs& s) {
-        const uint8_t* base = W + row * plan.rowbytes + seg_off;
+        int g = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxGroup; ++i)
+            if (i < a.ng && row >= a.start[i]) g = i;
+        const uint8_t* base = a.Wg[g] + (row - a.start[g]) * plan.rowbytes + seg_off;
 #pragma unroll
         for (int k = 0; k < 3; ++k) {
             const int idx = lane + 32 * k;
@@ -157,12 +167,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
     // CTA) so the weight stream keeps flowing while the prologue runs.
     if (worker) fill(r0, min(nrows, plan.rch));
     if (threadIdx.x == 0) {
-        const int64_t ahead_rows = static_cast<int64_t>(kDepth) * plan.nslots;
-        if (ahead_rows < nrows) {
-            const int64_t bytes = min(static_cast<int64_t>(kL2Prefetch), (nrows - ahead_rows) * plan.rowbytes);
-            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(W + (r0 + ahead_rows) * plan.rowbytes),
-                         "r"(static_cast<uint32_t>(bytes))
-                         : "memory");
+        // rows [r0 + ahead, r0 + ahead + n) may span matrices of the group
+        int64_t row = r0 + static_cast<int64_t>(kDepth) * plan.nslots;
+        int64_t budget = kL2Prefetch / plan.rowbytes;
+        for (int g = 0; g < a.ng && budget > 0; ++g) {
+            const int64_t gend = (g + 1 < a.ng) ? a.start[g + 1] : O;
+            if (row >= gend || row >= r1) continue;
+            const int64_t n = min(min(gend, r1) - row, budget);
+            if (n > 0) {
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.Wg[g] + (row - a.start[g]) *
+                                                                                           plan.rowbytes),
+                             "r"(static_cast<uint32_t>(n * plan.rowbytes))
+                             : "memory");
+                row += n;
+                budget -= n;
+            }
         }
     }
 
@@ -350,7 +369,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
             for (int t = threadIdx.x; t < crows; t += kThreads) {
                 float v = part[t * nseg];
                 for (int g = 1; g < nseg; ++g) v = __fadd_rn(v, part[t * nseg + g]);
-                y[c0 + t] = v;
+                const int64_t row = c0 + t;
+                int g = 0;
+#pragma unroll
+                for (int i = 1; i < kMaxGroup; ++i)
+                    if (i < a.ng && row >= a.start[i]) g = i;
+                a.yg[g][row - a.start[g]] = v;
             }
         }
         __syncthreads();
@@ -370,6 +394,10 @@ int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, c
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
     Args a{};
     a.W = static_cast<const uint8_t*>(W);
+    a.Wg[0] = a.W;
+    a.yg[0] = y;
+    a.start[0] = 0;
+    a.ng = 1;
     a.xq = static_cast<const uint8_t*>(xq);
     a.y = y;
     a.dbg = dbg;
@@ -385,27 +413,36 @@ int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, c
     return QDG_OK;
 }
 
-int gemv_rmsnorm_launch(const void* W, const float* x, const float* gamma, float eps, float* y, int64_t O, int64_t K,
-                        void* xq_out, cudaStream_t stream) {
-    if (!W || !x || !y) return QDG_EINVAL;
-    if (O <= 0 || K <= 0) return QDG_EINVAL;
+int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O, int count, const float* x,
+                        const float* gamma, float eps, int64_t K, void* xq_out, cudaStream_t stream) {
+    if (!W || !y || !O || !x) return QDG_EINVAL;
+    if (count < 1 || count > kMaxGroup || K <= 0) return QDG_EINVAL;
     if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
-    if (K % 256 != 0 || K > kFusedMaxK || O >= (int64_t(1) << 31)) return QDG_ESHAPE;
-    if (!aligned(W, 16) || !aligned(x, 16) || (gamma && !aligned(gamma, 16)) || !aligned(y, 4) ||
-        !aligned(xq_out, 4))
-        return QDG_EALIGN;
+    if (K % 256 != 0 || K > kFusedMaxK) return QDG_ESHAPE;
+    if (!aligned(x, 16) || (gamma && !aligned(gamma, 16)) || !aligned(xq_out, 4)) return QDG_EALIGN;
+    Args a{};
+    int64_t total = 0;
+    for (int g = 0; g < count; ++g) {
+        if (!W[g] || !y[g] || O[g] <= 0) return QDG_EINVAL;
+        if (!aligned(W[g], 16) || !aligned(y[g], 4)) return QDG_EALIGN;
+        a.Wg[g] = static_cast<const uint8_t*>(W[g]);
+        a.yg[g] = y[g];
+        a.start[g] = total;
+        total += O[g];
+    }
+    if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     const Plan plan = make_plan(K);
-    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
-    Args a{};
-    a.W = static_cast<const uint8_t*>(W);
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
+    a.ng = count;
+    a.W = a.Wg[0];
     a.x = x;
     a.gamma = gamma;
     a.eps = eps;
     a.xq_out = static_cast<uint8_t*>(xq_out);
-    a.y = y;
-    a.O = O;
+    a.y = a.yg[0];
+    a.O = total;
     a.K = static_cast<int>(K);
     const size_t smem = static_cast<size_t>(8) * K + static_cast<size_t>(K / 32) * 34;
     {
@@ -446,5 +483,11 @@ extern "C" int q4_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O
 
 extern "C" int q4_0_gemv_rmsnorm(const void* W, const float* x, const float* gamma, float eps, float* y, int64_t O,
                                  int64_t K, void* xq_out, qdg_stream_t stream) {
-    return qdg::gemv_rmsnorm_launch(W, x, gamma, eps, y, O, K, xq_out, reinterpret_cast<cudaStream_t>(stream));
+    return qdg::gemv_rmsnorm_launch(&W, &y, &O, 1, x, gamma, eps, K, xq_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int q4_0_gemv_rmsnorm_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                       const float* x, const float* gamma, float eps, int64_t K, void* xq_out,
+                                       qdg_stream_t stream) {
+    return qdg::gemv_rmsnorm_launch(W, y, O, count, x, gamma, eps, K, xq_out, reinterpret_cast<cudaStream_t>(stream));
 }

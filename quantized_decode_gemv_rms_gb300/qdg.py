@@ -50,6 +50,7 @@ def lib() -> ctypes.CDLL:
                 "qnorm_quantize_q8_0": ([p, i64, p, f32, i64, i64, p, p], i32),
                 "q4_0_q8_0_gemv": ([p, p, p, i64, i64, p], i32),
                 "q4_0_gemv_rmsnorm": ([p, p, p, f32, p, i64, i64, p, p], i32),
+                "q4_0_gemv_rmsnorm_group": ([p, p, p, i32, p, p, f32, i64, p, p], i32),
                 "q4_0_q8_0_gemm_small_n": ([p, p, p, i64, i64, i64, i64, p], i32),
                 "quantize_q4_0": ([p, i64, i64, i64, p, p], i32),
                 "qdg_device_status": ([p], i32),
@@ -132,6 +133,16 @@ def q4_0_gemv_rmsnorm(W, x, gamma, eps: float, y, O: int, K: int, xq_out=None, s
     """Fused RMSNorm*gamma -> Q8_0 -> GEMV (gamma=None: plain quantization)."""
     _check(lib().q4_0_gemv_rmsnorm(_ptr(W), _ptr(x), _ptr(gamma), float(eps), _ptr(y), O, K, _ptr(xq_out),
                                    _stream(stream)), "q4_0_gemv_rmsnorm")
+
+
+def q4_0_gemv_rmsnorm_group(Ws, ys, Os, x, gamma, eps: float, K: int, xq_out=None, stream=None) -> None:
+    """Fused route for up to 4 matrices sharing the input x (one launch)."""
+    n = len(Ws)
+    W_arr = (ctypes.c_void_p * n)(*[_ptr(w) for w in Ws])
+    y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in ys])
+    O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
+    _check(lib().q4_0_gemv_rmsnorm_group(W_arr, y_arr, O_arr, n, _ptr(x), _ptr(gamma), float(eps), K,
+                                         _ptr(xq_out), _stream(stream)), "q4_0_gemv_rmsnorm_group")
 
 
 def q4_0_q8_0_gemm_small_n(W, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:

@@ -82,6 +82,22 @@ def test_fused_host_validation(L):
     assert f(A16, A16, None, 1e-6, A16, 8, 256, A2, None) == -2         # xq_out not 4-byte aligned
 
 
+def test_fused_group_host_validation(L):
+    import ctypes
+    f = L.q4_0_gemv_rmsnorm_group
+    W = (ctypes.c_void_p * 2)(A16, A16)
+    Y = (ctypes.c_void_p * 2)(A16, A16)
+    O = (ctypes.c_int64 * 2)(8, 8)
+    assert f(W, Y, O, 0, A16, None, 1e-6, 256, None, None) == -1        # count 0
+    assert f(W, Y, O, 5, A16, None, 1e-6, 256, None, None) == -1        # count > 4
+    assert f(W, Y, O, 2, A16, None, 1e-6, 320, None, None) == -3        # K % 256
+    assert f(W, Y, O, 2, A16, None, 1e-6, 32768, None, None) == -3      # K beyond the fused maximum
+    Wb = (ctypes.c_void_p * 2)(A16, A2)
+    assert f(Wb, Y, O, 2, A16, None, 1e-6, 256, None, None) == -2       # second W misaligned
+    Ob = (ctypes.c_int64 * 2)(8, 0)
+    assert f(W, Y, Ob, 2, A16, None, 1e-6, 256, None, None) == -1       # empty matrix
+
+
 def test_small_n_host_validation(L):
     f = L.q4_0_q8_0_gemm_small_n
     assert f(A16, A16, A16, 8, 8, 256, 0, None) == -1      # N = 0

@@ -199,3 +199,41 @@ def test_fused_without_xq_out_and_with_pdl():
     xq_ref = oracle.quantize_q8_0(x, gam, 1e-6)
     _, y64, S = oracle.matvec(oracle.quantize_q4_0(w), xq_ref, K, threads=8)
     assert_within_tol(outs[0][None], y64, S)
+
+
+@pytest.mark.parametrize("Os,K", [((4096, 1024, 1024), 4096), ((14336, 14336), 4096), ((37, 1, 300, 5), 2048),
+                                  ((64, 128), 14336)])
+def test_fused_group_matches_single(Os, K):
+    """One grouped launch over matrices sharing the input equals one fused
+    launch per matrix, bit for bit, and matches the oracle."""
+    torch = torch_cuda()
+    seed = sum(Os) + K
+    x = synth.activations(seed, "x", 1, K, outlier_frac=0.01)
+    gam = synth.gamma(seed, "g", K)
+    xd, gd = to_dev(x[0]), to_dev(gam)
+    Ws, ws = [], []
+    for i, O in enumerate(Os):
+        w = synth.weights(seed, f"W{i}", O, K)
+        Wd = empty_u8(qdg.q4_0_nbytes(O, K))
+        qdg.quantize_q4_0(to_dev(w), Wd)
+        Ws.append(Wd)
+        ws.append(w)
+    ys_group = [torch.empty(O, dtype=torch.float32, device="cuda") for O in Os]
+    xq = torch.zeros(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device="cuda")
+    qdg.q4_0_gemv_rmsnorm_group(Ws, ys_group, Os, xd, gd, 1e-6, K, xq_out=xq)
+    ys_single = []
+    for Wd, O in zip(Ws, Os):
+        y = torch.empty(O, dtype=torch.float32, device="cuda")
+        qdg.q4_0_gemv_rmsnorm(Wd, xd, gd, 1e-6, y, O, K)
+        ys_single.append(y)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    xq_ref = oracle.quantize_q8_0(x, gam, 1e-6)
+    assert np.array_equal(to_host(xq).reshape(1, -1), xq_ref)
+    for i, (a, b) in enumerate(zip(ys_group, ys_single)):
+        ga, sb = to_host(a), to_host(b)
+        assert np.array_equal(ga.view(np.uint32), sb.view(np.uint32)), f"matrix {i}"
+        rows = None if Os[i] <= 2048 else synth.sample_indices(seed, f"r{i}", Os[i], 1024)
+        Wq_ref = oracle.quantize_q4_0(ws[i] if rows is None else ws[i][rows])
+        _, y64, S = oracle.matvec(Wq_ref, xq_ref, K, threads=8)
+        assert_within_tol((ga if rows is None else ga[rows])[None], y64, S)
