@@ -37,17 +37,13 @@ static __device__ unsigned g_flags_gemv;
 
 namespace {
 
-// Warps per CTA: 8 (two CTAs per SM, so consecutive launches can share an SM
-// under programmatic dependent launch) while a row needs at most 8 segments
-// (K <= 16384), else 16 (one CTA per SM).
-constexpr int kWarpsSmall = 8;
-constexpr int kWarpsLarge = 16;
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
 constexpr int kDepth = 3;                   // row-segments in flight per warp (the consume loop is unrolled by 3)
 constexpr int kSegBytes = 1152;             // 32 pairs x 36 bytes
-constexpr int kPartFloats = 2048;           // per-chunk partial sums (rows x segments)
+constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
-constexpr int kFusedMaxK = 16384;           // fused form stages x (and gamma) in shared memory
-constexpr size_t kFusedSmemBudget = 90 * 1024;   // dynamic shared memory of the fused form
+constexpr int kFusedMaxK = 16384;           // fused form stages x and gamma in shared memory
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
 
 struct Plan {
@@ -55,8 +51,7 @@ struct Plan {
     int nb;         // K/32
     int P;          // block pairs per row (K/64)
     int nseg;       // segments per row, ceil(P / 32)
-    int nslots;     // rows in flight per CTA = warps / nseg
-    int warps;      // warps per CTA (8 or 16)
+    int nslots;     // rows in flight per CTA = kWarps / nseg
     int rch;        // rows per chunk (partial-sum buffer capacity), multiple of nslots
 };
 
@@ -66,8 +61,7 @@ Plan make_plan(int64_t K) {
     p.rowbytes = p.nb * 18;
     p.P = static_cast<int>(K / 64);
     p.nseg = (p.P + 31) / 32;
-    p.warps = p.nseg <= kWarpsSmall ? kWarpsSmall : kWarpsLarge;
-    p.nslots = p.warps / p.nseg;
+    p.nslots = kWarps / p.nseg;
     p.rch = (kPartFloats / p.nseg) / p.nslots * p.nslots;
     return p;
 }
@@ -117,12 +111,10 @@ struct Args {
     int64_t O;
     int K;
     float eps;
-    int stage_gamma;        // fused form: gamma staged in shared memory (else read in place)
 };
 
-template <int kWarps, bool kFused, bool kDebug>
-__global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) gemv_kernel(const Args a, Plan plan) {
-    constexpr int kThreads = 32 * kWarps;
+template <bool kFused, bool kDebug>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan plan) {
     __shared__ __align__(16) uint8_t seg_buf[kWarps][kSegBytes];
     __shared__ float part[kPartFloats];
     __shared__ float norm_part[8];
@@ -204,14 +196,14 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) gemv_kernel(const Ar
         const int nb = K >> 5;
         float* xs = reinterpret_cast<float*>(fused_smem);
         float* gs = xs + K;
-        uint8_t* xqs = reinterpret_cast<uint8_t*>(a.stage_gamma ? gs + K : gs);
+        uint8_t* xqs = reinterpret_cast<uint8_t*>(gs + K);
         // (1) stage x and gamma with one wave of 16-byte loads
         {
             const float4* x4 = reinterpret_cast<const float4*>(a.x);
             const float4* g4 = reinterpret_cast<const float4*>(a.gamma);
             for (int i = threadIdx.x; i < K / 4; i += kThreads) {
                 reinterpret_cast<float4*>(xs)[i] = __ldg(x4 + i);
-                if (a.gamma != nullptr && a.stage_gamma) reinterpret_cast<float4*>(gs)[i] = __ldg(g4 + i);
+                if (a.gamma != nullptr) reinterpret_cast<float4*>(gs)[i] = __ldg(g4 + i);
             }
         }
         __syncthreads();
@@ -243,9 +235,7 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) gemv_kernel(const Ar
                 v[u] = 0.0f;
                 if (b < nb) {
                     v[u] = xs[(b << 5) + lane];
-                    if (a.gamma != nullptr)
-                        v[u] = __fmul_rn(__fmul_rn(v[u], s),
-                                         a.stage_gamma ? gs[(b << 5) + lane] : __ldg(a.gamma + (b << 5) + lane));
+                    if (a.gamma != nullptr) v[u] = __fmul_rn(__fmul_rn(v[u], s), gs[(b << 5) + lane]);
                 }
                 d[u] = fabsf(v[u]);
             }
@@ -393,12 +383,6 @@ __global__ void __launch_bounds__(32 * kWarps, 16 / kWarps) gemv_kernel(const Ar
 
 }  // namespace
 
-template <int kW>
-cudaError_t launch_gemv(const Args& a, const Plan& plan, int grid, cudaStream_t stream, bool dbg) {
-    if (dbg) return launch(gemv_kernel<kW, false, true>, dim3(grid), dim3(32 * kW), 0, stream, false, a, plan);
-    return launch(gemv_kernel<kW, false, false>, dim3(grid), dim3(32 * kW), 0, stream, true, a, plan);
-}
-
 int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream, int32_t* dbg) {
     if (!W || !xq || (!y && !dbg)) return QDG_EINVAL;
     if (O <= 0 || K <= 0) return QDG_EINVAL;
@@ -407,8 +391,7 @@ int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, c
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     const Plan plan = make_plan(K);
-    const int per_sm = 16 / plan.warps;
-    const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(dev.sms) * per_sm, O));
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
     Args a{};
     a.W = static_cast<const uint8_t*>(W);
     a.Wg[0] = a.W;
@@ -420,8 +403,11 @@ int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, c
     a.dbg = dbg;
     a.O = O;
     a.K = static_cast<int>(K);
-    const cudaError_t e = plan.warps == kWarpsSmall ? launch_gemv<kWarpsSmall>(a, plan, grid, stream, dbg != nullptr)
-                                                    : launch_gemv<kWarpsLarge>(a, plan, grid, stream, dbg != nullptr);
+    cudaError_t e;
+    if (dbg)
+        e = launch(gemv_kernel<false, true>, dim3(grid), dim3(kThreads), 0, stream, false, a, plan);
+    else
+        e = launch(gemv_kernel<false, false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(1);
     return QDG_OK;
@@ -447,7 +433,8 @@ int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O,
     if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
-    const Plan plan = make_plan(K);   // K <= 16384: 8 warps per CTA
+    const Plan plan = make_plan(K);
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
     a.ng = count;
     a.W = a.Wg[0];
     a.x = x;
@@ -457,27 +444,19 @@ int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O,
     a.y = a.yg[0];
     a.O = total;
     a.K = static_cast<int>(K);
-    // x (and gamma when it fits beside it) staged in shared memory; two CTAs
-    // per SM keep room for the next launch under PDL.
-    const size_t xq_bytes = static_cast<size_t>(K / 32) * 34;
-    a.stage_gamma = (gamma != nullptr && static_cast<size_t>(8) * K + xq_bytes <= kFusedSmemBudget) ? 1 : 0;
-    const size_t smem = static_cast<size_t>(a.stage_gamma ? 8 : 4) * K + xq_bytes;
+    const size_t smem = static_cast<size_t>(8) * K + static_cast<size_t>(K / 32) * 34;
     {
         static std::mutex mu;
-        static bool done = false;
+        static size_t set_bytes = 0;
         std::lock_guard<std::mutex> lock(mu);
-        if (!done) {
-            if (cudaFuncSetAttribute(gemv_kernel<kWarpsSmall, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(kFusedSmemBudget)) != cudaSuccess ||
-                cudaFuncSetAttribute(gemv_kernel<kWarpsSmall, true, false>,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+        if (set_bytes < smem) {
+            if (cudaFuncSetAttribute(gemv_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess)
                 return QDG_ECUDA;
-            done = true;
+            set_bytes = smem;
         }
     }
-    const int grid = static_cast<int>(std::min<int64_t>(static_cast<int64_t>(dev.sms) * 2, total));
-    const cudaError_t e =
-        launch(gemv_kernel<kWarpsSmall, true, false>, dim3(grid), dim3(32 * kWarpsSmall), smem, stream, true, a, plan);
+    const cudaError_t e = launch(gemv_kernel<true, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(5);
     return QDG_OK;
