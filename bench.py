@@ -381,17 +381,10 @@ def bench_ours(args, wl, world, rank, local):
     side.wait_stream(stream)
     graphs = {}
     counts = {}
-    # One graph holds N_INPUT_SETS consecutive steps (one per input set), as a
-    # multi-layer forward pass would: programmatic dependent launch chains the
-    # kernels inside a graph, while consecutive graph launches serialise.
     with torch.cuda.stream(side):
         for fz in (fused, not fused):
             before = [qdg.qdg_launch_count(i) for i in range(6)]
-
-            def steps(fz=fz):
-                for p in range(N_INPUT_SETS):
-                    step.run(step.x_dev[p], fused=fz)
-            graphs[fz] = capture(steps, side)
+            graphs[fz] = [capture(lambda p=p: step.run(step.x_dev[p], fused=fz), side) for p in range(N_INPUT_SETS)]
             after = [qdg.qdg_launch_count(i) for i in range(6)]
             counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(6)]
     stream.wait_stream(side)
@@ -402,16 +395,11 @@ def bench_ours(args, wl, world, rank, local):
               "per_step_launches": {"fused_norm_gemv": counts[fused][5], "standalone_quantize": counts[fused][0],
                                     "gemv": counts[fused][1]}}
 
-    def run_steps(n, fz=fused):
-        """n decode steps: whole graphs of N_INPUT_SETS steps, the remainder eagerly."""
-        if not args.graph:
-            for k in range(n):
-                step.run(step.x_dev[k % N_INPUT_SETS], fused=fz)
-            return
-        for _ in range(n // N_INPUT_SETS):
-            graphs[fz].replay()
-        for k in range(n % N_INPUT_SETS):
-            step.run(step.x_dev[k], fused=fz)
+    def one_step(k, fz=fused):
+        if args.graph:
+            graphs[fz][k % N_INPUT_SETS].replay()
+        else:
+            step.run(step.x_dev[k % N_INPUT_SETS], fused=fz)
 
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -420,10 +408,14 @@ def bench_ours(args, wl, world, rank, local):
     sampler = ClockSampler(smi_id)
     sampler.start()
     t_end = time.time() + 0.6                       # pre-roll: clocks under this load
+    k = 0
     while time.time() < t_end:
-        run_steps(200)
-        torch.cuda.synchronize()
-    run_steps(args.warmup)
+        one_step(k)
+        k += 1
+        if k % 200 == 0:
+            torch.cuda.synchronize()
+    for k in range(args.warmup):
+        one_step(k)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -431,7 +423,8 @@ def bench_ours(args, wl, world, rank, local):
     e1 = torch.cuda.Event(enable_timing=True)
     sampler.mark("t0")
     e0.record(stream)
-    run_steps(args.steps)
+    for k in range(args.steps):
+        one_step(k)
     e1.record(stream)
     torch.cuda.synchronize()
     sampler.mark("t1")
@@ -442,19 +435,24 @@ def bench_ours(args, wl, world, rank, local):
     if status != qdg.QDG_OK:
         raise RuntimeError(f"device status after timed region: {qdg.status_string(status)}")
     t_end = time.time() + 0.3                       # post-roll
+    k = 0
     while time.time() < t_end:
-        run_steps(200)
-        torch.cuda.synchronize()
+        one_step(k)
+        k += 1
+        if k % 200 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     clocks = sampler.stop()
 
     # ---- the other route, same number of steps, for comparison
-    run_steps(args.warmup, not fused)
+    for k in range(args.warmup):
+        one_step(k, not fused)
     torch.cuda.synchronize()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    run_steps(args.steps, not fused)
+    for k in range(args.steps):
+        one_step(k, not fused)
     f1.record(stream)
     torch.cuda.synchronize()
     ms_other = f0.elapsed_time(f1) / args.steps
@@ -496,19 +494,13 @@ def bench_ours(args, wl, world, rank, local):
     n_e2e = max(10, min(args.steps, 500))
     h2d = sum(t.numel() * 4 for t in step.x_host[0].values())
     d2h = sum(t.numel() * 4 for t in step.y_host.values())
-    e2e_graphs = None
-    if args.graph:
-        with torch.cuda.stream(side):
-            e2e_graphs = [capture(lambda p=p: step.run(step.x_dev[p], fused=fused), side) for p in range(N_INPUT_SETS)]
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
     for k in range(3):
-        _e2e_step(step, e2e_graphs, k, fused)
+        _e2e_step(step, graphs[fused] if args.graph else None, k, fused)
     torch.cuda.synchronize()
     barrier(world)
     f0.record(stream)
     for k in range(n_e2e):
-        _e2e_step(step, e2e_graphs, k, fused)
+        _e2e_step(step, graphs[fused] if args.graph else None, k, fused)
     f1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
@@ -545,8 +537,7 @@ def bench_ours(args, wl, world, rank, local):
                    "bytes_per_step": nbytes, "l2": "inputs larger than L2 (419 MB of weights per step vs 129 MB L2)",
                    "route": "fused RMSNorm->Q8_0->GEMV, one launch per projection" if fused
                    else "standalone quantize + GEMV",
-                   "launch": ((f"cuda graph of {N_INPUT_SETS} steps" if args.graph else "eager") +
-                              (" + PDL" if args.pdl else "")),
+                   "launch": ("cuda graph" if args.graph else "eager") + (" + PDL" if args.pdl else ""),
                    "parallelism": f"replicas x{world}"},
         "us_per_step": round(ms * 1e3, 2),
         "us_per_call": {k: round(v, 2) for k, v in per_call.items()},

@@ -119,13 +119,12 @@ QDG_API int q4_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, i
  *        for plain quantization.   eps >= 0 (inside the square root).
  * y      [O] fp32 (overwritten).
  * xq_out [K/32] Q8_0 or NULL: if given, receives the quantized activations.
- * K      multiple of 256, 256 <= K <= 16384 (the Q8_0 vector is kept in
+ * K      multiple of 256, 256 <= K <= 16384 (x and gamma are staged in
  *        shared memory).
  * The quantized activations are bit-identical to qnorm_quantize_q8_0's and y
- * is bit-identical to q4_0_q8_0_gemv on them.  The CTAs of a thread-block
- * cluster split the norm and the quantization between them and exchange the
- * results through distributed shared memory, while their first weight
- * segments are already in flight.
+ * is bit-identical to q4_0_q8_0_gemv on them.  Every CTA recomputes the
+ * norm and the quantization (the vector is small and L2-resident) while its
+ * first weight segments are already in flight.
  */
 QDG_API int q4_0_gemv_rmsnorm(const void* W, const float* x, const float* gamma, float eps, float* y,
                               int64_t O, int64_t K, void* xq_out, qdg_stream_t stream);

@@ -99,34 +99,6 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// Thread-block clusters: rank, size, hardware barrier (split arrive / wait),
-// and loads from another CTA's shared memory (distributed shared memory).
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ uint32_t cluster_size() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
-__device__ __forceinline__ void cluster_sync() {
-    cluster_arrive();
-    cluster_wait();
-}
-__device__ __forceinline__ uint32_t dsmem_ld_u32(const void* local, uint32_t rank) {
-    uint32_t raddr, v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
-    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(raddr) : "memory");
-    return v;
-}
-__device__ __forceinline__ float dsmem_ld_f32(const float* local, uint32_t rank) {
-    return __uint_as_float(dsmem_ld_u32(local, rank));
-}
-
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }
@@ -155,37 +127,24 @@ DeviceInfo device_info();
 bool pdl_enabled();
 void count_launch(int which);
 
-// Launch with the PDL attribute when enabled, and a cluster shape when cluster > 1.
+// Launch with the PDL attribute when enabled.
 template <typename Kern, typename... Args>
-cudaError_t launch_cluster(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool allow_pdl,
-                           int cluster, Args... args) {
+cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool allow_pdl,
+                   Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
+    cudaLaunchAttribute attr[1];
     cfg.attrs = attr;
     cfg.numAttrs = 0;
     if (allow_pdl && pdl_enabled()) {
-        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
-        ++cfg.numAttrs;
-    }
-    if (cluster > 1) {
-        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
-        attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(cluster);
-        attr[cfg.numAttrs].val.clusterDim.y = 1;
-        attr[cfg.numAttrs].val.clusterDim.z = 1;
-        ++cfg.numAttrs;
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 1;
     }
     return cudaLaunchKernelEx(&cfg, kernel, args...);
-}
-
-template <typename Kern, typename... Args>
-cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool allow_pdl,
-                   Args... args) {
-    return launch_cluster(kernel, grid, block, smem, stream, allow_pdl, 1, args...);
 }
 
 // Internal launchers shared with the debug hook (dbg != nullptr writes the

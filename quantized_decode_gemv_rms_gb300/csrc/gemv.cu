@@ -43,8 +43,7 @@ constexpr int kDepth = 3;                   // row-segments in flight per warp (
 constexpr int kSegBytes = 1152;             // 32 pairs x 36 bytes
 constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
-constexpr int kFusedMaxK = 16384;           // fused form keeps the Q8_0 vector in shared memory
-constexpr int kMaxCluster = 8;              // CTAs sharing the fused prologue
+constexpr int kFusedMaxK = 16384;           // fused form stages x and gamma in shared memory
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
 
 struct Plan {
@@ -193,82 +192,61 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
     float dxa = 0.0f, dxb = 0.0f;
     int sa = 0, sb = 0;
     if (kFused) {
-        // The CTAs of a thread-block cluster (C of them) share the work of the
-        // norm and of the quantization and exchange results through
-        // distributed shared memory; every CTA ends up with the whole Q8_0
-        // vector, bit-identical to the standalone quantize kernel's.
         const int K = a.K;
         const int nb = K >> 5;
-        const int C = static_cast<int>(cluster_size());
-        const int rank = static_cast<int>(cluster_rank());
-        uint8_t* xqs = fused_smem;                       // [nb][34] Q8_0 blocks (own range filled)
-        const int qb0 = rank * nb / C, qb1 = (rank + 1) * nb / C;
-
-        // Issue this CTA's quantization loads first: block b = qb0 + warp + u*kWarps, lane = element.
-        constexpr int kQ = 8;                            // up to 8 blocks per warp per round
-        float v[kQ], gv[kQ];
-        auto load_round = [&](int round) {
-#pragma unroll
-            for (int u = 0; u < kQ; ++u) {
-                const int b = qb0 + warp + (round * kQ + u) * kWarps;
-                v[u] = b < qb1 ? __ldg(a.x + (b << 5) + lane) : 0.0f;
-                gv[u] = (a.gamma != nullptr && b < qb1) ? __ldg(a.gamma + (b << 5) + lane) : 1.0f;
+        float* xs = reinterpret_cast<float*>(fused_smem);
+        float* gs = xs + K;
+        uint8_t* xqs = reinterpret_cast<uint8_t*>(gs + K);
+        // (1) stage x and gamma with one wave of 16-byte loads
+        {
+            const float4* x4 = reinterpret_cast<const float4*>(a.x);
+            const float4* g4 = reinterpret_cast<const float4*>(a.gamma);
+            for (int i = threadIdx.x; i < K / 4; i += kThreads) {
+                reinterpret_cast<float4*>(xs)[i] = __ldg(x4 + i);
+                if (a.gamma != nullptr) reinterpret_cast<float4*>(gs)[i] = __ldg(g4 + i);
             }
-        };
-        load_round(0);
-
-        // RMS statistic, fixed order: chain j sums x_i^2 over i = j (mod 256)
-        // ascending with fma; group g = chains 32g..32g+31 folds with the xor
-        // butterfly; total = ((g0+g1)+(g2+g3))+((g4+g5)+(g6+g7)).  This CTA
-        // computes groups [rank*8/C, (rank+1)*8/C).
+        }
+        __syncthreads();
+        // (2) RMS statistic in the library's fixed order: chain j (threads
+        // 0..255) sums x_i^2 over i = j (mod 256) ascending with fma; warp
+        // butterflies; ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).
         float s = 1.0f;
         if (a.gamma != nullptr) {
-            const int groups = 8 / C;
-            if (warp < groups) {
-                const int j = (rank * groups + warp) * 32 + lane;
+            if (threadIdx.x < 256) {
                 float acc = 0.0f;
-                for (int i0 = j; i0 < K; i0 += 256 * 8) {
-                    float xv[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int i = i0 + u * 256;
-                        xv[u] = i < K ? __ldg(a.x + i) : 0.0f;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        if (i0 + u * 256 < K) acc = __fmaf_rn(xv[u], xv[u], acc);
-                }
+                for (int i = threadIdx.x; i < K; i += 256) acc = __fmaf_rn(xs[i], xs[i], acc);
                 acc = warp_sum(acc);
-                if (lane == 0) norm_part[rank * groups + warp] = acc;
+                if (lane == 0) norm_part[warp] = acc;
             }
-            cluster_sync();
-            float gt[8];
-#pragma unroll
-            for (int g = 0; g < 8; ++g) gt[g] = dsmem_ld_f32(&norm_part[g], static_cast<uint32_t>(g / groups));
-            const float ss = __fadd_rn(__fadd_rn(__fadd_rn(gt[0], gt[1]), __fadd_rn(gt[2], gt[3])),
-                                       __fadd_rn(__fadd_rn(gt[4], gt[5]), __fadd_rn(gt[6], gt[7])));
+            __syncthreads();
+            const float ss = __fadd_rn(__fadd_rn(__fadd_rn(norm_part[0], norm_part[1]), __fadd_rn(norm_part[2], norm_part[3])),
+                                       __fadd_rn(__fadd_rn(norm_part[4], norm_part[5]), __fadd_rn(norm_part[6], norm_part[7])));
             const float mean = __fdiv_rn(ss, static_cast<float>(K));
             s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
         }
-
-        // Q8_0 blocks [qb0, qb1): v = (x*s)*gamma, d = max|v|/127, q = round(v/d).
-        const int rounds = (qb1 - qb0 + kQ * kWarps - 1) / (kQ * kWarps);
-        for (int round = 0; round < rounds; ++round) {
-            if (round > 0) load_round(round);
-            float d[kQ];
+        // (3) Q8_0 blocks, one per warp at a time (lane = element), four
+        // independent blocks interleaved; the arithmetic of the standalone
+        // quantize kernel: v = (x*s)*gamma, d = max|v|/127, q = round(v/d).
+        for (int b0 = warp; b0 < nb; b0 += 4 * kWarps) {
+            float v[4], d[4];
 #pragma unroll
-            for (int u = 0; u < kQ; ++u) {
-                if (a.gamma != nullptr) v[u] = __fmul_rn(__fmul_rn(v[u], s), gv[u]);
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * kWarps;
+                v[u] = 0.0f;
+                if (b < nb) {
+                    v[u] = xs[(b << 5) + lane];
+                    if (a.gamma != nullptr) v[u] = __fmul_rn(__fmul_rn(v[u], s), gs[(b << 5) + lane]);
+                }
                 d[u] = fabsf(v[u]);
             }
 #pragma unroll
             for (int h = 16; h >= 1; h >>= 1)
 #pragma unroll
-                for (int u = 0; u < kQ; ++u) d[u] = fmaxf(d[u], __shfl_xor_sync(0xffffffffu, d[u], h));
+                for (int u = 0; u < 4; ++u) d[u] = fmaxf(d[u], __shfl_xor_sync(0xffffffffu, d[u], h));
 #pragma unroll
-            for (int u = 0; u < kQ; ++u) {
-                const int b = qb0 + warp + (round * kQ + u) * kWarps;
-                if (b >= qb1) break;
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * kWarps;
+                if (b >= nb) break;
                 const float dd = __fdiv_rn(d[u], 127.0f);
                 int q = 0;
                 if (dd != 0.0f) {
@@ -285,35 +263,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
                 blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
             }
         }
-        cluster_sync();
-        if (a.xq_out != nullptr && blockIdx.x < C) {    // the first cluster publishes the vector
-            for (int i = threadIdx.x; i < (qb1 - qb0) * 34 / 2; i += kThreads)
-                reinterpret_cast<unsigned short*>(a.xq_out + qb0 * 34)[i] =
-                    reinterpret_cast<const unsigned short*>(xqs + qb0 * 34)[i];
+        __syncthreads();
+        if (a.xq_out != nullptr && blockIdx.x == 0) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(xqs);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(a.xq_out);
+            for (int i = threadIdx.x; i < nb * 34 / 4; i += kThreads) dst[i] = src[i];
         }
-        // this lane's two blocks, from the CTAs that quantized them
+        // (4) this lane's pair, from shared memory
         if (active) {
+            const uint32_t* xp = reinterpret_cast<const uint32_t*>(xqs + static_cast<size_t>(p) * 68);
             uint32_t w[17];
-            const int ba = 2 * p, bb = 2 * p + 1;
-            uint32_t ra = 0, rb = 0;   // owners: rank r quantized blocks [r*nb/C, (r+1)*nb/C)
-            for (int r = 1; r < C; ++r) {
-                if (ba >= r * nb / C) ra = static_cast<uint32_t>(r);
-                if (bb >= r * nb / C) rb = static_cast<uint32_t>(r);
-            }
-            // block ba occupies bytes [68p, 68p+34), block bb [68p+34, 68p+68)
-            const uint32_t* pa = reinterpret_cast<const uint32_t*>(xqs + static_cast<size_t>(p) * 68);
 #pragma unroll
-            for (int i = 0; i < 17; ++i) {
-                // word i spans bytes 4i..4i+3: words 0..7 in block ba, word 8 straddles, 9..16 in bb
-                if (i < 8) {
-                    w[i] = dsmem_ld_u32(pa + i, ra);
-                } else if (i == 8) {
-                    const uint32_t lo = dsmem_ld_u32(pa + 8, ra), hi = dsmem_ld_u32(pa + 8, rb);
-                    w[i] = (lo & 0xFFFFu) | (hi & 0xFFFF0000u);
-                } else {
-                    w[i] = dsmem_ld_u32(pa + i, rb);
-                }
-            }
+            for (int i = 0; i < 17; ++i) w[i] = xp[i];
             dxa = half_bits_to_float(w[0]);
 #pragma unroll
             for (int i = 0; i < 8; ++i) xa[i] = bytes_2_to_5(w[i], w[i + 1]);
@@ -329,9 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
 #pragma unroll
             for (int i = 0; i < 8; ++i) xa[i] = xb[i] = 0u;
         }
-        // Remote reads of this CTA's shared memory end here; the matching wait
-        // is at the end of the kernel, so no CTA leaves while others read it.
-        cluster_arrive();
     } else if (active) {
         const uint32_t* xp = reinterpret_cast<const uint32_t*>(a.xq + static_cast<size_t>(p) * 68);
         uint32_t w[17];
@@ -421,7 +379,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
         }
         __syncthreads();
     }
-    if (kFused) cluster_wait();
 }
 
 }  // namespace
@@ -477,6 +434,7 @@ int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O,
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     const Plan plan = make_plan(K);
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
     a.ng = count;
     a.W = a.Wg[0];
     a.x = x;
@@ -486,49 +444,19 @@ int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O,
     a.y = a.yg[0];
     a.O = total;
     a.K = static_cast<int>(K);
-    const size_t smem = static_cast<size_t>(K / 32) * 34;
-    // Largest cluster (8, 4, 2, 1) whose clusters can all be resident at once
-    // over (a multiple of it) the SMs.
-    static std::mutex mu;
-    static int cached_cluster = 0, cached_grid = 0;
-    int cluster, grid;
+    const size_t smem = static_cast<size_t>(8) * K + static_cast<size_t>(K / 32) * 34;
     {
+        static std::mutex mu;
+        static size_t set_bytes = 0;
         std::lock_guard<std::mutex> lock(mu);
-        if (cached_cluster == 0) {
+        if (set_bytes < smem) {
             if (cudaFuncSetAttribute(gemv_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(static_cast<size_t>(kFusedMaxK / 32) * 34)) != cudaSuccess ||
-                cudaFuncSetAttribute(gemv_kernel<true, false>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-                    cudaSuccess)
+                                     static_cast<int>(smem)) != cudaSuccess)
                 return QDG_ECUDA;
-            cached_cluster = 1;
-            cached_grid = dev.sms;
-            for (int c = kMaxCluster; c >= 2; c /= 2) {
-                cudaLaunchConfig_t cfg = {};
-                cfg.gridDim = dim3(static_cast<unsigned>(dev.sms / c * c));
-                cfg.blockDim = dim3(kThreads);
-                cfg.dynamicSmemBytes = static_cast<size_t>(kFusedMaxK / 32) * 34;
-                cudaLaunchAttribute attr;
-                attr.id = cudaLaunchAttributeClusterDimension;
-                attr.val.clusterDim.x = static_cast<unsigned>(c);
-                attr.val.clusterDim.y = 1;
-                attr.val.clusterDim.z = 1;
-                cfg.attrs = &attr;
-                cfg.numAttrs = 1;
-                int nclusters = 0;
-                if (cudaOccupancyMaxActiveClusters(&nclusters, gemv_kernel<true, false>, &cfg) == cudaSuccess &&
-                    nclusters * c >= dev.sms - dev.sms / 16) {
-                    cached_cluster = c;
-                    cached_grid = nclusters * c < dev.sms / c * c ? nclusters * c : dev.sms / c * c;
-                    break;
-                }
-                cudaGetLastError();
-            }
+            set_bytes = smem;
         }
-        cluster = cached_cluster;
-        grid = cached_grid;
     }
-    const cudaError_t e = launch_cluster(gemv_kernel<true, false>, dim3(grid), dim3(kThreads), smem, stream, true,
-                                         cluster, a, plan);
+    const cudaError_t e = launch(gemv_kernel<true, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(5);
     return QDG_OK;
