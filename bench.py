@@ -310,7 +310,7 @@ class DecodeStep:
         torch.cuda.empty_cache()      # release the fp32 staging of the weights
 
     def launches_per_step(self, fused=True):
-        return len(self.groups) if fused else len(self.wl.activations) + len(self.wl.matrices)
+        return len(self.groups) * (1 if fused else 2)
 
     def run_group(self, grp, xs, Ws=None):
         """One fused launch for projections that read the same activation."""
@@ -321,29 +321,20 @@ class DecodeStep:
                                          self.wl.eps, grp[0].cols)
 
     def run(self, xs, events=None, fused=True):
+        """One decode step in dependency order: for each group of projections
+        sharing an input -- fused: one launch (RMSNorm*gamma -> Q8_0 -> GEMV);
+        split: the quantize kernel, then one grouped GEMV launch."""
         qdg = self.qdg
-        if fused:
-            # one launch per group of projections sharing an input:
-            # RMSNorm*gamma -> Q8_0 -> GEMV over all rows of the group
-            for grp in self.groups:
+        for grp in self.groups:
+            if fused:
                 self.run_group(grp, xs)
-            return
-        i = 0
-        for tag, K in self.wl.activations.items():
-            g = self.gamma.get(tag)
-            if events:
-                events[i].record()
+                continue
+            tag = grp[0].source.split(":", 1)[1]
+            K = grp[0].cols
+            g = self.gamma.get(tag) if self.kinds[tag] == "norm" else None
             qdg.qnorm_quantize_q8_0(xs[tag], g, self.wl.eps, self.xq[tag], K=K, N=1)
-            i += 1
-        for m in self.wl.matrices:
-            tag = m.source.split(":", 1)[1]
-            if events:
-                events[i].record()
-            qdg.q4_0_q8_0_gemv(self.W[m.name], self.xq[tag], self.y[m.name], m.rows, m.cols)
-            i += 1
-        if events:
-            events[i].record()
-
+            qdg.q4_0_q8_0_gemv_group([self.W[m.name] for m in grp], [self.y[m.name] for m in grp],
+                                     [m.rows for m in grp], self.xq[tag], K)
 
 def capture(fn, side, count=1):
     """CUDA graph of `count` calls of fn (on the side stream)."""
@@ -365,7 +356,7 @@ def bench_ours(args, wl, world, rank, local):
     step = DecodeStep(wl, device)
     stream = torch.cuda.current_stream()
     nbytes = step_bytes(wl)
-    fused = not args.unfused
+    fused = args.fused
     L = step.launches_per_step(fused)
 
     # eager warm-up of both routes (also sets kernel attributes before capture)
@@ -381,25 +372,38 @@ def bench_ours(args, wl, world, rank, local):
     side.wait_stream(stream)
     graphs = {}
     counts = {}
+    # One graph holds N_INPUT_SETS consecutive steps (one per input set), as a
+    # multi-layer forward pass would: programmatic dependent launch chains the
+    # kernels inside a graph, while consecutive graph launches serialise.
     with torch.cuda.stream(side):
         for fz in (fused, not fused):
             before = [qdg.qdg_launch_count(i) for i in range(6)]
-            graphs[fz] = [capture(lambda p=p: step.run(step.x_dev[p], fused=fz), side) for p in range(N_INPUT_SETS)]
+
+            def steps(fz=fz):
+                for p in range(N_INPUT_SETS):
+                    step.run(step.x_dev[p], fused=fz)
+            graphs[fz] = capture(steps, side)
             after = [qdg.qdg_launch_count(i) for i in range(6)]
             counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(6)]
     stream.wait_stream(side)
     torch.cuda.synchronize()
-    if fused:
-        assert counts[True][5] == len(step.groups) and counts[True][0] == 0 and counts[True][1] == 0, counts
-    fusion = {"route": "fused" if fused else "unfused",
-              "per_step_launches": {"fused_norm_gemv": counts[fused][5], "standalone_quantize": counts[fused][0],
+    ng = len(step.groups)
+    assert counts[True][5] == ng and counts[True][0] == 0 and counts[True][1] == 0, counts
+    assert counts[False][0] == ng and counts[False][1] == ng and counts[False][5] == 0, counts
+    fusion = {"route": "fused" if fused else "split",
+              "per_step_launches": {"fused_norm_gemv": counts[fused][5], "quantize": counts[fused][0],
                                     "gemv": counts[fused][1]}}
 
-    def one_step(k, fz=fused):
-        if args.graph:
-            graphs[fz][k % N_INPUT_SETS].replay()
-        else:
-            step.run(step.x_dev[k % N_INPUT_SETS], fused=fz)
+    def run_steps(n, fz=fused):
+        """n decode steps: whole graphs of N_INPUT_SETS steps, the remainder eagerly."""
+        if not args.graph:
+            for k in range(n):
+                step.run(step.x_dev[k % N_INPUT_SETS], fused=fz)
+            return
+        for _ in range(n // N_INPUT_SETS):
+            graphs[fz].replay()
+        for k in range(n % N_INPUT_SETS):
+            step.run(step.x_dev[k], fused=fz)
 
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -408,14 +412,10 @@ def bench_ours(args, wl, world, rank, local):
     sampler = ClockSampler(smi_id)
     sampler.start()
     t_end = time.time() + 0.6                       # pre-roll: clocks under this load
-    k = 0
     while time.time() < t_end:
-        one_step(k)
-        k += 1
-        if k % 200 == 0:
-            torch.cuda.synchronize()
-    for k in range(args.warmup):
-        one_step(k)
+        run_steps(200)
+        torch.cuda.synchronize()
+    run_steps(args.warmup)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
@@ -423,8 +423,7 @@ def bench_ours(args, wl, world, rank, local):
     e1 = torch.cuda.Event(enable_timing=True)
     sampler.mark("t0")
     e0.record(stream)
-    for k in range(args.steps):
-        one_step(k)
+    run_steps(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     sampler.mark("t1")
@@ -435,89 +434,101 @@ def bench_ours(args, wl, world, rank, local):
     if status != qdg.QDG_OK:
         raise RuntimeError(f"device status after timed region: {qdg.status_string(status)}")
     t_end = time.time() + 0.3                       # post-roll
-    k = 0
     while time.time() < t_end:
-        one_step(k)
-        k += 1
-        if k % 200 == 0:
-            torch.cuda.synchronize()
+        run_steps(200)
+        torch.cuda.synchronize()
     torch.cuda.synchronize()
     clocks = sampler.stop()
 
     # ---- the other route, same number of steps, for comparison
-    for k in range(args.warmup):
-        one_step(k, not fused)
+    run_steps(args.warmup, not fused)
     torch.cuda.synchronize()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record(stream)
-    for k in range(args.steps):
-        one_step(k, not fused)
+    run_steps(args.steps, not fused)
     f1.record(stream)
     torch.cuda.synchronize()
     ms_other = f0.elapsed_time(f1) / args.steps
 
-    # ---- per-launch cost: a graph of C back-to-back launches of one group, each
-    # on its own copy of the weights (C copies exceed three L2 sizes, so every
+    # ---- per-launch cost of each group's launch (GEMV alone on a prepared Q8_0
+    # vector, and the fused launch): a graph of C back-to-back launches, each on
+    # its own copy of the weights (C copies exceed three L2 sizes, so every
     # launch streams its weights from HBM)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    per_call = {}
-    launch_bytes = {}
+    per_call = {"gemv": {}, "fused": {}}
+    launch_bytes = {"gemv": {}, "fused": {}}
+    for p_ in range(1):
+        step.run(step.x_dev[0], fused=False)          # the Q8_0 vectors of input set 0
+    torch.cuda.synchronize()
     for grp in step.groups:
         name = "+".join(m.name for m in grp)
+        tag = grp[0].source.split(":", 1)[1]
+        K = grp[0].cols
         gbytes = sum(workloads.q4_0_bytes(m.rows, m.cols) for m in grp)
         copies = int(min(160, max(2, -(-3 * l2 // gbytes))))
         Wc = [[step.W[m.name] for m in grp]] + [[step.W[m.name].clone() for m in grp] for _ in range(copies - 1)]
-        with torch.cuda.stream(side):
-            gr = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(gr, stream=side):
-                for c in range(copies):
+        for kind in ("gemv", "fused"):
+            def one(c, kind=kind):
+                if kind == "fused":
                     step.run_group(grp, step.x_dev[0], Ws=Wc[c])
-            gr.replay()
-            side.synchronize()
-            a0 = torch.cuda.Event(enable_timing=True)
-            a1 = torch.cuda.Event(enable_timing=True)
-            a0.record(side)
-            for _ in range(3):
+                else:
+                    qdg.q4_0_q8_0_gemv_group(Wc[c], [step.y[m.name] for m in grp], [m.rows for m in grp],
+                                             step.xq[tag], K)
+            with torch.cuda.stream(side):
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=side):
+                    for c in range(copies):
+                        one(c)
                 gr.replay()
-            a1.record(side)
-            side.synchronize()
-        per_call[name] = a0.elapsed_time(a1) * 1e3 / (3 * copies)
-        launch_bytes[name] = sum(fused_launch_bytes(m) for m in grp) - (
-            4 * grp[0].cols * (2 if grp[0].source.startswith("norm:") else 1) * (len(grp) - 1))
-        del gr, Wc
+                side.synchronize()
+                a0 = torch.cuda.Event(enable_timing=True)
+                a1 = torch.cuda.Event(enable_timing=True)
+                a0.record(side)
+                for _ in range(3):
+                    gr.replay()
+                a1.record(side)
+                side.synchronize()
+            per_call[kind][name] = a0.elapsed_time(a1) * 1e3 / (3 * copies)
+            del gr
+        xbytes = 4 * K * (2 if grp[0].source.startswith("norm:") else 1)
+        launch_bytes["fused"][name] = gbytes + xbytes + sum(4 * m.rows for m in grp)
+        launch_bytes["gemv"][name] = gbytes + workloads.q8_0_bytes(1, K) + sum(4 * m.rows for m in grp)
+        del Wc
         torch.cuda.empty_cache()
     torch.cuda.synchronize()
-    gbs_per_call = {n: launch_bytes[n] / (per_call[n] * 1e-6) / 1e9 for n in per_call}
+    gbs_per_call = {kind: {n: launch_bytes[kind][n] / (per_call[kind][n] * 1e-6) / 1e9 for n in per_call[kind]}
+                    for kind in per_call}
 
     # ---- end to end through the same calls, inputs from pinned host memory
     n_e2e = max(10, min(args.steps, 500))
     h2d = sum(t.numel() * 4 for t in step.x_host[0].values())
     d2h = sum(t.numel() * 4 for t in step.y_host.values())
+    e2e_graphs = None
+    if args.graph:
+        with torch.cuda.stream(side):
+            e2e_graphs = [capture(lambda p=p: step.run(step.x_dev[p], fused=fused), side) for p in range(N_INPUT_SETS)]
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
     for k in range(3):
-        _e2e_step(step, graphs[fused] if args.graph else None, k, fused)
+        _e2e_step(step, e2e_graphs, k, fused)
     torch.cuda.synchronize()
     barrier(world)
     f0.record(stream)
     for k in range(n_e2e):
-        _e2e_step(step, graphs[fused] if args.graph else None, k, fused)
+        _e2e_step(step, e2e_graphs, k, fused)
     f1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
 
     peaks, peak_src = measured_peaks()
-    if fused:
-        # Every launch of the fused step is the fused GEMV kernel: its average
-        # launch duration is at most the step time over the launches per step.
-        kern_bytes = sum(launch_bytes.values())
-        achieved = kern_bytes / (ms * 1e-3) / 1e9
-        kernel = "gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)"
-        traffic = ncu_traffic("gemv.cu")
-    else:
-        kern_bytes = sum(launch_bytes.values())
-        achieved = kern_bytes / (sum(per_call.values()) * 1e-6) / 1e9
-        kernel = "gemv_kernel<fused> (per-group graphs)"
-        traffic = None
+    kind = "fused" if fused else "gemv"
+    kern_bytes = sum(launch_bytes[kind].values())
+    # the dominant kernel's average launch from the per-launch graphs above
+    achieved = kern_bytes / (sum(per_call[kind].values()) * 1e-6) / 1e9
+    kernel = ("gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)" if fused
+              else "gemv_kernel (q4_0_q8_0_gemv_group)")
+    traffic = ncu_traffic("gemv.cu")
     roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)" if peak_src == "measured"
@@ -525,7 +536,8 @@ def bench_ours(args, wl, world, rank, local):
             "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
             "traffic_source": (traffic.get("what") if traffic else "no ncu capture of this source yet"),
             "algorithmic_bytes_per_launch": round(kern_bytes / len(step.groups)),
-            "launches_per_step": len(step.groups),
+            "launches_of_this_kernel_per_step": len(step.groups),
+            "achieved_over_whole_step": round(kern_bytes / (ms * 1e-3) / 1e9, 1),
             "frac_of_nominal_8TB": round(achieved / 8000.0, 4)}
     result = {
         "metric": METRIC, "value": round(nbytes * world / (ms * 1e-3) / 1e9, 1), "unit": UNIT,
@@ -535,16 +547,19 @@ def bench_ours(args, wl, world, rank, local):
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations with 1% x20 outliers)",
         "config": {"workload": wl.name, "batch": 1, "matrices": {m.name: [m.rows, m.cols] for m in wl.matrices},
                    "bytes_per_step": nbytes, "l2": "inputs larger than L2 (419 MB of weights per step vs 129 MB L2)",
-                   "route": "fused RMSNorm->Q8_0->GEMV, one launch per projection" if fused
-                   else "standalone quantize + GEMV",
-                   "launch": ("cuda graph" if args.graph else "eager") + (" + PDL" if args.pdl else ""),
+                   "route": ("fused: one RMSNorm->Q8_0->GEMV launch per group" if fused else
+                             "split: quantize kernel + grouped GEMV launch per group") +
+                            "; groups q+k+v, o, gate+up, down, head in dependency order",
+                   "launch": ((f"cuda graph of {N_INPUT_SETS} steps" if args.graph else "eager") +
+                              (" + PDL" if args.pdl else "")),
                    "parallelism": f"replicas x{world}"},
         "us_per_step": round(ms * 1e3, 2),
-        "us_per_call": {k: round(v, 2) for k, v in per_call.items()},
-        "gbs_per_call": {k: round(v, 1) for k, v in gbs_per_call.items()},
-        "per_call_note": ("one fused launch per group of projections sharing an input; graph of back-to-back "
-                          "launches on distinct weight copies (> 3 x L2), PDL as configured"),
-        "other_route": {"route": "standalone quantize + GEMV" if fused else "fused",
+        "us_per_call": {k: {n: round(v, 2) for n, v in d.items()} for k, d in per_call.items()},
+        "gbs_per_call": {k: {n: round(v, 1) for n, v in d.items()} for k, d in gbs_per_call.items()},
+        "per_call_note": ("one launch per group of projections sharing an input (gemv: on a prepared Q8_0 vector; "
+                          "fused: norm+quantize+GEMV); graph of back-to-back launches on distinct weight copies "
+                          "(> 3 x L2), PDL as configured"),
+        "other_route": {"route": "split" if fused else "fused",
                         "us_per_step": round(ms_other * 1e3, 2),
                         "value": round(nbytes / (ms_other * 1e-3) / 1e9, 1)},
         "fusion_check": fusion,
@@ -644,8 +659,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.LLAMA_8B.name, choices=sorted(workloads.ALL))
     ap.add_argument("--no-graph", dest="graph", action="store_false")
-    ap.add_argument("--unfused", action="store_true",
-                    help="time the standalone quantize + GEMV route (the fused route is the default)")
+    ap.add_argument("--fused", action="store_true",
+                    help="time the fused route (one norm+quantize+GEMV launch per group) as the main line; "
+                         "the default main line is quantize kernel + grouped GEMV per group")
     ap.add_argument("--pdl", action="store_true", default=True)
     ap.add_argument("--no-pdl", dest="pdl", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")

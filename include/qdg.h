@@ -108,6 +108,17 @@ QDG_API int q4_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, i
                    qdg_stream_t stream);
 
 /*
+ * q4_0_q8_0_gemv_group -- q4_0_q8_0_gemv for up to 4 matrices that read the
+ * same Q8_0 vector (a decode layer's q, k and v; its gate and up), in one
+ * launch: y[g] = W[g] * x.  W, y, O are host arrays of `count` (1..4) entries:
+ * device pointers W[g] ([O[g]][K/32] Q4_0, 16-byte aligned), y[g] ([O[g]]
+ * fp32), row counts O[g] >= 1; all matrices have the same K (multiple of 256,
+ * <= 32768).  Results are bit-identical to one q4_0_q8_0_gemv per matrix.
+ */
+QDG_API int q4_0_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                 const void* xq, int64_t K, qdg_stream_t stream);
+
+/*
  * q4_0_gemv_rmsnorm -- the fused decode route: RMS_NORM + MUL(gamma) + Q8_0
  * quantization + Q4_0 x Q8_0 GEMV in one kernel.  The norm/MUL pair is the
  * pattern whose fusion the Metal backend lost (about 5% of token generation)

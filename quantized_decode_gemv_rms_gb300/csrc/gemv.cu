@@ -383,25 +383,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
 
 }  // namespace
 
-int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream, int32_t* dbg) {
-    if (!W || !xq || (!y && !dbg)) return QDG_EINVAL;
-    if (O <= 0 || K <= 0) return QDG_EINVAL;
-    if (K % 256 != 0 || K > 32768 || O >= (int64_t(1) << 31)) return QDG_ESHAPE;
-    if (!aligned(W, 16) || !aligned(xq, 4) || !aligned(y, 4) || !aligned(dbg, 4)) return QDG_EALIGN;
+int gemv_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq, int64_t K,
+                      cudaStream_t stream, int32_t* dbg) {
+    if (!W || !O || !xq || (!y && !dbg)) return QDG_EINVAL;
+    if (count < 1 || count > kMaxGroup || K <= 0) return QDG_EINVAL;
+    if (dbg && count != 1) return QDG_EINVAL;
+    if (K % 256 != 0 || K > 32768) return QDG_ESHAPE;
+    if (!aligned(xq, 4) || !aligned(dbg, 4)) return QDG_EALIGN;
+    Args a{};
+    int64_t total = 0;
+    for (int g = 0; g < count; ++g) {
+        if (!W[g] || (!dbg && !y[g]) || O[g] <= 0) return QDG_EINVAL;
+        if (!aligned(W[g], 16) || (y && !aligned(y[g], 4))) return QDG_EALIGN;
+        a.Wg[g] = static_cast<const uint8_t*>(W[g]);
+        a.yg[g] = y ? y[g] : nullptr;
+        a.start[g] = total;
+        total += O[g];
+    }
+    if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     const Plan plan = make_plan(K);
-    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
-    Args a{};
-    a.W = static_cast<const uint8_t*>(W);
-    a.Wg[0] = a.W;
-    a.yg[0] = y;
-    a.start[0] = 0;
-    a.ng = 1;
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
+    a.ng = count;
+    a.W = a.Wg[0];
     a.xq = static_cast<const uint8_t*>(xq);
-    a.y = y;
+    a.y = a.yg[0];
     a.dbg = dbg;
-    a.O = O;
+    a.O = total;
     a.K = static_cast<int>(K);
     cudaError_t e;
     if (dbg)
@@ -411,6 +420,11 @@ int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, c
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(1);
     return QDG_OK;
+}
+
+int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream, int32_t* dbg) {
+    float* ys[1] = {y};
+    return gemv_launch_group(&W, y ? ys : nullptr, &O, 1, xq, K, stream, dbg);
 }
 
 int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O, int count, const float* x,
@@ -479,6 +493,12 @@ extern "C" int q4_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O
                               qdg_stream_t stream) {
     if (!y) return QDG_EINVAL;
     return qdg::gemv_launch(W, xq, y, O, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" int q4_0_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                    const void* xq, int64_t K, qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    return qdg::gemv_launch_group(W, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 extern "C" int q4_0_gemv_rmsnorm(const void* W, const float* x, const float* gamma, float eps, float* y, int64_t O,

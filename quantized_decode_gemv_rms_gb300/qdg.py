@@ -49,6 +49,7 @@ def lib() -> ctypes.CDLL:
             sig = {
                 "qnorm_quantize_q8_0": ([p, i64, p, f32, i64, i64, p, p], i32),
                 "q4_0_q8_0_gemv": ([p, p, p, i64, i64, p], i32),
+                "q4_0_q8_0_gemv_group": ([p, p, p, i32, p, i64, p], i32),
                 "q4_0_gemv_rmsnorm": ([p, p, p, f32, p, i64, i64, p, p], i32),
                 "q4_0_gemv_rmsnorm_group": ([p, p, p, i32, p, p, f32, i64, p, p], i32),
                 "q4_0_q8_0_gemm_small_n": ([p, p, p, i64, i64, i64, i64, p], i32),
@@ -127,6 +128,15 @@ def qnorm_quantize_q8_0(x, gamma, eps: float, xq, K: int | None = None, N: int |
 
 def q4_0_q8_0_gemv(W, xq, y, O: int, K: int, stream=None) -> None:
     _check(lib().q4_0_q8_0_gemv(_ptr(W), _ptr(xq), _ptr(y), O, K, _stream(stream)), "q4_0_q8_0_gemv")
+
+
+def q4_0_q8_0_gemv_group(Ws, ys, Os, xq, K: int, stream=None) -> None:
+    """GEMV for up to 4 matrices sharing one Q8_0 vector (one launch)."""
+    n = len(Ws)
+    W_arr = (ctypes.c_void_p * n)(*[_ptr(w) for w in Ws])
+    y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in ys])
+    O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
+    _check(lib().q4_0_q8_0_gemv_group(W_arr, y_arr, O_arr, n, _ptr(xq), K, _stream(stream)), "q4_0_q8_0_gemv_group")
 
 
 def q4_0_gemv_rmsnorm(W, x, gamma, eps: float, y, O: int, K: int, xq_out=None, stream=None) -> None:

@@ -98,6 +98,21 @@ def test_fused_group_host_validation(L):
     assert f(W, Y, Ob, 2, A16, None, 1e-6, 256, None, None) == -1       # empty matrix
 
 
+def test_gemv_group_host_validation(L):
+    import ctypes
+    f = L.q4_0_q8_0_gemv_group
+    W = (ctypes.c_void_p * 2)(A16, A16)
+    Y = (ctypes.c_void_p * 2)(A16, A16)
+    O = (ctypes.c_int64 * 2)(8, 8)
+    assert f(W, Y, O, 0, A16, 256, None) == -1          # count 0
+    assert f(W, Y, O, 5, A16, 256, None) == -1          # count > 4
+    assert f(W, None, O, 2, A16, 256, None) == -1       # no outputs
+    assert f(W, Y, O, 2, A16, 384, None) == -3          # K % 256
+    assert f(W, Y, O, 2, A2, 256, None) == -2           # xq not 4-byte aligned
+    Ob = (ctypes.c_int64 * 2)(8, -1)
+    assert f(W, Y, Ob, 2, A16, 256, None) == -1         # negative rows
+
+
 def test_small_n_host_validation(L):
     f = L.q4_0_q8_0_gemm_small_n
     assert f(A16, A16, A16, 8, 8, 256, 0, None) == -1      # N = 0

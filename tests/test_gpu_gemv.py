@@ -237,3 +237,31 @@ def test_fused_group_matches_single(Os, K):
         Wq_ref = oracle.quantize_q4_0(ws[i] if rows is None else ws[i][rows])
         _, y64, S = oracle.matvec(Wq_ref, xq_ref, K, threads=8)
         assert_within_tol((ga if rows is None else ga[rows])[None], y64, S)
+
+
+@pytest.mark.parametrize("Os,K", [((4096, 1024, 1024), 4096), ((37, 1, 300, 5), 2048), ((64, 128), 14336),
+                                  ((100, 50), 32768)])
+def test_gemv_group_matches_single(Os, K):
+    """One grouped GEMV launch over matrices sharing a Q8_0 vector equals one
+    launch per matrix, bit for bit, and matches the oracle."""
+    torch = torch_cuda()
+    seed = 7 * sum(Os) + K
+    x = synth.activations(seed, "x", 1, K)
+    xq_ref = oracle.quantize_q8_0(x, synth.gamma(seed, "g", K), 1e-6)
+    xd = to_dev(xq_ref)
+    Wqs = [oracle.quantize_q4_0(synth.weights(seed, f"W{i}", O, K)) for i, O in enumerate(Os)]
+    Wds = [to_dev(w) for w in Wqs]
+    ys = [torch.empty(O, dtype=torch.float32, device="cuda") for O in Os]
+    qdg.q4_0_q8_0_gemv_group(Wds, ys, Os, xd, K)
+    singles = []
+    for Wd, O in zip(Wds, Os):
+        y = torch.empty(O, dtype=torch.float32, device="cuda")
+        qdg.q4_0_q8_0_gemv(Wd, xd, y, O, K)
+        singles.append(y)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    for i, (a, b) in enumerate(zip(ys, singles)):
+        ga, sb = to_host(a), to_host(b)
+        assert np.array_equal(ga.view(np.uint32), sb.view(np.uint32)), f"matrix {i}"
+        _, y64, S = oracle.matvec(Wqs[i], xq_ref, K, threads=8)
+        assert_within_tol(ga[None], y64, S)
