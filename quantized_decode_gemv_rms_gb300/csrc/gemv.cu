@@ -39,9 +39,9 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kDepth = 4;                   // row-segments in flight per warp (consumed two at a time)
+constexpr int kDepth = 3;                   // row-segments in flight per warp (the consume loop is unrolled by 3)
 constexpr int kSegBytes = 1152;             // 32 pairs x 36 bytes
-constexpr int kPartFloats = 2048;           // per-chunk partial sums (rows x segments)
+constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
 constexpr int kFusedMaxK = 16384;           // fused form stages x and gamma in shared memory
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
@@ -115,7 +115,7 @@ struct Args {
 
 template <bool kFused, bool kDebug>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan plan) {
-    __shared__ __align__(16) uint8_t seg_buf[kWarps][2 * kSegBytes];
+    __shared__ __align__(16) uint8_t seg_buf[kWarps][kSegBytes];
     __shared__ float part[kPartFloats];
     __shared__ float norm_part[8];
     // fused form only: x [K] fp32, gamma [K] fp32, Q8_0 activations [K/32 x 34 B]
@@ -312,11 +312,22 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
     }
 
     uint8_t* buf = seg_buf[warp];
-    // The dot of one staged row-segment with this lane's pair.
-    auto dot_pair = [&](const uint8_t* sbuf, int64_t row) -> float {
+    // One row-segment: stage it through shared memory, refill its ring entry
+    // with the segment kDepth ahead, dot it, reduce it.
+    auto consume = [&](int64_t c0, int crows, int ri, SegRegs& entry) {
+        // Store first (this waits for the entry's loads, issued kDepth steps
+        // ago), then reuse the same registers for the segment kDepth ahead.
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+            const int idx = lane + 32 * q;
+            if (idx < seg_vec) *reinterpret_cast<uint4*>(buf + idx * 16) = entry.v[q];
+        }
+        const int ahead = ri + kDepth * plan.nslots;
+        if (ahead < crows) load_seg(c0 + ahead, entry);
+        __syncwarp();
         float acc = 0.0f;
         if (active) {
-            const uint32_t* wp = reinterpret_cast<const uint32_t*>(sbuf + lane * 36);
+            const uint32_t* wp = reinterpret_cast<const uint32_t*>(buf + lane * 36);
             uint32_t w[9];
 #pragma unroll
             for (int i = 0; i < 9; ++i) w[i] = wp[i];
@@ -329,42 +340,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
             acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
             acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
             if (kDebug) {
-                int32_t* d = dbg + row * plan.nb + 2 * p;
+                int32_t* d = dbg + (c0 + ri) * plan.nb + 2 * p;
                 d[0] = ia;
                 d[1] = ib;
             }
         }
-        return acc;
-    };
-    // Two row-segments (rows ri and ri + nslots of the chunk): stage both
-    // through shared memory (this waits for their loads, issued kDepth
-    // segments ago), refill the same ring registers with the segments kDepth
-    // ahead, dot both, and reduce the two sums across the warp together:
-    // half the warp folds row A, the other half row B.
-    auto consume2 = [&](int64_t c0, int crows, int ri, SegRegs& e0, SegRegs& e1) {
-        const int step = plan.nslots;
-        const bool has1 = ri + step < crows;
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-            const int idx = lane + 32 * q;
-            if (idx < seg_vec) {
-                *reinterpret_cast<uint4*>(buf + idx * 16) = e0.v[q];
-                if (has1) *reinterpret_cast<uint4*>(buf + kSegBytes + idx * 16) = e1.v[q];
-            }
-        }
-        if (ri + kDepth * step < crows) load_seg(c0 + ri + kDepth * step, e0);
-        if (ri + (kDepth + 1) * step < crows) load_seg(c0 + ri + (kDepth + 1) * step, e1);
         __syncwarp();
-        const float a0 = dot_pair(buf, c0 + ri);
-        const float a1 = has1 ? dot_pair(buf + kSegBytes, c0 + ri + step) : 0.0f;
-        __syncwarp();
-        const bool upper = (lane & 16) != 0;
-        float keep = upper ? a1 : a0;
-        keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, upper ? a0 : a1, 16));
-#pragma unroll
-        for (int h = 8; h >= 1; h >>= 1) keep = __fadd_rn(keep, __shfl_xor_sync(0xffffffffu, keep, h));
-        if (lane == 0) part[ri * nseg + seg] = keep;
-        if (lane == 16 && has1) part[(ri + step) * nseg + seg] = keep;
+        acc = warp_sum(acc);
+        if (lane == 0) part[ri * nseg + seg] = acc;
     };
 
     for (int64_t c0 = r0; c0 < r1; c0 += plan.rch) {
@@ -373,11 +356,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan pl
             if (c0 != r0) fill(c0, crows);
             // The ring is consumed in a loop unrolled by its depth so every
             // access to it uses a compile-time index: each step then waits only
-            // for its own loads, issued kDepth segments earlier.
+            // for its own loads, issued kDepth steps earlier.
             const int step = plan.nslots;
             for (int ri = slot; ri < crows; ri += kDepth * step) {
-                consume2(c0, crows, ri, pipe[0], pipe[1]);
-                if (ri + 2 * step < crows) consume2(c0, crows, ri + 2 * step, pipe[2], pipe[3]);
+                consume(c0, crows, ri, pipe[0]);
+                if (ri + step < crows) consume(c0, crows, ri + step, pipe[1]);
+                if (ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[2]);
             }
         }
         __syncthreads();
