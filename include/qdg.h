@@ -163,7 +163,13 @@ QDG_API int q4_0_gemv_rmsnorm_group(const void* const* W, float* const* y, const
  *
  * W   [O][K/32] Q4_0, 16-byte aligned.   xq  [N][K/32] Q8_0, 16-byte aligned.
  * y   [N][ldy] fp32: output vector n at y + n*ldy, ldy >= O.
- * K   multiple of 256, 256 <= K <= 65536.   1 <= N <= 8.
+ * K   multiple of 256, 256 <= K <= 32768.   1 <= N <= 8.
+ * The exact per-block integer sums are formed on the warp-level fp16 MMA
+ * (integer codes held exactly in fp16, fp32 accumulation) and scaled per
+ * block in fp32.  For K > 4096 the kernel runs as thread-block clusters of
+ * ceil(K/4096) CTAs that split K and combine their partial sums in a fixed
+ * order through distributed shared memory: no workspace, deterministic
+ * results.
  */
 QDG_API int q4_0_q8_0_gemm_small_n(const void* W, const void* xq, float* y, int64_t ldy,
                            int64_t O, int64_t K, int64_t N, qdg_stream_t stream);

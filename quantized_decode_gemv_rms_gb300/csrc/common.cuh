@@ -94,6 +94,14 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         : "memory");
 }
 
+// The same without a cache policy.
+__device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding grid's memory, and
 // allow the following grid to be scheduled.  No-ops without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -110,6 +118,24 @@ __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int h = 16; h >= 1; h >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, h));
     return v;
+}
+
+// (a0, a1) += (s0, s1) * (v0, v1), one packed fp32x2 fused multiply-add.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float s0, float s1, float v0, float v1) {
+    asm("{\n\t.reg .b64 s, v, a;\n\t"
+        "mov.b64 s, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\tmov.b64 a, {%0, %1};\n\t"
+        "fma.rn.f32x2 a, s, v, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s0), "f"(s1), "f"(v0), "f"(v1));
+}
+
+// (d0, d1) = (a0, a1) * (b0, b1), packed fp32x2.
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
 // ---------------------------------------------------------------- host side
@@ -143,6 +169,34 @@ cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 1;
+    }
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Launch as clusters of `cluster` CTAs along x (1 = no cluster attribute),
+// with the PDL attribute when enabled.
+template <typename Kern, typename... Args>
+cudaError_t launch_cluster(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool allow_pdl,
+                           int cluster, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    cfg.attrs = attr;
+    cfg.numAttrs = 0;
+    if (cluster > 1) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
+    if (allow_pdl && pdl_enabled()) {
+        attr[cfg.numAttrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[cfg.numAttrs].val.programmaticStreamSerializationAllowed = 1;
+        ++cfg.numAttrs;
     }
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }

@@ -5,25 +5,47 @@
 //
 // Still bound by the weight stream, but N dot products per weight make the
 // integer work N times larger than at N = 1, so the exact per-block sums are
-// formed with the integer tensor-core MMA m16n8k32 (u8 weights x s8
-// activations -> s32): one instruction covers 16 rows x 8 columns x one
-// 32-element block.  The Q4_0 nibble order lines up with its A fragment: a
-// lane's 32-bit word c of a block holds elements 4c..4c+3 in its low nibbles
-// and 16+4c..16+4c+3 in its high nibbles, exactly the lane's two A registers
-// for that row.  The "-8" of Q4_0 enters as the accumulator input
-// -8 * sum(q_x), itself one MMA with an all(-8) A operand.
+// formed by the warp-level fp16 MMA m16n8k16 (fp32 accumulation): 16 rows x
+// 8 columns x 16 elements per instruction.  The integer MMA forms of sm_103a
+// issue eight times slower than this one, and dp4a would need 64 operations
+// per weight block at N = 8.  The operands hold integers exactly in fp16:
+//   * low nibbles n become 1024 + n with one LOP3 ((v & 0x000F000F) |
+//     0x64006400); high nibbles stay in place and become 1024 + 16 n
+//     ((v & 0x00F000F0) | 0x64006400), so a 32-bit word of 8 nibbles costs
+//     one shift and four LOP3s;
+//   * the activation codes that meet low nibbles enter as q_x, those that
+//     meet high nibbles as q_x / 16 (exact in fp16); every product is then the
+//     integer (1024 + n) q_x or (64 + n) q_x, and every partial sum an integer
+//     of magnitude below 2^24, exact in fp32;
+//   * sum((n - 8) q_x) = D - 1032 S_lo - 72 S_hi, with S_lo, S_hi the sums of
+//     the block's first and last 16 activation codes, added in fp32 (exact).
+// The order of the 32 elements inside an MMA is free as long as A and B use
+// the same one: a lane's 32-bit word t of a Q4_0 block holds elements
+// 4t..4t+3 (low nibbles) and 16+4t..16+4t+3 (high nibbles); the first MMA of
+// a block takes the low nibbles, the second the high ones, and the lane's
+// activation fragments are built in that order once, at kernel start.
 //
-// Staging: each CTA owns a contiguous row range, processed in tiles of 32
-// rows; a producer warp copies, per stage, the tile's rows for 4 groups of 8
-// blocks plus the N activation chunks of those blocks with 1-D bulk copies
-// (TMA engine) into padded shared-memory rows (row strides = 16 mod 32 bytes,
-// so fragment loads are free of bank conflicts).  Eight consumer warps split
-// the stage's blocks, accumulate fp32 partials per (row, column) and reduce
-// across warps in a fixed order at the end of each tile.
+// Work split: a warp owns a chunk of 8 consecutive blocks of K (256
+// elements) and keeps the activation fragments, scales and corrections of
+// those blocks for all N columns in registers.  The CTA streams its row
+// tiles (16 rows x all of its chunks) through a ring of shared-memory
+// stages, one 3-D tensor copy (TMA) per tile that lands each chunk as its own
+// 16 x 144-byte slab (row stride 144 bytes: conflict-free fragment loads);
+// the last warp done with a stage refills it.  Each warp accumulates
+// d_w * d_x * isum in fp32 for its 16 rows x 8 columns.  A CTA holds up to 16 chunks (K <= 4096); for
+// larger K a thread-block cluster of ceil(K / 4096) CTAs splits K, and the
+// per-chunk partials are combined in a fixed order: first across the CTA's
+// warps in shared memory, then across the cluster's CTAs through distributed
+// shared memory.  No workspace, no atomics: results are deterministic.
+// Every wait is bounded; a timeout sets a flag, the warp stops computing,
+// waits for its copies in flight and leaves with the others.
 #include "common.cuh"
+#include "tma.cuh"
 
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 namespace qdg {
 
@@ -31,253 +53,448 @@ static __device__ unsigned g_flags_small_n;
 
 namespace {
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kTileRows = 32;                 // two 16-row MMA slabs
-constexpr int kGroupsPerStage = 4;            // 4 groups of 8 blocks = 1024 elements of K per stage
-constexpr int kBlocksPerStage = kGroupsPerStage * 8;
-constexpr int kWStride = kGroupsPerStage * 144 + 16;   // 592 = 16 mod 32
-constexpr int kXStride = kBlocksPerStage * 34 + 16;    // 1104 = 16 mod 32
-constexpr int kStageBytes = kTileRows * kWStride + 8 * kXStride;
-constexpr int kStages = 6;
-constexpr int kRedBytes = kConsumerWarps * 2 * 128 * 4;
-constexpr size_t kSmem = static_cast<size_t>(kStages) * kStageBytes + kRedBytes + 2 * kStages * 8 + 16;
-constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
+constexpr int kMaxWarps = 16;
+constexpr int kChunkBlocks = 8;                       // blocks of one row owned by a warp
+constexpr int kChunkBytes = kChunkBlocks * 18;        // 144 bytes, a multiple of 16
+constexpr int kTileRows = 16;                         // rows of one MMA
+constexpr int kUnitBytes = kTileRows * kChunkBytes;   // 2304 bytes per ring slot (18 x 128)
+constexpr int kBatchTilesPerSlot = 8;                 // row tiles per slot and batch of partial sums
+constexpr int kMaxCluster = 8;
+constexpr uint32_t kLoNib = 0x000F000Fu;
+constexpr uint32_t kHiNib = 0x00F000F0u;
+constexpr uint32_t kMagic = 0x64006400u;              // fp16 1024.0 in both halves
 
-static_assert(kWStride % 32 == 16 && kXStride % 32 == 16, "padded strides");
-static_assert(kStageBytes % 16 == 0, "stage alignment");
+static_assert(kChunkBytes % 16 == 0 && kUnitBytes % 128 == 0, "tensor-copy alignment");
 
-__device__ __forceinline__ void mma_u8s8(int& d0, int& d1, int& d2, int& d3, uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1, int c0, int c1, int c2, int c3) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%10,%11,%12,%13};"
-        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(c0), "r"(c1), "r"(c2), "r"(c3));
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Load a float from the shared memory of CTA `rank` of this cluster, at the
+// offset that `p` has in this CTA.
+__device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(p)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
 }
 
-__device__ __forceinline__ void mma_s8s8(int& d0, int& d1, int& d2, int& d3, uint32_t a, uint32_t b0,
-                                         uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%4,%4,%4}, {%5,%6}, "
-        "{%7,%7,%7,%7};"
-        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
-        : "r"(a), "r"(b0), "r"(b1), "r"(0));
+// Bits (0..3, 16..19) -> fp16 pair (1024 + n0, 1024 + n1); bits (4..7, 20..23)
+// -> (1024 + 16 n0, 1024 + 16 n1).
+__device__ __forceinline__ uint32_t lo_pair(uint32_t v) { return (v & kLoNib) | kMagic; }
+__device__ __forceinline__ uint32_t hi_pair(uint32_t v) { return (v & kHiNib) | kMagic; }
+
+// (d0, d1) = (a0, a1) + (b0, b1), packed fp32x2.
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
 
-// 32-bit word starting at a 2-byte aligned shared-memory address.
-__device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    if ((a & 3u) == 0) return *reinterpret_cast<const uint32_t*>(p);
-    const uint32_t lo = *reinterpret_cast<const uint32_t*>(p - 2);
-    const uint32_t hi = *reinterpret_cast<const uint32_t*>(p + 2);
-    return bytes_2_to_5(lo, hi);
+// D = A * B (C = 0), m16n8k16, fp16 operands, fp32 accumulation; then D += A2 * B2.
+__device__ __forceinline__ void hmma2(float& d0, float& d1, float& d2, float& d3, uint32_t a0, uint32_t a1,
+                                      uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1, uint32_t e0, uint32_t e1,
+                                      uint32_t e2, uint32_t e3, uint32_t f0, uint32_t f1) {
+    asm volatile(
+        "{\n\t.reg .f32 z;\n\tmov.f32 z, 0f00000000;\n\t"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {z,z,z,z};\n\t"
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%10,%11,%12,%13}, {%14,%15}, "
+        "{%0,%1,%2,%3};\n\t}"
+        : "=&f"(d0), "=&f"(d1), "=&f"(d2), "=&f"(d3)
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(e0), "r"(e1), "r"(e2), "r"(e3), "r"(f0),
+          "r"(f1));
+}
+
+// Word t of the nibbles of block b in a staged row (row start 16-byte aligned):
+// the block starts at 18b, its nibbles at 18b + 2, so the word is 4-byte
+// aligned for odd b and straddles two aligned words for even b.
+template <int kB>
+__device__ __forceinline__ uint32_t nibble_word(const uint8_t* row, int t) {
+    if (kB & 1) return *reinterpret_cast<const uint32_t*>(row + 18 * kB + 2 + 4 * t);
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(row + 18 * kB + 4 * t);
+    return bytes_2_to_5(p[0], p[1]);
 }
 
 struct Args {
-    const uint8_t* W;
+    CUtensorMap wmap;   // W as [chunk][row][144 bytes]; box = 16 rows x wmax chunks
     const uint8_t* xq;
     float* y;
     int32_t* dbg;
     int64_t ldy;
     int64_t O;
-    int rowbytes;   // K/32 * 18
-    int xrow;       // K/32 * 34
-    int nb;         // K/32
-    int groups;     // K/256
+    int nb;        // K / 32
     int N;
+    int chunks;    // K / 256
+    int csize;     // CTAs per cluster
+    int wmax;      // chunk warps per CTA (largest share of the cluster's CTAs)
+    int nslots;    // row tiles in flight per CTA (warps = wmax * nslots)
+    int bt;        // row tiles per batch of partial sums (a multiple of nslots)
+    int stages;    // tile stages in the ring
+    int part_floats;   // partial-sum area: bt * wmax * 128 floats, and room for the staged activations
 };
 
-template <bool kDebug>
-__global__ void __launch_bounds__(kThreads, 1) small_n_kernel(Args a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    float* red = reinterpret_cast<float*>(smem + static_cast<size_t>(kStages) * kStageBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kStages) * kStageBytes + kRedBytes);
-    uint64_t* empty = full + kStages;
-    // Set by a consumer warp whose wait gave up: the others stop computing but
-    // still reach every tile-end barrier, so no warp is left waiting.
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+// Per lane and block, in registers: fp16 activation fragments of column g.
+struct XBlock {
+    uint32_t b[4];
+};
+// Per warp, block and t, in shared memory (read as one 16-byte vector): the
+// corrections -1032 S_lo - 72 S_hi of columns 2t and 2t + 1, and their fp16
+// scales d_x packed in one word.
+struct XTab {
+    float m0, m1;
+    uint32_t dx;
+    uint32_t pad;
+};
 
+// d = a * b exactly (fp16 operands, fp32 result).
+__device__ __forceinline__ float mul_f16_f32(unsigned short a, unsigned short b) {
+    float d;
+    asm("{\n\t.reg .f16 ha, hb;\n\tmov.b16 ha, %1;\n\tmov.b16 hb, %2;\n\t"
+        "fma.rn.f32.f16 %0, ha, hb, 0f00000000;\n\t}"
+        : "=f"(d)
+        : "h"(a), "h"(b));
+    return d;
+}
+
+template <int kB>
+__device__ __forceinline__ void block_step(const uint8_t* ra, const uint8_t* rb, int t, const XBlock& x,
+                                           const XTab* tab, float (&acc)[4], float (&isum)[4]) {
+    const uint32_t w0 = nibble_word<kB>(ra, t);
+    const uint32_t w1 = nibble_word<kB>(rb, t);
+    const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
+    const unsigned short dw0 = *reinterpret_cast<const unsigned short*>(ra + 18 * kB);
+    const unsigned short dw1 = *reinterpret_cast<const unsigned short*>(rb + 18 * kB);
+    const XTab e = tab[kB * 4 + t];
+    float d0, d1, d2, d3;
+    // first MMA: low nibbles of bytes (0, 2) and (1, 3), rows g and g + 8;
+    // second MMA: high nibbles of the same bytes (x 16), activations / 16
+    hmma2(d0, d1, d2, d3, lo_pair(w0), lo_pair(w1), lo_pair(v0), lo_pair(v1), x.b[0], x.b[1], hi_pair(w0),
+          hi_pair(w1), hi_pair(v0), hi_pair(v1), x.b[2], x.b[3]);
+    fadd2(d0, d1, d0, d1, e.m0, e.m1);   // exact block sums, columns 2t, 2t + 1, row g
+    fadd2(d2, d3, d2, d3, e.m0, e.m1);   // row g + 8
+    const unsigned short dx0 = static_cast<unsigned short>(e.dx), dx1 = static_cast<unsigned short>(e.dx >> 16);
+    // d_w * d_x, exact in fp32
+    const float s0 = mul_f16_f32(dw0, dx0), s1 = mul_f16_f32(dw0, dx1);
+    const float s2 = mul_f16_f32(dw1, dx0), s3 = mul_f16_f32(dw1, dx1);
+    ffma2(acc[0], acc[1], s0, s1, d0, d1);
+    ffma2(acc[2], acc[3], s2, s3, d2, d3);
+    isum[0] = d0;
+    isum[1] = d1;
+    isum[2] = d2;
+    isum[3] = d3;
+}
+
+// fp16 pairs from the int8 codes of bytes (0, 2) or (1, 3) of v: x, or x / 16.
+__device__ __forceinline__ uint32_t act_pair(uint32_t v, uint32_t sel, bool div16) {
+    // (x + 128) as the low byte of an fp16 with exponent 2^10: 1152 + x
+    const uint32_t h = __byte_perm(v ^ 0x80808080u, 0x64646464u, sel);
+    uint32_t r;
+    if (div16)   // (1152 + x) / 16 - 72 = x / 16, one rounding of an exact value
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(h), "r"(0x2C002C00u), "r"(0xD480D480u));
+    else         // (1152 + x) - 1152
+        asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(h), "r"(0xE480E480u));
+    return r;
+}
+
+// Shared memory: [mbarriers][counters][pad], the per-warp tables, then the
+// stage ring, the batch partials and (cluster case) the per-CTA partials.
+constexpr int kMaxStages = 32;
+constexpr int kHeadBytes = 512;
+constexpr int kTabBytes = kMaxWarps * kChunkBlocks * 4 * 16;   // 8 KB
+
+template <bool kDebug, bool kCluster>
+__global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid_constant__ Args a) {
+    extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * a.O / gridDim.x;
-    const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * a.O / gridDim.x;
-    const int nrows = static_cast<int>(r1 - r0);
-    const int ntiles = (nrows + kTileRows - 1) / kTileRows;
-    const int nchunks = (a.groups + kGroupsPerStage - 1) / kGroupsPerStage;
-    const int nst = ntiles * nchunks;
+    const int g = lane >> 2;
+    const int t = lane & 3;
+    const int wmax = a.wmax;
+    const int nslots = a.nslots;
+    const int bt = a.bt;
+    const int S = a.stages;
+    const int stage_bytes = wmax * kUnitBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);                     // [S]
+    int* cnt = reinterpret_cast<int*>(smem + kMaxStages * sizeof(uint64_t)); // [S] consumer arrivals
+    int* issued_sh = cnt + kMaxStages;                                       // tiles issued so far
+    volatile int* abort_sh = issued_sh + 1;                                  // a wait gave up
+    uint64_t* xbar = full + kMaxStages - 1;                                  // activation copies (S < kMaxStages)
+    XTab* tab = reinterpret_cast<XTab*>(smem + kHeadBytes) + warp * kChunkBlocks * 4;   // [8 blocks][4]
+    uint8_t* ring = smem + kHeadBytes + kTabBytes;
+    float* part = reinterpret_cast<float*>(ring + S * stage_bytes);          // [bt][wmax][128]
+    float* loc = part + a.part_floats;                                       // [2][bt * 128], cluster case
 
+    const int csize = kCluster ? a.csize : 1;
+    const int rank = kCluster ? static_cast<int>(cluster_rank()) : 0;
+    const int ncl = static_cast<int>(gridDim.x) / csize;
+    const int cid = static_cast<int>(blockIdx.x) / csize;
+    const int64_t O = a.O;
+    // the cluster's row tiles [tile0, tile0 + ntiles); rows past O read as zero
+    const int64_t tiles = (O + kTileRows - 1) / kTileRows;
+    const int64_t tile0 = static_cast<int64_t>(cid) * tiles / ncl;
+    const int ntiles = static_cast<int>(static_cast<int64_t>(cid + 1) * tiles / ncl - tile0);
+    const int nbatch = (ntiles + bt - 1) / bt;
+
+    // this CTA's chunks of K, and this warp's chunk and row slot
+    const int ch0 = rank * a.chunks / csize;
+    const int cq = (rank + 1) * a.chunks / csize - ch0;
+    const int wl = warp % wmax;
+    const int slot = warp / wmax;
+    const bool worker = wl < cq;
+    const int chunk = ch0 + wl;
+
+    // Tile tau of the cluster's rows goes to stage s = tau % S; one tensor copy
+    // brings the 16 rows x wmax chunks of the CTA (chunk slabs of 16 x 144 B).
+    auto issue = [&](int s, int tau) {
+        mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
+        tma_load_3d(ring + s * stage_bytes, &a.wmap, 0, static_cast<int>((tile0 + tau) * kTileRows), ch0, &full[s]);
+    };
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            cnt[i] = 0;
         }
+        mbar_init(xbar, 1);
+        *abort_sh = 0;
         fence_barrier_init();
-        *abort_flag = 0;
     }
     __syncthreads();
     pdl_trigger();
+    const int n0 = ntiles < S ? ntiles : S;
+    if (threadIdx.x == 0 && n0 > 0) issue(0, 0);   // weights only: before waiting for the preceding grid
     pdl_wait();
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
-        const uint64_t policy = l2_policy_evict_first();
-        bool ok = true;
-        int issued = 0;
-        for (int k = 0; k < nst; ++k) {
-            const int s = k % kStages;
-            if (k >= kStages) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ((k / kStages) - 1) & 1));
-                if (!ok) break;
-            }
-            const int t = k / nchunks;
-            const int ck = k - t * nchunks;
-            const int64_t rt = r0 + static_cast<int64_t>(t) * kTileRows;
-            const int rows = static_cast<int>((r1 - rt) < kTileRows ? (r1 - rt) : kTileRows);
-            const int g0 = ck * kGroupsPerStage;
-            const int vg = (a.groups - g0) < kGroupsPerStage ? (a.groups - g0) : kGroupsPerStage;
-            const uint32_t wbytes = static_cast<uint32_t>(vg) * 144;
-            const uint32_t xbytes = static_cast<uint32_t>(vg) * 272;
-            uint8_t* st = smem + static_cast<size_t>(s) * kStageBytes;
-            if (lane == 0) mbar_arrive_expect_tx(&full[s], rows * wbytes + a.N * xbytes);
-            __syncwarp();
-            for (int i = lane; i < rows + a.N; i += 32) {
-                if (i < rows) {
-                    bulk_g2s(st + i * kWStride, a.W + (rt + i) * a.rowbytes + static_cast<int64_t>(g0) * 144, wbytes,
-                             &full[s], policy);
-                } else {
-                    const int n = i - rows;
-                    bulk_g2s(st + kTileRows * kWStride + n * kXStride,
-                             a.xq + static_cast<int64_t>(n) * a.xrow + static_cast<int64_t>(g0) * 272, xbytes,
-                             &full[s], policy);
+    // ---- the CTA's activation blocks (N rows x cq chunks of 272 bytes) land
+    // in the partial-sum area (sized for 8 rows) with one bulk copy per row, ahead of the rest
+    // of the weight stream; then each lane builds its fragments from there.
+    uint8_t* xsm = reinterpret_cast<uint8_t*>(part);   // [N][wmax * 272 + 16]
+    const int xrow_sm = wmax * kChunkBlocks * 34 + 16;  // padded: the 8 rows of a quad's loads hit 8 banks
+    if (threadIdx.x == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(cq * kChunkBlocks * 34);
+        mbar_arrive_expect_tx(xbar, bytes * static_cast<uint32_t>(a.N));
+        for (int n = 0; n < a.N; ++n)
+            bulk_g2s_plain(xsm + n * xrow_sm,
+                           a.xq + static_cast<int64_t>(n) * a.nb * 34 + static_cast<int64_t>(ch0) * kChunkBlocks * 34,
+                           bytes, xbar);
+        for (int tau = 1; tau < n0; ++tau) issue(tau, tau);
+        *issued_sh = n0;
+    }
+    if (!__all_sync(0xffffffffu, mbar_wait(xbar, 0)) && lane == 0) {
+        atomicOr(&g_flags_small_n, FLAG_TIMEOUT);
+        *abort_sh = 1;
+    }
+    uint32_t xlo[kChunkBlocks], xhi[kChunkBlocks], xd[kChunkBlocks];
+#pragma unroll
+    for (int b = 0; b < kChunkBlocks; ++b) {
+        xlo[b] = xhi[b] = xd[b] = 0;
+        if (worker && g < a.N) {
+            const unsigned short* h =
+                reinterpret_cast<const unsigned short*>(xsm + g * xrow_sm + (wl * kChunkBlocks + b) * 34);
+            xd[b] = h[0];
+            xlo[b] = static_cast<uint32_t>(h[1 + 2 * t]) | (static_cast<uint32_t>(h[2 + 2 * t]) << 16);
+            xhi[b] = static_cast<uint32_t>(h[9 + 2 * t]) | (static_cast<uint32_t>(h[10 + 2 * t]) << 16);
+        }
+    }
+    __syncthreads();   // the activation area becomes the partial-sum area
+    XBlock xs[kChunkBlocks];
+#pragma unroll
+    for (int b = 0; b < kChunkBlocks; ++b) {
+        const uint32_t lo = xlo[b], hi = xhi[b];
+        xs[b].b[0] = act_pair(lo, 0x4240u, false);   // elements 4t, 4t + 2
+        xs[b].b[1] = act_pair(lo, 0x4341u, false);   // elements 4t + 1, 4t + 3
+        xs[b].b[2] = act_pair(hi, 0x4240u, true);    // elements 16 + 4t, 16 + 4t + 2, divided by 16
+        xs[b].b[3] = act_pair(hi, 0x4341u, true);
+        int slo = __dp4a(static_cast<int>(lo), 0x01010101, 0);
+        int shi = __dp4a(static_cast<int>(hi), 0x01010101, 0);
+        slo += __shfl_xor_sync(0xffffffffu, slo, 1);
+        shi += __shfl_xor_sync(0xffffffffu, shi, 1);
+        slo += __shfl_xor_sync(0xffffffffu, slo, 2);
+        shi += __shfl_xor_sync(0xffffffffu, shi, 2);
+        const float mg = static_cast<float>(-1032 * slo - 72 * shi);   // of column g, exact
+        XTab e;
+        e.m0 = __shfl_sync(0xffffffffu, mg, 8 * t);
+        e.m1 = __shfl_sync(0xffffffffu, mg, 8 * t + 4);
+        e.dx = __shfl_sync(0xffffffffu, xd[b], 8 * t) | (__shfl_sync(0xffffffffu, xd[b], 8 * t + 4) << 16);
+        e.pad = 0;
+        if (g == 0) tab[b * 4 + t] = e;
+    }
+    __syncwarp();
+
+    bool ok = true;   // false once a wait gave up: stop computing, keep the barrier schedule
+    int s = slot;     // stage of this warp's next tile, tau % S (slot < nslots <= S)
+    uint32_t ph = 0;  // and its phase parity, (tau / S) & 1
+    for (int beta = 0; beta < nbatch; ++beta) {
+        for (int j = 0; j < bt / nslots; ++j) {
+            const int tb = j * nslots + slot;          // tile within the batch
+            const int tau = beta * bt + tb;            // tile within the cluster's rows
+            if (tau >= ntiles) break;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (worker && ok) {
+                ok = *abort_sh == 0 && __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
+                if (!ok && lane == 0) {
+                    atomicOr(&g_flags_small_n, FLAG_TIMEOUT);
+                    *abort_sh = 1;
                 }
             }
-            __syncwarp();
-            issued = k + 1;
-        }
-        if (!ok) {
-            if (lane == 0) atomicOr(&g_flags_small_n, FLAG_TIMEOUT);
-            for (int k = (issued - kStages > 0 ? issued - kStages : 0); k < issued; ++k)
-                mbar_wait(&full[k % kStages], (k / kStages) & 1);
-        }
-        return;
-    }
-
-    // ---------------------------------------------------------- consumers
-    const int cw = warp - 1;
-    const int g = lane >> 2;
-    const int c = lane & 3;
-    const bool colg = g < a.N;
-    const bool col0 = 2 * c < a.N;
-    const bool col1 = 2 * c + 1 < a.N;
-    float acc[2][4];
-#pragma unroll
-    for (int sl = 0; sl < 2; ++sl)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[sl][i] = 0.0f;
-
-    for (int k = 0; k < nst; ++k) {
-        const int s = k % kStages;
-        bool ok = *abort_flag == 0;
-        if (ok) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&full[s], (k / kStages) & 1));
-            if (!ok && lane == 0) {
-                atomicOr(&g_flags_small_n, FLAG_TIMEOUT);
-                *abort_flag = 1;
-            }
-        }
-        const int t = k / nchunks;
-        const int ck = k - t * nchunks;
-        const int64_t rt = r0 + static_cast<int64_t>(t) * kTileRows;
-        const int g0 = ck * kGroupsPerStage;
-        const int vg = (a.groups - g0) < kGroupsPerStage ? (a.groups - g0) : kGroupsPerStage;
-        const int vblocks = ok ? vg * 8 : 0;
-        const uint8_t* st = smem + static_cast<size_t>(s) * kStageBytes;
-        const uint8_t* xs = st + kTileRows * kWStride;
-        for (int bl = cw; bl < vblocks; bl += kConsumerWarps) {
-            uint32_t b0 = 0, b1 = 0;
-            if (colg) {
-                const uint8_t* xb = xs + g * kXStride + bl * 34;
-                b0 = lds_u32_a2(xb + 2 + 4 * c);
-                b1 = lds_u32_a2(xb + 18 + 4 * c);
-            }
-            const float dx0 = col0 ? half_bits_to_float(*reinterpret_cast<const unsigned short*>(
-                                         xs + (2 * c) * kXStride + bl * 34))
-                                   : 0.0f;
-            const float dx1 = col1 ? half_bits_to_float(*reinterpret_cast<const unsigned short*>(
-                                         xs + (2 * c + 1) * kXStride + bl * 34))
-                                   : 0.0f;
-            int m0, m1, m2, m3;   // -8 * sum(q_x) for columns 2c, 2c+1
-            mma_s8s8(m0, m1, m2, m3, 0xF8F8F8F8u, b0, b1);
-#pragma unroll
-            for (int sl = 0; sl < 2; ++sl) {
-                const uint8_t* wr0 = st + (sl * 16 + g) * kWStride + bl * 18;
-                const uint8_t* wr1 = wr0 + 8 * kWStride;
-                const uint32_t w0 = lds_u32_a2(wr0 + 2 + 4 * c);
-                const uint32_t w1 = lds_u32_a2(wr1 + 2 + 4 * c);
-                const float dw0 = half_bits_to_float(*reinterpret_cast<const unsigned short*>(wr0));
-                const float dw1 = half_bits_to_float(*reinterpret_cast<const unsigned short*>(wr1));
-                int d0, d1, d2, d3;
-                mma_u8s8(d0, d1, d2, d3, w0 & kNibbles, w1 & kNibbles, (w0 >> 4) & kNibbles, (w1 >> 4) & kNibbles,
-                         b0, b1, m0, m1, m0, m1);
-                acc[sl][0] = __fmaf_rn(__fmul_rn(dw0, dx0), static_cast<float>(d0), acc[sl][0]);
-                acc[sl][1] = __fmaf_rn(__fmul_rn(dw0, dx1), static_cast<float>(d1), acc[sl][1]);
-                acc[sl][2] = __fmaf_rn(__fmul_rn(dw1, dx0), static_cast<float>(d2), acc[sl][2]);
-                acc[sl][3] = __fmaf_rn(__fmul_rn(dw1, dx1), static_cast<float>(d3), acc[sl][3]);
+            if (worker && ok) {
+                const uint8_t* ra = ring + s * stage_bytes + wl * kUnitBytes + g * kChunkBytes;
+                const uint8_t* rb = ra + 8 * kChunkBytes;
+                float is[kChunkBlocks][4];
+                block_step<0>(ra, rb, t, xs[0], tab, acc, is[0]);
+                block_step<1>(ra, rb, t, xs[1], tab, acc, is[1]);
+                block_step<2>(ra, rb, t, xs[2], tab, acc, is[2]);
+                block_step<3>(ra, rb, t, xs[3], tab, acc, is[3]);
+                block_step<4>(ra, rb, t, xs[4], tab, acc, is[4]);
+                block_step<5>(ra, rb, t, xs[5], tab, acc, is[5]);
+                block_step<6>(ra, rb, t, xs[6], tab, acc, is[6]);
+                block_step<7>(ra, rb, t, xs[7], tab, acc, is[7]);
                 if (kDebug) {
-                    const int64_t row0 = rt + sl * 16 + g;
-                    const int64_t b = static_cast<int64_t>(g0) * 8 + bl;
-                    if (row0 < r1) {
-                        if (col0) a.dbg[((2 * c) * a.O + row0) * a.nb + b] = d0;
-                        if (col1) a.dbg[((2 * c + 1) * a.O + row0) * a.nb + b] = d1;
-                    }
-                    if (row0 + 8 < r1) {
-                        if (col0) a.dbg[((2 * c) * a.O + row0 + 8) * a.nb + b] = d2;
-                        if (col1) a.dbg[((2 * c + 1) * a.O + row0 + 8) * a.nb + b] = d3;
+                    const int64_t rt = (tile0 + tau) * kTileRows;
+#pragma unroll
+                    for (int b = 0; b < kChunkBlocks; ++b)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int64_t row = rt + g + 8 * (i >> 1);
+                            const int col = 2 * t + (i & 1);
+                            if (row < O && col < a.N)
+                                a.dbg[(col * O + row) * a.nb + chunk * kChunkBlocks + b] = static_cast<int32_t>(is[b][i]);
+                        }
+                }
+                // The warp is done with its slab of the stage: every value read
+                // from it was consumed by the MMAs above.  The last of the
+                // CTA's cq warps refills the stage with tile tau + S.
+                __syncwarp();
+                if (lane == 0 && atomicAdd(&cnt[s], 1) == cq - 1) {
+                    cnt[s] = 0;
+                    if (tau + S < ntiles && *abort_sh == 0) {
+                        issue(s, tau + S);
+                        atomicMax(issued_sh, tau + S + 1);
                     }
                 }
+                __syncwarp();
+            }
+            if (worker)
+                *reinterpret_cast<float4*>(part + (tb * wmax + wl) * 128 + lane * 4) =
+                    make_float4(acc[0], acc[1], acc[2], acc[3]);
+            s += nslots;
+            if (s >= S) {
+                s -= S;
+                ph ^= 1u;
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-
-        if (ck == nchunks - 1) {
-            // End of a row tile: fixed-order reduction across the consumer warps.
-            float* rw = red + cw * 256;
-#pragma unroll
-            for (int sl = 0; sl < 2; ++sl)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    rw[sl * 128 + lane * 4 + i] = acc[sl][i];
-                    acc[sl][i] = 0.0f;
-                }
-            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
-            const int e = threadIdx.x - 32;             // 0..255
-            const int sl = e >> 7;
-            const int ln = (e >> 2) & 31;
-            const int i = e & 3;
-            const int row = sl * 16 + (ln >> 2) + 8 * (i >> 1);
-            const int col = 2 * (ln & 3) + (i & 1);
-            float v = red[e];
-#pragma unroll
-            for (int w = 1; w < kConsumerWarps; ++w) v = __fadd_rn(v, red[w * 256 + e]);
-            if (a.y != nullptr && rt + row < r1 && col < a.N) a.y[col * a.ldy + rt + row] = v;
-            asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        __syncthreads();
+        // ---- batch reduction.  Index e of a tile's 128 partials = lane * 4 + i
+        // of the writing lane: row g + 8 (i >> 1), column 2t + (i & 1).
+        const int tiles_here = min(bt, ntiles - beta * bt);
+        const int64_t rbase = (tile0 + static_cast<int64_t>(beta) * bt) * kTileRows;
+        if (kDebug) {
+            __syncthreads();
+        } else if (!kCluster) {
+            for (int e = threadIdx.x; e < tiles_here * 128; e += blockDim.x) {
+                const int tb = e >> 7, l = (e >> 2) & 31, i = e & 3;
+                const int col = 2 * (l & 3) + (i & 1);
+                const int64_t row = rbase + tb * kTileRows + (l >> 2) + 8 * (i >> 1);
+                if (col >= a.N || row >= O) continue;
+                const float* src = part + tb * wmax * 128 + (e & 127);
+                float v = src[0];
+                for (int w = 1; w < cq; ++w) v = __fadd_rn(v, src[w * 128]);
+                a.y[col * a.ldy + row] = v;
+            }
+            __syncthreads();   // partials read before the next batch overwrites them
+        } else {
+            // clusters imply one slot
+            float* lb = loc + (beta & 1) * bt * 128;
+            for (int e = threadIdx.x; e < tiles_here * 128; e += blockDim.x) {
+                const float* src = part + (e >> 7) * wmax * 128 + (e & 127);
+                float v = src[0];
+                for (int w = 1; w < cq; ++w) v = __fadd_rn(v, src[w * 128]);
+                lb[e] = v;
+            }
+            __syncwarp();
+            cluster_sync();
+            const int per = (tiles_here * 128 + csize - 1) / csize;
+            const int e0 = rank * per;
+            const int e1 = min(tiles_here * 128, e0 + per);
+            for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += blockDim.x) {
+                const int tb = e >> 7, l = (e >> 2) & 31, i = e & 3;
+                const int col = 2 * (l & 3) + (i & 1);
+                const int64_t row = rbase + tb * kTileRows + (l >> 2) + 8 * (i >> 1);
+                if (col >= a.N || row >= O) continue;
+                float v = ld_cluster(lb + e, 0);
+                for (int q = 1; q < csize; ++q) v = __fadd_rn(v, ld_cluster(lb + e, static_cast<uint32_t>(q)));
+                a.y[col * a.ldy + row] = v;
+            }
         }
     }
+    // After a timeout: wait (bounded) for the copies of the last S tiles issued.
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_sh != 0) {
+        mbar_wait(xbar, 0);
+        const int n = *reinterpret_cast<volatile int*>(issued_sh);
+        for (int tau = (n - S > 0 ? n - S : 0); tau < n; ++tau) mbar_wait(&full[tau % S], (tau / S) & 1);
+    }
+    __syncwarp();
+    // No CTA leaves while the others of its cluster may still read its shared memory.
+    if (kCluster) cluster_sync();
 }
 
-std::mutex g_attr_mutex;
-bool g_attr_done[2] = {false, false};
+std::mutex g_mutex;
+bool g_attr_done[4] = {false, false, false, false};
+std::map<std::tuple<bool, int, int, size_t>, int> g_max_clusters;
 
-template <bool kDebug>
-cudaError_t ensure_smem() {
-    std::lock_guard<std::mutex> lock(g_attr_mutex);
-    if (g_attr_done[kDebug]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(small_n_kernel<kDebug>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmem));
-    if (e == cudaSuccess) g_attr_done[kDebug] = true;
-    return e;
+size_t smem_bytes(const Args& a) {
+    const size_t stage = static_cast<size_t>(a.wmax) * kUnitBytes;
+    return kHeadBytes + kTabBytes + a.stages * stage + static_cast<size_t>(a.part_floats) * sizeof(float) +
+           (a.csize > 1 ? 2 * static_cast<size_t>(a.bt) * 128 * sizeof(float) : 0);
+}
+
+template <bool kDebug, bool kCluster>
+int max_clusters(int csize, int warps, size_t smem, int sms) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    bool& done = g_attr_done[2 * kDebug + kCluster];
+    if (!done) {
+        if (cudaFuncSetAttribute(small_n_kernel<kDebug, kCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(device_info().smem_optin)) != cudaSuccess)
+            return -1;
+        done = true;
+    }
+    if (!kCluster) return sms;
+    const auto key = std::make_tuple(kDebug, csize, warps, smem);
+    auto it = g_max_clusters.find(key);
+    if (it != g_max_clusters.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(csize * (sms / csize)));
+    cfg.blockDim = dim3(static_cast<unsigned>(warps * 32));
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, small_n_kernel<kDebug, kCluster>, &cfg) != cudaSuccess || n < 1)
+        return -1;
+    g_max_clusters[key] = n;
+    return n;
+}
+
+template <bool kDebug, bool kCluster>
+cudaError_t launch_small_n(const Args& a, int warps, size_t smem, int sms, int64_t O, cudaStream_t stream) {
+    const int maxcl = max_clusters<kDebug, kCluster>(a.csize, warps, smem, sms);
+    if (maxcl < 1) return cudaErrorInvalidConfiguration;
+    const int64_t tiles = (O + kTileRows - 1) / kTileRows;
+    const int ncl = static_cast<int>(std::min<int64_t>(maxcl, tiles));
+    return launch_cluster(small_n_kernel<kDebug, kCluster>, dim3(static_cast<unsigned>(ncl * a.csize)),
+                          dim3(static_cast<unsigned>(warps * 32)), smem, stream, !kDebug, kCluster ? a.csize : 1, a);
 }
 
 }  // namespace
@@ -287,32 +504,44 @@ int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t
     if (!W || !xq || (!y && !dbg)) return QDG_EINVAL;
     if (O <= 0 || K <= 0 || N < 1 || N > 8) return QDG_EINVAL;
     if (!dbg && ldy < O) return QDG_EINVAL;
-    if (K % 256 != 0 || K > 65536 || O >= (int64_t(1) << 31)) return QDG_ESHAPE;
+    if (K % 256 != 0 || K > 32768 || O >= (int64_t(1) << 31) - kTileRows) return QDG_ESHAPE;
     if (!aligned(W, 16) || !aligned(xq, 16) || (y && !aligned(y, 4))) return QDG_EALIGN;
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
-    if (kSmem > dev.smem_optin) return QDG_ECUDA;
     Args a;
-    a.W = static_cast<const uint8_t*>(W);
     a.xq = static_cast<const uint8_t*>(xq);
     a.y = y;
     a.dbg = dbg;
     a.ldy = ldy;
     a.O = O;
     a.nb = static_cast<int>(K / 32);
-    a.rowbytes = a.nb * 18;
-    a.xrow = a.nb * 34;
-    a.groups = static_cast<int>(K / 256);
     a.N = static_cast<int>(N);
-    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
+    a.chunks = static_cast<int>(K / 256);
+    a.csize = (a.chunks + kMaxWarps - 1) / kMaxWarps;
+    a.wmax = (a.chunks + a.csize - 1) / a.csize;
+    a.nslots = kMaxWarps / a.wmax;
+    // kBatchTilesPerSlot row tiles per slot and batch of partial sums; the rest of shared
+    // memory holds as many tile stages as fit (at least two).
+    a.bt = kBatchTilesPerSlot * a.nslots;
+    // the partial-sum area first receives the activations: N x wmax chunks x 272 bytes
+    a.part_floats = std::max(a.bt * a.wmax * 128, 8 * (a.wmax * kChunkBlocks * 34 + 16) / 4);
+    if (a.csize > kMaxCluster) return QDG_ECUDA;
+    a.stages = 0;
+    const size_t fixed = smem_bytes(a);
+    const size_t stage = static_cast<size_t>(a.wmax) * kUnitBytes;
+    if (dev.smem_optin < fixed + 2 * stage) return QDG_ECUDA;
+    a.stages = static_cast<int>(std::min<size_t>(kMaxStages - 1, (dev.smem_optin - fixed) / stage));
+    const int warps = a.wmax * a.nslots;
+    const size_t smem = smem_bytes(a);
+    if (!encode_row_segments(&a.wmap, W, static_cast<int64_t>(a.nb) * 18, O, kChunkBytes, kTileRows, a.wmax))
+        return QDG_ECUDA;
     cudaError_t e;
-    if (dbg) {
-        e = ensure_smem<true>();
-        if (e == cudaSuccess) e = launch(small_n_kernel<true>, dim3(grid), dim3(kThreads), kSmem, stream, false, a);
-    } else {
-        e = ensure_smem<false>();
-        if (e == cudaSuccess) e = launch(small_n_kernel<false>, dim3(grid), dim3(kThreads), kSmem, stream, true, a);
-    }
+    if (dbg)
+        e = a.csize > 1 ? launch_small_n<true, true>(a, warps, smem, dev.sms, O, stream)
+                        : launch_small_n<true, false>(a, warps, smem, dev.sms, O, stream);
+    else
+        e = a.csize > 1 ? launch_small_n<false, true>(a, warps, smem, dev.sms, O, stream)
+                        : launch_small_n<false, false>(a, warps, smem, dev.sms, O, stream);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(2);
     return QDG_OK;

@@ -27,6 +27,7 @@
 // Every wait is bounded; a timeout sets a flag, the CTA stops working,
 // waits for its copies and MMAs in flight, frees tensor memory and exits.
 #include "common.cuh"
+#include "tma.cuh"
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -107,32 +108,7 @@ __device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
     return d;
 }
 
-// 2-D tiled tensor copy global -> shared (TMA), completion counted on bar.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
-            "r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
 
-// (a0, a1) += (s0, s1) * (v0, v1), one packed fp32x2 fused multiply-add.
-__device__ __forceinline__ void ffma2(float& a0, float& a1, float s0, float s1, float v0, float v1) {
-    asm("{\n\t.reg .b64 s, v, a;\n\t"
-        "mov.b64 s, {%2, %3};\n\tmov.b64 v, {%4, %5};\n\tmov.b64 a, {%0, %1};\n\t"
-        "fma.rn.f32x2 a, s, v, a;\n\tmov.b64 {%0, %1}, a;\n\t}"
-        : "+f"(a0), "+f"(a1)
-        : "f"(s0), "f"(s1), "f"(v0), "f"(v1));
-}
-
-// (d0, d1) = (a0, a1) * (b0, b1), packed fp32x2.
-__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 a, b, d;\n\t"
-        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(d0), "=f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
 
 // The 4-byte word starting at byte offset `off` (even, compile-time) of w[].
 template <int off>
@@ -469,36 +445,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
 std::mutex g_attr_mutex;
 bool g_attr_done[2] = {false, false};
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-        cudaGetLastError();
-    });
-    return fn;
-}
-
-// Rank-2 map over a row-major byte matrix read in boxes of box_bytes x 128 rows.
-bool encode_rows(CUtensorMap* map, const void* base, int64_t row_bytes, int64_t rows, int box_bytes,
-                 bool u16) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    const int esz = u16 ? 2 : 1;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(row_bytes / esz), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(row_bytes)};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_bytes / esz), 128u};
-    const cuuint32_t estr[2] = {1u, 1u};
-    return enc(map, u16 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base),
-               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <bool kDebug>
 cudaError_t ensure_smem() {
     std::lock_guard<std::mutex> lock(g_attr_mutex);
@@ -534,8 +480,8 @@ int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O,
     a.xrow = a.nb * 34;
     a.mtiles = static_cast<int>((O + BM - 1) / BM);
     a.ntiles = static_cast<int>((T + BN - 1) / BN);
-    if (!encode_rows(&a.wmap, W, a.rowbytes, O, CHUNK * 18, false) ||
-        !encode_rows(&a.xmap, xq, a.xrow, T, CHUNK * 34, true))
+    if (!encode_rows(&a.wmap, W, a.rowbytes, O, CHUNK * 18, 128, false) ||
+        !encode_rows(&a.xmap, xq, a.xrow, T, CHUNK * 34, 128, true))
         return QDG_ECUDA;
     const int64_t tiles = static_cast<int64_t>(a.mtiles) * a.ntiles;
     if (tiles > (1 << 30)) return QDG_ESHAPE;

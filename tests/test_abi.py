@@ -121,6 +121,7 @@ def test_small_n_host_validation(L):
     assert f(A16, A16, None, 8, 8, 256, 2, None) == -1
     assert f(A16, A16, A16, 8, 8, 384, 2, None) == -3      # K % 256
     assert f(A16, A2, A16, 8, 8, 256, 2, None) == -2       # xq must be 16-byte aligned
+    assert f(A16, A16, A16, 8, 8, 32768 + 256, 2, None) == -3   # K beyond the maximum
 
 
 def test_gemm_host_validation(L):

@@ -104,7 +104,11 @@ def test_gemv_special_blocks():
     assert y[1] == 0.0
 
 
-SMALLN_SHAPES = [(256, 256), (33, 512), (100, 4096), (1000, 2048), (4096, 14336), (14336, 4096)]
+# Covers one CTA per row range with 16 row slots (K = 256), 2 slots (K = 2048),
+# one slot (K = 4096), and clusters of 2 (K = 4352 split 8 + 9 chunks, 6144,
+# 8192), 4 (K = 14336) and 8 CTAs (K = 32768); ragged row tiles throughout.
+SMALLN_SHAPES = [(256, 256), (2500, 256), (33, 512), (100, 4096), (1000, 2048), (17, 4352), (300, 6144),
+                 (1, 8192), (4096, 14336), (14336, 4096), (40, 32768)]
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8])
@@ -125,6 +129,41 @@ def test_small_n_output_within_tolerance(O, K, N):
     y = gpu_small_n(Wq, xq, O, K, N, ldy=O + 5)
     _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
     assert_within_tol(y if rows is None else y[:, rows], y64, S)
+
+
+def _q8_blocks(codes, d):
+    """Q8_0 rows from int8 codes [N][K] and one fp16 scale per row."""
+    N, K = codes.shape
+    out = np.zeros((N, K // 32, 34), dtype=np.uint8)
+    out[:, :, 0:2] = np.array([np.float16(v) for v in d], dtype=np.float16).view(np.uint8).reshape(N, 1, 2)
+    out[:, :, 2:] = codes.reshape(N, K // 32, 32).astype(np.int8).view(np.uint8)
+    return out.reshape(N, -1)
+
+
+@pytest.mark.parametrize("K", [4096, 8192])
+def test_small_n_extreme_codes(K):
+    """Largest block sums the formats allow (|q_x| = 127 against nibbles 0
+    and 15), mixed with zero blocks and random ones, in every column."""
+    O, N = 48, 8
+    rng = np.random.default_rng(K)
+    W = np.zeros((O, K // 32, 18), dtype=np.uint8)
+    W[:, :, 0:2] = np.array([0.125], dtype=np.float16).view(np.uint8)
+    patterns = [0x00, 0xFF, 0x88, 0x0F, 0xF0, None]
+    for r in range(O):
+        p = patterns[r % len(patterns)]
+        W[r, :, 2:] = rng.integers(0, 256, (K // 32, 16)) if p is None else p
+    W = W.reshape(O, -1)
+    codes = np.empty((N, K), dtype=np.int64)
+    codes[0], codes[1] = 127, -127
+    codes[2] = np.where(np.arange(K) % 2 == 0, 127, -127)
+    codes[3] = 0
+    codes[4:] = rng.integers(-127, 128, (N - 4, K))
+    xq = _q8_blocks(codes, [0.5, 0.25, 1.0, 2.0, 0.03125, 1.5, 0.75, 3.0])
+    got = gpu_block_sums(W, xq, O, K, N, 1)
+    assert np.array_equal(got, oracle.block_sums(W, xq, K))
+    y = gpu_small_n(W, xq, O, K, N)
+    _, y64, S = oracle.matvec(W, xq, K)
+    assert_within_tol(y, y64, S)
 
 
 def test_small_n_one_column_matches_gemv_tolerance():
