@@ -594,6 +594,30 @@ def bench_extras(args, device):
         torch.cuda.synchronize()
         return float(np.median([a.elapsed_time(b) for a, b in evs])) * 1e3
 
+    side = torch.cuda.Stream(device)
+
+    def timed_graph(fn, count, replays=3):
+        """Per-call time from a CUDA graph of `count` back-to-back calls
+        fn(0..count-1) (PDL as configured), replayed `replays` times."""
+        for i in range(count):
+            fn(i)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(side):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=side):
+                for i in range(count):
+                    fn(i)
+            gr.replay()
+            side.synchronize()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(side)
+            for _ in range(replays):
+                gr.replay()
+            a1.record(side)
+            side.synchronize()
+        return a0.elapsed_time(a1) * 1e3 / (replays * count)
+
     def make_w(seed, name, O, K):
         Wq = torch.empty(qdg.q4_0_nbytes(O, K), dtype=torch.uint8, device=device)
         for r in range(0, O, 8192):
@@ -613,11 +637,12 @@ def bench_extras(args, device):
             xq = torch.empty(qdg.q8_0_nbytes(N, K), dtype=torch.uint8, device=device)
             qdg.qnorm_quantize_q8_0(x, g, 1e-6, xq)
             y = torch.empty((N, O), dtype=torch.float32, device=device)
-            us = timed(lambda i: qdg.q4_0_q8_0_gemm_small_n(Ws[i % copies], xq, y, O, O, K, N), 60)
+            us = timed_graph(lambda i: qdg.q4_0_q8_0_gemm_small_n(Ws[i % copies], xq, y, O, O, K, N), copies)
             nbytes = workloads.gemv_algorithmic_bytes(O, K, N)
             res[f"N{N}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
                             "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
-        out["small_n"][f"{O}x{K}"] = dict(res, weight_copies=copies)
+        out["small_n"][f"{O}x{K}"] = dict(res, weight_copies=copies,
+                                          timing="graph of back-to-back launches over the weight copies")
         del Ws, Wq
         torch.cuda.empty_cache()
     for (O, K, T) in (workloads.PREFILL_SHAPES if args.only in (None, "prefill") else ()):

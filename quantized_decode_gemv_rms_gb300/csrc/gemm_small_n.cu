@@ -268,12 +268,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
     __syncthreads();
     pdl_trigger();
     const int n0 = ntiles < S ? ntiles : S;
-    if (threadIdx.x == 0 && n0 > 0) issue(0, 0);   // weights only: before waiting for the preceding grid
     pdl_wait();
 
     // ---- the CTA's activation blocks (N rows x cq chunks of 272 bytes) land
-    // in the partial-sum area (sized for 8 rows) with one bulk copy per row, ahead of the rest
-    // of the weight stream; then each lane builds its fragments from there.
+    // in the partial-sum area (sized for 8 rows) with one bulk copy per row,
+    // issued before the weight tiles so that they do not queue behind them;
+    // then each lane builds its fragments from there.
     uint8_t* xsm = reinterpret_cast<uint8_t*>(part);   // [N][wmax * 272 + 16]
     const int xrow_sm = wmax * kChunkBlocks * 34 + 16;  // padded: the 8 rows of a quad's loads hit 8 banks
     if (threadIdx.x == 0) {
@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
             bulk_g2s_plain(xsm + n * xrow_sm,
                            a.xq + static_cast<int64_t>(n) * a.nb * 34 + static_cast<int64_t>(ch0) * kChunkBlocks * 34,
                            bytes, xbar);
-        for (int tau = 1; tau < n0; ++tau) issue(tau, tau);
+        for (int tau = 0; tau < n0; ++tau) issue(tau, tau);
         *issued_sh = n0;
     }
     if (!__all_sync(0xffffffffu, mbar_wait(xbar, 0)) && lane == 0) {
