@@ -651,11 +651,12 @@ def bench_extras(args, device):
         xq = torch.empty(qdg.q8_0_nbytes(T, K), dtype=torch.uint8, device=device)
         qdg.qnorm_quantize_q8_0(x, None, 0.0, xq)
         y = torch.empty((T, O), dtype=torch.float32, device=device)
-        us = timed(lambda i: qdg.q4_0_q8_0_gemm(Wq, xq, y, O, O, K, T), 30)
+        ws = torch.empty(qdg.q4_0_q8_0_gemm_workspace_bytes(K, T), dtype=torch.uint8, device=device)
+        us = timed(lambda i: qdg.q4_0_q8_0_gemm(Wq, xq, y, O, O, K, T, ws), 30)
         tflops = 2.0 * O * K * T / (us * 1e-6) / 1e12
         out["prefill"][f"{O}x{K}x{T}"] = {"us": round(us, 2), "tflops": round(tflops, 1),
                                           "frac_fp16_peak": round(tflops / peaks["bf16_tflops"], 4)}
-        del Wq, x, xq, y
+        del Wq, x, xq, y, ws
         torch.cuda.empty_cache()
     out["peak_note"] = ("small-N against the measured HBM copy bandwidth; prefill against the measured dense "
                         "bf16 burst peak (the fp16 tensor rate is the same nominal 2.25 PFLOP/s)")

@@ -182,14 +182,30 @@ QDG_API int q4_0_q8_0_gemm_small_n(const void* W, const void* xq, float* y, int6
  * W   [O][K/32] Q4_0, 16-byte aligned.   xq  [T][K/32] Q8_0, 16-byte aligned.
  * y   [T][ldy] fp32: the output for token t at y + t*ldy, ldy >= O.
  * K   multiple of 256, 256 <= K <= 65536.   1 <= O, T <= 2^30.
- * The exact per-block integer sums are formed on the fifth-generation tensor
- * cores (tcgen05.mma, fp16 operands holding the integer codes exactly, fp32
- * accumulation in tensor memory) and scaled per block on the CUDA cores.
- * Needs no workspace; every tile is owned by one CTA, so results are
+ * workspace: device memory of at least q4_0_q8_0_gemm_workspace_bytes(K, T)
+ *   bytes, 16-byte aligned, owned by the caller; contents need no
+ *   initialisation and are overwritten.  Two calls that overlap on the GPU
+ *   must not share a workspace.
+ * Two kernels: the first converts each activation block once into the
+ * tensor-core operand form (fp16 codes, fp32 scale) in the workspace; the
+ * second forms the exact per-block integer sums on the fifth-generation
+ * tensor cores (tcgen05.mma, fp16 operands holding the integer codes
+ * exactly, fp32 accumulation in tensor memory) and scales them per block on
+ * the CUDA cores.  Every output tile is owned by one CTA, so results are
  * deterministic.
+ * Errors: QDG_EINVAL (null pointer, sizes, workspace too small), QDG_ESHAPE,
+ * QDG_EALIGN, QDG_ECUDA (launch).
  */
 QDG_API int q4_0_q8_0_gemm(const void* W, const void* xq, float* y, int64_t ldy,
-                           int64_t O, int64_t K, int64_t T, qdg_stream_t stream);
+                           int64_t O, int64_t K, int64_t T, void* workspace,
+                           int64_t workspace_bytes, qdg_stream_t stream);
+
+/*
+ * q4_0_q8_0_gemm_workspace_bytes -- workspace size for q4_0_q8_0_gemm:
+ * ceil(T/128) * (K/32) * 8704 bytes (one converted activation record per
+ * 128-token tile and block).  Negative status for invalid K or T.
+ */
+QDG_API int64_t q4_0_q8_0_gemm_workspace_bytes(int64_t K, int64_t T);
 
 /*
  * quantize_q4_0 -- weight preparation: fp32 [O][ldw] -> Q4_0 [O][K/32].

@@ -132,8 +132,17 @@ extern "C" int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum
             return gemv_launch(W, xq, nullptr, O, K, s, isum);
         case 1:
             return small_n_launch(W, xq, nullptr, O, O, K, N, s, isum);
-        case 2:
-            return gemm_launch(W, xq, nullptr, O, O, K, N, s, isum);
+        case 2: {
+            // test hook: its own workspace, released after the launches complete
+            const int64_t bytes = gemm_workspace_bytes(K, N);
+            if (bytes < 0) return static_cast<int>(bytes);
+            void* ws = nullptr;
+            if (cudaMalloc(&ws, static_cast<size_t>(bytes)) != cudaSuccess) return QDG_ECUDA;
+            int rc = gemm_launch(W, xq, nullptr, O, O, K, N, ws, bytes, s, isum);
+            if (cudaStreamSynchronize(s) != cudaSuccess && rc == QDG_OK) rc = QDG_ECUDA;
+            cudaFree(ws);
+            return rc;
+        }
         default:
             return QDG_EINVAL;
     }

@@ -59,6 +59,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may stay suspended (issuing nothing) for
+// up to kSuspendNs while the phase is incomplete; it resumes as soon as the
+// phase completes.
+constexpr uint32_t kSuspendNs = 1000000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -66,13 +82,14 @@ __device__ __forceinline__ uint64_t global_ns() {
 }
 
 // Bounded wait for the phase of `parity` to complete.  False = gave up.
+// Each try suspends the thread in hardware until the phase completes (or up
+// to kSuspendNs), so waiting warps take no issue slots from working ones.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1; i < kSpinLimit; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 15u) == 0 && global_ns() - t0 > kWaitNs) return false;
-        if (i >= 32) __nanosleep(128);
+        if (mbar_try_wait_suspend(bar, parity)) return true;
+        if (global_ns() - t0 > kWaitNs) return false;
     }
     return false;
 }
@@ -207,8 +224,9 @@ int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, c
                 int32_t* dbg);
 int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t N,
                    cudaStream_t stream, int32_t* dbg);
-int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t T,
-                cudaStream_t stream, int32_t* dbg);
+int64_t gemm_workspace_bytes(int64_t K, int64_t T);
+int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t T, void* ws,
+                int64_t ws_bytes, cudaStream_t stream, int32_t* dbg);
 
 // Per-translation-unit device flags: read and clear (synchronises stream).
 unsigned flags_read_clear_quantize(cudaStream_t stream);

@@ -61,8 +61,8 @@ def lib() -> ctypes.CDLL:
                 "qdg_debug_block_sums": ([p, p, p, i64, i64, i64, i32, p], i32),
                 "qdg_debug_timeout_probe": ([p], i32),
             }
-            if hasattr(L, "q4_0_q8_0_gemm"):
-                sig["q4_0_q8_0_gemm"] = ([p, p, p, i64, i64, i64, i64, p], i32)
+            sig["q4_0_q8_0_gemm"] = ([p, p, p, i64, i64, i64, i64, p, i64, p], i32)
+            sig["q4_0_q8_0_gemm_workspace_bytes"] = ([i64, i64], i64)
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
                 fn.argtypes = args
@@ -160,11 +160,22 @@ def q4_0_q8_0_gemm_small_n(W, xq, y, ldy: int, O: int, K: int, N: int, stream=No
            "q4_0_q8_0_gemm_small_n")
 
 
-def q4_0_q8_0_gemm(W, xq, y, ldy: int, O: int, K: int, T: int, stream=None) -> None:
-    L = lib()
-    if not hasattr(L, "q4_0_q8_0_gemm"):
-        raise QdgError(QDG_EINVAL, "q4_0_q8_0_gemm is not in this build of libqdg.so")
-    _check(L.q4_0_q8_0_gemm(_ptr(W), _ptr(xq), _ptr(y), ldy, O, K, T, _stream(stream)), "q4_0_q8_0_gemm")
+def q4_0_q8_0_gemm_workspace_bytes(K: int, T: int) -> int:
+    n = int(lib().q4_0_q8_0_gemm_workspace_bytes(K, T))
+    if n < 0:
+        raise QdgError(n, "q4_0_q8_0_gemm_workspace_bytes")
+    return n
+
+
+def q4_0_q8_0_gemm(W, xq, y, ldy: int, O: int, K: int, T: int, workspace, workspace_bytes: int | None = None,
+                   stream=None) -> None:
+    """Prefill product; `workspace` is caller-owned device memory of at least
+    q4_0_q8_0_gemm_workspace_bytes(K, T) bytes (a uint8 tensor: its size is
+    used when workspace_bytes is None)."""
+    if workspace_bytes is None:
+        workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
+    _check(lib().q4_0_q8_0_gemm(_ptr(W), _ptr(xq), _ptr(y), ldy, O, K, T, _ptr(workspace), workspace_bytes,
+                                _stream(stream)), "q4_0_q8_0_gemm")
 
 
 def quantize_q4_0(w, Wq, O: int | None = None, K: int | None = None, ldw: int | None = None,

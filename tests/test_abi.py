@@ -24,7 +24,8 @@ def L():
 
 def test_header_declares_entry_points():
     names = declared_symbols()
-    for must in ("qnorm_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm", "quantize_q4_0",
+    for must in ("qnorm_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
+                 "q4_0_q8_0_gemm_workspace_bytes", "quantize_q4_0",
                  "qdg_device_status", "qdg_status_string"):
         assert must in names
 
@@ -126,12 +127,20 @@ def test_small_n_host_validation(L):
 
 def test_gemm_host_validation(L):
     f = L.q4_0_q8_0_gemm
-    assert f(A16, A16, None, 8, 8, 256, 4, None) == -1     # null y
-    assert f(A16, A16, A16, 4, 8, 256, 4, None) == -1      # ldy < O
-    assert f(A16, A16, A16, 8, 8, 256, 0, None) == -1      # T = 0
-    assert f(A16, A16, A16, 8, 8, 320, 4, None) == -3      # K % 256
-    assert f(A2, A16, A16, 8, 8, 256, 4, None) == -2       # W misaligned
-    assert f(A16, A2, A16, 8, 8, 256, 4, None) == -2       # xq misaligned
+    need = L.q4_0_q8_0_gemm_workspace_bytes(256, 4)
+    assert need == 1 * 8 * 8704                                      # one token tile, 8 blocks
+    assert L.q4_0_q8_0_gemm_workspace_bytes(256, 129) == 2 * 8 * 8704
+    assert L.q4_0_q8_0_gemm_workspace_bytes(320, 4) == -3             # K % 256
+    assert L.q4_0_q8_0_gemm_workspace_bytes(256, 0) == -1
+    assert f(A16, A16, None, 8, 8, 256, 4, A16, need, None) == -1     # null y
+    assert f(A16, A16, A16, 4, 8, 256, 4, A16, need, None) == -1      # ldy < O
+    assert f(A16, A16, A16, 8, 8, 256, 0, A16, need, None) == -1      # T = 0
+    assert f(A16, A16, A16, 8, 8, 320, 4, A16, need, None) == -3      # K % 256
+    assert f(A2, A16, A16, 8, 8, 256, 4, A16, need, None) == -2       # W misaligned
+    assert f(A16, A2, A16, 8, 8, 256, 4, A16, need, None) == -2       # xq misaligned
+    assert f(A16, A16, A16, 8, 8, 256, 4, None, need, None) == -1     # no workspace
+    assert f(A16, A16, A16, 8, 8, 256, 4, A16, need - 16, None) == -1 # workspace too small
+    assert f(A16, A16, A16, 8, 8, 256, 4, A2, need, None) == -2       # workspace misaligned
 
 
 def test_quantize_q4_0_host_validation(L):

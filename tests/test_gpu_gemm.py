@@ -22,7 +22,8 @@ def gpu_gemm(Wd, xd, O, K, T, ldy=None):
     torch = torch_cuda()
     ldy = O if ldy is None else ldy
     y = torch.full((T, ldy), float("nan"), dtype=torch.float32, device="cuda")
-    qdg.q4_0_q8_0_gemm(Wd, xd, y, ldy, O, K, T)
+    ws = torch.empty(qdg.q4_0_q8_0_gemm_workspace_bytes(K, T), dtype=torch.uint8, device="cuda")
+    qdg.q4_0_q8_0_gemm(Wd, xd, y, ldy, O, K, T, ws)
     torch.cuda.synchronize()
     assert qdg.qdg_device_status() == qdg.QDG_OK
     out = to_host(y)
