@@ -208,6 +208,21 @@ QDG_API int q4_0_q8_0_gemm(const void* W, const void* xq, float* y, int64_t ldy,
 QDG_API int64_t q4_0_q8_0_gemm_workspace_bytes(int64_t K, int64_t T);
 
 /*
+ * q4_0_q8_0_gemm_static -- q4_0_q8_0_gemm without a caller workspace and
+ * without any device allocation, for callers that cannot allocate device
+ * memory.  The pages have no counterpart: this is a library convenience.
+ * Its scratch is a 16 MiB array in the library's device memory, so the
+ * problem must satisfy q4_0_q8_0_gemm_workspace_bytes(K, T) <= 16 MiB
+ * (e.g. T <= 1920 tokens at K = 4096, T <= 512 at K = 14336); larger ones
+ * return QDG_ESHAPE.  The first call on a device looks up the array's
+ * address on that device (make it before any stream capture).  Nothing
+ * needs to start at zero.  All calls share the array: calls that overlap on
+ * the GPU race.  Other arguments and errors as q4_0_q8_0_gemm.
+ */
+QDG_API int q4_0_q8_0_gemm_static(const void* W, const void* xq, float* y, int64_t ldy,
+                                  int64_t O, int64_t K, int64_t T, qdg_stream_t stream);
+
+/*
  * quantize_q4_0 -- weight preparation: fp32 [O][ldw] -> Q4_0 [O][K/32].
  * Per block: m = the element of largest magnitude (the first one on ties),
  * d = m / -8 in fp32, q = min(15, floor(w/d + 8.5)), stored d = fp16(d); an

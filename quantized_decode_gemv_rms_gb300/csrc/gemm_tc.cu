@@ -615,3 +615,53 @@ extern "C" int q4_0_q8_0_gemm(const void* W, const void* xq, float* y, int64_t l
     return qdg::gemm_launch(W, xq, y, ldy, O, K, T, workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream),
                             nullptr);
 }
+
+// ---------------------------------------------------------------------------
+// q4_0_q8_0_gemm_static: the same product for callers that cannot allocate
+// device memory.  Its activation records live in a file-scope device array of
+// kStaticWorkspaceBytes (16 MiB); larger problems are rejected with
+// QDG_ESHAPE.  The array's device address is looked up once per device, on
+// that device's first call (which should therefore come before any stream
+// capture).  Nothing in the array needs to start at zero: every call writes
+// all the records it reads before reading them.  All calls share the array,
+// so calls that overlap on the GPU race.
+namespace qdg {
+namespace {
+
+constexpr int64_t kStaticWorkspaceBytes = int64_t(16) << 20;
+constexpr int kMaxDevices = 64;
+static __device__ __align__(256) uint8_t g_static_ws[kStaticWorkspaceBytes];
+
+std::mutex g_static_mutex;
+void* g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_ws on the current device (set-up on first use).
+void* static_workspace() {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_ptr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_ws) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_static_ptr[dev] = ptr;
+    }
+    return g_static_ptr[dev];
+}
+
+}  // namespace
+}  // namespace qdg
+
+extern "C" int q4_0_q8_0_gemm_static(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K,
+                                     int64_t T, qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    const int64_t bytes = qdg::gemm_workspace_bytes(K, T);
+    if (bytes < 0) return static_cast<int>(bytes);
+    if (bytes > qdg::kStaticWorkspaceBytes) return QDG_ESHAPE;
+    void* ws = qdg::static_workspace();
+    if (ws == nullptr) return QDG_ECUDA;
+    return qdg::gemm_launch(W, xq, y, ldy, O, K, T, ws, qdg::kStaticWorkspaceBytes,
+                            reinterpret_cast<cudaStream_t>(stream), nullptr);
+}

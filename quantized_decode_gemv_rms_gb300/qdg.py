@@ -63,6 +63,7 @@ def lib() -> ctypes.CDLL:
             }
             sig["q4_0_q8_0_gemm"] = ([p, p, p, i64, i64, i64, i64, p, i64, p], i32)
             sig["q4_0_q8_0_gemm_workspace_bytes"] = ([i64, i64], i64)
+            sig["q4_0_q8_0_gemm_static"] = ([p, p, p, i64, i64, i64, i64, p], i32)
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
                 fn.argtypes = args
@@ -176,6 +177,12 @@ def q4_0_q8_0_gemm(W, xq, y, ldy: int, O: int, K: int, T: int, workspace, worksp
         workspace_bytes = workspace.numel() * workspace.element_size() if hasattr(workspace, "numel") else 0
     _check(lib().q4_0_q8_0_gemm(_ptr(W), _ptr(xq), _ptr(y), ldy, O, K, T, _ptr(workspace), workspace_bytes,
                                 _stream(stream)), "q4_0_q8_0_gemm")
+
+
+def q4_0_q8_0_gemm_static(W, xq, y, ldy: int, O: int, K: int, T: int, stream=None) -> None:
+    """Prefill product with the library's own fixed-size scratch (no allocation)."""
+    _check(lib().q4_0_q8_0_gemm_static(_ptr(W), _ptr(xq), _ptr(y), ldy, O, K, T, _stream(stream)),
+           "q4_0_q8_0_gemm_static")
 
 
 def quantize_q4_0(w, Wq, O: int | None = None, K: int | None = None, ldw: int | None = None,
