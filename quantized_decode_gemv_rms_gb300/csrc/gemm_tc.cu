@@ -20,15 +20,15 @@
 // kernel loads one such 8704-byte record per block with a bulk copy.
 //
 // Warp roles in one persistent CTA per SM (tile 128 weight rows x 128 tokens):
-//   warp 0      producer (one thread): a 2-D tensor copy of a 128-row box of
-//               raw Q4_0 bytes, 8 blocks wide, per raw stage
+//   warp 0      producer: a 2-D tensor copy of a 128-row box of raw Q4_0
+//               bytes, 8 blocks wide, per raw stage, and the two bulk copies
+//               of each block's activation record (fp16 tile into the operand
+//               slot, scales into the scale ring), issued from eight lanes at
+//               once for four blocks
 //   warp 1      tensor-memory allocator and MMA issuer (one thread)
 //   warps 2-9   weight converters (row quarter x block parity, two per SMSP):
 //               raw blocks -> fp16 operand tiles in the canonical layout plus
-//               per-block fp32 scales; raw rows are read as 16-byte vectors.
-//               One warp per parity also issues the two bulk copies of each
-//               of its blocks' activation records (fp16 tile into the operand
-//               slot, scales into the scale ring)
+//               per-block fp32 scales; raw rows are read as 16-byte vectors
 //   warps 10-25 drain: tcgen05.ld of the block sums, y += d_w d_x isum with
 //               packed fp32x2 arithmetic
 // The converters are spread two per SMSP (measured: a drain warp sharing its
@@ -63,7 +63,8 @@ constexpr int XREC = OPB + BN * 4;       // activation record of the workspace: 
 constexpr int OP_BYTES = OPA + OPB;      // operand slot: [A tile][B tile], released when its MMAs complete
 constexpr int OS = 8;                    // operand slots
 constexpr int SC_BYTES = (BN + BM) * 4;  // scale entry: [d_x of 128 tokens][d_w of 128 rows], released by the drain
-constexpr int SR = 8;                    // scale entries
+constexpr int SR = 32;                   // scale entries
+constexpr int kCopyGroup = 4;            // blocks whose records the producer issues together
 constexpr int TB = 4;                    // block-sum buffers in tensor memory
 constexpr int TMEM_COLS = TB * BN;       // all 512 columns
 constexpr int kConvWarps = 8;                           // weight converters: 4 row quarters x 2 block parities
@@ -280,24 +281,66 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
     pdl_wait();
 
     if (warp < 2) {
-        if (warp == 0 && lane == 0) {
-            // -------------------------------------------------------- producer (one thread)
+        if (warp == 0) {
+            // -------------------------------------------------------- producer (one warp)
+            // One issuing thread manages about one bulk copy per 600 cycles
+            // (measured), so the copies of a group of four blocks go out from
+            // eight lanes at once: lanes 0-3 the fp16 tiles, lanes 4-7 the
+            // scales; lane 0 also issues the raw weight stage.
             int c = 0;   // raw weight chunks issued
+            int g = 0;   // blocks whose records were issued
             bool ok = true;
             for (int tile = blockIdx.x; tile < total_tiles && ok && !*abort_flag; tile += gridDim.x) {
                 const int m0 = (tile / a.ntiles) * BM;
-                for (int ch = 0; ch < nchunks; ++ch, ++c) {
-                    const int s = c % RS;
-                    if (c >= RS) ok = wait_or_abort(&raw_empty[s], ((c / RS) - 1) & 1, abort_flag);
+                const int nt = tile % a.ntiles;
+                for (int b = 0; b < a.nb; b += kCopyGroup, g += kCopyGroup) {
+                    if (b % CHUNK == 0) {
+                        const int s = c % RS;
+                        bool w = true;
+                        if (lane == 0 && c >= RS) w = wait_or_abort(&raw_empty[s], ((c / RS) - 1) & 1, abort_flag);
+                        ok = __shfl_sync(0xffffffffu, w, 0);
+                        if (!ok) break;
+                        if (lane == 0) {
+                            // Rows past O are zero-filled by the copy and
+                            // still count toward the transaction bytes.
+                            mbar_arrive_expect_tx(&raw_full[s], RAW_W);
+                            tma_load_2d(smem + s * RAW_W, &a.wmap, (b / CHUNK) * (CHUNK * 18), m0, &raw_full[s]);
+                        }
+                        ++c;
+                    }
+                    // Slots and scale entries free in order: waiting for the
+                    // last of the group covers the group.
+                    const int gl = g + kCopyGroup - 1;
+                    bool w = true;
+                    if (lane == 0) {
+                        if (gl >= OS) w = wait_or_abort(&op_empty[gl % OS], ((gl / OS) - 1) & 1, abort_flag);
+                        if (w && gl >= SR) w = wait_or_abort(&sc_empty[gl % SR], ((gl / SR) - 1) & 1, abort_flag);
+                    }
+                    ok = __shfl_sync(0xffffffffu, w, 0);
                     if (!ok) break;
-                    // Rows past O are zero-filled by the copy and still count
-                    // toward the transaction bytes.
-                    mbar_arrive_expect_tx(&raw_full[s], RAW_W);
-                    tma_load_2d(smem + s * RAW_W, &a.wmap, ch * (CHUNK * 18), m0, &raw_full[s]);
+                    if (lane < 2 * kCopyGroup) {
+                        const int u = lane % kCopyGroup;
+                        const int gu = g + u;
+                        const uint8_t* rec = a.xrec + (static_cast<int64_t>(nt) * a.nb + b + u) * XREC;
+                        if (lane < kCopyGroup) {
+                            mbar_arrive_expect_tx(&op_full[gu % OS], OPB);
+                            bulk_g2s_plain(smem + OFF_OPS + (gu % OS) * OP_BYTES + OPA, rec, OPB, &op_full[gu % OS]);
+                        } else {
+                            mbar_arrive_expect_tx(&sc_full[gu % SR], BN * 4);
+                            bulk_g2s_plain(smem + OFF_SC + (gu % SR) * SC_BYTES, rec + OPB, BN * 4, &sc_full[gu % SR]);
+                        }
+                    }
+                    __syncwarp();
                 }
             }
             // Copies still in flight must land before the CTA may exit.
-            for (int k = (c - RS > 0 ? c - RS : 0); k < c; ++k) mbar_wait(&raw_full[k % RS], (k / RS) & 1);
+            if (lane == 0) {
+                for (int k = (c - RS > 0 ? c - RS : 0); k < c; ++k) mbar_wait(&raw_full[k % RS], (k / RS) & 1);
+                if (*abort_flag) {
+                    for (int k = (g - OS > 0 ? g - OS : 0); k < g; ++k) mbar_wait(&op_full[k % OS], (k / OS) & 1);
+                    for (int k = (g - SR > 0 ? g - SR : 0); k < g; ++k) mbar_wait(&sc_full[k % SR], (k / SR) & 1);
+                }
+            }
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------------- MMA issuer (one thread)
             int g = 0;
@@ -336,22 +379,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
         const int ci = warp - 2;
         const int t = (ci & 3) * 32 + lane;          // weight row within the tile
         const int par = ci >> 2;
-        // The activation records of this parity's blocks are copied by one of
-        // its warps (ci 0 for even blocks, ci 5 for odd ones: SMSPs 2 and 3).
-        const bool copier = ci == (par ? 5 : 0) && lane == 0;
         int g0 = 0;                                   // first block of the current chunk
-        int issued = 0;                               // records copied by this thread (copier)
         bool ok = true;
-        auto copy_record = [&](int g, int nt, int b) {
-            const uint8_t* rec = a.xrec + (static_cast<int64_t>(nt) * a.nb + b) * XREC;
-            mbar_arrive_expect_tx(&op_full[g % OS], OPB);
-            bulk_g2s_plain(smem + OFF_OPS + (g % OS) * OP_BYTES + OPA, rec, OPB, &op_full[g % OS]);
-            mbar_arrive_expect_tx(&sc_full[g % SR], BN * 4);
-            bulk_g2s_plain(smem + OFF_SC + (g % SR) * SC_BYTES, rec + OPB, BN * 4, &sc_full[g % SR]);
-        };
         for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
             const int m0 = (tile / a.ntiles) * BM;
-            const int nt = tile % a.ntiles;
             const bool valid = m0 + t < a.O;
             for (int ch = 0; ch < nchunks && ok; ++ch, g0 += CHUNK) {
                 const int c = g0 / CHUNK;
@@ -369,11 +400,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     if (gb >= SR) w_ok = w_ok && wait_or_abort(&sc_empty[gb % SR], ((gb / SR) - 1) & 1, abort_flag);
                     ok = __all_sync(0xffffffffu, w_ok);
                     if (!ok) break;
-                    if (copier) {
-                        copy_record(ga, nt, ch * CHUNK + bl + par);
-                        copy_record(gb, nt, ch * CHUNK + bl + par + 2);
-                        issued = gb + 1;
-                    }
                     if (par == 0) {
                         convert_block<0>(st, bl, t, valid, smem + OFF_OPS + (ga % OS) * OP_BYTES,
                                          reinterpret_cast<float*>(smem + OFF_SC + (ga % SR) * SC_BYTES) + BN);
@@ -397,14 +423,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_tc_kernel(const __grid_const
                     }
                 }
             }
-        }
-        // After a timeout: the record copies still in flight must land before
-        // the CTA may exit (this parity's blocks among the last OS / SR).
-        if (copier && *abort_flag) {
-            for (int k = (issued - OS > 0 ? issued - OS : 0); k < issued; ++k)
-                if ((k & 1) == par) mbar_wait(&op_full[k % OS], (k / OS) & 1);
-            for (int k = (issued - SR > 0 ? issued - SR : 0); k < issued; ++k)
-                if ((k & 1) == par) mbar_wait(&sc_full[k % SR], (k / SR) & 1);
         }
     } else {
         // ------------------------------------------------------------ drain
