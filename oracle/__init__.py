@@ -66,6 +66,8 @@ def lib():
             L.orc_rms_scale.restype = c_f
             L.orc_quantize_q8_0.argtypes = [c_p, c_i64, c_p, c_f, c_i64, c_i64, c_p]
             L.orc_quantize_q8_0.restype = None
+            L.orc_quantize_q8_0_add.argtypes = [c_p, c_i64, c_p, c_p, c_i64, c_f, c_i64, c_i64, c_p]
+            L.orc_quantize_q8_0_add.restype = None
             L.orc_block_sums.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p]
             L.orc_block_sums.restype = None
             L.orc_matvec.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_i64, c_p, c_p, c_p]
@@ -101,14 +103,27 @@ def rms_scale(x: np.ndarray, eps: float) -> float:
     return float(lib().orc_rms_scale(_ptr(x), x.shape[-1], float(np.float32(eps))))
 
 
-def quantize_q8_0(x: np.ndarray, gamma: np.ndarray | None, eps: float = 1e-6) -> np.ndarray:
-    """fp32 [N][K] (or [K]) -> uint8 [N][K/32*34] Q8_0 blocks; gamma=None = no norm."""
+def quantize_q8_0(x: np.ndarray, gamma: np.ndarray | None, eps: float = 1e-6,
+                  add: np.ndarray | None = None) -> np.ndarray:
+    """fp32 [N][K] (or [K]) -> uint8 [N][K/32*34] Q8_0 blocks; gamma=None = no
+    norm; add = an fp32 addend applied after the norm and MUL: [K] (the same
+    for every vector) or [N][K]."""
     x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float32)
     N, K = x.shape
     assert K % QK == 0
     g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float32)
     out = np.empty((N, K // QK * Q8_BLOCK), dtype=np.uint8)
-    lib().orc_quantize_q8_0(_ptr(x), K, _ptr(g), float(np.float32(eps)), K, N, _ptr(out))
+    if add is None:
+        lib().orc_quantize_q8_0(_ptr(x), K, _ptr(g), float(np.float32(eps)), K, N, _ptr(out))
+        return out
+    a = np.ascontiguousarray(add, dtype=np.float32)
+    if a.ndim == 1:
+        assert a.shape[0] == K
+        ldadd = 0
+    else:
+        assert a.shape == (N, K)
+        ldadd = K
+    lib().orc_quantize_q8_0_add(_ptr(x), K, _ptr(g), _ptr(a), ldadd, float(np.float32(eps)), K, N, _ptr(out))
     return out
 
 

@@ -192,21 +192,28 @@ float orc_rms_scale(const float* x, int64_t K, float eps)
 }
 
 /* ---------------------------------------------------------------------- */
-/* Activation -> Q8_0, optionally through RMS_NORM then MUL by gamma.       */
+/* Activation -> Q8_0, optionally through RMS_NORM then MUL by gamma, and  */
+/* optionally an ADD after them (the RMS_NORM+MUL+ADD fusion pattern of     */
+/* [llama.cpp b10909: Metal backend fusion-table refactor, "CI and related  */
+/* fixes"]):                                                                */
 /*  gamma != NULL: v_i = (x_i * s) * gamma_i   (two fp32 products, in that   */
 /*                 order: normalise, then multiply)                         */
 /*  gamma == NULL: v_i = x_i (plain quantization, no norm)                   */
+/*  add != NULL:   v_i = v_i + a_i, one fp32 addition after the above, with  */
+/*                 a = add + n * ldadd for vector n (ldadd 0: one addend     */
+/*                 for every vector); the norm statistic is over x alone.   */
 /* Per block: amax = max |v|, d = amax / 127 (fp32), q = round(v / d) with   */
 /* halves away from zero, clamped to [-127, 127]; d == 0 gives q = 0; the   */
 /* stored scale is fp16(d), round to nearest even.                          */
 /* x is [N][ldx] (row n = one vector); xq is [N][K/32] blocks.              */
 /* ---------------------------------------------------------------------- */
-void orc_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float eps,
-                       int64_t K, int64_t N, uint8_t* xq)
+void orc_quantize_q8_0_add(const float* x, int64_t ldx, const float* gamma, const float* add, int64_t ldadd,
+                           float eps, int64_t K, int64_t N, uint8_t* xq)
 {
     const int64_t nb = K / QK;
     for (int64_t n = 0; n < N; ++n) {
         const float* xn = x + n * ldx;
+        const float* an = add ? add + n * ldadd : NULL;
         float s = gamma ? orc_rms_scale(xn, K, eps) : 1.0f;
         for (int64_t b = 0; b < nb; ++b) {
             float v[QK];
@@ -218,6 +225,8 @@ void orc_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float ep
                 } else {
                     v[j] = xn[i];
                 }
+                if (an)
+                    v[j] = v[j] + an[i];
             }
             float amax = 0.0f;
             for (int j = 0; j < QK; ++j)
@@ -238,6 +247,12 @@ void orc_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float ep
             }
         }
     }
+}
+
+void orc_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float eps,
+                       int64_t K, int64_t N, uint8_t* xq)
+{
+    orc_quantize_q8_0_add(x, ldx, gamma, NULL, 0, eps, K, N, xq);
 }
 
 /* ---------------------------------------------------------------------- */

@@ -339,3 +339,87 @@ def test_selection_and_permutation(orc):
     b = orc.matvec(Wp, xp, K)
     assert np.all(np.abs(a[1] - b[1]) <= 1e-12 * a[2])
     assert np.array_equal(orc.block_sums(Wp, xp, K)[0], isum[0][:, perm])
+
+
+# ---- RMS_NORM + MUL + ADD -> Q8_0 (the fusion pattern counted in the Metal
+# fusion-table refactor's CI notes): v = (x*s)*gamma + a, one fp32 add after
+# the two products; the RMS statistic is over x alone.
+
+def _half_away(r):
+    from fractions import Fraction
+    r = Fraction(r)
+    f = r.numerator // r.denominator
+    return f + 1 if (r - f) * 2 >= 1 and r > 0 else (f if r >= 0 else (f + 1 if (r - f) * 2 > 1 else f))
+
+
+def test_q8_add_closed_form(orc):
+    """x = 2 (constant), gamma = 1, eps = 0: x*s = 1 exactly, so v_j = 1 + a_j.
+    With a_j = (j - 8)/8, v_j = j/8, amax = 31/8 and q_j = round(127 j / 31)
+    (never a tie: 31 is odd)."""
+    from fractions import Fraction
+    K = 32
+    x = np.full((1, K), 2.0, np.float32)
+    a = ((np.arange(K) - 8) / 8).astype(np.float32)
+    q = orc.quantize_q8_0(x, np.ones(K, np.float32), 0.0, add=a)[0]
+    d = np.float32(np.float32(3.875) / np.float32(127.0))
+    assert q[:2].view(np.uint16)[0] == np.float16(d).view(np.uint16)
+    want = [_half_away(Fraction(127 * j, 31)) for j in range(K)]
+    assert list(q[2:].view(np.int8)) == want
+
+
+def test_q8_add_after_mul(orc):
+    """gamma = 2, a = 1: v = 1*2 + 1 = 3 everywhere (adding before the MUL would give 4)."""
+    K = 64
+    x = np.full((1, K), 2.0, np.float32)
+    q = orc.quantize_q8_0(x, np.full(K, 2.0, np.float32), 0.0, add=np.ones(K, np.float32))[0]
+    for b in range(K // 32):
+        blk = q[b * 34:(b + 1) * 34]
+        assert blk[:2].view(np.uint16)[0] == np.float16(np.float32(3.0) / np.float32(127.0)).view(np.uint16)
+        assert np.all(blk[2:].view(np.int8) == 127)
+
+
+def test_q8_add_norm_over_x_only(orc):
+    """Large addends leave the statistic alone: x = 2 gives x*s = 1 whatever a is."""
+    from fractions import Fraction
+    K = 32
+    x = np.full((1, K), 2.0, np.float32)
+    a = (64.0 * (np.arange(K) - 16)).astype(np.float32)            # v_j = 1 + 64 (j - 16), exact
+    q = orc.quantize_q8_0(x, np.ones(K, np.float32), 0.0, add=a)[0]
+    v = [1 + 64 * (j - 16) for j in range(K)]
+    amax = max(abs(t) for t in v)                                  # 1023 at j = 0
+    assert q[:2].view(np.uint16)[0] == np.float16(np.float32(amax) / np.float32(127.0)).view(np.uint16)
+    want = [_half_away(Fraction(127 * t, amax)) for t in v]
+    assert list(q[2:].view(np.int8)) == want
+
+
+def test_q8_add_zero_is_identity(orc):
+    rng = np.random.default_rng(11)
+    N, K = 3, 512
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    g = (1 + 0.1 * rng.standard_normal(K)).astype(np.float32)
+    base = orc.quantize_q8_0(x, g, 1e-6)
+    assert np.array_equal(orc.quantize_q8_0(x, g, 1e-6, add=np.zeros(K, np.float32)), base)
+    assert np.array_equal(orc.quantize_q8_0(x, g, 1e-6, add=np.zeros((N, K), np.float32)), base)
+
+
+def test_q8_add_plain_is_sum_then_quantize(orc):
+    """Without gamma the ADD reduces to quantizing the fp32 sum x + a."""
+    rng = np.random.default_rng(12)
+    N, K = 2, 256
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    a = rng.standard_normal((N, K)).astype(np.float32)
+    assert np.array_equal(orc.quantize_q8_0(x, None, add=a), orc.quantize_q8_0(x + a, None))
+
+
+def test_q8_add_rows_and_broadcast(orc):
+    """Row n uses its own addend row; a broadcast addend equals the same row repeated."""
+    rng = np.random.default_rng(13)
+    N, K = 3, 256
+    x = rng.standard_normal((N, K)).astype(np.float32)
+    g = rng.standard_normal(K).astype(np.float32)
+    a = rng.standard_normal((N, K)).astype(np.float32)
+    rows = orc.quantize_q8_0(x, g, 1e-6, add=a)
+    for n in range(N):
+        assert np.array_equal(rows[n], orc.quantize_q8_0(x[n], g, 1e-6, add=a[n])[0])
+    assert np.array_equal(orc.quantize_q8_0(x, g, 1e-6, add=a[1]),
+                          orc.quantize_q8_0(x, g, 1e-6, add=np.tile(a[1], (N, 1))))
