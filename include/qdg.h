@@ -94,6 +94,22 @@ QDG_API int qnorm_quantize_q8_0(const float* x, int64_t ldx, const float* gamma,
                         int64_t K, int64_t N, void* xq, qdg_stream_t stream);
 
 /*
+ * qnorm_add_quantize_q8_0 -- fused RMS_NORM + MUL(gamma) + ADD + Q8_0
+ * quantization  [llama.cpp b10909, section "CI and related fixes" (the
+ * RMS_NORM+MUL+ADD fusion pattern)].
+ *
+ * As qnorm_quantize_q8_0, with v_i = (x_i*s)*gamma_i + a_i (or x_i + a_i
+ * when gamma is NULL): one IEEE fp32 addition after the products.  The RMS
+ * statistic is over x alone.
+ * add    fp32 addend, 4-byte aligned: vector n uses add + n*ldadd; ldadd = 0
+ *        uses the same K values for every vector, otherwise ldadd >= K.
+ * Errors: QDG_EINVAL also for a NULL add or 0 < ldadd < K.
+ */
+QDG_API int qnorm_add_quantize_q8_0(const float* x, int64_t ldx, const float* gamma,
+                                    const float* add, int64_t ldadd, float eps, int64_t K,
+                                    int64_t N, void* xq, qdg_stream_t stream);
+
+/*
  * q4_0_q8_0_gemv -- y = W * x for one Q8_0 vector (batch-1 decode, the
  * "mmvq" route)  [GGML: Backend abstraction and hardware acceleration,
  * section "CUDA: mmvq, mmq, cublas -- three matrix paths"].
@@ -101,8 +117,8 @@ QDG_API int qnorm_quantize_q8_0(const float* x, int64_t ldx, const float* gamma,
  * W   [O][K/32] Q4_0, 16-byte aligned.      xq  [K/32] Q8_0, 4-byte aligned.
  * y   [O] fp32, 4-byte aligned (overwritten).
  * K   multiple of 256, 256 <= K <= 32768.   1 <= O < 2^31.
- * W is streamed once from HBM through a shared-memory ring filled by bulk
- * asynchronous copies; the result is deterministic (fixed reduction order).
+ * W is streamed once from HBM with 16-byte loads issued several row
+ * segments ahead; the result is deterministic (fixed reduction order).
  */
 QDG_API int q4_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K,
                    qdg_stream_t stream);

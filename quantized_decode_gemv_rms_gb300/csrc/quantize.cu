@@ -1,5 +1,5 @@
-// quantize.cu -- the fused RMS_NORM + MUL(gamma) -> Q8_0 activation kernel
-// and the load-time fp32 -> Q4_0 weight quantizer.
+// quantize.cu -- the fused RMS_NORM + MUL(gamma) [+ ADD] -> Q8_0 activation
+// kernel and the load-time fp32 -> Q4_0 weight quantizer.
 //
 // RMS_NORM followed by MUL is the pattern whose fusion the Metal backend
 // lost, costing about 5% of token-generation speed [llama.cpp b10909: Metal
@@ -27,9 +27,12 @@ constexpr int kBlocksPerCta = 32;     // Q8_0 blocks quantized by one CTA (4 per
 //   the 8 warp totals combine as ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).
 //   Quantization: warp w takes blocks w, w+8, ... of the slice, lane l
 //   element 32b+l.
+//   add (optional): v = (x*s)*gamma + a, one fp32 addition after the MUL
+//   (the RMS_NORM+MUL+ADD pattern), a = add + n*ldadd (ldadd 0: broadcast).
 __global__ void __launch_bounds__(kNormThreads)
-qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restrict__ gamma, float eps, int K,
-                int splits, uint8_t* __restrict__ xq) {
+qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restrict__ gamma,
+                const float* __restrict__ add, int64_t ldadd, float eps, int K, int splits,
+                uint8_t* __restrict__ xq) {
     pdl_wait();
     pdl_trigger();
     const int64_t n = blockIdx.x / splits;
@@ -38,18 +41,20 @@ qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restric
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const float* xn = x + n * ldx;
+    const float* an = add != nullptr ? add + n * ldadd : nullptr;
     const int nb = K >> 5;
     const int b0 = split * kBlocksPerCta;
     const int b1 = min(nb, b0 + kBlocksPerCta);
 
     // Issue this CTA's slice loads first; they overlap the reduction below.
     constexpr int kPer = kBlocksPerCta / (kNormThreads / 32);
-    float xv[kPer], gv[kPer];
+    float xv[kPer], gv[kPer], av[kPer];
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {
         const int b = b0 + warp + u * (kNormThreads / 32);
         xv[u] = b < b1 ? __ldg(xn + (b << 5) + lane) : 0.0f;
         gv[u] = (gamma != nullptr && b < b1) ? __ldg(gamma + (b << 5) + lane) : 1.0f;
+        av[u] = (an != nullptr && b < b1) ? __ldg(an + (b << 5) + lane) : 0.0f;
     }
 
     float s = 1.0f;
@@ -83,6 +88,7 @@ qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restric
         if (b >= b1) break;
         float v = xv[u];
         if (gamma != nullptr) v = __fmul_rn(__fmul_rn(v, s), gv[u]);
+        if (an != nullptr) v = __fadd_rn(v, av[u]);
         float amax = fabsf(v);
 #pragma unroll
         for (int h = 16; h >= 1; h >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, h));
@@ -163,21 +169,39 @@ unsigned flags_read_clear_quantize(cudaStream_t stream) {
 
 using namespace qdg;
 
-extern "C" int qnorm_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float eps, int64_t K, int64_t N,
-                                   void* xq, qdg_stream_t stream) {
+namespace {
+
+int qnorm_launch(const float* x, int64_t ldx, const float* gamma, const float* add, int64_t ldadd, float eps,
+                 int64_t K, int64_t N, void* xq, qdg_stream_t stream) {
     if (!x || !xq) return QDG_EINVAL;
     if (K <= 0 || N <= 0 || ldx < K) return QDG_EINVAL;
+    if (add && ldadd != 0 && ldadd < K) return QDG_EINVAL;
     if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
     if (K % 32 != 0 || K > (1 << 20)) return QDG_ESHAPE;
     const int splits = static_cast<int>((K / 32 + kBlocksPerCta - 1) / kBlocksPerCta);
     if (N * splits > 0x7fffffff) return QDG_ESHAPE;
-    if (!aligned(x, 4) || !aligned(xq, 2) || (gamma && !aligned(gamma, 4))) return QDG_EALIGN;
+    if (!aligned(x, 4) || !aligned(xq, 2) || (gamma && !aligned(gamma, 4)) || (add && !aligned(add, 4)))
+        return QDG_EALIGN;
     cudaError_t e = launch(qnorm_q8_kernel, dim3(static_cast<unsigned>(N * splits)), dim3(kNormThreads), 0,
-                           reinterpret_cast<cudaStream_t>(stream), true, x, ldx, gamma, eps, static_cast<int>(K),
-                           splits, static_cast<uint8_t*>(xq));
+                           reinterpret_cast<cudaStream_t>(stream), true, x, ldx, gamma, add, add ? ldadd : int64_t(0),
+                           eps, static_cast<int>(K), splits, static_cast<uint8_t*>(xq));
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(0);
     return QDG_OK;
+}
+
+}  // namespace
+
+extern "C" int qnorm_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, float eps, int64_t K, int64_t N,
+                                   void* xq, qdg_stream_t stream) {
+    return qnorm_launch(x, ldx, gamma, nullptr, 0, eps, K, N, xq, stream);
+}
+
+extern "C" int qnorm_add_quantize_q8_0(const float* x, int64_t ldx, const float* gamma, const float* add,
+                                       int64_t ldadd, float eps, int64_t K, int64_t N, void* xq,
+                                       qdg_stream_t stream) {
+    if (!add) return QDG_EINVAL;
+    return qnorm_launch(x, ldx, gamma, add, ldadd, eps, K, N, xq, stream);
 }
 
 extern "C" int quantize_q4_0(const float* w, int64_t ldw, int64_t O, int64_t K, void* Wq, qdg_stream_t stream) {

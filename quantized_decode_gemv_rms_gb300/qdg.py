@@ -48,6 +48,7 @@ def lib() -> ctypes.CDLL:
             i64, p, f32, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
             sig = {
                 "qnorm_quantize_q8_0": ([p, i64, p, f32, i64, i64, p, p], i32),
+                "qnorm_add_quantize_q8_0": ([p, i64, p, p, i64, f32, i64, i64, p, p], i32),
                 "q4_0_q8_0_gemv": ([p, p, p, i64, i64, p], i32),
                 "q4_0_q8_0_gemv_group": ([p, p, p, i32, p, i64, p], i32),
                 "q4_0_gemv_rmsnorm": ([p, p, p, f32, p, i64, i64, p, p], i32),
@@ -126,6 +127,21 @@ def qnorm_quantize_q8_0(x, gamma, eps: float, xq, K: int | None = None, N: int |
     _check(lib().qnorm_quantize_q8_0(_ptr(x), ldx, _ptr(gamma), float(eps), K, N, _ptr(xq), _stream(stream)),
            "qnorm_quantize_q8_0")
 
+
+
+def qnorm_add_quantize_q8_0(x, gamma, add, eps: float, xq, K: int | None = None, N: int | None = None,
+                            ldx: int | None = None, ldadd: int | None = None, stream=None) -> None:
+    """Fused RMSNorm*gamma + add -> Q8_0.  add fp32 [K] (broadcast, ldadd 0) or [N][ldadd]."""
+    if K is None:
+        K = x.shape[-1]
+    if N is None:
+        N = 1 if x.dim() == 1 else x.shape[0]
+    if ldx is None:
+        ldx = K if x.dim() == 1 else x.stride(0)
+    if ldadd is None:
+        ldadd = 0 if add.dim() == 1 else add.stride(0)
+    _check(lib().qnorm_add_quantize_q8_0(_ptr(x), ldx, _ptr(gamma), _ptr(add), ldadd, float(eps), K, N, _ptr(xq),
+                                         _stream(stream)), "qnorm_add_quantize_q8_0")
 
 def q4_0_q8_0_gemv(W, xq, y, O: int, K: int, stream=None) -> None:
     _check(lib().q4_0_q8_0_gemv(_ptr(W), _ptr(xq), _ptr(y), O, K, _stream(stream)), "q4_0_q8_0_gemv")

@@ -24,7 +24,7 @@ def L():
 
 def test_header_declares_entry_points():
     names = declared_symbols()
-    for must in ("qnorm_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
+    for must in ("qnorm_quantize_q8_0", "qnorm_add_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
                  "q4_0_q8_0_gemm_workspace_bytes", "quantize_q4_0",
                  "qdg_device_status", "qdg_status_string"):
         assert must in names
@@ -60,6 +60,14 @@ def test_qnorm_host_validation(L):
     assert f(A2, 256, None, 1e-6, 256, 1, A16, None) == -2            # x misaligned
     assert f(A16, 256, A2, 1e-6, 256, 1, A16, None) == -2             # gamma misaligned
     assert f(A16, 256, None, 1e-6, 256, 1, A16 + 1, None) == -2       # xq misaligned
+
+
+def test_qnorm_add_host_validation(L):
+    f = L.qnorm_add_quantize_q8_0
+    assert f(A16, 256, A16, None, 0, 1e-6, 256, 1, A16, None) == -1     # null addend
+    assert f(A16, 256, A16, A16, 100, 1e-6, 256, 2, A16, None) == -1    # 0 < ldadd < K
+    assert f(A16, 256, A16, A2 + 1, 0, 1e-6, 256, 1, A16, None) == -2   # addend misaligned
+    assert f(A16, 256, A16, A16, 0, 1e-6, 48, 1, A16, None) == -3       # K % 32
 
 
 def test_gemv_host_validation(L):

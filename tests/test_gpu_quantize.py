@@ -39,6 +39,47 @@ def test_qnorm_bit_exact(K, norm):
     assert np.array_equal(got, ref)
 
 
+def run_qnorm_add(x, gamma, add, eps, ldadd_pad=0):
+    torch = torch_cuda()
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    N, K = x.shape
+    add = np.ascontiguousarray(add, dtype=np.float32)
+    if add.ndim == 2 and ldadd_pad:
+        buf = np.zeros((N, K + ldadd_pad), dtype=np.float32)
+        buf[:, :K] = add
+        ad, ldadd = to_dev(buf), K + ldadd_pad
+    else:
+        ad, ldadd = to_dev(add), (0 if add.ndim == 1 else K)
+    xq = empty_u8(qdg.q8_0_nbytes(N, K))
+    qdg.qnorm_add_quantize_q8_0(to_dev(x), None if gamma is None else to_dev(gamma), ad, eps, xq, K=K, N=N,
+                                ldadd=ldadd)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    return to_host(xq).reshape(N, -1)
+
+
+@pytest.mark.parametrize("K", [32, 256, 4096, 14336])
+@pytest.mark.parametrize("norm", [True, False])
+@pytest.mark.parametrize("per_row", [True, False])
+def test_qnorm_add_bit_exact(K, norm, per_row):
+    """RMS_NORM + MUL + ADD -> Q8_0 against the oracle, byte for byte; the
+    addend is residual-like (same scale as x, 1% outliers)."""
+    N = 3
+    x = synth.activations(20 + K, "qa-x", N, K, outlier_frac=0.01)
+    gam = synth.gamma(20 + K, "qa-g", K) if norm else None
+    a = synth.activations(20 + K, "qa-a", N, K, outlier_frac=0.01)
+    add = a if per_row else a[0]
+    got = run_qnorm_add(x, gam, add, 1e-6, ldadd_pad=16 if per_row else 0)
+    assert np.array_equal(got, oracle.quantize_q8_0(x, gam, 1e-6, add=add))
+
+
+def test_qnorm_add_zero_matches_plain_entry():
+    K, N = 2048, 2
+    x = synth.activations(31, "qa0", N, K)
+    gam = synth.gamma(31, "qa0", K)
+    assert np.array_equal(run_qnorm_add(x, gam, np.zeros(K, np.float32), 1e-6), run_qnorm(x, gam, 1e-6))
+
+
 def test_qnorm_many_columns_and_stride():
     K, N = 4096, 512
     x = synth.activations(4, "prefill-x", N, K)
