@@ -263,8 +263,11 @@ QDG_API const char* qdg_status_string(int status);
  * Options (process-wide).  QDG_OPT_PDL = 1 launches the decode kernels with
  * programmatic dependent launch: a kernel may start streaming W while the
  * previous kernel on the stream is still running, and waits for it before
- * reading activations or writing outputs.  Enable it only when W is not
- * written by the kernel launched immediately before on the same stream.
+ * reading activations or writing outputs.  The quantize kernels let their
+ * successor launch before they wait themselves, so a product that follows a
+ * quantize may start reading W while the kernel ahead of that quantize is
+ * still running.  Enable it only when W is not written by the last two
+ * kernels launched before the product on the same stream.
  * Default 0.  Returns QDG_EINVAL for an unknown option.
  */
 enum qdg_option { QDG_OPT_PDL = 1 };

@@ -114,7 +114,10 @@ struct Args {
 };
 
 template <bool kFused, bool kDebug>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const Args a, Plan plan) {
+// 96 registers a thread (no spills): one CTA of 512 threads then leaves room
+// on its SM for a CTA of the quantize kernel, so the next vector's quantize
+// can be resident, and start, while this product is still streaming.
+__global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
     __shared__ __align__(16) uint8_t seg_buf[kWarps][kSegBytes];
     __shared__ float part[kPartFloats];
     __shared__ float norm_part[8];

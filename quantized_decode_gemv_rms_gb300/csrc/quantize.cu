@@ -33,8 +33,10 @@ __global__ void __launch_bounds__(kNormThreads)
 qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restrict__ gamma,
                 const float* __restrict__ add, int64_t ldadd, float eps, int K, int splits,
                 uint8_t* __restrict__ xq) {
-    pdl_wait();
+    // Let the next kernel (the product that reads xq) launch at once: it
+    // streams its weights while this kernel waits for its own predecessor.
     pdl_trigger();
+    pdl_wait();
     const int64_t n = blockIdx.x / splits;
     const int split = blockIdx.x - static_cast<int>(n * splits);
     const int tid = threadIdx.x;
