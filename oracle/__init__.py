@@ -68,6 +68,10 @@ def lib():
             L.orc_quantize_q8_0.restype = None
             L.orc_quantize_q8_0_add.argtypes = [c_p, c_i64, c_p, c_p, c_i64, c_f, c_i64, c_i64, c_p]
             L.orc_quantize_q8_0_add.restype = None
+            L.orc_q4_0_seg_row_bytes.argtypes = [c_i64]
+            L.orc_q4_0_seg_row_bytes.restype = c_i64
+            L.orc_repack_q4_0_seg.argtypes = [c_p, c_i64, c_i64, c_p]
+            L.orc_repack_q4_0_seg.restype = None
             L.orc_block_sums.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p]
             L.orc_block_sums.restype = None
             L.orc_matvec.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_i64, c_p, c_p, c_p]
@@ -95,6 +99,23 @@ def quantize_q4_0(w: np.ndarray) -> np.ndarray:
     assert K % QK == 0
     out = np.empty((O, K // QK * Q4_BLOCK), dtype=np.uint8)
     lib().orc_quantize_q4_0(_ptr(w), O, K, _ptr(out))
+    return out
+
+
+def q4_0_seg_row_bytes(K: int) -> int:
+    """Bytes of one row in the Q4_0 segment layout (see oracle.c)."""
+    assert K % 256 == 0 and K > 0
+    return int(lib().orc_q4_0_seg_row_bytes(K))
+
+
+def repack_q4_0_seg(Wq: np.ndarray, K: int) -> np.ndarray:
+    """uint8 [O][K/32*18] Q4_0 rows -> uint8 [O][q4_0_seg_row_bytes(K)],
+    the load-time segment layout (a byte rearrangement; see oracle.c)."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    assert K % 256 == 0 and Wq.shape[1] == K // QK * Q4_BLOCK
+    O = Wq.shape[0]
+    out = np.empty((O, q4_0_seg_row_bytes(K)), dtype=np.uint8)
+    lib().orc_repack_q4_0_seg(_ptr(Wq), O, K, _ptr(out))
     return out
 
 

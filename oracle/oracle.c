@@ -143,6 +143,59 @@ void orc_quantize_q4_0(const float* w, int64_t rows, int64_t K, uint8_t* out)
     }
 }
 
+/* ---------------------------------------------------------------------- */
+/* Segment layout of Q4_0 rows.  A weight row is rearranged once, at load   */
+/* time, for the way the GPU reads it -- the GPU counterpart of the CPU back */
+/* end's load-time repack of Q4 weights  [GGML: Backend abstraction and     */
+/* hardware acceleration, section "How build switches become runtime        */
+/* capabilities", build-option table, GGML_CPU_REPACK].  The pages name the */
+/* repack but not a layout; this one is the library's:                      */
+/*   a row of nb = K/32 blocks (K a multiple of 256) is cut into segments of */
+/*   64 blocks; the last segment holds r = nb - 64*(nseg-1) blocks.          */
+/*   Segment s starts at byte 1152*s and holds 16*r_s + 128 bytes:          */
+/*     bytes 16*i .. 16*i+15: the 16 nibble bytes of block 64*s+i, as in    */
+/*       the Q4_0 block;                                                    */
+/*     then 32 little-endian 32-bit words; word l holds the fp16 scale of    */
+/*       block 64*s+l in its low half and that of block 64*s+32+l in its    */
+/*       high half; a half whose block does not exist is 0.                 */
+/*   Row bytes = 1152*(nseg-1) + 16*r_last + 128 (= 18*nb when 64 divides nb). */
+/* ---------------------------------------------------------------------- */
+int64_t orc_q4_0_seg_row_bytes(int64_t K)
+{
+    const int64_t nb = K / QK;
+    const int64_t nseg = (nb + 63) / 64;
+    const int64_t r_last = nb - 64 * (nseg - 1);
+    return 1152 * (nseg - 1) + 16 * r_last + 128;
+}
+
+void orc_repack_q4_0_seg(const uint8_t* W, int64_t O, int64_t K, uint8_t* out)
+{
+    const int64_t nb = K / QK;
+    const int64_t nseg = (nb + 63) / 64;
+    const int64_t rb = orc_q4_0_seg_row_bytes(K);
+    for (int64_t o = 0; o < O; ++o) {
+        const uint8_t* row = W + o * nb * 18;
+        uint8_t* dst = out + o * rb;
+        for (int64_t s = 0; s < nseg; ++s) {
+            const int64_t first = 64 * s;
+            const int64_t r = (nb - first < 64) ? nb - first : 64;
+            uint8_t* seg = dst + 1152 * s;
+            for (int64_t i = 0; i < r; ++i)
+                memcpy(seg + 16 * i, row + (first + i) * 18 + 2, 16);
+            uint8_t* words = seg + 16 * r;
+            for (int l = 0; l < 32; ++l) {
+                uint16_t lo = 0, hi = 0;
+                if (l < r)
+                    lo = rd_u16(row + (first + l) * 18);
+                if (32 + l < r)
+                    hi = rd_u16(row + (first + 32 + l) * 18);
+                wr_u16(words + 4 * l, lo);
+                wr_u16(words + 4 * l + 2, hi);
+            }
+        }
+    }
+}
+
 /* Element j (0..31) of a Q4_0 block, as the code q in 0..15. */
 static int q4_code(const uint8_t* blk, int j)
 {

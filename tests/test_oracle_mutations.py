@@ -31,6 +31,10 @@ MUTATIONS = {
     "add_dropped": ("v[j] = v[j] + an[i];", "v[j] = v[j];"),
     "add_before_mul": ("v[j] = v[j] + an[i];", "v[j] = v[j] + an[i] * (gamma ? gamma[i] : 1.0f);"),
     "add_row_stride_ignored": ("const float* an = add ? add + n * ldadd : NULL;", "const float* an = add;"),
+    "seg_scale_halves_swapped": ("wr_u16(words + 4 * l, lo);", "wr_u16(words + 4 * l, hi);"),
+    "seg_scales_in_block_order": ("if (32 + l < r)\n                    hi = rd_u16(row + (first + 32 + l) * 18);",
+                                  "if (2 * l + 1 < r)\n                    hi = rd_u16(row + (first + 2 * l + 1) * 18);"),
+    "seg_rows_unpadded": ("return 1152 * (nseg - 1) + 16 * r_last + 128;", "return nb * 18 + 128 * 0 + 0 * r_last;"),
 }
 
 

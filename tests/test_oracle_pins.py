@@ -423,3 +423,66 @@ def test_q8_add_rows_and_broadcast(orc):
         assert np.array_equal(rows[n], orc.quantize_q8_0(x[n], g, 1e-6, add=a[n])[0])
     assert np.array_equal(orc.quantize_q8_0(x, g, 1e-6, add=a[1]),
                           orc.quantize_q8_0(x, g, 1e-6, add=np.tile(a[1], (N, 1))))
+
+
+# ---------------------------------------------------------------- Q4_0 segment layout
+SEG_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "q4_0_seg_layout.json")
+
+
+def seg_golden():
+    with open(SEG_GOLDEN) as f:
+        return json.load(f)
+
+
+def test_seg_row_bytes_golden(orc):
+    g = seg_golden()["row_bytes"]
+    assert [orc.q4_0_seg_row_bytes(K) for K in g["K"]] == g["bytes"]
+
+
+def test_seg_layout_golden_spots(orc):
+    g = seg_golden()["one_row"]
+    K = g["K"]
+    nb = K // 32
+    row = np.zeros(nb * 18, dtype=np.uint8)
+    for b in range(nb):                      # the fixture's input rule
+        row[b * 18] = b
+        row[b * 18 + 1] = 0x10
+        for j in range(16):
+            row[b * 18 + 2 + j] = (5 * b + 3 * j + 1) % 256
+    out = orc.repack_q4_0_seg(row[None, :], K)[0]
+    assert out.shape[0] == 1408
+    for sp in g["spots"]:
+        at, want = sp["at"], sp["bytes"]
+        assert list(out[at:at + len(want)]) == want, sp["derivation"]
+
+
+@pytest.mark.parametrize("K", [256, 2304, 4096, 4352])
+def test_seg_layout_moves_every_byte_once(orc, K):
+    """Every block's 16 nibble bytes appear once, intact and in block order
+    within the row's nibble areas; every block's scale appears once among the
+    scale words; the remaining halves are zero."""
+    rng = np.random.default_rng(K)
+    O, nb = 3, K // 32
+    Wq = rng.integers(0, 256, size=(O, nb * 18), dtype=np.uint8)
+    Wq.reshape(O, nb, 18)[:, :, 1] = rng.integers(1, 0x7B, size=(O, nb), dtype=np.uint8)  # non-zero finite scales
+    out = orc.repack_q4_0_seg(Wq, K)
+    assert out.shape == (O, orc.q4_0_seg_row_bytes(K))
+    for o in range(O):
+        nib, scales = [], []
+        pos = 0
+        left = nb
+        while left > 0:
+            r = min(64, left)
+            nib.append(out[o, pos:pos + 16 * r].reshape(r, 16))
+            w = out[o, pos + 16 * r:pos + 16 * r + 128].copy().view(np.uint16).reshape(32, 2)
+            scales.append(w)
+            pos += 16 * r + 128
+            left -= r
+        assert pos == out.shape[1]
+        got_nib = np.concatenate(nib)
+        assert np.array_equal(got_nib, Wq[o].reshape(nb, 18)[:, 2:])
+        want_sc = Wq[o].reshape(nb, 18)[:, :2].copy().view(np.uint16)[:, 0]
+        halves = np.concatenate([s.reshape(-1) for s in scales])
+        nz = halves[halves != 0]
+        assert sorted(nz.tolist()) == sorted(want_sc.tolist())
+        assert np.count_nonzero(halves) == nb
