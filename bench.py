@@ -268,7 +268,7 @@ def time_oracle(wl, budget_s, row_frac, steps=None, warmup=1):
 
 # ---------------------------------------------------------------- GPU leg
 class DecodeStep:
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, layout="plain"):
         import torch
         from quantized_decode_gemv_rms_gb300 import qdg
         self.qdg = qdg
@@ -286,6 +286,14 @@ class DecodeStep:
                 qdg.quantize_q4_0(wd, Wq[r * (m.cols // 32) * 18:r1 * (m.cols // 32) * 18], O=r1 - r, K=m.cols)
                 del wd
             self.W[m.name] = Wq
+        # the segment layout of every matrix (repacked once, at load); the split
+        # route's GEMV reads it when layout == "seg", the per-launch timings always
+        self.layout = layout
+        self.Wr = {}
+        for m in wl.matrices:
+            Wr = torch.empty(qdg.q4_0_seg_nbytes(m.rows, m.cols), dtype=torch.uint8, device=device)
+            qdg.q4_0_repack_seg(self.W[m.name], Wr, m.rows, m.cols)
+            self.Wr[m.name] = Wr
         torch.cuda.synchronize()
         self.gamma = {tag: torch.from_numpy(synth.gamma(wl.seed, tag, K)).to(device)
                       for tag, K in wl.activations.items() if self.kinds[tag] == "norm"}
@@ -333,8 +341,19 @@ class DecodeStep:
             K = grp[0].cols
             g = self.gamma.get(tag) if self.kinds[tag] == "norm" else None
             qdg.qnorm_quantize_q8_0(xs[tag], g, self.wl.eps, self.xq[tag], K=K, N=1)
-            qdg.q4_0_q8_0_gemv_group([self.W[m.name] for m in grp], [self.y[m.name] for m in grp],
-                                     [m.rows for m in grp], self.xq[tag], K)
+            self.gemv_group(grp, self.xq[tag])
+
+    def gemv_group(self, grp, xq, Ws=None, layout=None):
+        """The grouped GEMV of one group on its prepared Q8_0 vector."""
+        layout = layout or self.layout
+        K = grp[0].cols
+        ys, Os = [self.y[m.name] for m in grp], [m.rows for m in grp]
+        if layout == "seg":
+            Ws = Ws if Ws is not None else [self.Wr[m.name] for m in grp]
+            self.qdg.q4_0s_q8_0_gemv_group(Ws, ys, Os, xq, K)
+        else:
+            Ws = Ws if Ws is not None else [self.W[m.name] for m in grp]
+            self.qdg.q4_0_q8_0_gemv_group(Ws, ys, Os, xq, K)
 
 def capture(fn, side, count=1):
     """CUDA graph of `count` calls of fn (on the side stream)."""
@@ -353,7 +372,7 @@ def bench_ours(args, wl, world, rank, local):
     device = torch.device("cuda", local)
     qdg.lib()
     qdg.qdg_set_option(qdg.QDG_OPT_PDL, 1 if args.pdl else 0)
-    step = DecodeStep(wl, device)
+    step = DecodeStep(wl, device, layout=args.layout)
     stream = torch.cuda.current_stream()
     nbytes = step_bytes(wl)
     fused = args.fused
@@ -377,22 +396,24 @@ def bench_ours(args, wl, world, rank, local):
     # kernels inside a graph, while consecutive graph launches serialise.
     with torch.cuda.stream(side):
         for fz in (fused, not fused):
-            before = [qdg.qdg_launch_count(i) for i in range(6)]
+            before = [qdg.qdg_launch_count(i) for i in range(8)]
 
             def steps(fz=fz):
                 for p in range(N_INPUT_SETS):
                     step.run(step.x_dev[p], fused=fz)
             graphs[fz] = capture(steps, side)
-            after = [qdg.qdg_launch_count(i) for i in range(6)]
-            counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(6)]
+            after = [qdg.qdg_launch_count(i) for i in range(8)]
+            counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(8)]
     stream.wait_stream(side)
     torch.cuda.synchronize()
     ng = len(step.groups)
-    assert counts[True][5] == ng and counts[True][0] == 0 and counts[True][1] == 0, counts
-    assert counts[False][0] == ng and counts[False][1] == ng and counts[False][5] == 0, counts
+    gk = 6 if args.layout == "seg" else 1          # launch counter of the split route's GEMV
+    assert counts[True][5] == ng and counts[True][0] == 0 and counts[True][gk] == 0, counts
+    assert counts[False][0] == ng and counts[False][gk] == ng and counts[False][5] == 0, counts
+    assert counts[False][7 - gk] == 0 and counts[True][7 - gk] == 0, counts
     fusion = {"route": "fused" if fused else "split",
               "per_step_launches": {"fused_norm_gemv": counts[fused][5], "quantize": counts[fused][0],
-                                    "gemv": counts[fused][1]}}
+                                    "gemv" + ("_seg" if args.layout == "seg" else ""): counts[fused][gk]}}
 
     def run_steps(n, fz=fused):
         """n decode steps: whole graphs of N_INPUT_SETS steps, the remainder eagerly."""
@@ -456,8 +477,9 @@ def bench_ours(args, wl, world, rank, local):
     # its own copy of the weights (C copies exceed three L2 sizes, so every
     # launch streams its weights from HBM)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    per_call = {"gemv": {}, "fused": {}}
-    launch_bytes = {"gemv": {}, "fused": {}}
+    kinds = ["gemv", "gemv_seg", "fused"]
+    per_call = {k: {} for k in kinds}
+    launch_bytes = {k: {} for k in kinds}
     for p_ in range(1):
         step.run(step.x_dev[0], fused=False)          # the Q8_0 vectors of input set 0
     torch.cuda.synchronize()
@@ -467,14 +489,15 @@ def bench_ours(args, wl, world, rank, local):
         K = grp[0].cols
         gbytes = sum(workloads.q4_0_bytes(m.rows, m.cols) for m in grp)
         copies = int(min(160, max(2, -(-3 * l2 // gbytes))))
-        Wc = [[step.W[m.name] for m in grp]] + [[step.W[m.name].clone() for m in grp] for _ in range(copies - 1)]
-        for kind in ("gemv", "fused"):
-            def one(c, kind=kind):
+        for kind in kinds:
+            src = step.Wr if kind == "gemv_seg" else step.W
+            Wc = [[src[m.name] for m in grp]] + [[src[m.name].clone() for m in grp] for _ in range(copies - 1)]
+
+            def one(c, kind=kind, Wc=Wc):
                 if kind == "fused":
                     step.run_group(grp, step.x_dev[0], Ws=Wc[c])
                 else:
-                    qdg.q4_0_q8_0_gemv_group(Wc[c], [step.y[m.name] for m in grp], [m.rows for m in grp],
-                                             step.xq[tag], K)
+                    step.gemv_group(grp, step.xq[tag], Ws=Wc[c], layout="seg" if kind == "gemv_seg" else "plain")
             with torch.cuda.stream(side):
                 gr = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(gr, stream=side):
@@ -490,12 +513,12 @@ def bench_ours(args, wl, world, rank, local):
                 a1.record(side)
                 side.synchronize()
             per_call[kind][name] = a0.elapsed_time(a1) * 1e3 / (3 * copies)
-            del gr
+            del gr, Wc
+            torch.cuda.empty_cache()
         xbytes = 4 * K * (2 if grp[0].source.startswith("norm:") else 1)
         launch_bytes["fused"][name] = gbytes + xbytes + sum(4 * m.rows for m in grp)
         launch_bytes["gemv"][name] = gbytes + workloads.q8_0_bytes(1, K) + sum(4 * m.rows for m in grp)
-        del Wc
-        torch.cuda.empty_cache()
+        launch_bytes["gemv_seg"][name] = launch_bytes["gemv"][name]
     torch.cuda.synchronize()
     gbs_per_call = {kind: {n: launch_bytes[kind][n] / (per_call[kind][n] * 1e-6) / 1e9 for n in per_call[kind]}
                     for kind in per_call}
@@ -522,13 +545,14 @@ def bench_ours(args, wl, world, rank, local):
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
 
     peaks, peak_src = measured_peaks()
-    kind = "fused" if fused else "gemv"
+    kind = "fused" if fused else ("gemv_seg" if args.layout == "seg" else "gemv")
     kern_bytes = sum(launch_bytes[kind].values())
     # the dominant kernel's average launch from the per-launch graphs above
     achieved = kern_bytes / (sum(per_call[kind].values()) * 1e-6) / 1e9
-    kernel = ("gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)" if fused
-              else "gemv_kernel (q4_0_q8_0_gemv_group)")
-    traffic = ncu_traffic("gemv.cu")
+    kernel = {"fused": "gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)",
+              "gemv": "gemv_kernel (q4_0_q8_0_gemv_group)",
+              "gemv_seg": "gemv_seg_kernel (q4_0s_q8_0_gemv_group)"}[kind]
+    traffic = ncu_traffic("gemv_seg.cu" if kind == "gemv_seg" else "gemv.cu")
     roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)" if peak_src == "measured"
@@ -548,7 +572,9 @@ def bench_ours(args, wl, world, rank, local):
         "config": {"workload": wl.name, "batch": 1, "matrices": {m.name: [m.rows, m.cols] for m in wl.matrices},
                    "bytes_per_step": nbytes, "l2": "inputs larger than L2 (419 MB of weights per step vs 129 MB L2)",
                    "route": ("fused: one RMSNorm->Q8_0->GEMV launch per group" if fused else
-                             "split: quantize kernel + grouped GEMV launch per group") +
+                             "split: quantize kernel + grouped GEMV launch per group" +
+                             ("; weights in the segment layout (repacked at load)" if args.layout == "seg"
+                              else "; weights in plain Q4_0 blocks")) +
                             "; groups q+k+v, o, gate+up, down, head in dependency order",
                    "launch": ((f"cuda graph of {N_INPUT_SETS} steps" if args.graph else "eager") +
                               (" + PDL" if args.pdl else "")),
@@ -557,6 +583,7 @@ def bench_ours(args, wl, world, rank, local):
         "us_per_call": {k: {n: round(v, 2) for n, v in d.items()} for k, d in per_call.items()},
         "gbs_per_call": {k: {n: round(v, 1) for n, v in d.items()} for k, d in gbs_per_call.items()},
         "per_call_note": ("one launch per group of projections sharing an input (gemv: on a prepared Q8_0 vector; "
+                          "gemv_seg: the same on weights in the segment layout; "
                           "fused: norm+quantize+GEMV); graph of back-to-back launches on distinct weight copies "
                           "(> 3 x L2), PDL as configured"),
         "other_route": {"route": "split" if fused else "fused",
@@ -688,6 +715,9 @@ def main():
     ap.add_argument("--fused", action="store_true",
                     help="time the fused route (one norm+quantize+GEMV launch per group) as the main line; "
                          "the default main line is quantize kernel + grouped GEMV per group")
+    ap.add_argument("--layout", choices=["seg", "plain"], default="plain",
+                    help="weight layout the split route's GEMV reads: plain = Q4_0 blocks as stored (default), "
+                         "seg = segment layout repacked at load")
     ap.add_argument("--pdl", action="store_true", default=True)
     ap.add_argument("--no-pdl", dest="pdl", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")

@@ -249,6 +249,54 @@ QDG_API int quantize_q4_0(const float* w, int64_t ldw, int64_t O, int64_t K, voi
                   qdg_stream_t stream);
 
 /*
+ * Segment layout of Q4_0 weights (load-time repack).  GGML's CPU back end
+ * rearranges Q4 weights once, when they are loaded, for its own kernels
+ * [GGML: Backend abstraction and hardware acceleration, section "How build
+ * switches become runtime capabilities", build-option table,
+ * GGML_CPU_REPACK]; the pages give no layout.  This library's GPU layout
+ * keeps each row contiguous and splits it into segments of 64 blocks:
+ * segment s starts at byte 1152*s and holds the 16 nibble bytes of each of
+ * its r blocks (block 64s+i at byte 16*i, bytes as in the Q4_0 block), then
+ * 32 little-endian words, word l = fp16 scale of block 64s+l (low half) and
+ * of block 64s+32+l (high half), 0 where that block does not exist.
+ * Row bytes = 1152*(nseg-1) + 16*r_last + 128 (18*K/32 when 2048 divides K).
+ * Every product of this layout gives the same exact block sums as the plain
+ * layout; rows of several matrices that read one input (gate and up) may be
+ * repacked into one buffer back to back and multiplied as one matrix.
+ */
+
+/* Bytes of one row in the segment layout; QDG_EINVAL (K <= 0) or QDG_ESHAPE
+ * (K not a multiple of 256 or above 32768). */
+QDG_API int64_t q4_0_seg_row_bytes(int64_t K);
+
+/*
+ * q4_0_repack_seg -- W [O][K/32] Q4_0 (2-byte aligned) -> Wr [O][row bytes]
+ * in the segment layout (16-byte aligned, caller-owned, not overlapping W).
+ * A byte rearrangement, bit-exact; runs once at load time.  K multiple of
+ * 256, <= 32768.  Asynchronous on `stream`.
+ */
+QDG_API int q4_0_repack_seg(const void* W, void* Wr, int64_t O, int64_t K, qdg_stream_t stream);
+
+/*
+ * q4_0s_q8_0_gemv -- q4_0_q8_0_gemv on weights in the segment layout.
+ * Wr  [O][q4_0_seg_row_bytes(K)], 16-byte aligned.  xq [K/32] Q8_0, 2-byte
+ * aligned.  y [O] fp32 (overwritten).  K multiple of 256, <= 32768;
+ * 1 <= O < 2^31.  Each lane reads its blocks' nibbles with 16-byte loads and
+ * their scales with one 4-byte load, issued four row segments ahead, straight
+ * into registers; deterministic (fixed reduction order).
+ */
+QDG_API int q4_0s_q8_0_gemv(const void* Wr, const void* xq, float* y, int64_t O, int64_t K,
+                            qdg_stream_t stream);
+
+/*
+ * q4_0s_q8_0_gemv_group -- q4_0s_q8_0_gemv for up to 4 segment-layout
+ * matrices reading one Q8_0 vector, in one launch (argument rules as
+ * q4_0_q8_0_gemv_group).  Bit-identical to one call per matrix.
+ */
+QDG_API int q4_0s_q8_0_gemv_group(const void* const* Wr, float* const* y, const int64_t* O, int count,
+                                  const void* xq, int64_t K, qdg_stream_t stream);
+
+/*
  * qdg_device_status -- synchronise `stream`, then read and clear the device
  * flags of every kernel of this library on the current device.  Returns
  * QDG_OK, QDG_ETIMEOUT (a bounded wait gave up; that call's output is
@@ -276,7 +324,8 @@ QDG_API int qdg_set_option(int option, int64_t value);
 /*
  * qdg_launch_count -- number of kernels this library has launched in this
  * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
- * 4 weight quantize, 5 fused norm+gemv, -1 total.  Lets a caller check that the fused kernel
+ * 4 weight quantize, 5 fused norm+gemv, 6 segment-layout gemv, 7 repack,
+ * -1 total.  Lets a caller check that the fused kernel
  * is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);
@@ -285,7 +334,8 @@ QDG_API int64_t qdg_launch_count(int which);
  * qdg_debug_block_sums -- test hook.  Runs the production inner loop of one
  * product path and writes the exact per-block integer sums
  * isum[n][o][b] = sum_j (q_w - 8) * q_x  (int32 [N][O][K/32]) instead of y.
- * path: 0 = gemv (N must be 1), 1 = small-N, 2 = prefill gemm (N = T tokens).
+ * path: 0 = gemv (N must be 1), 1 = small-N, 2 = prefill gemm (N = T tokens),
+ * 3 = segment-layout gemv (W in the segment layout, N must be 1).
  * Same argument rules as the corresponding entry point.
  */
 QDG_API int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum, int64_t O,

@@ -1,0 +1,366 @@
+// gemv_seg.cu -- batch-1 Q4_0 x Q8_0 matrix-vector product on weights held in
+// the segment layout, and the load-time repack that produces that layout.
+//
+// The CPU back end of GGML rearranges Q4 weights once, when they are loaded,
+// into a layout its dot-product kernels read faster [GGML: Backend
+// abstraction and hardware acceleration, section "How build switches become
+// runtime capabilities", build-option table, GGML_CPU_REPACK].  This file is
+// the GPU counterpart.  The plain Q4_0 block is 18 bytes, so its nibbles are
+// only 2-byte aligned and a coalesced reader has to pass them through shared
+// memory; the segment layout separates nibbles from scales so that every
+// lane reads its own blocks straight into registers:
+//   a row of nb = K/32 blocks is cut into segments of 64 blocks; segment s
+//   starts at byte 1152*s and holds the 16 nibble bytes of each of its r
+//   blocks (block 64s+i at 16*i, bytes as in the Q4_0 block), then 32 words,
+//   word l = fp16 scale of block 64s+l (low half) and of block 64s+32+l (high
+//   half), 0 where that block does not exist.  Row bytes = 1152*(nseg-1) +
+//   16*r_last + 128, equal to 18*nb when 64 divides nb.
+//
+// GEMV design (same row/segment work split as the plain-layout kernel):
+//   * Each CTA (16 warps, one per SM) owns a contiguous range of rows; warp w
+//     works on segment w % nseg of rows slot, slot + nslots, ...
+//   * Lane l of a warp owns blocks 64s+l and 64s+32+l of its segment: two
+//     coalesced 16-byte nibble loads (512 contiguous bytes per warp each) and
+//     one 4-byte scale-word load per row-segment, issued kDepth row-segments
+//     ahead of use; the matching Q8_0 activations stay in registers.
+//   * Exact block sums with dp4a (minus 8 * sum(q_x)), scaled by d_w * d_x,
+//     warp shuffle reduction, segment partials combined per row in a fixed
+//     order (deterministic).
+//   * Programmatic dependent launch: the first row-segments of W are
+//     requested before the kernel waits for the preceding grid.
+#include "common.cuh"
+
+#include <algorithm>
+
+namespace qdg {
+
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kDepth = 4;                   // row-segments in flight per warp (the consume loop is unrolled by 4)
+constexpr int kSegStride = 1152;            // bytes from one segment to the next: 64 x 16 nibble bytes + 128
+constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
+constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
+constexpr int kMaxGroup = 4;
+constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
+
+struct Plan {
+    int rowbytes;   // bytes of one row in the segment layout
+    int nb;         // K/32
+    int nseg;       // segments per row, ceil(nb / 64)
+    int rlast;      // blocks in the last segment (8..64)
+    int nslots;     // rows in flight per CTA = kWarps / nseg
+    int rch;        // rows per chunk (partial-sum buffer capacity), multiple of nslots
+};
+
+int64_t seg_row_bytes(int64_t K) {
+    const int64_t nb = K / 32;
+    const int64_t nseg = (nb + 63) / 64;
+    return kSegStride * (nseg - 1) + 16 * (nb - 64 * (nseg - 1)) + 128;
+}
+
+Plan make_plan(int64_t K) {
+    Plan p{};
+    p.nb = static_cast<int>(K / 32);
+    p.nseg = (p.nb + 63) / 64;
+    p.rlast = p.nb - 64 * (p.nseg - 1);
+    p.rowbytes = static_cast<int>(seg_row_bytes(K));
+    p.nslots = kWarps / p.nseg;
+    p.rch = (kPartFloats / p.nseg) / p.nslots * p.nslots;
+    return p;
+}
+
+__device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream4(const uint8_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Sum over one block of (code) * q_x, codes unsigned 0..15: low nibbles of
+// word i are elements 4i..4i+3, high nibbles elements 16+4i..16+4i+3.
+__device__ __forceinline__ int block_dot(const uint4& q, const uint32_t* x) {
+    int acc = 0;
+    acc = __dp4a(static_cast<int>(q.x & kNibbles), static_cast<int>(x[0]), acc);
+    acc = __dp4a(static_cast<int>((q.x >> 4) & kNibbles), static_cast<int>(x[4]), acc);
+    acc = __dp4a(static_cast<int>(q.y & kNibbles), static_cast<int>(x[1]), acc);
+    acc = __dp4a(static_cast<int>((q.y >> 4) & kNibbles), static_cast<int>(x[5]), acc);
+    acc = __dp4a(static_cast<int>(q.z & kNibbles), static_cast<int>(x[2]), acc);
+    acc = __dp4a(static_cast<int>((q.z >> 4) & kNibbles), static_cast<int>(x[6]), acc);
+    acc = __dp4a(static_cast<int>(q.w & kNibbles), static_cast<int>(x[3]), acc);
+    acc = __dp4a(static_cast<int>((q.w >> 4) & kNibbles), static_cast<int>(x[7]), acc);
+    return acc;
+}
+
+// One lane's share of one row-segment.
+struct Entry {
+    uint4 a, b;     // nibbles of blocks 64s+l and 64s+32+l
+    uint32_t sc;    // their scales (low, high half)
+};
+
+struct Args {
+    const uint8_t* Wg[kMaxGroup];   // stacked matrices sharing one input
+    float* yg[kMaxGroup];
+    int64_t start[kMaxGroup];
+    int ng;
+    const uint8_t* xq;
+    int32_t* dbg;
+    int64_t O;
+};
+
+// Q8_0 block b of the activations: scale and the 32 codes as 8 words, from
+// 2-byte loads (a 34-byte block is only 2-byte aligned).
+__device__ __forceinline__ void load_act(const uint8_t* xq, int b, uint32_t* x, float& d, int& sum) {
+    const unsigned short* h = reinterpret_cast<const unsigned short*>(xq + static_cast<size_t>(b) * 34);
+    d = half_bits_to_float(__ldg(h));
+    sum = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        x[i] = static_cast<uint32_t>(__ldg(h + 1 + 2 * i)) | (static_cast<uint32_t>(__ldg(h + 2 + 2 * i)) << 16);
+        sum = __dp4a(static_cast<int>(x[i]), 0x01010101, sum);
+    }
+}
+
+// 96 registers a thread: one CTA of 512 threads leaves room on its SM for a
+// CTA of the quantize kernel that prepares the next input.
+template <bool kDebug>
+__global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, const __grid_constant__ Plan plan) {
+    __shared__ float part[kPartFloats];
+    const int64_t O = a.O;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nseg = plan.nseg;
+    const int seg = warp % nseg;
+    const int slot = warp / nseg;
+    const bool worker = slot < plan.nslots;
+    const int r = (seg == nseg - 1) ? plan.rlast : 64;     // blocks in this warp's segment
+    const bool has_a = worker && lane < r;
+    const bool has_b = worker && lane + 32 < r;
+    const int nib_off = seg * kSegStride + 16 * lane;      // block 64s+l; block 64s+32+l is 512 bytes on
+    const int sc_off = seg * kSegStride + 16 * r + 4 * lane;
+
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * O / gridDim.x;
+    const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * O / gridDim.x;
+    const int nrows = static_cast<int>(r1 - r0);
+
+    pdl_trigger();
+
+    Entry pipe[kDepth] = {};
+    auto load_seg = [&](int64_t row, Entry& e) {
+        int g = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxGroup; ++i)
+            if (i < a.ng && row >= a.start[i]) g = i;
+        const uint8_t* base = a.Wg[g] + (row - a.start[g]) * plan.rowbytes;
+        if (has_a) e.a = ldg_stream16(base + nib_off);
+        if (has_b) e.b = ldg_stream16(base + nib_off + 512);
+        e.sc = ldg_stream4(base + sc_off);
+    };
+    auto fill = [&](int64_t c0, int crows) {
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) {
+            const int ri = slot + d * plan.nslots;
+            if (ri < crows) load_seg(c0 + ri, pipe[d]);
+        }
+    };
+
+    if (worker) fill(r0, min(nrows, plan.rch));
+    if (threadIdx.x == 0) {
+        int64_t row = r0 + static_cast<int64_t>(kDepth) * plan.nslots;
+        int64_t budget = kL2Prefetch / plan.rowbytes;
+        for (int g = 0; g < a.ng && budget > 0; ++g) {
+            const int64_t gend = (g + 1 < a.ng) ? a.start[g + 1] : O;
+            if (row >= gend || row >= r1) continue;
+            const int64_t n = min(min(gend, r1) - row, budget);
+            if (n > 0) {
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.Wg[g] + (row - a.start[g]) *
+                                                                                           plan.rowbytes),
+                             "r"(static_cast<uint32_t>(n * plan.rowbytes))
+                             : "memory");
+                row += n;
+                budget -= n;
+            }
+        }
+    }
+
+    pdl_wait();
+
+    uint32_t xa[8], xb[8];
+    float dxa = 0.0f, dxb = 0.0f;
+    int sa = 0, sb = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) xa[i] = xb[i] = 0u;
+    if (has_a) load_act(a.xq, seg * 64 + lane, xa, dxa, sa);
+    if (has_b) load_act(a.xq, seg * 64 + 32 + lane, xb, dxb, sb);
+
+    auto consume = [&](int64_t c0, int crows, int ri, Entry& entry) {
+        const Entry cur = entry;
+        const int ahead = ri + kDepth * plan.nslots;
+        if (ahead < crows) load_seg(c0 + ahead, entry);
+        // lanes without a block hold zero activations and zero scales
+        const int ia = block_dot(cur.a, xa) - 8 * sa;
+        const int ib = block_dot(cur.b, xb) - 8 * sb;
+        const float dwa = half_bits_to_float(cur.sc);
+        const float dwb = half_bits_to_float(cur.sc >> 16);
+        float acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
+        acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
+        if (kDebug) {
+            int32_t* d = a.dbg + (c0 + ri) * plan.nb + seg * 64 + lane;
+            if (has_a) d[0] = ia;
+            if (has_b) d[32] = ib;
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) part[ri * nseg + seg] = acc;
+    };
+
+    for (int64_t c0 = r0; c0 < r1; c0 += plan.rch) {
+        const int crows = static_cast<int>((r1 - c0) < plan.rch ? (r1 - c0) : plan.rch);
+        if (worker) {
+            if (c0 != r0) fill(c0, crows);
+            const int step = plan.nslots;
+            for (int ri = slot; ri < crows; ri += kDepth * step) {
+                consume(c0, crows, ri, pipe[0]);
+                if (ri + step < crows) consume(c0, crows, ri + step, pipe[1]);
+                if (ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[2]);
+                if (ri + 3 * step < crows) consume(c0, crows, ri + 3 * step, pipe[3]);
+            }
+        }
+        __syncthreads();
+        if (!kDebug) {
+            for (int t = threadIdx.x; t < crows; t += kThreads) {
+                float v = part[t * nseg];
+                for (int g = 1; g < nseg; ++g) v = __fadd_rn(v, part[t * nseg + g]);
+                const int64_t row = c0 + t;
+                int g = 0;
+#pragma unroll
+                for (int i = 1; i < kMaxGroup; ++i)
+                    if (i < a.ng && row >= a.start[i]) g = i;
+                a.yg[g][row - a.start[g]] = v;
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Repack: one warp per (row, segment).  Lane l moves the nibbles of blocks
+// 64s+l and 64s+32+l (eight 2-byte loads each, one 16-byte store) and writes
+// scale word l.
+__global__ void __launch_bounds__(256) repack_seg_kernel(const uint8_t* __restrict__ W, uint8_t* __restrict__ out,
+                                                         int64_t O, int nb, int nseg, int64_t rowbytes) {
+    const int64_t gw = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= O * nseg) return;
+    const int64_t o = gw / nseg;
+    const int s = static_cast<int>(gw - o * nseg);
+    const int first = 64 * s;
+    const int r = min(64, nb - first);
+    const uint8_t* row = W + o * static_cast<int64_t>(nb) * 18;
+    uint8_t* seg = out + o * rowbytes + static_cast<int64_t>(kSegStride) * s;
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        if (i >= r) continue;
+        const unsigned short* blk = reinterpret_cast<const unsigned short*>(row + static_cast<int64_t>(first + i) * 18);
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = static_cast<uint32_t>(blk[1 + 2 * k]) | (static_cast<uint32_t>(blk[2 + 2 * k]) << 16);
+        *reinterpret_cast<uint4*>(seg + 16 * i) = make_uint4(w[0], w[1], w[2], w[3]);
+        if (h == 0)
+            lo = blk[0];
+        else
+            hi = blk[0];
+    }
+    *reinterpret_cast<uint32_t*>(seg + 16 * r + 4 * lane) = lo | (hi << 16);
+}
+
+}  // namespace
+
+int gemv_seg_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq,
+                          int64_t K, cudaStream_t stream, int32_t* dbg) {
+    if (!W || !O || !xq || (!y && !dbg)) return QDG_EINVAL;
+    if (count < 1 || count > kMaxGroup || K <= 0) return QDG_EINVAL;
+    if (dbg && count != 1) return QDG_EINVAL;
+    if (K % 256 != 0 || K > 32768) return QDG_ESHAPE;
+    if (!aligned(xq, 2) || !aligned(dbg, 4)) return QDG_EALIGN;
+    Args a{};
+    int64_t total = 0;
+    for (int g = 0; g < count; ++g) {
+        if (!W[g] || (!dbg && !y[g]) || O[g] <= 0) return QDG_EINVAL;
+        if (!aligned(W[g], 16) || (y && !aligned(y[g], 4))) return QDG_EALIGN;
+        a.Wg[g] = static_cast<const uint8_t*>(W[g]);
+        a.yg[g] = y ? y[g] : nullptr;
+        a.start[g] = total;
+        total += O[g];
+    }
+    if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
+    const DeviceInfo dev = device_info();
+    if (dev.device < 0) return QDG_ECUDA;
+    const Plan plan = make_plan(K);
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
+    a.ng = count;
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.dbg = dbg;
+    a.O = total;
+    cudaError_t e;
+    if (dbg)
+        e = launch(gemv_seg_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, false, a, plan);
+    else
+        e = launch(gemv_seg_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
+    if (e != cudaSuccess) return QDG_ECUDA;
+    count_launch(6);
+    return QDG_OK;
+}
+
+int gemv_seg_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
+                    int32_t* dbg) {
+    float* ys[1] = {y};
+    return gemv_seg_launch_group(&W, y ? ys : nullptr, &O, 1, xq, K, stream, dbg);
+}
+
+}  // namespace qdg
+
+using namespace qdg;
+
+extern "C" int64_t q4_0_seg_row_bytes(int64_t K) {
+    if (K <= 0) return QDG_EINVAL;
+    if (K % 256 != 0 || K > 32768) return QDG_ESHAPE;
+    return seg_row_bytes(K);
+}
+
+extern "C" int q4_0_repack_seg(const void* W, void* Wr, int64_t O, int64_t K, qdg_stream_t stream) {
+    if (!W || !Wr || O <= 0 || K <= 0) return QDG_EINVAL;
+    if (K % 256 != 0 || K > 32768) return QDG_ESHAPE;
+    if (!aligned(W, 2) || !aligned(Wr, 16)) return QDG_EALIGN;
+    const int nb = static_cast<int>(K / 32);
+    const int nseg = (nb + 63) / 64;
+    const int64_t warps = O * nseg;
+    const int64_t blocks = (warps + 7) / 8;
+    if (blocks > 0x7fffffff) return QDG_ESHAPE;
+    repack_seg_kernel<<<static_cast<unsigned>(blocks), 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(W), static_cast<uint8_t*>(Wr), O, nb, nseg, seg_row_bytes(K));
+    if (cudaGetLastError() != cudaSuccess) return QDG_ECUDA;
+    count_launch(7);
+    return QDG_OK;
+}
+
+extern "C" int q4_0s_q8_0_gemv(const void* Wr, const void* xq, float* y, int64_t O, int64_t K,
+                               qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    return gemv_seg_launch(Wr, xq, y, O, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" int q4_0s_q8_0_gemv_group(const void* const* Wr, float* const* y, const int64_t* O, int count,
+                                     const void* xq, int64_t K, qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    return gemv_seg_launch_group(Wr, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}

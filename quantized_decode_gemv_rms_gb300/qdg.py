@@ -65,6 +65,10 @@ def lib() -> ctypes.CDLL:
             sig["q4_0_q8_0_gemm"] = ([p, p, p, i64, i64, i64, i64, p, i64, p], i32)
             sig["q4_0_q8_0_gemm_workspace_bytes"] = ([i64, i64], i64)
             sig["q4_0_q8_0_gemm_static"] = ([p, p, p, i64, i64, i64, i64, p], i32)
+            sig["q4_0_seg_row_bytes"] = ([i64], i64)
+            sig["q4_0_repack_seg"] = ([p, p, i64, i64, p], i32)
+            sig["q4_0s_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
+            sig["q4_0s_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
                 fn.argtypes = args
@@ -154,6 +158,37 @@ def q4_0_q8_0_gemv_group(Ws, ys, Os, xq, K: int, stream=None) -> None:
     y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in ys])
     O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
     _check(lib().q4_0_q8_0_gemv_group(W_arr, y_arr, O_arr, n, _ptr(xq), K, _stream(stream)), "q4_0_q8_0_gemv_group")
+
+
+def q4_0_seg_row_bytes(K: int) -> int:
+    """Bytes of one row of K weights in the segment layout."""
+    r = int(lib().q4_0_seg_row_bytes(K))
+    _check(min(r, 0), "q4_0_seg_row_bytes")
+    return r
+
+
+def q4_0_seg_nbytes(O: int, K: int) -> int:
+    return O * q4_0_seg_row_bytes(K)
+
+
+def q4_0_repack_seg(W, Wr, O: int, K: int, stream=None) -> None:
+    """Q4_0 rows -> segment layout (load time, bit-exact rearrangement)."""
+    _check(lib().q4_0_repack_seg(_ptr(W), _ptr(Wr), O, K, _stream(stream)), "q4_0_repack_seg")
+
+
+def q4_0s_q8_0_gemv(Wr, xq, y, O: int, K: int, stream=None) -> None:
+    """y = W * x with W in the segment layout."""
+    _check(lib().q4_0s_q8_0_gemv(_ptr(Wr), _ptr(xq), _ptr(y), O, K, _stream(stream)), "q4_0s_q8_0_gemv")
+
+
+def q4_0s_q8_0_gemv_group(Ws, ys, Os, xq, K: int, stream=None) -> None:
+    """Segment-layout GEMV for up to 4 matrices sharing one Q8_0 vector."""
+    n = len(Ws)
+    W_arr = (ctypes.c_void_p * n)(*[_ptr(w) for w in Ws])
+    y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in ys])
+    O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
+    _check(lib().q4_0s_q8_0_gemv_group(W_arr, y_arr, O_arr, n, _ptr(xq), K, _stream(stream)),
+           "q4_0s_q8_0_gemv_group")
 
 
 def q4_0_gemv_rmsnorm(W, x, gamma, eps: float, y, O: int, K: int, xq_out=None, stream=None) -> None:

@@ -25,7 +25,8 @@ def L():
 def test_header_declares_entry_points():
     names = declared_symbols()
     for must in ("qnorm_quantize_q8_0", "qnorm_add_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
-                 "q4_0_q8_0_gemm_workspace_bytes", "quantize_q4_0",
+                 "q4_0_q8_0_gemm_workspace_bytes", "quantize_q4_0", "q4_0_repack_seg", "q4_0s_q8_0_gemv",
+                 "q4_0s_q8_0_gemv_group", "q4_0_seg_row_bytes",
                  "qdg_device_status", "qdg_status_string"):
         assert must in names
 
@@ -79,6 +80,36 @@ def test_gemv_host_validation(L):
     assert f(A16, A16, A16, 8, 65536, None) == -3     # K beyond the maximum
     assert f(A2, A16, A16, 8, 256, None) == -2        # W not 16-byte aligned
     assert f(A16, A2, A16, 8, 256, None) == -2        # xq not 4-byte aligned
+
+
+def test_seg_layout_host_validation(L):
+    import oracle
+    for K in (256, 2304, 4096, 4352, 14336, 32768):
+        assert L.q4_0_seg_row_bytes(K) == oracle.q4_0_seg_row_bytes(K)
+    assert L.q4_0_seg_row_bytes(0) == -1
+    assert L.q4_0_seg_row_bytes(128) == -3
+    assert L.q4_0_seg_row_bytes(65536) == -3
+    r = L.q4_0_repack_seg
+    assert r(None, A16, 8, 256, None) == -1
+    assert r(A16, None, 8, 256, None) == -1
+    assert r(A16, A16, 0, 256, None) == -1
+    assert r(A16, A16, 8, 96, None) == -3          # K % 256
+    assert r(A16 + 1, A16, 8, 256, None) == -2     # W not 2-byte aligned
+    assert r(A16, A2, 8, 256, None) == -2          # Wr not 16-byte aligned
+    f = L.q4_0s_q8_0_gemv
+    assert f(None, A16, A16, 8, 256, None) == -1
+    assert f(A16, A16, None, 8, 256, None) == -1
+    assert f(A16, A16, A16, 0, 256, None) == -1
+    assert f(A16, A16, A16, 8, 128, None) == -3
+    assert f(A16, A16, A16, 8, 65536, None) == -3
+    assert f(A2, A16, A16, 8, 256, None) == -2     # Wr not 16-byte aligned
+    assert f(A16, A16 + 1, A16, 8, 256, None) == -2  # xq not 2-byte aligned
+    g = L.q4_0s_q8_0_gemv_group
+    W = (ctypes.c_void_p * 5)(*([A16] * 5))
+    Y = (ctypes.c_void_p * 5)(*([A16] * 5))
+    O = (ctypes.c_int64 * 5)(*([8] * 5))
+    assert g(W, Y, O, 5, A16, 256, None) == -1    # more than 4 matrices
+    assert g(W, Y, O, 0, A16, 256, None) == -1
 
 
 def test_fused_host_validation(L):
@@ -164,11 +195,12 @@ def test_options_and_counters(L):
     assert L.qdg_set_option(1, 2) == -1
     assert L.qdg_set_option(1, 0) == 0
     assert L.qdg_launch_count(-1) >= 0
-    assert L.qdg_launch_count(7) == -1
-    assert L.qdg_launch_count(5) >= 0
+    assert L.qdg_launch_count(8) == -1
+    assert L.qdg_launch_count(7) >= 0
     assert L.qdg_debug_block_sums(A16, A16, None, 8, 256, 1, 0, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 1, 9, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 0, None) == -1   # gemv path needs N == 1
+    assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 3, None) == -1   # so does the segment-layout gemv
 
 
 def test_binding_names_match_header():

@@ -1,0 +1,159 @@
+"""GPU parity of the segment layout (load-time repack of Q4_0 rows) and of the
+GEMV that reads it: the repack byte for byte against the oracle's, exact
+per-block integer sums, fp32 outputs within 1e-5 * sum_b |d_w d_x isum_b|,
+grouped and concatenated matrices, PDL on/off."""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_decode_gemv_rms_gb300 import qdg, synth
+from helpers import assert_within_tol, empty_u8, to_dev, to_host, torch_cuda
+
+pytestmark = pytest.mark.gpu
+
+
+def problem(seed, O, K, outliers=0.0):
+    w = synth.weights(seed, "W", O, K)
+    x = synth.activations(seed, "x", 1, K, outlier_frac=outliers)
+    gam = synth.gamma(seed, "g", K)
+    return oracle.quantize_q4_0(w), oracle.quantize_q8_0(x, gam, 1e-6)
+
+
+def gpu_repack(Wq, O, K):
+    torch = torch_cuda()
+    Wr = empty_u8(qdg.q4_0_seg_nbytes(O, K))
+    Wr.fill_(0xA5)
+    qdg.q4_0_repack_seg(to_dev(Wq), Wr, O, K)
+    torch.cuda.synchronize()
+    return to_host(Wr).reshape(O, -1)
+
+
+def gpu_gemv_seg(Wr, xq, O, K):
+    torch = torch_cuda()
+    y = torch.full((O,), float("nan"), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemv(to_dev(Wr), to_dev(xq), y, O, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    return to_host(y)
+
+
+# one segment of 8 blocks (K = 256); ragged last segments (2304, 4352, 6400);
+# whole segments (4096, 14336, 32768 = 16 segments, one row slot per CTA);
+# row counts below, at and above the SM count and ragged.
+SEG_SHAPES = [(1, 256), (300, 256), (37, 2304), (1000, 2048), (152, 4096), (153, 4096), (17, 4352),
+              (600, 6400), (4096, 14336), (64, 32768), (3000, 768)]
+
+
+@pytest.mark.parametrize("O,K", SEG_SHAPES)
+def test_repack_matches_oracle_bytes(O, K):
+    Wq, _ = problem(O + 5 * K, O, K)
+    assert np.array_equal(gpu_repack(Wq, O, K), oracle.repack_q4_0_seg(Wq, K))
+
+
+@pytest.mark.parametrize("O,K", SEG_SHAPES)
+def test_seg_gemv_block_sums_exact(O, K):
+    Wq, xq = problem(O * 7 + K, O, K)
+    Wr = oracle.repack_q4_0_seg(Wq, K)
+    torch = torch_cuda()
+    isum = torch.full((1, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(to_dev(Wr), to_dev(xq), isum, O, K, 1, 3)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(isum), oracle.block_sums(Wq, xq, K))
+
+
+@pytest.mark.parametrize("O,K", SEG_SHAPES)
+def test_seg_gemv_output_within_tolerance(O, K):
+    Wq, xq = problem(O * 11 + K, O, K, outliers=0.01)
+    y = gpu_gemv_seg(oracle.repack_q4_0_seg(Wq, K), xq, O, K)
+    _, y64, S = oracle.matvec(Wq, xq, K, threads=8)
+    assert_within_tol(y[None, :], y64, S)
+
+
+def test_seg_gemv_special_blocks():
+    """All-zero codes -> -8 d_w sum(q_x); all-8 -> 0; all-15 -> 7 d_w sum(q_x)."""
+    K, O = 2304, 3
+    rng = np.random.default_rng(2)
+    xq = oracle.quantize_q8_0(rng.standard_normal((1, K)).astype(np.float32), None)
+    W = np.zeros((O, K // 32 * 18), dtype=np.uint8)
+    d = np.array([np.float16(0.25).view(np.uint16)], dtype=np.uint16).view(np.uint8)
+    for r, byte in enumerate((0x00, 0x88, 0xFF)):
+        for b in range(K // 32):
+            W[r, b * 18:b * 18 + 2] = d
+            W[r, b * 18 + 2:b * 18 + 18] = byte
+    y = gpu_gemv_seg(oracle.repack_q4_0_seg(W, K), xq, O, K)
+    _, y64, S = oracle.matvec(W, xq, K)
+    assert_within_tol(y[None, :], y64, S)
+    assert y[1] == 0.0
+
+
+def test_seg_group_and_concatenation_match_single_calls():
+    """q, k, v as a group, and gate + up repacked back to back into one buffer
+    and multiplied as one matrix: bit-identical to one call per matrix."""
+    torch = torch_cuda()
+    K = 4096
+    xq = problem(5, 8, K)[1]
+    xd = to_dev(xq)
+    shapes = {"q": 1024, "k": 256, "v": 256, "gate": 1536, "up": 1536}
+    Wq = {n: oracle.quantize_q4_0(synth.weights(9, n, O, K)) for n, O in shapes.items()}
+    Wr = {n: to_dev(oracle.repack_q4_0_seg(Wq[n], K)) for n in shapes}
+    single = {}
+    for n, O in shapes.items():
+        y = torch.empty(O, dtype=torch.float32, device="cuda")
+        qdg.q4_0s_q8_0_gemv(Wr[n], xd, y, O, K)
+        single[n] = y
+    ys = [torch.empty(shapes[n], dtype=torch.float32, device="cuda") for n in ("q", "k", "v")]
+    qdg.q4_0s_q8_0_gemv_group([Wr[n] for n in ("q", "k", "v")], ys, [shapes[n] for n in ("q", "k", "v")], xd, K)
+    # gate and up repacked on the GPU into the two halves of one buffer
+    rb = qdg.q4_0_seg_row_bytes(K)
+    cat = empty_u8(2 * 1536 * rb)
+    qdg.q4_0_repack_seg(to_dev(Wq["gate"]), cat[:1536 * rb], 1536, K)
+    qdg.q4_0_repack_seg(to_dev(Wq["up"]), cat[1536 * rb:], 1536, K)
+    ycat = torch.empty(3072, dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemv(cat, xd, ycat, 3072, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    for n, y in zip(("q", "k", "v"), ys):
+        assert np.array_equal(to_host(y).view(np.uint32), to_host(single[n]).view(np.uint32)), n
+    got = to_host(ycat)
+    assert np.array_equal(got[:1536].view(np.uint32), to_host(single["gate"]).view(np.uint32))
+    assert np.array_equal(got[1536:].view(np.uint32), to_host(single["up"]).view(np.uint32))
+    _, y64, S = oracle.matvec(np.concatenate([Wq["gate"], Wq["up"]]), xq, K, threads=8)
+    assert_within_tol(got[None, :], y64, S)
+
+
+def test_seg_gemv_deterministic_and_pdl_invariant():
+    torch = torch_cuda()
+    O, K = 4096, 14336
+    Wq, xq = problem(78, O, K)
+    Wd, xd = to_dev(oracle.repack_q4_0_seg(Wq, K)), to_dev(xq)
+    outs = []
+    for pdl in (0, 1, 0):
+        qdg.qdg_set_option(qdg.QDG_OPT_PDL, pdl)
+        y = torch.empty(O, dtype=torch.float32, device="cuda")
+        for _ in range(3):
+            qdg.q4_0s_q8_0_gemv(Wd, xd, y, O, K)
+        torch.cuda.synchronize()
+        outs.append(to_host(y))
+    qdg.qdg_set_option(qdg.QDG_OPT_PDL, 0)
+    assert all(np.array_equal(outs[0].view(np.uint32), o.view(np.uint32)) for o in outs[1:])
+
+
+def test_seg_gemv_vocab_head_sampled():
+    """The 128256 x 4096 vocab head, repacked on the GPU from Q4_0 bytes the
+    oracle made, on 2048 sampled rows."""
+    torch = torch_cuda()
+    O, K = 128256, 4096
+    rows = np.sort(synth.sample_indices(O, "head-rows", O, 2048))
+    Wq = np.empty((O, K // 32 * 18), dtype=np.uint8)
+    for r in range(0, O, 16384):
+        r1 = min(O, r + 16384)
+        Wq[r:r1] = oracle.quantize_q4_0(synth.weights(3, "head", O, K, row_begin=r, row_end=r1))
+    xq = oracle.quantize_q8_0(synth.activations(3, "x", 1, K, outlier_frac=0.01), synth.gamma(3, "g", K), 1e-6)
+    Wr = empty_u8(qdg.q4_0_seg_nbytes(O, K))
+    qdg.q4_0_repack_seg(to_dev(Wq), Wr, O, K)
+    y = torch.empty(O, dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemv(Wr, to_dev(xq), y, O, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
+    assert_within_tol(to_host(y)[rows][None, :], y64, S)
