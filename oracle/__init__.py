@@ -72,6 +72,10 @@ def lib():
             L.orc_q4_0_seg_row_bytes.restype = c_i64
             L.orc_repack_q4_0_seg.argtypes = [c_p, c_i64, c_i64, c_p]
             L.orc_repack_q4_0_seg.restype = None
+            L.orc_block_sums_q8w.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p]
+            L.orc_block_sums_q8w.restype = None
+            L.orc_matvec_q8w.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_i64, c_p, c_p, c_p]
+            L.orc_matvec_q8w.restype = None
             L.orc_block_sums.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p]
             L.orc_block_sums.restype = None
             L.orc_matvec.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_i64, c_p, c_p, c_p]
@@ -148,24 +152,28 @@ def quantize_q8_0(x: np.ndarray, gamma: np.ndarray | None, eps: float = 1e-6,
     return out
 
 
-def block_sums(Wq: np.ndarray, xq: np.ndarray, K: int) -> np.ndarray:
-    """int32 [N][O][K/32] exact block sums."""
+def block_sums(Wq: np.ndarray, xq: np.ndarray, K: int, wtype: str = "q4_0") -> np.ndarray:
+    """int32 [N][O][K/32] exact block sums; wtype "q4_0" (Q4_0 weights) or
+    "q8_0" (Q8_0 weights)."""
     Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
     xq = np.ascontiguousarray(np.atleast_2d(xq), dtype=np.uint8)
     O = Wq.shape[0]
     N = xq.shape[0]
+    assert Wq.shape[1] == K // QK * (Q4_BLOCK if wtype == "q4_0" else Q8_BLOCK)
     out = np.empty((N, O, K // QK), dtype=np.int32)
-    lib().orc_block_sums(_ptr(Wq), _ptr(xq), O, K, N, _ptr(out))
+    fn = lib().orc_block_sums if wtype == "q4_0" else lib().orc_block_sums_q8w
+    fn(_ptr(Wq), _ptr(xq), O, K, N, _ptr(out))
     return out
 
 
 def matvec(Wq: np.ndarray, xq: np.ndarray, K: int, rows: np.ndarray | None = None,
-           threads: int = 1):
+           threads: int = 1, wtype: str = "q4_0"):
     """Reference y for N vectors: returns (y32 [N][R], y64 [N][R], S [N][R]).
 
     ``rows`` restricts the evaluation to the given row indices of Wq (R of
     them); otherwise all O rows.  ``threads`` > 1 splits rows over Python
     threads (the C call releases the GIL); results do not depend on it.
+    ``wtype`` "q4_0" (Q4_0 weights) or "q8_0" (Q8_0 weights).
     """
     Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
     xq = np.ascontiguousarray(np.atleast_2d(xq), dtype=np.uint8)
@@ -179,6 +187,8 @@ def matvec(Wq: np.ndarray, xq: np.ndarray, K: int, rows: np.ndarray | None = Non
     y64 = np.empty((N, R), dtype=np.float64)
     S = np.empty((N, R), dtype=np.float64)
     L = lib()
+    assert Wq.shape[1] == K // QK * (Q4_BLOCK if wtype == "q4_0" else Q8_BLOCK)
+    mv = L.orc_matvec if wtype == "q4_0" else L.orc_matvec_q8w
 
     def run(lo, hi):
         if hi <= lo:
@@ -187,7 +197,7 @@ def matvec(Wq: np.ndarray, xq: np.ndarray, K: int, rows: np.ndarray | None = Non
         a = np.empty((N, hi - lo), dtype=np.float32)
         b = np.empty((N, hi - lo), dtype=np.float64)
         c = np.empty((N, hi - lo), dtype=np.float64)
-        L.orc_matvec(_ptr(Wq), _ptr(xq), O, K, N, _ptr(sub), hi - lo, _ptr(a), _ptr(b), _ptr(c))
+        mv(_ptr(Wq), _ptr(xq), O, K, N, _ptr(sub), hi - lo, _ptr(a), _ptr(b), _ptr(c))
         y32[:, lo:hi] = a
         y64[:, lo:hi] = b
         S[:, lo:hi] = c

@@ -369,3 +369,63 @@ void orc_matvec(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64
         }
     }
 }
+
+/* ---------------------------------------------------------------------- */
+/* Q8_0 weights.  The stack's conversion step picks the weight type, Q4_K or */
+/* Q8_0, and every back end's kernels must know each type  [GGML: Backend    */
+/* abstraction and hardware acceleration, sections "How one production call */
+/* lands on the hardware" and "Metal and Vulkan"].  A Q8_0 weight row is K/32 */
+/* Q8_0 blocks (the activation format above, made by the same quantizer with */
+/* no norm); the product takes per block the exact integer sum               */
+/* isum = sum_j qw_j * qx_j (both signed) and y = sum_b d_w * d_x * isum_b.   */
+/* ---------------------------------------------------------------------- */
+void orc_block_sums_q8w(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64_t N,
+                        int32_t* isum)
+{
+    const int64_t nb = K / QK;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t o = 0; o < O; ++o)
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = W + (o * nb + b) * 34;
+                const uint8_t* xb = xq + (n * nb + b) * 34;
+                int32_t acc = 0;
+                for (int j = 0; j < QK; ++j)
+                    acc += (int32_t)(int8_t)wb[2 + j] * (int32_t)(int8_t)xb[2 + j];
+                isum[(n * O + o) * nb + b] = acc;
+            }
+}
+
+/* Reference product for Q8_0 weights, as orc_matvec: dequantize both operands */
+/* and take the dot product in fp64 (every term exact); S as there.            */
+void orc_matvec_q8w(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64_t N,
+                    const int64_t* rows, int64_t nrows, float* y32, double* y64, double* S)
+{
+    const int64_t nb = K / QK;
+    if (!rows)
+        nrows = O;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t t = 0; t < nrows; ++t) {
+            int64_t o = rows ? rows[t] : t;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* wb = W + (o * nb + b) * 34;
+                const uint8_t* xb = xq + (n * nb + b) * 34;
+                double dw = (double)orc_f16_to_f32(rd_u16(wb));
+                double dx = (double)orc_f16_to_f32(rd_u16(xb));
+                double blk = 0.0;
+                int64_t isum = 0;
+                for (int j = 0; j < QK; ++j) {
+                    double wv = dw * (double)(int8_t)wb[2 + j];
+                    double xv = dx * (double)(int8_t)xb[2 + j];
+                    blk += wv * xv;
+                    isum += (int64_t)(int8_t)wb[2 + j] * (int64_t)(int8_t)xb[2 + j];
+                }
+                acc += blk;
+                mag += fabs(dw * dx * (double)isum);
+            }
+            if (y32) y32[n * nrows + t] = (float)acc;
+            if (y64) y64[n * nrows + t] = acc;
+            if (S) S[n * nrows + t] = mag;
+        }
+    }
+}

@@ -31,6 +31,9 @@ MUTATIONS = {
     "add_dropped": ("v[j] = v[j] + an[i];", "v[j] = v[j];"),
     "add_before_mul": ("v[j] = v[j] + an[i];", "v[j] = v[j] + an[i] * (gamma ? gamma[i] : 1.0f);"),
     "add_row_stride_ignored": ("const float* an = add ? add + n * ldadd : NULL;", "const float* an = add;"),
+    "q8w_weight_unsigned": ("acc += (int32_t)(int8_t)wb[2 + j] * (int32_t)(int8_t)xb[2 + j];",
+                            "acc += (int32_t)wb[2 + j] * (int32_t)(int8_t)xb[2 + j];"),
+    "q8w_weight_scale_dropped": ("double wv = dw * (double)(int8_t)wb[2 + j];", "double wv = (double)(int8_t)wb[2 + j];"),
     "seg_scale_halves_swapped": ("wr_u16(words + 4 * l, lo);", "wr_u16(words + 4 * l, hi);"),
     "seg_scales_in_block_order": ("if (32 + l < r)\n                    hi = rd_u16(row + (first + 32 + l) * 18);",
                                   "if (2 * l + 1 < r)\n                    hi = rd_u16(row + (first + 2 * l + 1) * 18);"),

@@ -486,3 +486,47 @@ def test_seg_layout_moves_every_byte_once(orc, K):
         nz = halves[halves != 0]
         assert sorted(nz.tolist()) == sorted(want_sc.tolist())
         assert np.count_nonzero(halves) == nb
+
+
+# ---------------------------------------------------------------- Q8_0 weights
+def _q8_block(codes, d_bits):
+    blk = np.zeros(34, dtype=np.uint8)
+    blk[0] = d_bits & 0xFF
+    blk[1] = d_bits >> 8
+    blk[2:] = np.array(codes, dtype=np.int8).view(np.uint8)
+    return blk
+
+
+@pytest.mark.parametrize("case", ["q8w_dot", "q8w_extreme"])
+def test_q8w_golden(orc, case):
+    g = golden()[case]
+    W = _q8_block(g["w_codes"], g["w_d_bits"])[None, :]
+    x = _q8_block(g["x_codes"], g["x_d_bits"])[None, :]
+    assert orc.block_sums(W, x, 32, wtype="q8_0")[0, 0, 0] == g["isum"]
+    y32, y64, S = orc.matvec(W, x, 32, wtype="q8_0")
+    assert y64[0, 0] == g["y"] and y32[0, 0] == np.float32(g["y"])
+    assert S[0, 0] == abs(g["y"])
+
+
+@pytest.mark.parametrize("O,K,N", [(3, 64, 2), (2, 96, 1)])
+def test_q8w_exact_rational(orc, O, K, N):
+    """Brute force in exact rationals from the block definition (independent unpack)."""
+    rng = np.random.default_rng(O * K + N)
+    W = orc.quantize_q8_0(rng.standard_normal((O, K)).astype(np.float32), None)
+    x = orc.quantize_q8_0(rng.standard_normal((N, K)).astype(np.float32), None)
+    qw, dw = unpack_q8(W, K)
+    qx, dx = unpack_q8(x, K)
+    isum = orc.block_sums(W, x, K, wtype="q8_0")
+    _, y64, S = orc.matvec(W, x, K, wtype="q8_0")
+    for n in range(N):
+        for o in range(O):
+            exact = Fraction(0)
+            mag = Fraction(0)
+            for b in range(K // 32):
+                s = sum(int(qw[o, 32 * b + j]) * int(qx[n, 32 * b + j]) for j in range(32))
+                assert isum[n, o, b] == s
+                term = Fraction(float(dw[o, b])) * Fraction(float(dx[n, b])) * s
+                exact += term
+                mag += abs(term)
+            assert abs(Fraction(float(y64[n, o])) - exact) <= Fraction(1, 10 ** 12) * (mag + 1)
+            assert abs(float(S[n, o]) - float(mag)) <= 1e-12 * float(mag) + 1e-300
