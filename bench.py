@@ -268,7 +268,7 @@ def time_oracle(wl, budget_s, row_frac, steps=None, warmup=1):
 
 # ---------------------------------------------------------------- GPU leg
 class DecodeStep:
-    def __init__(self, wl, device, layout="plain"):
+    def __init__(self, wl, device, layout="seg"):
         import torch
         from quantized_decode_gemv_rms_gb300 import qdg
         self.qdg = qdg
@@ -685,6 +685,28 @@ def bench_extras(args, device):
                                           "frac_fp16_peak": round(tflops / peaks["bf16_tflops"], 4)}
         del Wq, x, xq, y, ws
         torch.cuda.empty_cache()
+    # Q8_0 weights (batch-1 GEMV): gate-shaped and down-shaped matrices, rotating weight copies
+    out["q8_0_weights"] = {}
+    for (O, K) in (workloads.SMALL_N_SHAPES if args.only in (None, "q8w") else ()):
+        W8 = torch.empty(O * (K // 32) * 34, dtype=torch.uint8, device=device)
+        for r in range(0, O, 8192):
+            r1 = min(O, r + 8192)
+            w = torch.from_numpy(synth.weights(workloads.SMALL_N_SEED, f"q8w-{O}x{K}", O, K, row_begin=r,
+                                               row_end=r1)).to(device)
+            qdg.qnorm_quantize_q8_0(w, None, 0.0, W8[r * (K // 32) * 34:r1 * (K // 32) * 34], K=K, N=r1 - r)
+        copies = max(2, -(-3 * l2 // W8.numel()))
+        Ws = [W8] + [W8.clone() for _ in range(copies - 1)]
+        x = torch.from_numpy(synth.activations(workloads.SMALL_N_SEED, f"q8w-x-{K}", 1, K)).to(device)
+        xq = torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
+        qdg.qnorm_quantize_q8_0(x, None, 0.0, xq)
+        y = torch.empty(O, dtype=torch.float32, device=device)
+        us = timed_graph(lambda i: qdg.q8_0_q8_0_gemv(Ws[i % copies], xq, y, O, K), copies)
+        nbytes = O * (K // 32) * 34 + (K // 32) * 34 + 4 * O
+        out["q8_0_weights"][f"{O}x{K}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                           "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                                           "weight_copies": copies}
+        del Ws, W8
+        torch.cuda.empty_cache()
     out["peak_note"] = ("small-N against the measured HBM copy bandwidth; prefill against the measured dense "
                         "bf16 burst peak (the fp16 tensor rate is the same nominal 2.25 PFLOP/s)")
     torch.cuda.synchronize()
@@ -715,16 +737,16 @@ def main():
     ap.add_argument("--fused", action="store_true",
                     help="time the fused route (one norm+quantize+GEMV launch per group) as the main line; "
                          "the default main line is quantize kernel + grouped GEMV per group")
-    ap.add_argument("--layout", choices=["seg", "plain"], default="plain",
-                    help="weight layout the split route's GEMV reads: plain = Q4_0 blocks as stored (default), "
-                         "seg = segment layout repacked at load")
+    ap.add_argument("--layout", choices=["seg", "plain"], default="seg",
+                    help="weight layout the split route's GEMV reads: seg = segment layout repacked at load "
+                         "(default), plain = Q4_0 blocks as stored")
     ap.add_argument("--pdl", action="store_true", default=True)
     ap.add_argument("--no-pdl", dest="pdl", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the small-N and prefill timings")
-    ap.add_argument("--only", choices=["small_n", "prefill"], default=None,
+    ap.add_argument("--only", choices=["small_n", "prefill", "q8w"], default=None,
                     help="time only that product (one JSON object with its numbers)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -748,12 +770,13 @@ def main():
         print(json.dumps(line))
         return
 
-    if args.only in ("small_n", "prefill"):
+    if args.only in ("small_n", "prefill", "q8w"):
         import torch
         torch.cuda.set_device(local)
         ex = bench_extras(args, torch.device("cuda", local))
+        key = "q8_0_weights" if args.only == "q8w" else args.only
         if rank == 0:
-            print(json.dumps({"only": args.only, args.only: ex[args.only]}))
+            print(json.dumps({"only": args.only, key: ex[key]}))
         return
     result, step = bench_ours(args, wl, world, rank, local)
     if args.extras and rank == 0:

@@ -249,6 +249,26 @@ QDG_API int quantize_q4_0(const float* w, int64_t ldw, int64_t O, int64_t K, voi
                   qdg_stream_t stream);
 
 /*
+ * q8_0_q8_0_gemv -- y = W * x with Q8_0 weights: the stack's conversion step
+ * picks the weight type (Q4_K or Q8_0) and every back end's matrix kernels
+ * must know each type [GGML: Backend abstraction and hardware acceleration,
+ * sections "How one production call lands on the hardware" and "Metal and
+ * Vulkan"].  W [O][K/32] Q8_0 blocks (34 bytes: fp16 d, 32 int8 codes; made,
+ * for example, by qnorm_quantize_q8_0 with gamma = NULL), 16-byte aligned.
+ * xq [K/32] Q8_0, 4-byte aligned.  y [O] fp32 (overwritten).  K multiple of
+ * 256, <= 32768; 1 <= O < 2^31.  Per block the exact integer sum of code
+ * products, scaled by d_w * d_x; deterministic.  8.5 bits per weight are
+ * streamed, so it takes about 1.9x the time of the Q4_0 product.
+ */
+QDG_API int q8_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K,
+                           qdg_stream_t stream);
+
+/* q8_0_q8_0_gemv for up to 4 Q8_0 matrices reading one Q8_0 vector, in one
+ * launch (argument rules as q4_0_q8_0_gemv_group). */
+QDG_API int q8_0_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                 const void* xq, int64_t K, qdg_stream_t stream);
+
+/*
  * Segment layout of Q4_0 weights (load-time repack).  GGML's CPU back end
  * rearranges Q4 weights once, when they are loaded, for its own kernels
  * [GGML: Backend abstraction and hardware acceleration, section "How build
@@ -311,11 +331,8 @@ QDG_API const char* qdg_status_string(int status);
  * Options (process-wide).  QDG_OPT_PDL = 1 launches the decode kernels with
  * programmatic dependent launch: a kernel may start streaming W while the
  * previous kernel on the stream is still running, and waits for it before
- * reading activations or writing outputs.  The quantize kernels let their
- * successor launch before they wait themselves, so a product that follows a
- * quantize may start reading W while the kernel ahead of that quantize is
- * still running.  Enable it only when W is not written by the last two
- * kernels launched before the product on the same stream.
+ * reading activations or writing outputs.  Enable it only when W is not
+ * written by the kernel launched immediately before on the same stream.
  * Default 0.  Returns QDG_EINVAL for an unknown option.
  */
 enum qdg_option { QDG_OPT_PDL = 1 };
@@ -325,7 +342,7 @@ QDG_API int qdg_set_option(int option, int64_t value);
  * qdg_launch_count -- number of kernels this library has launched in this
  * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
  * 4 weight quantize, 5 fused norm+gemv, 6 segment-layout gemv, 7 repack,
- * -1 total.  Lets a caller check that the fused kernel
+ * 8 Q8_0-weight gemv, -1 total.  Lets a caller check that the fused kernel
  * is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);
@@ -335,7 +352,8 @@ QDG_API int64_t qdg_launch_count(int which);
  * product path and writes the exact per-block integer sums
  * isum[n][o][b] = sum_j (q_w - 8) * q_x  (int32 [N][O][K/32]) instead of y.
  * path: 0 = gemv (N must be 1), 1 = small-N, 2 = prefill gemm (N = T tokens),
- * 3 = segment-layout gemv (W in the segment layout, N must be 1).
+ * 3 = segment-layout gemv (W in the segment layout, N must be 1),
+ * 4 = Q8_0-weight gemv (W in Q8_0 blocks, N must be 1).
  * Same argument rules as the corresponding entry point.
  */
 QDG_API int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum, int64_t O,

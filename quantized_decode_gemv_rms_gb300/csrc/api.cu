@@ -13,7 +13,7 @@ namespace {
 std::mutex g_dev_mutex;
 DeviceInfo g_dev_cache[64];
 std::atomic<int> g_pdl{0};
-std::atomic<int64_t> g_counts[8];
+std::atomic<int64_t> g_counts[9];
 }  // namespace
 
 DeviceInfo device_info() {
@@ -84,7 +84,7 @@ extern "C" int64_t qdg_launch_count(int which) {
         for (auto& c : g_counts) t += c.load();
         return t;
     }
-    if (which < 0 || which >= 8) return -1;
+    if (which < 0 || which >= 9) return -1;
     return g_counts[which].load();
 }
 
@@ -146,6 +146,9 @@ extern "C" int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum
         case 3:
             if (N != 1) return QDG_EINVAL;
             return gemv_seg_launch(W, xq, nullptr, O, K, s, isum);
+        case 4:
+            if (N != 1) return QDG_EINVAL;
+            return gemv_q8w_launch(W, xq, nullptr, O, K, s, isum);
         default:
             return QDG_EINVAL;
     }

@@ -222,6 +222,8 @@ cudaError_t launch_cluster(Kern kernel, dim3 grid, dim3 block, size_t smem, cuda
 // exact per-block integer sums [N][O][K/32] as the kernel forms them).
 int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
                 int32_t* dbg);
+int gemv_q8w_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
+                    int32_t* dbg);
 int gemv_seg_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
                     int32_t* dbg);
 int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t N,

@@ -39,15 +39,28 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kDepth = 3;                   // row-segments in flight per warp (the consume loop is unrolled by 3)
-constexpr int kSegBytes = 1152;             // 32 pairs x 36 bytes
-constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
 constexpr int kFusedMaxK = 16384;           // fused form stages x and gamma in shared memory
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
 
+// Weight types.  A lane owns one pair of consecutive blocks per segment of
+// 32 pairs.  Q4_0: 18-byte blocks, 36-byte pairs, 1152-byte segments read as
+// three 16-byte loads per lane, three segments in flight per warp.  Q8_0:
+// 34-byte blocks, 68-byte pairs, 2176-byte segments read as five loads per
+// lane, two segments in flight (about the same registers, more bytes).
+enum { kQ4 = 0, kQ8 = 1 };
+template <int kW>
+struct WT {
+    static constexpr int kBlockBytes = kW == kQ4 ? 18 : 34;
+    static constexpr int kPairBytes = 2 * kBlockBytes;
+    static constexpr int kSegBytes = 32 * kPairBytes;
+    static constexpr int kLoads = (kSegBytes / 16 + 31) / 32;
+    static constexpr int kDepth = kW == kQ4 ? 3 : 2;
+    static constexpr int kPartFloats = kW == kQ4 ? 4096 : 2048;   // per-chunk partial sums (rows x segments)
+};
+
 struct Plan {
-    int rowbytes;   // K/32 * 18
+    int rowbytes;   // K/32 * block bytes
     int nb;         // K/32
     int P;          // block pairs per row (K/64)
     int nseg;       // segments per row, ceil(P / 32)
@@ -55,14 +68,15 @@ struct Plan {
     int rch;        // rows per chunk (partial-sum buffer capacity), multiple of nslots
 };
 
+template <int kW>
 Plan make_plan(int64_t K) {
     Plan p{};
     p.nb = static_cast<int>(K / 32);
-    p.rowbytes = p.nb * 18;
+    p.rowbytes = p.nb * WT<kW>::kBlockBytes;
     p.P = static_cast<int>(K / 64);
     p.nseg = (p.P + 31) / 32;
     p.nslots = kWarps / p.nseg;
-    p.rch = (kPartFloats / p.nseg) / p.nslots * p.nslots;
+    p.rch = (WT<kW>::kPartFloats / p.nseg) / p.nslots * p.nslots;
     return p;
 }
 
@@ -87,9 +101,10 @@ __device__ __forceinline__ int block_dot(uint32_t q0, uint32_t q1, uint32_t q2, 
     return acc;
 }
 
-// The 16-byte chunks of one row-segment held by a lane: indices lane, lane+32, lane+64.
+// The 16-byte chunks of one row-segment held by a lane: indices lane, lane+32, ...
+template <int kW>
 struct SegRegs {
-    uint4 v[3];
+    uint4 v[WT<kW>::kLoads];
 };
 
 constexpr int kMaxGroup = 4;   // matrices sharing one input in a grouped launch
@@ -113,13 +128,16 @@ struct Args {
     float eps;
 };
 
-template <bool kFused, bool kDebug>
 // 96 registers a thread (no spills): one CTA of 512 threads then leaves room
 // on its SM for a CTA of the quantize kernel, so the next vector's quantize
 // can be resident, and start, while this product is still streaming.
+template <int kW, bool kFused, bool kDebug>
 __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
+    using T = WT<kW>;
+    constexpr int kDepth = T::kDepth;
+    constexpr int kSegBytes = T::kSegBytes;
     __shared__ __align__(16) uint8_t seg_buf[kWarps][kSegBytes];
-    __shared__ float part[kPartFloats];
+    __shared__ float part[T::kPartFloats];
     __shared__ float norm_part[8];
     // fused form only: x [K] fp32, gamma [K] fp32, Q8_0 activations [K/32 x 34 B]
     extern __shared__ __align__(16) uint8_t fused_smem[];
@@ -136,7 +154,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
     const bool active = worker && p < plan.P;
     // this warp's segment within a row: byte offset and number of 16-byte chunks
     const int seg_off = seg * kSegBytes;
-    const int seg_vec = worker ? (min(plan.P, seg * 32 + 32) - seg * 32) * 36 / 16 : 0;
+    const int seg_vec = worker ? (min(plan.P, seg * 32 + 32) - seg * 32) * T::kPairBytes / 16 : 0;
 
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * O / gridDim.x;
     const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * O / gridDim.x;
@@ -144,15 +162,15 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
 
     pdl_trigger();
 
-    SegRegs pipe[kDepth];
-    auto load_seg = [&](int64_t row, SegRegs& s) {
+    SegRegs<kW> pipe[kDepth];
+    auto load_seg = [&](int64_t row, SegRegs<kW>& s) {
         int g = 0;
 #pragma unroll
         for (int i = 1; i < kMaxGroup; ++i)
             if (i < a.ng && row >= a.start[i]) g = i;
         const uint8_t* base = a.Wg[g] + (row - a.start[g]) * plan.rowbytes + seg_off;
 #pragma unroll
-        for (int k = 0; k < 3; ++k) {
+        for (int k = 0; k < T::kLoads; ++k) {
             const int idx = lane + 32 * k;
             if (idx < seg_vec) s.v[k] = ldg_stream(base + idx * 16);
         }
@@ -317,11 +335,11 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
     uint8_t* buf = seg_buf[warp];
     // One row-segment: stage it through shared memory, refill its ring entry
     // with the segment kDepth ahead, dot it, reduce it.
-    auto consume = [&](int64_t c0, int crows, int ri, SegRegs& entry) {
+    auto consume = [&](int64_t c0, int crows, int ri, SegRegs<kW>& entry) {
         // Store first (this waits for the entry's loads, issued kDepth steps
         // ago), then reuse the same registers for the segment kDepth ahead.
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
+        for (int q = 0; q < T::kLoads; ++q) {
             const int idx = lane + 32 * q;
             if (idx < seg_vec) *reinterpret_cast<uint4*>(buf + idx * 16) = entry.v[q];
         }
@@ -330,16 +348,35 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
         __syncwarp();
         float acc = 0.0f;
         if (active) {
-            const uint32_t* wp = reinterpret_cast<const uint32_t*>(buf + lane * 36);
-            uint32_t w[9];
+            int ia, ib;
+            float dwa, dwb;
+            if (kW == kQ4) {
+                const uint32_t* wp = reinterpret_cast<const uint32_t*>(buf + lane * 36);
+                uint32_t w[9];
 #pragma unroll
-            for (int i = 0; i < 9; ++i) w[i] = wp[i];
-            const int ia = block_dot(bytes_2_to_5(w[0], w[1]), bytes_2_to_5(w[1], w[2]), bytes_2_to_5(w[2], w[3]),
-                                     bytes_2_to_5(w[3], w[4]), xa) -
-                           8 * sa;
-            const int ib = block_dot(w[5], w[6], w[7], w[8], xb) - 8 * sb;
-            const float dwa = half_bits_to_float(w[0]);
-            const float dwb = half_bits_to_float(w[4] >> 16);
+                for (int i = 0; i < 9; ++i) w[i] = wp[i];
+                ia = block_dot(bytes_2_to_5(w[0], w[1]), bytes_2_to_5(w[1], w[2]), bytes_2_to_5(w[2], w[3]),
+                               bytes_2_to_5(w[3], w[4]), xa) -
+                     8 * sa;
+                ib = block_dot(w[5], w[6], w[7], w[8], xb) - 8 * sb;
+                dwa = half_bits_to_float(w[0]);
+                dwb = half_bits_to_float(w[4] >> 16);
+            } else {
+                // Q8_0 pair: scale a, 32 codes of a (bytes 2..33), scale b, 32 codes of b (word aligned)
+                const uint32_t* wp = reinterpret_cast<const uint32_t*>(buf + lane * 68);
+                uint32_t w[17];
+#pragma unroll
+                for (int i = 0; i < 17; ++i) w[i] = wp[i];
+                ia = 0;
+                ib = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    ia = __dp4a(static_cast<int>(bytes_2_to_5(w[i], w[i + 1])), static_cast<int>(xa[i]), ia);
+                    ib = __dp4a(static_cast<int>(w[9 + i]), static_cast<int>(xb[i]), ib);
+                }
+                dwa = half_bits_to_float(w[0]);
+                dwb = half_bits_to_float(w[8] >> 16);
+            }
             acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
             acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
             if (kDebug) {
@@ -364,7 +401,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
             for (int ri = slot; ri < crows; ri += kDepth * step) {
                 consume(c0, crows, ri, pipe[0]);
                 if (ri + step < crows) consume(c0, crows, ri + step, pipe[1]);
-                if (ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[2]);
+                if (kDepth > 2 && ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[kDepth > 2 ? 2 : 0]);
             }
         }
         __syncthreads();
@@ -384,9 +421,8 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
     }
 }
 
-}  // namespace
-
-int gemv_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq, int64_t K,
+template <int kW>
+int gemv_launch_typed(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq, int64_t K,
                       cudaStream_t stream, int32_t* dbg) {
     if (!W || !O || !xq || (!y && !dbg)) return QDG_EINVAL;
     if (count < 1 || count > kMaxGroup || K <= 0) return QDG_EINVAL;
@@ -406,7 +442,7 @@ int gemv_launch_group(const void* const* W, float* const* y, const int64_t* O, i
     if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
-    const Plan plan = make_plan(K);
+    const Plan plan = make_plan<kW>(K);
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
     a.ng = count;
     a.W = a.Wg[0];
@@ -417,12 +453,30 @@ int gemv_launch_group(const void* const* W, float* const* y, const int64_t* O, i
     a.K = static_cast<int>(K);
     cudaError_t e;
     if (dbg)
-        e = launch(gemv_kernel<false, true>, dim3(grid), dim3(kThreads), 0, stream, false, a, plan);
+        e = launch(gemv_kernel<kW, false, true>, dim3(grid), dim3(kThreads), 0, stream, false, a, plan);
     else
-        e = launch(gemv_kernel<false, false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
+        e = launch(gemv_kernel<kW, false, false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
-    count_launch(1);
+    count_launch(kW == kQ4 ? 1 : 8);
     return QDG_OK;
+}
+
+}  // namespace
+
+int gemv_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq, int64_t K,
+                      cudaStream_t stream, int32_t* dbg) {
+    return gemv_launch_typed<kQ4>(W, y, O, count, xq, K, stream, dbg);
+}
+
+int gemv_q8w_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq,
+                          int64_t K, cudaStream_t stream, int32_t* dbg) {
+    return gemv_launch_typed<kQ8>(W, y, O, count, xq, K, stream, dbg);
+}
+
+int gemv_q8w_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
+                    int32_t* dbg) {
+    float* ys[1] = {y};
+    return gemv_q8w_launch_group(&W, y ? ys : nullptr, &O, 1, xq, K, stream, dbg);
 }
 
 int gemv_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream, int32_t* dbg) {
@@ -450,7 +504,7 @@ int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O,
     if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
-    const Plan plan = make_plan(K);
+    const Plan plan = make_plan<kQ4>(K);
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
     a.ng = count;
     a.W = a.Wg[0];
@@ -467,13 +521,13 @@ int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O,
         static size_t set_bytes = 0;
         std::lock_guard<std::mutex> lock(mu);
         if (set_bytes < smem) {
-            if (cudaFuncSetAttribute(gemv_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            if (cudaFuncSetAttribute(gemv_kernel<kQ4, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(smem)) != cudaSuccess)
                 return QDG_ECUDA;
             set_bytes = smem;
         }
     }
-    const cudaError_t e = launch(gemv_kernel<true, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
+    const cudaError_t e = launch(gemv_kernel<kQ4, true, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(5);
     return QDG_OK;
@@ -513,4 +567,15 @@ extern "C" int q4_0_gemv_rmsnorm_group(const void* const* W, float* const* y, co
                                        const float* x, const float* gamma, float eps, int64_t K, void* xq_out,
                                        qdg_stream_t stream) {
     return qdg::gemv_rmsnorm_launch(W, y, O, count, x, gamma, eps, K, xq_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int q8_0_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K, qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    return qdg::gemv_q8w_launch(W, xq, y, O, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" int q8_0_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                    const void* xq, int64_t K, qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    return qdg::gemv_q8w_launch_group(W, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }

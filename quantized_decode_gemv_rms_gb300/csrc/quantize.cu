@@ -18,13 +18,17 @@ namespace {
 
 constexpr int kNormThreads = 256;     // the fixed reduction order is defined over 256 lanes
 constexpr int kBlocksPerCta = 32;     // Q8_0 blocks quantized by one CTA (4 per warp)
+constexpr int kStageMax = 8192;       // vectors up to this length are read for the norm in one wave of loads
+constexpr int kStagePer = kStageMax / 4 / kNormThreads;   // 16-byte loads per thread in that wave
 
 // Grid: (vectors * splits).  Every CTA of a vector recomputes the vector's
 // sum of squares in the library's fixed order (so all CTAs agree bit for
 // bit), then quantizes its own slice of kBlocksPerCta blocks.
 //   Sum of squares: thread j sums x_i^2 for i = j (mod 256) with an fma chain
 //   in ascending i; each warp combines with an xor butterfly (16,8,4,2,1);
-//   the 8 warp totals combine as ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).
+//   the 8 warp totals combine as ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)).  A
+//   16-byte aligned vector of up to kStageMax elements is first read whole,
+//   in one wave of 16-byte loads, into shared memory (the chains are the same).
 //   Quantization: warp w takes blocks w, w+8, ... of the slice, lane l
 //   element 32b+l.
 //   add (optional): v = (x*s)*gamma + a, one fp32 addition after the MUL
@@ -33,9 +37,6 @@ __global__ void __launch_bounds__(kNormThreads)
 qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restrict__ gamma,
                 const float* __restrict__ add, int64_t ldadd, float eps, int K, int splits,
                 uint8_t* __restrict__ xq) {
-    // Let the next kernel (the product that reads xq) launch at once: it
-    // streams its weights while this kernel waits for its own predecessor.
-    pdl_trigger();
     pdl_wait();
     const int64_t n = blockIdx.x / splits;
     const int split = blockIdx.x - static_cast<int>(n * splits);
@@ -62,17 +63,37 @@ qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restric
     float s = 1.0f;
     if (gamma != nullptr) {
         __shared__ float wsum[kNormThreads / 32];
+        __shared__ __align__(16) float xs[kStageMax];
         float acc = 0.0f;
-        for (int i0 = tid; i0 < K; i0 += kNormThreads * 8) {
-            float v[8];
+        if (K <= kStageMax && (reinterpret_cast<uintptr_t>(xn) & 15) == 0) {
+            // the whole vector in one wave of 16-byte loads (one memory round
+            // trip), staged in shared memory; then each chain in order
+            const int k4 = K >> 2;
+            float4 t[kStagePer];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int i = i0 + u * kNormThreads;
-                v[u] = i < K ? __ldg(xn + i) : 0.0f;
+            for (int u = 0; u < kStagePer; ++u) {
+                const int i = tid + u * kNormThreads;
+                if (i < k4) t[u] = __ldg(reinterpret_cast<const float4*>(xn) + i);
             }
 #pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (i0 + u * kNormThreads < K) acc = __fmaf_rn(v[u], v[u], acc);
+            for (int u = 0; u < kStagePer; ++u) {
+                const int i = tid + u * kNormThreads;
+                if (i < k4) reinterpret_cast<float4*>(xs)[i] = t[u];
+            }
+            __syncthreads();
+            for (int i = tid; i < K; i += kNormThreads) acc = __fmaf_rn(xs[i], xs[i], acc);
+        } else {
+            for (int i0 = tid; i0 < K; i0 += kNormThreads * 8) {
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int i = i0 + u * kNormThreads;
+                    v[u] = i < K ? __ldg(xn + i) : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (i0 + u * kNormThreads < K) acc = __fmaf_rn(v[u], v[u], acc);
+            }
         }
         acc = warp_sum(acc);
         if (lane == 0) wsum[warp] = acc;
@@ -83,6 +104,9 @@ qnorm_q8_kernel(const float* __restrict__ x, int64_t ldx, const float* __restric
         s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
     }
 
+    // The inputs are in: let the next kernel (the product that reads xq)
+    // launch and start streaming its weights while the blocks are quantized.
+    pdl_trigger();
     uint8_t* out = xq + n * nb * 34;
 #pragma unroll
     for (int u = 0; u < kPer; ++u) {

@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
             sig["q4_0_q8_0_gemm"] = ([p, p, p, i64, i64, i64, i64, p, i64, p], i32)
             sig["q4_0_q8_0_gemm_workspace_bytes"] = ([i64, i64], i64)
             sig["q4_0_q8_0_gemm_static"] = ([p, p, p, i64, i64, i64, i64, p], i32)
+            sig["q8_0_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
+            sig["q8_0_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
             sig["q4_0_seg_row_bytes"] = ([i64], i64)
             sig["q4_0_repack_seg"] = ([p, p, i64, i64, p], i32)
             sig["q4_0s_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
@@ -158,6 +160,20 @@ def q4_0_q8_0_gemv_group(Ws, ys, Os, xq, K: int, stream=None) -> None:
     y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in ys])
     O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
     _check(lib().q4_0_q8_0_gemv_group(W_arr, y_arr, O_arr, n, _ptr(xq), K, _stream(stream)), "q4_0_q8_0_gemv_group")
+
+
+def q8_0_q8_0_gemv(W, xq, y, O: int, K: int, stream=None) -> None:
+    """y = W * x with Q8_0 weights."""
+    _check(lib().q8_0_q8_0_gemv(_ptr(W), _ptr(xq), _ptr(y), O, K, _stream(stream)), "q8_0_q8_0_gemv")
+
+
+def q8_0_q8_0_gemv_group(Ws, ys, Os, xq, K: int, stream=None) -> None:
+    """Q8_0-weight GEMV for up to 4 matrices sharing one Q8_0 vector (one launch)."""
+    n = len(Ws)
+    W_arr = (ctypes.c_void_p * n)(*[_ptr(w) for w in Ws])
+    y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in ys])
+    O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
+    _check(lib().q8_0_q8_0_gemv_group(W_arr, y_arr, O_arr, n, _ptr(xq), K, _stream(stream)), "q8_0_q8_0_gemv_group")
 
 
 def q4_0_seg_row_bytes(K: int) -> int:

@@ -26,7 +26,7 @@ def test_header_declares_entry_points():
     names = declared_symbols()
     for must in ("qnorm_quantize_q8_0", "qnorm_add_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
                  "q4_0_q8_0_gemm_workspace_bytes", "quantize_q4_0", "q4_0_repack_seg", "q4_0s_q8_0_gemv",
-                 "q4_0s_q8_0_gemv_group", "q4_0_seg_row_bytes",
+                 "q4_0s_q8_0_gemv_group", "q4_0_seg_row_bytes", "q8_0_q8_0_gemv", "q8_0_q8_0_gemv_group",
                  "qdg_device_status", "qdg_status_string"):
         assert must in names
 
@@ -80,6 +80,23 @@ def test_gemv_host_validation(L):
     assert f(A16, A16, A16, 8, 65536, None) == -3     # K beyond the maximum
     assert f(A2, A16, A16, 8, 256, None) == -2        # W not 16-byte aligned
     assert f(A16, A2, A16, 8, 256, None) == -2        # xq not 4-byte aligned
+
+
+def test_q8w_gemv_host_validation(L):
+    f = L.q8_0_q8_0_gemv
+    assert f(None, A16, A16, 8, 256, None) == -1
+    assert f(A16, A16, None, 8, 256, None) == -1
+    assert f(A16, A16, A16, 0, 256, None) == -1
+    assert f(A16, A16, A16, 8, 128, None) == -3       # K % 256
+    assert f(A16, A16, A16, 8, 65536, None) == -3     # K beyond the maximum
+    assert f(A2, A16, A16, 8, 256, None) == -2        # W not 16-byte aligned
+    assert f(A16, A2, A16, 8, 256, None) == -2        # xq not 4-byte aligned
+    g = L.q8_0_q8_0_gemv_group
+    W = (ctypes.c_void_p * 5)(*([A16] * 5))
+    Y = (ctypes.c_void_p * 5)(*([A16] * 5))
+    O = (ctypes.c_int64 * 5)(*([8] * 5))
+    assert g(W, Y, O, 5, A16, 256, None) == -1
+    assert g(W, None, O, 2, A16, 256, None) == -1
 
 
 def test_seg_layout_host_validation(L):
@@ -195,12 +212,13 @@ def test_options_and_counters(L):
     assert L.qdg_set_option(1, 2) == -1
     assert L.qdg_set_option(1, 0) == 0
     assert L.qdg_launch_count(-1) >= 0
-    assert L.qdg_launch_count(8) == -1
-    assert L.qdg_launch_count(7) >= 0
+    assert L.qdg_launch_count(9) == -1
+    assert L.qdg_launch_count(8) >= 0
     assert L.qdg_debug_block_sums(A16, A16, None, 8, 256, 1, 0, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 1, 9, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 0, None) == -1   # gemv path needs N == 1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 3, None) == -1   # so does the segment-layout gemv
+    assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 4, None) == -1   # and the Q8_0-weight gemv
 
 
 def test_binding_names_match_header():
