@@ -89,14 +89,6 @@ __device__ __forceinline__ float ld_cluster(const float* p, uint32_t rank) {
 __device__ __forceinline__ uint32_t lo_pair(uint32_t v) { return (v & kLoNib) | kMagic; }
 __device__ __forceinline__ uint32_t hi_pair(uint32_t v) { return (v & kHiNib) | kMagic; }
 
-// (d0, d1) = (a0, a1) + (b0, b1), packed fp32x2.
-__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-    asm("{\n\t.reg .b64 a, b, d;\n\t"
-        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
-        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
-        : "=f"(d0), "=f"(d1)
-        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
-}
 
 // D = A * B (C = 0), m16n8k16, fp16 operands, fp32 accumulation; then D += A2 * B2.
 __device__ __forceinline__ void hmma2(float& d0, float& d1, float& d2, float& d3, uint32_t a0, uint32_t a1,
@@ -110,6 +102,12 @@ __device__ __forceinline__ void hmma2(float& d0, float& d1, float& d2, float& d3
         : "=&f"(d0), "=&f"(d1), "=&f"(d2), "=&f"(d3)
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "r"(e0), "r"(e1), "r"(e2), "r"(e3), "r"(f0),
           "r"(f1));
+}
+
+// (d0, d1) += (b0, b1), packed fp32x2.
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%0, %1};\n\tmov.b64 b, {%2, %3};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}" : "+f"(d0), "+f"(d1) : "f"(b0), "f"(b1));
 }
 
 // Word t of the nibbles of block b in a staged row (row start 16-byte aligned):
@@ -145,23 +143,12 @@ struct XBlock {
     uint32_t b[4];
 };
 // Per warp, block and t, in shared memory (read as one 16-byte vector): the
-// corrections -1032 S_lo - 72 S_hi of columns 2t and 2t + 1, and their fp16
-// scales d_x packed in one word.
+// corrections -1032 S_lo - 72 S_hi of columns 2t and 2t + 1, and their
+// scales d_x in fp32.
 struct XTab {
     float m0, m1;
-    uint32_t dx;
-    uint32_t pad;
+    float dx0, dx1;
 };
-
-// d = a * b exactly (fp16 operands, fp32 result).
-__device__ __forceinline__ float mul_f16_f32(unsigned short a, unsigned short b) {
-    float d;
-    asm("{\n\t.reg .f16 ha, hb;\n\tmov.b16 ha, %1;\n\tmov.b16 hb, %2;\n\t"
-        "fma.rn.f32.f16 %0, ha, hb, 0f00000000;\n\t}"
-        : "=f"(d)
-        : "h"(a), "h"(b));
-    return d;
-}
 
 template <int kB>
 __device__ __forceinline__ void block_step(const uint8_t* ra, const uint8_t* rb, int t, const XBlock& x,
@@ -174,15 +161,18 @@ __device__ __forceinline__ void block_step(const uint8_t* ra, const uint8_t* rb,
     const XTab e = tab[kB * 4 + t];
     float d0, d1, d2, d3;
     // first MMA: low nibbles of bytes (0, 2) and (1, 3), rows g and g + 8;
-    // second MMA: high nibbles of the same bytes (x 16), activations / 16
+    // second MMA: high nibbles of the same bytes (x 16), activations / 16;
+    // plus the columns' corrections: d = the exact block sums of columns 2t,
+    // 2t + 1 for rows g (d0, d1) and g + 8 (d2, d3).
     hmma2(d0, d1, d2, d3, lo_pair(w0), lo_pair(w1), lo_pair(v0), lo_pair(v1), x.b[0], x.b[1], hi_pair(w0),
           hi_pair(w1), hi_pair(v0), hi_pair(v1), x.b[2], x.b[3]);
-    fadd2(d0, d1, d0, d1, e.m0, e.m1);   // exact block sums, columns 2t, 2t + 1, row g
-    fadd2(d2, d3, d2, d3, e.m0, e.m1);   // row g + 8
-    const unsigned short dx0 = static_cast<unsigned short>(e.dx), dx1 = static_cast<unsigned short>(e.dx >> 16);
-    // d_w * d_x, exact in fp32
-    const float s0 = mul_f16_f32(dw0, dx0), s1 = mul_f16_f32(dw0, dx1);
-    const float s2 = mul_f16_f32(dw1, dx0), s3 = mul_f16_f32(dw1, dx1);
+    // acc += (d_w * d_x) * isum; the scale product is exact in fp32
+    fadd2(d0, d1, e.m0, e.m1);
+    fadd2(d2, d3, e.m0, e.m1);
+    const float dwa = half_bits_to_float(dw0), dwb = half_bits_to_float(dw1);
+    float s0, s1, s2, s3;
+    fmul2(s0, s1, dwa, dwa, e.dx0, e.dx1);
+    fmul2(s2, s3, dwb, dwb, e.dx0, e.dx1);
     ffma2(acc[0], acc[1], s0, s1, d0, d1);
     ffma2(acc[2], acc[3], s2, s3, d2, d3);
     isum[0] = d0;
@@ -321,8 +311,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
         XTab e;
         e.m0 = __shfl_sync(0xffffffffu, mg, 8 * t);
         e.m1 = __shfl_sync(0xffffffffu, mg, 8 * t + 4);
-        e.dx = __shfl_sync(0xffffffffu, xd[b], 8 * t) | (__shfl_sync(0xffffffffu, xd[b], 8 * t + 4) << 16);
-        e.pad = 0;
+        e.dx0 = half_bits_to_float(__shfl_sync(0xffffffffu, xd[b], 8 * t));
+        e.dx1 = half_bits_to_float(__shfl_sync(0xffffffffu, xd[b], 8 * t + 4));
         if (g == 0) tab[b * 4 + t] = e;
     }
     __syncwarp();
