@@ -108,7 +108,8 @@ extern "C" int qdg_device_status(qdg_stream_t stream) {
         return QDG_ECUDA;
     }
     unsigned f = 0;
-    const unsigned parts[] = {flags_read_clear_quantize(s), flags_read_clear_gemv(s), flags_read_clear_small_n(s),
+    const unsigned parts[] = {flags_read_clear_quantize(s), flags_read_clear_gemv(s), flags_read_clear_gemv_seg(s),
+                              flags_read_clear_small_n(s),
                               flags_read_clear_gemm(s), flags_read_clear_api(s)};
     for (unsigned p : parts) {
         if (p == ~0u) {

@@ -235,6 +235,7 @@ int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O,
 // Per-translation-unit device flags: read and clear (synchronises stream).
 unsigned flags_read_clear_quantize(cudaStream_t stream);
 unsigned flags_read_clear_gemv(cudaStream_t stream);
+unsigned flags_read_clear_gemv_seg(cudaStream_t stream);
 unsigned flags_read_clear_small_n(cudaStream_t stream);
 unsigned flags_read_clear_gemm(cudaStream_t stream);
 unsigned flags_read_clear_api(cudaStream_t stream);

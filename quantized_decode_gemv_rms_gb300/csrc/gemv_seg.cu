@@ -35,13 +35,15 @@
 
 namespace qdg {
 
+static __device__ unsigned g_flags_gemv_seg;
+
 namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kDepth = 5;                   // row-segments in flight per warp (the consume loop is unrolled by 5)
 constexpr int kSegStride = 1152;            // bytes from one segment to the next: 64 x 16 nibble bytes + 128
-constexpr int kPartFloats = 4096;           // per-chunk partial sums (rows x segments)
+constexpr int kPartFloats = 3072;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
 constexpr int kMaxGroup = 4;
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
@@ -113,19 +115,23 @@ struct Args {
     int64_t start[kMaxGroup];
     int ng;
     const uint8_t* xq;
+    int xq_bulk;            // xq is 16-byte aligned: one bulk copy brings it into shared memory
     int32_t* dbg;
     int64_t O;
 };
 
 // Q8_0 block b of the activations: scale and the 32 codes as 8 words, from
-// 2-byte loads (a 34-byte block is only 2-byte aligned).
+// 2-byte loads (a 34-byte block is only 2-byte aligned), out of shared memory
+// (kShared) or global memory.
+template <bool kShared>
 __device__ __forceinline__ void load_act(const uint8_t* xq, int b, uint32_t* x, float& d, int& sum) {
     const unsigned short* h = reinterpret_cast<const unsigned short*>(xq + static_cast<size_t>(b) * 34);
-    d = half_bits_to_float(__ldg(h));
+    auto ld = [&](int i) -> uint32_t { return kShared ? h[i] : __ldg(h + i); };
+    d = half_bits_to_float(ld(0));
     sum = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        x[i] = static_cast<uint32_t>(__ldg(h + 1 + 2 * i)) | (static_cast<uint32_t>(__ldg(h + 2 + 2 * i)) << 16);
+        x[i] = ld(1 + 2 * i) | (ld(2 + 2 * i) << 16);
         sum = __dp4a(static_cast<int>(x[i]), 0x01010101, sum);
     }
 }
@@ -135,6 +141,8 @@ __device__ __forceinline__ void load_act(const uint8_t* xq, int b, uint32_t* x, 
 template <bool kDebug>
 __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, const __grid_constant__ Plan plan) {
     __shared__ float part[kPartFloats];
+    __shared__ uint64_t xbar;                       // the bulk copy of xq
+    extern __shared__ __align__(16) uint8_t xs[];   // xq (K/32 x 34 bytes) when a.xq_bulk
     const int64_t O = a.O;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -152,6 +160,11 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
     const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * O / gridDim.x;
     const int nrows = static_cast<int>(r1 - r0);
 
+    if (threadIdx.x == 0) {
+        mbar_init(&xbar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
     pdl_trigger();
 
     Entry pipe[kDepth] = {};
@@ -199,8 +212,21 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
     int sa = 0, sb = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) xa[i] = xb[i] = 0u;
-    if (has_a) load_act(a.xq, seg * 64 + lane, xa, dxa, sa);
-    if (has_b) load_act(a.xq, seg * 64 + 32 + lane, xb, dxb, sb);
+    if (a.xq_bulk) {
+        // one bulk copy of the whole vector (one round trip), then the
+        // lanes' blocks out of shared memory
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(plan.nb * 34);
+            mbar_arrive_expect_tx(&xbar, bytes);
+            bulk_g2s_plain(xs, a.xq, bytes, &xbar);
+        }
+        if (!mbar_wait(&xbar, 0)) atomicOr(&g_flags_gemv_seg, FLAG_TIMEOUT);
+        if (has_a) load_act<true>(xs, seg * 64 + lane, xa, dxa, sa);
+        if (has_b) load_act<true>(xs, seg * 64 + 32 + lane, xb, dxb, sb);
+    } else {
+        if (has_a) load_act<false>(a.xq, seg * 64 + lane, xa, dxa, sa);
+        if (has_b) load_act<false>(a.xq, seg * 64 + 32 + lane, xb, dxb, sb);
+    }
 
     // One row-segment: dot the entry, then refill it with the segment kDepth
     // ahead (the refill goes into the registers just read, so no copy of the
@@ -315,13 +341,15 @@ int gemv_seg_launch_group(const void* const* W, float* const* y, const int64_t* 
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
     a.ng = count;
     a.xq = static_cast<const uint8_t*>(xq);
+    a.xq_bulk = aligned(xq, 16) ? 1 : 0;
+    const size_t smem = a.xq_bulk ? static_cast<size_t>(plan.nb) * 34 : 0;   // a multiple of 16 (K % 256 == 0)
     a.dbg = dbg;
     a.O = total;
     cudaError_t e;
     if (dbg)
-        e = launch(gemv_seg_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, false, a, plan);
+        e = launch(gemv_seg_kernel<true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);
     else
-        e = launch(gemv_seg_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
+        e = launch(gemv_seg_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(6);
     return QDG_OK;
@@ -331,6 +359,17 @@ int gemv_seg_launch(const void* W, const void* xq, float* y, int64_t O, int64_t 
                     int32_t* dbg) {
     float* ys[1] = {y};
     return gemv_seg_launch_group(&W, y ? ys : nullptr, &O, 1, xq, K, stream, dbg);
+}
+
+unsigned flags_read_clear_gemv_seg(cudaStream_t stream) {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_flags_gemv_seg, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return ~0u;
+    if (cudaMemcpyToSymbolAsync(g_flags_gemv_seg, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+        return ~0u;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ~0u;
+    return v;
 }
 
 }  // namespace qdg
