@@ -43,6 +43,7 @@ from quantized_decode_gemv_rms_gb300 import synth, workloads  # noqa: E402
 METRIC = "Q4_0×Q8_0 GEMV HBM GB/s (fraction of GB300 peak) and µs/call at batch 1"
 UNIT = "GB/s"
 N_INPUT_SETS = 4
+FUSED_SEG_MAX_K = 8192      # the segment-layout fused kernel stages x and gamma whole
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
@@ -317,16 +318,26 @@ class DecodeStep:
         torch.cuda.synchronize()
         torch.cuda.empty_cache()      # release the fp32 staging of the weights
 
-    def launches_per_step(self, fused=True):
-        return len(self.groups) * (1 if fused else 2)
+    def fusable(self, grp, layout=None):
+        """Whether the fused route can serve this group (the segment-layout
+        fused kernel stages the input whole: K <= FUSED_SEG_MAX_K)."""
+        return (layout or self.layout) == "plain" or grp[0].cols <= FUSED_SEG_MAX_K
 
-    def run_group(self, grp, xs, Ws=None):
+    def launches_per_step(self, fused=True):
+        return sum(1 if fused and self.fusable(g) else 2 for g in self.groups)
+
+    def run_group(self, grp, xs, Ws=None, layout=None):
         """One fused launch for projections that read the same activation."""
+        layout = layout or self.layout
         tag = grp[0].source.split(":", 1)[1]
         g = self.gamma.get(tag) if self.kinds[tag] == "norm" else None
-        Ws = Ws if Ws is not None else [self.W[m.name] for m in grp]
-        self.qdg.q4_0_gemv_rmsnorm_group(Ws, [self.y[m.name] for m in grp], [m.rows for m in grp], xs[tag], g,
-                                         self.wl.eps, grp[0].cols)
+        ys, Os = [self.y[m.name] for m in grp], [m.rows for m in grp]
+        if layout == "seg":
+            Ws = Ws if Ws is not None else [self.Wr[m.name] for m in grp]
+            self.qdg.q4_0s_gemv_rmsnorm_group(Ws, ys, Os, xs[tag], g, self.wl.eps, grp[0].cols)
+        else:
+            Ws = Ws if Ws is not None else [self.W[m.name] for m in grp]
+            self.qdg.q4_0_gemv_rmsnorm_group(Ws, ys, Os, xs[tag], g, self.wl.eps, grp[0].cols)
 
     def run(self, xs, events=None, fused=True):
         """One decode step in dependency order: for each group of projections
@@ -334,7 +345,7 @@ class DecodeStep:
         split: the quantize kernel, then one grouped GEMV launch."""
         qdg = self.qdg
         for grp in self.groups:
-            if fused:
+            if fused and self.fusable(grp):
                 self.run_group(grp, xs)
                 continue
             tag = grp[0].source.split(":", 1)[1]
@@ -396,23 +407,27 @@ def bench_ours(args, wl, world, rank, local):
     # kernels inside a graph, while consecutive graph launches serialise.
     with torch.cuda.stream(side):
         for fz in (fused, not fused):
-            before = [qdg.qdg_launch_count(i) for i in range(8)]
+            before = [qdg.qdg_launch_count(i) for i in range(10)]
 
             def steps(fz=fz):
                 for p in range(N_INPUT_SETS):
                     step.run(step.x_dev[p], fused=fz)
             graphs[fz] = capture(steps, side)
-            after = [qdg.qdg_launch_count(i) for i in range(8)]
-            counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(8)]
+            after = [qdg.qdg_launch_count(i) for i in range(10)]
+            counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(10)]
     stream.wait_stream(side)
     torch.cuda.synchronize()
     ng = len(step.groups)
     gk = 6 if args.layout == "seg" else 1          # launch counter of the split route's GEMV
-    assert counts[True][5] == ng and counts[True][0] == 0 and counts[True][gk] == 0, counts
-    assert counts[False][0] == ng and counts[False][gk] == ng and counts[False][5] == 0, counts
-    assert counts[False][7 - gk] == 0 and counts[True][7 - gk] == 0, counts
+    fk = 9 if args.layout == "seg" else 5          # and of the fused kernel
+    nf = sum(1 for g in step.groups if step.fusable(g))
+    assert counts[True][fk] == nf and counts[True][0] == ng - nf and counts[True][gk] == ng - nf, counts
+    assert counts[False][0] == ng and counts[False][gk] == ng and counts[False][fk] == 0, counts
+    for c in counts.values():
+        assert c[7 - gk] == 0 and c[14 - fk] == 0, counts
     fusion = {"route": "fused" if fused else "split",
-              "per_step_launches": {"fused_norm_gemv": counts[fused][5], "quantize": counts[fused][0],
+              "per_step_launches": {"fused_norm_gemv" + ("_seg" if args.layout == "seg" else ""): counts[fused][fk],
+                                    "quantize": counts[fused][0],
                                     "gemv" + ("_seg" if args.layout == "seg" else ""): counts[fused][gk]}}
 
     def run_steps(n, fz=fused):
@@ -477,7 +492,7 @@ def bench_ours(args, wl, world, rank, local):
     # its own copy of the weights (C copies exceed three L2 sizes, so every
     # launch streams its weights from HBM)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    kinds = ["gemv", "gemv_seg", "fused"]
+    kinds = ["gemv", "gemv_seg", "fused", "fused_seg"]
     per_call = {k: {} for k in kinds}
     launch_bytes = {k: {} for k in kinds}
     for p_ in range(1):
@@ -490,12 +505,14 @@ def bench_ours(args, wl, world, rank, local):
         gbytes = sum(workloads.q4_0_bytes(m.rows, m.cols) for m in grp)
         copies = int(min(160, max(2, -(-3 * l2 // gbytes))))
         for kind in kinds:
-            src = step.Wr if kind == "gemv_seg" else step.W
+            if kind == "fused_seg" and not step.fusable(grp, "seg"):
+                continue
+            src = step.Wr if kind.endswith("_seg") else step.W
             Wc = [[src[m.name] for m in grp]] + [[src[m.name].clone() for m in grp] for _ in range(copies - 1)]
 
             def one(c, kind=kind, Wc=Wc):
-                if kind == "fused":
-                    step.run_group(grp, step.x_dev[0], Ws=Wc[c])
+                if kind.startswith("fused"):
+                    step.run_group(grp, step.x_dev[0], Ws=Wc[c], layout="seg" if kind == "fused_seg" else "plain")
                 else:
                     step.gemv_group(grp, step.xq[tag], Ws=Wc[c], layout="seg" if kind == "gemv_seg" else "plain")
             with torch.cuda.stream(side):
@@ -519,6 +536,7 @@ def bench_ours(args, wl, world, rank, local):
         launch_bytes["fused"][name] = gbytes + xbytes + sum(4 * m.rows for m in grp)
         launch_bytes["gemv"][name] = gbytes + workloads.q8_0_bytes(1, K) + sum(4 * m.rows for m in grp)
         launch_bytes["gemv_seg"][name] = launch_bytes["gemv"][name]
+        launch_bytes["fused_seg"][name] = launch_bytes["fused"][name]
     torch.cuda.synchronize()
     gbs_per_call = {kind: {n: launch_bytes[kind][n] / (per_call[kind][n] * 1e-6) / 1e9 for n in per_call[kind]}
                     for kind in per_call}
@@ -545,14 +563,22 @@ def bench_ours(args, wl, world, rank, local):
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
 
     peaks, peak_src = measured_peaks()
-    kind = "fused" if fused else ("gemv_seg" if args.layout == "seg" else "gemv")
-    kern_bytes = sum(launch_bytes[kind].values())
+    def main_kind(grp):
+        if args.layout == "seg":
+            return "fused_seg" if fused and step.fusable(grp) else "gemv_seg"
+        return "fused" if fused else "gemv"
+    mk = {"+".join(m.name for m in g): main_kind(g) for g in step.groups}
+    kern_bytes = sum(launch_bytes[k][n] for n, k in mk.items())
     # the dominant kernel's average launch from the per-launch graphs above
-    achieved = kern_bytes / (sum(per_call[kind].values()) * 1e-6) / 1e9
-    kernel = {"fused": "gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)",
-              "gemv": "gemv_kernel (q4_0_q8_0_gemv_group)",
-              "gemv_seg": "gemv_seg_kernel (q4_0s_q8_0_gemv_group)"}[kind]
-    traffic = ncu_traffic("gemv_seg.cu" if kind == "gemv_seg" else "gemv.cu")
+    achieved = kern_bytes / (sum(per_call[k][n] for n, k in mk.items()) * 1e-6) / 1e9
+    names = {"fused": "gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)",
+             "gemv": "gemv_kernel (q4_0_q8_0_gemv_group)",
+             "gemv_seg": "gemv_seg_kernel (q4_0s_q8_0_gemv_group)",
+             "fused_seg": "gemv_seg_kernel<fused> (q4_0s_gemv_rmsnorm_group)"}
+    kernel = " + ".join(sorted({names[k] for k in mk.values()}))
+    used = set(mk.values())
+    traffic = (ncu_traffic("gemv_seg.cu") if used == {"gemv_seg"} else
+               ncu_traffic("gemv.cu") if used == {"gemv"} else None)
     roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)" if peak_src == "measured"
@@ -571,10 +597,11 @@ def bench_ours(args, wl, world, rank, local):
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations with 1% x20 outliers)",
         "config": {"workload": wl.name, "batch": 1, "matrices": {m.name: [m.rows, m.cols] for m in wl.matrices},
                    "bytes_per_step": nbytes, "l2": "inputs larger than L2 (419 MB of weights per step vs 129 MB L2)",
-                   "route": ("fused: one RMSNorm->Q8_0->GEMV launch per group" if fused else
-                             "split: quantize kernel + grouped GEMV launch per group" +
-                             ("; weights in the segment layout (repacked at load)" if args.layout == "seg"
-                              else "; weights in plain Q4_0 blocks")) +
+                   "route": (("fused: one RMSNorm->Q8_0->GEMV launch per group" +
+                              (f" (K <= {FUSED_SEG_MAX_K}; split for larger K)" if args.layout == "seg" else ""))
+                             if fused else "split: quantize kernel + grouped GEMV launch per group") +
+                            ("; weights in the segment layout (repacked at load)" if args.layout == "seg"
+                             else "; weights in plain Q4_0 blocks") +
                             "; groups q+k+v, o, gate+up, down, head in dependency order",
                    "launch": ((f"cuda graph of {N_INPUT_SETS} steps" if args.graph else "eager") +
                               (" + PDL" if args.pdl else "")),
@@ -584,7 +611,8 @@ def bench_ours(args, wl, world, rank, local):
         "gbs_per_call": {k: {n: round(v, 1) for n, v in d.items()} for k, d in gbs_per_call.items()},
         "per_call_note": ("one launch per group of projections sharing an input (gemv: on a prepared Q8_0 vector; "
                           "gemv_seg: the same on weights in the segment layout; "
-                          "fused: norm+quantize+GEMV); graph of back-to-back launches on distinct weight copies "
+                          "fused: norm+quantize+GEMV; fused_seg: the same on the segment layout, K <= 8192); "
+                          "graph of back-to-back launches on distinct weight copies "
                           "(> 3 x L2), PDL as configured"),
         "other_route": {"route": "split" if fused else "fused",
                         "us_per_step": round(ms_other * 1e3, 2),

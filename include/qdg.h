@@ -317,6 +317,23 @@ QDG_API int q4_0s_q8_0_gemv_group(const void* const* Wr, float* const* y, const 
                                   const void* xq, int64_t K, qdg_stream_t stream);
 
 /*
+ * q4_0s_gemv_rmsnorm_group -- the fused route on the segment layout: for up
+ * to 4 matrices Wr[g] (segment layout, [O[g]] rows) that share the input x,
+ * one launch runs RMS_NORM + MUL by gamma + Q8_0 quantization of x and the
+ * products y[g] = Wr[g] * xq  [llama.cpp b10909: Metal backend fusion-table
+ * refactor, introduction (RMS_NORM+MUL); GGML: Backend abstraction and
+ * hardware acceleration, section "CUDA: mmvq, mmq, cublas -- three matrix
+ * paths"].  Every CTA quantizes the whole vector with the arithmetic and the
+ * summation order of qnorm_quantize_q8_0, so xq (optionally copied to xq_out,
+ * [K/32] Q8_0, 4-byte aligned) is bit-identical to it and y equals
+ * q4_0s_q8_0_gemv_group on that xq.  x, gamma: fp32 [K], 16-byte aligned;
+ * gamma = NULL quantizes x without a norm.  K multiple of 256, <= 8192.
+ */
+QDG_API int q4_0s_gemv_rmsnorm_group(const void* const* Wr, float* const* y, const int64_t* O, int count,
+                                     const float* x, const float* gamma, float eps, int64_t K, void* xq_out,
+                                     qdg_stream_t stream);
+
+/*
  * qdg_device_status -- synchronise `stream`, then read and clear the device
  * flags of every kernel of this library on the current device.  Returns
  * QDG_OK, QDG_ETIMEOUT (a bounded wait gave up; that call's output is
@@ -342,7 +359,7 @@ QDG_API int qdg_set_option(int option, int64_t value);
  * qdg_launch_count -- number of kernels this library has launched in this
  * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
  * 4 weight quantize, 5 fused norm+gemv, 6 segment-layout gemv, 7 repack,
- * 8 Q8_0-weight gemv, -1 total.  Lets a caller check that the fused kernel
+ * 8 Q8_0-weight gemv, 9 fused norm+gemv on the segment layout, -1 total.  Lets a caller check that the fused kernel
  * is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);

@@ -32,6 +32,7 @@
 #include "common.cuh"
 
 #include <algorithm>
+#include <mutex>
 
 namespace qdg {
 
@@ -46,6 +47,7 @@ constexpr int kSegStride = 1152;            // bytes from one segment to the nex
 constexpr int kPartFloats = 3072;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
 constexpr int kMaxGroup = 4;
+constexpr int kFusedMaxK = 8192;            // fused form: x and gamma staged whole in shared memory
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
 
 struct Plan {
@@ -118,6 +120,12 @@ struct Args {
     int xq_bulk;            // xq is 16-byte aligned: one bulk copy brings it into shared memory
     int32_t* dbg;
     int64_t O;
+    // fused form: fp32 activations, gamma (NULL = no norm), epsilon, optional
+    // copy of the Q8_0 vector (written by CTA 0)
+    const float* x;
+    const float* gamma;
+    float eps;
+    uint8_t* xq_out;
 };
 
 // Q8_0 block b of the activations: scale and the 32 codes as 8 words, from
@@ -138,11 +146,24 @@ __device__ __forceinline__ void load_act(const uint8_t* xq, int b, uint32_t* x, 
 
 // 96 registers a thread: one CTA of 512 threads leaves room on its SM for a
 // CTA of the quantize kernel that prepares the next input.
-template <bool kDebug>
+//
+// Fused form (kFused): the RMS_NORM, the MUL by gamma and the Q8_0
+// quantization of the input run in every CTA before its product, with the
+// arithmetic and the summation order of the standalone quantize kernel, so
+// that the Q8_0 vector is the same bit for bit:
+//   x and gamma arrive in shared memory by two bulk copies (one round trip);
+//   chain j (threads 0..255) sums x_i^2 over i = j (mod 256) ascending with
+//   fma; xor butterflies (16, 8, 4, 2, 1) in each warp; warp totals
+//   ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)); s = 1/sqrt(sum/K + eps);
+//   block b (warp b mod 16, lane = element): v = (x*s)*gamma, d = max|v|/127,
+//   q = round(v/d) (halves away from zero), clamped to +-127.
+template <bool kFused, bool kDebug>
 __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, const __grid_constant__ Plan plan) {
     __shared__ float part[kPartFloats];
-    __shared__ uint64_t xbar;                       // the bulk copy of xq
-    extern __shared__ __align__(16) uint8_t xs[];   // xq (K/32 x 34 bytes) when a.xq_bulk
+    __shared__ float norm_part[8];
+    __shared__ uint64_t xbar;                       // the bulk copies of xq (or of x and gamma)
+    // xq (K/32 x 34 bytes) when a.xq_bulk or kFused; fused form: then x, gamma (K fp32 each)
+    extern __shared__ __align__(16) uint8_t xs[];
     const int64_t O = a.O;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -212,7 +233,77 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
     int sa = 0, sb = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) xa[i] = xb[i] = 0u;
-    if (a.xq_bulk) {
+    if (kFused) {
+        const int nb = plan.nb;
+        const int K = nb * 32;
+        float* xf = reinterpret_cast<float*>(xs + nb * 34);   // nb * 34 is a multiple of 16
+        float* gf = xf + K;
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(K) * 4;
+            mbar_arrive_expect_tx(&xbar, a.gamma != nullptr ? 2 * bytes : bytes);
+            bulk_g2s_plain(xf, a.x, bytes, &xbar);
+            if (a.gamma != nullptr) bulk_g2s_plain(gf, a.gamma, bytes, &xbar);
+        }
+        if (!mbar_wait(&xbar, 0)) atomicOr(&g_flags_gemv_seg, FLAG_TIMEOUT);
+        float s = 1.0f;
+        if (a.gamma != nullptr) {
+            if (threadIdx.x < 256) {
+                float acc = 0.0f;
+                for (int i = threadIdx.x; i < K; i += 256) acc = __fmaf_rn(xf[i], xf[i], acc);
+                acc = warp_sum(acc);
+                if (lane == 0) norm_part[warp] = acc;
+            }
+            __syncthreads();
+            const float ss = __fadd_rn(__fadd_rn(__fadd_rn(norm_part[0], norm_part[1]), __fadd_rn(norm_part[2], norm_part[3])),
+                                       __fadd_rn(__fadd_rn(norm_part[4], norm_part[5]), __fadd_rn(norm_part[6], norm_part[7])));
+            const float mean = __fdiv_rn(ss, static_cast<float>(K));
+            s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, a.eps)));
+        }
+        for (int b0 = warp; b0 < nb; b0 += 4 * kWarps) {
+            float v[4], d[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * kWarps;
+                v[u] = 0.0f;
+                if (b < nb) {
+                    v[u] = xf[(b << 5) + lane];
+                    if (a.gamma != nullptr) v[u] = __fmul_rn(__fmul_rn(v[u], s), gf[(b << 5) + lane]);
+                }
+                d[u] = fabsf(v[u]);
+            }
+#pragma unroll
+            for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+                for (int u = 0; u < 4; ++u) d[u] = fmaxf(d[u], __shfl_xor_sync(0xffffffffu, d[u], h));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int b = b0 + u * kWarps;
+                if (b >= nb) break;
+                const float dd = __fdiv_rn(d[u], 127.0f);
+                int q = 0;
+                if (dd != 0.0f) {
+                    float rr = roundf(__fdiv_rn(v[u], dd));
+                    rr = fminf(fmaxf(rr, -127.0f), 127.0f);
+                    q = static_cast<int>(rr);
+                }
+                uint8_t* blk = xs + b * 34;
+                if (lane == 0) {
+                    const __half dh = __float2half_rn(dd);
+                    *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
+                    if (__hisinf(dh)) atomicOr(&g_flags_gemv_seg, FLAG_OVERFLOW);
+                }
+                blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
+            }
+        }
+        __syncthreads();
+        if (a.xq_out != nullptr && blockIdx.x == 0) {
+            const uint32_t* src = reinterpret_cast<const uint32_t*>(xs);
+            uint32_t* dst = reinterpret_cast<uint32_t*>(a.xq_out);
+            for (int i = threadIdx.x; i < nb * 34 / 4; i += kThreads) dst[i] = src[i];
+        }
+        if (has_a) load_act<true>(xs, seg * 64 + lane, xa, dxa, sa);
+        if (has_b) load_act<true>(xs, seg * 64 + 32 + lane, xb, dxb, sb);
+    } else if (a.xq_bulk) {
         // one bulk copy of the whole vector (one round trip), then the
         // lanes' blocks out of shared memory
         if (threadIdx.x == 0) {
@@ -347,11 +438,58 @@ int gemv_seg_launch_group(const void* const* W, float* const* y, const int64_t* 
     a.O = total;
     cudaError_t e;
     if (dbg)
-        e = launch(gemv_seg_kernel<true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);
+        e = launch(gemv_seg_kernel<false, true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);
     else
-        e = launch(gemv_seg_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
+        e = launch(gemv_seg_kernel<false, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(6);
+    return QDG_OK;
+}
+
+int gemv_seg_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O, int count, const float* x,
+                            const float* gamma, float eps, int64_t K, void* xq_out, cudaStream_t stream) {
+    if (!W || !y || !O || !x) return QDG_EINVAL;
+    if (count < 1 || count > kMaxGroup || K <= 0) return QDG_EINVAL;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
+    if (K % 256 != 0 || K > kFusedMaxK) return QDG_ESHAPE;
+    if (!aligned(x, 16) || (gamma && !aligned(gamma, 16)) || !aligned(xq_out, 4)) return QDG_EALIGN;
+    Args a{};
+    int64_t total = 0;
+    for (int g = 0; g < count; ++g) {
+        if (!W[g] || !y[g] || O[g] <= 0) return QDG_EINVAL;
+        if (!aligned(W[g], 16) || !aligned(y[g], 4)) return QDG_EALIGN;
+        a.Wg[g] = static_cast<const uint8_t*>(W[g]);
+        a.yg[g] = y[g];
+        a.start[g] = total;
+        total += O[g];
+    }
+    if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
+    const DeviceInfo dev = device_info();
+    if (dev.device < 0) return QDG_ECUDA;
+    const Plan plan = make_plan(K);
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
+    a.ng = count;
+    a.x = x;
+    a.gamma = gamma;
+    a.eps = eps;
+    a.xq_out = static_cast<uint8_t*>(xq_out);
+    a.O = total;
+    const size_t smem = static_cast<size_t>(plan.nb) * 34 + static_cast<size_t>(8) * K;
+    {
+        static std::mutex mu;
+        static bool set = false;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!set) {
+            const size_t most = static_cast<size_t>(kFusedMaxK / 32) * 34 + static_cast<size_t>(8) * kFusedMaxK;
+            if (cudaFuncSetAttribute(gemv_seg_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(most)) != cudaSuccess)
+                return QDG_ECUDA;
+            set = true;
+        }
+    }
+    const cudaError_t e = launch(gemv_seg_kernel<true, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
+    if (e != cudaSuccess) return QDG_ECUDA;
+    count_launch(9);
     return QDG_OK;
 }
 
@@ -408,4 +546,10 @@ extern "C" int q4_0s_q8_0_gemv_group(const void* const* Wr, float* const* y, con
                                      const void* xq, int64_t K, qdg_stream_t stream) {
     if (!y) return QDG_EINVAL;
     return gemv_seg_launch_group(Wr, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" int q4_0s_gemv_rmsnorm_group(const void* const* Wr, float* const* y, const int64_t* O, int count,
+                                        const float* x, const float* gamma, float eps, int64_t K, void* xq_out,
+                                        qdg_stream_t stream) {
+    return gemv_seg_rmsnorm_launch(Wr, y, O, count, x, gamma, eps, K, xq_out, reinterpret_cast<cudaStream_t>(stream));
 }

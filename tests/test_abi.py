@@ -26,7 +26,7 @@ def test_header_declares_entry_points():
     names = declared_symbols()
     for must in ("qnorm_quantize_q8_0", "qnorm_add_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
                  "q4_0_q8_0_gemm_workspace_bytes", "quantize_q4_0", "q4_0_repack_seg", "q4_0s_q8_0_gemv",
-                 "q4_0s_q8_0_gemv_group", "q4_0_seg_row_bytes", "q8_0_q8_0_gemv", "q8_0_q8_0_gemv_group",
+                 "q4_0s_q8_0_gemv_group", "q4_0s_gemv_rmsnorm_group", "q4_0_seg_row_bytes", "q8_0_q8_0_gemv", "q8_0_q8_0_gemv_group",
                  "qdg_device_status", "qdg_status_string"):
         assert must in names
 
@@ -139,6 +139,21 @@ def test_fused_host_validation(L):
     assert f(A16, A16, None, 1e-6, A16, 8, 256, A2, None) == -2         # xq_out not 4-byte aligned
 
 
+def test_fused_seg_host_validation(L):
+    f = L.q4_0s_gemv_rmsnorm_group
+    W = (ctypes.c_void_p * 2)(A16, A16)
+    Y = (ctypes.c_void_p * 2)(A16, A16)
+    O = (ctypes.c_int64 * 2)(8, 8)
+    assert f(W, Y, O, 2, None, None, 1e-6, 256, None, None) == -1      # null x
+    assert f(W, Y, O, 0, A16, None, 1e-6, 256, None, None) == -1       # count 0
+    assert f(W, Y, O, 2, A16, None, -1.0, 256, None, None) == -1       # eps < 0
+    assert f(W, Y, O, 2, A16, None, 1e-6, 320, None, None) == -3       # K % 256
+    assert f(W, Y, O, 2, A16, None, 1e-6, 16384, None, None) == -3     # K beyond the fused maximum
+    assert f(W, Y, O, 2, A16 + 4, None, 1e-6, 256, None, None) == -2   # x not 16-byte aligned
+    assert f(W, Y, O, 2, A16, A16 + 8, 1e-6, 256, None, None) == -2    # gamma not 16-byte aligned
+    assert f(W, Y, O, 2, A16, None, 1e-6, 256, A2, None) == -2         # xq_out not 4-byte aligned
+
+
 def test_fused_group_host_validation(L):
     import ctypes
     f = L.q4_0_gemv_rmsnorm_group
@@ -212,8 +227,8 @@ def test_options_and_counters(L):
     assert L.qdg_set_option(1, 2) == -1
     assert L.qdg_set_option(1, 0) == 0
     assert L.qdg_launch_count(-1) >= 0
-    assert L.qdg_launch_count(9) == -1
-    assert L.qdg_launch_count(8) >= 0
+    assert L.qdg_launch_count(10) == -1
+    assert L.qdg_launch_count(9) >= 0
     assert L.qdg_debug_block_sums(A16, A16, None, 8, 256, 1, 0, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 1, 9, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 0, None) == -1   # gemv path needs N == 1

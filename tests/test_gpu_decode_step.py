@@ -3,7 +3,7 @@ benchmark times: a CUDA graph of consecutive steps (one per input set) with
 programmatic dependent launch, through the benchmark's own step object.
 Sampled rows of every projection (the first and last rows, rows on both sides
 of CTA boundaries, and random rows) are compared with the oracle, for the
-split route on the plain and on the segment layout and for the fused route."""
+split and the fused route, each on the plain and on the segment layout."""
 import numpy as np
 import pytest
 
@@ -62,11 +62,11 @@ def step8b():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("route", ["split-plain", "split-seg", "fused"])
+@pytest.mark.parametrize("route", ["split-plain", "split-seg", "fused-plain", "fused-seg"])
 def test_decode_step_full_size_sampled(step8b, expected, route):
     torch = torch_cuda()
-    fused = route == "fused"
-    step8b.layout = "seg" if route == "split-seg" else "plain"
+    fused = route.startswith("fused")
+    step8b.layout = "seg" if route.endswith("-seg") else "plain"
     for p in range(3):                      # eager warm-up (also sets kernel attributes)
         step8b.run(step8b.x_dev[p], fused=fused)
     torch.cuda.synchronize()

@@ -157,3 +157,51 @@ def test_seg_gemv_vocab_head_sampled():
     assert qdg.qdg_device_status() == qdg.QDG_OK
     _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
     assert_within_tol(to_host(y)[rows][None, :], y64, S)
+
+
+@pytest.mark.parametrize("K", [256, 2304, 4096, 8192])
+@pytest.mark.parametrize("norm", [True, False])
+def test_fused_seg_matches_oracle_and_split(K, norm):
+    """The fused form on the segment layout: its Q8_0 vector is the oracle's
+    byte for byte, and its outputs equal the split product on that vector bit
+    for bit (same kernel arithmetic after the activations)."""
+    torch = torch_cuda()
+    O = 1000 + K // 8
+    seed = K + (7 if norm else 0)
+    Wq = oracle.quantize_q4_0(synth.weights(seed, "Wf", O, K))
+    x = synth.activations(seed, "xf", 1, K, outlier_frac=0.01)[0]
+    gam = synth.gamma(seed, "gf", K) if norm else None
+    xq_ref = oracle.quantize_q8_0(x[None, :], gam, 1e-6)
+    Wd = to_dev(oracle.repack_q4_0_seg(Wq, K))
+    xq_out = empty_u8(qdg.q8_0_nbytes(1, K))
+    y = torch.full((O,), float("nan"), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_gemv_rmsnorm_group([Wd], [y], [O], to_dev(x), None if gam is None else to_dev(gam), 1e-6, K,
+                                 xq_out=xq_out)
+    y_split = torch.empty(O, dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemv(Wd, to_dev(xq_ref), y_split, O, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert np.array_equal(to_host(xq_out).reshape(1, -1), xq_ref)
+    got = to_host(y)
+    assert np.array_equal(got.view(np.uint32), to_host(y_split).view(np.uint32))
+    _, y64, S = oracle.matvec(Wq, xq_ref, K, threads=8)
+    assert_within_tol(got[None, :], y64, S)
+
+
+def test_fused_seg_group():
+    """q, k, v in one fused launch against the oracle."""
+    torch = torch_cuda()
+    K = 4096
+    shapes = {"q": 4096, "k": 1024, "v": 1024}
+    Wq = {n: oracle.quantize_q4_0(synth.weights(12, n, O, K)) for n, O in shapes.items()}
+    Wd = [to_dev(oracle.repack_q4_0_seg(Wq[n], K)) for n in shapes]
+    x = synth.activations(12, "xg", 1, K, outlier_frac=0.01)[0]
+    gam = synth.gamma(12, "gg", K)
+    xq_ref = oracle.quantize_q8_0(x[None, :], gam, 1e-6)
+    ys = [torch.empty(O, dtype=torch.float32, device="cuda") for O in shapes.values()]
+    qdg.q4_0s_gemv_rmsnorm_group(Wd, ys, list(shapes.values()), to_dev(x), to_dev(gam), 1e-6, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    for n, y in zip(shapes, ys):
+        _, y64, S = oracle.matvec(Wq[n], xq_ref, K, threads=8)
+        assert_within_tol(to_host(y)[None, :], y64, S, what=n)

@@ -23,8 +23,8 @@ MUTATIONS = {
     "q8_scale_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
     "q8_truncation": ("float r = roundf(v[j] / d);", "float r = truncf(v[j] / d);"),
     "q4_scale_sign": ("float d = m / -8.0f;", "float d = m / 8.0f;"),
-    "activation_column_ignored": ("const uint8_t* xb = xq + (n * nb + b) * 34;\n                double dw",
-                                  "const uint8_t* xb = xq + (b) * 34;\n                double dw"),
+    "activation_column_ignored": ("* 18;\n                const uint8_t* xb = xq + (n * nb + b) * 34;\n                double dw",
+                                  "* 18;\n                const uint8_t* xb = xq + (b) * 34;\n                double dw"),
     "f16_truncating": ("double r = nearbyint(n);", "double r = floor(n);"),
     "mean_over_k_minus_1": ("float mean = ss / (float)K;", "float mean = ss / (float)(K - 1);"),
     "weight_scale_dropped": ("blk += wv * xv;", "blk += (double)(q4_code(wb, j) - 8) * xv;"),
