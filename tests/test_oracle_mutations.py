@@ -27,7 +27,7 @@ MUTATIONS = {
                                   "* 18;\n                const uint8_t* xb = xq + (b) * 34;\n                double dw"),
     "f16_truncating": ("double r = nearbyint(n);", "double r = floor(n);"),
     "mean_over_k_minus_1": ("float mean = ss / (float)K;", "float mean = ss / (float)(K - 1);"),
-    "weight_scale_dropped": ("blk += wv * xv;", "blk += (double)(q4_code(wb, j) - 8) * xv;"),
+    "weight_scale_dropped": ("double wv = dw * (double)(q4_code(wb, j) - 8);", "double wv = (double)(q4_code(wb, j) - 8);"),
     "add_dropped": ("v[j] = v[j] + an[i];", "v[j] = v[j];"),
     "add_before_mul": ("v[j] = v[j] + an[i];", "v[j] = v[j] + an[i] * (gamma ? gamma[i] : 1.0f);"),
     "add_row_stride_ignored": ("const float* an = add ? add + n * ldadd : NULL;", "const float* an = add;"),
