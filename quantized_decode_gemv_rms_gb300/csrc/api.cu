@@ -150,6 +150,10 @@ extern "C" int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum
         case 4:
             if (N != 1) return QDG_EINVAL;
             return gemv_q8w_launch(W, xq, nullptr, O, K, s, isum);
+        case 5:
+            if (N == 1) return gemv_seg_launch(W, xq, nullptr, O, K, s, isum);
+            if (N == 2) return gemv_seg2_launch(W, xq, nullptr, O, O, K, s, isum);
+            return QDG_EINVAL;
         default:
             return QDG_EINVAL;
     }

@@ -406,6 +406,169 @@ __global__ void __launch_bounds__(256) repack_seg_kernel(const uint8_t* __restri
     *reinterpret_cast<uint32_t*>(seg + 16 * r + 4 * lane) = lo | (hi << 16);
 }
 
+// Two activation vectors that share one pass over the weights (the smallest
+// case of the small-N product): the same row/segment split and register ring
+// as the one-vector kernel, the nibbles of each block unpacked once and dotted
+// with both vectors by dp4a.  y[n][row] at y + n * ldy.  One matrix per
+// launch.  A separate kernel, so that the one-vector kernel's code is not
+// touched by the second vector's registers.
+struct Args2 {
+    const uint8_t* W;
+    const uint8_t* xq;      // two Q8_0 vectors, K/32 blocks each, back to back
+    int xq_bulk;
+    float* y;
+    int64_t ldy;
+    int32_t* dbg;           // [2][O][K/32] exact block sums instead of y
+    int64_t O;
+};
+
+__device__ __forceinline__ int nib_dot(const uint32_t* lo, const uint32_t* hi, const uint32_t* x) {
+    int acc = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc = __dp4a(static_cast<int>(lo[i]), static_cast<int>(x[i]), acc);
+        acc = __dp4a(static_cast<int>(hi[i]), static_cast<int>(x[4 + i]), acc);
+    }
+    return acc;
+}
+
+template <bool kDebug>
+__global__ void __maxnreg__(128) gemv_seg2_kernel(const __grid_constant__ Args2 a, const __grid_constant__ Plan plan) {
+    __shared__ float part[kPartFloats];
+    __shared__ uint64_t xbar;
+    extern __shared__ __align__(16) uint8_t xs[];   // both Q8_0 vectors when a.xq_bulk
+    const int64_t O = a.O;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nseg = plan.nseg;
+    const int seg = warp % nseg;
+    const int slot = warp / nseg;
+    const bool worker = slot < plan.nslots;
+    const int r = (seg == nseg - 1) ? plan.rlast : 64;
+    const bool has_a = worker && lane < r;
+    const bool has_b = worker && lane + 32 < r;
+    const int nib_off = seg * kSegStride + 16 * lane;
+    const int sc_off = seg * kSegStride + 16 * r + 4 * lane;
+
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * O / gridDim.x;
+    const int64_t r1 = static_cast<int64_t>(blockIdx.x + 1) * O / gridDim.x;
+    const int nrows = static_cast<int>(r1 - r0);
+
+    if (threadIdx.x == 0) {
+        mbar_init(&xbar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    Entry pipe[kDepth] = {};
+    auto load_seg = [&](int64_t row, Entry& e) {
+        const uint8_t* base = a.W + row * plan.rowbytes;
+        if (has_a) e.a = ldg_stream16(base + nib_off);
+        if (has_b) e.b = ldg_stream16(base + nib_off + 512);
+        e.sc = ldg_stream4(base + sc_off);
+    };
+    auto fill = [&](int64_t c0, int crows) {
+#pragma unroll
+        for (int d = 0; d < kDepth; ++d) {
+            const int ri = slot + d * plan.nslots;
+            if (ri < crows) load_seg(c0 + ri, pipe[d]);
+        }
+    };
+    if (worker) fill(r0, min(nrows, plan.rch));
+
+    pdl_wait();
+
+    uint32_t xa[2][8], xb[2][8];
+    float dxa[2] = {0.0f, 0.0f}, dxb[2] = {0.0f, 0.0f};
+    int sa[2] = {0, 0}, sb[2] = {0, 0};
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xa[n][i] = xb[n][i] = 0u;
+    const int vec = plan.nb * 34;   // bytes of one Q8_0 vector
+    if (a.xq_bulk) {
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(&xbar, static_cast<uint32_t>(2 * vec));
+            bulk_g2s_plain(xs, a.xq, static_cast<uint32_t>(2 * vec), &xbar);
+        }
+        if (!mbar_wait(&xbar, 0)) atomicOr(&g_flags_gemv_seg, FLAG_TIMEOUT);
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            if (has_a) load_act<true>(xs + n * vec, seg * 64 + lane, xa[n], dxa[n], sa[n]);
+            if (has_b) load_act<true>(xs + n * vec, seg * 64 + 32 + lane, xb[n], dxb[n], sb[n]);
+        }
+    } else {
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            if (has_a) load_act<false>(a.xq + n * vec, seg * 64 + lane, xa[n], dxa[n], sa[n]);
+            if (has_b) load_act<false>(a.xq + n * vec, seg * 64 + 32 + lane, xb[n], dxb[n], sb[n]);
+        }
+    }
+
+    // dot the entry with both vectors, refill it, reduce both partials
+    auto consume = [&](int64_t c0, int crows, int ri, Entry& entry) {
+        const Entry& cur = entry;
+        const uint32_t la[4] = {cur.a.x & kNibbles, cur.a.y & kNibbles, cur.a.z & kNibbles, cur.a.w & kNibbles};
+        const uint32_t ha[4] = {(cur.a.x >> 4) & kNibbles, (cur.a.y >> 4) & kNibbles, (cur.a.z >> 4) & kNibbles,
+                                (cur.a.w >> 4) & kNibbles};
+        const uint32_t lb[4] = {cur.b.x & kNibbles, cur.b.y & kNibbles, cur.b.z & kNibbles, cur.b.w & kNibbles};
+        const uint32_t hb[4] = {(cur.b.x >> 4) & kNibbles, (cur.b.y >> 4) & kNibbles, (cur.b.z >> 4) & kNibbles,
+                                (cur.b.w >> 4) & kNibbles};
+        const float dwa = half_bits_to_float(cur.sc);
+        const float dwb = half_bits_to_float(cur.sc >> 16);
+        float acc[2];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            const int ia = nib_dot(la, ha, xa[n]) - 8 * sa[n];
+            const int ib = nib_dot(lb, hb, xb[n]) - 8 * sb[n];
+            acc[n] = __fmul_rn(__fmul_rn(dwa, dxa[n]), static_cast<float>(ia));
+            acc[n] = __fmaf_rn(__fmul_rn(dwb, dxb[n]), static_cast<float>(ib), acc[n]);
+            if (kDebug) {
+                int32_t* d = a.dbg + (n * O + c0 + ri) * plan.nb + seg * 64 + lane;
+                if (has_a) d[0] = ia;
+                if (has_b) d[32] = ib;
+            }
+        }
+        const int ahead = ri + kDepth * plan.nslots;
+        if (ahead < crows) load_seg(c0 + ahead, entry);
+        // both partials in one butterfly: after the first exchange lanes 0..15
+        // carry vector 0 and lanes 16..31 vector 1, each summed in the order of
+        // a plain warp reduction; the totals end in lanes 0 and 16
+        const bool upper = (lane & 16) != 0;
+        float v = upper ? acc[1] : acc[0];
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, upper ? acc[0] : acc[1], 16));
+#pragma unroll
+        for (int h = 8; h >= 1; h >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, h));
+        if ((lane & 15) == 0) part[(ri * nseg + seg) * 2 + (upper ? 1 : 0)] = v;
+    };
+
+    for (int64_t c0 = r0; c0 < r1; c0 += plan.rch) {
+        const int crows = static_cast<int>((r1 - c0) < plan.rch ? (r1 - c0) : plan.rch);
+        if (worker) {
+            if (c0 != r0) fill(c0, crows);
+            const int step = plan.nslots;
+            for (int ri = slot; ri < crows; ri += kDepth * step) {
+                consume(c0, crows, ri, pipe[0]);
+                if (ri + step < crows) consume(c0, crows, ri + step, pipe[1]);
+                if (ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[2]);
+                if (ri + 3 * step < crows) consume(c0, crows, ri + 3 * step, pipe[3]);
+                if (ri + 4 * step < crows) consume(c0, crows, ri + 4 * step, pipe[4]);
+            }
+        }
+        __syncthreads();
+        if (!kDebug) {
+            for (int t = threadIdx.x; t < 2 * crows; t += kThreads) {
+                const int row = t >> 1, n = t & 1;
+                float v = part[row * nseg * 2 + n];
+                for (int g = 1; g < nseg; ++g) v = __fadd_rn(v, part[(row * nseg + g) * 2 + n]);
+                a.y[n * a.ldy + c0 + row] = v;
+            }
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 int gemv_seg_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq,
@@ -493,6 +656,51 @@ int gemv_seg_rmsnorm_launch(const void* const* W, float* const* y, const int64_t
     return QDG_OK;
 }
 
+int gemv_seg2_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K,
+                     cudaStream_t stream, int32_t* dbg) {
+    if (!W || !xq || (!y && !dbg) || O <= 0 || K <= 0 || (y && ldy < O)) return QDG_EINVAL;
+    if (K % 256 != 0 || K > 32768) return QDG_ESHAPE;
+    if (O >= (int64_t(1) << 31)) return QDG_ESHAPE;
+    if (!aligned(W, 16) || !aligned(xq, 2) || !aligned(y, 4) || !aligned(dbg, 4)) return QDG_EALIGN;
+    const DeviceInfo dev = device_info();
+    if (dev.device < 0) return QDG_ECUDA;
+    Plan plan = make_plan(K);
+    plan.rch = (kPartFloats / (plan.nseg * 2)) / plan.nslots * plan.nslots;
+    Args2 a{};
+    a.W = static_cast<const uint8_t*>(W);
+    a.xq = static_cast<const uint8_t*>(xq);
+    a.xq_bulk = aligned(xq, 16) ? 1 : 0;
+    a.y = y;
+    a.ldy = ldy;
+    a.dbg = dbg;
+    a.O = O;
+    const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
+    const size_t smem = a.xq_bulk ? static_cast<size_t>(2) * plan.nb * 34 : 0;
+    {
+        // both vectors of the largest K (2 x 1024 x 34 bytes) exceed the default 48 KB
+        static std::mutex mu;
+        static bool set = false;
+        std::lock_guard<std::mutex> lock(mu);
+        if (!set) {
+            const int most = 2 * (32768 / 32) * 34;
+            if (cudaFuncSetAttribute(gemv_seg2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(gemv_seg2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
+                    cudaSuccess)
+                return QDG_ECUDA;
+            set = true;
+        }
+    }
+    cudaError_t e;
+    if (dbg)
+        e = launch(gemv_seg2_kernel<true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);
+    else
+        e = launch(gemv_seg2_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
+    if (e != cudaSuccess) return QDG_ECUDA;
+    count_launch(6);
+    return QDG_OK;
+}
+
 int gemv_seg_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
                     int32_t* dbg) {
     float* ys[1] = {y};
@@ -552,4 +760,16 @@ extern "C" int q4_0s_gemv_rmsnorm_group(const void* const* Wr, float* const* y, 
                                         const float* x, const float* gamma, float eps, int64_t K, void* xq_out,
                                         qdg_stream_t stream) {
     return gemv_seg_rmsnorm_launch(Wr, y, O, count, x, gamma, eps, K, xq_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int q4_0s_q8_0_gemm_small_n(const void* Wr, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K,
+                                       int64_t N, qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N == 1) {
+        if (ldy < O) return QDG_EINVAL;
+        return gemv_seg_launch(Wr, xq, y, O, K, s, nullptr);
+    }
+    if (N == 2) return gemv_seg2_launch(Wr, xq, y, ldy, O, K, s, nullptr);
+    return QDG_EINVAL;
 }

@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
             sig["q8_0_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
             sig["q8_0_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
             sig["q4_0s_gemv_rmsnorm_group"] = ([p, p, p, i32, p, p, f32, i64, p, p], i32)
+            sig["q4_0s_q8_0_gemm_small_n"] = ([p, p, p, i64, i64, i64, i64, p], i32)
             sig["q4_0_seg_row_bytes"] = ([i64], i64)
             sig["q4_0_repack_seg"] = ([p, p, i64, i64, p], i32)
             sig["q4_0s_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
@@ -232,6 +233,12 @@ def q4_0s_gemv_rmsnorm_group(Ws, ys, Os, x, gamma, eps: float, K: int, xq_out=No
     O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
     _check(lib().q4_0s_gemv_rmsnorm_group(W_arr, y_arr, O_arr, n, _ptr(x), _ptr(gamma), float(eps), K,
                                           _ptr(xq_out), _stream(stream)), "q4_0s_gemv_rmsnorm_group")
+
+
+def q4_0s_q8_0_gemm_small_n(Wr, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:
+    """Small-N product on the segment layout, N = 1 or 2."""
+    _check(lib().q4_0s_q8_0_gemm_small_n(_ptr(Wr), _ptr(xq), _ptr(y), ldy, O, K, N, _stream(stream)),
+           "q4_0s_q8_0_gemm_small_n")
 
 
 def q4_0_q8_0_gemm_small_n(W, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:

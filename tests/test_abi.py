@@ -26,7 +26,7 @@ def test_header_declares_entry_points():
     names = declared_symbols()
     for must in ("qnorm_quantize_q8_0", "qnorm_add_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
                  "q4_0_q8_0_gemm_workspace_bytes", "quantize_q4_0", "q4_0_repack_seg", "q4_0s_q8_0_gemv",
-                 "q4_0s_q8_0_gemv_group", "q4_0s_gemv_rmsnorm_group", "q4_0_seg_row_bytes", "q8_0_q8_0_gemv", "q8_0_q8_0_gemv_group",
+                 "q4_0s_q8_0_gemv_group", "q4_0s_gemv_rmsnorm_group", "q4_0s_q8_0_gemm_small_n", "q4_0_seg_row_bytes", "q8_0_q8_0_gemv", "q8_0_q8_0_gemv_group",
                  "qdg_device_status", "qdg_status_string"):
         assert must in names
 
@@ -137,6 +137,18 @@ def test_fused_host_validation(L):
     assert f(A16, A16 + 4, None, 1e-6, A16, 8, 256, None, None) == -2   # x not 16-byte aligned
     assert f(A16, A16, A16 + 8, 1e-6, A16, 8, 256, None, None) == -2    # gamma not 16-byte aligned
     assert f(A16, A16, None, 1e-6, A16, 8, 256, A2, None) == -2         # xq_out not 4-byte aligned
+
+
+def test_seg_small_n_host_validation(L):
+    f = L.q4_0s_q8_0_gemm_small_n
+    assert f(A16, A16, A16, 8, 8, 256, 3, None) == -1      # N = 3 is not served on this layout
+    assert f(A16, A16, A16, 8, 8, 256, 0, None) == -1      # N = 0
+    assert f(A16, A16, None, 8, 8, 256, 2, None) == -1     # null y
+    assert f(A16, A16, A16, 4, 8, 256, 2, None) == -1      # ldy < O
+    assert f(A16, A16, A16, 8, 8, 384, 2, None) == -3      # K % 256
+    assert f(A2, A16, A16, 8, 8, 256, 2, None) == -2       # Wr not 16-byte aligned
+    assert f(A16, A16 + 1, A16, 8, 8, 256, 2, None) == -2  # xq not 2-byte aligned
+    assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 3, 5, None) == -1   # segment small-N: N <= 2
 
 
 def test_fused_seg_host_validation(L):

@@ -205,3 +205,59 @@ def test_fused_seg_group():
     for n, y in zip(shapes, ys):
         _, y64, S = oracle.matvec(Wq[n], xq_ref, K, threads=8)
         assert_within_tol(to_host(y)[None, :], y64, S, what=n)
+
+
+SEG2_SHAPES = [(1, 256), (300, 256), (37, 2304), (1000, 2048), (153, 4096), (17, 4352), (4096, 14336),
+               (14336, 4096), (40, 32768)]
+
+
+@pytest.mark.parametrize("O,K", SEG2_SHAPES)
+def test_seg_small_n2_block_sums_exact(O, K):
+    torch = torch_cuda()
+    w = synth.weights(O + 3 * K, "W2", O, K)
+    x = synth.activations(O + 3 * K, "x2", 2, K, outlier_frac=0.01)
+    Wq, xq = oracle.quantize_q4_0(w), oracle.quantize_q8_0(x, None)
+    isum = torch.full((2, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(to_dev(oracle.repack_q4_0_seg(Wq, K)), to_dev(xq), isum, O, K, 2, 5)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(isum), oracle.block_sums(Wq, xq, K))
+
+
+@pytest.mark.parametrize("O,K", SEG2_SHAPES)
+@pytest.mark.parametrize("N", [1, 2])
+def test_seg_small_n_output_within_tolerance(O, K, N):
+    """y [N][ldy] with ldy > O: the padding stays untouched."""
+    torch = torch_cuda()
+    w = synth.weights(O * 5 + K + N, "W2", O, K)
+    x = synth.activations(O * 5 + K + N, "x2", N, K, outlier_frac=0.01)
+    gam = synth.gamma(O + K, "g2", K)
+    Wq, xq = oracle.quantize_q4_0(w), oracle.quantize_q8_0(x, gam, 1e-6)
+    ldy = O + 3
+    y = torch.full((N, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemm_small_n(to_dev(oracle.repack_q4_0_seg(Wq, K)), to_dev(xq), y, ldy, O, K, N)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    got = to_host(y)
+    assert np.all(np.isnan(got[:, O:]))
+    rows = None if O <= 4096 else synth.sample_indices(O, "rows2", O, 2048)
+    _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
+    assert_within_tol(got[:, :O] if rows is None else got[:, rows], y64, S)
+
+
+def test_seg_small_n2_matches_two_single_calls():
+    """Each column of the two-vector product equals the one-vector kernel's
+    result within the tolerance, and both columns are deterministic."""
+    torch = torch_cuda()
+    O, K = 14336, 4096
+    Wq = oracle.quantize_q4_0(synth.weights(21, "W22", O, K))
+    xq = oracle.quantize_q8_0(synth.activations(21, "x22", 2, K, outlier_frac=0.01), None)
+    Wd, xd = to_dev(oracle.repack_q4_0_seg(Wq, K)), to_dev(xq)
+    y2 = torch.empty((2, O), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemm_small_n(Wd, xd, y2, O, O, K, 2)
+    y2b = torch.empty((2, O), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemm_small_n(Wd, xd, y2b, O, O, K, 2)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(y2).view(np.uint32), to_host(y2b).view(np.uint32))
+    rows = synth.sample_indices(O, "rows22", O, 1024)
+    _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
+    assert_within_tol(to_host(y2)[:, rows], y64, S)
