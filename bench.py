@@ -299,14 +299,33 @@ class DecodeStep:
         self.gamma = {tag: torch.from_numpy(synth.gamma(wl.seed, tag, K)).to(device)
                       for tag, K in wl.activations.items() if self.kinds[tag] == "norm"}
         # input sets: host (pinned) and device copies
-        self.x_host = [{tag: torch.from_numpy(synth.activations(wl.seed, f"x:{tag}:{p}", 1, K,
-                                                                outlier_frac=wl.outlier_frac)[0]).pin_memory()
-                        for tag, K in wl.activations.items()} for p in range(N_INPUT_SETS)]
-        self.x_dev = [{tag: t.to(device) for tag, t in xs.items()} for xs in self.x_host]
+        # input sets: one pinned host buffer and one device buffer per set, holding every
+        # activation vector back to back (one copy moves a step's inputs); outputs likewise
+        xoff, off = {}, 0
+        for tag, K in wl.activations.items():
+            xoff[tag] = (off, K)
+            off += K
+        self.x_host_flat, self.x_dev_flat, self.x_host, self.x_dev = [], [], [], []
+        for p in range(N_INPUT_SETS):
+            hf = torch.empty(off, dtype=torch.float32).pin_memory()
+            for tag, (o, K) in xoff.items():
+                hf[o:o + K] = torch.from_numpy(synth.activations(wl.seed, f"x:{tag}:{p}", 1, K,
+                                                                 outlier_frac=wl.outlier_frac)[0])
+            df = hf.to(device)
+            self.x_host_flat.append(hf)
+            self.x_dev_flat.append(df)
+            self.x_host.append({tag: hf[o:o + K] for tag, (o, K) in xoff.items()})
+            self.x_dev.append({tag: df[o:o + K] for tag, (o, K) in xoff.items()})
         self.xq = {tag: torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
                    for tag, K in wl.activations.items()}
-        self.y = {m.name: torch.empty(m.rows, dtype=torch.float32, device=device) for m in wl.matrices}
-        self.y_host = {m.name: torch.empty(m.rows, dtype=torch.float32).pin_memory() for m in wl.matrices}
+        ytotal = sum(m.rows for m in wl.matrices)
+        self.y_flat = torch.empty(ytotal, dtype=torch.float32, device=device)
+        self.y_host_flat = torch.empty(ytotal, dtype=torch.float32).pin_memory()
+        self.y, self.y_host, off = {}, {}, 0
+        for m in wl.matrices:
+            self.y[m.name] = self.y_flat[off:off + m.rows]
+            self.y_host[m.name] = self.y_host_flat[off:off + m.rows]
+            off += m.rows
         # consecutive projections with the same input (and K) form one launch
         self.groups = []
         for m in wl.matrices:
@@ -541,23 +560,35 @@ def bench_ours(args, wl, world, rank, local):
     gbs_per_call = {kind: {n: launch_bytes[kind][n] / (per_call[kind][n] * 1e-6) / 1e9 for n in per_call[kind]}
                     for kind in per_call}
 
-    # ---- end to end through the same calls, inputs from pinned host memory
-    n_e2e = max(10, min(args.steps, 500))
+    # ---- end to end through the same calls, inputs from pinned host memory:
+    # every step copies its input vectors host -> device (one copy), runs, and
+    # copies every output device -> host (one copy); with graphs, the copies are
+    # nodes of the same graph as the kernels (N_INPUT_SETS steps per graph)
+    n_e2e = N_INPUT_SETS * max(3, min(args.steps, 500) // N_INPUT_SETS)
     h2d = sum(t.numel() * 4 for t in step.x_host[0].values())
     d2h = sum(t.numel() * 4 for t in step.y_host.values())
-    e2e_graphs = None
+    e2e_graph = None
     if args.graph:
+        def e2e_steps():
+            for p in range(N_INPUT_SETS):
+                _e2e_step(step, None, p, fused)
         with torch.cuda.stream(side):
-            e2e_graphs = [capture(lambda p=p: step.run(step.x_dev[p], fused=fused), side) for p in range(N_INPUT_SETS)]
+            e2e_graph = capture(e2e_steps, side)
         stream.wait_stream(side)
         torch.cuda.synchronize()
-    for k in range(3):
-        _e2e_step(step, e2e_graphs, k, fused)
+
+    def run_e2e(n):
+        if e2e_graph is not None:
+            for _ in range(n // N_INPUT_SETS):
+                e2e_graph.replay()
+        else:
+            for k in range(n):
+                _e2e_step(step, None, k, fused)
+    run_e2e(N_INPUT_SETS)
     torch.cuda.synchronize()
     barrier(world)
     f0.record(stream)
-    for k in range(n_e2e):
-        _e2e_step(step, e2e_graphs, k, fused)
+    run_e2e(n_e2e)
     f1.record(stream)
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
@@ -620,7 +651,10 @@ def bench_ours(args, wl, world, rank, local):
         "fusion_check": fusion,
         "roofline": roof,
         "e2e": {"value": round(nbytes * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": UNIT,
-                "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": ("every step: one host-to-device copy of its input vectors from pinned memory, the step "
+                        "through the C ABI, one device-to-host copy of all outputs" +
+                        (f"; copies and kernels in one CUDA graph of {N_INPUT_SETS} steps" if args.graph else ""))},
         "gpu_launches": int(L * args.steps),
         "clocks": clocks,
     }
@@ -758,14 +792,9 @@ def bench_extras(args, device):
 
 def _e2e_step(step, graphs, k, fused=True):
     p = k % N_INPUT_SETS
-    for tag, t in step.x_host[p].items():
-        step.x_dev[p][tag].copy_(t, non_blocking=True)
-    if graphs:
-        graphs[p].replay()
-    else:
-        step.run(step.x_dev[p], fused=fused)
-    for name, t in step.y_host.items():
-        t.copy_(step.y[name], non_blocking=True)
+    step.x_dev_flat[p].copy_(step.x_host_flat[p], non_blocking=True)   # every input vector, one copy
+    step.run(step.x_dev[p], fused=fused)
+    step.y_host_flat.copy_(step.y_flat, non_blocking=True)              # every output, one copy
 
 
 def main():
