@@ -335,7 +335,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
     uint8_t* buf = seg_buf[warp];
     // One row-segment: stage it through shared memory, refill its ring entry
     // with the segment kDepth ahead, dot it, reduce it.
-    auto consume = [&](int64_t c0, int crows, int ri, SegRegs<kW>& entry) {
+    auto consume = [&](int64_t c0, int crows, int ri, SegRegs<kW>& entry) -> float {
         // Store first (this waits for the entry's loads, issued kDepth steps
         // ago), then reuse the same registers for the segment kDepth ahead.
 #pragma unroll
@@ -386,8 +386,23 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
             }
         }
         __syncwarp();
-        acc = warp_sum(acc);
-        if (lane == 0) part[ri * nseg + seg] = acc;
+        if (kW == kQ4) {
+            acc = warp_sum(acc);
+            if (lane == 0) part[ri * nseg + seg] = acc;
+        }
+        return acc;
+    };
+    // Q8_0 weights: two row-segments (rows ri and ri2) reduced in one
+    // butterfly; after the first exchange lanes 0..15 carry row ri and lanes
+    // 16..31 row ri2, each summed in the order of a plain warp reduction.
+    auto reduce2 = [&](int ri, int ri2, bool two, float acc0, float acc1) {
+        const bool upper = (lane & 16) != 0;
+        float v = upper ? acc1 : acc0;
+        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, upper ? acc0 : acc1, 16));
+#pragma unroll
+        for (int h = 8; h >= 1; h >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, h));
+        if (lane == 0) part[ri * nseg + seg] = v;
+        if (lane == 16 && two) part[ri2 * nseg + seg] = v;
     };
 
     for (int64_t c0 = r0; c0 < r1; c0 += plan.rch) {
@@ -398,10 +413,20 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
             // access to it uses a compile-time index: each step then waits only
             // for its own loads, issued kDepth steps earlier.
             const int step = plan.nslots;
-            for (int ri = slot; ri < crows; ri += kDepth * step) {
-                consume(c0, crows, ri, pipe[0]);
-                if (ri + step < crows) consume(c0, crows, ri + step, pipe[1]);
-                if (kDepth > 2 && ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[kDepth > 2 ? 2 : 0]);
+            if (kW == kQ8) {
+                for (int ri = slot; ri < crows; ri += 2 * step) {
+                    const float p0 = consume(c0, crows, ri, pipe[0]);
+                    const bool two = ri + step < crows;
+                    const float p1 = two ? consume(c0, crows, ri + step, pipe[1]) : 0.0f;
+                    reduce2(ri, ri + step, two, p0, p1);
+                }
+            } else {
+                for (int ri = slot; ri < crows; ri += kDepth * step) {
+                    consume(c0, crows, ri, pipe[0]);
+                    if (ri + step < crows) consume(c0, crows, ri + step, pipe[1]);
+                    if (kDepth > 2 && ri + 2 * step < crows)
+                        consume(c0, crows, ri + 2 * step, pipe[kDepth > 2 ? 2 : 0]);
+                }
             }
         }
         __syncthreads();
