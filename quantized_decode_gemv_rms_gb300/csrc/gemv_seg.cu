@@ -25,9 +25,8 @@
 //     ahead of use (74 KB in flight per SM); the matching Q8_0 activations
 //     stay in registers.
 //   * Exact block sums with dp4a (minus 8 * sum(q_x)), scaled by d_w * d_x;
-//     the ring is consumed in pairs of rows whose partials share one warp
-//     butterfly; segment partials combined per row in a fixed order
-//     (deterministic).
+//     the four rows of the ring share one warp butterfly; segment partials
+//     combined per row in a fixed order (deterministic).
 //   * Programmatic dependent launch: the first row-segments of W are
 //     requested before the kernel waits for the preceding grid.
 #include "common.cuh"
@@ -43,7 +42,7 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kDepth1 = 4;                  // one-vector kernel: row-segments in flight per warp (consumed in pairs)
+constexpr int kDepth1 = 4;                  // one-vector kernel: row-segments in flight per warp (reduced together)
 constexpr int kDepth = 5;                   // two-vector kernel: row-segments in flight per warp (loop unrolled by 5)
 constexpr int kSegStride = 1152;            // bytes from one segment to the next: 64 x 16 nibble bytes + 128
 constexpr int kPartFloats = 3072;           // per-chunk partial sums (rows x segments)
@@ -325,8 +324,8 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
     // ahead (the refill goes into the registers just read, so no copy of the
     // entry is kept alive across the loads); returns the lane's partial.
     // Measured on GB300 this order streams about 20% faster than refilling
-    // before the dot, and sharing the butterfly between two rows (reduce2)
-    // took the 8B decode step from 88.3 to 86.2 us.
+    // before the dot; sharing one butterfly between the ring's rows (reduce4)
+    // took the 8B decode step from 88.3 to 84.6 us.
     auto consume = [&](int64_t c0, int crows, int ri, Entry& entry) -> float {
         const Entry& cur = entry;
         // lanes without a block hold zero activations and zero scales
@@ -345,16 +344,21 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
         if (ahead < crows) load_seg(c0 + ahead, entry);
         return acc;
     };
-    // two row-segments (rows ri and ri + step) reduced in one butterfly: after
-    // the first exchange lanes 0..15 carry row ri and lanes 16..31 the other
-    auto reduce2 = [&](int ri, int ri2, bool two, float acc0, float acc1) {
-        const bool upper = (lane & 16) != 0;
-        float v = upper ? acc1 : acc0;
-        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, upper ? acc0 : acc1, 16));
+    // four row-segments (rows ri + k * step) reduced in one butterfly: the
+    // xor-16 exchange leaves rows 0, 1 in lanes 0..15 and rows 2, 3 in lanes
+    // 16..31, the xor-8 exchange one row per eight lanes; every row is summed
+    // in the order of a plain warp reduction and ends in lane 8 * k
+    auto reduce4 = [&](int ri, int step, int crows, float v0, float v1, float v2, float v3) {
+        const bool up16 = (lane & 16) != 0, up8 = (lane & 8) != 0;
+        float k0 = up16 ? v2 : v0, k1 = up16 ? v3 : v1;
+        k0 = __fadd_rn(k0, __shfl_xor_sync(0xffffffffu, up16 ? v0 : v2, 16));
+        k1 = __fadd_rn(k1, __shfl_xor_sync(0xffffffffu, up16 ? v1 : v3, 16));
+        float m = up8 ? k1 : k0;
+        m = __fadd_rn(m, __shfl_xor_sync(0xffffffffu, up8 ? k0 : k1, 8));
 #pragma unroll
-        for (int h = 8; h >= 1; h >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, h));
-        if (lane == 0) part[ri * nseg + seg] = v;
-        if (lane == 16 && two) part[ri2 * nseg + seg] = v;
+        for (int h = 4; h >= 1; h >>= 1) m = __fadd_rn(m, __shfl_xor_sync(0xffffffffu, m, h));
+        const int k = lane >> 3;
+        if ((lane & 7) == 0 && ri + k * step < crows) part[(ri + k * step) * nseg + seg] = m;
     };
 
     for (int64_t c0 = r0; c0 < r1; c0 += plan.rch) {
@@ -363,18 +367,11 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
             if (c0 != r0) fill(c0, crows);
             const int step = plan.nslots;
             for (int ri = slot; ri < crows; ri += kDepth1 * step) {
-                {
-                    const float p0 = consume(c0, crows, ri, pipe[0]);
-                    const bool two = ri + step < crows;
-                    const float p1 = two ? consume(c0, crows, ri + step, pipe[1]) : 0.0f;
-                    reduce2(ri, ri + step, two, p0, p1);
-                }
-                if (ri + 2 * step < crows) {
-                    const float p0 = consume(c0, crows, ri + 2 * step, pipe[2]);
-                    const bool two = ri + 3 * step < crows;
-                    const float p1 = two ? consume(c0, crows, ri + 3 * step, pipe[3]) : 0.0f;
-                    reduce2(ri + 2 * step, ri + 3 * step, two, p0, p1);
-                }
+                const float p0 = consume(c0, crows, ri, pipe[0]);
+                const float p1 = ri + step < crows ? consume(c0, crows, ri + step, pipe[1]) : 0.0f;
+                const float p2 = ri + 2 * step < crows ? consume(c0, crows, ri + 2 * step, pipe[2]) : 0.0f;
+                const float p3 = ri + 3 * step < crows ? consume(c0, crows, ri + 3 * step, pipe[3]) : 0.0f;
+                reduce4(ri, step, crows, p0, p1, p2, p3);
             }
         }
         __syncthreads();
