@@ -42,8 +42,7 @@ namespace {
 
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kDepth1 = 4;                  // one-vector kernel: row-segments in flight per warp (reduced together)
-constexpr int kDepth = 5;                   // two-vector kernel: row-segments in flight per warp (loop unrolled by 5)
+constexpr int kDepth1 = 4;                  // row-segments in flight per warp, reduced together in one butterfly
 constexpr int kSegStride = 1152;            // bytes from one segment to the next: 64 x 16 nibble bytes + 128
 constexpr int kPartFloats = 3072;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
@@ -479,7 +478,7 @@ __global__ void __maxnreg__(128) gemv_seg2_kernel(const __grid_constant__ Args2 
     __syncthreads();
     pdl_trigger();
 
-    Entry pipe[kDepth] = {};
+    Entry pipe[kDepth1] = {};
     auto load_seg = [&](int64_t row, Entry& e) {
         const uint8_t* base = a.W + row * plan.rowbytes;
         if (has_a) e.a = ldg_stream16(base + nib_off);
@@ -488,7 +487,7 @@ __global__ void __maxnreg__(128) gemv_seg2_kernel(const __grid_constant__ Args2 
     };
     auto fill = [&](int64_t c0, int crows) {
 #pragma unroll
-        for (int d = 0; d < kDepth; ++d) {
+        for (int d = 0; d < kDepth1; ++d) {
             const int ri = slot + d * plan.nslots;
             if (ri < crows) load_seg(c0 + ri, pipe[d]);
         }
@@ -524,8 +523,8 @@ __global__ void __maxnreg__(128) gemv_seg2_kernel(const __grid_constant__ Args2 
         }
     }
 
-    // dot the entry with both vectors, refill it, reduce both partials
-    auto consume = [&](int64_t c0, int crows, int ri, Entry& entry) {
+    // dot the entry with both vectors, refill it; returns the lane's two partials
+    auto consume = [&](int64_t c0, int crows, int ri, Entry& entry, float& r0v, float& r1v) {
         const Entry& cur = entry;
         const uint32_t la[4] = {cur.a.x & kNibbles, cur.a.y & kNibbles, cur.a.z & kNibbles, cur.a.w & kNibbles};
         const uint32_t ha[4] = {(cur.a.x >> 4) & kNibbles, (cur.a.y >> 4) & kNibbles, (cur.a.z >> 4) & kNibbles,
@@ -548,17 +547,31 @@ __global__ void __maxnreg__(128) gemv_seg2_kernel(const __grid_constant__ Args2 
                 if (has_b) d[32] = ib;
             }
         }
-        const int ahead = ri + kDepth * plan.nslots;
+        const int ahead = ri + kDepth1 * plan.nslots;
         if (ahead < crows) load_seg(c0 + ahead, entry);
-        // both partials in one butterfly: after the first exchange lanes 0..15
-        // carry vector 0 and lanes 16..31 vector 1, each summed in the order of
-        // a plain warp reduction; the totals end in lanes 0 and 16
-        const bool upper = (lane & 16) != 0;
-        float v = upper ? acc[1] : acc[0];
-        v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, upper ? acc[0] : acc[1], 16));
+        r0v = acc[0];
+        r1v = acc[1];
+    };
+
+    // eight partials (four rows x two vectors, v[2 r + n]) in one butterfly:
+    // the xor-16, xor-8 and xor-4 exchanges leave value 4 b16 + 2 b8 + b4 in
+    // the lanes whose bits 4, 3, 2 are b16, b8, b4, each summed in the order of
+    // a plain warp reduction; the totals end in lanes 4 g
+    auto reduce8 = [&](int ri, int step, int crows, const float (&v)[8]) {
+        const bool u16 = (lane & 16) != 0, u8 = (lane & 8) != 0, u4 = (lane & 4) != 0;
+        float w4[4], w2[2];
 #pragma unroll
-        for (int h = 8; h >= 1; h >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, h));
-        if ((lane & 15) == 0) part[(ri * nseg + seg) * 2 + (upper ? 1 : 0)] = v;
+        for (int q = 0; q < 4; ++q)
+            w4[q] = __fadd_rn(u16 ? v[4 + q] : v[q], __shfl_xor_sync(0xffffffffu, u16 ? v[q] : v[4 + q], 16));
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            w2[q] = __fadd_rn(u8 ? w4[2 + q] : w4[q], __shfl_xor_sync(0xffffffffu, u8 ? w4[q] : w4[2 + q], 8));
+        float c = __fadd_rn(u4 ? w2[1] : w2[0], __shfl_xor_sync(0xffffffffu, u4 ? w2[0] : w2[1], 4));
+        c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, 2));
+        c = __fadd_rn(c, __shfl_xor_sync(0xffffffffu, c, 1));
+        const int g = lane >> 2;
+        const int row = ri + (g >> 1) * step;
+        if ((lane & 3) == 0 && row < crows) part[(row * nseg + seg) * 2 + (g & 1)] = c;
     };
 
     for (int64_t c0 = r0; c0 < r1; c0 += plan.rch) {
@@ -566,12 +579,13 @@ __global__ void __maxnreg__(128) gemv_seg2_kernel(const __grid_constant__ Args2 
         if (worker) {
             if (c0 != r0) fill(c0, crows);
             const int step = plan.nslots;
-            for (int ri = slot; ri < crows; ri += kDepth * step) {
-                consume(c0, crows, ri, pipe[0]);
-                if (ri + step < crows) consume(c0, crows, ri + step, pipe[1]);
-                if (ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[2]);
-                if (ri + 3 * step < crows) consume(c0, crows, ri + 3 * step, pipe[3]);
-                if (ri + 4 * step < crows) consume(c0, crows, ri + 4 * step, pipe[4]);
+            for (int ri = slot; ri < crows; ri += kDepth1 * step) {
+                float v[8] = {};
+                consume(c0, crows, ri, pipe[0], v[0], v[1]);
+                if (ri + step < crows) consume(c0, crows, ri + step, pipe[1], v[2], v[3]);
+                if (ri + 2 * step < crows) consume(c0, crows, ri + 2 * step, pipe[2], v[4], v[5]);
+                if (ri + 3 * step < crows) consume(c0, crows, ri + 3 * step, pipe[3], v[6], v[7]);
+                reduce8(ri, step, crows, v);
             }
         }
         __syncthreads();
