@@ -426,14 +426,14 @@ def bench_ours(args, wl, world, rank, local):
     # kernels inside a graph, while consecutive graph launches serialise.
     with torch.cuda.stream(side):
         for fz in (fused, not fused):
-            before = [qdg.qdg_launch_count(i) for i in range(10)]
+            before = [qdg.qdg_launch_count(i) for i in range(11)]
 
             def steps(fz=fz):
                 for p in range(N_INPUT_SETS):
                     step.run(step.x_dev[p], fused=fz)
             graphs[fz] = capture(steps, side)
-            after = [qdg.qdg_launch_count(i) for i in range(10)]
-            counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(10)]
+            after = [qdg.qdg_launch_count(i) for i in range(11)]
+            counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(11)]
     stream.wait_stream(side)
     torch.cuda.synchronize()
     ng = len(step.groups)
@@ -561,37 +561,43 @@ def bench_ours(args, wl, world, rank, local):
                     for kind in per_call}
 
     # ---- end to end through the same calls, inputs from pinned host memory:
-    # every step copies its input vectors host -> device (one copy), runs, and
-    # copies every output device -> host (one copy); with graphs, the copies are
-    # nodes of the same graph as the kernels (N_INPUT_SETS steps per graph)
+    # every step moves its input vectors host -> device (one copy), runs, and
+    # moves every output device -> host (one copy).  The headline stages with
+    # the library's copy kernel (qdg_stage_copy); the copy-engine variant is
+    # measured beside it.  With graphs, the copies are nodes of the same graph
+    # as the kernels (N_INPUT_SETS steps per graph).
     n_e2e = N_INPUT_SETS * max(3, min(args.steps, 500) // N_INPUT_SETS)
     h2d = sum(t.numel() * 4 for t in step.x_host[0].values())
     d2h = sum(t.numel() * 4 for t in step.y_host.values())
-    e2e_graph = None
-    if args.graph:
-        def e2e_steps():
-            for p in range(N_INPUT_SETS):
-                _e2e_step(step, None, p, fused)
-        with torch.cuda.stream(side):
-            e2e_graph = capture(e2e_steps, side)
-        stream.wait_stream(side)
-        torch.cuda.synchronize()
 
-    def run_e2e(n):
-        if e2e_graph is not None:
-            for _ in range(n // N_INPUT_SETS):
-                e2e_graph.replay()
-        else:
-            for k in range(n):
-                _e2e_step(step, None, k, fused)
-    run_e2e(N_INPUT_SETS)
-    torch.cuda.synchronize()
-    barrier(world)
-    f0.record(stream)
-    run_e2e(n_e2e)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    ms_e2e = max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
+    def measure_e2e(staging):
+        e2e_graph = None
+        if args.graph:
+            def e2e_steps():
+                for p in range(N_INPUT_SETS):
+                    _e2e_step(step, None, p, fused, staging)
+            with torch.cuda.stream(side):
+                e2e_graph = capture(e2e_steps, side)
+            stream.wait_stream(side)
+            torch.cuda.synchronize()
+
+        def run_e2e(n):
+            if e2e_graph is not None:
+                for _ in range(n // N_INPUT_SETS):
+                    e2e_graph.replay()
+            else:
+                for k in range(n):
+                    _e2e_step(step, None, k, fused, staging)
+        run_e2e(N_INPUT_SETS)
+        torch.cuda.synchronize()
+        barrier(world)
+        f0.record(stream)
+        run_e2e(n_e2e)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(f0.elapsed_time(f1) / n_e2e, world, device)
+    ms_e2e = measure_e2e("kernel")
+    ms_e2e_engine = measure_e2e("engine")
 
     peaks, peak_src = measured_peaks()
     def main_kind(grp):
@@ -653,8 +659,12 @@ def bench_ours(args, wl, world, rank, local):
         "e2e": {"value": round(nbytes * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": UNIT,
                 "ms_per_step": round(ms_e2e, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": ("every step: one host-to-device copy of its input vectors from pinned memory, the step "
-                        "through the C ABI, one device-to-host copy of all outputs" +
-                        (f"; copies and kernels in one CUDA graph of {N_INPUT_SETS} steps" if args.graph else ""))},
+                        "through the C ABI, one device-to-host copy of all outputs; both copies by the library's "
+                        "staging kernel (qdg_stage_copy) reading and writing the mapped pinned buffers" +
+                        (f"; copies and kernels in one CUDA graph of {N_INPUT_SETS} steps" if args.graph else "")),
+                "copy_engine": {"value": round(nbytes * world / (ms_e2e_engine * 1e-3) / 1e9, 1),
+                                "ms_per_step": round(ms_e2e_engine, 5),
+                                "how": "the same with stream-ordered copy-engine copies instead of the kernel"}},
         "gpu_launches": int(L * args.steps),
         "clocks": clocks,
     }
@@ -790,11 +800,21 @@ def bench_extras(args, device):
     return out
 
 
-def _e2e_step(step, graphs, k, fused=True):
+def _e2e_step(step, graphs, k, fused=True, staging="kernel"):
+    """One step from host buffers: every input vector in (one copy), the step,
+    every output out (one copy).  staging="kernel": the library's staging
+    kernel reads and writes the mapped pinned buffers (the copies stay in the
+    chain of dependent launches); "engine": stream-ordered copy-engine copies."""
     p = k % N_INPUT_SETS
-    step.x_dev_flat[p].copy_(step.x_host_flat[p], non_blocking=True)   # every input vector, one copy
+    if staging == "kernel":
+        step.qdg.qdg_stage_copy(step.x_dev_flat[p], step.x_host_flat[p])
+    else:
+        step.x_dev_flat[p].copy_(step.x_host_flat[p], non_blocking=True)
     step.run(step.x_dev[p], fused=fused)
-    step.y_host_flat.copy_(step.y_flat, non_blocking=True)              # every output, one copy
+    if staging == "kernel":
+        step.qdg.qdg_stage_copy(step.y_host_flat, step.y_flat)
+    else:
+        step.y_host_flat.copy_(step.y_flat, non_blocking=True)
 
 
 def main():

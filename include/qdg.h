@@ -370,11 +370,30 @@ enum qdg_option { QDG_OPT_PDL = 1 };
 QDG_API int qdg_set_option(int option, int64_t value);
 
 /*
+ * qdg_stage_copy -- copy `bytes` bytes from src to dst with a kernel on
+ * `stream`: the host <-> device move of a decode step's input vectors and
+ * outputs.  Either pointer may be device memory or pinned host memory that is
+ * mapped into the device's address space (memory from cudaHostAlloc, or
+ * PyTorch's pin_memory(), on a unified-address system); the kernel reaches
+ * host memory over the CPU-GPU link, so no copy engine is involved and, with
+ * QDG_OPT_PDL set, the copy stays in the chain of dependent launches (the
+ * kernel waits for the preceding grid before it touches either buffer, and
+ * the next kernel may launch while it runs).
+ *   dst, src  16-byte aligned, non-overlapping; caller-owned.
+ *   bytes     a multiple of 16 (0: nothing launched).
+ * Errors: QDG_EINVAL for a null pointer, negative size, overlapping ranges,
+ * or a pointer the device cannot reach (pageable host memory); QDG_EALIGN
+ * for an unaligned pointer or size; QDG_ECUDA if the launch fails.
+ * Asynchronous: dst is complete when the stream reaches the copy's end.
+ */
+QDG_API int qdg_stage_copy(void* dst, const void* src, int64_t bytes, qdg_stream_t stream);
+
+/*
  * qdg_launch_count -- number of kernels this library has launched in this
  * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
  * 4 weight quantize, 5 fused norm+gemv, 6 segment-layout gemv, 7 repack,
- * 8 Q8_0-weight gemv, 9 fused norm+gemv on the segment layout, -1 total.  Lets a caller check that the fused kernel
- * is the one that ran.
+ * 8 Q8_0-weight gemv, 9 fused norm+gemv on the segment layout, 10 staging copy, -1 total.  Lets a caller check
+ * that the fused kernel is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);
 

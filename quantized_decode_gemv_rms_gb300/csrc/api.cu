@@ -13,7 +13,7 @@ namespace {
 std::mutex g_dev_mutex;
 DeviceInfo g_dev_cache[64];
 std::atomic<int> g_pdl{0};
-std::atomic<int64_t> g_counts[10];
+std::atomic<int64_t> g_counts[11];
 }  // namespace
 
 DeviceInfo device_info() {
@@ -84,7 +84,7 @@ extern "C" int64_t qdg_launch_count(int which) {
         for (auto& c : g_counts) t += c.load();
         return t;
     }
-    if (which < 0 || which >= 10) return -1;
+    if (which < 0 || which >= 11) return -1;
     return g_counts[which].load();
 }
 

@@ -73,6 +73,7 @@ def lib() -> ctypes.CDLL:
             sig["q4_0_repack_seg"] = ([p, p, i64, i64, p], i32)
             sig["q4_0s_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
             sig["q4_0s_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
+            sig["qdg_stage_copy"] = ([p, p, i64, p], i32)
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
                 fn.argtypes = args
@@ -192,6 +193,14 @@ def q4_0_seg_nbytes(O: int, K: int) -> int:
 def q4_0_repack_seg(W, Wr, O: int, K: int, stream=None) -> None:
     """Q4_0 rows -> segment layout (load time, bit-exact rearrangement)."""
     _check(lib().q4_0_repack_seg(_ptr(W), _ptr(Wr), O, K, _stream(stream)), "q4_0_repack_seg")
+
+
+def qdg_stage_copy(dst, src, nbytes: int | None = None, stream=None) -> None:
+    """Kernel copy between device memory and mapped pinned host memory (a
+    step's inputs in, its outputs out); nbytes defaults to src's size."""
+    if nbytes is None:
+        nbytes = src.numel() * src.element_size()
+    _check(lib().qdg_stage_copy(_ptr(dst), _ptr(src), int(nbytes), _stream(stream)), "qdg_stage_copy")
 
 
 def q4_0s_q8_0_gemv(Wr, xq, y, O: int, K: int, stream=None) -> None:

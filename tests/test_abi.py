@@ -234,13 +234,24 @@ def test_quantize_q4_0_host_validation(L):
     assert f(A2 + 1, 32, 1, 32, A16, None) == -2
 
 
+def test_stage_copy_rejects_bad_arguments(L):
+    f = L.qdg_stage_copy
+    assert f(None, A16, 16, None) == -1
+    assert f(A16, None, 16, None) == -1
+    assert f(A16, A16, -16, None) == -1
+    assert f(A16, A16, 0, None) == 0                     # nothing to do, nothing launched
+    assert f(A16 + 8, A16, 16, None) == -2
+    assert f(A16, A16 + 4, 16, None) == -2
+    assert f(A16, A16, 24, None) == -2                   # size not a multiple of 16
+
+
 def test_options_and_counters(L):
     assert L.qdg_set_option(99, 1) == -1
     assert L.qdg_set_option(1, 2) == -1
     assert L.qdg_set_option(1, 0) == 0
     assert L.qdg_launch_count(-1) >= 0
-    assert L.qdg_launch_count(10) == -1
-    assert L.qdg_launch_count(9) >= 0
+    assert L.qdg_launch_count(11) == -1
+    assert L.qdg_launch_count(10) >= 0
     assert L.qdg_debug_block_sums(A16, A16, None, 8, 256, 1, 0, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 1, 9, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 2, 0, None) == -1   # gemv path needs N == 1
