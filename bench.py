@@ -495,6 +495,23 @@ def bench_ours(args, wl, world, rank, local):
     torch.cuda.synchronize()
     clocks = sampler.stop()
 
+    # ---- spread of the step time: events around each of R graph replays
+    # (N_INPUT_SETS steps each), outside the timed region above
+    dist = None
+    if args.graph:
+        reps = max(20, min(200, args.steps // N_INPUT_SETS))
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        evs[0].record(stream)
+        for i in range(reps):
+            graphs[fused].replay()
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+        per = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / N_INPUT_SETS for i in range(reps))
+        pick = lambda q: per[min(reps - 1, int(round(q * (reps - 1))))]
+        dist = {"p10": round(pick(0.1), 2), "p50": round(pick(0.5), 2), "p90": round(pick(0.9), 2),
+                "samples": reps, "unit": "us per step",
+                "how": f"CUDA events around each replay of the {N_INPUT_SETS}-step graph"}
+
     # ---- the other route, same number of steps, for comparison
     run_steps(args.warmup, not fused)
     torch.cuda.synchronize()
@@ -644,6 +661,7 @@ def bench_ours(args, wl, world, rank, local):
                               (" + PDL" if args.pdl else "")),
                    "parallelism": f"replicas x{world}"},
         "us_per_step": round(ms * 1e3, 2),
+        "us_per_step_spread": dist,
         "us_per_call": {k: {n: round(v, 2) for n, v in d.items()} for k, d in per_call.items()},
         "gbs_per_call": {k: {n: round(v, 1) for n, v in d.items()} for k, d in gbs_per_call.items()},
         "per_call_note": ("one launch per group of projections sharing an input (gemv: on a prepared Q8_0 vector; "
