@@ -758,22 +758,24 @@ def bench_extras(args, device):
             nbytes = workloads.gemv_algorithmic_bytes(O, K, N)
             res[f"N{N}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
                             "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
-        # N = 2 on the segment layout (dp4a, one unpack for both vectors)
+        # every N on the segment layout (N = 2: dp4a with one unpack for both
+        # vectors; N >= 3: the MMA kernel with lanes loading straight into registers)
         Wr = torch.empty(qdg.q4_0_seg_nbytes(O, K), dtype=torch.uint8, device=device)
         qdg.q4_0_repack_seg(Wq, Wr, O, K)
         Wrs = [Wr] + [Wr.clone() for _ in range(copies - 1)]
-        x = torch.from_numpy(synth.activations(workloads.SMALL_N_SEED, f"smalln-x-{K}", 2, K)).to(device)
-        xq = torch.empty(qdg.q8_0_nbytes(2, K), dtype=torch.uint8, device=device)
-        qdg.qnorm_quantize_q8_0(x, g, 1e-6, xq)
-        y = torch.empty((2, O), dtype=torch.float32, device=device)
-        us = timed_graph(lambda i: qdg.q4_0s_q8_0_gemm_small_n(Wrs[i % copies], xq, y, O, O, K, 2), copies)
-        nbytes = workloads.gemv_algorithmic_bytes(O, K, 2)
-        res["N2_seg"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-                         "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
+        for N in workloads.SMALL_N_COLS:
+            x = torch.from_numpy(synth.activations(workloads.SMALL_N_SEED, f"smalln-x-{K}", N, K)).to(device)
+            xq = torch.empty(qdg.q8_0_nbytes(N, K), dtype=torch.uint8, device=device)
+            qdg.qnorm_quantize_q8_0(x, g, 1e-6, xq)
+            y = torch.empty((N, O), dtype=torch.float32, device=device)
+            us = timed_graph(lambda i: qdg.q4_0s_q8_0_gemm_small_n(Wrs[i % copies], xq, y, O, O, K, N), copies)
+            nbytes = workloads.gemv_algorithmic_bytes(O, K, N)
+            res[f"N{N}_seg"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4)}
         del Wrs, Wr
         out["small_n"][f"{O}x{K}"] = dict(res, weight_copies=copies,
                                           timing="graph of back-to-back launches over the weight copies; "
-                                                 "N2_seg = the two-vector kernel on the segment layout")
+                                                 "N<n> = plain Q4_0 layout, N<n>_seg = the same on the segment layout")
         del Ws, Wq
         torch.cuda.empty_cache()
     for (O, K, T) in (workloads.PREFILL_SHAPES if args.only in (None, "prefill") else ()):

@@ -318,14 +318,17 @@ QDG_API int q4_0s_q8_0_gemv_group(const void* const* Wr, float* const* y, const 
 
 /*
  * q4_0s_q8_0_gemm_small_n -- the small-N product on the segment layout for
- * N = 1 or 2 vectors sharing one pass over W (the smallest speculative-decode
- * batches; N = 3..8 use q4_0_q8_0_gemm_small_n on the plain layout).  At
- * N = 2 each block's nibbles are unpacked once and dotted with both vectors
- * by dp4a (the MMA route's operand building costs more than it saves at this
- * N).  Wr [O][q4_0_seg_row_bytes(K)], 16-byte aligned; xq: N Q8_0 vectors of
- * K/32 blocks back to back, 2-byte aligned (16-byte alignment lets one bulk
- * copy bring them in); y: [N][ldy] fp32, ldy >= O.  K multiple of 256,
- * <= 32768; 1 <= O < 2^31.  QDG_EINVAL for other N.
+ * N = 1..8 vectors sharing one pass over W (speculative / parallel decode).
+ * N = 1 is q4_0s_q8_0_gemv.  At N = 2 each block's nibbles are unpacked once
+ * and dotted with both vectors by dp4a.  N = 3..8 form the exact block sums
+ * with the fp16 warp MMA as q4_0_q8_0_gemm_small_n does, each lane loading
+ * its own nibble and scale words straight from the segment layout into
+ * registers (two row tiles ahead); for K > 4096 a thread-block cluster of
+ * ceil(K/4096) CTAs splits K.  Wr [O][q4_0_seg_row_bytes(K)], 16-byte
+ * aligned; xq: N Q8_0 vectors of K/32 blocks back to back (16-byte aligned
+ * for N >= 3, 2-byte aligned for N <= 2); y: [N][ldy] fp32, ldy >= O.
+ * K multiple of 256, <= 32768; 1 <= O < 2^31.  Deterministic (fixed
+ * reduction order).  QDG_EINVAL for N outside 1..8.
  */
 QDG_API int q4_0s_q8_0_gemm_small_n(const void* Wr, const void* xq, float* y, int64_t ldy, int64_t O,
                                     int64_t K, int64_t N, qdg_stream_t stream);
@@ -404,7 +407,7 @@ QDG_API int64_t qdg_launch_count(int which);
  * path: 0 = gemv (N must be 1), 1 = small-N, 2 = prefill gemm (N = T tokens),
  * 3 = segment-layout gemv (W in the segment layout, N must be 1),
  * 4 = Q8_0-weight gemv (W in Q8_0 blocks, N must be 1), 5 = segment-layout
- * small-N (W in the segment layout, N = 1 or 2).
+ * small-N (W in the segment layout, N = 1..8).
  * Same argument rules as the corresponding entry point.
  */
 QDG_API int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum, int64_t O,

@@ -109,7 +109,7 @@ extern "C" int qdg_device_status(qdg_stream_t stream) {
     }
     unsigned f = 0;
     const unsigned parts[] = {flags_read_clear_quantize(s), flags_read_clear_gemv(s), flags_read_clear_gemv_seg(s),
-                              flags_read_clear_small_n(s),
+                              flags_read_clear_small_n(s), flags_read_clear_small_n_seg(s),
                               flags_read_clear_gemm(s), flags_read_clear_api(s)};
     for (unsigned p : parts) {
         if (p == ~0u) {
@@ -153,7 +153,7 @@ extern "C" int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum
         case 5:
             if (N == 1) return gemv_seg_launch(W, xq, nullptr, O, K, s, isum);
             if (N == 2) return gemv_seg2_launch(W, xq, nullptr, O, O, K, s, isum);
-            return QDG_EINVAL;
+            return small_n_seg_launch(W, xq, nullptr, O, O, K, N, s, isum);
         default:
             return QDG_EINVAL;
     }

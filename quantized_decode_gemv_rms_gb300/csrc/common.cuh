@@ -230,6 +230,8 @@ int gemv_seg_launch(const void* W, const void* xq, float* y, int64_t O, int64_t 
                     int32_t* dbg);
 int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t N,
                    cudaStream_t stream, int32_t* dbg);
+int small_n_seg_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t N,
+                       cudaStream_t stream, int32_t* dbg);
 int64_t gemm_workspace_bytes(int64_t K, int64_t T);
 int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t T, void* ws,
                 int64_t ws_bytes, cudaStream_t stream, int32_t* dbg);
@@ -239,6 +241,7 @@ unsigned flags_read_clear_quantize(cudaStream_t stream);
 unsigned flags_read_clear_gemv(cudaStream_t stream);
 unsigned flags_read_clear_gemv_seg(cudaStream_t stream);
 unsigned flags_read_clear_small_n(cudaStream_t stream);
+unsigned flags_read_clear_small_n_seg(cudaStream_t stream);
 unsigned flags_read_clear_gemm(cudaStream_t stream);
 unsigned flags_read_clear_api(cudaStream_t stream);
 

@@ -245,7 +245,7 @@ def q4_0s_gemv_rmsnorm_group(Ws, ys, Os, x, gamma, eps: float, K: int, xq_out=No
 
 
 def q4_0s_q8_0_gemm_small_n(Wr, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:
-    """Small-N product on the segment layout, N = 1 or 2."""
+    """Small-N product on the segment layout, N = 1..8."""
     _check(lib().q4_0s_q8_0_gemm_small_n(_ptr(Wr), _ptr(xq), _ptr(y), ldy, O, K, N, _stream(stream)),
            "q4_0s_q8_0_gemm_small_n")
 

@@ -141,14 +141,17 @@ def test_fused_host_validation(L):
 
 def test_seg_small_n_host_validation(L):
     f = L.q4_0s_q8_0_gemm_small_n
-    assert f(A16, A16, A16, 8, 8, 256, 3, None) == -1      # N = 3 is not served on this layout
+    assert f(A16, A16, A16, 8, 8, 256, 9, None) == -1      # N = 9
     assert f(A16, A16, A16, 8, 8, 256, 0, None) == -1      # N = 0
+    assert f(A16, A16, A16, 4, 8, 256, 3, None) == -1      # ldy < O (MMA path)
+    assert f(A16, A16, A16, 8, 8, 384, 5, None) == -3      # K % 256 (MMA path)
+    assert f(A16, A16 + 2, A16, 8, 8, 256, 8, None) == -2  # xq not 16-byte aligned (MMA path)
     assert f(A16, A16, None, 8, 8, 256, 2, None) == -1     # null y
     assert f(A16, A16, A16, 4, 8, 256, 2, None) == -1      # ldy < O
     assert f(A16, A16, A16, 8, 8, 384, 2, None) == -3      # K % 256
     assert f(A2, A16, A16, 8, 8, 256, 2, None) == -2       # Wr not 16-byte aligned
     assert f(A16, A16 + 1, A16, 8, 8, 256, 2, None) == -2  # xq not 2-byte aligned
-    assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 3, 5, None) == -1   # segment small-N: N <= 2
+    assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 9, 5, None) == -1   # segment small-N: N <= 8
 
 
 def test_fused_seg_host_validation(L):

@@ -212,19 +212,20 @@ SEG2_SHAPES = [(1, 256), (300, 256), (37, 2304), (1000, 2048), (153, 4096), (17,
 
 
 @pytest.mark.parametrize("O,K", SEG2_SHAPES)
-def test_seg_small_n2_block_sums_exact(O, K):
+@pytest.mark.parametrize("N", [2, 3, 8])
+def test_seg_small_n_block_sums_exact(O, K, N):
     torch = torch_cuda()
     w = synth.weights(O + 3 * K, "W2", O, K)
-    x = synth.activations(O + 3 * K, "x2", 2, K, outlier_frac=0.01)
+    x = synth.activations(O + 3 * K + N, "x2", N, K, outlier_frac=0.01)
     Wq, xq = oracle.quantize_q4_0(w), oracle.quantize_q8_0(x, None)
-    isum = torch.full((2, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
-    qdg.qdg_debug_block_sums(to_dev(oracle.repack_q4_0_seg(Wq, K)), to_dev(xq), isum, O, K, 2, 5)
+    isum = torch.full((N, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(to_dev(oracle.repack_q4_0_seg(Wq, K)), to_dev(xq), isum, O, K, N, 5)
     torch.cuda.synchronize()
     assert np.array_equal(to_host(isum), oracle.block_sums(Wq, xq, K))
 
 
 @pytest.mark.parametrize("O,K", SEG2_SHAPES)
-@pytest.mark.parametrize("N", [1, 2])
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 8])
 def test_seg_small_n_output_within_tolerance(O, K, N):
     """y [N][ldy] with ldy > O: the padding stays untouched."""
     torch = torch_cuda()
@@ -261,3 +262,21 @@ def test_seg_small_n2_matches_two_single_calls():
     rows = synth.sample_indices(O, "rows22", O, 1024)
     _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
     assert_within_tol(to_host(y2)[:, rows], y64, S)
+
+
+@pytest.mark.parametrize("O,K,N", [(14336, 4096, 8), (4096, 14336, 8), (1000, 2048, 3), (37, 2304, 5),
+                                   (300, 256, 4), (40, 32768, 6)])
+def test_seg_small_n_mma_matches_plain_layout_kernel(O, K, N):
+    """N >= 3 on the segment layout runs the plain-layout kernel's arithmetic
+    in the same order, so the two agree bit for bit."""
+    torch = torch_cuda()
+    Wq = oracle.quantize_q4_0(synth.weights(O + K, "W3", O, K))
+    xq = oracle.quantize_q8_0(synth.activations(O + K + N, "x3", N, K, outlier_frac=0.01), None)
+    ys = torch.full((N, O), float("nan"), dtype=torch.float32, device="cuda")
+    yp = torch.full((N, O), float("nan"), dtype=torch.float32, device="cuda")
+    xd = to_dev(xq)
+    qdg.q4_0s_q8_0_gemm_small_n(to_dev(oracle.repack_q4_0_seg(Wq, K)), xd, ys, O, O, K, N)
+    qdg.q4_0_q8_0_gemm_small_n(to_dev(Wq), xd, yp, O, O, K, N)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert np.array_equal(to_host(ys).view(np.uint32), to_host(yp).view(np.uint32))
