@@ -5,28 +5,23 @@
 // paths": the vector case of the quantized matrix-vector route].
 //
 // Arithmetic and work split are those of the plain-layout kernel
-// (gemm_small_n.cu): exact block sums from the fp16 warp MMA m16n8k16 on
-// integer-valued operands, a warp per 8-block chunk of K with its activation
-// fragments in registers, 16-row tiles, partial sums combined in a fixed
-// order across the CTA's warps and, for K > 4096, across a thread-block
-// cluster.  What differs is how the weights arrive.  In the segment layout a
-// lane's word t of block b of a row (its elements 4t..4t+3 and 16+4t..
-// 16+4t+3) is one aligned 32-bit word at 1152 s + 16 i + 4 t, and the fp16
-// scales of a chunk's 8 blocks are 8 consecutive aligned words at the end of
-// the segment.  So each lane loads its own operands straight from global
-// memory into registers -- no tensor copies, no shared-memory stages, no
-// per-tile refill hand-off between warps -- with the next two tiles of its
-// chunk in flight (a two-entry register ring, each entry dotted before it is
-// refilled, as in the segment-layout GEMV).
-//
-// Measured on GB300 this path is slower than the plain-layout kernel (about
-// 19 against 12 us for N = 8 on 14336 x 4096): each 4-byte load of a warp
-// touches 16 bytes in each of 8 rows, and a deeper (three-tile) ring did not
-// change the time.  It exists so that weights kept only in the segment
-// layout serve every N from 1 to 8; the plain layout is the faster choice
-// for N >= 3.
+// (gemm_small_n.cu), so the results are the same bit for bit: exact block
+// sums from the fp16 warp MMA m16n8k16 on integer-valued operands, a warp per
+// 8-block chunk of K with its activation fragments in registers, 16-row
+// tiles, partial sums combined in a fixed order across the CTA's warps and,
+// for K > 4096, across a thread-block cluster.  What differs is the weight
+// path.  In the segment layout a chunk's bytes of one row are 128 contiguous
+// nibble bytes and 32 contiguous scale bytes, so each warp stages only what
+// it reads itself: per tile, five 16-byte asynchronous copies a lane (every
+// warp instruction moving four whole 128-byte row pieces) into a private
+// three-tile ring in shared memory, with no hand-off between warps.  The
+// staged rows are 144 and 48 bytes apart, so the 8 rows a fragment load
+// touches fall in 8 different bank groups; a lane's word t of block i
+// (elements 4t..4t+3 and 16+4t..16+4t+3) is one aligned 32-bit load, and a
+// block's fp16 scale one broadcast 32-bit load.
 #include "common.cuh"
 #include "small_n.cuh"
+#include "tma.cuh"
 
 #include <algorithm>
 #include <map>
@@ -61,60 +56,40 @@ struct SArgs {
     int part_floats; // partial-sum area (also receives the activations)
 };
 
-// One tile's operands for one lane: word t of each of the chunk's 8 blocks
-// of rows g and g + 8, and the 8 scale words of each row (block j's scale is
-// the low or the high half of word j, the same half for the whole chunk).
-struct Unit {
-    uint32_t wa[kChunkBlocks], wb[kChunkBlocks];
-    uint4 sa0, sa1, sb0, sb1;
-};
-
-__device__ __forceinline__ uint32_t ldg_u32(const uint8_t* p) { return __ldg(reinterpret_cast<const unsigned*>(p)); }
-__device__ __forceinline__ uint4 ldg_u128(const uint8_t* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
-
-// Rows past O are not read; their operands are zero.
-__device__ __forceinline__ void load_unit(const SArgs& a, int64_t row0, int g, int noff, int soff, Unit& u) {
-    const int64_t ra = row0 + g, rb = ra + 8;
-    if (ra < a.O) {
-        const uint8_t* p = a.W + ra * a.rowbytes;
-#pragma unroll
-        for (int j = 0; j < kChunkBlocks; ++j) u.wa[j] = ldg_u32(p + noff + 16 * j);
-        u.sa0 = ldg_u128(p + soff);
-        u.sa1 = ldg_u128(p + soff + 16);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kChunkBlocks; ++j) u.wa[j] = 0u;
-        u.sa0 = u.sa1 = make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (rb < a.O) {
-        const uint8_t* p = a.W + rb * a.rowbytes;
-#pragma unroll
-        for (int j = 0; j < kChunkBlocks; ++j) u.wb[j] = ldg_u32(p + noff + 16 * j);
-        u.sb0 = ldg_u128(p + soff);
-        u.sb1 = ldg_u128(p + soff + 16);
-    } else {
-#pragma unroll
-        for (int j = 0; j < kChunkBlocks; ++j) u.wb[j] = 0u;
-        u.sb0 = u.sb1 = make_uint4(0u, 0u, 0u, 0u);
-    }
+// 16-byte asynchronous copy global -> shared (L2 only); src_bytes 0 writes
+// zeros and reads nothing.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 
-template <int kJ>
-__device__ __forceinline__ uint32_t word_of(const uint4& lo, const uint4& hi) {
-    const uint4& v = kJ < 4 ? lo : hi;
-    return (kJ & 3) == 0 ? v.x : (kJ & 3) == 1 ? v.y : (kJ & 3) == 2 ? v.z : v.w;
-}
+// A warp's stage: its chunk's bytes of one 16-row tile, [16 rows][128 nibble
+// bytes + 16 pad] then [16 rows][32 scale bytes + 16 pad].  The 144- and
+// 48-byte row strides put the 8 rows a fragment load touches in 8 different
+// bank groups.
+constexpr int kNibStride = 144;
+constexpr int kScStride = 48;
+constexpr int kWarpStage = kTileRows * (kNibStride + kScStride);   // 3072 bytes
+constexpr int kSegStages = 3;                                       // tiles of a warp in flight
 
-// Block kJ of the chunk for rows g, g + 8 and columns 2t, 2t + 1: the exact
-// block sums (d0..d3) and acc += d_w d_x isum, as in the plain-layout kernel.
-// hs: 0 or 16, the half of the scale words that holds this chunk's scales.
+// Block kJ of the chunk for rows g, g + 8 of a staged tile, columns 2t, 2t + 1:
+// the exact block sums (d0..d3) and acc += d_w d_x isum, as in the
+// plain-layout kernel.  hs: 0 or 16, the half of the scale words that holds
+// this chunk's scales.
 template <int kJ>
-__device__ __forceinline__ void seg_block_step(const Unit& u, int hs, int t, const XBlock& x, const XTab* tab,
-                                               float (&acc)[4], float (&isum)[4]) {
-    const uint32_t w0 = u.wa[kJ], w1 = u.wb[kJ];
+__device__ __forceinline__ void staged_block_step(const uint8_t* st, int g, int t, int hs, const XBlock& x,
+                                                  const XTab* tab, float (&acc)[4], float (&isum)[4]) {
+    const uint32_t w0 = *reinterpret_cast<const uint32_t*>(st + g * kNibStride + 16 * kJ + 4 * t);
+    const uint32_t w1 = *reinterpret_cast<const uint32_t*>(st + (g + 8) * kNibStride + 16 * kJ + 4 * t);
+    const uint8_t* sc = st + kTileRows * kNibStride;
+    const uint32_t dw0 = *reinterpret_cast<const uint32_t*>(sc + g * kScStride + 4 * kJ) >> hs;
+    const uint32_t dw1 = *reinterpret_cast<const uint32_t*>(sc + (g + 8) * kScStride + 4 * kJ) >> hs;
     const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
-    const uint32_t dw0 = word_of<kJ>(u.sa0, u.sa1) >> hs;
-    const uint32_t dw1 = word_of<kJ>(u.sb0, u.sb1) >> hs;
     const XTab e = tab[kJ * 4 + t];
     float d0, d1, d2, d3;
     hmma2(d0, d1, d2, d3, lo_pair(w0), lo_pair(w1), lo_pair(v0), lo_pair(v1), x.b[0], x.b[1], hi_pair(w0),
@@ -134,9 +109,12 @@ __device__ __forceinline__ void seg_block_step(const Unit& u, int hs, int t, con
 }
 
 // Shared memory: [head: activation barrier, abort flag][per-warp tables]
-// [partial sums, which first receive the activations][cluster partials].
+// [per-warp stage rings][partial sums, which first receive the
+// activations][cluster partials].
 constexpr int kSHeadBytes = 128;
-constexpr int kSTabBytes = kMaxWarps * kChunkBlocks * 4 * 16;   // 8 KB
+constexpr int kSTabBytes = kMaxWarps * kChunkBlocks * 4 * 16;     // 8 KB
+constexpr int kSRingBytes = kMaxWarps * kSegStages * kWarpStage;   // 144 KB
+constexpr int kSegBatchTiles = 6;                                  // row tiles per slot and batch of partial sums
 
 template <bool kDebug, bool kCluster>
 __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_seg_kernel(const __grid_constant__ SArgs a) {
@@ -151,8 +129,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_seg_kernel(const __
     uint64_t* xbar = reinterpret_cast<uint64_t*>(smem);
     volatile int* abort_sh = reinterpret_cast<volatile int*>(smem + 8);
     XTab* tab = reinterpret_cast<XTab*>(smem + kSHeadBytes) + warp * kChunkBlocks * 4;   // [8 blocks][4]
-    float* part = reinterpret_cast<float*>(smem + kSHeadBytes + kSTabBytes);            // [bt][wmax][128]
-    float* loc = part + a.part_floats;                                                  // [2][bt * 128]
+    uint8_t* wring = smem + kSHeadBytes + kSTabBytes + warp * kSegStages * kWarpStage;
+    float* part = reinterpret_cast<float*>(smem + kSHeadBytes + kSTabBytes + kSRingBytes);   // [bt][wmax][128]
+    float* loc = part + a.part_floats;                                                       // [2][bt * 128]
 
     const int csize = kCluster ? a.csize : 1;
     const int rank = kCluster ? static_cast<int>(cluster_rank()) : 0;
@@ -164,20 +143,47 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_seg_kernel(const __
     const int ntiles = static_cast<int>(static_cast<int64_t>(cid + 1) * tiles / ncl - tile0);
     const int nbatch = (ntiles + bt - 1) / bt;
 
-    // this CTA's chunks of K, this warp's chunk and row slot, and where the
-    // chunk's words sit in a row of the segment layout
+    // this CTA's chunks of K (as in the plain-layout kernel), this warp's
+    // chunk and row slot, and where the chunk's bytes sit in a row
     const int ch0 = rank * a.chunks / csize;
     const int cq = (rank + 1) * a.chunks / csize - ch0;
     const int wl = warp % wmax;
     const int slot = warp / wmax;
     const bool worker = wl < cq;
     const int chunk = ch0 + wl;
-    const int seg = chunk >> 3;                           // 8 chunks of 8 blocks per segment
-    const int i0 = (chunk & 7) * kChunkBlocks;            // first block of the chunk within its segment
-    const int rs = seg == a.nseg - 1 ? a.rlast : 64;      // blocks in that segment
-    const int noff = seg * kSegBytes + 16 * i0 + 4 * t;
-    const int soff = seg * kSegBytes + 16 * rs + 4 * (i0 & 31);
+    const int seg = chunk >> 3;                            // 8 chunks of 8 blocks per segment
+    const int i0 = (chunk & 7) * kChunkBlocks;             // first block of the chunk within its segment
+    const int rs = seg == a.nseg - 1 ? a.rlast : 64;       // blocks in that segment
+    const int64_t nib_off = static_cast<int64_t>(seg) * kSegBytes + 16 * i0;
+    const int64_t sc_off = static_cast<int64_t>(seg) * kSegBytes + 16 * rs + 4 * (i0 & 31);
     const int hs = i0 >= 32 ? 16 : 0;
+
+    // The warp's own tiles are tau = slot, slot + nslots, ...; the k-th of
+    // them goes to stage k % kSegStages of the warp's ring.  One call: the
+    // chunk's 128 nibble bytes of the 16 rows (four 16-byte copies a lane,
+    // each warp instruction covering four whole 128-byte row pieces) and its
+    // 32 scale bytes (one copy a lane), then one commit.  Rows past O are
+    // zero-filled without being read.
+    auto issue = [&](int stage, int tau) {
+        uint8_t* st = wring + stage * kWarpStage;
+        if (tau < ntiles) {
+            const int64_t r0 = (tile0 + tau) * kTileRows;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int row = 4 * k + (lane >> 3), piece = lane & 7;
+                const bool in = r0 + row < O;
+                const uint8_t* src = a.W + (in ? (r0 + row) * a.rowbytes + nib_off + 16 * piece : 0);
+                cp_async16(st + row * kNibStride + 16 * piece, src, in ? 16u : 0u);
+            }
+            {
+                const int row = lane >> 1, piece = lane & 1;
+                const bool in = r0 + row < O;
+                const uint8_t* src = a.W + (in ? (r0 + row) * a.rowbytes + sc_off + 16 * piece : 0);
+                cp_async16(st + kTileRows * kNibStride + row * kScStride + 16 * piece, src, in ? 16u : 0u);
+            }
+        }
+        cp_async_commit();   // one group per call, empty or not, so that the wait count is fixed
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(xbar, 1);
@@ -186,13 +192,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_seg_kernel(const __
     }
     __syncthreads();
     pdl_trigger();
-
-    // The weights do not depend on the preceding kernel: the first two tiles
-    // of this warp's chunk are requested before the dependency wait.
-    Unit ring0, ring1;
+    // The weights do not depend on the preceding kernel: the warp's first
+    // tiles are requested before the dependency wait.
     if (worker) {
-        if (slot < ntiles) load_unit(a, (tile0 + slot) * kTileRows, g, noff, soff, ring0);
-        if (slot + nslots < ntiles) load_unit(a, (tile0 + slot + nslots) * kTileRows, g, noff, soff, ring1);
+#pragma unroll
+        for (int k = 0; k < kSegStages; ++k) issue(k, slot + k * nslots);
     }
     pdl_wait();
 
@@ -249,50 +253,51 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_seg_kernel(const __
         if (g == 0) tab[b * 4 + t] = e;
     }
     __syncwarp();
-    const bool ok = *abort_sh == 0;
 
-    // One tile of this warp's chunk from ring entry u (tile tb of batch beta):
-    // the 8 block steps, the partials into the batch area, then the entry is
-    // refilled with the warp's tile two ahead.
-    auto tile_step = [&](Unit& u, int beta, int tb) {
-        const int tau = beta * bt + tb;
-        if (tau >= ntiles) return;
-        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (worker && ok) {
-            float is[kChunkBlocks][4];
-            seg_block_step<0>(u, hs, t, xs[0], tab, acc, is[0]);
-            seg_block_step<1>(u, hs, t, xs[1], tab, acc, is[1]);
-            seg_block_step<2>(u, hs, t, xs[2], tab, acc, is[2]);
-            seg_block_step<3>(u, hs, t, xs[3], tab, acc, is[3]);
-            seg_block_step<4>(u, hs, t, xs[4], tab, acc, is[4]);
-            seg_block_step<5>(u, hs, t, xs[5], tab, acc, is[5]);
-            seg_block_step<6>(u, hs, t, xs[6], tab, acc, is[6]);
-            seg_block_step<7>(u, hs, t, xs[7], tab, acc, is[7]);
-            if (kDebug) {
-                const int64_t rt = (tile0 + tau) * kTileRows;
-#pragma unroll
-                for (int b = 0; b < kChunkBlocks; ++b)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int64_t row = rt + g + 8 * (i >> 1);
-                        const int col = 2 * t + (i & 1);
-                        if (row < O && col < a.N)
-                            a.dbg[(col * O + row) * a.nb + chunk * kChunkBlocks + b] = static_cast<int32_t>(is[b][i]);
-                    }
-            }
-            const int ahead = tau + 2 * nslots;
-            if (ahead < ntiles) load_unit(a, (tile0 + ahead) * kTileRows, g, noff, soff, u);
-        }
-        if (worker)
-            *reinterpret_cast<float4*>(part + (tb * wmax + wl) * 128 + lane * 4) =
-                make_float4(acc[0], acc[1], acc[2], acc[3]);
-    };
+    const bool ok = *abort_sh == 0;   // the same in every warp after the barrier above
 
-    const int per = bt / nslots;   // tiles of one warp per batch: kBatchTilesPerSlot, even
+    int stage = 0;    // the stage of this warp's next tile: its tile count modulo kSegStages
     for (int beta = 0; beta < nbatch; ++beta) {
-        for (int j = 0; j < per; j += 2) {
-            tile_step(ring0, beta, j * nslots + slot);
-            tile_step(ring1, beta, (j + 1) * nslots + slot);
+        for (int j = 0; j < bt / nslots; ++j) {
+            const int tb = j * nslots + slot;          // tile within the batch
+            const int tau = beta * bt + tb;            // tile within the cluster's rows
+            if (tau >= ntiles) break;
+            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (worker) {
+                cp_async_wait<kSegStages - 1>();       // this lane's copies of the tile have landed
+                __syncwarp();                          // and every lane's
+                const uint8_t* st = wring + stage * kWarpStage;
+                if (ok) {
+                    float is[kChunkBlocks][4];
+                    staged_block_step<0>(st, g, t, hs, xs[0], tab, acc, is[0]);
+                    staged_block_step<1>(st, g, t, hs, xs[1], tab, acc, is[1]);
+                    staged_block_step<2>(st, g, t, hs, xs[2], tab, acc, is[2]);
+                    staged_block_step<3>(st, g, t, hs, xs[3], tab, acc, is[3]);
+                    staged_block_step<4>(st, g, t, hs, xs[4], tab, acc, is[4]);
+                    staged_block_step<5>(st, g, t, hs, xs[5], tab, acc, is[5]);
+                    staged_block_step<6>(st, g, t, hs, xs[6], tab, acc, is[6]);
+                    staged_block_step<7>(st, g, t, hs, xs[7], tab, acc, is[7]);
+                    if (kDebug) {
+                        const int64_t rt = (tile0 + tau) * kTileRows;
+#pragma unroll
+                        for (int b = 0; b < kChunkBlocks; ++b)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                const int64_t row = rt + g + 8 * (i >> 1);
+                                const int col = 2 * t + (i & 1);
+                                if (row < O && col < a.N)
+                                    a.dbg[(col * O + row) * a.nb + chunk * kChunkBlocks + b] =
+                                        static_cast<int32_t>(is[b][i]);
+                            }
+                    }
+                }
+                __syncwarp();                          // every lane is done with the stage
+                issue(stage, tau + kSegStages * nslots);
+                stage = stage + 1 == kSegStages ? 0 : stage + 1;
+            }
+            if (worker)
+                *reinterpret_cast<float4*>(part + (tb * wmax + wl) * 128 + lane * 4) =
+                    make_float4(acc[0], acc[1], acc[2], acc[3]);
         }
         __syncthreads();
         // ---- batch reduction.  Index e of a tile's 128 partials = lane * 4 + i
@@ -338,7 +343,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_seg_kernel(const __
             }
         }
     }
-    // After a timeout: wait (bounded) for the activation copy.
+    // Copies still in flight (none unless a warp stopped early) land before
+    // the CTA may exit; after a timeout, wait (bounded) for the activation copy.
+    cp_async_wait<0>();
     __syncthreads();
     if (threadIdx.x == 0 && *abort_sh != 0) mbar_wait(xbar, 0);
     __syncwarp();
@@ -351,7 +358,7 @@ bool g_seg_attr_done[4] = {false, false, false, false};
 std::map<std::tuple<bool, int, int, size_t>, int> g_seg_max_clusters;
 
 size_t seg_smem_bytes(const SArgs& a) {
-    return kSHeadBytes + kSTabBytes + static_cast<size_t>(a.part_floats) * sizeof(float) +
+    return kSHeadBytes + kSTabBytes + kSRingBytes + static_cast<size_t>(a.part_floats) * sizeof(float) +
            (a.csize > 1 ? 2 * static_cast<size_t>(a.bt) * 128 * sizeof(float) : 0);
 }
 
@@ -425,12 +432,12 @@ int small_n_seg_launch(const void* W, const void* xq, float* y, int64_t ldy, int
     a.csize = (a.chunks + kMaxWarps - 1) / kMaxWarps;
     a.wmax = (a.chunks + a.csize - 1) / a.csize;
     a.nslots = kMaxWarps / a.wmax;
-    a.bt = kBatchTilesPerSlot * a.nslots;
+    a.bt = kSegBatchTiles * a.nslots;
     a.part_floats = std::max(a.bt * a.wmax * 128, 8 * (a.wmax * kChunkBlocks * 34 + 16) / 4);
     if (a.csize > kMaxCluster) return QDG_ECUDA;
+    if (dev.smem_optin < seg_smem_bytes(a)) return QDG_ECUDA;
     const int warps = a.wmax * a.nslots;
     const size_t smem = seg_smem_bytes(a);
-    if (dev.smem_optin < smem) return QDG_ECUDA;
     cudaError_t e;
     if (dbg)
         e = a.csize > 1 ? launch_small_n_seg<true, true>(a, warps, smem, dev.sms, O, stream)

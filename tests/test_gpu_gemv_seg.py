@@ -265,10 +265,11 @@ def test_seg_small_n2_matches_two_single_calls():
 
 
 @pytest.mark.parametrize("O,K,N", [(14336, 4096, 8), (4096, 14336, 8), (1000, 2048, 3), (37, 2304, 5),
-                                   (300, 256, 4), (40, 32768, 6)])
+                                   (300, 256, 4), (153, 4096, 7), (40, 32768, 6)])
 def test_seg_small_n_mma_matches_plain_layout_kernel(O, K, N):
     """N >= 3 on the segment layout runs the plain-layout kernel's arithmetic
-    in the same order, so the two agree bit for bit."""
+    in the same order (same chunks, same cluster split), so the two agree bit
+    for bit."""
     torch = torch_cuda()
     Wq = oracle.quantize_q4_0(synth.weights(O + K, "W3", O, K))
     xq = oracle.quantize_q8_0(synth.activations(O + K + N, "x3", N, K, outlier_frac=0.01), None)
