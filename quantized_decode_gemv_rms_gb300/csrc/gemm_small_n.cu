@@ -54,6 +54,10 @@ static __device__ unsigned g_flags_small_n;
 
 namespace {
 
+constexpr int kChunkBytes = kChunkBlocks * 18;        // 144 bytes of a row per chunk, a multiple of 16
+constexpr int kUnitBytes = kTileRows * kChunkBytes;   // 2304 bytes per ring slot (18 x 128)
+constexpr int kBatchTilesPerSlot = 8;                 // row tiles per slot and batch of partial sums
+
 static_assert(kChunkBytes % 16 == 0 && kUnitBytes % 128 == 0, "tensor-copy alignment");
 
 // Word t of the nibbles of block b in a staged row (row start 16-byte aligned):

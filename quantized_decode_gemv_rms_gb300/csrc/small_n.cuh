@@ -11,10 +11,7 @@ namespace {
 
 constexpr int kMaxWarps = 16;
 constexpr int kChunkBlocks = 8;                       // blocks of one row owned by a warp
-constexpr int kChunkBytes = kChunkBlocks * 18;        // 144 bytes, a multiple of 16
 constexpr int kTileRows = 16;                         // rows of one MMA
-constexpr int kUnitBytes = kTileRows * kChunkBytes;   // 2304 bytes per ring slot (18 x 128)
-constexpr int kBatchTilesPerSlot = 8;                 // row tiles per slot and batch of partial sums
 constexpr int kMaxCluster = 8;
 constexpr uint32_t kLoNib = 0x000F000Fu;
 constexpr uint32_t kHiNib = 0x00F000F0u;
