@@ -247,8 +247,8 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
-def time_oracle(wl, budget_s, row_frac, steps=None, warmup=1):
-    cores = cpu_cores()
+def time_oracle(wl, budget_s, row_frac, steps=None, warmup=1, threads=None):
+    cores = threads or cpu_cores()
     Wq_rows, inputs = oracle_setup(wl, row_frac)
     for _ in range(max(1, warmup)):
         oracle_decode_sample(wl, row_frac, cores, inputs, Wq_rows)  # untimed
@@ -900,6 +900,13 @@ def main():
         result["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                                   "sample": f"every 16th row of each matrix + all activations; {done} passes "
                                             f"in {el:.1f} s ({nb / 1e9:.2f} GB)"}
+        # the same oracle on one thread (its rows are independent, so the
+        # multi-threaded result is the same bit for bit)
+        rate1, _, done1, el1, nb1 = time_oracle(wl, max(1.0, args.cpu_budget / 4), 1.0 / 16, threads=1)
+        result["cpu_baseline"]["single_thread"] = {
+            "value": round(rate1, 4), "unit": UNIT, "cores": 1,
+            "sample": f"every 16th row of each matrix + all activations; {done1} passes in {el1:.1f} s "
+                      f"({nb1 / 1e9:.2f} GB)"}
     if rank == 0:
         print(json.dumps(result))
     if world > 1:
