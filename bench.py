@@ -530,6 +530,8 @@ def bench_ours(args, wl, world, rank, local):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     kinds = ["gemv", "gemv_seg", "fused", "fused_seg"]
     per_call = {k: {} for k in kinds}
+    spread_kind = "gemv_seg" if args.layout == "seg" else "gemv"
+    per_call_spread = {}
     launch_bytes = {k: {} for k in kinds}
     for p_ in range(1):
         step.run(step.x_dev[0], fused=False)          # the Q8_0 vectors of input set 0
@@ -558,14 +560,20 @@ def bench_ours(args, wl, world, rank, local):
                         one(c)
                 gr.replay()
                 side.synchronize()
-                a0 = torch.cuda.Event(enable_timing=True)
-                a1 = torch.cuda.Event(enable_timing=True)
-                a0.record(side)
-                for _ in range(3):
+                # events around every replay: the mean per launch, and for the
+                # timed kernel kind also the spread over the replays
+                reps = 21 if kind == spread_kind else 3
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+                evs[0].record(side)
+                for r in range(reps):
                     gr.replay()
-                a1.record(side)
+                    evs[r + 1].record(side)
                 side.synchronize()
-            per_call[kind][name] = a0.elapsed_time(a1) * 1e3 / (3 * copies)
+            per_call[kind][name] = evs[0].elapsed_time(evs[reps]) * 1e3 / (reps * copies)
+            if kind == spread_kind:
+                per = sorted(evs[r].elapsed_time(evs[r + 1]) * 1e3 / copies for r in range(reps))
+                per_call_spread[name] = {"p10": round(per[2], 2), "p50": round(per[10], 2), "p90": round(per[18], 2),
+                                         "replays": reps, "launches_per_replay": copies}
             del gr, Wc
             torch.cuda.empty_cache()
         xbytes = 4 * K * (2 if grp[0].source.startswith("norm:") else 1)
@@ -663,6 +671,8 @@ def bench_ours(args, wl, world, rank, local):
         "us_per_step": round(ms * 1e3, 2),
         "us_per_step_spread": dist,
         "us_per_call": {k: {n: round(v, 2) for n, v in d.items()} for k, d in per_call.items()},
+        "us_per_call_spread": {"kind": spread_kind, "groups": per_call_spread,
+                               "how": "mean launch time within each of 21 graph replays; p10/p50/p90 over replays"},
         "gbs_per_call": {k: {n: round(v, 1) for n, v in d.items()} for k, d in gbs_per_call.items()},
         "per_call_note": ("one launch per group of projections sharing an input (gemv: on a prepared Q8_0 vector; "
                           "gemv_seg: the same on weights in the segment layout; "
