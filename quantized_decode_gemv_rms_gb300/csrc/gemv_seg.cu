@@ -72,9 +72,14 @@ Plan make_plan(int64_t K) {
     p.rlast = p.nb - 64 * (p.nseg - 1);
     p.rowbytes = static_cast<int>(seg_row_bytes(K));
     p.nslots = kWarps / p.nseg;
-    p.rch = (kPartFloats / p.nseg) / p.nslots * p.nslots;
+    p.rch = p.nslots > 0 ? (kPartFloats / p.nseg) / p.nslots * p.nslots : 0;
     return p;
 }
+
+// Every segment of a row needs a warp: K <= 32768 gives at most kWarps
+// segments, so a plan always has a row slot and a positive chunk.
+static_assert(kWarps * 64 * 32 >= 32768, "one warp per segment at the largest K");
+bool plan_ok(const Plan& p) { return p.nslots >= 1 && p.rch >= 1; }
 
 __device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
     uint4 v;
@@ -624,6 +629,7 @@ int gemv_seg_launch_group(const void* const* W, float* const* y, const int64_t* 
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     const Plan plan = make_plan(K);
+    if (!plan_ok(plan)) return QDG_ESHAPE;
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
     a.ng = count;
     a.xq = static_cast<const uint8_t*>(xq);
@@ -662,6 +668,7 @@ int gemv_seg_rmsnorm_launch(const void* const* W, float* const* y, const int64_t
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     const Plan plan = make_plan(K);
+    if (!plan_ok(plan)) return QDG_ESHAPE;
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
     a.ng = count;
     a.x = x;
@@ -697,6 +704,7 @@ int gemv_seg2_launch(const void* W, const void* xq, float* y, int64_t ldy, int64
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
     Plan plan = make_plan(K);
+    if (!plan_ok(plan)) return QDG_ESHAPE;
     plan.rch = (kPartFloats / (plan.nseg * 2)) / plan.nslots * plan.nslots;
     Args2 a{};
     a.W = static_cast<const uint8_t*>(W);
