@@ -224,6 +224,13 @@ QDG_API int q4_0_q8_0_gemm(const void* W, const void* xq, float* y, int64_t ldy,
 QDG_API int64_t q4_0_q8_0_gemm_workspace_bytes(int64_t K, int64_t T);
 
 /*
+ * q4_0_q8_0_gemm_workspace_size -- the same figure with the argument list
+ * (O, K, T) of the product itself; O does not change it (O < 1 gives
+ * QDG_EINVAL).
+ */
+QDG_API int64_t q4_0_q8_0_gemm_workspace_size(int64_t O, int64_t K, int64_t T);
+
+/*
  * q4_0_q8_0_gemm_static -- q4_0_q8_0_gemm without a caller workspace and
  * without any device allocation, for callers that cannot allocate device
  * memory.  The pages have no counterpart: this is a library convenience.

@@ -627,6 +627,11 @@ unsigned flags_read_clear_gemm(cudaStream_t stream) {
 
 extern "C" int64_t q4_0_q8_0_gemm_workspace_bytes(int64_t K, int64_t T) { return qdg::gemm_workspace_bytes(K, T); }
 
+extern "C" int64_t q4_0_q8_0_gemm_workspace_size(int64_t O, int64_t K, int64_t T) {
+    if (O < 1) return QDG_EINVAL;
+    return qdg::gemm_workspace_bytes(K, T);
+}
+
 extern "C" int q4_0_q8_0_gemm(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t T,
                               void* workspace, int64_t workspace_bytes, qdg_stream_t stream) {
     if (!y) return QDG_EINVAL;

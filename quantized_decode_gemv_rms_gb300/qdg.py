@@ -64,6 +64,7 @@ def lib() -> ctypes.CDLL:
             }
             sig["q4_0_q8_0_gemm"] = ([p, p, p, i64, i64, i64, i64, p, i64, p], i32)
             sig["q4_0_q8_0_gemm_workspace_bytes"] = ([i64, i64], i64)
+            sig["q4_0_q8_0_gemm_workspace_size"] = ([i64, i64, i64], i64)
             sig["q4_0_q8_0_gemm_static"] = ([p, p, p, i64, i64, i64, i64, p], i32)
             sig["q8_0_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
             sig["q8_0_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
@@ -253,6 +254,13 @@ def q4_0s_q8_0_gemm_small_n(Wr, xq, y, ldy: int, O: int, K: int, N: int, stream=
 def q4_0_q8_0_gemm_small_n(W, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:
     _check(lib().q4_0_q8_0_gemm_small_n(_ptr(W), _ptr(xq), _ptr(y), ldy, O, K, N, _stream(stream)),
            "q4_0_q8_0_gemm_small_n")
+
+
+def q4_0_q8_0_gemm_workspace_size(O: int, K: int, T: int) -> int:
+    n = int(lib().q4_0_q8_0_gemm_workspace_size(O, K, T))
+    if n < 0:
+        raise QdgError(n, "q4_0_q8_0_gemm_workspace_size")
+    return n
 
 
 def q4_0_q8_0_gemm_workspace_bytes(K: int, T: int) -> int:

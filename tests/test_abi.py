@@ -25,7 +25,7 @@ def L():
 def test_header_declares_entry_points():
     names = declared_symbols()
     for must in ("qnorm_quantize_q8_0", "qnorm_add_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
-                 "q4_0_q8_0_gemm_workspace_bytes", "quantize_q4_0", "q4_0_repack_seg", "q4_0s_q8_0_gemv",
+                 "q4_0_q8_0_gemm_workspace_bytes", "q4_0_q8_0_gemm_workspace_size", "qdg_stage_copy", "quantize_q4_0", "q4_0_repack_seg", "q4_0s_q8_0_gemv",
                  "q4_0s_q8_0_gemv_group", "q4_0s_gemv_rmsnorm_group", "q4_0s_q8_0_gemm_small_n", "q4_0_seg_row_bytes", "q8_0_q8_0_gemv", "q8_0_q8_0_gemv_group",
                  "qdg_device_status", "qdg_status_string"):
         assert must in names
@@ -218,6 +218,8 @@ def test_gemm_host_validation(L):
     assert L.q4_0_q8_0_gemm_workspace_bytes(256, 129) == 2 * 8 * 8704
     assert L.q4_0_q8_0_gemm_workspace_bytes(320, 4) == -3             # K % 256
     assert L.q4_0_q8_0_gemm_workspace_bytes(256, 0) == -1
+    assert L.q4_0_q8_0_gemm_workspace_size(14336, 256, 129) == 2 * 8 * 8704   # O does not change it
+    assert L.q4_0_q8_0_gemm_workspace_size(0, 256, 129) == -1
     assert f(A16, A16, None, 8, 8, 256, 4, A16, need, None) == -1     # null y
     assert f(A16, A16, A16, 4, 8, 256, 4, A16, need, None) == -1      # ldy < O
     assert f(A16, A16, A16, 8, 8, 256, 0, A16, need, None) == -1      # T = 0
