@@ -267,9 +267,26 @@ def time_oracle(wl, budget_s, row_frac, steps=None, warmup=1, threads=None):
     return nbytes / el / 1e9, cores, done, el, nbytes
 
 
+def oracle_leg(wl, seconds, threads=None):
+    """The oracle timed by the reference arm's own code in a fresh process,
+    so that the benchmark process (its CUDA context, pinned buffers and
+    threads) does not weigh on it and both legs measure the same thing.
+    Returns the reference arm's JSON line."""
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", wl.name,
+           "--steps", "1", "--warmup", "3", "--oracle-seconds", str(seconds)]
+    if threads:
+        cmd += ["--oracle-threads", str(threads)]
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "LOCAL_RANK", "WORLD_SIZE", "LOCAL_WORLD_SIZE", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run(cmd, capture_output=True, text=True, timeout=600, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle leg failed: {r.stderr[-2000:]}")
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 # ---------------------------------------------------------------- GPU leg
 class DecodeStep:
-    def __init__(self, wl, device, layout="seg"):
+    def __init__(self, wl, device, layout="seg", copies=1):
         import torch
         from quantized_decode_gemv_rms_gb300 import qdg
         self.qdg = qdg
@@ -295,6 +312,13 @@ class DecodeStep:
             Wr = torch.empty(qdg.q4_0_seg_nbytes(m.rows, m.cols), dtype=torch.uint8, device=device)
             qdg.q4_0_repack_seg(self.W[m.name], Wr, m.rows, m.cols)
             self.Wr[m.name] = Wr
+        # weight copies the step rotates through (copy c of every matrix, in
+        # the layout given here): a workload whose weights fit in L2 needs
+        # several, so that every step reads its weights from HBM
+        self.copies = copies
+        self.copies_layout = layout
+        src = self.Wr if layout == "seg" else self.W
+        self.Wcopies = [src] + [{n: t.clone() for n, t in src.items()} for _ in range(copies - 1)]
         torch.cuda.synchronize()
         self.gamma = {tag: torch.from_numpy(synth.gamma(wl.seed, tag, K)).to(device)
                       for tag, K in wl.activations.items() if self.kinds[tag] == "norm"}
@@ -358,20 +382,29 @@ class DecodeStep:
             Ws = Ws if Ws is not None else [self.W[m.name] for m in grp]
             self.qdg.q4_0_gemv_rmsnorm_group(Ws, ys, Os, xs[tag], g, self.wl.eps, grp[0].cols)
 
-    def run(self, xs, events=None, fused=True):
+    def copy_weights(self, grp, copy):
+        """The matrices of a group in weight copy `copy` (None = the layout's own)."""
+        if copy == 0:
+            return None
+        assert self.layout == self.copies_layout, "weight copies exist for one layout only"
+        return [self.Wcopies[copy][m.name] for m in grp]
+
+    def run(self, xs, events=None, fused=True, copy=0):
         """One decode step in dependency order: for each group of projections
         sharing an input -- fused: one launch (RMSNorm*gamma -> Q8_0 -> GEMV);
-        split: the quantize kernel, then one grouped GEMV launch."""
+        split: the quantize kernel, then one grouped GEMV launch.  `copy`
+        picks the weight copy the step reads."""
         qdg = self.qdg
         for grp in self.groups:
+            Ws = self.copy_weights(grp, copy)
             if fused and self.fusable(grp):
-                self.run_group(grp, xs)
+                self.run_group(grp, xs, Ws=Ws)
                 continue
             tag = grp[0].source.split(":", 1)[1]
             K = grp[0].cols
             g = self.gamma.get(tag) if self.kinds[tag] == "norm" else None
             qdg.qnorm_quantize_q8_0(xs[tag], g, self.wl.eps, self.xq[tag], K=K, N=1)
-            self.gemv_group(grp, self.xq[tag])
+            self.gemv_group(grp, self.xq[tag], Ws=Ws)
 
     def gemv_group(self, grp, xq, Ws=None, layout=None):
         """The grouped GEMV of one group on its prepared Q8_0 vector."""
@@ -402,7 +435,14 @@ def bench_ours(args, wl, world, rank, local):
     device = torch.device("cuda", local)
     qdg.lib()
     qdg.qdg_set_option(qdg.QDG_OPT_PDL, 1 if args.pdl else 0)
-    step = DecodeStep(wl, device, layout=args.layout)
+    # A step whose weights fit three times in L2 rotates through weight
+    # copies (a multiple of the input sets), so every step streams from HBM.
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    wbytes = sum(workloads.q4_0_bytes(m.rows, m.cols) for m in wl.matrices)
+    need = -(-3 * l2 // wbytes)                      # ceil(3 L2 / weight bytes)
+    copies = 1 if wbytes > 3 * l2 else N_INPUT_SETS * -(-need // N_INPUT_SETS)
+    spg = max(N_INPUT_SETS, copies)                 # steps per graph: every input set and copy once
+    step = DecodeStep(wl, device, layout=args.layout, copies=copies)
     stream = torch.cuda.current_stream()
     nbytes = step_bytes(wl)
     fused = args.fused
@@ -421,19 +461,20 @@ def bench_ours(args, wl, world, rank, local):
     side.wait_stream(stream)
     graphs = {}
     counts = {}
-    # One graph holds N_INPUT_SETS consecutive steps (one per input set), as a
-    # multi-layer forward pass would: programmatic dependent launch chains the
-    # kernels inside a graph, while consecutive graph launches serialise.
+    # One graph holds spg consecutive steps (input set k % N_INPUT_SETS,
+    # weight copy k % copies), as a multi-layer forward pass would:
+    # programmatic dependent launch chains the kernels inside a graph, while
+    # consecutive graph launches serialise.
     with torch.cuda.stream(side):
         for fz in (fused, not fused):
             before = [qdg.qdg_launch_count(i) for i in range(11)]
 
             def steps(fz=fz):
-                for p in range(N_INPUT_SETS):
-                    step.run(step.x_dev[p], fused=fz)
+                for k in range(spg):
+                    step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % copies)
             graphs[fz] = capture(steps, side)
             after = [qdg.qdg_launch_count(i) for i in range(11)]
-            counts[fz] = [(after[i] - before[i]) // N_INPUT_SETS for i in range(11)]
+            counts[fz] = [(after[i] - before[i]) // spg for i in range(11)]
     stream.wait_stream(side)
     torch.cuda.synchronize()
     ng = len(step.groups)
@@ -450,15 +491,15 @@ def bench_ours(args, wl, world, rank, local):
                                     "gemv" + ("_seg" if args.layout == "seg" else ""): counts[fused][gk]}}
 
     def run_steps(n, fz=fused):
-        """n decode steps: whole graphs of N_INPUT_SETS steps, the remainder eagerly."""
+        """n decode steps: whole graphs of spg steps, the remainder eagerly."""
         if not args.graph:
             for k in range(n):
-                step.run(step.x_dev[k % N_INPUT_SETS], fused=fz)
+                step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % copies)
             return
-        for _ in range(n // N_INPUT_SETS):
+        for _ in range(n // spg):
             graphs[fz].replay()
-        for k in range(n % N_INPUT_SETS):
-            step.run(step.x_dev[k], fused=fz)
+        for k in range(n % spg):
+            step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % copies)
 
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -496,21 +537,21 @@ def bench_ours(args, wl, world, rank, local):
     clocks = sampler.stop()
 
     # ---- spread of the step time: events around each of R graph replays
-    # (N_INPUT_SETS steps each), outside the timed region above
+    # (spg steps each), outside the timed region above
     dist = None
     if args.graph:
-        reps = max(20, min(200, args.steps // N_INPUT_SETS))
+        reps = max(20, min(200, args.steps // spg))
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
         evs[0].record(stream)
         for i in range(reps):
             graphs[fused].replay()
             evs[i + 1].record(stream)
         torch.cuda.synchronize()
-        per = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / N_INPUT_SETS for i in range(reps))
+        per = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / spg for i in range(reps))
         pick = lambda q: per[min(reps - 1, int(round(q * (reps - 1))))]
         dist = {"p10": round(pick(0.1), 2), "p50": round(pick(0.5), 2), "p90": round(pick(0.9), 2),
                 "samples": reps, "unit": "us per step",
-                "how": f"CUDA events around each replay of the {N_INPUT_SETS}-step graph"}
+                "how": f"CUDA events around each replay of the {spg}-step graph"}
 
     # ---- the other route, same number of steps, for comparison
     run_steps(args.warmup, not fused)
@@ -527,7 +568,6 @@ def bench_ours(args, wl, world, rank, local):
     # vector, and the fused launch): a graph of C back-to-back launches, each on
     # its own copy of the weights (C copies exceed three L2 sizes, so every
     # launch streams its weights from HBM)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
     kinds = ["gemv", "gemv_seg", "fused", "fused_seg"]
     per_call = {k: {} for k in kinds}
     spread_kind = "gemv_seg" if args.layout == "seg" else "gemv"
@@ -590,8 +630,8 @@ def bench_ours(args, wl, world, rank, local):
     # moves every output device -> host (one copy).  The headline stages with
     # the library's copy kernel (qdg_stage_copy); the copy-engine variant is
     # measured beside it.  With graphs, the copies are nodes of the same graph
-    # as the kernels (N_INPUT_SETS steps per graph).
-    n_e2e = N_INPUT_SETS * max(3, min(args.steps, 500) // N_INPUT_SETS)
+    # as the kernels (spg steps per graph).
+    n_e2e = spg * max(3, min(args.steps, 500) // spg)
     h2d = sum(t.numel() * 4 for t in step.x_host[0].values())
     d2h = sum(t.numel() * 4 for t in step.y_host.values())
 
@@ -599,8 +639,8 @@ def bench_ours(args, wl, world, rank, local):
         e2e_graph = None
         if args.graph:
             def e2e_steps():
-                for p in range(N_INPUT_SETS):
-                    _e2e_step(step, None, p, fused, staging)
+                for k in range(spg):
+                    _e2e_step(step, None, k, fused, staging, copy=k % copies)
             with torch.cuda.stream(side):
                 e2e_graph = capture(e2e_steps, side)
             stream.wait_stream(side)
@@ -608,12 +648,12 @@ def bench_ours(args, wl, world, rank, local):
 
         def run_e2e(n):
             if e2e_graph is not None:
-                for _ in range(n // N_INPUT_SETS):
+                for _ in range(n // spg):
                     e2e_graph.replay()
             else:
                 for k in range(n):
-                    _e2e_step(step, None, k, fused, staging)
-        run_e2e(N_INPUT_SETS)
+                    _e2e_step(step, None, k, fused, staging, copy=k % copies)
+        run_e2e(spg)
         torch.cuda.synchronize()
         barrier(world)
         f0.record(stream)
@@ -656,16 +696,22 @@ def bench_ours(args, wl, world, rank, local):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "i32 (int4 x int8 block sums) + f32 scaling",
-        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) activations with 1% x20 outliers)",
+        "data": ("synthetic (seeded N(0,0.02) weights, N(0,1) activations" +
+                 (f" with {wl.outlier_frac:.0%} x{wl.outlier_mult:g} outliers)" if wl.outlier_frac else ")")),
         "config": {"workload": wl.name, "batch": 1, "matrices": {m.name: [m.rows, m.cols] for m in wl.matrices},
-                   "bytes_per_step": nbytes, "l2": "inputs larger than L2 (419 MB of weights per step vs 129 MB L2)",
+                   "bytes_per_step": nbytes,
+                   "l2": (f"inputs larger than L2 ({wbytes / 1e6:.0f} MB of weights per step vs "
+                          f"{l2 / 1e6:.0f} MB L2)" if copies == 1 else
+                          f"weights rotate through {copies} copies ({copies * wbytes / 1e6:.0f} MB, more than "
+                          f"three times the {l2 / 1e6:.0f} MB L2), so every step reads its weights from HBM"),
                    "route": (("fused: one RMSNorm->Q8_0->GEMV launch per group" +
                               (f" (K <= {FUSED_SEG_MAX_K}; split for larger K)" if args.layout == "seg" else ""))
                              if fused else "split: quantize kernel + grouped GEMV launch per group") +
                             ("; weights in the segment layout (repacked at load)" if args.layout == "seg"
                              else "; weights in plain Q4_0 blocks") +
-                            "; groups q+k+v, o, gate+up, down, head in dependency order",
-                   "launch": ((f"cuda graph of {N_INPUT_SETS} steps" if args.graph else "eager") +
+                            "; groups " + ", ".join("+".join(m.name for m in g) for g in step.groups) +
+                            " in dependency order",
+                   "launch": ((f"cuda graph of {spg} steps" if args.graph else "eager") +
                               (" + PDL" if args.pdl else "")),
                    "parallelism": f"replicas x{world}"},
         "us_per_step": round(ms * 1e3, 2),
@@ -689,7 +735,7 @@ def bench_ours(args, wl, world, rank, local):
                 "how": ("every step: one host-to-device copy of its input vectors from pinned memory, the step "
                         "through the C ABI, one device-to-host copy of all outputs; both copies by the library's "
                         "staging kernel (qdg_stage_copy) reading and writing the mapped pinned buffers" +
-                        (f"; copies and kernels in one CUDA graph of {N_INPUT_SETS} steps" if args.graph else "")),
+                        (f"; copies and kernels in one CUDA graph of {spg} steps" if args.graph else "")),
                 "copy_engine": {"value": round(nbytes * world / (ms_e2e_engine * 1e-3) / 1e9, 1),
                                 "ms_per_step": round(ms_e2e_engine, 5),
                                 "how": "the same with stream-ordered copy-engine copies instead of the kernel"}},
@@ -830,7 +876,7 @@ def bench_extras(args, device):
     return out
 
 
-def _e2e_step(step, graphs, k, fused=True, staging="kernel"):
+def _e2e_step(step, graphs, k, fused=True, staging="kernel", copy=0):
     """One step from host buffers: every input vector in (one copy), the step,
     every output out (one copy).  staging="kernel": the library's staging
     kernel reads and writes the mapped pinned buffers (the copies stay in the
@@ -840,7 +886,7 @@ def _e2e_step(step, graphs, k, fused=True, staging="kernel"):
         step.qdg.qdg_stage_copy(step.x_dev_flat[p], step.x_host_flat[p])
     else:
         step.x_dev_flat[p].copy_(step.x_host_flat[p], non_blocking=True)
-    step.run(step.x_dev[p], fused=fused)
+    step.run(step.x_dev[p], fused=fused, copy=copy)
     if staging == "kernel":
         step.qdg.qdg_stage_copy(step.y_host_flat, step.y_flat)
     else:
@@ -864,6 +910,10 @@ def main():
     ap.add_argument("--pdl", action="store_true", default=True)
     ap.add_argument("--no-pdl", dest="pdl", action="store_false")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--oracle-seconds", type=float, default=0.0,
+                    help="reference arm: time the oracle for this many seconds instead of --steps passes")
+    ap.add_argument("--oracle-threads", type=int, default=0,
+                    help="reference arm: host threads for the oracle (default: every core this process may use)")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the small-N and prefill timings")
@@ -879,14 +929,17 @@ def main():
         if rank != 0:
             return
         row_frac = 1.0 / 16
-        rate, cores, done, el, nb = time_oracle(wl, 0, row_frac, steps=args.steps, warmup=args.warmup)
+        rate, cores, done, el, nb = time_oracle(wl, args.oracle_seconds, row_frac,
+                                                steps=None if args.oracle_seconds > 0 else args.steps,
+                                                warmup=args.warmup, threads=args.oracle_threads or None)
         line = {"impl": "reference", "metric": METRIC, "value": round(rate, 4), "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / done * 1e3, 3),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": "f64 (oracle: dequantize-then-dot)", "data": "synthetic",
                 "config": {"workload": wl.name, "batch": 1},
                 "cpu_baseline": {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                                 "sample": f"every 16th row of each matrix + all activations, {done} steps"},
+                                 "sample": f"every 16th row of each matrix + all activations; {done} passes "
+                                           f"in {el:.1f} s ({nb / 1e9:.2f} GB)"},
                 "e2e": {"value": round(rate, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -906,17 +959,13 @@ def main():
         torch.cuda.empty_cache()
         result["extras"] = bench_extras(args, torch.device("cuda", local))
     if rank == 0 and world == 1 and args.cpu_baseline:
-        rate, cores, done, el, nb = time_oracle(wl, args.cpu_budget, 1.0 / 16)
-        result["cpu_baseline"] = {"value": round(rate, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                                  "sample": f"every 16th row of each matrix + all activations; {done} passes "
-                                            f"in {el:.1f} s ({nb / 1e9:.2f} GB)"}
-        # the same oracle on one thread (its rows are independent, so the
-        # multi-threaded result is the same bit for bit)
-        rate1, _, done1, el1, nb1 = time_oracle(wl, max(1.0, args.cpu_budget / 4), 1.0 / 16, threads=1)
-        result["cpu_baseline"]["single_thread"] = {
-            "value": round(rate1, 4), "unit": UNIT, "cores": 1,
-            "sample": f"every 16th row of each matrix + all activations; {done1} passes in {el1:.1f} s "
-                      f"({nb1 / 1e9:.2f} GB)"}
+        # the reference arm's code in a fresh process, on every core, then on one
+        # thread (its rows are independent, so both give the same bits)
+        ref = oracle_leg(wl, args.cpu_budget)
+        result["cpu_baseline"] = dict(ref["cpu_baseline"], how="bench.py --impl reference in a fresh process")
+        ref1 = oracle_leg(wl, max(1.0, args.cpu_budget / 4), threads=1)
+        result["cpu_baseline"]["single_thread"] = {k: ref1["cpu_baseline"][k] for k in ("value", "unit", "cores",
+                                                                                        "sample")}
     if rank == 0:
         print(json.dumps(result))
     if world > 1:

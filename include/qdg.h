@@ -226,19 +226,25 @@ QDG_API int64_t q4_0_q8_0_gemm_workspace_bytes(int64_t K, int64_t T);
 /*
  * q4_0_q8_0_gemm_workspace_size -- the same figure with the argument list
  * (O, K, T) of the product itself; O does not change it (O < 1 gives
- * QDG_EINVAL).
+ * QDG_EINVAL, O > 2^30 QDG_ESHAPE, as the product would).
  */
 QDG_API int64_t q4_0_q8_0_gemm_workspace_size(int64_t O, int64_t K, int64_t T);
 
 /*
  * q4_0_q8_0_gemm_static -- q4_0_q8_0_gemm without a caller workspace and
- * without any device allocation, for callers that cannot allocate device
- * memory.  The pages have no counterpart: this is a library convenience.
- * Its scratch is a 16 MiB array in the library's device memory, so the
+ * without any device allocation.  The pages have no counterpart: this is a
+ * library convenience for callers that cannot allocate device memory, such
+ * as a plug-in whose host program owns every byte of the GPU through its
+ * own pool, or code that runs where cudaMalloc is not permitted (inside a
+ * stream capture, or under a fixed memory budget).
+ * Its scratch is a 16 MiB array in the library's device memory (held by
+ * every GPU that loads the library until the process exits), so the
  * problem must satisfy q4_0_q8_0_gemm_workspace_bytes(K, T) <= 16 MiB
  * (e.g. T <= 1920 tokens at K = 4096, T <= 512 at K = 14336); larger ones
  * return QDG_ESHAPE.  The first call on a device looks up the array's
- * address on that device (make it before any stream capture).  Nothing
+ * address on that device (make it before any stream capture); the address
+ * is kept for the life of the process, so after cudaDeviceReset the library
+ * must be unloaded and loaded again before this entry is used.  Nothing
  * needs to start at zero.  All calls share the array: calls that overlap on
  * the GPU race.  Other arguments and errors as q4_0_q8_0_gemm.
  */

@@ -3,7 +3,9 @@
 #include "common.cuh"
 
 #include <atomic>
+#include <map>
 #include <mutex>
+#include <utility>
 
 namespace qdg {
 
@@ -59,6 +61,20 @@ unsigned flags_read_clear_api(cudaStream_t stream) {
         return ~0u;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return ~0u;
     return v;
+}
+
+cudaError_t ensure_smem_limit(const void* func, size_t bytes) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, size_t> done;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    size_t& have = done[std::make_pair(dev, func)];
+    if (have >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess) have = bytes;
+    return e;
 }
 
 bool pdl_enabled() { return g_pdl.load(std::memory_order_relaxed) != 0; }

@@ -170,6 +170,12 @@ DeviceInfo device_info();
 bool pdl_enabled();
 void count_launch(int which);
 
+// Raise `func`'s dynamic shared-memory limit to at least `bytes` on the
+// current device.  The attribute belongs to a (device, kernel) pair, so the
+// record of what was set is kept per device; later calls that need no more
+// than was set cost one map lookup.
+cudaError_t ensure_smem_limit(const void* func, size_t bytes);
+
 // Launch with the PDL attribute when enabled.
 template <typename Kern, typename... Args>
 cudaError_t launch(Kern kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool allow_pdl,

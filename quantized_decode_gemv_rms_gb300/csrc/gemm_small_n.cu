@@ -362,8 +362,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
 }
 
 std::mutex g_mutex;
-bool g_attr_done[4] = {false, false, false, false};
-std::map<std::tuple<bool, int, int, size_t>, int> g_max_clusters;
+std::map<std::tuple<int, bool, int, int, size_t>, int> g_max_clusters;
 
 size_t smem_bytes(const Args& a) {
     const size_t stage = static_cast<size_t>(a.wmax) * kUnitBytes;
@@ -374,15 +373,13 @@ size_t smem_bytes(const Args& a) {
 template <bool kDebug, bool kCluster>
 int max_clusters(int csize, int warps, size_t smem, int sms) {
     std::lock_guard<std::mutex> lock(g_mutex);
-    bool& done = g_attr_done[2 * kDebug + kCluster];
-    if (!done) {
-        if (cudaFuncSetAttribute(small_n_kernel<kDebug, kCluster>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(device_info().smem_optin)) != cudaSuccess)
-            return -1;
-        done = true;
-    }
+    const DeviceInfo dev = device_info();
+    if (dev.device < 0) return -1;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(small_n_kernel<kDebug, kCluster>), dev.smem_optin) != cudaSuccess)
+        return -1;
     if (!kCluster) return sms;
-    const auto key = std::make_tuple(kDebug, csize, warps, smem);
+    // the occupancy answer depends on the device, so the record is kept per device
+    const auto key = std::make_tuple(dev.device, kDebug, csize, warps, smem);
     auto it = g_max_clusters.find(key);
     if (it != g_max_clusters.end()) return it->second;
     cudaLaunchConfig_t cfg = {};

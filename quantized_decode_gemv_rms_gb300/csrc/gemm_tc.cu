@@ -546,17 +546,9 @@ __global__ void __launch_bounds__(BN) act_records_kernel(const uint8_t* __restri
     reinterpret_cast<float*>(out + OPB)[r] = d;
 }
 
-std::mutex g_attr_mutex;
-bool g_attr_done[2] = {false, false};
-
 template <bool kDebug>
 cudaError_t ensure_smem() {
-    std::lock_guard<std::mutex> lock(g_attr_mutex);
-    if (g_attr_done[kDebug]) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<kDebug>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmem));
-    if (e == cudaSuccess) g_attr_done[kDebug] = true;
-    return e;
+    return ensure_smem_limit(reinterpret_cast<const void*>(gemm_tc_kernel<kDebug>), kSmem);
 }
 
 }  // namespace
@@ -629,6 +621,7 @@ extern "C" int64_t q4_0_q8_0_gemm_workspace_bytes(int64_t K, int64_t T) { return
 
 extern "C" int64_t q4_0_q8_0_gemm_workspace_size(int64_t O, int64_t K, int64_t T) {
     if (O < 1) return QDG_EINVAL;
+    if (O > (1 << 30)) return QDG_ESHAPE;   // the product refuses such an O as well
     return qdg::gemm_workspace_bytes(K, T);
 }
 

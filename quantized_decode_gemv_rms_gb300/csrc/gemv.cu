@@ -29,7 +29,6 @@
 #include "common.cuh"
 
 #include <algorithm>
-#include <mutex>
 
 namespace qdg {
 
@@ -541,17 +540,8 @@ int gemv_rmsnorm_launch(const void* const* W, float* const* y, const int64_t* O,
     a.O = total;
     a.K = static_cast<int>(K);
     const size_t smem = static_cast<size_t>(8) * K + static_cast<size_t>(K / 32) * 34;
-    {
-        static std::mutex mu;
-        static size_t set_bytes = 0;
-        std::lock_guard<std::mutex> lock(mu);
-        if (set_bytes < smem) {
-            if (cudaFuncSetAttribute(gemv_kernel<kQ4, true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(smem)) != cudaSuccess)
-                return QDG_ECUDA;
-            set_bytes = smem;
-        }
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(gemv_kernel<kQ4, true, false>), smem) != cudaSuccess)
+        return QDG_ECUDA;
     const cudaError_t e = launch(gemv_kernel<kQ4, true, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(5);

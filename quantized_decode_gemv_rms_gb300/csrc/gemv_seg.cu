@@ -32,7 +32,6 @@
 #include "common.cuh"
 
 #include <algorithm>
-#include <mutex>
 
 namespace qdg {
 
@@ -677,18 +676,8 @@ int gemv_seg_rmsnorm_launch(const void* const* W, float* const* y, const int64_t
     a.xq_out = static_cast<uint8_t*>(xq_out);
     a.O = total;
     const size_t smem = static_cast<size_t>(plan.nb) * 34 + static_cast<size_t>(8) * K;
-    {
-        static std::mutex mu;
-        static bool set = false;
-        std::lock_guard<std::mutex> lock(mu);
-        if (!set) {
-            const size_t most = static_cast<size_t>(kFusedMaxK / 32) * 34 + static_cast<size_t>(8) * kFusedMaxK;
-            if (cudaFuncSetAttribute(gemv_seg_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(most)) != cudaSuccess)
-                return QDG_ECUDA;
-            set = true;
-        }
-    }
+    if (ensure_smem_limit(reinterpret_cast<const void*>(gemv_seg_kernel<true, false>), smem) != cudaSuccess)
+        return QDG_ECUDA;
     const cudaError_t e = launch(gemv_seg_kernel<true, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(9);
@@ -716,21 +705,10 @@ int gemv_seg2_launch(const void* W, const void* xq, float* y, int64_t ldy, int64
     a.O = O;
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, O));
     const size_t smem = a.xq_bulk ? static_cast<size_t>(2) * plan.nb * 34 : 0;
-    {
-        // both vectors of the largest K (2 x 1024 x 34 bytes) exceed the default 48 KB
-        static std::mutex mu;
-        static bool set = false;
-        std::lock_guard<std::mutex> lock(mu);
-        if (!set) {
-            const int most = 2 * (32768 / 32) * 34;
-            if (cudaFuncSetAttribute(gemv_seg2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
-                    cudaSuccess ||
-                cudaFuncSetAttribute(gemv_seg2_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) !=
-                    cudaSuccess)
-                return QDG_ECUDA;
-            set = true;
-        }
-    }
+    // both vectors of a large K (up to 2 x 1024 x 34 bytes) exceed the default 48 KB
+    if (ensure_smem_limit(reinterpret_cast<const void*>(gemv_seg2_kernel<false>), smem) != cudaSuccess ||
+        ensure_smem_limit(reinterpret_cast<const void*>(gemv_seg2_kernel<true>), smem) != cudaSuccess)
+        return QDG_ECUDA;
     cudaError_t e;
     if (dbg)
         e = launch(gemv_seg2_kernel<true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);

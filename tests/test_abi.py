@@ -220,6 +220,7 @@ def test_gemm_host_validation(L):
     assert L.q4_0_q8_0_gemm_workspace_bytes(256, 0) == -1
     assert L.q4_0_q8_0_gemm_workspace_size(14336, 256, 129) == 2 * 8 * 8704   # O does not change it
     assert L.q4_0_q8_0_gemm_workspace_size(0, 256, 129) == -1
+    assert L.q4_0_q8_0_gemm_workspace_size((1 << 30) + 1, 256, 129) == -3   # the product refuses this O
     assert f(A16, A16, None, 8, 8, 256, 4, A16, need, None) == -1     # null y
     assert f(A16, A16, A16, 4, 8, 256, 4, A16, need, None) == -1      # ldy < O
     assert f(A16, A16, A16, 8, 8, 256, 0, A16, need, None) == -1      # T = 0
