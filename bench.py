@@ -440,9 +440,9 @@ def bench_ours(args, wl, world, rank, local):
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     wbytes = sum(workloads.q4_0_bytes(m.rows, m.cols) for m in wl.matrices)
     need = -(-3 * l2 // wbytes)                      # ceil(3 L2 / weight bytes)
-    copies = 1 if wbytes > 3 * l2 else N_INPUT_SETS * -(-need // N_INPUT_SETS)
-    spg = max(N_INPUT_SETS, copies)                 # steps per graph: every input set and copy once
-    step = DecodeStep(wl, device, layout=args.layout, copies=copies)
+    wcopies = 1 if wbytes > 3 * l2 else N_INPUT_SETS * -(-need // N_INPUT_SETS)
+    spg = max(N_INPUT_SETS, wcopies)                 # steps per graph: every input set and copy once
+    step = DecodeStep(wl, device, layout=args.layout, copies=wcopies)
     stream = torch.cuda.current_stream()
     nbytes = step_bytes(wl)
     fused = args.fused
@@ -462,7 +462,7 @@ def bench_ours(args, wl, world, rank, local):
     graphs = {}
     counts = {}
     # One graph holds spg consecutive steps (input set k % N_INPUT_SETS,
-    # weight copy k % copies), as a multi-layer forward pass would:
+    # weight copy k % wcopies), as a multi-layer forward pass would:
     # programmatic dependent launch chains the kernels inside a graph, while
     # consecutive graph launches serialise.
     with torch.cuda.stream(side):
@@ -471,7 +471,7 @@ def bench_ours(args, wl, world, rank, local):
 
             def steps(fz=fz):
                 for k in range(spg):
-                    step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % copies)
+                    step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % wcopies)
             graphs[fz] = capture(steps, side)
             after = [qdg.qdg_launch_count(i) for i in range(11)]
             counts[fz] = [(after[i] - before[i]) // spg for i in range(11)]
@@ -494,12 +494,12 @@ def bench_ours(args, wl, world, rank, local):
         """n decode steps: whole graphs of spg steps, the remainder eagerly."""
         if not args.graph:
             for k in range(n):
-                step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % copies)
+                step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % wcopies)
             return
         for _ in range(n // spg):
             graphs[fz].replay()
         for k in range(n % spg):
-            step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % copies)
+            step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % wcopies)
 
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -640,7 +640,7 @@ def bench_ours(args, wl, world, rank, local):
         if args.graph:
             def e2e_steps():
                 for k in range(spg):
-                    _e2e_step(step, None, k, fused, staging, copy=k % copies)
+                    _e2e_step(step, None, k, fused, staging, copy=k % wcopies)
             with torch.cuda.stream(side):
                 e2e_graph = capture(e2e_steps, side)
             stream.wait_stream(side)
@@ -652,7 +652,7 @@ def bench_ours(args, wl, world, rank, local):
                     e2e_graph.replay()
             else:
                 for k in range(n):
-                    _e2e_step(step, None, k, fused, staging, copy=k % copies)
+                    _e2e_step(step, None, k, fused, staging, copy=k % wcopies)
         run_e2e(spg)
         torch.cuda.synchronize()
         barrier(world)
@@ -701,8 +701,8 @@ def bench_ours(args, wl, world, rank, local):
         "config": {"workload": wl.name, "batch": 1, "matrices": {m.name: [m.rows, m.cols] for m in wl.matrices},
                    "bytes_per_step": nbytes,
                    "l2": (f"inputs larger than L2 ({wbytes / 1e6:.0f} MB of weights per step vs "
-                          f"{l2 / 1e6:.0f} MB L2)" if copies == 1 else
-                          f"weights rotate through {copies} copies ({copies * wbytes / 1e6:.0f} MB, more than "
+                          f"{l2 / 1e6:.0f} MB L2)" if wcopies == 1 else
+                          f"weights rotate through {wcopies} copies ({wcopies * wbytes / 1e6:.0f} MB, more than "
                           f"three times the {l2 / 1e6:.0f} MB L2), so every step reads its weights from HBM"),
                    "route": (("fused: one RMSNorm->Q8_0->GEMV launch per group" +
                               (f" (K <= {FUSED_SEG_MAX_K}; split for larger K)" if args.layout == "seg" else ""))
