@@ -358,6 +358,8 @@ class DecodeStep:
                 self.groups[-1].append(m)
             else:
                 self.groups.append([m])
+        # the chain route's sync words (zero; every chain launch leaves them zero)
+        self.sync = torch.zeros(qdg.q4_0s_gemv_chain_sync_bytes(), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()      # release the fp32 staging of the weights
 
@@ -366,8 +368,10 @@ class DecodeStep:
         fused kernel stages the input whole: K <= FUSED_SEG_MAX_K)."""
         return (layout or self.layout) == "plain" or grp[0].cols <= FUSED_SEG_MAX_K
 
-    def launches_per_step(self, fused=True):
-        return sum(1 if fused and self.fusable(g) else 2 for g in self.groups)
+    def launches_per_step(self, route="split"):
+        if route == "chain":
+            return 1
+        return sum(1 if route == "fused" and self.fusable(g) else 2 for g in self.groups)
 
     def run_group(self, grp, xs, Ws=None, layout=None):
         """One fused launch for projections that read the same activation."""
@@ -389,12 +393,32 @@ class DecodeStep:
         assert self.layout == self.copies_layout, "weight copies exist for one layout only"
         return [self.Wcopies[copy][m.name] for m in grp]
 
-    def run(self, xs, events=None, fused=True, copy=0):
-        """One decode step in dependency order: for each group of projections
-        sharing an input -- fused: one launch (RMSNorm*gamma -> Q8_0 -> GEMV);
-        split: the quantize kernel, then one grouped GEMV launch.  `copy`
-        picks the weight copy the step reads."""
+    def chain_stages(self, xs, copy=0):
+        """The step as chain stages: one per group, in dependency order."""
+        stages = []
+        for grp in self.groups:
+            tag = grp[0].source.split(":", 1)[1]
+            Ws = self.copy_weights(grp, copy) or [self.Wr[m.name] for m in grp]
+            stages.append({"x": xs[tag], "gamma": self.gamma.get(tag) if self.kinds[tag] == "norm" else None,
+                           "K": grp[0].cols, "Ws": Ws, "ys": [self.y[m.name] for m in grp],
+                           "Os": [m.rows for m in grp], "xq_out": self.xq[tag]})
+        return stages
+
+    def run(self, xs, events=None, fused=True, copy=0, route=None):
+        """One decode step in dependency order.  route "chain": one launch
+        runs every group (norm/quantize, then the grouped GEMV), each group
+        after the previous one's outputs; for each group of projections
+        sharing an input -- "fused": one launch (RMSNorm*gamma -> Q8_0 ->
+        GEMV); "split": the quantize kernel, then one grouped GEMV launch.
+        Without a route, `fused` picks between the last two.  `copy` picks the
+        weight copy the step reads."""
         qdg = self.qdg
+        route = route or ("fused" if fused else "split")
+        if route == "chain":
+            assert self.layout == "seg", "the chain reads the segment layout"
+            qdg.q4_0s_gemv_chain(self.chain_stages(xs, copy), self.wl.eps, self.sync)
+            return
+        fused = route == "fused"
         for grp in self.groups:
             Ws = self.copy_weights(grp, copy)
             if fused and self.fusable(grp):
@@ -445,13 +469,14 @@ def bench_ours(args, wl, world, rank, local):
     step = DecodeStep(wl, device, layout=args.layout, copies=wcopies)
     stream = torch.cuda.current_stream()
     nbytes = step_bytes(wl)
-    fused = args.fused
-    L = step.launches_per_step(fused)
+    route = args.route
+    routes = [route] + [r for r in ("chain", "split", "fused") if r != route and (r != "chain" or args.layout == "seg")]
+    L = step.launches_per_step(route)
 
-    # eager warm-up of both routes (also sets kernel attributes before capture)
-    for fz in (True, False):
+    # eager warm-up of every route (also sets kernel attributes before capture)
+    for r in routes:
         for i in range(3):
-            step.run(step.x_dev[i % N_INPUT_SETS], fused=fz)
+            step.run(step.x_dev[i % N_INPUT_SETS], route=r)
     torch.cuda.synchronize()
     assert qdg.qdg_device_status() == qdg.QDG_OK
 
@@ -465,41 +490,49 @@ def bench_ours(args, wl, world, rank, local):
     # weight copy k % wcopies), as a multi-layer forward pass would:
     # programmatic dependent launch chains the kernels inside a graph, while
     # consecutive graph launches serialise.
+    NC = 12                                         # launch counters of the library
     with torch.cuda.stream(side):
-        for fz in (fused, not fused):
-            before = [qdg.qdg_launch_count(i) for i in range(11)]
+        for r in routes:
+            before = [qdg.qdg_launch_count(i) for i in range(NC)]
 
-            def steps(fz=fz):
+            def steps(r=r):
                 for k in range(spg):
-                    step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % wcopies)
-            graphs[fz] = capture(steps, side)
-            after = [qdg.qdg_launch_count(i) for i in range(11)]
-            counts[fz] = [(after[i] - before[i]) // spg for i in range(11)]
+                    step.run(step.x_dev[k % N_INPUT_SETS], route=r, copy=k % wcopies)
+            graphs[r] = capture(steps, side)
+            after = [qdg.qdg_launch_count(i) for i in range(NC)]
+            counts[r] = [(after[i] - before[i]) // spg for i in range(NC)]
     stream.wait_stream(side)
     torch.cuda.synchronize()
     ng = len(step.groups)
     gk = 6 if args.layout == "seg" else 1          # launch counter of the split route's GEMV
     fk = 9 if args.layout == "seg" else 5          # and of the fused kernel
     nf = sum(1 for g in step.groups if step.fusable(g))
-    assert counts[True][fk] == nf and counts[True][0] == ng - nf and counts[True][gk] == ng - nf, counts
-    assert counts[False][0] == ng and counts[False][gk] == ng and counts[False][fk] == 0, counts
+    if "fused" in counts:
+        c = counts["fused"]
+        assert c[fk] == nf and c[0] == ng - nf and c[gk] == ng - nf and c[11] == 0, counts
+    if "split" in counts:
+        c = counts["split"]
+        assert c[0] == ng and c[gk] == ng and c[fk] == 0 and c[11] == 0, counts
+    if "chain" in counts:
+        c = counts["chain"]
+        assert c[11] == 1 and sum(c) == 1, counts
     for c in counts.values():
         assert c[7 - gk] == 0 and c[14 - fk] == 0, counts
-    fusion = {"route": "fused" if fused else "split",
-              "per_step_launches": {"fused_norm_gemv" + ("_seg" if args.layout == "seg" else ""): counts[fused][fk],
-                                    "quantize": counts[fused][0],
-                                    "gemv" + ("_seg" if args.layout == "seg" else ""): counts[fused][gk]}}
+    sfx = "_seg" if args.layout == "seg" else ""
+    fusion = {"route": route,
+              "per_step_launches": {"chain": counts[route][11], "fused_norm_gemv" + sfx: counts[route][fk],
+                                    "quantize": counts[route][0], "gemv" + sfx: counts[route][gk]}}
 
-    def run_steps(n, fz=fused):
+    def run_steps(n, r=route):
         """n decode steps: whole graphs of spg steps, the remainder eagerly."""
         if not args.graph:
             for k in range(n):
-                step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % wcopies)
+                step.run(step.x_dev[k % N_INPUT_SETS], route=r, copy=k % wcopies)
             return
         for _ in range(n // spg):
-            graphs[fz].replay()
+            graphs[r].replay()
         for k in range(n % spg):
-            step.run(step.x_dev[k % N_INPUT_SETS], fused=fz, copy=k % wcopies)
+            step.run(step.x_dev[k % N_INPUT_SETS], route=r, copy=k % wcopies)
 
     try:
         smi_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
@@ -544,7 +577,7 @@ def bench_ours(args, wl, world, rank, local):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
         evs[0].record(stream)
         for i in range(reps):
-            graphs[fused].replay()
+            graphs[route].replay()
             evs[i + 1].record(stream)
         torch.cuda.synchronize()
         per = sorted(evs[i].elapsed_time(evs[i + 1]) * 1e3 / spg for i in range(reps))
@@ -553,16 +586,18 @@ def bench_ours(args, wl, world, rank, local):
                 "samples": reps, "unit": "us per step",
                 "how": f"CUDA events around each replay of the {spg}-step graph"}
 
-    # ---- the other route, same number of steps, for comparison
-    run_steps(args.warmup, not fused)
-    torch.cuda.synchronize()
+    # ---- the other routes, same number of steps, for comparison
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    run_steps(args.steps, not fused)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    ms_other = f0.elapsed_time(f1) / args.steps
+    ms_other = {}
+    for r in routes[1:]:
+        run_steps(args.warmup, r)
+        torch.cuda.synchronize()
+        f0.record(stream)
+        run_steps(args.steps, r)
+        f1.record(stream)
+        torch.cuda.synchronize()
+        ms_other[r] = f0.elapsed_time(f1) / args.steps
 
     # ---- per-launch cost of each group's launch (GEMV alone on a prepared Q8_0
     # vector, and the fused launch): a graph of C back-to-back launches, each on
@@ -640,7 +675,7 @@ def bench_ours(args, wl, world, rank, local):
         if args.graph:
             def e2e_steps():
                 for k in range(spg):
-                    _e2e_step(step, None, k, fused, staging, copy=k % wcopies)
+                    _e2e_step(step, None, k, route=route, staging=staging, copy=k % wcopies)
             with torch.cuda.stream(side):
                 e2e_graph = capture(e2e_steps, side)
             stream.wait_stream(side)
@@ -652,7 +687,7 @@ def bench_ours(args, wl, world, rank, local):
                     e2e_graph.replay()
             else:
                 for k in range(n):
-                    _e2e_step(step, None, k, fused, staging, copy=k % wcopies)
+                    _e2e_step(step, None, k, route=route, staging=staging, copy=k % wcopies)
         run_e2e(spg)
         torch.cuda.synchronize()
         barrier(world)
@@ -665,30 +700,38 @@ def bench_ours(args, wl, world, rank, local):
     ms_e2e_engine = measure_e2e("engine")
 
     peaks, peak_src = measured_peaks()
-    def main_kind(grp):
-        if args.layout == "seg":
-            return "fused_seg" if fused and step.fusable(grp) else "gemv_seg"
-        return "fused" if fused else "gemv"
-    mk = {"+".join(m.name for m in g): main_kind(g) for g in step.groups}
-    kern_bytes = sum(launch_bytes[k][n] for n, k in mk.items())
-    # the dominant kernel's average launch from the per-launch graphs above
-    achieved = kern_bytes / (sum(per_call[k][n] for n, k in mk.items()) * 1e-6) / 1e9
-    names = {"fused": "gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)",
-             "gemv": "gemv_kernel (q4_0_q8_0_gemv_group)",
-             "gemv_seg": "gemv_seg_kernel (q4_0s_q8_0_gemv_group)",
-             "fused_seg": "gemv_seg_kernel<fused> (q4_0s_gemv_rmsnorm_group)"}
-    kernel = " + ".join(sorted({names[k] for k in mk.values()}))
-    used = set(mk.values())
-    traffic = (ncu_traffic("gemv_seg.cu") if used == {"gemv_seg"} else
-               ncu_traffic("gemv.cu") if used == {"gemv"} else None)
+    if route == "chain":
+        # one launch is the whole step: its algorithmic bytes over the average
+        # launch time of the timed region (events on the launching stream)
+        kernel = "gemv_chain_kernel (q4_0s_gemv_chain)"
+        kern_bytes, launches = nbytes, 1
+        achieved = nbytes / (ms * 1e-3) / 1e9
+        traffic = ncu_traffic("gemv_chain.cu")
+    else:
+        def main_kind(grp):
+            if args.layout == "seg":
+                return "fused_seg" if route == "fused" and step.fusable(grp) else "gemv_seg"
+            return "fused" if route == "fused" else "gemv"
+        mk = {"+".join(m.name for m in g): main_kind(g) for g in step.groups}
+        kern_bytes, launches = sum(launch_bytes[k][n] for n, k in mk.items()), len(step.groups)
+        # the dominant kernel's average launch from the per-launch graphs above
+        achieved = kern_bytes / (sum(per_call[k][n] for n, k in mk.items()) * 1e-6) / 1e9
+        names = {"fused": "gemv_kernel<fused> (q4_0_gemv_rmsnorm_group)",
+                 "gemv": "gemv_kernel (q4_0_q8_0_gemv_group)",
+                 "gemv_seg": "gemv_seg_kernel (q4_0s_q8_0_gemv_group)",
+                 "fused_seg": "gemv_seg_kernel<fused> (q4_0s_gemv_rmsnorm_group)"}
+        kernel = " + ".join(sorted({names[k] for k in mk.values()}))
+        used = set(mk.values())
+        traffic = (ncu_traffic("gemv_seg.cu") if used == {"gemv_seg"} else
+                   ncu_traffic("gemv.cu") if used == {"gemv"} else None)
     roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)" if peak_src == "measured"
                             else "fallback 6.8 TB/s"),
             "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
             "traffic_source": (traffic.get("what") if traffic else "no ncu capture of this source yet"),
-            "algorithmic_bytes_per_launch": round(kern_bytes / len(step.groups)),
-            "launches_of_this_kernel_per_step": len(step.groups),
+            "algorithmic_bytes_per_launch": round(kern_bytes / launches),
+            "launches_of_this_kernel_per_step": launches,
             "achieved_over_whole_step": round(kern_bytes / (ms * 1e-3) / 1e9, 1),
             "frac_of_nominal_8TB": round(achieved / 8000.0, 4)}
     result = {
@@ -704,9 +747,12 @@ def bench_ours(args, wl, world, rank, local):
                           f"{l2 / 1e6:.0f} MB L2)" if wcopies == 1 else
                           f"weights rotate through {wcopies} copies ({wcopies * wbytes / 1e6:.0f} MB, more than "
                           f"three times the {l2 / 1e6:.0f} MB L2), so every step reads its weights from HBM"),
-                   "route": (("fused: one RMSNorm->Q8_0->GEMV launch per group" +
-                              (f" (K <= {FUSED_SEG_MAX_K}; split for larger K)" if args.layout == "seg" else ""))
-                             if fused else "split: quantize kernel + grouped GEMV launch per group") +
+                   "route": ({"chain": "chain: one launch per step (every group's RMSNorm->Q8_0 and grouped GEMV, "
+                                       "each group after the previous group's outputs)",
+                              "fused": "fused: one RMSNorm->Q8_0->GEMV launch per group" +
+                                       (f" (K <= {FUSED_SEG_MAX_K}; split for larger K)" if args.layout == "seg"
+                                        else ""),
+                              "split": "split: quantize kernel + grouped GEMV launch per group"}[route]) +
                             ("; weights in the segment layout (repacked at load)" if args.layout == "seg"
                              else "; weights in plain Q4_0 blocks") +
                             "; groups " + ", ".join("+".join(m.name for m in g) for g in step.groups) +
@@ -725,9 +771,8 @@ def bench_ours(args, wl, world, rank, local):
                           "fused: norm+quantize+GEMV; fused_seg: the same on the segment layout, K <= 8192); "
                           "graph of back-to-back launches on distinct weight copies "
                           "(> 3 x L2), PDL as configured"),
-        "other_route": {"route": "split" if fused else "fused",
-                        "us_per_step": round(ms_other * 1e3, 2),
-                        "value": round(nbytes / (ms_other * 1e-3) / 1e9, 1)},
+        "other_routes": {r: {"us_per_step": round(v * 1e3, 2), "value": round(nbytes / (v * 1e-3) / 1e9, 1)}
+                         for r, v in ms_other.items()},
         "fusion_check": fusion,
         "roofline": roof,
         "e2e": {"value": round(nbytes * world / (ms_e2e * 1e-3) / 1e9, 1), "unit": UNIT,
@@ -876,7 +921,7 @@ def bench_extras(args, device):
     return out
 
 
-def _e2e_step(step, graphs, k, fused=True, staging="kernel", copy=0):
+def _e2e_step(step, graphs, k, fused=True, staging="kernel", copy=0, route=None):
     """One step from host buffers: every input vector in (one copy), the step,
     every output out (one copy).  staging="kernel": the library's staging
     kernel reads and writes the mapped pinned buffers (the copies stay in the
@@ -886,7 +931,7 @@ def _e2e_step(step, graphs, k, fused=True, staging="kernel", copy=0):
         step.qdg.qdg_stage_copy(step.x_dev_flat[p], step.x_host_flat[p])
     else:
         step.x_dev_flat[p].copy_(step.x_host_flat[p], non_blocking=True)
-    step.run(step.x_dev[p], fused=fused, copy=copy)
+    step.run(step.x_dev[p], fused=fused, copy=copy, route=route)
     if staging == "kernel":
         step.qdg.qdg_stage_copy(step.y_host_flat, step.y_flat)
     else:
@@ -901,9 +946,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.LLAMA_8B.name, choices=sorted(workloads.ALL))
     ap.add_argument("--no-graph", dest="graph", action="store_false")
-    ap.add_argument("--fused", action="store_true",
-                    help="time the fused route (one norm+quantize+GEMV launch per group) as the main line; "
-                         "the default main line is quantize kernel + grouped GEMV per group")
+    ap.add_argument("--route", choices=["chain", "split", "fused"], default="chain",
+                    help="the timed main line: chain = one launch per step (default); split = quantize kernel + "
+                         "grouped GEMV per group; fused = one norm+quantize+GEMV launch per group")
     ap.add_argument("--layout", choices=["seg", "plain"], default="seg",
                     help="weight layout the split route's GEMV reads: seg = segment layout repacked at load "
                          "(default), plain = Q4_0 blocks as stored")

@@ -364,6 +364,56 @@ QDG_API int q4_0s_gemv_rmsnorm_group(const void* const* Wr, float* const* y, con
                                      qdg_stream_t stream);
 
 /*
+ * q4_0s_gemv_chain -- the stages of a decode step in one launch.  Stage g
+ * quantizes its input (RMS_NORM * gamma -> Q8_0, or plain Q8_0 when gamma is
+ * NULL; the arithmetic of qnorm_quantize_q8_0, so the Q8_0 vector is the
+ * same bit for bit) and multiplies it by up to four matrices in the segment
+ * layout (q4_0_repack_seg), as q4_0s_q8_0_gemv_group does.  Stage g+1 reads
+ * its input only after every output of stage g is written, so a stage may
+ * read what an earlier stage wrote (its x may be an earlier stage's y).
+ *   [RMS_NORM+MUL as one fused step: llama.cpp b10909: Metal backend
+ *   fusion-table refactor, introduction and section "CI and related fixes";
+ *   batch-1 decode on the quantized matrix-vector route: GGML: Backend
+ *   abstraction and hardware acceleration, section "CUDA: mmvq, mmq,
+ *   cublas -- three matrix paths"]
+ * The pages describe the separate kernels; running a step's stages as one
+ * persistent launch (cooperative: one CTA per SM, all resident, meeting at a
+ * device-wide barrier between stages) is this library's GB300 design: it
+ * removes the launch and grid-completion gaps at every stage boundary.
+ *
+ * stages   host array of nstages (1..8) stage descriptions:
+ *   x        fp32 [K] input, 16-byte aligned.
+ *   gamma    fp32 [K], 16-byte aligned, or NULL (no norm).
+ *   xq_out   Q8_0 [K/32] copy of the stage's quantized input, or NULL.
+ *   K        multiple of 256, 256 <= K <= 16384.
+ *   count    matrices that read this input, 1..4; W[i] segment-layout
+ *            weights of O[i] rows (16-byte aligned), y[i] fp32 [O[i]]
+ *            (4-byte aligned); sum of O[i] < 2^31.
+ * eps      epsilon of the norm (>= 0), added to the mean square inside the root.
+ * sync     device array of q4_0s_gemv_chain_sync_bytes() bytes, 4-byte
+ *          aligned, zeroed once before its first use; every launch leaves it
+ *          zero again.  Launches that may run at the same time need separate
+ *          arrays.  After a QDG_ETIMEOUT report it must be zeroed again.
+ * Errors: QDG_EINVAL, QDG_ESHAPE, QDG_EALIGN as the single calls;
+ * QDG_ECUDA if the cooperative launch is refused.  Results are
+ * deterministic: every output row is summed in a fixed order.
+ */
+typedef struct {
+    const float* x;
+    const float* gamma;
+    void* xq_out;
+    int64_t K;
+    int count;
+    const void* W[4];
+    float* y[4];
+    int64_t O[4];
+} qdg_chain_stage;
+
+QDG_API int64_t q4_0s_gemv_chain_sync_bytes(void);
+QDG_API int q4_0s_gemv_chain(const qdg_chain_stage* stages, int nstages, float eps, void* sync,
+                             qdg_stream_t stream);
+
+/*
  * qdg_device_status -- synchronise `stream`, then read and clear the device
  * flags of every kernel of this library on the current device.  Returns
  * QDG_OK, QDG_ETIMEOUT (a bounded wait gave up; that call's output is
@@ -408,7 +458,8 @@ QDG_API int qdg_stage_copy(void* dst, const void* src, int64_t bytes, qdg_stream
  * qdg_launch_count -- number of kernels this library has launched in this
  * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
  * 4 weight quantize, 5 fused norm+gemv, 6 segment-layout gemv, 7 repack,
- * 8 Q8_0-weight gemv, 9 fused norm+gemv on the segment layout, 10 staging copy, -1 total.  Lets a caller check
+ * 8 Q8_0-weight gemv, 9 fused norm+gemv on the segment layout, 10 staging copy,
+ * 11 decode-step chain, -1 total.  Lets a caller check
  * that the fused kernel is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);

@@ -15,7 +15,7 @@ namespace {
 std::mutex g_dev_mutex;
 DeviceInfo g_dev_cache[64];
 std::atomic<int> g_pdl{0};
-std::atomic<int64_t> g_counts[11];
+std::atomic<int64_t> g_counts[12];
 }  // namespace
 
 DeviceInfo device_info() {
@@ -100,7 +100,7 @@ extern "C" int64_t qdg_launch_count(int which) {
         for (auto& c : g_counts) t += c.load();
         return t;
     }
-    if (which < 0 || which >= 11) return -1;
+    if (which < 0 || which >= 12) return -1;
     return g_counts[which].load();
 }
 
@@ -126,7 +126,8 @@ extern "C" int qdg_device_status(qdg_stream_t stream) {
     unsigned f = 0;
     const unsigned parts[] = {flags_read_clear_quantize(s), flags_read_clear_gemv(s), flags_read_clear_gemv_seg(s),
                               flags_read_clear_small_n(s), flags_read_clear_small_n_seg(s),
-                              flags_read_clear_gemm(s), flags_read_clear_api(s)};
+                              flags_read_clear_gemm(s), flags_read_clear_api(s),
+                              flags_read_clear_chain(s)};
     for (unsigned p : parts) {
         if (p == ~0u) {
             cudaGetLastError();

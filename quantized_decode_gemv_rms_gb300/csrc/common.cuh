@@ -239,6 +239,7 @@ int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t
 int small_n_seg_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t N,
                        cudaStream_t stream, int32_t* dbg);
 int64_t gemm_workspace_bytes(int64_t K, int64_t T);
+int chain_launch(const qdg_chain_stage* stages, int nstages, float eps, void* sync, cudaStream_t stream);
 int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t T, void* ws,
                 int64_t ws_bytes, cudaStream_t stream, int32_t* dbg);
 
@@ -250,5 +251,6 @@ unsigned flags_read_clear_small_n(cudaStream_t stream);
 unsigned flags_read_clear_small_n_seg(cudaStream_t stream);
 unsigned flags_read_clear_gemm(cudaStream_t stream);
 unsigned flags_read_clear_api(cudaStream_t stream);
+unsigned flags_read_clear_chain(cudaStream_t stream);
 
 }  // namespace qdg

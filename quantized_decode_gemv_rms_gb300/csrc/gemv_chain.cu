@@ -1,0 +1,531 @@
+// gemv_chain.cu -- the stages of a decode step (RMS_NORM * gamma -> Q8_0 of
+// a stage's input, then the Q4_0 x Q8_0 products that read it) run by one
+// persistent launch, each stage after every output of the stage before it.
+//
+// Why one launch.  A stage boundary on the chain of separate launches
+// (quantize kernel, then GEMV) costs two grid completions, a launch and a
+// round trip for the Q8_0 vector that queues behind the GEMV's own weight
+// loads: measured per-CTA timelines of the 8B-shaped step on GB300 showed
+// 4.5-5.5 us from the end of one GEMV to the first block dot of the next,
+// with HBM mostly idle, at each of five boundaries.  The pages tie a lost
+// RMS_NORM+MUL fusion to a ~5% token-generation loss [llama.cpp b10909:
+// Metal backend fusion-table refactor, introduction]; the fusion here goes
+// one step further and takes the launch boundary out as well.
+//
+// Design (one CTA of 16 warps per SM, cooperative launch: every CTA is
+// resident, so CTAs may wait on one another):
+//   * Stage input.  After the stage barrier every CTA copies x (and gamma)
+//     into shared memory with 16-byte cp.async copies cached in L2 only,
+//     forms sum(x^2) in the library's fixed order and quantizes every block
+//     with the arithmetic of the standalone quantize kernel, so its Q8_0
+//     vector is the same bit for bit (CTA 0 also writes it out when asked).
+//     The codes go to two shared planes (bytes 0-15 and 16-31 of each block)
+//     so that lanes reading consecutive blocks hit distinct banks; the fp32
+//     scale and the code sum of each block sit beside them.
+//   * Products.  The stage's matrices are stacked row by row.  Work comes in
+//     units of U consecutive rows (U = 4, 2 or 1 by the segment count, so a
+//     unit has at least four row-segments); each warp takes units from a
+//     global counter, so CTAs on slower SMs simply take fewer.  A warp runs
+//     a unit's row-segments segment by segment through an eight-deep
+//     register ring (two 16-byte nibble loads and one scale word per lane,
+//     the segment layout of gemv_seg.cu), reloads its activation blocks from
+//     shared memory once per segment, accumulates each row in a lane
+//     register, and reduces the unit's rows in one transposed butterfly.
+//     The order of every row's sum is fixed, whichever warp takes the unit.
+//   * Stage boundary.  A warp that runs out of units takes its first unit of
+//     the next stage and asks L2 to prefetch its rows, so HBM keeps
+//     streaming while the CTAs meet at the barrier (release/acquire through
+//     an arrival counter) and requantize the next input.
+//   * The sync words (unit and arrival counters) start at zero; the last CTA
+//     to finish returns them to zero for the next launch.
+// Every wait is bounded; a timeout sets the device flag (QDG_ETIMEOUT).
+#include "common.cuh"
+
+#include <algorithm>
+
+namespace qdg {
+
+static __device__ unsigned g_flags_chain;
+
+namespace {
+
+constexpr int kWarps = 16;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxStages = 8;
+constexpr int kMaxMats = 4;
+constexpr int kMaxK = 16384;
+constexpr int kMaxBlocks = kMaxK / 32;
+constexpr int kDepth = 8;                   // row-segments in flight per warp
+constexpr int kSegStride = 1152;            // segment layout: 64 x 16 nibble bytes + 128 bytes of scale words
+constexpr int kPrefetchCap = 9216;          // bytes of its first unit a warp prefetches into L2 at a stage change
+constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
+constexpr size_t kSmemBytes = static_cast<size_t>(2) * kMaxK * 4 + static_cast<size_t>(kMaxBlocks) * (16 + 16 + 8);
+
+struct Stage {
+    const float* x;
+    const float* gamma;          // nullptr: plain quantization
+    uint8_t* xq_out;             // nullptr: the Q8_0 vector is not written out
+    const uint8_t* W[kMaxMats];  // segment layout
+    float* y[kMaxMats];
+    int64_t start[kMaxMats];     // first stacked row of matrix i
+    int64_t rows;                // stacked rows
+    int64_t units;               // ceil(rows / U)
+    int count;
+    int K, nb, nseg, rlast, rowbytes;
+    int U;                       // rows per unit: 4, 2 or 1
+};
+
+struct ChainArgs {
+    Stage st[kMaxStages];
+    int nstages;
+    float eps;
+    unsigned* sync;              // [kMaxStages] unit counters, then [kMaxStages] arrival counters
+};
+
+__device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_stream4(const uint8_t* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Sum over one block of code * q_x, codes unsigned 0..15: low nibbles of
+// word i are elements 4i..4i+3, high nibbles elements 16+4i..16+4i+3.
+__device__ __forceinline__ int block_dot(const uint4& q, const uint4& x0, const uint4& x1) {
+    int acc = 0;
+    acc = __dp4a(static_cast<int>(q.x & kNibbles), static_cast<int>(x0.x), acc);
+    acc = __dp4a(static_cast<int>((q.x >> 4) & kNibbles), static_cast<int>(x1.x), acc);
+    acc = __dp4a(static_cast<int>(q.y & kNibbles), static_cast<int>(x0.y), acc);
+    acc = __dp4a(static_cast<int>((q.y >> 4) & kNibbles), static_cast<int>(x1.y), acc);
+    acc = __dp4a(static_cast<int>(q.z & kNibbles), static_cast<int>(x0.z), acc);
+    acc = __dp4a(static_cast<int>((q.z >> 4) & kNibbles), static_cast<int>(x1.z), acc);
+    acc = __dp4a(static_cast<int>(q.w & kNibbles), static_cast<int>(x0.w), acc);
+    acc = __dp4a(static_cast<int>((q.w >> 4) & kNibbles), static_cast<int>(x1.w), acc);
+    return acc;
+}
+
+struct Entry {
+    uint4 a, b;     // nibbles of blocks 64s+l and 64s+32+l
+    uint32_t sc;    // their scales (low, high half)
+};
+
+// Shared-memory image of a stage's quantized input.
+struct ActSmem {
+    uint4* p0;      // [nb] codes 0..15 of each block
+    uint4* p1;      // [nb] codes 16..31
+    int2* ds;       // [nb] (fp32 bits of the fp16 scale, sum of the codes)
+};
+
+// The warp's take of one unit from the stage's counter (lane 0 asks).
+__device__ __forceinline__ int64_t take_unit(unsigned* ctr, int lane) {
+    unsigned u = 0;
+    if (lane == 0) u = atomicAdd(ctr, 1u);
+    return static_cast<int64_t>(__shfl_sync(0xffffffffu, u, 0));
+}
+
+__device__ __forceinline__ int matrix_of(const Stage& S, int64_t row) {
+    int g = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxMats; ++i)
+        if (i < S.count && row >= S.start[i]) g = i;
+    return g;
+}
+
+__device__ __forceinline__ void prefetch_unit(const Stage& S, int64_t unit, int lane) {
+    if (lane != 0 || unit >= S.units) return;
+    const int64_t row = unit * S.U;
+    const int g = matrix_of(S, row);
+    const int64_t mend = (g + 1 < S.count) ? S.start[g + 1] : S.rows;
+    const int64_t n = min(static_cast<int64_t>(S.U), mend - row);
+    const int64_t bytes = min(n * S.rowbytes, static_cast<int64_t>(kPrefetchCap));
+    l2_prefetch(S.W[g] + (row - S.start[g]) * S.rowbytes, static_cast<uint32_t>(bytes));
+}
+
+// Bounded wait of thread 0 until `count` CTAs have arrived.
+__device__ __forceinline__ void wait_arrivals(const unsigned* arrive, unsigned count) {
+    if (ld_acquire(arrive) >= count) return;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < kSpinLimit; ++i) {
+        __nanosleep(64);
+        if (ld_acquire(arrive) >= count) return;
+        if (global_ns() - t0 > kWaitNs) break;
+    }
+    atomicOr(&g_flags_chain, FLAG_TIMEOUT);
+}
+
+// Stage input -> shared memory, statistic, Q8_0 blocks into the planes (and
+// out to global memory from CTA 0 when asked).  Same arithmetic and order as
+// qnorm_q8_kernel: chains j = i mod 256 summed with fma in ascending i, xor
+// butterflies (16, 8, 4, 2, 1), ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)),
+// s = 1/sqrt(sum/K + eps); v = (x*s)*gamma; d = max|v|/127; q = round(v/d)
+// (halves away from zero), clamped to +-127; stored scale fp16(d).
+__device__ void stage_input(const Stage& S, float eps, float* xs, float* gs, const ActSmem& act, float* wsum) {
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int K = S.K;
+    for (int i = tid * 4; i < K; i += kThreads * 4) {
+        cp_async16(xs + i, S.x + i);
+        if (S.gamma != nullptr) cp_async16(gs + i, S.gamma + i);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    float s = 1.0f;
+    if (S.gamma != nullptr) {
+        if (tid < 256) {
+            float acc = 0.0f;
+            for (int i = tid; i < K; i += 256) acc = __fmaf_rn(xs[i], xs[i], acc);
+            acc = warp_sum(acc);
+            if (lane == 0) wsum[warp] = acc;
+        }
+        __syncthreads();
+        const float ss = __fadd_rn(__fadd_rn(__fadd_rn(wsum[0], wsum[1]), __fadd_rn(wsum[2], wsum[3])),
+                                   __fadd_rn(__fadd_rn(wsum[4], wsum[5]), __fadd_rn(wsum[6], wsum[7])));
+        const float mean = __fdiv_rn(ss, static_cast<float>(K));
+        s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+    }
+    const bool out = S.xq_out != nullptr && blockIdx.x == 0;
+    uint8_t* c0 = reinterpret_cast<uint8_t*>(act.p0);
+    uint8_t* c1 = reinterpret_cast<uint8_t*>(act.p1);
+    for (int b0 = warp; b0 < S.nb; b0 += 4 * kWarps) {
+        float v[4], m[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int b = b0 + u * kWarps;
+            v[u] = 0.0f;
+            if (b < S.nb) {
+                v[u] = xs[(b << 5) + lane];
+                if (S.gamma != nullptr) v[u] = __fmul_rn(__fmul_rn(v[u], s), gs[(b << 5) + lane]);
+            }
+            m[u] = fabsf(v[u]);
+        }
+#pragma unroll
+        for (int h = 16; h >= 1; h >>= 1)
+#pragma unroll
+            for (int u = 0; u < 4; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], h));
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int b = b0 + u * kWarps;
+            if (b >= S.nb) break;
+            const float d = __fdiv_rn(m[u], 127.0f);
+            int q = 0;
+            if (d != 0.0f) {
+                float r = roundf(__fdiv_rn(v[u], d));
+                r = fminf(fmaxf(r, -127.0f), 127.0f);
+                q = static_cast<int>(r);
+            }
+            const int qsum = __reduce_add_sync(0xffffffffu, q);
+            const __half dh = __float2half_rn(d);
+            const uint8_t code = static_cast<uint8_t>(static_cast<int8_t>(q));
+            if (lane < 16)
+                c0[16 * b + lane] = code;
+            else
+                c1[16 * b + lane - 16] = code;
+            if (lane == 0) {
+                act.ds[b] = make_int2(__float_as_int(__half2float(dh)), qsum);
+                if (__hisinf(dh)) atomicOr(&g_flags_chain, FLAG_OVERFLOW);
+            }
+            if (out) {
+                uint8_t* blk = S.xq_out + static_cast<int64_t>(b) * 34;
+                if (lane == 0) *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
+                blk[2 + lane] = code;
+            }
+        }
+    }
+    __syncthreads();
+}
+
+// One stage's products, one warp.  Items are the unit's row-segments in the
+// order (segment s, row r), r fastest; the ring holds kDepth of them.
+// cu, n1: the warp's first two units (already taken); returns nothing, but
+// leaves every unit the warp took consumed.
+template <int U>
+__device__ void stage_products(const Stage& S, const ActSmem& act, unsigned* ctr, int64_t cu, int64_t n1) {
+    static_assert(kDepth % U == 0 && U <= 4, "unit rows divide the ring");
+    const int lane = threadIdx.x & 31;
+    const int nseg = S.nseg;                  // U * nseg >= 4 items per unit: the loader is at most two units ahead
+    int64_t n2 = take_unit(ctr, lane);
+
+    // loader position: unit slot (0: cu, 1: n1, 2: n2), segment, row
+    int ls = 0, lr = 0, lk = 0;
+    auto load_item = [&](Entry& e) {
+        const int64_t unit = lk == 0 ? cu : (lk == 1 ? n1 : n2);
+        const int64_t row = unit * U + lr;
+        e.a = make_uint4(0, 0, 0, 0);
+        e.b = e.a;
+        e.sc = 0;
+        if (unit < S.units && row < S.rows) {
+            const int g = matrix_of(S, row);
+            const int r = (ls == nseg - 1) ? S.rlast : 64;
+            const uint8_t* base = S.W[g] + (row - S.start[g]) * S.rowbytes + ls * kSegStride;
+            if (lane < r) e.a = ldg_stream16(base + 16 * lane);
+            if (lane + 32 < r) e.b = ldg_stream16(base + 16 * lane + 512);
+            e.sc = ldg_stream4(base + 16 * r + 4 * lane);
+        }
+        if (++lr == U) {
+            lr = 0;
+            if (++ls == nseg) {
+                ls = 0;
+                ++lk;
+            }
+        }
+    };
+
+    Entry ring[kDepth];
+#pragma unroll
+    for (int k = 0; k < kDepth; ++k) load_item(ring[k]);
+
+    // consumer: segment of the current item; activations of that segment
+    int cs = 0;
+    uint4 xa0, xa1, xb0, xb1;
+    float dxa = 0.0f, dxb = 0.0f;
+    int sa = 0, sb = 0;
+    float acc[U];
+#pragma unroll
+    for (int r = 0; r < U; ++r) acc[r] = 0.0f;
+
+    while (cu < S.units) {
+#pragma unroll
+        for (int k = 0; k < kDepth; ++k) {
+            const int r = k % U;
+            if (r == 0) {
+                // a new segment: this lane's two activation blocks
+                const int ba = 64 * cs + lane, bb = ba + 32;
+                const int rseg = (cs == nseg - 1) ? S.rlast : 64;
+                xa0 = xa1 = xb0 = xb1 = make_uint4(0, 0, 0, 0);
+                dxa = dxb = 0.0f;
+                sa = sb = 0;
+                if (lane < rseg) {
+                    xa0 = act.p0[ba];
+                    xa1 = act.p1[ba];
+                    const int2 t = act.ds[ba];
+                    dxa = __int_as_float(t.x);
+                    sa = t.y;
+                }
+                if (lane + 32 < rseg) {
+                    xb0 = act.p0[bb];
+                    xb1 = act.p1[bb];
+                    const int2 t = act.ds[bb];
+                    dxb = __int_as_float(t.x);
+                    sb = t.y;
+                }
+            }
+            Entry& e = ring[k];
+            const int ia = block_dot(e.a, xa0, xa1) - 8 * sa;
+            const int ib = block_dot(e.b, xb0, xb1) - 8 * sb;
+            const float dwa = half_bits_to_float(e.sc);
+            const float dwb = half_bits_to_float(e.sc >> 16);
+            float p = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
+            p = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), p);
+            acc[r] = __fadd_rn(acc[r], p);
+            load_item(e);   // refill with the item kDepth ahead
+            if (r == U - 1) {
+                if (++cs == nseg) {
+                    // the unit is complete: its U rows in one transposed butterfly
+                    const bool up16 = (lane & 16) != 0, up8 = (lane & 8) != 0;
+                    const float v0 = acc[0], v1 = U > 1 ? acc[1] : 0.0f;
+                    const float v2 = U > 2 ? acc[2] : 0.0f, v3 = U > 3 ? acc[3] : 0.0f;
+                    float k0 = up16 ? v2 : v0, k1 = up16 ? v3 : v1;
+                    k0 = __fadd_rn(k0, __shfl_xor_sync(0xffffffffu, up16 ? v0 : v2, 16));
+                    k1 = __fadd_rn(k1, __shfl_xor_sync(0xffffffffu, up16 ? v1 : v3, 16));
+                    float mm = up8 ? k1 : k0;
+                    mm = __fadd_rn(mm, __shfl_xor_sync(0xffffffffu, up8 ? k0 : k1, 8));
+#pragma unroll
+                    for (int h = 4; h >= 1; h >>= 1) mm = __fadd_rn(mm, __shfl_xor_sync(0xffffffffu, mm, h));
+                    const int q = lane >> 3;
+                    const int64_t row = cu * U + q;
+                    if ((lane & 7) == 0 && q < U && row < S.rows) {
+                        const int g = matrix_of(S, row);
+                        S.y[g][row - S.start[g]] = mm;
+                    }
+#pragma unroll
+                    for (int rr = 0; rr < U; ++rr) acc[rr] = 0.0f;
+                    cs = 0;
+                    cu = n1;
+                    n1 = n2;
+                    n2 = take_unit(ctr, lane);
+                    --lk;
+                    if (cu >= S.units) break;
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_constant__ ChainArgs a) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    __shared__ float wsum[8];
+    float* xs = reinterpret_cast<float*>(smem);
+    float* gs = xs + kMaxK;
+    ActSmem act;
+    act.p0 = reinterpret_cast<uint4*>(gs + kMaxK);
+    act.p1 = act.p0 + kMaxBlocks;
+    act.ds = reinterpret_cast<int2*>(act.p1 + kMaxBlocks);
+    const int lane = threadIdx.x & 31;
+    unsigned* ctr = a.sync;
+    unsigned* arrive = a.sync + kMaxStages;
+
+    // first two units of stage 0; their rows start streaming into L2 before
+    // the wait for the preceding grid
+    int64_t u0 = take_unit(&ctr[0], lane);
+    int64_t u1 = take_unit(&ctr[0], lane);
+    prefetch_unit(a.st[0], u0, lane);
+    pdl_wait();
+
+    for (int g = 0; g < a.nstages; ++g) {
+        const Stage& S = a.st[g];
+        stage_input(S, a.eps, xs, gs, act, wsum);
+        if (S.U == 4)
+            stage_products<4>(S, act, &ctr[g], u0, u1);
+        else if (S.U == 2)
+            stage_products<2>(S, act, &ctr[g], u0, u1);
+        else
+            stage_products<1>(S, act, &ctr[g], u0, u1);
+        if (g + 1 < a.nstages) {
+            u0 = take_unit(&ctr[g + 1], lane);
+            u1 = take_unit(&ctr[g + 1], lane);
+            prefetch_unit(a.st[g + 1], u0, lane);
+            __syncthreads();   // every output of this CTA for stage g is written
+            if (threadIdx.x == 0) {
+                __threadfence();
+                atomicAdd(&arrive[g], 1u);
+                wait_arrivals(&arrive[g], gridDim.x);
+                __threadfence();
+            }
+            __syncthreads();
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned prev = atomicAdd(&arrive[a.nstages - 1], 1u);
+        if (prev == gridDim.x - 1) {
+            // every CTA is past every use of the counters: back to zero
+            for (int g = 0; g < a.nstages; ++g) {
+                atomicExch(&ctr[g], 0u);
+                atomicExch(&arrive[g], 0u);
+            }
+            __threadfence();
+        }
+    }
+}
+
+}  // namespace
+
+unsigned flags_read_clear_chain(cudaStream_t stream) {
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_flags_chain, sizeof(v), 0, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return ~0u;
+    if (cudaMemcpyToSymbolAsync(g_flags_chain, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+        return ~0u;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ~0u;
+    return v;
+}
+
+int chain_launch(const qdg_chain_stage* stages, int nstages, float eps, void* sync, cudaStream_t stream) {
+    if (!stages || !sync) return QDG_EINVAL;
+    if (nstages < 1 || nstages > kMaxStages) return QDG_EINVAL;
+    if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
+    if (!aligned(sync, 4)) return QDG_EALIGN;
+    ChainArgs a{};
+    a.nstages = nstages;
+    a.eps = eps;
+    a.sync = static_cast<unsigned*>(sync);
+    for (int g = 0; g < nstages; ++g) {
+        const qdg_chain_stage& in = stages[g];
+        Stage& S = a.st[g];
+        if (!in.x || in.count < 1 || in.count > kMaxMats || in.K <= 0) return QDG_EINVAL;
+        if (in.K % 256 != 0 || in.K > kMaxK) return QDG_ESHAPE;
+        if (!aligned(in.x, 16) || (in.gamma && !aligned(in.gamma, 16)) || !aligned(in.xq_out, 2)) return QDG_EALIGN;
+        S.x = in.x;
+        S.gamma = in.gamma;
+        S.xq_out = static_cast<uint8_t*>(in.xq_out);
+        int64_t total = 0;
+        for (int i = 0; i < in.count; ++i) {
+            if (!in.W[i] || !in.y[i] || in.O[i] <= 0) return QDG_EINVAL;
+            if (!aligned(in.W[i], 16) || !aligned(in.y[i], 4)) return QDG_EALIGN;
+            S.W[i] = static_cast<const uint8_t*>(in.W[i]);
+            S.y[i] = in.y[i];
+            S.start[i] = total;
+            total += in.O[i];
+        }
+        if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
+        S.count = in.count;
+        S.rows = total;
+        S.K = static_cast<int>(in.K);
+        S.nb = S.K / 32;
+        S.nseg = (S.nb + 63) / 64;
+        S.rlast = S.nb - 64 * (S.nseg - 1);
+        S.rowbytes = static_cast<int>(q4_0_seg_row_bytes(in.K));
+        S.U = S.nseg <= 2 ? 4 : (S.nseg <= 4 ? 2 : 1);
+        S.units = (total + S.U - 1) / S.U;
+    }
+    const DeviceInfo dev = device_info();
+    if (dev.device < 0) return QDG_ECUDA;
+    if (kSmemBytes > dev.smem_optin) return QDG_ECUDA;
+    if (ensure_smem_limit(reinterpret_cast<const void*>(gemv_chain_kernel), kSmemBytes) != cudaSuccess)
+        return QDG_ECUDA;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(dev.sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: they wait on one another
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (pdl_enabled()) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_chain_kernel, a);
+    if (e != cudaSuccess && cfg.numAttrs == 2) {
+        // a cooperative launch that may not also be a programmatic dependent:
+        // launch it stream-ordered instead
+        cudaGetLastError();
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, gemv_chain_kernel, a);
+    }
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return QDG_ECUDA;
+    }
+    count_launch(11);
+    return QDG_OK;
+}
+
+}  // namespace qdg
+
+using namespace qdg;
+
+extern "C" int64_t q4_0s_gemv_chain_sync_bytes(void) { return static_cast<int64_t>(2 * kMaxStages * sizeof(unsigned)); }
+
+extern "C" int q4_0s_gemv_chain(const qdg_chain_stage* stages, int nstages, float eps, void* sync,
+                                qdg_stream_t stream) {
+    return chain_launch(stages, nstages, eps, sync, reinterpret_cast<cudaStream_t>(stream));
+}

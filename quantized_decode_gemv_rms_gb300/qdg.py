@@ -75,6 +75,8 @@ def lib() -> ctypes.CDLL:
             sig["q4_0s_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
             sig["q4_0s_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
             sig["qdg_stage_copy"] = ([p, p, i64, p], i32)
+            sig["q4_0s_gemv_chain_sync_bytes"] = ([], i64)
+            sig["q4_0s_gemv_chain"] = ([p, i32, f32, p, p], i32)
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
                 fn.argtypes = args
@@ -243,6 +245,42 @@ def q4_0s_gemv_rmsnorm_group(Ws, ys, Os, x, gamma, eps: float, K: int, xq_out=No
     O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
     _check(lib().q4_0s_gemv_rmsnorm_group(W_arr, y_arr, O_arr, n, _ptr(x), _ptr(gamma), float(eps), K,
                                           _ptr(xq_out), _stream(stream)), "q4_0s_gemv_rmsnorm_group")
+
+
+class ChainStage(ctypes.Structure):
+    """qdg_chain_stage of include/qdg.h."""
+    _fields_ = [("x", ctypes.c_void_p), ("gamma", ctypes.c_void_p), ("xq_out", ctypes.c_void_p),
+                ("K", ctypes.c_int64), ("count", ctypes.c_int),
+                ("W", ctypes.c_void_p * 4), ("y", ctypes.c_void_p * 4), ("O", ctypes.c_int64 * 4)]
+
+
+def q4_0s_gemv_chain_sync_bytes() -> int:
+    return int(lib().q4_0s_gemv_chain_sync_bytes())
+
+
+def chain_stages(stages):
+    """Marshal stage descriptions -- dicts with x, gamma (or None), K, Ws, ys,
+    Os and optionally xq_out -- into the C array the chain call takes."""
+    arr = (ChainStage * len(stages))()
+    for d, st in zip(arr, stages):
+        d.x = _ptr(st["x"])
+        d.gamma = _ptr(st.get("gamma"))
+        d.xq_out = _ptr(st.get("xq_out"))
+        d.K = int(st["K"])
+        n = len(st["Ws"])
+        d.count = n
+        for i in range(min(n, 4)):
+            d.W[i] = _ptr(st["Ws"][i])
+            d.y[i] = _ptr(st["ys"][i])
+            d.O[i] = int(st["Os"][i])
+    return arr
+
+
+def q4_0s_gemv_chain(stages, eps: float, sync, stream=None) -> None:
+    """A decode step's stages (norm/quantize + grouped segment-layout GEMV each)
+    in one launch; ``stages`` as for chain_stages(), or its result."""
+    arr = stages if isinstance(stages, ctypes.Array) else chain_stages(stages)
+    _check(lib().q4_0s_gemv_chain(arr, len(arr), float(eps), _ptr(sync), _stream(stream)), "q4_0s_gemv_chain")
 
 
 def q4_0s_q8_0_gemm_small_n(Wr, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:

@@ -27,7 +27,7 @@ def test_header_declares_entry_points():
     for must in ("qnorm_quantize_q8_0", "qnorm_add_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
                  "q4_0_q8_0_gemm_workspace_bytes", "q4_0_q8_0_gemm_workspace_size", "qdg_stage_copy", "quantize_q4_0", "q4_0_repack_seg", "q4_0s_q8_0_gemv",
                  "q4_0s_q8_0_gemv_group", "q4_0s_gemv_rmsnorm_group", "q4_0s_q8_0_gemm_small_n", "q4_0_seg_row_bytes", "q8_0_q8_0_gemv", "q8_0_q8_0_gemv_group",
-                 "qdg_device_status", "qdg_status_string"):
+                 "q4_0s_gemv_chain", "q4_0s_gemv_chain_sync_bytes", "qdg_device_status", "qdg_status_string"):
         assert must in names
 
 
@@ -256,7 +256,7 @@ def test_options_and_counters(L):
     assert L.qdg_set_option(1, 2) == -1
     assert L.qdg_set_option(1, 0) == 0
     assert L.qdg_launch_count(-1) >= 0
-    assert L.qdg_launch_count(11) == -1
+    assert L.qdg_launch_count(12) == -1
     assert L.qdg_launch_count(10) >= 0
     assert L.qdg_debug_block_sums(A16, A16, None, 8, 256, 1, 0, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 1, 9, None) == -1
@@ -271,3 +271,33 @@ def test_binding_names_match_header():
         if name in ("qdg_status_string",):
             continue
         assert hasattr(qdg, name), f"binding lacks {name}"
+
+
+def test_chain_host_validation(L):
+    from quantized_decode_gemv_rms_gb300 import qdg
+    assert L.q4_0s_gemv_chain_sync_bytes() == 64
+
+    def stage(K=4096, count=1, x=A16, gamma=None, W=A16, y=A16, O=8):
+        st = (qdg.ChainStage * 1)()
+        st[0].x, st[0].gamma, st[0].K, st[0].count = x, gamma, K, count
+        for i in range(4):
+            st[0].W[i], st[0].y[i], st[0].O[i] = W, y, O
+        return st
+
+    f = L.q4_0s_gemv_chain
+    two = (qdg.ChainStage * 9)()
+    assert f(stage(), 0, 1e-6, A16, None) == -1                   # no stage
+    assert f(two, 9, 1e-6, A16, None) == -1                       # more than eight stages
+    assert f(stage(), 1, 1e-6, None, None) == -1                  # no sync words
+    assert f(stage(), 1, -1.0, A16, None) == -1                   # eps < 0
+    assert f(stage(), 1, 1e-6, A2 + 1, None) == -2                # sync words misaligned
+    assert f(stage(count=0), 1, 1e-6, A16, None) == -1            # no matrix
+    assert f(stage(count=5), 1, 1e-6, A16, None) == -1            # more than four matrices
+    assert f(stage(x=None), 1, 1e-6, A16, None) == -1             # null x
+    assert f(stage(K=320), 1, 1e-6, A16, None) == -3              # K % 256
+    assert f(stage(K=16384 + 256), 1, 1e-6, A16, None) == -3      # K beyond the maximum
+    assert f(stage(x=A2), 1, 1e-6, A16, None) == -2               # x must be 16-byte aligned
+    assert f(stage(gamma=A2), 1, 1e-6, A16, None) == -2           # gamma likewise
+    assert f(stage(W=A2), 1, 1e-6, A16, None) == -2               # weights 16-byte aligned
+    assert f(stage(O=0), 1, 1e-6, A16, None) == -1                # no rows
+    assert f(stage(W=None), 1, 1e-6, A16, None) == -1             # null weights

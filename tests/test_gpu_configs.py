@@ -112,23 +112,24 @@ def test_1b_weights_match_oracle(step1b, expected_1b):
                               oracle.repack_q4_0_seg(Wq[m.name], m.cols)), m.name
 
 
-@pytest.mark.parametrize("route", ["split-seg", "fused-seg", "split-plain", "fused-plain"])
+@pytest.mark.parametrize("route", ["chain-seg", "split-seg", "fused-seg", "split-plain", "fused-plain"])
 def test_1b_decode_step_every_row(step1b, expected_1b, route):
     """Each input set's step replayed from one graph; after every step all
-    outputs (and, on the split route, the Q8_0 vectors) are checked."""
+    outputs (and, on the split and chain routes, the Q8_0 vectors) are checked."""
     torch = torch_cuda()
     _, exp = expected_1b
-    fused = route.startswith("fused")
+    r = route.split("-")[0]
+    fused = r == "fused"
     step1b.layout = "seg" if route.endswith("-seg") else "plain"
     for p in range(bench.N_INPUT_SETS):
-        step1b.run(step1b.x_dev[p], fused=fused)
+        step1b.run(step1b.x_dev[p], route=r)
     torch.cuda.synchronize()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     graphs = []
     with torch.cuda.stream(side):
         for p in range(bench.N_INPUT_SETS):
-            graphs.append(bench.capture(lambda p=p: step1b.run(step1b.x_dev[p], fused=fused), side))
+            graphs.append(bench.capture(lambda p=p: step1b.run(step1b.x_dev[p], route=r), side))
     torch.cuda.current_stream().wait_stream(side)
     for p in range(bench.N_INPUT_SETS):
         step1b.y_flat.fill_(float("nan"))

@@ -3,7 +3,8 @@ benchmark times: a CUDA graph of consecutive steps (one per input set) with
 programmatic dependent launch, through the benchmark's own step object.
 Sampled rows of every projection (the first and last rows, rows on both sides
 of CTA boundaries, and random rows) are compared with the oracle, for the
-split and the fused route, each on the plain and on the segment layout."""
+split and the fused route, each on the plain and on the segment layout, and
+for the chain route (one launch per step)."""
 import numpy as np
 import pytest
 
@@ -62,18 +63,18 @@ def step8b():
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("route", ["split-plain", "split-seg", "fused-plain", "fused-seg"])
+@pytest.mark.parametrize("route", ["split-plain", "split-seg", "fused-plain", "fused-seg", "chain-seg"])
 def test_decode_step_full_size_sampled(step8b, expected, route):
     torch = torch_cuda()
-    fused = route.startswith("fused")
+    r = route.split("-")[0]
     step8b.layout = "seg" if route.endswith("-seg") else "plain"
     for p in range(3):                      # eager warm-up (also sets kernel attributes)
-        step8b.run(step8b.x_dev[p], fused=fused)
+        step8b.run(step8b.x_dev[p], route=r)
     torch.cuda.synchronize()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        g = bench.capture(lambda: [step8b.run(step8b.x_dev[p], fused=fused) for p in range(bench.N_INPUT_SETS)],
+        g = bench.capture(lambda: [step8b.run(step8b.x_dev[p], route=r) for p in range(bench.N_INPUT_SETS)],
                           side)
     torch.cuda.current_stream().wait_stream(side)
     for y in step8b.y.values():
@@ -88,20 +89,20 @@ def test_decode_step_full_size_sampled(step8b, expected, route):
         assert_within_tol(got[None, :], y64, S, what=f"{route}:{m.name}")
 
 
-@pytest.mark.parametrize("staging", ["kernel", "engine"])
-def test_decode_step_from_host_buffers(step8b, expected, staging):
+@pytest.mark.parametrize("staging,route", [("kernel", "chain"), ("engine", "chain"), ("kernel", "fused")])
+def test_decode_step_from_host_buffers(step8b, expected, staging, route):
     """The end-to-end form the benchmark times: inputs staged in from pinned
     host memory, the step, every output staged out, in one graph with PDL;
     the host copies of the outputs are checked against the oracle."""
     torch = torch_cuda()
     step8b.layout = "seg"
     for p in range(bench.N_INPUT_SETS):
-        bench._e2e_step(step8b, None, p, True, staging)
+        bench._e2e_step(step8b, None, p, staging=staging, route=route)
     torch.cuda.synchronize()
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
-        g = bench.capture(lambda: [bench._e2e_step(step8b, None, p, True, staging)
+        g = bench.capture(lambda: [bench._e2e_step(step8b, None, p, staging=staging, route=route)
                                    for p in range(bench.N_INPUT_SETS)], side)
     torch.cuda.current_stream().wait_stream(side)
     step8b.y_host_flat.fill_(float("nan"))
@@ -113,4 +114,4 @@ def test_decode_step_from_host_buffers(step8b, expected, staging):
     for m in WL.matrices:
         rows, y64, S = expected[m.name]
         got = step8b.y_host[m.name].numpy()[rows]
-        assert_within_tol(got[None, :], y64, S, what=f"{staging}:{m.name}")
+        assert_within_tol(got[None, :], y64, S, what=f"{staging}:{route}:{m.name}")
