@@ -147,8 +147,9 @@ def test_chain_stage_reads_earlier_output():
         Wq[o, b, 2:] = rng.integers(0, 256, size=16, dtype=np.uint8)
     h0["Wq"][0] = Wq.reshape(O0, -1)
     xq0 = oracle.quantize_q8_0(h0["x"], h0["gamma"], EPS)
+    # y0_64 is exact (one block's product, at most 38 significant bits), so
+    # y0_32 is that value rounded once, as the kernel rounds its single product
     y0_32, y0_64, S0 = oracle.matvec(h0["Wq"][0], xq0, K0)
-    assert np.array_equal(y0_32[0].astype(np.float64), y0_64[0]), "stage 0 outputs are not exact single products"
     h1 = make_stage(8, O0, (O1,), True)
     h1["x"] = y0_32.astype(np.float32)
     d0 = to_device_stage(h0)
