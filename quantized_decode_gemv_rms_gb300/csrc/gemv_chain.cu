@@ -139,12 +139,29 @@ struct ActSmem {
     int2* ds;       // [nb] (fp32 bits of the fp16 scale, sum of the codes)
 };
 
-// The warp's take of one unit from the stage's counter (lane 0 asks).
-__device__ __forceinline__ int64_t take_unit(unsigned* ctr, int lane) {
-    unsigned u = 0;
-    if (lane == 0) u = atomicAdd(ctr, 1u);
-    return static_cast<int64_t>(__shfl_sync(0xffffffffu, u, 0));
-}
+// A warp's source of units: batches of kBatch consecutive units taken from
+// the stage's global counter (lane 0 asks; the batch is shared by shuffle).
+// Units come out in increasing order.
+constexpr int kBatch = 1;
+struct UnitSource {
+    unsigned* ctr;
+    unsigned base;
+    int left;
+    __device__ __forceinline__ void reset(unsigned* c) {
+        ctr = c;
+        base = 0;
+        left = 0;
+    }
+    __device__ __forceinline__ int64_t take(int lane) {
+        if (left == 0) {
+            unsigned u = 0;
+            if (lane == 0) u = atomicAdd(ctr, static_cast<unsigned>(kBatch));
+            base = __shfl_sync(0xffffffffu, u, 0);
+            left = kBatch;
+        }
+        return static_cast<int64_t>(base) + (kBatch - left--);
+    }
+};
 
 __device__ __forceinline__ int matrix_of(const Stage& S, int64_t row) {
     int g = 0;
@@ -262,11 +279,11 @@ __device__ void stage_input(const Stage& S, float eps, float* xs, float* gs, con
 // cu, n1: the warp's first two units (already taken); returns nothing, but
 // leaves every unit the warp took consumed.
 template <int U>
-__device__ void stage_products(const Stage& S, const ActSmem& act, unsigned* ctr, int64_t cu, int64_t n1) {
+__device__ void stage_products(const Stage& S, const ActSmem& act, UnitSource& src, int64_t cu, int64_t n1) {
     static_assert(kDepth % U == 0 && U <= 4, "unit rows divide the ring");
     const int lane = threadIdx.x & 31;
     const int nseg = S.nseg;                  // U * nseg >= 4 items per unit: the loader is at most two units ahead
-    int64_t n2 = take_unit(ctr, lane);
+    int64_t n2 = src.take(lane);
 
     // loader position: unit slot (0: cu, 1: n1, 2: n2), segment, row
     int ls = 0, lr = 0, lk = 0;
@@ -365,7 +382,7 @@ __device__ void stage_products(const Stage& S, const ActSmem& act, unsigned* ctr
                     cs = 0;
                     cu = n1;
                     n1 = n2;
-                    n2 = take_unit(ctr, lane);
+                    n2 = src.take(lane);
                     --lk;
                     if (cu >= S.units) break;
                 }
@@ -389,8 +406,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
 
     // first two units of stage 0; their rows start streaming into L2 before
     // the wait for the preceding grid
-    int64_t u0 = take_unit(&ctr[0], lane);
-    int64_t u1 = take_unit(&ctr[0], lane);
+    UnitSource src;
+    src.reset(&ctr[0]);
+    int64_t u0 = src.take(lane);
+    int64_t u1 = src.take(lane);
     prefetch_unit(a.st[0], u0, lane);
     pdl_wait();
 
@@ -398,14 +417,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
         const Stage& S = a.st[g];
         stage_input(S, a.eps, xs, gs, act, wsum);
         if (S.U == 4)
-            stage_products<4>(S, act, &ctr[g], u0, u1);
+            stage_products<4>(S, act, src, u0, u1);
         else if (S.U == 2)
-            stage_products<2>(S, act, &ctr[g], u0, u1);
+            stage_products<2>(S, act, src, u0, u1);
         else
-            stage_products<1>(S, act, &ctr[g], u0, u1);
+            stage_products<1>(S, act, src, u0, u1);
         if (g + 1 < a.nstages) {
-            u0 = take_unit(&ctr[g + 1], lane);
-            u1 = take_unit(&ctr[g + 1], lane);
+            src.reset(&ctr[g + 1]);
+            u0 = src.take(lane);
+            u1 = src.take(lane);
             prefetch_unit(a.st[g + 1], u0, lane);
             __syncthreads();   // every output of this CTA for stage g is written
             if (threadIdx.x == 0) {
