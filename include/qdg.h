@@ -388,11 +388,11 @@ QDG_API int q4_0s_gemv_rmsnorm_group(const void* const* Wr, float* const* y, con
  *   K        multiple of 256, 256 <= K <= 16384.
  *   count    matrices that read this input, 1..4; W[i] segment-layout
  *            weights of O[i] rows (16-byte aligned), y[i] fp32 [O[i]]
- *            (4-byte aligned); sum of O[i] < 2^31.
+ *            (4-byte aligned); sum of O[i] < 2^30.
  * eps      epsilon of the norm (>= 0), added to the mean square inside the root.
- * sync     device array of q4_0s_gemv_chain_sync_bytes() bytes, 4-byte
- *          aligned, zeroed once before its first use; every launch leaves it
- *          zero again.  Launches that may run at the same time need separate
+ * sync     device array of q4_0s_gemv_chain_sync_bytes() bytes (the stage
+ *          barriers' arrival counters), 4-byte aligned, zeroed once before
+ *          its first use; every launch leaves it zero again.  Launches that may run at the same time need separate
  *          arrays.  After a QDG_ETIMEOUT report it must be zeroed again.
  * Errors: QDG_EINVAL, QDG_ESHAPE, QDG_EALIGN as the single calls;
  * QDG_ECUDA if the cooperative launch is refused.  Results are
