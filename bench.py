@@ -358,8 +358,8 @@ class DecodeStep:
                 self.groups[-1].append(m)
             else:
                 self.groups.append([m])
-        # the chain route's sync words (zero; every chain launch leaves them zero)
-        self.sync = torch.zeros(qdg.q4_0s_gemv_chain_sync_bytes(), dtype=torch.uint8, device=device)
+        # the chain route's workspace (zeroed once; every chain launch leaves its counters zero)
+        self.chain_ws = torch.zeros(qdg.q4_0s_gemv_chain_workspace_bytes(), dtype=torch.uint8, device=device)
         torch.cuda.synchronize()
         torch.cuda.empty_cache()      # release the fp32 staging of the weights
 
@@ -416,7 +416,7 @@ class DecodeStep:
         route = route or ("fused" if fused else "split")
         if route == "chain":
             assert self.layout == "seg", "the chain reads the segment layout"
-            qdg.q4_0s_gemv_chain(self.chain_stages(xs, copy), self.wl.eps, self.sync)
+            qdg.q4_0s_gemv_chain(self.chain_stages(xs, copy), self.wl.eps, self.chain_ws)
             return
         fused = route == "fused"
         for grp in self.groups:

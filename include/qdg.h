@@ -390,10 +390,12 @@ QDG_API int q4_0s_gemv_rmsnorm_group(const void* const* Wr, float* const* y, con
  *            weights of O[i] rows (16-byte aligned), y[i] fp32 [O[i]]
  *            (4-byte aligned); sum of O[i] < 2^30.
  * eps      epsilon of the norm (>= 0), added to the mean square inside the root.
- * sync     device array of q4_0s_gemv_chain_sync_bytes() bytes (the stage
- *          barriers' arrival counters), 4-byte aligned, zeroed once before
- *          its first use; every launch leaves it zero again.  Launches that may run at the same time need separate
- *          arrays.  After a QDG_ETIMEOUT report it must be zeroed again.
+ * workspace  device memory of q4_0s_gemv_chain_workspace_bytes() bytes,
+ *          16-byte aligned, zeroed once before its first use: the stage
+ *          barriers' arrival counters (64 bytes, left zero by every launch)
+ *          and the image of a stage's quantized input.  Launches that may run
+ *          at the same time need separate workspaces.  After a QDG_ETIMEOUT
+ *          report it must be zeroed again.
  * Errors: QDG_EINVAL, QDG_ESHAPE, QDG_EALIGN as the single calls;
  * QDG_ECUDA if the cooperative launch is refused.  Results are
  * deterministic: every output row is summed in a fixed order.
@@ -409,8 +411,8 @@ typedef struct {
     int64_t O[4];
 } qdg_chain_stage;
 
-QDG_API int64_t q4_0s_gemv_chain_sync_bytes(void);
-QDG_API int q4_0s_gemv_chain(const qdg_chain_stage* stages, int nstages, float eps, void* sync,
+QDG_API int64_t q4_0s_gemv_chain_workspace_bytes(void);
+QDG_API int q4_0s_gemv_chain(const qdg_chain_stage* stages, int nstages, float eps, void* workspace,
                              qdg_stream_t stream);
 
 /*

@@ -61,7 +61,9 @@ constexpr int kDepth = 8;                   // row-segments in flight per warp
 constexpr int kSegStride = 1152;            // segment layout: 64 x 16 nibble bytes + 128 bytes of scale words
 constexpr int kPrefetchCap = 9216;          // bytes of its first unit a warp prefetches into L2 at a stage change
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
-constexpr size_t kSmemBytes = static_cast<size_t>(2) * kMaxK * 4 + static_cast<size_t>(kMaxBlocks) * (16 + 16 + 8);
+constexpr size_t kImageBytes = static_cast<size_t>(kMaxBlocks) * (16 + 16 + 8);   // a stage input's block image
+constexpr size_t kSmemBytes = static_cast<size_t>(kMaxK) * 4 + kImageBytes;
+constexpr int kCounters = 16;   // [0, 8): stage-done barriers, [8, 16): input-ready barriers
 
 struct Stage {
     const float* x;
@@ -81,7 +83,7 @@ struct ChainArgs {
     Stage st[kMaxStages];
     int nstages;
     float eps;
-    unsigned* sync;              // [kMaxStages] arrival counters (the rest of the sync words is spare)
+    unsigned* sync;              // kCounters arrival counters, then the block image (kImageBytes)
 };
 
 __device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
@@ -195,34 +197,51 @@ __device__ __forceinline__ void wait_arrivals(const unsigned* arrive, unsigned c
     if (ld_acquire(arrive) >= count) return;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 0; i < kSpinLimit; ++i) {
-        __nanosleep(64);
+        __nanosleep(20);
         if (ld_acquire(arrive) >= count) return;
         if (global_ns() - t0 > kWaitNs) break;
     }
     atomicOr(&g_flags_chain, FLAG_TIMEOUT);
 }
 
-// Stage input -> shared memory, statistic, Q8_0 blocks into the planes (and
-// out to global memory from CTA 0 when asked).  Same arithmetic and order as
-// qnorm_q8_kernel: chains j = i mod 256 summed with fma in ascending i, xor
-// butterflies (16, 8, 4, 2, 1), ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)),
-// s = 1/sqrt(sum/K + eps); v = (x*s)*gamma; d = max|v|/127; q = round(v/d)
-// (halves away from zero), clamped to +-127; stored scale fp16(d).
-__device__ void stage_input(const Stage& S, float eps, float* xs, float* gs, const ActSmem& act, float* wsum) {
+// Bounded grid-wide barrier on an arrival counter (release/acquire).
+__device__ __forceinline__ void grid_barrier(unsigned* ctr) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ctr, 1u);
+        wait_arrivals(ctr, gridDim.x);
+        __threadfence();
+    }
+    __syncthreads();
+}
+
+// Stage input: the statistic, this CTA's share of the Q8_0 blocks, a grid
+// barrier, then every block's image in shared memory.  Same arithmetic and
+// order as qnorm_q8_kernel: chains j = i mod 256 summed with fma in
+// ascending i, xor butterflies (16, 8, 4, 2, 1),
+// ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)), s = 1/sqrt(sum/K + eps);
+// v = (x*s)*gamma; d = max|v|/127; q = round(v/d) (halves away from zero),
+// clamped to +-127; stored scale fp16(d).
+//   Every CTA forms the statistic (it needs all of x, 16 KB at K = 4096);
+//   block b is quantized by warp b / G of CTA b mod G (G CTAs) and written
+//   to the workspace image (and to xq_out when asked); after the barrier
+//   each CTA copies the whole image into shared memory.  (Quantizing every
+//   block in every CTA measured 2.5 us per 4096 elements on GB300: about
+//   40 cycles a block on the SM, times K/32 blocks.)
+__device__ void stage_input(const Stage& S, float eps, float* xs, const ActSmem& act, float* wsum, uint8_t* image,
+                            unsigned* ready) {
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
     const int K = S.K, nb = S.nb;
     const float* x = S.x;
     const float* gamma = S.gamma;
     uint8_t* xq_out = S.xq_out;
-    for (int i = tid * 4; i < K; i += kThreads * 4) {
-        cp_async16(xs + i, x + i);
-        if (gamma != nullptr) cp_async16(gs + i, gamma + i);
-    }
-    cp_async_wait_all();
-    __syncthreads();
     float s = 1.0f;
     if (gamma != nullptr) {
+        for (int i = tid * 4; i < K; i += kThreads * 4) cp_async16(xs + i, x + i);
+        cp_async_wait_all();
+        __syncthreads();
         if (tid < 256) {
             float acc = 0.0f;
             for (int i = tid; i < K; i += 256) acc = __fmaf_rn(xs[i], xs[i], acc);
@@ -235,54 +254,46 @@ __device__ void stage_input(const Stage& S, float eps, float* xs, float* gs, con
         const float mean = __fdiv_rn(ss, static_cast<float>(K));
         s = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
     }
-    const bool out = xq_out != nullptr && blockIdx.x == 0;
-    uint8_t* c0 = reinterpret_cast<uint8_t*>(act.p0);
-    uint8_t* c1 = reinterpret_cast<uint8_t*>(act.p1);
-    for (int b0 = warp; b0 < nb; b0 += 4 * kWarps) {
-        float v[4], m[4];
+    const int b = static_cast<int>(blockIdx.x) + warp * static_cast<int>(gridDim.x);
+    if (b < nb) {
+        float v;
+        if (gamma != nullptr)
+            v = __fmul_rn(__fmul_rn(xs[(b << 5) + lane], s), __ldg(gamma + (b << 5) + lane));
+        else
+            v = __ldcg(x + (b << 5) + lane);   // x may be an earlier stage's output: read it at L2
+        float m = fabsf(v);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int b = b0 + u * kWarps;
-            v[u] = 0.0f;
-            if (b < nb) {
-                v[u] = xs[(b << 5) + lane];
-                if (gamma != nullptr) v[u] = __fmul_rn(__fmul_rn(v[u], s), gs[(b << 5) + lane]);
-            }
-            m[u] = fabsf(v[u]);
+        for (int h = 16; h >= 1; h >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, h));
+        const float d = __fdiv_rn(m, 127.0f);
+        int q = 0;
+        if (d != 0.0f) {
+            float r = roundf(__fdiv_rn(v, d));
+            r = fminf(fmaxf(r, -127.0f), 127.0f);
+            q = static_cast<int>(r);
         }
-#pragma unroll
-        for (int h = 16; h >= 1; h >>= 1)
-#pragma unroll
-            for (int u = 0; u < 4; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(0xffffffffu, m[u], h));
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int b = b0 + u * kWarps;
-            if (b >= nb) break;
-            const float d = __fdiv_rn(m[u], 127.0f);
-            int q = 0;
-            if (d != 0.0f) {
-                float r = roundf(__fdiv_rn(v[u], d));
-                r = fminf(fmaxf(r, -127.0f), 127.0f);
-                q = static_cast<int>(r);
-            }
-            const int qsum = __reduce_add_sync(0xffffffffu, q);
-            const __half dh = __float2half_rn(d);
-            const uint8_t code = static_cast<uint8_t>(static_cast<int8_t>(q));
-            if (lane < 16)
-                c0[16 * b + lane] = code;
-            else
-                c1[16 * b + lane - 16] = code;
-            if (lane == 0) {
-                act.ds[b] = make_int2(__float_as_int(__half2float(dh)), qsum);
-                if (__hisinf(dh)) atomicOr(&g_flags_chain, FLAG_OVERFLOW);
-            }
-            if (out) {
-                uint8_t* blk = xq_out + static_cast<int64_t>(b) * 34;
-                if (lane == 0) *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
-                blk[2 + lane] = code;
-            }
+        const int qsum = __reduce_add_sync(0xffffffffu, q);
+        const __half dh = __float2half_rn(d);
+        const uint8_t code = static_cast<uint8_t>(static_cast<int8_t>(q));
+        image[(lane < 16 ? 0 : 16 * kMaxBlocks - 16) + 16 * b + lane] = code;
+        if (lane == 0) {
+            reinterpret_cast<int2*>(image + 32 * kMaxBlocks)[b] = make_int2(__float_as_int(__half2float(dh)), qsum);
+            if (__hisinf(dh)) atomicOr(&g_flags_chain, FLAG_OVERFLOW);
+        }
+        if (xq_out != nullptr) {
+            uint8_t* blk = xq_out + static_cast<int64_t>(b) * 34;
+            if (lane == 0) *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
+            blk[2 + lane] = code;
         }
     }
+    grid_barrier(ready);
+    // the image: planes of nb x 16 bytes at 0 and 16 kMaxBlocks, (scale, sum) pairs at 32 kMaxBlocks
+    uint8_t* dst = reinterpret_cast<uint8_t*>(act.p0);
+    for (int i = tid * 16; i < 16 * nb; i += kThreads * 16) {
+        cp_async16(dst + i, image + i);
+        cp_async16(dst + 16 * kMaxBlocks + i, image + 16 * kMaxBlocks + i);
+    }
+    for (int i = tid * 16; i < 8 * nb; i += kThreads * 16) cp_async16(dst + 32 * kMaxBlocks + i, image + 32 * kMaxBlocks + i);
+    cp_async_wait_all();
     __syncthreads();
 }
 
@@ -413,13 +424,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
     __shared__ __align__(16) Stage cur;
     static_assert(sizeof(Stage) % 4 == 0 && sizeof(Stage) / 4 <= kThreads, "stage copy by one word a thread");
     float* xs = reinterpret_cast<float*>(smem);
-    float* gs = xs + kMaxK;
     ActSmem act;
-    act.p0 = reinterpret_cast<uint4*>(gs + kMaxK);
+    act.p0 = reinterpret_cast<uint4*>(xs + kMaxK);
     act.p1 = act.p0 + kMaxBlocks;
     act.ds = reinterpret_cast<int2*>(act.p1 + kMaxBlocks);
     const int lane = threadIdx.x & 31;
     unsigned* arrive = a.sync;
+    uint8_t* image = reinterpret_cast<uint8_t*>(a.sync + kCounters);
 
     // first two units of stage 0; their rows start streaming into L2 before
     // the wait for the preceding grid
@@ -437,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
             reinterpret_cast<uint32_t*>(&cur)[threadIdx.x] = reinterpret_cast<const uint32_t*>(&a.st[g])[threadIdx.x];
         __syncthreads();
         const Stage& S = cur;
-        stage_input(S, a.eps, xs, gs, act, wsum);
+        stage_input(S, a.eps, xs, act, wsum, image, &arrive[kMaxStages + g]);
         // the next stage's input heads for L2 while this stage streams
         if (g + 1 < a.nstages && blockIdx.x == 0 && threadIdx.x == 0) prefetch_input(a.st[g + 1]);
         if (S.U == 4)
@@ -456,14 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
             prefetch_unit(a.st[g + 1], u0, lane);
             prefetch_unit(a.st[g + 1], u1, lane);
             prefetch_unit(a.st[g + 1], u2, lane);
-            __syncthreads();   // every output of this CTA for stage g is written
-            if (threadIdx.x == 0) {
-                __threadfence();
-                atomicAdd(&arrive[g], 1u);
-                wait_arrivals(&arrive[g], gridDim.x);
-                __threadfence();
-            }
-            __syncthreads();
+            grid_barrier(&arrive[g]);   // every output of stage g is written
         }
     }
     __syncthreads();
@@ -472,7 +476,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
         const unsigned prev = atomicAdd(&arrive[a.nstages - 1], 1u);
         if (prev == gridDim.x - 1) {
             // every CTA is past every use of the counters: back to zero
-            for (int g = 0; g < a.nstages; ++g) atomicExch(&arrive[g], 0u);
+            for (int c = 0; c < kCounters; ++c) atomicExch(&arrive[c], 0u);
             __threadfence();
         }
     }
@@ -495,7 +499,7 @@ int chain_launch(const qdg_chain_stage* stages, int nstages, float eps, void* sy
     if (!stages || !sync) return QDG_EINVAL;
     if (nstages < 1 || nstages > kMaxStages) return QDG_EINVAL;
     if (!(eps >= 0.0f) || std::isinf(eps)) return QDG_EINVAL;
-    if (!aligned(sync, 4)) return QDG_EALIGN;
+    if (!aligned(sync, 16)) return QDG_EALIGN;
     ChainArgs a{};
     a.nstages = nstages;
     a.eps = eps;
@@ -569,9 +573,11 @@ int chain_launch(const qdg_chain_stage* stages, int nstages, float eps, void* sy
 
 using namespace qdg;
 
-extern "C" int64_t q4_0s_gemv_chain_sync_bytes(void) { return static_cast<int64_t>(2 * kMaxStages * sizeof(unsigned)); }
+extern "C" int64_t q4_0s_gemv_chain_workspace_bytes(void) {
+    return static_cast<int64_t>(kCounters * sizeof(unsigned) + kImageBytes);
+}
 
-extern "C" int q4_0s_gemv_chain(const qdg_chain_stage* stages, int nstages, float eps, void* sync,
+extern "C" int q4_0s_gemv_chain(const qdg_chain_stage* stages, int nstages, float eps, void* workspace,
                                 qdg_stream_t stream) {
-    return chain_launch(stages, nstages, eps, sync, reinterpret_cast<cudaStream_t>(stream));
+    return chain_launch(stages, nstages, eps, workspace, reinterpret_cast<cudaStream_t>(stream));
 }

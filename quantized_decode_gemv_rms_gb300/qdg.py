@@ -75,7 +75,7 @@ def lib() -> ctypes.CDLL:
             sig["q4_0s_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
             sig["q4_0s_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
             sig["qdg_stage_copy"] = ([p, p, i64, p], i32)
-            sig["q4_0s_gemv_chain_sync_bytes"] = ([], i64)
+            sig["q4_0s_gemv_chain_workspace_bytes"] = ([], i64)
             sig["q4_0s_gemv_chain"] = ([p, i32, f32, p, p], i32)
             for name, (args, res) in sig.items():
                 fn = getattr(L, name)
@@ -254,8 +254,8 @@ class ChainStage(ctypes.Structure):
                 ("W", ctypes.c_void_p * 4), ("y", ctypes.c_void_p * 4), ("O", ctypes.c_int64 * 4)]
 
 
-def q4_0s_gemv_chain_sync_bytes() -> int:
-    return int(lib().q4_0s_gemv_chain_sync_bytes())
+def q4_0s_gemv_chain_workspace_bytes() -> int:
+    return int(lib().q4_0s_gemv_chain_workspace_bytes())
 
 
 def chain_stages(stages):
@@ -276,11 +276,11 @@ def chain_stages(stages):
     return arr
 
 
-def q4_0s_gemv_chain(stages, eps: float, sync, stream=None) -> None:
+def q4_0s_gemv_chain(stages, eps: float, workspace, stream=None) -> None:
     """A decode step's stages (norm/quantize + grouped segment-layout GEMV each)
     in one launch; ``stages`` as for chain_stages(), or its result."""
     arr = stages if isinstance(stages, ctypes.Array) else chain_stages(stages)
-    _check(lib().q4_0s_gemv_chain(arr, len(arr), float(eps), _ptr(sync), _stream(stream)), "q4_0s_gemv_chain")
+    _check(lib().q4_0s_gemv_chain(arr, len(arr), float(eps), _ptr(workspace), _stream(stream)), "q4_0s_gemv_chain")
 
 
 def q4_0s_q8_0_gemm_small_n(Wr, xq, y, ldy: int, O: int, K: int, N: int, stream=None) -> None:

@@ -27,7 +27,7 @@ def test_header_declares_entry_points():
     for must in ("qnorm_quantize_q8_0", "qnorm_add_quantize_q8_0", "q4_0_q8_0_gemv", "q4_0_q8_0_gemm_small_n", "q4_0_q8_0_gemm",
                  "q4_0_q8_0_gemm_workspace_bytes", "q4_0_q8_0_gemm_workspace_size", "qdg_stage_copy", "quantize_q4_0", "q4_0_repack_seg", "q4_0s_q8_0_gemv",
                  "q4_0s_q8_0_gemv_group", "q4_0s_gemv_rmsnorm_group", "q4_0s_q8_0_gemm_small_n", "q4_0_seg_row_bytes", "q8_0_q8_0_gemv", "q8_0_q8_0_gemv_group",
-                 "q4_0s_gemv_chain", "q4_0s_gemv_chain_sync_bytes", "qdg_device_status", "qdg_status_string"):
+                 "q4_0s_gemv_chain", "q4_0s_gemv_chain_workspace_bytes", "qdg_device_status", "qdg_status_string"):
         assert must in names
 
 
@@ -275,7 +275,7 @@ def test_binding_names_match_header():
 
 def test_chain_host_validation(L):
     from quantized_decode_gemv_rms_gb300 import qdg
-    assert L.q4_0s_gemv_chain_sync_bytes() == 64
+    assert L.q4_0s_gemv_chain_workspace_bytes() == 64 + 512 * 40
 
     def stage(K=4096, count=1, x=A16, gamma=None, W=A16, y=A16, O=8):
         st = (qdg.ChainStage * 1)()
@@ -288,9 +288,9 @@ def test_chain_host_validation(L):
     two = (qdg.ChainStage * 9)()
     assert f(stage(), 0, 1e-6, A16, None) == -1                   # no stage
     assert f(two, 9, 1e-6, A16, None) == -1                       # more than eight stages
-    assert f(stage(), 1, 1e-6, None, None) == -1                  # no sync words
+    assert f(stage(), 1, 1e-6, None, None) == -1                  # no workspace
     assert f(stage(), 1, -1.0, A16, None) == -1                   # eps < 0
-    assert f(stage(), 1, 1e-6, A2 + 1, None) == -2                # sync words misaligned
+    assert f(stage(), 1, 1e-6, A2, None) == -2                    # workspace not 16-byte aligned
     assert f(stage(count=0), 1, 1e-6, A16, None) == -1            # no matrix
     assert f(stage(count=5), 1, 1e-6, A16, None) == -1            # more than four matrices
     assert f(stage(x=None), 1, 1e-6, A16, None) == -1             # null x

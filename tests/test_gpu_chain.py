@@ -5,7 +5,7 @@ within 1e-5 * sum_b |d_w d_x isum_b| of the oracle's fp64 product.
 Cases: ragged and whole last segments (K = 256 .. 16384, units of 4, 2 and 1
 rows), row counts that leave a partial last unit, groups of up to four
 matrices, the most stages a launch takes, repeated launches and graph
-replays on one set of sync words (left zero by every launch), and a stage
+replays on one workspace (its counters left zero by every launch), and a stage
 whose input is an earlier stage's output."""
 import numpy as np
 import pytest
@@ -43,9 +43,13 @@ def to_device_stage(st):
             "xq_out": torch.zeros(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device="cuda")}
 
 
-def new_sync():
+def new_workspace():
     torch = torch_cuda()
-    return torch.zeros(qdg.q4_0s_gemv_chain_sync_bytes(), dtype=torch.uint8, device="cuda")
+    return torch.zeros(qdg.q4_0s_gemv_chain_workspace_bytes(), dtype=torch.uint8, device="cuda")
+
+
+def counters_zero(ws):
+    return int(ws[:64].sum()) == 0
 
 
 def check(dev_stages, host_stages, what=""):
@@ -76,27 +80,27 @@ def test_chain_single_stage(K, Os, norm):
     torch = torch_cuda()
     h = make_stage(K + sum(Os), K, Os, norm, outliers=0.01)
     d = to_device_stage(h)
-    sync = new_sync()
-    qdg.q4_0s_gemv_chain([d], EPS, sync)
+    ws = new_workspace()
+    qdg.q4_0s_gemv_chain([d], EPS, ws)
     torch.cuda.synchronize()
     assert qdg.qdg_device_status() == qdg.QDG_OK
     check([d], [h], f"K={K}")
-    assert int(sync.sum()) == 0, "sync words not returned to zero"
+    assert counters_zero(ws), "barrier counters not returned to zero"
 
 
 def test_chain_eight_stages_and_repeats():
     """The most stages one launch takes, three launches in a row and a graph
-    of two launches replayed twice on one set of sync words; every launch
-    gives the same bits."""
+    of two launches replayed twice on one workspace; every launch gives the
+    same bits."""
     torch = torch_cuda()
     shapes = [(4096, (4096, 1024, 1024), True), (4096, (4096,), False), (4096, (2000, 2000), True),
               (14336, (4096,), False), (2048, (300,), True), (256, (64, 64, 64, 64), True),
               (8192, (500,), True), (4096, (6000,), True)]
     hs = [make_stage(100 + g, K, Os, norm) for g, (K, Os, norm) in enumerate(shapes)]
     ds = [to_device_stage(h) for h in hs]
-    sync = new_sync()
+    ws = new_workspace()
     arr = qdg.chain_stages(ds)
-    qdg.q4_0s_gemv_chain(arr, EPS, sync)
+    qdg.q4_0s_gemv_chain(arr, EPS, ws)
     torch.cuda.synchronize()
     assert qdg.qdg_device_status() == qdg.QDG_OK
     check(ds, hs, "8 stages")
@@ -105,7 +109,7 @@ def test_chain_eight_stages_and_repeats():
         for d in ds:
             for y in d["ys"]:
                 y.fill_(float("nan"))
-        qdg.q4_0s_gemv_chain(arr, EPS, sync)
+        qdg.q4_0s_gemv_chain(arr, EPS, ws)
         torch.cuda.synchronize()
         again = [to_host(y) for d in ds for y in d["ys"]]
         assert all(np.array_equal(a.view(np.uint32), b.view(np.uint32)) for a, b in zip(first, again))
@@ -114,8 +118,8 @@ def test_chain_eight_stages_and_repeats():
     with torch.cuda.stream(side):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr, stream=side):
-            qdg.q4_0s_gemv_chain(arr, EPS, sync)
-            qdg.q4_0s_gemv_chain(arr, EPS, sync)
+            qdg.q4_0s_gemv_chain(arr, EPS, ws)
+            qdg.q4_0s_gemv_chain(arr, EPS, ws)
     torch.cuda.current_stream().wait_stream(side)
     for _ in range(2):
         for d in ds:
@@ -126,7 +130,7 @@ def test_chain_eight_stages_and_repeats():
         assert qdg.qdg_device_status() == qdg.QDG_OK
         again = [to_host(y) for d in ds for y in d["ys"]]
         assert all(np.array_equal(a.view(np.uint32), b.view(np.uint32)) for a, b in zip(first, again))
-    assert int(sync.sum()) == 0
+    assert counters_zero(ws)
 
 
 def test_chain_stage_reads_earlier_output():
@@ -155,8 +159,8 @@ def test_chain_stage_reads_earlier_output():
     d0 = to_device_stage(h0)
     d1 = to_device_stage(h1)
     d1["x"] = d0["ys"][0]                                 # the chain reads stage 0's output
-    sync = new_sync()
-    qdg.q4_0s_gemv_chain([d0, d1], EPS, sync)
+    ws = new_workspace()
+    qdg.q4_0s_gemv_chain([d0, d1], EPS, ws)
     torch.cuda.synchronize()
     assert qdg.qdg_device_status() == qdg.QDG_OK
     assert np.array_equal(to_host(d0["ys"][0]).view(np.uint32), y0_32[0].view(np.uint32))
