@@ -159,14 +159,16 @@ struct ActSmem {
     int2* ds;       // [nb] (fp32 bits of the fp16 scale, sum of the codes)
 };
 
-// A warp's units of a stage: w, w + W, w + 2W, ... with w the warp's index
-// in the grid and W the number of warps, so that consecutive units go to the
-// warps of one CTA, then of the next.  (Measured on GB300 against warps
-// taking units one by one from a global counter: 112 against 130 us for the
-// 8B-shaped step; the counter's atomics serialise.)
+// A warp's units of a stage: c + G (w + 16 k), k = 0, 1, ... for warp w of
+// CTA c (G CTAs), so that consecutive units go to consecutive CTAs and even
+// a stage of fewer units than warps keeps every SM streaming.  (Measured on
+// GB300 against warps taking units one by one from a global counter: 112
+// against 130 us for the 8B-shaped step; the counter's atomics serialise.)
 struct UnitSource {
     int next;
-    __device__ __forceinline__ void reset() { next = static_cast<int>(blockIdx.x) * kWarps + (threadIdx.x >> 5); }
+    __device__ __forceinline__ void reset() {
+        next = static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) * (threadIdx.x >> 5);
+    }
     __device__ __forceinline__ int take() {
         const int u = next;
         next += static_cast<int>(gridDim.x) * kWarps;
@@ -204,14 +206,15 @@ __device__ __forceinline__ void wait_arrivals(const unsigned* arrive, unsigned c
     atomicOr(&g_flags_chain, FLAG_TIMEOUT);
 }
 
-// Bounded grid-wide barrier on an arrival counter (release/acquire).
+// Bounded grid-wide barrier on an arrival counter: the CTA's writes are
+// released by its arrival (after the CTA barrier, so every thread's), and
+// the acquiring load of the full count orders the reads that follow (the
+// CTA barrier after it passes the order on to every thread).
 __device__ __forceinline__ void grid_barrier(unsigned* ctr) {
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(ctr, 1u);
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
         wait_arrivals(ctr, gridDim.x);
-        __threadfence();
     }
     __syncthreads();
 }
