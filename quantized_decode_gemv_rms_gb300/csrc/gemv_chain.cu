@@ -300,45 +300,74 @@ __device__ void stage_input(const Stage& S, float eps, float* xs, const ActSmem&
     __syncthreads();
 }
 
-// One stage's products, one warp.  Items are the unit's row-segments in the
-// order (segment s, row r), r fastest; the ring holds kDepth of them.
-// cu, n1: the warp's first two units (already taken); returns nothing, but
-// leaves every unit the warp took consumed.
+// A warp's place in a stage's items.  Items are a unit's row-segments in the
+// order (segment s, row r), r fastest; U * nseg >= 4 items a unit, so the
+// loader, kDepth items ahead of the consumer, is at most two units ahead.
+struct WarpState {
+    int cu, n1, n2;     // the unit being consumed and the next two
+    int lk, ls, lr;     // loader: unit slot (0: cu, 1: n1, 2: n2), segment, row
+};
+
+// Load the loader's item into e and advance the loader.
 template <int U>
-__device__ void stage_products(const Stage& S, const ActSmem& act, UnitSource& src, int cu, int n1, int n2) {
+__device__ __forceinline__ void load_item(const Stage& S, WarpState& w, Entry& e, int lane) {
+    const int unit = w.lk == 0 ? w.cu : (w.lk == 1 ? w.n1 : w.n2);
+    const int64_t row = static_cast<int64_t>(unit) * U + w.lr;
+    e.a = make_uint4(0, 0, 0, 0);
+    e.b = e.a;
+    e.sc = 0;
+    if (unit < S.units && row < S.rows) {
+        const int g = matrix_of(S, row);
+        const int r = (w.ls == S.nseg - 1) ? S.rlast : 64;
+        const uint8_t* base = S.W[g] + (row - S.start[g]) * S.rowbytes + w.ls * kSegStride;
+        if (lane < r) e.a = ldg_stream16(base + 16 * lane);
+        if (lane + 32 < r) e.b = ldg_stream16(base + 16 * lane + 512);
+        e.sc = ldg_stream4(base + 16 * r + 4 * lane);
+    }
+    if (++w.lr == U) {
+        w.lr = 0;
+        if (++w.ls == S.nseg) {
+            w.ls = 0;
+            ++w.lk;
+        }
+    }
+}
+
+// Take the warp's first three units of a stage and fill the ring with its
+// first kDepth items (weights only: this may run before the stage's input
+// is ready); the rows of the later units head for L2.
+template <int U>
+__device__ __forceinline__ void fill_ring(const Stage& S, WarpState& w, Entry (&ring)[kDepth], UnitSource& src,
+                                          int lane) {
+    w.cu = src.take();
+    w.n1 = src.take();
+    w.n2 = src.take();
+    w.lk = w.ls = w.lr = 0;
+#pragma unroll
+    for (int k = 0; k < kDepth; ++k) load_item<U>(S, w, ring[k], lane);
+    prefetch_unit(S, w.n1, lane);
+    prefetch_unit(S, w.n2, lane);
+}
+
+__device__ __forceinline__ void fill_ring_any(const Stage& S, WarpState& w, Entry (&ring)[kDepth], UnitSource& src,
+                                              int lane) {
+    if (S.U == 4)
+        fill_ring<4>(S, w, ring, src, lane);
+    else if (S.U == 2)
+        fill_ring<2>(S, w, ring, src, lane);
+    else
+        fill_ring<1>(S, w, ring, src, lane);
+}
+
+// One stage's products, one warp, from a filled ring: consume every unit the
+// warp takes; each item is dotted and its ring entry refilled with the item
+// kDepth ahead.
+template <int U>
+__device__ __forceinline__ void stage_products(const Stage& S, const ActSmem& act, UnitSource& src, WarpState& w,
+                                               Entry (&ring)[kDepth]) {
     static_assert(kDepth % U == 0 && U <= 4, "unit rows divide the ring");
     const int lane = threadIdx.x & 31;
-    const int nseg = S.nseg;                  // U * nseg >= 4 items per unit: the loader is at most two units ahead
-
-    // loader position: unit slot (0: cu, 1: n1, 2: n2), segment, row
-    int ls = 0, lr = 0, lk = 0;
-    auto load_item = [&](Entry& e) {
-        const int unit = lk == 0 ? cu : (lk == 1 ? n1 : n2);
-        const int64_t row = static_cast<int64_t>(unit) * U + lr;
-        e.a = make_uint4(0, 0, 0, 0);
-        e.b = e.a;
-        e.sc = 0;
-        if (unit < S.units && row < S.rows) {
-            const int g = matrix_of(S, row);
-            const int r = (ls == nseg - 1) ? S.rlast : 64;
-            const uint8_t* base = S.W[g] + (row - S.start[g]) * S.rowbytes + ls * kSegStride;
-            if (lane < r) e.a = ldg_stream16(base + 16 * lane);
-            if (lane + 32 < r) e.b = ldg_stream16(base + 16 * lane + 512);
-            e.sc = ldg_stream4(base + 16 * r + 4 * lane);
-        }
-        if (++lr == U) {
-            lr = 0;
-            if (++ls == nseg) {
-                ls = 0;
-                ++lk;
-            }
-        }
-    };
-
-    Entry ring[kDepth];
-#pragma unroll
-    for (int k = 0; k < kDepth; ++k) load_item(ring[k]);
-
+    const int nseg = S.nseg;
     // consumer: segment of the current item; activations of that segment
     int cs = 0;
     uint4 xa0, xa1, xb0, xb1;
@@ -348,7 +377,7 @@ __device__ void stage_products(const Stage& S, const ActSmem& act, UnitSource& s
 #pragma unroll
     for (int r = 0; r < U; ++r) acc[r] = 0.0f;
 
-    while (cu < S.units) {
+    while (w.cu < S.units) {
 #pragma unroll
         for (int k = 0; k < kDepth; ++k) {
             const int r = k % U;
@@ -382,7 +411,7 @@ __device__ void stage_products(const Stage& S, const ActSmem& act, UnitSource& s
             float p = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
             p = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), p);
             acc[r] = __fadd_rn(acc[r], p);
-            load_item(e);   // refill with the item kDepth ahead
+            load_item<U>(S, w, e, lane);   // refill with the item kDepth ahead
             if (r == U - 1) {
                 if (++cs == nseg) {
                     // the unit is complete: its U rows in one transposed butterfly
@@ -397,7 +426,7 @@ __device__ void stage_products(const Stage& S, const ActSmem& act, UnitSource& s
 #pragma unroll
                     for (int h = 4; h >= 1; h >>= 1) mm = __fadd_rn(mm, __shfl_xor_sync(0xffffffffu, mm, h));
                     const int q = lane >> 3;
-                    const int64_t row = static_cast<int64_t>(cu) * U + q;
+                    const int64_t row = static_cast<int64_t>(w.cu) * U + q;
                     if ((lane & 7) == 0 && q < U && row < S.rows) {
                         const int g = matrix_of(S, row);
                         S.y[g][row - S.start[g]] = mm;
@@ -405,11 +434,11 @@ __device__ void stage_products(const Stage& S, const ActSmem& act, UnitSource& s
 #pragma unroll
                     for (int rr = 0; rr < U; ++rr) acc[rr] = 0.0f;
                     cs = 0;
-                    cu = n1;
-                    n1 = n2;
-                    n2 = src.take();
-                    --lk;
-                    if (cu >= S.units) break;
+                    w.cu = w.n1;
+                    w.n1 = w.n2;
+                    w.n2 = src.take();
+                    --w.lk;
+                    if (w.cu >= S.units) break;
                 }
             }
         }
@@ -435,41 +464,40 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_chain_kernel(const __grid_co
     unsigned* arrive = a.sync;
     uint8_t* image = reinterpret_cast<uint8_t*>(a.sync + kCounters);
 
-    // first two units of stage 0; their rows start streaming into L2 before
-    // the wait for the preceding grid
+    // Stage 0's first items are loaded (and its next units prefetched into
+    // L2) before the wait for the preceding grid: weights never depend on it.
+    if (threadIdx.x < sizeof(Stage) / 4)
+        reinterpret_cast<uint32_t*>(&cur)[threadIdx.x] = reinterpret_cast<const uint32_t*>(&a.st[0])[threadIdx.x];
+    __syncthreads();
     UnitSource src;
     src.reset();
-    int u0 = src.take(), u1 = src.take(), u2 = src.take();
-    prefetch_unit(a.st[0], u0, lane);
-    prefetch_unit(a.st[0], u1, lane);
-    prefetch_unit(a.st[0], u2, lane);
-    if (blockIdx.x == 0 && threadIdx.x == 0) prefetch_input(a.st[0]);
+    WarpState w;
+    Entry ring[kDepth];
+    fill_ring_any(cur, w, ring, src, lane);
+    if (blockIdx.x == 0 && threadIdx.x == 0) prefetch_input(cur);
     pdl_wait();
 
     for (int g = 0; g < a.nstages; ++g) {
-        if (threadIdx.x < sizeof(Stage) / 4)
-            reinterpret_cast<uint32_t*>(&cur)[threadIdx.x] = reinterpret_cast<const uint32_t*>(&a.st[g])[threadIdx.x];
-        __syncthreads();
         const Stage& S = cur;
         stage_input(S, a.eps, xs, act, wsum, image, &arrive[kMaxStages + g]);
         // the next stage's input heads for L2 while this stage streams
         if (g + 1 < a.nstages && blockIdx.x == 0 && threadIdx.x == 0) prefetch_input(a.st[g + 1]);
         if (S.U == 4)
-            stage_products<4>(S, act, src, u0, u1, u2);
+            stage_products<4>(S, act, src, w, ring);
         else if (S.U == 2)
-            stage_products<2>(S, act, src, u0, u1, u2);
+            stage_products<2>(S, act, src, w, ring);
         else
-            stage_products<1>(S, act, src, u0, u1, u2);
+            stage_products<1>(S, act, src, w, ring);
         if (g + 1 < a.nstages) {
-            // the warp's first units of the next stage start streaming into
-            // L2 while the CTAs meet at the barrier
+            // the next stage's first items are in flight while the CTAs meet
+            // at the barrier and quantize its input
+            __syncthreads();
+            if (threadIdx.x < sizeof(Stage) / 4)
+                reinterpret_cast<uint32_t*>(&cur)[threadIdx.x] =
+                    reinterpret_cast<const uint32_t*>(&a.st[g + 1])[threadIdx.x];
+            __syncthreads();
             src.reset();
-            u0 = src.take();
-            u1 = src.take();
-            u2 = src.take();
-            prefetch_unit(a.st[g + 1], u0, lane);
-            prefetch_unit(a.st[g + 1], u1, lane);
-            prefetch_unit(a.st[g + 1], u2, lane);
+            fill_ring_any(cur, w, ring, src, lane);
             grid_barrier(&arrive[g]);   // every output of stage g is written
         }
     }
