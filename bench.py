@@ -946,9 +946,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=workloads.LLAMA_8B.name, choices=sorted(workloads.ALL))
     ap.add_argument("--no-graph", dest="graph", action="store_false")
-    ap.add_argument("--route", choices=["chain", "split", "fused"], default="chain",
-                    help="the timed main line: chain = one launch per step (default); split = quantize kernel + "
-                         "grouped GEMV per group; fused = one norm+quantize+GEMV launch per group")
+    ap.add_argument("--route", choices=["chain", "split", "fused"], default="split",
+                    help="the timed main line: split = quantize kernel + grouped GEMV per group (default); "
+                         "fused = one norm+quantize+GEMV launch per group; chain = one persistent launch per step")
     ap.add_argument("--layout", choices=["seg", "plain"], default="seg",
                     help="weight layout the split route's GEMV reads: seg = segment layout repacked at load "
                          "(default), plain = Q4_0 blocks as stored")
