@@ -429,3 +429,185 @@ void orc_matvec_q8w(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, i
         }
     }
 }
+
+/* ---------------------------------------------------------------------- */
+/* Q4_K weights.  The conversion step picks Q4_K for weights [GGML: Backend */
+/* abstraction and hardware acceleration, section "How one production call */
+/* lands on the hardware"], but the pages give no block format.  The        */
+/* library reads it as GGML's k-quant super-block of 256 weights (8 sub-     */
+/* blocks of 32), 144 bytes:                                                */
+/*   bytes 0-1   fp16 d    (multiplies the sub-block scales)                */
+/*   bytes 2-3   fp16 dmin (multiplies the sub-block mins)                  */
+/*   bytes 4-15  s[0..11]: eight 6-bit scales sc_j and eight 6-bit mins m_j: */
+/*                 j < 4:  sc_j = s[j] & 63,          m_j = s[j+4] & 63      */
+/*                 j >= 4: sc_j = (s[j+4] & 15) + 16 * (s[j-4] >> 6),        */
+/*                         m_j  = (s[j+4] >> 4) + 16 * (s[j] >> 6)           */
+/*   bytes 16-143: codes; byte 16 + 32p + i holds element i of sub-block 2p  */
+/*                 in its low nibble and element i of sub-block 2p+1 in its  */
+/*                 high nibble (p = 0..3, i = 0..31).                        */
+/*   Element i of sub-block j = d * sc_j * q - dmin * m_j, q in 0..15.       */
+/* A row of K weights (K a multiple of 256) is K/256 super-blocks.          */
+/* ---------------------------------------------------------------------- */
+static void q4k_scale_min(const uint8_t* blk, int j, int* sc, int* m)
+{
+    const uint8_t* s = blk + 4;
+    if (j < 4) {
+        *sc = s[j] & 63;
+        *m = s[j + 4] & 63;
+    } else {
+        *sc = (s[j + 4] & 15) + 16 * (s[j - 4] >> 6);
+        *m = (s[j + 4] >> 4) + 16 * (s[j] >> 6);
+    }
+}
+
+/* Code q (0..15) of element e (0..255) of a super-block. */
+static int q4k_code(const uint8_t* blk, int e)
+{
+    int j = e / 32, i = e % 32;
+    uint8_t byte = blk[16 + 32 * (j / 2) + i];
+    return (j % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+}
+
+static int round_half_away_clamp(float v, int lo, int hi)
+{
+    float r = roundf(v);
+    int q = (int)r;
+    return q < lo ? lo : (q > hi ? hi : q);
+}
+
+/* Q4_K quantization (input preparation; the library's plain reading of the   */
+/* k-quant recipe, all fp32 operations):                                      */
+/*   sub-block j: lo = min w, hi = max w; mn_j = -lo if lo < 0 else 0;        */
+/*     a_j = (hi + mn_j) / 15 (the code step);                                */
+/*   D = max_j a_j / 63, Dm = max_j mn_j / 63; stored d = fp16(D),            */
+/*     dmin = fp16(Dm); dd, ddm = their fp32 values;                          */
+/*   sc_j = round(a_j / dd), m_j = round(mn_j / ddm) (0 when the divisor is 0), */
+/*     halves away from zero, clamped to 0..63;                              */
+/*   q = round((w + ddm*m_j) / (dd*sc_j)) clamped to 0..15 (0 when the step   */
+/*     dd*sc_j is 0).                                                         */
+void orc_quantize_q4_k(const float* w, int64_t rows, int64_t K, uint8_t* out)
+{
+    const int64_t nsb = K / 256;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const float* v = w + r * K + sb * 256;
+            uint8_t* blk = out + (r * nsb + sb) * 144;
+            float a[8], mn[8], amax = 0.0f, mnmax = 0.0f;
+            for (int j = 0; j < 8; ++j) {
+                float lo = v[32 * j], hi = v[32 * j];
+                for (int i = 1; i < 32; ++i) {
+                    if (v[32 * j + i] < lo) lo = v[32 * j + i];
+                    if (v[32 * j + i] > hi) hi = v[32 * j + i];
+                }
+                mn[j] = lo < 0.0f ? -lo : 0.0f;
+                a[j] = (hi + mn[j]) / 15.0f;
+                if (a[j] > amax) amax = a[j];
+                if (mn[j] > mnmax) mnmax = mn[j];
+            }
+            uint16_t dh = orc_f32_to_f16(amax / 63.0f), dmh = orc_f32_to_f16(mnmax / 63.0f);
+            float dd = orc_f16_to_f32(dh), ddm = orc_f16_to_f32(dmh);
+            int sc[8], m[8];
+            for (int j = 0; j < 8; ++j) {
+                sc[j] = dd > 0.0f ? round_half_away_clamp(a[j] / dd, 0, 63) : 0;
+                m[j] = ddm > 0.0f ? round_half_away_clamp(mn[j] / ddm, 0, 63) : 0;
+            }
+            memset(blk, 0, 144);
+            wr_u16(blk, dh);
+            wr_u16(blk + 2, dmh);
+            uint8_t* s = blk + 4;
+            for (int j = 0; j < 4; ++j) {
+                s[j] = (uint8_t)((sc[j] & 63) | ((sc[j + 4] >> 4) << 6));
+                s[j + 4] = (uint8_t)((m[j] & 63) | ((m[j + 4] >> 4) << 6));
+                s[j + 8] = (uint8_t)((sc[j + 4] & 15) | ((m[j + 4] & 15) << 4));
+            }
+            for (int j = 0; j < 8; ++j) {
+                float step = dd * (float)sc[j];
+                float off = ddm * (float)m[j];
+                for (int i = 0; i < 32; ++i) {
+                    int q = 0;
+                    if (step > 0.0f) {
+                        float t = v[32 * j + i] + off;
+                        q = round_half_away_clamp(t / step, 0, 15);
+                    }
+                    uint8_t* byte = blk + 16 + 32 * (j / 2) + i;
+                    *byte = (uint8_t)((j % 2 == 0) ? ((*byte & 0xF0) | q) : ((*byte & 0x0F) | (q << 4)));
+                }
+            }
+        }
+    }
+}
+
+/* Dequantized weights in fp64 (every value d*sc*q - dmin*m is exact there). */
+void orc_dequantize_q4_k(const uint8_t* W, int64_t rows, int64_t K, double* out)
+{
+    const int64_t nsb = K / 256;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const uint8_t* blk = W + (r * nsb + sb) * 144;
+            double d = (double)orc_f16_to_f32(rd_u16(blk)), dmin = (double)orc_f16_to_f32(rd_u16(blk + 2));
+            for (int e = 0; e < 256; ++e) {
+                int sc, m;
+                q4k_scale_min(blk, e / 32, &sc, &m);
+                out[r * K + sb * 256 + e] = d * (double)sc * (double)q4k_code(blk, e) - dmin * (double)m;
+            }
+        }
+}
+
+/* Exact integer sums per 32-weight sub-block (= per Q8_0 block of the      */
+/* activations): isum[n][o][b] = sum_i q_i * qx_i (codes 0..15 times int8).  */
+void orc_block_sums_q4k(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64_t N, int32_t* isum)
+{
+    const int64_t nb = K / QK, nsb = K / 256;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t o = 0; o < O; ++o)
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* blk = W + (o * nsb + b / 8) * 144;
+                const uint8_t* xb = xq + (n * nb + b) * 34;
+                int32_t acc = 0;
+                for (int i = 0; i < QK; ++i)
+                    acc += q4k_code(blk, (int)(b % 8) * 32 + i) * (int32_t)(int8_t)xb[2 + i];
+                isum[(n * O + o) * nb + b] = acc;
+            }
+}
+
+/* Reference product for Q4_K weights: dequantize both operands, dot product */
+/* in fp64.  S[n][o] = sum over sub-blocks b of                             */
+/*   |d_x * d * sc_b * isum_b| + |d_x * dmin * m_b * xsum_b|                 */
+/* (xsum_b = sum of the activation codes), the magnitude of the two terms    */
+/* each sub-block contributes; it scales the output tolerance.              */
+void orc_matvec_q4k(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64_t N,
+                    const int64_t* rows, int64_t nrows, float* y32, double* y64, double* S)
+{
+    const int64_t nb = K / QK, nsb = K / 256;
+    if (!rows)
+        nrows = O;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t t = 0; t < nrows; ++t) {
+            int64_t o = rows ? rows[t] : t;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* blk = W + (o * nsb + b / 8) * 144;
+                const uint8_t* xb = xq + (n * nb + b) * 34;
+                double d = (double)orc_f16_to_f32(rd_u16(blk)), dmin = (double)orc_f16_to_f32(rd_u16(blk + 2));
+                double dx = (double)orc_f16_to_f32(rd_u16(xb));
+                int sc, m;
+                q4k_scale_min(blk, (int)(b % 8), &sc, &m);
+                double sub = 0.0;
+                int64_t isum = 0, xsum = 0;
+                for (int i = 0; i < QK; ++i) {
+                    int q = q4k_code(blk, (int)(b % 8) * 32 + i);
+                    int qx = (int8_t)xb[2 + i];
+                    double wv = d * (double)sc * (double)q - dmin * (double)m;
+                    sub += wv * (dx * (double)qx);
+                    isum += (int64_t)q * qx;
+                    xsum += qx;
+                }
+                acc += sub;
+                mag += fabs(dx * d * (double)sc * (double)isum) + fabs(dx * dmin * (double)m * (double)xsum);
+            }
+            if (y32) y32[n * nrows + t] = (float)acc;
+            if (y64) y64[n * nrows + t] = acc;
+            if (S) S[n * nrows + t] = mag;
+        }
+    }
+}

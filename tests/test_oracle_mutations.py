@@ -38,6 +38,15 @@ MUTATIONS = {
     "seg_scales_in_block_order": ("if (32 + l < r)\n                    hi = rd_u16(row + (first + 32 + l) * 18);",
                                   "if (2 * l + 1 < r)\n                    hi = rd_u16(row + (first + 2 * l + 1) * 18);"),
     "seg_rows_unpadded": ("return 1152 * (nseg - 1) + 16 * r_last + 128;", "return nb * 18 + 128 * 0 + 0 * r_last;"),
+    "q4k_nibbles_swapped": ("return (j % 2 == 0) ? (byte & 0x0F) : (byte >> 4);",
+                            "return (j % 2 == 0) ? (byte >> 4) : (byte & 0x0F);"),
+    "q4k_high_scale_bits_misplaced": ("*sc = (s[j + 4] & 15) + 16 * (s[j - 4] >> 6);",
+                                      "*sc = (s[j + 4] & 15) + 16 * (s[j] >> 6);"),
+    "q4k_min_added": ("out[r * K + sb * 256 + e] = d * (double)sc * (double)q4k_code(blk, e) - dmin * (double)m;",
+                      "out[r * K + sb * 256 + e] = d * (double)sc * (double)q4k_code(blk, e) + dmin * (double)m;"),
+    "q4k_product_min_dropped": ("double wv = d * (double)sc * (double)q - dmin * (double)m;",
+                                "double wv = d * (double)sc * (double)q;"),
+    "q4k_code_group_stride": ("uint8_t byte = blk[16 + 32 * (j / 2) + i];", "uint8_t byte = blk[16 + 16 * j + i];"),
 }
 
 

@@ -530,3 +530,84 @@ def test_q8w_exact_rational(orc, O, K, N):
                 mag += abs(term)
             assert abs(Fraction(float(y64[n, o])) - exact) <= Fraction(1, 10 ** 12) * (mag + 1)
             assert abs(float(S[n, o]) - float(mag)) <= 1e-12 * float(mag) + 1e-300
+
+
+# ---------------------------------------------------------------- Q4_K weights
+def _q4k_golden_block(g):
+    """The hand-derived super-block: header bytes as written in the golden
+    file, codes by its rule and nibble placement."""
+    blk = np.zeros(144, dtype=np.uint8)
+    blk[0], blk[1] = g["d_bits"] & 0xFF, g["d_bits"] >> 8
+    blk[2], blk[3] = g["dmin_bits"] & 0xFF, g["dmin_bits"] >> 8
+    blk[4:16] = g["scales_bytes"]
+    for j in range(8):
+        for i in range(32):
+            q = (i + 3 * j) % 16
+            b = 16 + 32 * (j // 2) + i
+            blk[b] |= np.uint8(q if j % 2 == 0 else q << 4)
+    return blk
+
+
+def _ones_q8(nblocks, d_bits):
+    x = np.zeros((1, nblocks * 34), dtype=np.uint8)
+    for b in range(nblocks):
+        x[0, 34 * b] = d_bits & 0xFF
+        x[0, 34 * b + 1] = d_bits >> 8
+        x[0, 34 * b + 2:34 * b + 34] = 1
+    return x
+
+
+def test_q4k_golden(orc):
+    g = golden()["q4k_superblock"]
+    blk = _q4k_golden_block(g)
+    for k, v in g["spot_bytes"].items():
+        assert int(blk[int(k)]) == v
+    deq = orc.dequantize_q4_k(blk[None, :], 256)[0]
+    for k, v in g["spot_values"].items():
+        assert deq[int(k)] == v
+    for j in range(8):
+        for i in range(32):
+            assert deq[32 * j + i] == 0.5 * g["sc"][j] * ((i + 3 * j) % 16) - 0.25 * g["m"][j], (j, i)
+    x = _ones_q8(8, g["x_d_bits"])
+    isum = orc.block_sums(blk[None, :], x, 256, wtype="q4_k")
+    assert np.all(isum == g["isum_each"])
+    y32, y64, S = orc.matvec(blk[None, :], x, 256, wtype="q4_k")
+    assert y64[0, 0] == g["y"] and y32[0, 0] == np.float32(g["y"]) and S[0, 0] == g["S"]
+
+
+def test_q4k_quantizer_special_blocks(orc):
+    w = np.zeros((3, 256), dtype=np.float32)
+    w[1, :] = 0.75                                     # one positive constant
+    w[2, :] = np.tile((np.arange(32) % 16) * 0.25 - 1.0, 8)   # codes 0..15 on an exact grid
+    Wq = orc.quantize_q4_k(w)
+    deq = orc.dequantize_q4_k(Wq, 256)
+    assert np.all(Wq[0] == 0) and np.all(deq[0] == 0.0)       # zero block: everything zero
+    assert np.all(np.abs(deq[1] - 0.75) <= 0.75 * 2.0 ** -8)   # within the fp16 scale's rounding
+    nib = Wq[2, 16:]
+    codes = np.concatenate([np.stack([nib[32 * p:32 * p + 32] & 15, nib[32 * p:32 * p + 32] >> 4]).reshape(-1)
+                            for p in range(4)])
+    assert np.array_equal(codes, np.tile(np.arange(32) % 16, 8))
+    assert np.max(np.abs(deq[2] - w[2])) <= 4e-3
+
+
+def test_q4k_quantizer_roundtrip_random(orc):
+    rng = np.random.default_rng(11)
+    w = (rng.standard_normal((24, 1024)) * 0.02).astype(np.float32)
+    Wq = orc.quantize_q4_k(w)
+    deq = orc.dequantize_q4_k(Wq, 1024)
+    err = np.abs(deq - w).reshape(24, 32, 32).max(axis=2)
+    rng_ = (w.reshape(24, 32, 32).max(axis=2) - np.minimum(w.reshape(24, 32, 32).min(axis=2), 0))
+    assert np.all(err <= 0.75 * rng_ / 15 + 1e-7)      # within three quarters of a code step
+
+
+def test_q4k_matvec_vs_numpy_dequant(orc):
+    rng = np.random.default_rng(12)
+    K = 512
+    W = orc.quantize_q4_k((rng.standard_normal((5, K)) * 0.02).astype(np.float32))
+    x = orc.quantize_q8_0(rng.standard_normal((2, K)).astype(np.float32), None)
+    qx = x.reshape(2, K // 32, 34)
+    dx = qx[:, :, :2].copy().view(np.float16).astype(np.float64)[:, :, 0]
+    xv = (qx[:, :, 2:].view(np.int8).astype(np.float64) * dx[:, :, None]).reshape(2, K)
+    ref = xv @ orc.dequantize_q4_k(W, K).T
+    _, y64, S = orc.matvec(W, x, K, wtype="q4_k")
+    assert np.all(np.abs(y64 - ref) <= 1e-12 * (S + 1e-30))
