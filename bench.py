@@ -914,6 +914,30 @@ def bench_extras(args, device):
                                            "weight_copies": copies}
         del Ws, W8
         torch.cuda.empty_cache()
+    # Q4_K weights (batch-1 GEMV): the same shapes, quantized on the GPU at
+    # load time, rotating weight copies
+    out["q4_k_weights"] = {}
+    for (O, K) in (workloads.SMALL_N_SHAPES if args.only in (None, "q4k") else ()):
+        W4 = torch.empty(O * (K // 256) * 144, dtype=torch.uint8, device=device)
+        for r in range(0, O, 8192):
+            r1 = min(O, r + 8192)
+            w = torch.from_numpy(synth.weights(workloads.SMALL_N_SEED, f"q4k-{O}x{K}", O, K, row_begin=r,
+                                               row_end=r1)).to(device)
+            qdg.quantize_q4_k(w, W4[r * (K // 256) * 144:r1 * (K // 256) * 144], O=r1 - r, K=K)
+            del w
+        copies = max(2, -(-3 * l2 // W4.numel()))
+        Ws = [W4] + [W4.clone() for _ in range(copies - 1)]
+        x = torch.from_numpy(synth.activations(workloads.SMALL_N_SEED, f"q4k-x-{K}", 1, K)).to(device)
+        xq = torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
+        qdg.qnorm_quantize_q8_0(x, None, 0.0, xq)
+        y = torch.empty(O, dtype=torch.float32, device=device)
+        us = timed_graph(lambda i: qdg.q4_k_q8_0_gemv(Ws[i % copies], xq, y, O, K), copies)
+        nbytes = O * (K // 256) * 144 + (K // 32) * 34 + 4 * O
+        out["q4_k_weights"][f"{O}x{K}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                           "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                                           "weight_copies": copies}
+        del Ws, W4
+        torch.cuda.empty_cache()
     out["peak_note"] = ("small-N against the measured HBM copy bandwidth; prefill against the measured dense "
                         "bf16 burst peak (the fp16 tensor rate is the same nominal 2.25 PFLOP/s)")
     torch.cuda.synchronize()
@@ -962,7 +986,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the small-N and prefill timings")
-    ap.add_argument("--only", choices=["small_n", "prefill", "q8w"], default=None,
+    ap.add_argument("--only", choices=["small_n", "prefill", "q8w", "q4k"], default=None,
                     help="time only that product (one JSON object with its numbers)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -989,11 +1013,11 @@ def main():
         print(json.dumps(line))
         return
 
-    if args.only in ("small_n", "prefill", "q8w"):
+    if args.only in ("small_n", "prefill", "q8w", "q4k"):
         import torch
         torch.cuda.set_device(local)
         ex = bench_extras(args, torch.device("cuda", local))
-        key = "q8_0_weights" if args.only == "q8w" else args.only
+        key = {"q8w": "q8_0_weights", "q4k": "q4_k_weights"}.get(args.only, args.only)
         if rank == 0:
             print(json.dumps({"only": args.only, key: ex[key]}))
         return

@@ -282,6 +282,50 @@ QDG_API int q8_0_q8_0_gemv_group(const void* const* W, float* const* y, const in
                                  const void* xq, int64_t K, qdg_stream_t stream);
 
 /*
+ * quantize_q4_k -- weight preparation: fp32 [O][ldw] -> Q4_K [O][K/256]
+ * super-blocks (format under q4_k_q8_0_gemv below).  The library's plain
+ * reading of the k-quant recipe (the pages name Q4_K but give no
+ * quantizer): per 32-weight sub-block j, mn_j = max(0, -min w) and
+ * a_j = (max w + mn_j) / 15; d = fp16(max_j a_j / 63), dmin =
+ * fp16(max_j mn_j / 63); sc_j = round(a_j / d), m_j = round(mn_j / dmin)
+ * clamped to 0..63; q = round((w + dmin m_j) / (d sc_j)) clamped to 0..15
+ * (halves away from zero; 0 where a divisor is 0); each step one IEEE fp32
+ * operation.  Load time, not the decode path.  K multiple of 256,
+ * ldw >= K; w and Wq 4-byte aligned.
+ */
+QDG_API int quantize_q4_k(const float* w, int64_t ldw, int64_t O, int64_t K, void* Wq,
+                          qdg_stream_t stream);
+
+/*
+ * q4_k_q8_0_gemv -- y = W * x with Q4_K weights, the other weight type the
+ * conversion step picks [GGML: Backend abstraction and hardware
+ * acceleration, sections "How one production call lands on the hardware"
+ * and "Metal and Vulkan"].  The pages give no block format; the library
+ * reads Q4_K as GGML's 256-weight k-quant super-block of 144 bytes:
+ *   bytes 0-1 fp16 d, bytes 2-3 fp16 dmin, bytes 4-15 s[0..11] packing
+ *   eight 6-bit sub-block scales sc_j and mins m_j (j < 4: sc_j = s[j] & 63,
+ *   m_j = s[j+4] & 63; j >= 4: sc_j = (s[j+4] & 15) + 16 (s[j-4] >> 6),
+ *   m_j = (s[j+4] >> 4) + 16 (s[j] >> 6)), bytes 16-143 the codes: byte
+ *   16 + 32p + i holds element i of sub-block 2p (low nibble) and of
+ *   sub-block 2p+1 (high nibble).  Weight = d sc_j q - dmin m_j, q in 0..15.
+ * W [O][K/256] super-blocks (row = 18 K/32 bytes, as Q4_0), 16-byte aligned.
+ * xq [K/32] Q8_0, 4-byte aligned: each Q8_0 block meets one 32-weight
+ * sub-block.  y [O] fp32 (overwritten).  K multiple of 256, <= 32768;
+ * 1 <= O < 2^31.  Per sub-block the exact integer sums isum = sum q q_x and
+ * xsum = sum q_x, then d_x (d sc isum - dmin m xsum) in fp32; results agree
+ * with the exact value within 1e-5 * sum |d_x d sc isum| + |d_x dmin m xsum|.
+ * Deterministic.  4.5 bits per weight, the segment/row split of the Q4_0
+ * product.
+ */
+QDG_API int q4_k_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K,
+                           qdg_stream_t stream);
+
+/* q4_k_q8_0_gemv for up to 4 Q4_K matrices reading one Q8_0 vector, in one
+ * launch (argument rules as q4_0_q8_0_gemv_group). */
+QDG_API int q4_k_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                 const void* xq, int64_t K, qdg_stream_t stream);
+
+/*
  * Segment layout of Q4_0 weights (load-time repack).  GGML's CPU back end
  * rearranges Q4 weights once, when they are loaded, for its own kernels
  * [GGML: Backend abstraction and hardware acceleration, section "How build
@@ -461,7 +505,7 @@ QDG_API int qdg_stage_copy(void* dst, const void* src, int64_t bytes, qdg_stream
  * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
  * 4 weight quantize, 5 fused norm+gemv, 6 segment-layout gemv, 7 repack,
  * 8 Q8_0-weight gemv, 9 fused norm+gemv on the segment layout, 10 staging copy,
- * 11 decode-step chain, -1 total.  Lets a caller check
+ * 11 decode-step chain, 12 Q4_K-weight gemv, -1 total.  Lets a caller check
  * that the fused kernel is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);
@@ -473,7 +517,8 @@ QDG_API int64_t qdg_launch_count(int which);
  * path: 0 = gemv (N must be 1), 1 = small-N, 2 = prefill gemm (N = T tokens),
  * 3 = segment-layout gemv (W in the segment layout, N must be 1),
  * 4 = Q8_0-weight gemv (W in Q8_0 blocks, N must be 1), 5 = segment-layout
- * small-N (W in the segment layout, N = 1..8).
+ * small-N (W in the segment layout, N = 1..8), 6 = Q4_K-weight gemv (W in
+ * Q4_K super-blocks, N must be 1; isum = sum q q_x per 32-weight sub-block).
  * Same argument rules as the corresponding entry point.
  */
 QDG_API int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum, int64_t O,
