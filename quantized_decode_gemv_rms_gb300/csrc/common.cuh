@@ -119,6 +119,15 @@ __device__ __forceinline__ void bulk_g2s_plain(void* dst, const void* src, uint3
                  : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared, cached in L2 only (so it reads
+// what other CTAs wrote before a grid-wide synchronisation); completes at
+// cp_async_wait_all of the same thread.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Programmatic dependent launch: wait for the preceding grid's memory, and
 // allow the following grid to be scheduled.  No-ops without the attribute.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

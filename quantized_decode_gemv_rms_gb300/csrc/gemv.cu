@@ -267,24 +267,33 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
             for (int h = 16; h >= 1; h >>= 1)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) d[u] = fmaxf(d[u], __shfl_xor_sync(0xffffffffu, d[u], h));
+            // the four blocks' divisions and roundings are independent: all
+            // first (a block past nb has v = 0 and gives q = 0), then the
+            // stores, so that the four dependent chains overlap
+            float dd[4];
+            int q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                dd[u] = __fdiv_rn(d[u], 127.0f);
+                q[u] = 0;
+                if (dd[u] != 0.0f) {
+                    float r = roundf(__fdiv_rn(v[u], dd[u]));
+                    r = fminf(fmaxf(r, -127.0f), 127.0f);
+                    q[u] = static_cast<int>(r);
+                }
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int b = b0 + u * kWarps;
-                if (b >= nb) break;
-                const float dd = __fdiv_rn(d[u], 127.0f);
-                int q = 0;
-                if (dd != 0.0f) {
-                    float r = roundf(__fdiv_rn(v[u], dd));
-                    r = fminf(fmaxf(r, -127.0f), 127.0f);
-                    q = static_cast<int>(r);
+                if (b < nb) {
+                    uint8_t* blk = xqs + b * 34;
+                    if (lane == 0) {
+                        const __half dh = __float2half_rn(dd[u]);
+                        *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
+                        if (__hisinf(dh)) atomicOr(&g_flags_gemv, FLAG_OVERFLOW);
+                    }
+                    blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q[u]));
                 }
-                uint8_t* blk = xqs + b * 34;
-                if (lane == 0) {
-                    const __half dh = __float2half_rn(dd);
-                    *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
-                    if (__hisinf(dh)) atomicOr(&g_flags_gemv, FLAG_OVERFLOW);
-                }
-                blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
             }
         }
         __syncthreads();

@@ -242,13 +242,13 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
         const int K = nb * 32;
         float* xf = reinterpret_cast<float*>(xs + nb * 34);   // nb * 34 is a multiple of 16
         float* gf = xf + K;
-        if (threadIdx.x == 0) {
-            const uint32_t bytes = static_cast<uint32_t>(K) * 4;
-            mbar_arrive_expect_tx(&xbar, a.gamma != nullptr ? 2 * bytes : bytes);
-            bulk_g2s_plain(xf, a.x, bytes, &xbar);
-            if (a.gamma != nullptr) bulk_g2s_plain(gf, a.gamma, bytes, &xbar);
+        // x and gamma by 16-byte asynchronous copies spread over the CTA
+        for (int i = 4 * threadIdx.x; i < K; i += 4 * kThreads) {
+            cp_async16(xf + i, a.x + i);
+            if (a.gamma != nullptr) cp_async16(gf + i, a.gamma + i);
         }
-        if (!mbar_wait(&xbar, 0)) atomicOr(&g_flags_gemv_seg, FLAG_TIMEOUT);
+        cp_async_wait_all();
+        __syncthreads();
         float s = 1.0f;
         if (a.gamma != nullptr) {
             if (threadIdx.x < 256) {
@@ -279,24 +279,33 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
             for (int h = 16; h >= 1; h >>= 1)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) d[u] = fmaxf(d[u], __shfl_xor_sync(0xffffffffu, d[u], h));
+            // the four blocks' divisions and roundings are independent: all
+            // first (a block past nb has v = 0 and gives q = 0), then the
+            // stores, so that the four dependent chains overlap
+            float dd[4];
+            int q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                dd[u] = __fdiv_rn(d[u], 127.0f);
+                q[u] = 0;
+                if (dd[u] != 0.0f) {
+                    float rr = roundf(__fdiv_rn(v[u], dd[u]));
+                    rr = fminf(fmaxf(rr, -127.0f), 127.0f);
+                    q[u] = static_cast<int>(rr);
+                }
+            }
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int b = b0 + u * kWarps;
-                if (b >= nb) break;
-                const float dd = __fdiv_rn(d[u], 127.0f);
-                int q = 0;
-                if (dd != 0.0f) {
-                    float rr = roundf(__fdiv_rn(v[u], dd));
-                    rr = fminf(fmaxf(rr, -127.0f), 127.0f);
-                    q = static_cast<int>(rr);
+                if (b < nb) {
+                    uint8_t* blk = xs + b * 34;
+                    if (lane == 0) {
+                        const __half dh = __float2half_rn(dd[u]);
+                        *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
+                        if (__hisinf(dh)) atomicOr(&g_flags_gemv_seg, FLAG_OVERFLOW);
+                    }
+                    blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q[u]));
                 }
-                uint8_t* blk = xs + b * 34;
-                if (lane == 0) {
-                    const __half dh = __float2half_rn(dd);
-                    *reinterpret_cast<unsigned short*>(blk) = __half_as_ushort(dh);
-                    if (__hisinf(dh)) atomicOr(&g_flags_gemv_seg, FLAG_OVERFLOW);
-                }
-                blk[2 + lane] = static_cast<uint8_t>(static_cast<int8_t>(q));
             }
         }
         __syncthreads();
@@ -308,14 +317,12 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
         if (has_a) load_act<true>(xs, seg * 64 + lane, xa, dxa, sa);
         if (has_b) load_act<true>(xs, seg * 64 + 32 + lane, xb, dxb, sb);
     } else if (a.xq_bulk) {
-        // one bulk copy of the whole vector (one round trip), then the
-        // lanes' blocks out of shared memory
-        if (threadIdx.x == 0) {
-            const uint32_t bytes = static_cast<uint32_t>(plan.nb * 34);
-            mbar_arrive_expect_tx(&xbar, bytes);
-            bulk_g2s_plain(xs, a.xq, bytes, &xbar);
-        }
-        if (!mbar_wait(&xbar, 0)) atomicOr(&g_flags_gemv_seg, FLAG_TIMEOUT);
+        // the whole vector by 16-byte asynchronous copies spread over the
+        // CTA (one round trip), then the lanes' blocks out of shared memory
+        const int n16 = plan.nb * 34 / 16;   // K % 256 == 0: a whole number of 16-byte pieces
+        for (int i = threadIdx.x; i < n16; i += kThreads) cp_async16(xs + 16 * i, a.xq + 16 * i);
+        cp_async_wait_all();
+        __syncthreads();
         if (has_a) load_act<true>(xs, seg * 64 + lane, xa, dxa, sa);
         if (has_b) load_act<true>(xs, seg * 64 + 32 + lane, xb, dxb, sb);
     } else {

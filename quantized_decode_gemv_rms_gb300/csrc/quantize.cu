@@ -17,7 +17,11 @@ static __device__ unsigned g_flags_quantize;
 namespace {
 
 constexpr int kNormThreads = 256;     // the fixed reduction order is defined over 256 lanes
-constexpr int kBlocksPerCta = 32;     // Q8_0 blocks quantized by one CTA (4 per warp)
+// Q8_0 blocks quantized by one CTA: one per warp.  A block is a dependent
+// chain of about 380 SM cycles (the five-step maximum alone about 135,
+// measured on GB300), so a warp with four blocks spent about 1.5 us on a
+// decode-step boundary; more CTAs with one block a warp cut that to one chain.
+constexpr int kBlocksPerCta = 8;
 constexpr int kStageMax = 8192;       // vectors up to this length are read for the norm in one wave of loads
 constexpr int kStagePer = kStageMax / 4 / kNormThreads;   // 16-byte loads per thread in that wave
 
