@@ -242,13 +242,13 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
         const int K = nb * 32;
         float* xf = reinterpret_cast<float*>(xs + nb * 34);   // nb * 34 is a multiple of 16
         float* gf = xf + K;
-        // x and gamma by 16-byte asynchronous copies spread over the CTA
-        for (int i = 4 * threadIdx.x; i < K; i += 4 * kThreads) {
-            cp_async16(xf + i, a.x + i);
-            if (a.gamma != nullptr) cp_async16(gf + i, a.gamma + i);
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(K) * 4;
+            mbar_arrive_expect_tx(&xbar, a.gamma != nullptr ? 2 * bytes : bytes);
+            bulk_g2s_plain(xf, a.x, bytes, &xbar);
+            if (a.gamma != nullptr) bulk_g2s_plain(gf, a.gamma, bytes, &xbar);
         }
-        cp_async_wait_all();
-        __syncthreads();
+        if (!mbar_wait(&xbar, 0)) atomicOr(&g_flags_gemv_seg, FLAG_TIMEOUT);
         float s = 1.0f;
         if (a.gamma != nullptr) {
             if (threadIdx.x < 256) {
@@ -317,12 +317,16 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
         if (has_a) load_act<true>(xs, seg * 64 + lane, xa, dxa, sa);
         if (has_b) load_act<true>(xs, seg * 64 + 32 + lane, xb, dxb, sb);
     } else if (a.xq_bulk) {
-        // the whole vector by 16-byte asynchronous copies spread over the
-        // CTA (one round trip), then the lanes' blocks out of shared memory
-        const int n16 = plan.nb * 34 / 16;   // K % 256 == 0: a whole number of 16-byte pieces
-        for (int i = threadIdx.x; i < n16; i += kThreads) cp_async16(xs + 16 * i, a.xq + 16 * i);
-        cp_async_wait_all();
-        __syncthreads();
+        // one bulk copy of the whole vector (one round trip), then the
+        // lanes' blocks out of shared memory (measured on GB300: 16-byte
+        // cp.async copies from every thread queue behind the weight loads
+        // already in flight and arrived 0.5-1 us later)
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = static_cast<uint32_t>(plan.nb * 34);
+            mbar_arrive_expect_tx(&xbar, bytes);
+            bulk_g2s_plain(xs, a.xq, bytes, &xbar);
+        }
+        if (!mbar_wait(&xbar, 0)) atomicOr(&g_flags_gemv_seg, FLAG_TIMEOUT);
         if (has_a) load_act<true>(xs, seg * 64 + lane, xa, dxa, sa);
         if (has_b) load_act<true>(xs, seg * 64 + 32 + lane, xb, dxb, sb);
     } else {
