@@ -314,8 +314,9 @@ QDG_API int quantize_q4_k(const float* w, int64_t ldw, int64_t O, int64_t K, voi
  * 1 <= O < 2^31.  Per sub-block the exact integer sums isum = sum q q_x and
  * xsum = sum q_x, then d_x (d sc isum - dmin m xsum) in fp32; results agree
  * with the exact value within 1e-5 * sum |d_x d sc isum| + |d_x dmin m xsum|.
- * Deterministic.  4.5 bits per weight, the segment/row split of the Q4_0
- * product.
+ * Deterministic.  4.5 bits per weight; a super-block is nine 16-byte words,
+ * so lanes load their codes and headers straight into registers (the
+ * row/segment split of q4_0s_q8_0_gemv, no repack needed).
  */
 QDG_API int q4_k_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K,
                            qdg_stream_t stream);

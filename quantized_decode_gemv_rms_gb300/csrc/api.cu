@@ -127,7 +127,7 @@ extern "C" int qdg_device_status(qdg_stream_t stream) {
     const unsigned parts[] = {flags_read_clear_quantize(s), flags_read_clear_gemv(s), flags_read_clear_gemv_seg(s),
                               flags_read_clear_small_n(s), flags_read_clear_small_n_seg(s),
                               flags_read_clear_gemm(s), flags_read_clear_api(s),
-                              flags_read_clear_chain(s)};
+                              flags_read_clear_chain(s), flags_read_clear_gemv_q4k(s)};
     for (unsigned p : parts) {
         if (p == ~0u) {
             cudaGetLastError();

@@ -263,5 +263,6 @@ unsigned flags_read_clear_small_n_seg(cudaStream_t stream);
 unsigned flags_read_clear_gemm(cudaStream_t stream);
 unsigned flags_read_clear_api(cudaStream_t stream);
 unsigned flags_read_clear_chain(cudaStream_t stream);
+unsigned flags_read_clear_gemv_q4k(cudaStream_t stream);
 
 }  // namespace qdg

@@ -47,19 +47,15 @@ constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
 // three 16-byte loads per lane, three segments in flight per warp.  Q8_0:
 // 34-byte blocks, 68-byte pairs, 2176-byte segments read as five loads per
 // lane, two segments in flight (about the same registers, more bytes).
-// Q4_K: 144-byte super-blocks of 256 weights, i.e. 18 bytes per 32 weights
-// like Q4_0, so a 1152-byte segment is eight super-blocks and lane l owns
-// sub-blocks 2(l%4) and 2(l%4)+1 of super-block l/4 (the same 64 weights,
-// and so the same activation pair, as a Q4_0 lane).
-enum { kQ4 = 0, kQ8 = 1, kQ4K = 2 };
+enum { kQ4 = 0, kQ8 = 1 };
 template <int kW>
 struct WT {
-    static constexpr int kBlockBytes = kW == kQ8 ? 34 : 18;   // bytes per 32 weights
+    static constexpr int kBlockBytes = kW == kQ4 ? 18 : 34;
     static constexpr int kPairBytes = 2 * kBlockBytes;
     static constexpr int kSegBytes = 32 * kPairBytes;
     static constexpr int kLoads = (kSegBytes / 16 + 31) / 32;
-    static constexpr int kDepth = kW == kQ8 ? 2 : 3;
-    static constexpr int kPartFloats = kW == kQ8 ? 2048 : 4096;   // per-chunk partial sums (rows x segments)
+    static constexpr int kDepth = kW == kQ4 ? 3 : 2;
+    static constexpr int kPartFloats = kW == kQ4 ? 4096 : 2048;   // per-chunk partial sums (rows x segments)
 };
 
 struct Plan {
@@ -373,44 +369,6 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
                 ib = block_dot(w[5], w[6], w[7], w[8], xb) - 8 * sb;
                 dwa = half_bits_to_float(w[0]);
                 dwb = half_bits_to_float(w[4] >> 16);
-            } else if (kW == kQ4K) {
-                // super-block lane/4 of the segment, sub-blocks j0 = 2(lane%4) and j0+1:
-                // header words (d | dmin << 16, then the twelve scale bytes), and
-                // the 32 code bytes of the pair (low nibbles j0, high nibbles j0+1)
-                const uint8_t* sbp = buf + (lane >> 2) * 144;
-                const uint4 h = *reinterpret_cast<const uint4*>(sbp);
-                const uint4 c0 = *reinterpret_cast<const uint4*>(sbp + 16 + 32 * (lane & 3));
-                const uint4 c1 = *reinterpret_cast<const uint4*>(sbp + 32 + 32 * (lane & 3));
-                const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-                int sa4 = 0, sb4 = 0;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    sa4 = __dp4a(static_cast<int>(cw[i] & kNibbles), static_cast<int>(xa[i]), sa4);
-                    sb4 = __dp4a(static_cast<int>((cw[i] >> 4) & kNibbles), static_cast<int>(xb[i]), sb4);
-                }
-                ia = sa4;
-                ib = sb4;
-                // 6-bit scale and min of sub-block j (t = j mod 4): j < 4 from the
-                // low six bits of scale bytes t and 4+t; j >= 4 from the nibbles
-                // of byte 8+t, topped by the high two bits of bytes t and 4+t
-                const int t0 = 2 * (lane & 1);
-                const bool high = (lane & 2) != 0;
-                int sc[2], mn[2];
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int sh = 8 * (t0 + u);
-                    const uint32_t b1 = (h.y >> sh) & 255u, b2 = (h.z >> sh) & 255u, b3 = (h.w >> sh) & 255u;
-                    sc[u] = static_cast<int>(high ? ((b3 & 15u) | ((b1 >> 6) << 4)) : (b1 & 63u));
-                    mn[u] = static_cast<int>(high ? ((b3 >> 4) | ((b2 >> 6) << 4)) : (b2 & 63u));
-                }
-                const float d = half_bits_to_float(h.x), dmin = half_bits_to_float(h.x >> 16);
-                // d * sc and dmin * m are exact in fp32 (11 + 6 significant bits)
-                const float ta = __fmaf_rn(__fmul_rn(d, static_cast<float>(sc[0])), static_cast<float>(ia),
-                                           -__fmul_rn(__fmul_rn(dmin, static_cast<float>(mn[0])), static_cast<float>(sa)));
-                const float tb = __fmaf_rn(__fmul_rn(d, static_cast<float>(sc[1])), static_cast<float>(ib),
-                                           -__fmul_rn(__fmul_rn(dmin, static_cast<float>(mn[1])), static_cast<float>(sb)));
-                dwa = ta;
-                dwb = tb;
             } else {
                 // Q8_0 pair: scale a, 32 codes of a (bytes 2..33), scale b, 32 codes of b (word aligned)
                 const uint32_t* wp = reinterpret_cast<const uint32_t*>(buf + lane * 68);
@@ -427,14 +385,8 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
                 dwa = half_bits_to_float(w[0]);
                 dwb = half_bits_to_float(w[8] >> 16);
             }
-            if (kW == kQ4K) {
-                // dwa, dwb hold the sub-blocks' d sc isum - dmin m xsum
-                acc = __fmul_rn(dxa, dwa);
-                acc = __fmaf_rn(dxb, dwb, acc);
-            } else {
-                acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
-                acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
-            }
+            acc = __fmul_rn(__fmul_rn(dwa, dxa), static_cast<float>(ia));
+            acc = __fmaf_rn(__fmul_rn(dwb, dxb), static_cast<float>(ib), acc);
             if (kDebug) {
                 int32_t* d = dbg + (c0 + ri) * plan.nb + 2 * p;
                 d[0] = ia;
@@ -442,7 +394,7 @@ __global__ void __maxnreg__(96) gemv_kernel(const Args a, Plan plan) {
             }
         }
         __syncwarp();
-        if (kW != kQ8) {
+        if (kW == kQ4) {
             acc = warp_sum(acc);
             if (lane == 0) part[ri * nseg + seg] = acc;
         }
@@ -538,7 +490,7 @@ int gemv_launch_typed(const void* const* W, float* const* y, const int64_t* O, i
     else
         e = launch(gemv_kernel<kW, false, false>, dim3(grid), dim3(kThreads), 0, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
-    count_launch(kW == kQ4 ? 1 : (kW == kQ8 ? 8 : 12));
+    count_launch(kW == kQ4 ? 1 : 8);
     return QDG_OK;
 }
 
@@ -552,17 +504,6 @@ int gemv_launch_group(const void* const* W, float* const* y, const int64_t* O, i
 int gemv_q8w_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq,
                           int64_t K, cudaStream_t stream, int32_t* dbg) {
     return gemv_launch_typed<kQ8>(W, y, O, count, xq, K, stream, dbg);
-}
-
-int gemv_q4k_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq,
-                          int64_t K, cudaStream_t stream, int32_t* dbg) {
-    return gemv_launch_typed<kQ4K>(W, y, O, count, xq, K, stream, dbg);
-}
-
-int gemv_q4k_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
-                    int32_t* dbg) {
-    float* ys[1] = {y};
-    return gemv_q4k_launch_group(&W, y ? ys : nullptr, &O, 1, xq, K, stream, dbg);
 }
 
 int gemv_q8w_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
@@ -661,15 +602,4 @@ extern "C" int q8_0_q8_0_gemv_group(const void* const* W, float* const* y, const
                                     const void* xq, int64_t K, qdg_stream_t stream) {
     if (!y) return QDG_EINVAL;
     return qdg::gemv_q8w_launch_group(W, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
-}
-
-extern "C" int q4_k_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K, qdg_stream_t stream) {
-    if (!y) return QDG_EINVAL;
-    return qdg::gemv_q4k_launch(W, xq, y, O, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
-}
-
-extern "C" int q4_k_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
-                                    const void* xq, int64_t K, qdg_stream_t stream) {
-    if (!y) return QDG_EINVAL;
-    return qdg::gemv_q4k_launch_group(W, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
