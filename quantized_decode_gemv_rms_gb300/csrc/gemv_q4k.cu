@@ -172,11 +172,13 @@ __global__ void __maxnreg__(96) gemv_q4k_kernel(const __grid_constant__ Args a, 
         load_act(xsrc, 2 * p + 1, xb, dxb, sb);
     }
 
-    // the 6-bit scale and min of sub-blocks 2g (u = 0) and 2g+1 (u = 1):
-    // sub-blocks 0..3 take the low six bits of scale bytes t and 4+t; 4..7
-    // the nibbles of byte 8+t topped by the high two bits of bytes t and 4+t
-    // (t = sub-block mod 4)
-    const int t0 = 2 * (g & 1);
+    // the 6-bit scale and min of sub-blocks 2g and 2g+1 (t = 2(g mod 2) and
+    // t + 1 within the scale words): sub-blocks 0..3 take the low six bits of
+    // scale bytes t and 4+t; 4..7 the nibbles of byte 8+t topped by the high
+    // two bits of bytes t and 4+t.  Both sub-blocks at once on byte pairs:
+    // P1 = bytes (t, t+1) of word 1 (scale bytes 0..3), P2 of word 2, P3 of
+    // word 3, each in the low 16 bits by one byte permute.
+    const uint32_t sel = (g & 1) ? 0x3232u : 0x1010u;       // bytes (2, 3) or (0, 1), twice
     const bool high = g >= 2;
     auto consume = [&](int64_t c0, int crows, int ri, Entry& entry) -> float {
         const Entry& e = entry;
@@ -187,23 +189,20 @@ __global__ void __maxnreg__(96) gemv_q4k_kernel(const __grid_constant__ Args a, 
             ia = __dp4a(static_cast<int>(cw[i] & kNibbles), static_cast<int>(xa[i]), ia);
             ib = __dp4a(static_cast<int>((cw[i] >> 4) & kNibbles), static_cast<int>(xb[i]), ib);
         }
-        float sc[2], mn[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-            const int sh = 8 * (t0 + u);
-            const uint32_t b1 = (e.h.y >> sh) & 255u, b2 = (e.h.z >> sh) & 255u, b3 = (e.h.w >> sh) & 255u;
-            sc[u] = static_cast<float>(high ? ((b3 & 15u) | ((b1 >> 6) << 4)) : (b1 & 63u));
-            mn[u] = static_cast<float>(high ? ((b3 >> 4) | ((b2 >> 6) << 4)) : (b2 & 63u));
-        }
+        const uint32_t P1 = __byte_perm(e.h.y, 0, sel) & 0xFFFFu;
+        const uint32_t P2 = __byte_perm(e.h.z, 0, sel) & 0xFFFFu;
+        const uint32_t P3 = __byte_perm(e.h.w, 0, sel) & 0xFFFFu;
+        const uint32_t SC = high ? ((P3 & 0x0F0Fu) | ((P1 >> 2) & 0x3030u)) : (P1 & 0x3F3Fu);
+        const uint32_t MN = high ? (((P3 >> 4) & 0x0F0Fu) | ((P2 >> 2) & 0x3030u)) : (P2 & 0x3F3Fu);
+        // integer products first (sc isum < 2^22, m xsum < 2^18: exact), then
+        // one rounding each against the fp16 d and dmin
         const float d = half_bits_to_float(e.h.x), dmin = half_bits_to_float(e.h.x >> 16);
-        // d sc and dmin m are exact in fp32 (11 + 6 significant bits)
-        const float ta = __fmaf_rn(__fmul_rn(d, sc[0]), static_cast<float>(ia),
-                                   -__fmul_rn(__fmul_rn(dmin, mn[0]), static_cast<float>(sa)));
-        const float tb = __fmaf_rn(__fmul_rn(d, sc[1]), static_cast<float>(ib),
-                                   -__fmul_rn(__fmul_rn(dmin, mn[1]), static_cast<float>(sb)));
+        const float ta = __fmaf_rn(d, static_cast<float>(static_cast<int>(SC & 0xFFu) * ia),
+                                   -__fmul_rn(dmin, static_cast<float>(static_cast<int>(MN & 0xFFu) * sa)));
+        const float tb = __fmaf_rn(d, static_cast<float>(static_cast<int>(SC >> 8) * ib),
+                                   -__fmul_rn(dmin, static_cast<float>(static_cast<int>(MN >> 8) * sb)));
         float acc = __fmul_rn(dxa, ta);
-        acc = __fmaf_rn(dxb, tb, acc);
-        if (!has) acc = 0.0f;
+        acc = __fmaf_rn(dxb, tb, acc);   // lanes without a super-block hold zero activations and codes
         if (kDebug && has) {
             int32_t* dst = a.dbg + (c0 + ri) * plan.nb + 2 * p;
             dst[0] = ia;
