@@ -914,6 +914,15 @@ def bench_extras(args, device):
                                            "weight_copies": copies}
         del Ws, W8
         torch.cuda.empty_cache()
+    # the quantize kernel alone on the decode step's activation shapes (one
+    # vector, with and without the norm): a graph of back-to-back launches
+    out["qnorm"] = {}
+    for (K, norm) in (((4096, True), (14336, False)) if args.only in (None, "qnorm") else ()):
+        x = torch.from_numpy(synth.activations(workloads.SMALL_N_SEED, f"qn-x-{K}", 1, K)).to(device)
+        g = torch.from_numpy(synth.gamma(workloads.SMALL_N_SEED, f"qn-g-{K}", K)).to(device) if norm else None
+        xq = torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
+        us = timed_graph(lambda i: qdg.qnorm_quantize_q8_0(x, g, 1e-6, xq), 20)
+        out["qnorm"][f"K{K}{'_norm' if norm else '_plain'}"] = {"us": round(us, 2)}
     # Q4_K weights (batch-1 GEMV): the same shapes, quantized on the GPU at
     # load time, rotating weight copies
     out["q4_k_weights"] = {}
@@ -986,7 +995,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the small-N and prefill timings")
-    ap.add_argument("--only", choices=["small_n", "prefill", "q8w", "q4k"], default=None,
+    ap.add_argument("--only", choices=["small_n", "prefill", "q8w", "q4k", "qnorm"], default=None,
                     help="time only that product (one JSON object with its numbers)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -1013,7 +1022,7 @@ def main():
         print(json.dumps(line))
         return
 
-    if args.only in ("small_n", "prefill", "q8w", "q4k"):
+    if args.only in ("small_n", "prefill", "q8w", "q4k", "qnorm"):
         import torch
         torch.cuda.set_device(local)
         ex = bench_extras(args, torch.device("cuda", local))
