@@ -378,13 +378,16 @@ QDG_API int q4_0s_q8_0_gemv_group(const void* const* Wr, float* const* y, const 
  * q4_0s_q8_0_gemm_small_n -- the small-N product on the segment layout for
  * N = 1..8 vectors sharing one pass over W (speculative / parallel decode).
  * N = 1 is q4_0s_q8_0_gemv.  At N = 2 each block's nibbles are unpacked once
- * and dotted with both vectors by dp4a.  N = 3..8 form the exact block sums
- * with the fp16 warp MMA as q4_0_q8_0_gemm_small_n does, each lane loading
- * its own nibble and scale words straight from the segment layout into
- * registers (two row tiles ahead); for K > 4096 a thread-block cluster of
- * ceil(K/4096) CTAs splits K.  Wr [O][q4_0_seg_row_bytes(K)], 16-byte
- * aligned; xq: N Q8_0 vectors of K/32 blocks back to back (16-byte aligned
- * for N >= 3, 2-byte aligned for N <= 2); y: [N][ldy] fp32, ldy >= O.
+ * and dotted with both vectors by dp4a.  At N = 3, 4 with K <= 16384 a lane
+ * owns one block of a half-segment and keeps that block of every vector in
+ * registers; the exact block sums come from dp4a, eight rows in flight per
+ * warp.  Otherwise (N = 5..8, or K > 16384) the exact block sums come from
+ * the fp16 warp MMA as in q4_0_q8_0_gemm_small_n (same arithmetic and order,
+ * bit-identical), each warp staging its own tiles with cp.async; for
+ * K > 4096 a thread-block cluster of ceil(K/4096) CTAs splits K.
+ * Wr [O][q4_0_seg_row_bytes(K)], 16-byte aligned; xq: N Q8_0 vectors of K/32
+ * blocks back to back (16-byte aligned for N >= 3, 2-byte aligned for
+ * N <= 2); y: [N][ldy] fp32, ldy >= O.
  * K multiple of 256, <= 32768; 1 <= O < 2^31.  Deterministic (fixed
  * reduction order).  QDG_EINVAL for N outside 1..8.
  */
@@ -506,7 +509,8 @@ QDG_API int qdg_stage_copy(void* dst, const void* src, int64_t bytes, qdg_stream
  * process, per kernel: which = 0 qnorm/quantize, 1 gemv, 2 small-N, 3 gemm,
  * 4 weight quantize, 5 fused norm+gemv, 6 segment-layout gemv, 7 repack,
  * 8 Q8_0-weight gemv, 9 fused norm+gemv on the segment layout, 10 staging copy,
- * 11 decode-step chain, 12 Q4_K-weight gemv, -1 total.  Lets a caller check
+ * 11 decode-step chain, 12 Q4_K-weight gemv, 13 three/four-vector segment-layout
+ * small-N, -1 total.  Lets a caller check
  * that the fused kernel is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);

@@ -15,7 +15,7 @@ namespace {
 std::mutex g_dev_mutex;
 DeviceInfo g_dev_cache[64];
 std::atomic<int> g_pdl{0};
-std::atomic<int64_t> g_counts[13];
+std::atomic<int64_t> g_counts[14];
 }  // namespace
 
 DeviceInfo device_info() {
@@ -100,7 +100,7 @@ extern "C" int64_t qdg_launch_count(int which) {
         for (auto& c : g_counts) t += c.load();
         return t;
     }
-    if (which < 0 || which >= 13) return -1;
+    if (which < 0 || which >= 14) return -1;
     return g_counts[which].load();
 }
 
@@ -127,7 +127,8 @@ extern "C" int qdg_device_status(qdg_stream_t stream) {
     const unsigned parts[] = {flags_read_clear_quantize(s), flags_read_clear_gemv(s), flags_read_clear_gemv_seg(s),
                               flags_read_clear_small_n(s), flags_read_clear_small_n_seg(s),
                               flags_read_clear_gemm(s), flags_read_clear_api(s),
-                              flags_read_clear_chain(s), flags_read_clear_gemv_q4k(s)};
+                              flags_read_clear_chain(s), flags_read_clear_gemv_q4k(s),
+                              flags_read_clear_gemv_segn(s)};
     for (unsigned p : parts) {
         if (p == ~0u) {
             cudaGetLastError();
@@ -173,6 +174,7 @@ extern "C" int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum
         case 5:
             if (N == 1) return gemv_seg_launch(W, xq, nullptr, O, K, s, isum);
             if (N == 2) return gemv_seg2_launch(W, xq, nullptr, O, O, K, s, isum);
+            if (gemv_segn_supported(K, N)) return gemv_segn_launch(W, xq, nullptr, O, O, K, N, s, isum);
             return small_n_seg_launch(W, xq, nullptr, O, O, K, N, s, isum);
         default:
             return QDG_EINVAL;

@@ -249,6 +249,10 @@ int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t
                    cudaStream_t stream, int32_t* dbg);
 int small_n_seg_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t N,
                        cudaStream_t stream, int32_t* dbg);
+// three or four vectors on the segment layout by dp4a (one block a lane), K <= 16384
+bool gemv_segn_supported(int64_t K, int64_t N);
+int gemv_segn_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t N,
+                     cudaStream_t stream, int32_t* dbg);
 int64_t gemm_workspace_bytes(int64_t K, int64_t T);
 int chain_launch(const qdg_chain_stage* stages, int nstages, float eps, void* sync, cudaStream_t stream);
 int gemm_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K, int64_t T, void* ws,
@@ -264,5 +268,6 @@ unsigned flags_read_clear_gemm(cudaStream_t stream);
 unsigned flags_read_clear_api(cudaStream_t stream);
 unsigned flags_read_clear_chain(cudaStream_t stream);
 unsigned flags_read_clear_gemv_q4k(cudaStream_t stream);
+unsigned flags_read_clear_gemv_segn(cudaStream_t stream);
 
 }  // namespace qdg

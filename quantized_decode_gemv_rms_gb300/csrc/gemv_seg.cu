@@ -800,5 +800,6 @@ extern "C" int q4_0s_q8_0_gemm_small_n(const void* Wr, const void* xq, float* y,
         return gemv_seg_launch(Wr, xq, y, O, K, s, nullptr);
     }
     if (N == 2) return gemv_seg2_launch(Wr, xq, y, ldy, O, K, s, nullptr);
+    if (gemv_segn_supported(K, N)) return gemv_segn_launch(Wr, xq, y, ldy, O, K, N, s, nullptr);
     return small_n_seg_launch(Wr, xq, y, ldy, O, K, N, s, nullptr);
 }

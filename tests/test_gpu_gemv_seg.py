@@ -212,7 +212,7 @@ SEG2_SHAPES = [(1, 256), (300, 256), (37, 2304), (1000, 2048), (153, 4096), (17,
 
 
 @pytest.mark.parametrize("O,K", SEG2_SHAPES)
-@pytest.mark.parametrize("N", [2, 3, 8])
+@pytest.mark.parametrize("N", [2, 3, 4, 8])
 def test_seg_small_n_block_sums_exact(O, K, N):
     torch = torch_cuda()
     w = synth.weights(O + 3 * K, "W2", O, K)
@@ -264,12 +264,13 @@ def test_seg_small_n2_matches_two_single_calls():
     assert_within_tol(to_host(y2)[:, rows], y64, S)
 
 
-@pytest.mark.parametrize("O,K,N", [(14336, 4096, 8), (4096, 14336, 8), (1000, 2048, 3), (37, 2304, 5),
-                                   (300, 256, 4), (153, 4096, 7), (40, 32768, 6)])
+@pytest.mark.parametrize("O,K,N", [(14336, 4096, 8), (4096, 14336, 8), (1000, 2048, 5), (37, 2304, 5),
+                                   (300, 256, 6), (153, 4096, 7), (40, 32768, 6), (40, 32768, 3),
+                                   (33, 16640, 4)])
 def test_seg_small_n_mma_matches_plain_layout_kernel(O, K, N):
-    """N >= 3 on the segment layout runs the plain-layout kernel's arithmetic
-    in the same order (same chunks, same cluster split), so the two agree bit
-    for bit."""
+    """Where the segment layout takes the MMA kernel (N >= 5, or K > 16384)
+    it runs the plain-layout kernel's arithmetic in the same order (same
+    chunks, same cluster split), so the two agree bit for bit."""
     torch = torch_cuda()
     Wq = oracle.quantize_q4_0(synth.weights(O + K, "W3", O, K))
     xq = oracle.quantize_q8_0(synth.activations(O + K + N, "x3", N, K, outlier_frac=0.01), None)
@@ -281,3 +282,66 @@ def test_seg_small_n_mma_matches_plain_layout_kernel(O, K, N):
     torch.cuda.synchronize()
     assert qdg.qdg_device_status() == qdg.QDG_OK
     assert np.array_equal(to_host(ys).view(np.uint32), to_host(yp).view(np.uint32))
+
+
+# three and four vectors, K <= 16384: the dp4a kernel with one block a lane
+# (half-segments: K = 256 and 2304 have a last half of 8 blocks, 4352 a
+# whole-block-free second half, 14336 fourteen halves, 16384 sixteen)
+SEGN_SHAPES = [(1, 256), (77, 256), (37, 2304), (17, 4352), (1000, 2048), (153, 4096), (4096, 14336),
+               (14336, 4096), (300, 16384), (2500, 8192)]
+
+
+@pytest.mark.parametrize("O,K", SEGN_SHAPES)
+@pytest.mark.parametrize("N", [3, 4])
+def test_segn_block_sums_and_outputs(O, K, N):
+    """Exact block sums through the test hook, outputs within the tolerance
+    (every row up to 4096 rows, 2048 sampled rows beyond), padding of y
+    untouched, two launches bit for bit the same, and the launch counted as
+    this kernel's."""
+    torch = torch_cuda()
+    seed = 7 * O + K + N
+    Wq = oracle.quantize_q4_0(synth.weights(seed, "Wn", O, K))
+    xq = oracle.quantize_q8_0(synth.activations(seed, "xn", N, K, outlier_frac=0.01),
+                              synth.gamma(seed, "gn", K), 1e-6)
+    Wd, xd = to_dev(oracle.repack_q4_0_seg(Wq, K)), to_dev(xq)
+    isum = torch.full((N, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(Wd, xd, isum, O, K, N, 5)
+    ldy = O + 5
+    y = torch.full((N, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    y2 = torch.full((N, ldy), float("nan"), dtype=torch.float32, device="cuda")
+    before = qdg.qdg_launch_count(13)
+    qdg.q4_0s_q8_0_gemm_small_n(Wd, xd, y, ldy, O, K, N)
+    qdg.q4_0s_q8_0_gemm_small_n(Wd, xd, y2, ldy, O, K, N)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert qdg.qdg_launch_count(13) - before == 2
+    rows = None if O <= 4096 else synth.sample_indices(seed, "rowsn", O, 2048)
+    ref = oracle.block_sums(Wq if rows is None else Wq[rows], xq, K)
+    got_isum = to_host(isum) if rows is None else to_host(isum)[:, rows]
+    assert np.array_equal(got_isum, ref)
+    got = to_host(y)
+    assert np.all(np.isnan(got[:, O:]))
+    assert np.array_equal(got.view(np.uint32), to_host(y2).view(np.uint32))
+    _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
+    assert_within_tol(got[:, :O] if rows is None else got[:, rows], y64, S)
+
+
+def test_segn_unaligned_activations():
+    """A 2-byte aligned vector set (not 16-byte aligned) is read from global
+    memory instead of one bulk copy; same results bit for bit."""
+    torch = torch_cuda()
+    O, K, N = 999, 4096, 4
+    Wq = oracle.quantize_q4_0(synth.weights(5, "Wu", O, K))
+    xq = oracle.quantize_q8_0(synth.activations(5, "xu", N, K), None)
+    Wd = to_dev(oracle.repack_q4_0_seg(Wq, K))
+    xa = to_dev(xq)
+    buf = torch.zeros(xq.size + 16, dtype=torch.uint8, device="cuda")
+    buf[2:2 + xq.size] = xa.reshape(-1)
+    xu = buf[2:2 + xq.size]
+    ya = torch.empty((N, O), dtype=torch.float32, device="cuda")
+    yu = torch.empty((N, O), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemm_small_n(Wd, xa, ya, O, O, K, N)
+    qdg.q4_0s_q8_0_gemm_small_n(Wd, xu, yu, O, O, K, N)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert np.array_equal(to_host(ya).view(np.uint32), to_host(yu).view(np.uint32))
