@@ -67,15 +67,16 @@ def source_hash(*paths):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel_file: str):
+def ncu_traffic(kernel_file: str, workload: str):
     """Per-launch DRAM bytes of a kernel from the committed ncu summary, or
-    None when the summary is missing or was taken on a different source."""
+    None when the summary is missing, was taken on a different source, or on
+    another workload (the per-launch bytes belong to the captured shapes)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
-    e = d.get(kernel_file)
+    e = d.get(f"{kernel_file}:{workload}")
     if not e or e.get("source_sha") != source_hash(os.path.join("quantized_decode_gemv_rms_gb300", "csrc",
                                                                  kernel_file)):
         return None
@@ -706,7 +707,7 @@ def bench_ours(args, wl, world, rank, local):
         kernel = "gemv_chain_kernel (q4_0s_gemv_chain)"
         kern_bytes, launches = nbytes, 1
         achieved = nbytes / (ms * 1e-3) / 1e9
-        traffic = ncu_traffic("gemv_chain.cu")
+        traffic = ncu_traffic("gemv_chain.cu", wl.name)
     else:
         def main_kind(grp):
             if args.layout == "seg":
@@ -722,14 +723,15 @@ def bench_ours(args, wl, world, rank, local):
                  "fused_seg": "gemv_seg_kernel<fused> (q4_0s_gemv_rmsnorm_group)"}
         kernel = " + ".join(sorted({names[k] for k in mk.values()}))
         used = set(mk.values())
-        traffic = (ncu_traffic("gemv_seg.cu") if used == {"gemv_seg"} else
-                   ncu_traffic("gemv.cu") if used == {"gemv"} else None)
+        traffic = (ncu_traffic("gemv_seg.cu", wl.name) if used == {"gemv_seg"} else
+                   ncu_traffic("gemv.cu", wl.name) if used == {"gemv"} else None)
     roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
             "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "peak_source": ("measured: MEASURED_PEAKS.json hbm_gbs (copy bandwidth)" if peak_src == "measured"
                             else "fallback 6.8 TB/s"),
             "traffic": (traffic["dram_bytes_per_launch"] if traffic else None),
-            "traffic_source": (traffic.get("what") if traffic else "no ncu capture of this source yet"),
+            "traffic_source": (traffic.get("what") if traffic else
+                               "no ncu capture of this source on this workload"),
             "algorithmic_bytes_per_launch": round(kern_bytes / launches),
             "launches_of_this_kernel_per_step": launches,
             "achieved_over_whole_step": round(kern_bytes / (ms * 1e-3) / 1e9, 1),
