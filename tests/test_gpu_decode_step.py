@@ -89,10 +89,12 @@ def test_decode_step_full_size_sampled(step8b, expected, route):
         assert_within_tol(got[None, :], y64, S, what=f"{route}:{m.name}")
 
 
-@pytest.mark.parametrize("staging,route", [("kernel", "chain"), ("engine", "chain"), ("kernel", "fused")])
+@pytest.mark.parametrize("staging,route", [("direct", "split"), ("direct", "chain"), ("kernel", "chain"),
+                                           ("engine", "chain"), ("kernel", "fused"), ("direct", "fused")])
 def test_decode_step_from_host_buffers(step8b, expected, staging, route):
-    """The end-to-end form the benchmark times: inputs staged in from pinned
-    host memory, the step, every output staged out, in one graph with PDL;
+    """The end-to-end forms the benchmark times: inputs staged in from pinned
+    host memory, the step, every output moved out (stored straight into the
+    mapped pinned buffer by the GEMVs, or staged out), in one graph with PDL;
     the host copies of the outputs are checked against the oracle."""
     torch = torch_cuda()
     step8b.layout = "seg"
