@@ -34,8 +34,9 @@ QK = 32
 Q4_BLOCK = 18
 Q8_BLOCK = 34
 Q4K_BLOCK = 144          # one Q4_K super-block: 256 weights
+Q5K_BLOCK = 176          # one Q5_K super-block: 256 weights
 # bytes per 32 weights of each weight type
-_BYTES_PER_32 = {"q4_0": Q4_BLOCK, "q8_0": Q8_BLOCK, "q4_k": Q4K_BLOCK // 8}
+_BYTES_PER_32 = {"q4_0": Q4_BLOCK, "q8_0": Q8_BLOCK, "q4_k": Q4K_BLOCK // 8, "q5_k": Q5K_BLOCK // 8}
 
 
 def build(force: bool = False) -> str:
@@ -91,6 +92,14 @@ def lib():
             L.orc_block_sums_q4k.restype = None
             L.orc_matvec_q4k.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_i64, c_p, c_p, c_p]
             L.orc_matvec_q4k.restype = None
+            L.orc_quantize_q5_k.argtypes = [c_p, c_i64, c_i64, c_p]
+            L.orc_quantize_q5_k.restype = None
+            L.orc_dequantize_q5_k.argtypes = [c_p, c_i64, c_i64, c_p]
+            L.orc_dequantize_q5_k.restype = None
+            L.orc_block_sums_q5k.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p]
+            L.orc_block_sums_q5k.restype = None
+            L.orc_matvec_q5k.argtypes = [c_p, c_p, c_i64, c_i64, c_i64, c_p, c_i64, c_p, c_p, c_p]
+            L.orc_matvec_q5k.restype = None
             _lib = L
     return _lib
 
@@ -133,6 +142,25 @@ def dequantize_q4_k(Wq: np.ndarray, K: int) -> np.ndarray:
     assert K % 256 == 0 and Wq.shape[1] == K // 256 * Q4K_BLOCK
     out = np.empty((Wq.shape[0], K), dtype=np.float64)
     lib().orc_dequantize_q4_k(_ptr(Wq), Wq.shape[0], K, _ptr(out))
+    return out
+
+
+def quantize_q5_k(w: np.ndarray) -> np.ndarray:
+    """fp32 [O][K] -> uint8 [O][K/256*176] (Q5_K super-blocks, row-major; see oracle.c)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    O, K = w.shape
+    assert K % 256 == 0
+    out = np.empty((O, K // 256 * Q5K_BLOCK), dtype=np.uint8)
+    lib().orc_quantize_q5_k(_ptr(w), O, K, _ptr(out))
+    return out
+
+
+def dequantize_q5_k(Wq: np.ndarray, K: int) -> np.ndarray:
+    """uint8 [O][K/256*176] -> fp64 [O][K], every value d*sc*q - dmin*m exact."""
+    Wq = np.ascontiguousarray(np.atleast_2d(Wq), dtype=np.uint8)
+    assert K % 256 == 0 and Wq.shape[1] == K // 256 * Q5K_BLOCK
+    out = np.empty((Wq.shape[0], K), dtype=np.float64)
+    lib().orc_dequantize_q5_k(_ptr(Wq), Wq.shape[0], K, _ptr(out))
     return out
 
 
@@ -184,15 +212,16 @@ def quantize_q8_0(x: np.ndarray, gamma: np.ndarray | None, eps: float = 1e-6,
 
 def block_sums(Wq: np.ndarray, xq: np.ndarray, K: int, wtype: str = "q4_0") -> np.ndarray:
     """int32 [N][O][K/32] exact block sums; wtype "q4_0" (Q4_0 weights,
-    sum (q-8) qx), "q8_0" (Q8_0 weights) or "q4_k" (Q4_K weights, sum q qx per
-    32-weight sub-block)."""
+    sum (q-8) qx), "q8_0" (Q8_0 weights), "q4_k" or "q5_k" (k-quant weights,
+    sum q qx per 32-weight sub-block)."""
     Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
     xq = np.ascontiguousarray(np.atleast_2d(xq), dtype=np.uint8)
     O = Wq.shape[0]
     N = xq.shape[0]
     assert Wq.shape[1] == K // QK * _BYTES_PER_32[wtype]
     out = np.empty((N, O, K // QK), dtype=np.int32)
-    fn = {"q4_0": lib().orc_block_sums, "q8_0": lib().orc_block_sums_q8w, "q4_k": lib().orc_block_sums_q4k}[wtype]
+    fn = {"q4_0": lib().orc_block_sums, "q8_0": lib().orc_block_sums_q8w, "q4_k": lib().orc_block_sums_q4k,
+          "q5_k": lib().orc_block_sums_q5k}[wtype]
     fn(_ptr(Wq), _ptr(xq), O, K, N, _ptr(out))
     return out
 
@@ -204,7 +233,7 @@ def matvec(Wq: np.ndarray, xq: np.ndarray, K: int, rows: np.ndarray | None = Non
     ``rows`` restricts the evaluation to the given row indices of Wq (R of
     them); otherwise all O rows.  ``threads`` > 1 splits rows over Python
     threads (the C call releases the GIL); results do not depend on it.
-    ``wtype`` "q4_0" (Q4_0 weights), "q8_0" (Q8_0 weights) or "q4_k" (Q4_K).
+    ``wtype`` "q4_0" (Q4_0 weights), "q8_0" (Q8_0 weights), "q4_k" (Q4_K) or "q5_k" (Q5_K).
     """
     Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
     xq = np.ascontiguousarray(np.atleast_2d(xq), dtype=np.uint8)
@@ -219,7 +248,7 @@ def matvec(Wq: np.ndarray, xq: np.ndarray, K: int, rows: np.ndarray | None = Non
     S = np.empty((N, R), dtype=np.float64)
     L = lib()
     assert Wq.shape[1] == K // QK * _BYTES_PER_32[wtype]
-    mv = {"q4_0": L.orc_matvec, "q8_0": L.orc_matvec_q8w, "q4_k": L.orc_matvec_q4k}[wtype]
+    mv = {"q4_0": L.orc_matvec, "q8_0": L.orc_matvec_q8w, "q4_k": L.orc_matvec_q4k, "q5_k": L.orc_matvec_q5k}[wtype]
 
     def run(lo, hi):
         if hi <= lo:

@@ -611,3 +611,154 @@ void orc_matvec_q4k(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, i
         }
     }
 }
+
+/* ---------------------------------------------------------------------- */
+/* Q5_K weights.  The pages name Q5_K beside Q4_K (the GPU MoE tests compare */
+/* Q4_K/Q5_K results [llama.cpp b10981: OpenVINO backend optimises stateful */
+/* decode and GPU MoE inference, section "GPU MoE, env vars"]) but give no  */
+/* format.  The library reads it as GGML's 5-bit k-quant super-block of 256  */
+/* weights (8 sub-blocks of 32), 176 bytes:                                 */
+/*   bytes 0-15    as in Q4_K: fp16 d, fp16 dmin, the twelve bytes of 6-bit  */
+/*                 scales sc_j and mins m_j (same packing);                 */
+/*   bytes 16-47   qh[0..31]: bit j of qh[i] is the top bit (value 16) of    */
+/*                 element i of sub-block j;                                */
+/*   bytes 48-175  the low four bits, placed as the Q4_K codes: byte         */
+/*                 48 + 32p + i holds element i of sub-block 2p in its low   */
+/*                 nibble and element i of sub-block 2p+1 in its high one.   */
+/*   Element i of sub-block j = d * sc_j * q - dmin * m_j, q in 0..31.       */
+/* ---------------------------------------------------------------------- */
+static int q5k_code(const uint8_t* blk, int e)
+{
+    int sub = e / 32, i = e % 32;
+    uint8_t low4 = blk[48 + 32 * (sub / 2) + i];
+    int lo = (sub % 2 == 0) ? (low4 & 0x0F) : (low4 >> 4);
+    return lo + 16 * ((blk[16 + i] >> sub) & 1);
+}
+
+/* Q5_K quantization: the Q4_K recipe above with 31 code steps per sub-block */
+/* (a_j = (hi + mn_j) / 31; q clamped to 0..31), every step one fp32         */
+/* operation.                                                               */
+void orc_quantize_q5_k(const float* w, int64_t rows, int64_t K, uint8_t* out)
+{
+    const int64_t nsb = K / 256;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const float* v = w + r * K + sb * 256;
+            uint8_t* blk = out + (r * nsb + sb) * 176;
+            float step5[8], off5[8], a5[8], mn5[8], amax5 = 0.0f, mnmax5 = 0.0f;
+            for (int j = 0; j < 8; ++j) {
+                float lo = v[32 * j], hi = v[32 * j];
+                for (int i = 1; i < 32; ++i) {
+                    if (v[32 * j + i] < lo) lo = v[32 * j + i];
+                    if (v[32 * j + i] > hi) hi = v[32 * j + i];
+                }
+                mn5[j] = lo < 0.0f ? -lo : 0.0f;
+                a5[j] = (hi + mn5[j]) / 31.0f;
+                if (a5[j] > amax5) amax5 = a5[j];
+                if (mn5[j] > mnmax5) mnmax5 = mn5[j];
+            }
+            uint16_t dh = orc_f32_to_f16(amax5 / 63.0f), dmh = orc_f32_to_f16(mnmax5 / 63.0f);
+            float dd = orc_f16_to_f32(dh), ddm = orc_f16_to_f32(dmh);
+            int sc5[8], m5[8];
+            for (int j = 0; j < 8; ++j) {
+                sc5[j] = dd > 0.0f ? round_half_away_clamp(a5[j] / dd, 0, 63) : 0;
+                m5[j] = ddm > 0.0f ? round_half_away_clamp(mn5[j] / ddm, 0, 63) : 0;
+                step5[j] = dd * (float)sc5[j];
+                off5[j] = ddm * (float)m5[j];
+            }
+            memset(blk, 0, 176);
+            wr_u16(blk, dh);
+            wr_u16(blk + 2, dmh);
+            uint8_t* s = blk + 4;
+            for (int j = 0; j < 4; ++j) {
+                s[j] = (uint8_t)((sc5[j] & 63) | ((sc5[j + 4] >> 4) << 6));
+                s[j + 4] = (uint8_t)((m5[j] & 63) | ((m5[j + 4] >> 4) << 6));
+                s[j + 8] = (uint8_t)((sc5[j + 4] & 15) | ((m5[j + 4] & 15) << 4));
+            }
+            for (int j = 0; j < 8; ++j) {
+                for (int i = 0; i < 32; ++i) {
+                    int q5 = 0;
+                    if (step5[j] > 0.0f)
+                        q5 = round_half_away_clamp((v[32 * j + i] + off5[j]) / step5[j], 0, 31);
+                    uint8_t* low = blk + 48 + 32 * (j / 2) + i;
+                    *low = (uint8_t)((j % 2 == 0) ? ((*low & 0xF0) | (q5 & 15)) : ((*low & 0x0F) | ((q5 & 15) << 4)));
+                    blk[16 + i] = (uint8_t)(blk[16 + i] | ((q5 >> 4) << j));
+                }
+            }
+        }
+    }
+}
+
+/* Dequantized Q5_K weights in fp64 (exact there). */
+void orc_dequantize_q5_k(const uint8_t* W, int64_t rows, int64_t K, double* out)
+{
+    const int64_t nsb = K / 256;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const uint8_t* blk = W + (r * nsb + sb) * 176;
+            const double dd = (double)orc_f16_to_f32(rd_u16(blk));
+            const double ddmin = (double)orc_f16_to_f32(rd_u16(blk + 2));
+            for (int e = 0; e < 256; ++e) {
+                int scale, mins;
+                q4k_scale_min(blk, e / 32, &scale, &mins);
+                out[r * K + sb * 256 + e] = dd * (double)scale * (double)q5k_code(blk, e) - ddmin * (double)mins;
+            }
+        }
+}
+
+/* Exact integer sums per 32-weight sub-block: sum_i q_i * qx_i (codes      */
+/* 0..31 times int8).                                                        */
+void orc_block_sums_q5k(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64_t N, int32_t* isum)
+{
+    const int64_t nb = K / QK, nsb = K / 256;
+    for (int64_t n = 0; n < N; ++n)
+        for (int64_t o = 0; o < O; ++o)
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* sblk = W + (o * nsb + b / 8) * 176;
+                const uint8_t* xblk = xq + (n * nb + b) * 34;
+                int32_t total = 0;
+                for (int i = 0; i < QK; ++i)
+                    total += q5k_code(sblk, (int)(b % 8) * 32 + i) * (int32_t)(int8_t)xblk[2 + i];
+                isum[(n * O + o) * nb + b] = total;
+            }
+}
+
+/* Reference product for Q5_K weights, as orc_matvec_q4k: fp64 dot product  */
+/* of the dequantized operands; S = sum over sub-blocks of                  */
+/* |d_x d sc isum| + |d_x dmin m xsum|.                                      */
+void orc_matvec_q5k(const uint8_t* W, const uint8_t* xq, int64_t O, int64_t K, int64_t N,
+                    const int64_t* rows, int64_t nrows, float* y32, double* y64, double* S)
+{
+    const int64_t nb = K / QK, nsb = K / 256;
+    if (!rows)
+        nrows = O;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t t = 0; t < nrows; ++t) {
+            int64_t o = rows ? rows[t] : t;
+            double total = 0.0, bound = 0.0;
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t* sblk = W + (o * nsb + b / 8) * 176;
+                const uint8_t* xblk = xq + (n * nb + b) * 34;
+                const double dd = (double)orc_f16_to_f32(rd_u16(sblk));
+                const double ddmin = (double)orc_f16_to_f32(rd_u16(sblk + 2));
+                const double dx = (double)orc_f16_to_f32(rd_u16(xblk));
+                int scale, mins;
+                q4k_scale_min(sblk, (int)(b % 8), &scale, &mins);
+                double part = 0.0;
+                int64_t qsum = 0, xsum = 0;
+                for (int i = 0; i < QK; ++i) {
+                    const int q5 = q5k_code(sblk, (int)(b % 8) * 32 + i);
+                    const int qx = (int8_t)xblk[2 + i];
+                    part += (dd * (double)scale * (double)q5 - ddmin * (double)mins) * (dx * (double)qx);
+                    qsum += (int64_t)q5 * qx;
+                    xsum += qx;
+                }
+                total += part;
+                bound += fabs(dx * dd * (double)scale * (double)qsum) + fabs(dx * ddmin * (double)mins * (double)xsum);
+            }
+            if (y32) y32[n * nrows + t] = (float)total;
+            if (y64) y64[n * nrows + t] = total;
+            if (S) S[n * nrows + t] = bound;
+        }
+    }
+}

@@ -47,6 +47,20 @@ MUTATIONS = {
     "q4k_product_min_dropped": ("double wv = d * (double)sc * (double)q - dmin * (double)m;",
                                 "double wv = d * (double)sc * (double)q;"),
     "q4k_code_group_stride": ("uint8_t byte = blk[16 + 32 * (j / 2) + i];", "uint8_t byte = blk[16 + 16 * j + i];"),
+    "q5k_top_bit_dropped": ("return lo + 16 * ((blk[16 + i] >> sub) & 1);", "return lo;"),
+    "q5k_top_bit_of_pair": ("return lo + 16 * ((blk[16 + i] >> sub) & 1);",
+                            "return lo + 16 * ((blk[16 + i] >> (sub / 2)) & 1);"),
+    "q5k_top_bit_weight_32": ("return lo + 16 * ((blk[16 + i] >> sub) & 1);",
+                              "return lo + 32 * ((blk[16 + i] >> sub) & 1);"),
+    "q5k_low_nibbles_swapped": ("int lo = (sub % 2 == 0) ? (low4 & 0x0F) : (low4 >> 4);",
+                                "int lo = (sub % 2 == 0) ? (low4 >> 4) : (low4 & 0x0F);"),
+    "q5k_codes_at_q4k_offset": ("uint8_t low4 = blk[48 + 32 * (sub / 2) + i];",
+                                "uint8_t low4 = blk[16 + 32 * (sub / 2) + i];"),
+    "q5k_quantizer_15_steps": ("a5[j] = (hi + mn5[j]) / 31.0f;", "a5[j] = (hi + mn5[j]) / 15.0f;"),
+    "q5k_quantizer_top_bit_misplaced": ("blk[16 + i] = (uint8_t)(blk[16 + i] | ((q5 >> 4) << j));",
+                                        "blk[16 + i] = (uint8_t)(blk[16 + i] | ((q5 >> 4) << (7 - j)));"),
+    "q5k_min_added": ("out[r * K + sb * 256 + e] = dd * (double)scale * (double)q5k_code(blk, e) - ddmin * (double)mins;",
+                      "out[r * K + sb * 256 + e] = dd * (double)scale * (double)q5k_code(blk, e) + ddmin * (double)mins;"),
 }
 
 

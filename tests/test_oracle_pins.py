@@ -611,3 +611,97 @@ def test_q4k_matvec_vs_numpy_dequant(orc):
     ref = xv @ orc.dequantize_q4_k(W, K).T
     _, y64, S = orc.matvec(W, x, K, wtype="q4_k")
     assert np.all(np.abs(y64 - ref) <= 1e-12 * (S + 1e-30))
+
+
+# ---------------------------------------------------------------- Q5_K weights
+def _q5k_golden_block(g):
+    """The hand-derived Q5_K super-block: header bytes from the golden file,
+    codes by its rule, low four bits placed as the Q4_K codes from byte 48,
+    top bits in qh (bit j of byte 16 + i for element i of sub-block j)."""
+    blk = np.zeros(176, dtype=np.uint8)
+    blk[0], blk[1] = g["d_bits"] & 0xFF, g["d_bits"] >> 8
+    blk[2], blk[3] = g["dmin_bits"] & 0xFF, g["dmin_bits"] >> 8
+    blk[4:16] = g["scales_bytes"]
+    for j in range(8):
+        for i in range(32):
+            q = (i + 3 * j) % 32
+            b = 48 + 32 * (j // 2) + i
+            blk[b] |= np.uint8((q & 15) if j % 2 == 0 else (q & 15) << 4)
+            blk[16 + i] |= np.uint8((q >> 4) << j)
+    return blk
+
+
+def _q5k_codes(Wrow):
+    """Codes of one Q5_K super-block by the documented placement (Python)."""
+    qh, low = Wrow[16:48], Wrow[48:176]
+    out = np.zeros(256, dtype=np.int64)
+    for j in range(8):
+        for i in range(32):
+            byte = int(low[32 * (j // 2) + i])
+            lo = byte & 15 if j % 2 == 0 else byte >> 4
+            out[32 * j + i] = lo + 16 * ((int(qh[i]) >> j) & 1)
+    return out
+
+
+def test_q5k_golden(orc):
+    g = golden()["q5k_superblock"]
+    blk = _q5k_golden_block(g)
+    for k, v in g["spot_bytes"].items():
+        assert int(blk[int(k)]) == v, k
+    deq = orc.dequantize_q5_k(blk[None, :], 256)[0]
+    for k, v in g["spot_values"].items():
+        assert deq[int(k)] == v, k
+    for j in range(8):
+        for i in range(32):
+            assert deq[32 * j + i] == 0.5 * g["sc"][j] * ((i + 3 * j) % 32) - 0.25 * g["m"][j], (j, i)
+    x = _ones_q8(8, g["x_d_bits"])
+    isum = orc.block_sums(blk[None, :], x, 256, wtype="q5_k")
+    assert np.all(isum == g["isum_each"])
+    y32, y64, S = orc.matvec(blk[None, :], x, 256, wtype="q5_k")
+    assert y64[0, 0] == g["y"] and y32[0, 0] == np.float32(g["y"]) and S[0, 0] == g["S"]
+
+
+def test_q5k_quantizer_special_blocks(orc):
+    w = np.zeros((3, 256), dtype=np.float32)
+    w[1, :] = 0.75                                     # one positive constant
+    w[2, :] = np.tile(np.arange(32) * 0.25 - 1.0, 8)  # codes 0..31 on an exact grid
+    Wq = orc.quantize_q5_k(w)
+    deq = orc.dequantize_q5_k(Wq, 256)
+    assert np.all(Wq[0] == 0) and np.all(deq[0] == 0.0)       # zero block: everything zero
+    assert np.all(np.abs(deq[1] - 0.75) <= 0.75 * 2.0 ** -8)   # within the fp16 scale's rounding
+    assert np.array_equal(_q5k_codes(Wq[2]), np.tile(np.arange(32), 8))
+    assert np.max(np.abs(deq[2] - w[2])) <= 4e-3
+
+
+def test_q5k_quantizer_roundtrip_random(orc):
+    rng = np.random.default_rng(13)
+    w = (rng.standard_normal((24, 1024)) * 0.02).astype(np.float32)
+    Wq = orc.quantize_q5_k(w)
+    deq = orc.dequantize_q5_k(Wq, 1024)
+    err = np.abs(deq - w).reshape(24, 32, 32).max(axis=2)
+    rng_ = (w.reshape(24, 32, 32).max(axis=2) - np.minimum(w.reshape(24, 32, 32).min(axis=2), 0))
+    assert np.all(err <= 0.75 * rng_ / 31 + 1e-7)      # within three quarters of a code step
+    # the codes the bytes hold are the ones the dequantizer used
+    for r in range(3):
+        codes = _q5k_codes(Wq[r, :176])
+        assert codes.max() <= 31 and codes.min() >= 0
+
+
+def test_q5k_matvec_vs_numpy_dequant(orc):
+    rng = np.random.default_rng(14)
+    K = 512
+    W = orc.quantize_q5_k((rng.standard_normal((5, K)) * 0.02).astype(np.float32))
+    x = orc.quantize_q8_0(rng.standard_normal((2, K)).astype(np.float32), None)
+    qx = x.reshape(2, K // 32, 34)
+    dx = qx[:, :, :2].copy().view(np.float16).astype(np.float64)[:, :, 0]
+    xv = (qx[:, :, 2:].view(np.int8).astype(np.float64) * dx[:, :, None]).reshape(2, K)
+    ref = xv @ orc.dequantize_q5_k(W, K).T
+    _, y64, S = orc.matvec(W, x, K, wtype="q5_k")
+    assert np.all(np.abs(y64 - ref) <= 1e-12 * (S + 1e-30))
+    # exact block sums against a Python restatement of the code placement
+    isum = orc.block_sums(W, x, K, wtype="q5_k")
+    qxi = qx[:, :, 2:].view(np.int8).astype(np.int64)
+    for o in range(5):
+        codes = np.concatenate([_q5k_codes(W[o, 176 * s:176 * (s + 1)]) for s in range(K // 256)])
+        ref_sums = (codes.reshape(K // 32, 32)[None] * qxi).sum(axis=2)
+        assert np.array_equal(isum[:, o, :], ref_sums)
