@@ -937,30 +937,34 @@ def bench_extras(args, device):
         xq = torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
         us = timed_graph(lambda i: qdg.qnorm_quantize_q8_0(x, g, 1e-6, xq), 20)
         out["qnorm"][f"K{K}{'_norm' if norm else '_plain'}"] = {"us": round(us, 2)}
-    # Q4_K weights (batch-1 GEMV): the same shapes, quantized on the GPU at
-    # load time, rotating weight copies
-    out["q4_k_weights"] = {}
-    for (O, K) in (workloads.SMALL_N_SHAPES if args.only in (None, "q4k") else ()):
-        W4 = torch.empty(O * (K // 256) * 144, dtype=torch.uint8, device=device)
-        for r in range(0, O, 8192):
-            r1 = min(O, r + 8192)
-            w = torch.from_numpy(synth.weights(workloads.SMALL_N_SEED, f"q4k-{O}x{K}", O, K, row_begin=r,
-                                               row_end=r1)).to(device)
-            qdg.quantize_q4_k(w, W4[r * (K // 256) * 144:r1 * (K // 256) * 144], O=r1 - r, K=K)
-            del w
-        copies = max(2, -(-3 * l2 // W4.numel()))
-        Ws = [W4] + [W4.clone() for _ in range(copies - 1)]
-        x = torch.from_numpy(synth.activations(workloads.SMALL_N_SEED, f"q4k-x-{K}", 1, K)).to(device)
-        xq = torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
-        qdg.qnorm_quantize_q8_0(x, None, 0.0, xq)
-        y = torch.empty(O, dtype=torch.float32, device=device)
-        us = timed_graph(lambda i: qdg.q4_k_q8_0_gemv(Ws[i % copies], xq, y, O, K), copies)
-        nbytes = O * (K // 256) * 144 + (K // 32) * 34 + 4 * O
-        out["q4_k_weights"][f"{O}x{K}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
-                                           "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
-                                           "weight_copies": copies}
-        del Ws, W4
-        torch.cuda.empty_cache()
+    # k-quant weights (batch-1 GEMV): Q4_K (144-byte super-blocks) and Q5_K
+    # (176-byte), the same shapes, quantized on the GPU at load time,
+    # rotating weight copies
+    kquants = (("q4k", "q4_k_weights", 144, qdg.quantize_q4_k, qdg.q4_k_q8_0_gemv),
+               ("q5k", "q5_k_weights", 176, qdg.quantize_q5_k, qdg.q5_k_q8_0_gemv))
+    for tag, key, sb, quantize, gemv in kquants:
+        out[key] = {}
+        for (O, K) in (workloads.SMALL_N_SHAPES if args.only in (None, tag) else ()):
+            Wk = torch.empty(O * (K // 256) * sb, dtype=torch.uint8, device=device)
+            for r in range(0, O, 8192):
+                r1 = min(O, r + 8192)
+                w = torch.from_numpy(synth.weights(workloads.SMALL_N_SEED, f"{tag}-{O}x{K}", O, K, row_begin=r,
+                                                   row_end=r1)).to(device)
+                quantize(w, Wk[r * (K // 256) * sb:r1 * (K // 256) * sb], O=r1 - r, K=K)
+                del w
+            copies = max(2, -(-3 * l2 // Wk.numel()))
+            Ws = [Wk] + [Wk.clone() for _ in range(copies - 1)]
+            x = torch.from_numpy(synth.activations(workloads.SMALL_N_SEED, f"{tag}-x-{K}", 1, K)).to(device)
+            xq = torch.empty(qdg.q8_0_nbytes(1, K), dtype=torch.uint8, device=device)
+            qdg.qnorm_quantize_q8_0(x, None, 0.0, xq)
+            y = torch.empty(O, dtype=torch.float32, device=device)
+            us = timed_graph(lambda i: gemv(Ws[i % copies], xq, y, O, K), copies)
+            nbytes = O * (K // 256) * sb + (K // 32) * 34 + 4 * O
+            out[key][f"{O}x{K}"] = {"us": round(us, 2), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+                                    "frac": round(nbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"], 4),
+                                    "weight_copies": copies}
+            del Ws, Wk
+            torch.cuda.empty_cache()
     out["peak_note"] = ("small-N against the measured HBM copy bandwidth; prefill against the measured dense "
                         "bf16 burst peak (the fp16 tensor rate is the same nominal 2.25 PFLOP/s)")
     torch.cuda.synchronize()
@@ -1013,7 +1017,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the small-N and prefill timings")
-    ap.add_argument("--only", choices=["small_n", "prefill", "q8w", "q4k", "qnorm"], default=None,
+    ap.add_argument("--only", choices=["small_n", "prefill", "q8w", "q4k", "q5k", "qnorm"], default=None,
                     help="time only that product (one JSON object with its numbers)")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -1040,11 +1044,11 @@ def main():
         print(json.dumps(line))
         return
 
-    if args.only in ("small_n", "prefill", "q8w", "q4k", "qnorm"):
+    if args.only in ("small_n", "prefill", "q8w", "q4k", "q5k", "qnorm"):
         import torch
         torch.cuda.set_device(local)
         ex = bench_extras(args, torch.device("cuda", local))
-        key = {"q8w": "q8_0_weights", "q4k": "q4_k_weights"}.get(args.only, args.only)
+        key = {"q8w": "q8_0_weights", "q4k": "q4_k_weights", "q5k": "q5_k_weights"}.get(args.only, args.only)
         if rank == 0:
             print(json.dumps({"only": args.only, key: ex[key]}))
         return

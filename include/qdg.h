@@ -327,6 +327,42 @@ QDG_API int q4_k_q8_0_gemv_group(const void* const* W, float* const* y, const in
                                  const void* xq, int64_t K, qdg_stream_t stream);
 
 /*
+ * quantize_q5_k -- weight preparation: fp32 [O][ldw] -> Q5_K [O][K/256]
+ * super-blocks (format under q5_k_q8_0_gemv below).  The steps of
+ * quantize_q4_k with 31 code steps per sub-block: a_j = (max w + mn_j) / 31,
+ * q = round((w + dmin m_j) / (d sc_j)) clamped to 0..31; each step one IEEE
+ * fp32 operation.  Load time.  K multiple of 256, ldw >= K; w and Wq 4-byte
+ * aligned.
+ */
+QDG_API int quantize_q5_k(const float* w, int64_t ldw, int64_t O, int64_t K, void* Wq,
+                          qdg_stream_t stream);
+
+/*
+ * q5_k_q8_0_gemv -- y = W * x with Q5_K weights, the 5-bit k-quant the pages
+ * name beside Q4_K [llama.cpp b10981: OpenVINO backend optimises stateful
+ * decode and GPU MoE inference, section "GPU MoE, env vars"].  No format on
+ * the pages; the library reads Q5_K as GGML's 256-weight super-block of 176
+ * bytes: bytes 0-15 as Q4_K (fp16 d, fp16 dmin, the twelve packed bytes of
+ * 6-bit scales sc_j and mins m_j), bytes 16-47 qh[0..31] (bit j of qh[i] is
+ * the top bit, value 16, of element i of sub-block j), bytes 48-175 the low
+ * four bits placed as the Q4_K codes (byte 48 + 32p + i: element i of
+ * sub-block 2p in the low nibble, of 2p+1 in the high nibble).  Weight =
+ * d sc_j q - dmin m_j, q in 0..31.  W [O][K/256 * 176 bytes], 16-byte
+ * aligned; xq [K/32] Q8_0, 2-byte aligned; y [O] fp32.  K multiple of 256,
+ * <= 32768; 1 <= O < 2^31.  Exact sub-block sums isum = sum q q_x and
+ * xsum = sum q_x, then d_x (d sc isum - dmin m xsum) in fp32 (tolerance as
+ * q4_k_q8_0_gemv).  Deterministic.  5.5 bits per weight; the kernel of
+ * q4_k_q8_0_gemv with each lane also loading its super-block's qh bytes.
+ */
+QDG_API int q5_k_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K,
+                           qdg_stream_t stream);
+
+/* q5_k_q8_0_gemv for up to 4 Q5_K matrices reading one Q8_0 vector, in one
+ * launch (argument rules as q4_0_q8_0_gemv_group). */
+QDG_API int q5_k_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                 const void* xq, int64_t K, qdg_stream_t stream);
+
+/*
  * Segment layout of Q4_0 weights (load-time repack).  GGML's CPU back end
  * rearranges Q4 weights once, when they are loaded, for its own kernels
  * [GGML: Backend abstraction and hardware acceleration, section "How build
@@ -510,7 +546,7 @@ QDG_API int qdg_stage_copy(void* dst, const void* src, int64_t bytes, qdg_stream
  * 4 weight quantize, 5 fused norm+gemv, 6 segment-layout gemv, 7 repack,
  * 8 Q8_0-weight gemv, 9 fused norm+gemv on the segment layout, 10 staging copy,
  * 11 decode-step chain, 12 Q4_K-weight gemv, 13 three/four-vector segment-layout
- * small-N, -1 total.  Lets a caller check
+ * small-N, 14 Q5_K-weight gemv, -1 total.  Lets a caller check
  * that the fused kernel is the one that ran.
  */
 QDG_API int64_t qdg_launch_count(int which);
@@ -523,7 +559,8 @@ QDG_API int64_t qdg_launch_count(int which);
  * 3 = segment-layout gemv (W in the segment layout, N must be 1),
  * 4 = Q8_0-weight gemv (W in Q8_0 blocks, N must be 1), 5 = segment-layout
  * small-N (W in the segment layout, N = 1..8), 6 = Q4_K-weight gemv (W in
- * Q4_K super-blocks, N must be 1; isum = sum q q_x per 32-weight sub-block).
+ * Q4_K super-blocks, N must be 1; isum = sum q q_x per 32-weight sub-block),
+ * 7 = Q5_K-weight gemv (W in Q5_K super-blocks, N must be 1; isum as for 6).
  * Same argument rules as the corresponding entry point.
  */
 QDG_API int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum, int64_t O,

@@ -15,7 +15,7 @@ namespace {
 std::mutex g_dev_mutex;
 DeviceInfo g_dev_cache[64];
 std::atomic<int> g_pdl{0};
-std::atomic<int64_t> g_counts[14];
+std::atomic<int64_t> g_counts[15];
 }  // namespace
 
 DeviceInfo device_info() {
@@ -100,7 +100,7 @@ extern "C" int64_t qdg_launch_count(int which) {
         for (auto& c : g_counts) t += c.load();
         return t;
     }
-    if (which < 0 || which >= 14) return -1;
+    if (which < 0 || which >= 15) return -1;
     return g_counts[which].load();
 }
 
@@ -171,6 +171,9 @@ extern "C" int qdg_debug_block_sums(const void* W, const void* xq, int32_t* isum
         case 6:
             if (N != 1) return QDG_EINVAL;
             return gemv_q4k_launch(W, xq, nullptr, O, K, s, isum);
+        case 7:
+            if (N != 1) return QDG_EINVAL;
+            return gemv_q5k_launch(W, xq, nullptr, O, K, s, isum);
         case 5:
             if (N == 1) return gemv_seg_launch(W, xq, nullptr, O, K, s, isum);
             if (N == 2) return gemv_seg2_launch(W, xq, nullptr, O, O, K, s, isum);

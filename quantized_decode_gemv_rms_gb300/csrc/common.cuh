@@ -241,6 +241,8 @@ int gemv_q8w_launch(const void* W, const void* xq, float* y, int64_t O, int64_t 
                     int32_t* dbg);
 int gemv_q4k_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
                     int32_t* dbg);
+int gemv_q5k_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
+                    int32_t* dbg);
 int gemv_seg2_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t O, int64_t K,
                      cudaStream_t stream, int32_t* dbg);
 int gemv_seg_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,

@@ -23,6 +23,16 @@
 //     from the header, d_x (d sc isum - dmin m xsum) in fp32; the ring's
 //     four rows share one transposed warp butterfly; segment partials are
 //     combined per row in a fixed order (deterministic).
+//
+// Q5_K weights (the 5-bit k-quant beside Q4_K [llama.cpp b10981: OpenVINO
+// backend optimises stateful decode and GPU MoE inference, section "GPU MoE,
+// env vars"]; the library reads it as GGML's 176-byte super-block: the Q4_K
+// header, 32 bytes qh with bit j of qh[i] the top bit (16) of element i of
+// sub-block j, then the low four bits placed as the Q4_K codes) take the
+// same kernel with kQ5: a segment is 8 super-blocks of 176 bytes, a lane
+// also loads the 32 qh bytes (shared with the three other lanes of its
+// super-block) and merges bits 2g and 2g+1 of each byte into its codes
+// before the dp4a, so that q runs over 0..31.
 #include "common.cuh"
 
 #include <algorithm>
@@ -36,7 +46,6 @@ namespace {
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kDepth = 4;                   // row-segments in flight per warp
-constexpr int kSegBytes = 1152;             // 8 super-blocks of 144 bytes
 constexpr int kPartFloats = 3072;
 constexpr int kMaxGroup = 4;
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
@@ -50,11 +59,15 @@ struct Plan {
     int rch;        // rows per chunk of partial sums, a multiple of nslots
 };
 
-Plan make_plan(int64_t K) {
+// bytes of one super-block: Q4_K 144, Q5_K 176
+template <bool kQ5>
+constexpr int kSuper = kQ5 ? 176 : 144;
+
+Plan make_plan(int64_t K, int sb_bytes) {
     Plan p{};
     const int nsb = static_cast<int>(K / 256);
     p.nb = static_cast<int>(K / 32);
-    p.rowbytes = nsb * 144;
+    p.rowbytes = nsb * sb_bytes;
     p.nseg = (nsb + 7) / 8;
     p.slast = nsb - 8 * (p.nseg - 1);
     p.nslots = kWarps / p.nseg;
@@ -72,7 +85,8 @@ __device__ __forceinline__ uint4 ldg_stream16(const uint8_t* p) {
 
 struct Entry {
     uint4 h;        // d | dmin << 16, then the twelve scale bytes
-    uint4 c0, c1;   // the pair's 32 code bytes
+    uint4 c0, c1;   // the pair's 32 code bytes (Q5_K: their low four bits)
+    uint4 q0, q1;   // Q5_K: the super-block's 32 qh bytes (unused for Q4_K)
 };
 
 struct Args {
@@ -99,8 +113,11 @@ __device__ __forceinline__ void load_act(const uint8_t* xq, int b, uint32_t* x, 
     }
 }
 
-template <bool kDebug>
-__global__ void __maxnreg__(96) gemv_q4k_kernel(const __grid_constant__ Args a, const __grid_constant__ Plan plan) {
+// Q4_K: 96 registers a thread (a quantize CTA fits beside it on the decode
+// step); Q5_K: 128, for its 80-byte ring entries.
+template <bool kQ5, bool kDebug>
+__global__ void __maxnreg__(kQ5 ? 128 : 96) gemv_q4k_kernel(const __grid_constant__ Args a,
+                                                            const __grid_constant__ Plan plan) {
     __shared__ float part[kPartFloats];
     __shared__ uint64_t xbar;
     extern __shared__ __align__(16) uint8_t xs[];   // the Q8_0 vector when a.xq_bulk
@@ -114,7 +131,7 @@ __global__ void __maxnreg__(96) gemv_q4k_kernel(const __grid_constant__ Args a, 
     const int nsb_here = (seg == nseg - 1) ? plan.slast : 8;
     const bool has = worker && (lane >> 2) < nsb_here;
     const int g = lane & 3;                                  // sub-blocks 2g, 2g+1 of the super-block
-    const int hdr_off = seg * kSegBytes + (lane >> 2) * 144;
+    const int hdr_off = (seg * 8 + (lane >> 2)) * kSuper<kQ5>;
     const int p = seg * 32 + lane;                           // Q8_0 blocks 2p, 2p+1
 
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * O / gridDim.x;
@@ -137,8 +154,13 @@ __global__ void __maxnreg__(96) gemv_q4k_kernel(const __grid_constant__ Args a, 
         if (has) {
             const uint8_t* sb = a.Wg[m] + (row - a.start[m]) * plan.rowbytes + hdr_off;
             e.h = ldg_stream16(sb);
-            e.c0 = ldg_stream16(sb + 16 + 32 * g);
-            e.c1 = ldg_stream16(sb + 32 + 32 * g);
+            if (kQ5) {
+                e.q0 = ldg_stream16(sb + 16);
+                e.q1 = ldg_stream16(sb + 32);
+            }
+            constexpr int kCodes = kQ5 ? 48 : 16;
+            e.c0 = ldg_stream16(sb + kCodes + 32 * g);
+            e.c1 = ldg_stream16(sb + kCodes + 16 + 32 * g);
         }
     };
     auto fill = [&](int64_t c0, int crows) {
@@ -183,18 +205,26 @@ __global__ void __maxnreg__(96) gemv_q4k_kernel(const __grid_constant__ Args a, 
     auto consume = [&](int64_t c0, int crows, int ri, Entry& entry) -> float {
         const Entry& e = entry;
         const uint32_t cw[8] = {e.c0.x, e.c0.y, e.c0.z, e.c0.w, e.c1.x, e.c1.y, e.c1.z, e.c1.w};
+        const uint32_t qh[8] = {e.q0.x, e.q0.y, e.q0.z, e.q0.w, e.q1.x, e.q1.y, e.q1.z, e.q1.w};
         int ia = 0, ib = 0;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            ia = __dp4a(static_cast<int>(cw[i] & kNibbles), static_cast<int>(xa[i]), ia);
-            ib = __dp4a(static_cast<int>((cw[i] >> 4) & kNibbles), static_cast<int>(xb[i]), ib);
+            uint32_t ca = cw[i] & kNibbles, cb = (cw[i] >> 4) & kNibbles;
+            if (kQ5) {
+                // top bits of sub-blocks 2g (bit 2g of each qh byte) and 2g+1
+                const uint32_t t = qh[i] >> (2 * g);
+                ca |= (t & 0x01010101u) << 4;
+                cb |= (t & 0x02020202u) << 3;
+            }
+            ia = __dp4a(static_cast<int>(ca), static_cast<int>(xa[i]), ia);
+            ib = __dp4a(static_cast<int>(cb), static_cast<int>(xb[i]), ib);
         }
         const uint32_t P1 = __byte_perm(e.h.y, 0, sel) & 0xFFFFu;
         const uint32_t P2 = __byte_perm(e.h.z, 0, sel) & 0xFFFFu;
         const uint32_t P3 = __byte_perm(e.h.w, 0, sel) & 0xFFFFu;
         const uint32_t SC = high ? ((P3 & 0x0F0Fu) | ((P1 >> 2) & 0x3030u)) : (P1 & 0x3F3Fu);
         const uint32_t MN = high ? (((P3 >> 4) & 0x0F0Fu) | ((P2 >> 2) & 0x3030u)) : (P2 & 0x3F3Fu);
-        // integer products first (sc isum < 2^22, m xsum < 2^18: exact), then
+        // integer products first (sc isum < 2^23, m xsum < 2^18: exact), then
         // one rounding each against the fp16 d and dmin
         const float d = half_bits_to_float(e.h.x), dmin = half_bits_to_float(e.h.x >> 16);
         const float ta = __fmaf_rn(d, static_cast<float>(static_cast<int>(SC & 0xFFu) * ia),
@@ -258,10 +288,9 @@ __global__ void __maxnreg__(96) gemv_q4k_kernel(const __grid_constant__ Args a, 
     }
 }
 
-}  // namespace
-
-int gemv_q4k_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq,
-                          int64_t K, cudaStream_t stream, int32_t* dbg) {
+template <bool kQ5>
+int kquant_launch_group(const void* const* W, float* const* y, const int64_t* O, int count, const void* xq,
+                        int64_t K, cudaStream_t stream, int32_t* dbg) {
     if (!W || !O || !xq || (!y && !dbg)) return QDG_EINVAL;
     if (count < 1 || count > kMaxGroup || K <= 0) return QDG_EINVAL;
     if (dbg && count != 1) return QDG_EINVAL;
@@ -280,7 +309,7 @@ int gemv_q4k_launch_group(const void* const* W, float* const* y, const int64_t* 
     if (total >= (int64_t(1) << 31)) return QDG_ESHAPE;
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
-    const Plan plan = make_plan(K);
+    const Plan plan = make_plan(K, kSuper<kQ5>);
     if (plan.nslots < 1 || plan.rch < 1) return QDG_ESHAPE;   // cannot happen for K <= 32768: 16 segments at most
     const int grid = static_cast<int>(std::min<int64_t>(dev.sms, total));
     a.ng = count;
@@ -291,18 +320,26 @@ int gemv_q4k_launch_group(const void* const* W, float* const* y, const int64_t* 
     a.O = total;
     cudaError_t e;
     if (dbg)
-        e = launch(gemv_q4k_kernel<true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);
+        e = launch(gemv_q4k_kernel<kQ5, true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);
     else
-        e = launch(gemv_q4k_kernel<false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
+        e = launch(gemv_q4k_kernel<kQ5, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
-    count_launch(12);
+    count_launch(kQ5 ? 14 : 12);
     return QDG_OK;
 }
+
+}  // namespace
 
 int gemv_q4k_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
                     int32_t* dbg) {
     float* ys[1] = {y};
-    return gemv_q4k_launch_group(&W, y ? ys : nullptr, &O, 1, xq, K, stream, dbg);
+    return kquant_launch_group<false>(&W, y ? ys : nullptr, &O, 1, xq, K, stream, dbg);
+}
+
+int gemv_q5k_launch(const void* W, const void* xq, float* y, int64_t O, int64_t K, cudaStream_t stream,
+                    int32_t* dbg) {
+    float* ys[1] = {y};
+    return kquant_launch_group<true>(&W, y ? ys : nullptr, &O, 1, xq, K, stream, dbg);
 }
 
 unsigned flags_read_clear_gemv_q4k(cudaStream_t stream) {
@@ -329,5 +366,16 @@ extern "C" int q4_k_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O
 extern "C" int q4_k_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
                                     const void* xq, int64_t K, qdg_stream_t stream) {
     if (!y) return QDG_EINVAL;
-    return gemv_q4k_launch_group(W, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+    return kquant_launch_group<false>(W, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" int q5_k_q8_0_gemv(const void* W, const void* xq, float* y, int64_t O, int64_t K, qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    return gemv_q5k_launch(W, xq, y, O, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
+}
+
+extern "C" int q5_k_q8_0_gemv_group(const void* const* W, float* const* y, const int64_t* O, int count,
+                                    const void* xq, int64_t K, qdg_stream_t stream) {
+    if (!y) return QDG_EINVAL;
+    return kquant_launch_group<true>(W, y, O, count, xq, K, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }

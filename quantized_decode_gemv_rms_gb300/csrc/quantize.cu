@@ -275,6 +275,88 @@ __global__ void quantize_q4_k_kernel(const float* __restrict__ w, int64_t ldw, i
     for (int k = 0; k < 36; ++k) dst[k] = out[k];
 }
 
+// One thread per Q5_K super-block (176 bytes: the Q4_K header, 32 bytes of
+// top bits, 128 bytes of low four bits), the Q4_K steps with 31 code steps
+// per sub-block, each one IEEE fp32 operation (the same bytes as the
+// library's reference quantizer).
+__global__ void quantize_q5_k_kernel(const float* __restrict__ w, int64_t ldw, int64_t O, int K,
+                                     uint8_t* __restrict__ Wq) {
+    const int nsb = K >> 8;
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= O * nsb) return;
+    const int64_t row = idx / nsb;
+    const int sbi = static_cast<int>(idx - row * nsb);
+    const float* v = w + row * ldw + (static_cast<int64_t>(sbi) << 8);
+    float a[8], mn[8], amax = 0.0f, mnmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float lo = __ldg(v + 32 * j), hi = lo;
+        for (int i = 1; i < 32; ++i) {
+            const float t = __ldg(v + 32 * j + i);
+            if (t < lo) lo = t;
+            if (t > hi) hi = t;
+        }
+        mn[j] = lo < 0.0f ? -lo : 0.0f;
+        a[j] = __fdiv_rn(__fadd_rn(hi, mn[j]), 31.0f);
+        if (a[j] > amax) amax = a[j];
+        if (mn[j] > mnmax) mnmax = mn[j];
+    }
+    const __half dh = __float2half_rn(__fdiv_rn(amax, 63.0f));
+    const __half dmh = __float2half_rn(__fdiv_rn(mnmax, 63.0f));
+    const float dd = __half2float(dh), ddm = __half2float(dmh);
+    int sc[8], m[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        sc[j] = dd > 0.0f ? round_clamp(__fdiv_rn(a[j], dd), 63) : 0;
+        m[j] = ddm > 0.0f ? round_clamp(__fdiv_rn(mn[j], ddm), 63) : 0;
+    }
+    uint32_t out[44];
+    out[0] = static_cast<uint32_t>(__half_as_ushort(dh)) | (static_cast<uint32_t>(__half_as_ushort(dmh)) << 16);
+    uint8_t s[12];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        s[j] = static_cast<uint8_t>((sc[j] & 63) | ((sc[j + 4] >> 4) << 6));
+        s[j + 4] = static_cast<uint8_t>((m[j] & 63) | ((m[j + 4] >> 4) << 6));
+        s[j + 8] = static_cast<uint8_t>((sc[j + 4] & 15) | ((m[j + 4] & 15) << 4));
+    }
+#pragma unroll
+    for (int k = 0; k < 3; ++k)
+        out[1 + k] = static_cast<uint32_t>(s[4 * k]) | (static_cast<uint32_t>(s[4 * k + 1]) << 8) |
+                     (static_cast<uint32_t>(s[4 * k + 2]) << 16) | (static_cast<uint32_t>(s[4 * k + 3]) << 24);
+    uint32_t qh[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) qh[k] = 0u;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const float step0 = __fmul_rn(dd, static_cast<float>(sc[2 * p]));
+        const float off0 = __fmul_rn(ddm, static_cast<float>(m[2 * p]));
+        const float step1 = __fmul_rn(dd, static_cast<float>(sc[2 * p + 1]));
+        const float off1 = __fmul_rn(ddm, static_cast<float>(m[2 * p + 1]));
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+            uint32_t word = 0, top = 0;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = 4 * i4 + u;
+                int q0 = 0, q1 = 0;
+                if (step0 > 0.0f)
+                    q0 = round_clamp(__fdiv_rn(__fadd_rn(__ldg(v + 64 * p + i), off0), step0), 31);
+                if (step1 > 0.0f)
+                    q1 = round_clamp(__fdiv_rn(__fadd_rn(__ldg(v + 64 * p + 32 + i), off1), step1), 31);
+                word |= static_cast<uint32_t>((q0 & 15) | ((q1 & 15) << 4)) << (8 * u);
+                top |= static_cast<uint32_t>(((q0 >> 4) << (2 * p)) | ((q1 >> 4) << (2 * p + 1))) << (8 * u);
+            }
+            out[12 + 8 * p + i4] = word;
+            qh[i4] |= top;
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) out[4 + k] = qh[k];
+    uint32_t* dst = reinterpret_cast<uint32_t*>(Wq + idx * 176);
+#pragma unroll
+    for (int k = 0; k < 44; ++k) dst[k] = out[k];
+}
+
 }  // namespace
 
 unsigned flags_read_clear_quantize(cudaStream_t stream) {
@@ -355,6 +437,23 @@ extern "C" int quantize_q4_k(const float* w, int64_t ldw, int64_t O, int64_t K, 
     const int64_t grid = (sbs + threads - 1) / threads;
     if (grid > 0x7fffffff) return QDG_ESHAPE;
     cudaError_t e = launch(quantize_q4_k_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0,
+                           reinterpret_cast<cudaStream_t>(stream), false, w, ldw, O, static_cast<int>(K),
+                           static_cast<uint8_t*>(Wq));
+    if (e != cudaSuccess) return QDG_ECUDA;
+    count_launch(4);
+    return QDG_OK;
+}
+
+extern "C" int quantize_q5_k(const float* w, int64_t ldw, int64_t O, int64_t K, void* Wq, qdg_stream_t stream) {
+    if (!w || !Wq) return QDG_EINVAL;
+    if (O <= 0 || K <= 0 || ldw < K) return QDG_EINVAL;
+    if (K % 256 != 0 || K > (1 << 20)) return QDG_ESHAPE;
+    if (!aligned(w, 4) || !aligned(Wq, 4)) return QDG_EALIGN;
+    const int64_t sbs = O * (K / 256);
+    const int threads = 128;
+    const int64_t grid = (sbs + threads - 1) / threads;
+    if (grid > 0x7fffffff) return QDG_ESHAPE;
+    cudaError_t e = launch(quantize_q5_k_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), 0,
                            reinterpret_cast<cudaStream_t>(stream), false, w, ldw, O, static_cast<int>(K),
                            static_cast<uint8_t*>(Wq));
     if (e != cudaSuccess) return QDG_ECUDA;

@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
             sig["q4_k_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
             sig["quantize_q4_k"] = ([p, i64, i64, i64, p, p], i32)
             sig["q4_k_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
+            sig["q5_k_q8_0_gemv"] = ([p, p, p, i64, i64, p], i32)
+            sig["quantize_q5_k"] = ([p, i64, i64, i64, p, p], i32)
+            sig["q5_k_q8_0_gemv_group"] = ([p, p, p, i32, p, i64, p], i32)
             sig["q4_0s_gemv_rmsnorm_group"] = ([p, p, p, i32, p, p, f32, i64, p, p], i32)
             sig["q4_0s_q8_0_gemm_small_n"] = ([p, p, p, i64, i64, i64, i64, p], i32)
             sig["q4_0_seg_row_bytes"] = ([i64], i64)
@@ -205,6 +208,28 @@ def q4_k_q8_0_gemv_group(Ws, ys, Os, xq, K: int, stream=None) -> None:
     y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in ys])
     O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
     _check(lib().q4_k_q8_0_gemv_group(W_arr, y_arr, O_arr, n, _ptr(xq), K, _stream(stream)), "q4_k_q8_0_gemv_group")
+
+
+def quantize_q5_k(w, Wq, O: int | None = None, K: int | None = None, ldw: int | None = None,
+                  stream=None) -> None:
+    """fp32 [O][K] weights -> Q5_K super-blocks (load-time preparation)."""
+    if O is None:
+        O, K = w.shape
+    ldw = K if ldw is None else ldw
+    _check(lib().quantize_q5_k(_ptr(w), ldw, O, K, _ptr(Wq), _stream(stream)), "quantize_q5_k")
+
+
+def q5_k_q8_0_gemv(W, xq, y, O: int, K: int, stream=None) -> None:
+    """y = W * x with Q5_K weights (256-weight super-blocks, see include/qdg.h)."""
+    _check(lib().q5_k_q8_0_gemv(_ptr(W), _ptr(xq), _ptr(y), O, K, _stream(stream)), "q5_k_q8_0_gemv")
+
+
+def q5_k_q8_0_gemv_group(Ws, ys, Os, xq, K: int, stream=None) -> None:
+    n = len(Ws)
+    W_arr = (ctypes.c_void_p * n)(*[_ptr(w) for w in Ws])
+    y_arr = (ctypes.c_void_p * n)(*[_ptr(t) for t in ys])
+    O_arr = (ctypes.c_int64 * n)(*[int(o) for o in Os])
+    _check(lib().q5_k_q8_0_gemv_group(W_arr, y_arr, O_arr, n, _ptr(xq), K, _stream(stream)), "q5_k_q8_0_gemv_group")
 
 
 def q4_0_seg_row_bytes(K: int) -> int:

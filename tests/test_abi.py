@@ -256,8 +256,8 @@ def test_options_and_counters(L):
     assert L.qdg_set_option(1, 2) == -1
     assert L.qdg_set_option(1, 0) == 0
     assert L.qdg_launch_count(-1) >= 0
-    assert L.qdg_launch_count(13) >= 0
-    assert L.qdg_launch_count(14) == -1
+    assert L.qdg_launch_count(14) >= 0
+    assert L.qdg_launch_count(15) == -1
     assert L.qdg_launch_count(10) >= 0
     assert L.qdg_debug_block_sums(A16, A16, None, 8, 256, 1, 0, None) == -1
     assert L.qdg_debug_block_sums(A16, A16, A16, 8, 256, 1, 9, None) == -1
