@@ -98,7 +98,7 @@ struct EntryN {
 template <int NV, bool kDebug>
 __global__ void __launch_bounds__(kThreads, 1) gemv_segn_kernel(const __grid_constant__ ArgsN a,
                                                                 const __grid_constant__ PlanN plan) {
-    static_assert(NV >= 1 && NV <= 4, "four vectors at most: sixteen partials per butterfly");
+    static_assert(NV == 3 || NV == 4, "three or four vectors: sixteen partials per butterfly");
     __shared__ float part[kPartFloats];
     __shared__ uint64_t xbar;
     extern __shared__ __align__(16) uint8_t xs[];   // the NV vectors when a.xq_bulk
@@ -129,11 +129,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_segn_kernel(const __grid_con
     pdl_trigger();
 
     EntryN pipe[kDepth] = {};
-    auto load = [&](int64_t row, EntryN& e) {
-        const uint8_t* base = a.W + row * plan.rowbytes;
-        if (has) e.q = ldg_stream16(base + nib_off);
-        e.sc = ldg_stream4(base + sc_off);
+    auto load_at = [&](const uint8_t* rowp, EntryN& e) {
+        if (has) e.q = ldg_stream16(rowp + nib_off);
+        e.sc = ldg_stream4(rowp + sc_off);
     };
+    auto load = [&](int64_t row, EntryN& e) { load_at(a.W + row * plan.rowbytes, e); };
     auto fill = [&](int64_t c0, int crows) {
 #pragma unroll
         for (int d = 0; d < kDepth; ++d) {
@@ -195,13 +195,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_segn_kernel(const __grid_con
     }
 
     // dot the entry with every vector, then refill it with the row kDepth
-    // slots ahead; v[4 k + n] = the lane's partial for vector n
+    // slots ahead; v[4 k + n] = the lane's partial for vector n.  Entries
+    // are consumed in row order, so their refills are consecutive rows of
+    // this warp's slot: one running pointer, advanced by a slot stride.
+    const uint8_t* wnext = nullptr;
+    const int64_t wstride = static_cast<int64_t>(plan.nslots) * plan.rowbytes;
     auto consume = [&](int64_t c0, int crows, int ri, EntryN& entry, float (&v)[16], int k) {
         const uint4 q = entry.q;
         const uint32_t lo[4] = {q.x & kNibbles, q.y & kNibbles, q.z & kNibbles, q.w & kNibbles};
         const uint32_t hi[4] = {(q.x >> 4) & kNibbles, (q.y >> 4) & kNibbles, (q.z >> 4) & kNibbles,
                                 (q.w >> 4) & kNibbles};
         const float dw = half_bits_to_float(entry.sc >> sc_shift);
+        float f[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
         for (int n = 0; n < NV; ++n) {
             int acc = base[n];
@@ -210,11 +215,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_segn_kernel(const __grid_con
                 acc = __dp4a(static_cast<int>(lo[i]), static_cast<int>(xv[n][i]), acc);
                 acc = __dp4a(static_cast<int>(hi[i]), static_cast<int>(xv[n][4 + i]), acc);
             }
-            v[4 * k + n] = __fmul_rn(__fmul_rn(dw, dx[n]), static_cast<float>(acc));
+            f[n] = static_cast<float>(acc);
             if (kDebug && has) a.dbg[(n * O + c0 + ri) * plan.nb + b] = acc;
         }
+        // (d_w d_x) isum, two vectors per packed multiply (same roundings)
+        float s0, s1, s2, s3;
+        fmul2(s0, s1, dw, dw, dx[0], dx[1]);
+        fmul2(v[4 * k], v[4 * k + 1], s0, s1, f[0], f[1]);
+        if (NV == 4) {
+            fmul2(s2, s3, dw, dw, dx[2], dx[NV - 1]);
+            fmul2(v[4 * k + 2], v[4 * k + 3], s2, s3, f[2], f[3]);
+        } else {
+            v[4 * k + 2] = __fmul_rn(__fmul_rn(dw, dx[2]), f[2]);
+            v[4 * k + 3] = 0.0f;
+        }
         const int ahead = ri + kDepth * plan.nslots;
-        if (ahead < crows) load(c0 + ahead, entry);
+        if (ahead < crows) {
+            load_at(wnext, entry);
+            wnext += wstride;
+        }
     };
 
     // sixteen partials v[4 k + n] (row ri + k step, vector n) in one
@@ -245,10 +264,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_segn_kernel(const __grid_con
     auto group4 = [&](int64_t c0, int crows, int ri, int step, int o) {
         float v[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+        for (int k = 0; k < 4; ++k) {
+            if (ri + k * step < crows) {
+                consume(c0, crows, ri + k * step, pipe[o + k], v, k);
+            } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            if (ri + k * step < crows) consume(c0, crows, ri + k * step, pipe[o + k], v, k);
+                for (int n = 0; n < 4; ++n) v[4 * k + n] = 0.0f;
+            }
+        }
         if (!kDebug) reduce16(ri, step, crows, v);
     };
 
@@ -256,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_segn_kernel(const __grid_con
         const int crows = static_cast<int>((r1 - c0) < plan.rch ? (r1 - c0) : plan.rch);
         if (worker) {
             if (c0 != r0) fill(c0, crows);
+            wnext = a.W + (c0 + slot + static_cast<int64_t>(kDepth) * plan.nslots) * plan.rowbytes;
             const int step = plan.nslots;
             for (int ri = slot; ri < crows; ri += kDepth * step) {
                 group4(c0, crows, ri, step, 0);
