@@ -441,7 +441,8 @@ QDG_API int q4_0s_q8_0_gemm_small_n(const void* Wr, const void* xq, float* y, in
  * summation order of qnorm_quantize_q8_0, so xq (optionally copied to xq_out,
  * [K/32] Q8_0, 4-byte aligned) is bit-identical to it and y equals
  * q4_0s_q8_0_gemv_group on that xq.  x, gamma: fp32 [K], 16-byte aligned;
- * gamma = NULL quantizes x without a norm.  K multiple of 256, <= 8192.
+ * gamma = NULL quantizes x without a norm.  K multiple of 256, <= 16384
+ * (x and gamma are staged whole in shared memory).
  */
 QDG_API int q4_0s_gemv_rmsnorm_group(const void* const* Wr, float* const* y, const int64_t* O, int count,
                                      const float* x, const float* gamma, float eps, int64_t K, void* xq_out,

@@ -46,7 +46,7 @@ constexpr int kSegStride = 1152;            // bytes from one segment to the nex
 constexpr int kPartFloats = 3072;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
 constexpr int kMaxGroup = 4;
-constexpr int kFusedMaxK = 8192;            // fused form: x and gamma staged whole in shared memory
+constexpr int kFusedMaxK = 16384;           // fused form: x and gamma staged whole in shared memory (128 KB)
 constexpr uint32_t kNibbles = 0x0F0F0F0Fu;
 
 struct Plan {

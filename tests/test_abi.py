@@ -163,7 +163,7 @@ def test_fused_seg_host_validation(L):
     assert f(W, Y, O, 0, A16, None, 1e-6, 256, None, None) == -1       # count 0
     assert f(W, Y, O, 2, A16, None, -1.0, 256, None, None) == -1       # eps < 0
     assert f(W, Y, O, 2, A16, None, 1e-6, 320, None, None) == -3       # K % 256
-    assert f(W, Y, O, 2, A16, None, 1e-6, 16384, None, None) == -3     # K beyond the fused maximum
+    assert f(W, Y, O, 2, A16, None, 1e-6, 16640, None, None) == -3     # K beyond the fused maximum (16384)
     assert f(W, Y, O, 2, A16 + 4, None, 1e-6, 256, None, None) == -2   # x not 16-byte aligned
     assert f(W, Y, O, 2, A16, A16 + 8, 1e-6, 256, None, None) == -2    # gamma not 16-byte aligned
     assert f(W, Y, O, 2, A16, None, 1e-6, 256, A2, None) == -2         # xq_out not 4-byte aligned

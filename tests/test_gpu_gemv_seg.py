@@ -159,7 +159,7 @@ def test_seg_gemv_vocab_head_sampled():
     assert_within_tol(to_host(y)[rows][None, :], y64, S)
 
 
-@pytest.mark.parametrize("K", [256, 2304, 4096, 8192])
+@pytest.mark.parametrize("K", [256, 2304, 4096, 8192, 14336, 16384])
 @pytest.mark.parametrize("norm", [True, False])
 def test_fused_seg_matches_oracle_and_split(K, norm):
     """The fused form on the segment layout: its Q8_0 vector is the oracle's
