@@ -146,13 +146,8 @@ __global__ void __maxnreg__(kQ5 ? 128 : 96) gemv_q4k_kernel(const __grid_constan
     pdl_trigger();
 
     Entry pipe[kDepth] = {};
-    auto load_seg = [&](int64_t row, Entry& e) {
-        int m = 0;
-#pragma unroll
-        for (int i = 1; i < kMaxGroup; ++i)
-            if (i < a.ng && row >= a.start[i]) m = i;
+    auto load_at = [&](const uint8_t* sb, Entry& e) {
         if (has) {
-            const uint8_t* sb = a.Wg[m] + (row - a.start[m]) * plan.rowbytes + hdr_off;
             e.h = ldg_stream16(sb);
             if (kQ5) {
                 e.q0 = ldg_stream16(sb + 16);
@@ -163,6 +158,16 @@ __global__ void __maxnreg__(kQ5 ? 128 : 96) gemv_q4k_kernel(const __grid_constan
             e.c1 = ldg_stream16(sb + kCodes + 16 + 32 * g);
         }
     };
+    // the super-block of this lane in row `row` (of whichever grouped matrix
+    // holds it)
+    auto row_ptr = [&](int64_t row) {
+        int m = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxGroup; ++i)
+            if (i < a.ng && row >= a.start[i]) m = i;
+        return a.Wg[m] + (row - a.start[m]) * plan.rowbytes + hdr_off;
+    };
+    auto load_seg = [&](int64_t row, Entry& e) { load_at(row_ptr(row), e); };
     auto fill = [&](int64_t c0, int crows) {
 #pragma unroll
         for (int d = 0; d < kDepth; ++d) {
@@ -200,6 +205,8 @@ __global__ void __maxnreg__(kQ5 ? 128 : 96) gemv_q4k_kernel(const __grid_constan
     // two bits of bytes t and 4+t.  Both sub-blocks at once on byte pairs:
     // P1 = bytes (t, t+1) of word 1 (scale bytes 0..3), P2 of word 2, P3 of
     // word 3, each in the low 16 bits by one byte permute.
+    const uint8_t* wnext = nullptr;
+    const int64_t wstride = static_cast<int64_t>(plan.nslots) * plan.rowbytes;
     const uint32_t sel = (g & 1) ? 0x3232u : 0x1010u;       // bytes (2, 3) or (0, 1), twice
     const bool high = g >= 2;
     auto consume = [&](int64_t c0, int crows, int ri, Entry& entry) -> float {
@@ -239,7 +246,16 @@ __global__ void __maxnreg__(kQ5 ? 128 : 96) gemv_q4k_kernel(const __grid_constan
             dst[1] = ib;
         }
         const int ahead = ri + kDepth * plan.nslots;
-        if (ahead < crows) load_seg(c0 + ahead, entry);
+        if (ahead < crows) {
+            // one matrix: the refills of a slot are consecutive rows of it, a
+            // running pointer; grouped matrices: look the row up
+            if (a.ng == 1) {
+                load_at(wnext, entry);
+                wnext += wstride;
+            } else {
+                load_seg(c0 + ahead, entry);
+            }
+        }
         return acc;
     };
     // four row-segments (rows ri + k step) in one butterfly: after the xor-16
@@ -262,6 +278,7 @@ __global__ void __maxnreg__(kQ5 ? 128 : 96) gemv_q4k_kernel(const __grid_constan
         const int crows = static_cast<int>((r1 - c0) < plan.rch ? (r1 - c0) : plan.rch);
         if (worker) {
             if (c0 != r0) fill(c0, crows);
+            if (a.ng == 1) wnext = row_ptr(c0 + slot + static_cast<int64_t>(kDepth) * plan.nslots);
             const int step = plan.nslots;
             for (int ri = slot; ri < crows; ri += kDepth * step) {
                 const float q0 = consume(c0, crows, ri, pipe[0]);
