@@ -12,6 +12,8 @@ not available here; these stand in for them):
                    fraction of the entries of each vector, chosen uniformly
                    without replacement, multiplied by a factor (20)
   * gamma        ~ U(0.5, 1.5)         fp32 [K]
+  * raw bytes    ~ U{0..255}            uint8, for large block-format inputs
+                   whose fields need no particular distribution
 """
 from __future__ import annotations
 
@@ -82,6 +84,12 @@ def gamma(seed: int, name: str, cols: int) -> np.ndarray:
     """fp32 [cols] ~ U(0.5, 1.5)."""
     g = _gen(seed, f"gamma:{name}")
     return g.uniform(0.5, 1.5, size=cols).astype(np.float32)
+
+
+def raw_bytes(seed: int, name: str, count: int) -> np.ndarray:
+    """uint8 [count], uniform over 0..255 (stand-in bytes of a block format
+    whose every field is then valid or overwritten by the caller)."""
+    return _gen(seed, name).integers(0, 256, size=count, dtype=np.uint8)
 
 
 def sample_indices(seed: int, name: str, total: int, count: int) -> np.ndarray:

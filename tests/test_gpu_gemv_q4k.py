@@ -165,3 +165,35 @@ def test_quantize_q4_k_matches_oracle_bytes(O, K):
     qdg.quantize_q4_k(to_dev(w), Wq, O=O, K=K)
     torch.cuda.synchronize()
     assert np.array_equal(to_host(Wq).reshape(O, -1), oracle.quantize_q4_k(w))
+
+
+@pytest.mark.parametrize("wtype", ["q4_k", "q5_k"])
+def test_kquant_rows_in_two_chunks(wtype):
+    """More rows per CTA than one chunk of partial sums holds (K = 32768:
+    16 segments, 192 rows a chunk; O = 29500 gives 194-195 rows a CTA), so
+    each CTA refills its ring across a chunk boundary.  Super-blocks are
+    seeded random bytes with fixed finite scales (every code, scale and min
+    byte pattern is a valid block); exact block sums and outputs on sampled
+    rows against the oracle."""
+    torch = torch_cuda()
+    O, K = 29500, 32768
+    sbb = 144 if wtype == "q4_k" else 176
+    nsb = K // 256
+    W = synth.raw_bytes(29, f"{wtype}-chunks", O * nsb * sbb).reshape(O, nsb, sbb)
+    W[:, :, 0:2] = np.frombuffer(np.float16(0.003).tobytes(), dtype=np.uint8)
+    W[:, :, 2:4] = np.frombuffer(np.float16(0.001).tobytes(), dtype=np.uint8)
+    W = W.reshape(O, -1)
+    xq = oracle.quantize_q8_0(synth.activations(29, "xc", 1, K), None)
+    Wd, xd = to_dev(W), to_dev(xq)
+    rows = synth.sample_indices(29, "rows-chunks", O, 384)
+    path = 6 if wtype == "q4_k" else 7
+    isum = torch.full((1, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(Wd, xd, isum, O, K, 1, path)
+    y = torch.full((O,), float("nan"), dtype=torch.float32, device="cuda")
+    gemv = qdg.q4_k_q8_0_gemv if wtype == "q4_k" else qdg.q5_k_q8_0_gemv
+    gemv(Wd, xd, y, O, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert np.array_equal(to_host(isum)[:, rows], oracle.block_sums(W[rows], xq, K, wtype=wtype))
+    _, y64, S = oracle.matvec(W, xq, K, rows=rows, threads=8, wtype=wtype)
+    assert_within_tol(to_host(y)[rows][None, :], y64, S)
