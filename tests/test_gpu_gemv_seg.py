@@ -345,3 +345,38 @@ def test_segn_unaligned_activations():
     torch.cuda.synchronize()
     assert qdg.qdg_device_status() == qdg.QDG_OK
     assert np.array_equal(to_host(ya).view(np.uint32), to_host(yu).view(np.uint32))
+
+
+def raw_q4_0(seed, name, O, K):
+    """Seeded random Q4_0 rows (every nibble pattern is a valid block) with a
+    fixed finite fp16 scale in every block."""
+    W = synth.raw_bytes(seed, name, O * (K // 32) * 18).reshape(O, K // 32, 18)
+    W[:, :, 0:2] = np.frombuffer(np.float16(0.004).tobytes(), dtype=np.uint8)
+    return W.reshape(O, -1)
+
+
+@pytest.mark.parametrize("O,K,N", [(29500, 32768, 1), (7500, 16384, 4), (9900, 16384, 3)])
+def test_seg_rows_in_two_chunks(O, K, N):
+    """More rows per CTA than one chunk of partial sums holds, so each CTA
+    fills its ring again at the chunk boundary: the batch-1 GEMV at K = 32768
+    (192 rows a chunk, 194-195 rows a CTA) and the three/four-vector dp4a
+    kernel at K = 16384 (four vectors: 48 rows a chunk, 49-50 rows a CTA;
+    three: 64 rows a chunk, 65-66 rows a CTA).  Exact block sums and outputs
+    on sampled rows."""
+    torch = torch_cuda()
+    Wq = raw_q4_0(O + N, "Wchunks", O, K)
+    xq = oracle.quantize_q8_0(synth.activations(O + N, "xchunks", N, K, outlier_frac=0.01), None)
+    Wd, xd = to_dev(oracle.repack_q4_0_seg(Wq, K)), to_dev(xq)
+    rows = synth.sample_indices(O + N, "rows-chunks", O, 384)
+    isum = torch.full((N, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(Wd, xd, isum, O, K, N, 3 if N == 1 else 5)
+    y = torch.full((N, O), float("nan"), dtype=torch.float32, device="cuda")
+    if N == 1:
+        qdg.q4_0s_q8_0_gemv(Wd, xd, y[0], O, K)
+    else:
+        qdg.q4_0s_q8_0_gemm_small_n(Wd, xd, y, O, O, K, N)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert np.array_equal(to_host(isum)[:, rows], oracle.block_sums(Wq[rows], xq, K))
+    _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
+    assert_within_tol(to_host(y)[:, rows], y64, S)
