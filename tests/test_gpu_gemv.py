@@ -304,3 +304,49 @@ def test_gemv_group_matches_single(Os, K):
         assert np.array_equal(ga.view(np.uint32), sb.view(np.uint32)), f"matrix {i}"
         _, y64, S = oracle.matvec(Wqs[i], xq_ref, K, threads=8)
         assert_within_tol(ga[None], y64, S)
+
+
+def raw_blocks(seed, name, O, K, block_bytes, d):
+    """Seeded random rows of 32-element blocks (Q4_0: 18 bytes, Q8_0: 34)
+    with a fixed finite fp16 scale in every block; Q8_0 codes of -128, which
+    the quantizer never writes, become -127."""
+    W = synth.raw_bytes(seed, name, O * (K // 32) * block_bytes).reshape(O, K // 32, block_bytes)
+    W[:, :, 0:2] = np.frombuffer(np.float16(d).tobytes(), dtype=np.uint8)
+    if block_bytes == 34:
+        codes = W[:, :, 2:]
+        codes[codes == 0x80] = 0x81
+    return W.reshape(O, -1)
+
+
+@pytest.mark.parametrize("kind", ["gemv", "fused", "q8w"])
+def test_rows_in_two_chunks(kind):
+    """More rows per CTA than one chunk of partial sums holds, so each CTA
+    fills its ring again at the chunk boundary: the Q4_0 GEMV at K = 32768
+    (256 rows a chunk; O = 39500 gives 259-260 rows a CTA), its fused form at
+    K = 16384 (512 rows; O = 78000: 513-514) and the Q8_0-weight GEMV at
+    K = 32768 (128 rows; O = 19800: 130-131).  Exact block sums of the
+    product kernel and outputs on sampled rows against the oracle."""
+    torch = torch_cuda()
+    O, K = {"gemv": (39500, 32768), "fused": (78000, 16384), "q8w": (19800, 32768)}[kind]
+    q8w = kind == "q8w"
+    W = raw_blocks(O, "Wc", O, K, 34 if q8w else 18, 0.0005 if q8w else 0.004)
+    x = synth.activations(O, "xc", 1, K, outlier_frac=0.01)
+    gam = synth.gamma(O, "gc", K)
+    xq = oracle.quantize_q8_0(x, gam, 1e-6)
+    Wd, xd = to_dev(W), to_dev(xq)
+    rows = synth.sample_indices(O, "rows-c", O, 384)
+    isum = torch.full((1, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(Wd, xd, isum, O, K, 1, 4 if q8w else 0)
+    y = torch.full((O,), float("nan"), dtype=torch.float32, device="cuda")
+    if kind == "gemv":
+        qdg.q4_0_q8_0_gemv(Wd, xd, y, O, K)
+    elif kind == "q8w":
+        qdg.q8_0_q8_0_gemv(Wd, xd, y, O, K)
+    else:
+        qdg.q4_0_gemv_rmsnorm(Wd, to_dev(x[0]), to_dev(gam), 1e-6, y, O, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    wtype = "q8_0" if q8w else "q4_0"
+    assert np.array_equal(to_host(isum)[:, rows], oracle.block_sums(W[rows], xq, K, wtype=wtype))
+    _, y64, S = oracle.matvec(W, xq, K, rows=rows, threads=8, wtype=wtype)
+    assert_within_tol(to_host(y)[rows][None, :], y64, S)

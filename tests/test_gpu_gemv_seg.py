@@ -355,11 +355,12 @@ def raw_q4_0(seed, name, O, K):
     return W.reshape(O, -1)
 
 
-@pytest.mark.parametrize("O,K,N", [(29500, 32768, 1), (7500, 16384, 4), (9900, 16384, 3)])
+@pytest.mark.parametrize("O,K,N", [(29500, 32768, 1), (14800, 32768, 2), (7500, 16384, 4), (9900, 16384, 3)])
 def test_seg_rows_in_two_chunks(O, K, N):
     """More rows per CTA than one chunk of partial sums holds, so each CTA
     fills its ring again at the chunk boundary: the batch-1 GEMV at K = 32768
-    (192 rows a chunk, 194-195 rows a CTA) and the three/four-vector dp4a
+    (192 rows a chunk, 194-195 rows a CTA), the two-vector kernel at K = 32768
+    (96 rows a chunk, 97-98 rows a CTA) and the three/four-vector dp4a
     kernel at K = 16384 (four vectors: 48 rows a chunk, 49-50 rows a CTA;
     three: 64 rows a chunk, 65-66 rows a CTA).  Exact block sums and outputs
     on sampled rows."""
@@ -380,3 +381,26 @@ def test_seg_rows_in_two_chunks(O, K, N):
     assert np.array_equal(to_host(isum)[:, rows], oracle.block_sums(Wq[rows], xq, K))
     _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
     assert_within_tol(to_host(y)[:, rows], y64, S)
+
+
+def test_fused_seg_rows_in_two_chunks():
+    """The fused norm+quantize+GEMV on the segment layout with more rows per
+    CTA than one chunk holds (K = 16384: 384 rows a chunk; O = 58400 gives
+    384-385 rows a CTA): its Q8_0 vector is the oracle's byte for byte and its
+    outputs are within tolerance on sampled rows."""
+    torch = torch_cuda()
+    O, K = 58400, 16384
+    Wq = raw_q4_0(O, "Wfc", O, K)
+    x = synth.activations(O, "xfc", 1, K, outlier_frac=0.01)[0]
+    gam = synth.gamma(O, "gfc", K)
+    xq_ref = oracle.quantize_q8_0(x[None, :], gam, 1e-6)
+    Wd = to_dev(oracle.repack_q4_0_seg(Wq, K))
+    xq_out = empty_u8(qdg.q8_0_nbytes(1, K))
+    y = torch.full((O,), float("nan"), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_gemv_rmsnorm_group([Wd], [y], [O], to_dev(x), to_dev(gam), 1e-6, K, xq_out=xq_out)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert np.array_equal(to_host(xq_out).reshape(1, -1), xq_ref)
+    rows = synth.sample_indices(O, "rows-fc", O, 384)
+    _, y64, S = oracle.matvec(Wq, xq_ref, K, rows=rows, threads=8)
+    assert_within_tol(to_host(y)[rows][None, :], y64, S)
