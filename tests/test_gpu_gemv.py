@@ -350,3 +350,32 @@ def test_rows_in_two_chunks(kind):
     assert np.array_equal(to_host(isum)[:, rows], oracle.block_sums(W[rows], xq, K, wtype=wtype))
     _, y64, S = oracle.matvec(W, xq, K, rows=rows, threads=8, wtype=wtype)
     assert_within_tol(to_host(y)[rows][None, :], y64, S)
+
+
+@pytest.mark.parametrize("layout,O,K", [("plain", 20000, 4096), ("plain", 5000, 14336), ("seg", 15000, 4096)])
+@pytest.mark.parametrize("N", [3, 8])
+def test_small_n_rows_in_two_batches(layout, O, K, N):
+    """More row tiles per CTA (or cluster) than one batch of partial sums
+    holds, so the partials are combined twice: plain layout, 8 tiles a batch
+    (K = 4096, one CTA: 131-132 rows; K = 14336, clusters of four CTAs:
+    131-132 rows a cluster, the cluster form's double-buffered batch
+    partials); segment layout, 6 tiles a batch (K = 4096: 98-99 rows).  Exact
+    block sums and outputs on sampled rows."""
+    torch = torch_cuda()
+    Wq = raw_blocks(O + K + N, "Wb", O, K, 18, 0.004)
+    xq = oracle.quantize_q8_0(synth.activations(O + N, "xb", N, K, outlier_frac=0.01), None)
+    seg = layout == "seg"
+    Wd, xd = to_dev(oracle.repack_q4_0_seg(Wq, K) if seg else Wq), to_dev(xq)
+    isum = torch.full((N, O, K // 32), -2 ** 31, dtype=torch.int32, device="cuda")
+    qdg.qdg_debug_block_sums(Wd, xd, isum, O, K, N, 5 if seg else 1)
+    y = torch.full((N, O), float("nan"), dtype=torch.float32, device="cuda")
+    if seg:
+        qdg.q4_0s_q8_0_gemm_small_n(Wd, xd, y, O, O, K, N)
+    else:
+        qdg.q4_0_q8_0_gemm_small_n(Wd, xd, y, O, O, K, N)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    rows = synth.sample_indices(O + N, "rows-b", O, 512)
+    assert np.array_equal(to_host(isum)[:, rows], oracle.block_sums(Wq[rows], xq, K))
+    _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
+    assert_within_tol(to_host(y)[:, rows], y64, S)
