@@ -42,6 +42,8 @@ namespace {
 constexpr int kWarps = 16;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kDepth1 = 4;                  // row-segments in flight per warp, reduced together in one butterfly
+constexpr int kDepthDeep = 8;               // the same for long launches (128 registers: no quantize CTA fits beside)
+constexpr int kDeepRows = 384;              // rows per CTA from which a launch takes the deep ring
 constexpr int kSegStride = 1152;            // bytes from one segment to the next: 64 x 16 nibble bytes + 128
 constexpr int kPartFloats = 3072;           // per-chunk partial sums (rows x segments)
 constexpr int kL2Prefetch = 96 * 1024;      // bytes of W prefetched into L2 per CTA at start
@@ -161,8 +163,10 @@ __device__ __forceinline__ void load_act(const uint8_t* xq, int b, uint32_t* x, 
 //   ((w0+w1)+(w2+w3))+((w4+w5)+(w6+w7)); s = 1/sqrt(sum/K + eps);
 //   block b (warp b mod 16, lane = element): v = (x*s)*gamma, d = max|v|/127,
 //   q = round(v/d) (halves away from zero), clamped to +-127.
-template <bool kFused, bool kDebug>
-__global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, const __grid_constant__ Plan plan) {
+template <bool kFused, bool kDebug, bool kDeep = false>
+__global__ void __maxnreg__(kDeep ? 128 : 96) gemv_seg_kernel(const __grid_constant__ Args a,
+                                                              const __grid_constant__ Plan plan) {
+    constexpr int kDepth = kDeep ? kDepthDeep : kDepth1;
     __shared__ float part[kPartFloats];
     __shared__ float norm_part[8];
     __shared__ uint64_t xbar;                       // the bulk copies of xq (or of x and gamma)
@@ -192,7 +196,7 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
     __syncthreads();
     pdl_trigger();
 
-    Entry pipe[kDepth1] = {};
+    Entry pipe[kDepth] = {};
     auto load_seg = [&](int64_t row, Entry& e) {
         int g = 0;
 #pragma unroll
@@ -205,7 +209,7 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
     };
     auto fill = [&](int64_t c0, int crows) {
 #pragma unroll
-        for (int d = 0; d < kDepth1; ++d) {
+        for (int d = 0; d < kDepth; ++d) {
             const int ri = slot + d * plan.nslots;
             if (ri < crows) load_seg(c0 + ri, pipe[d]);
         }
@@ -213,7 +217,7 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
 
     if (worker) fill(r0, min(nrows, plan.rch));
     if (threadIdx.x == 0) {
-        int64_t row = r0 + static_cast<int64_t>(kDepth1) * plan.nslots;
+        int64_t row = r0 + static_cast<int64_t>(kDepth) * plan.nslots;
         int64_t budget = kL2Prefetch / plan.rowbytes;
         for (int g = 0; g < a.ng && budget > 0; ++g) {
             const int64_t gend = (g + 1 < a.ng) ? a.start[g + 1] : O;
@@ -334,7 +338,7 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
         if (has_b) load_act<false>(a.xq, seg * 64 + 32 + lane, xb, dxb, sb);
     }
 
-    // One row-segment: dot the entry, then refill it with the segment kDepth1
+    // One row-segment: dot the entry, then refill it with the segment kDepth
     // ahead (the refill goes into the registers just read, so no copy of the
     // entry is kept alive across the loads); returns the lane's partial.
     // Measured on GB300 this order streams about 20% faster than refilling
@@ -354,7 +358,7 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
             if (has_a) d[0] = ia;
             if (has_b) d[32] = ib;
         }
-        const int ahead = ri + kDepth1 * plan.nslots;
+        const int ahead = ri + kDepth * plan.nslots;
         if (ahead < crows) load_seg(c0 + ahead, entry);
         return acc;
     };
@@ -380,12 +384,19 @@ __global__ void __maxnreg__(96) gemv_seg_kernel(const __grid_constant__ Args a, 
         if (worker) {
             if (c0 != r0) fill(c0, crows);
             const int step = plan.nslots;
-            for (int ri = slot; ri < crows; ri += kDepth1 * step) {
-                const float p0 = consume(c0, crows, ri, pipe[0]);
-                const float p1 = ri + step < crows ? consume(c0, crows, ri + step, pipe[1]) : 0.0f;
-                const float p2 = ri + 2 * step < crows ? consume(c0, crows, ri + 2 * step, pipe[2]) : 0.0f;
-                const float p3 = ri + 3 * step < crows ? consume(c0, crows, ri + 3 * step, pipe[3]) : 0.0f;
-                reduce4(ri, step, crows, p0, p1, p2, p3);
+            for (int ri = slot; ri < crows; ri += kDepth * step) {
+                // four ring entries (rows ri + k step) per butterfly; the deep
+                // ring turns through two such groups
+#pragma unroll
+                for (int h = 0; h < kDepth / 4; ++h) {
+                    const int rj = ri + 4 * h * step;
+                    if (h > 0 && rj >= crows) break;
+                    const float p0 = consume(c0, crows, rj, pipe[4 * h]);
+                    const float p1 = rj + step < crows ? consume(c0, crows, rj + step, pipe[4 * h + 1]) : 0.0f;
+                    const float p2 = rj + 2 * step < crows ? consume(c0, crows, rj + 2 * step, pipe[4 * h + 2]) : 0.0f;
+                    const float p3 = rj + 3 * step < crows ? consume(c0, crows, rj + 3 * step, pipe[4 * h + 3]) : 0.0f;
+                    reduce4(rj, step, crows, p0, p1, p2, p3);
+                }
             }
         }
         __syncthreads();
@@ -648,10 +659,16 @@ int gemv_seg_launch_group(const void* const* W, float* const* y, const int64_t* 
     a.dbg = dbg;
     a.O = total;
     cudaError_t e;
+    // a long launch (the vocabulary head) takes the eight-deep ring: twice the
+    // bytes in flight per warp; the following quantize kernel then waits for
+    // SMs to free up, which the CTAs' spread of finishing times provides
+    const bool deep = (total + grid - 1) / grid >= kDeepRows;
     if (dbg)
-        e = launch(gemv_seg_kernel<false, true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);
+        e = deep ? launch(gemv_seg_kernel<false, true, true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan)
+                 : launch(gemv_seg_kernel<false, true>, dim3(grid), dim3(kThreads), smem, stream, false, a, plan);
     else
-        e = launch(gemv_seg_kernel<false, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
+        e = deep ? launch(gemv_seg_kernel<false, false, true>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan)
+                 : launch(gemv_seg_kernel<false, false>, dim3(grid), dim3(kThreads), smem, stream, true, a, plan);
     if (e != cudaSuccess) return QDG_ECUDA;
     count_launch(6);
     return QDG_OK;
