@@ -28,11 +28,13 @@
 // Work split: a warp owns a chunk of 8 consecutive blocks of K (256
 // elements) and keeps the activation fragments, scales and corrections of
 // those blocks for all N columns in registers.  The CTA streams its row
-// tiles (16 rows x all of its chunks) through a ring of shared-memory
+// tiles (32 rows x all of its chunks) through a ring of shared-memory
 // stages, one 3-D tensor copy (TMA) per tile that lands each chunk as its own
-// 16 x 144-byte slab (row stride 144 bytes: conflict-free fragment loads);
+// 32 x 144-byte slab (row stride 144 bytes: conflict-free fragment loads);
 // the last warp done with a stage refills it.  Each warp accumulates
-// d_w * d_x * isum in fp32 for its 16 rows x 8 columns.  A CTA holds up to 16 chunks (K <= 4096); for
+// d_w * d_x * isum in fp32 for its 32 rows x 8 columns (two MMA row groups
+// share a tile's waits, refill and partial-sum stores, and each block's
+// activation fragments and column table).  A CTA holds up to 16 chunks (K <= 4096); for
 // larger K a thread-block cluster of ceil(K / 4096) CTAs splits K, and the
 // per-chunk partials are combined in a fixed order: first across the CTA's
 // warps in shared memory, then across the cluster's CTAs through distributed
@@ -55,8 +57,10 @@ static __device__ unsigned g_flags_small_n;
 namespace {
 
 constexpr int kChunkBytes = kChunkBlocks * 18;        // 144 bytes of a row per chunk, a multiple of 16
-constexpr int kUnitBytes = kTileRows * kChunkBytes;   // 2304 bytes per ring slot (18 x 128)
-constexpr int kBatchTilesPerSlot = 8;                 // row tiles per slot and batch of partial sums
+constexpr int kRows = 2 * kTileRows;                  // rows of a tile: two MMA row groups share its bookkeeping
+constexpr int kUnitBytes = kRows * kChunkBytes;       // 4608 bytes per ring slot (36 x 128)
+constexpr int kPartTile = kRows * 8;                  // partial sums of one tile and warp: 32 rows x 8 columns
+constexpr int kBatchTilesPerSlot = 4;                 // row tiles per slot and batch of partial sums
 
 static_assert(kChunkBytes % 16 == 0 && kUnitBytes % 128 == 0, "tensor-copy alignment");
 
@@ -71,7 +75,7 @@ __device__ __forceinline__ uint32_t nibble_word(const uint8_t* row, int t) {
 }
 
 struct Args {
-    CUtensorMap wmap;   // W as [chunk][row][144 bytes]; box = 16 rows x wmax chunks
+    CUtensorMap wmap;   // W as [chunk][row][144 bytes]; box = 32 rows x wmax chunks
     const uint8_t* xq;
     float* y;
     int32_t* dbg;
@@ -88,35 +92,43 @@ struct Args {
     int part_floats;   // partial-sum area: bt * wmax * 128 floats, and room for the staged activations
 };
 
+// One block of the warp's chunk for the tile's 32 rows: rows g, g + 8 (ra, rb)
+// and g + 16, g + 24 (rc, rd), each pair one m16 MMA row group; the
+// activation fragments and the column table serve both.
 template <int kB>
-__device__ __forceinline__ void block_step(const uint8_t* ra, const uint8_t* rb, int t, const XBlock& x,
-                                           const XTab* tab, float (&acc)[4], float (&isum)[4]) {
-    const uint32_t w0 = nibble_word<kB>(ra, t);
-    const uint32_t w1 = nibble_word<kB>(rb, t);
-    const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
-    const unsigned short dw0 = *reinterpret_cast<const unsigned short*>(ra + 18 * kB);
-    const unsigned short dw1 = *reinterpret_cast<const unsigned short*>(rb + 18 * kB);
+__device__ __forceinline__ void block_step(const uint8_t* ra, const uint8_t* rb, const uint8_t* rc, const uint8_t* rd,
+                                           int t, const XBlock& x, const XTab* tab, float (&acc)[8],
+                                           float (&isum)[8]) {
     const XTab e = tab[kB * 4 + t];
-    float d0, d1, d2, d3;
-    // first MMA: low nibbles of bytes (0, 2) and (1, 3), rows g and g + 8;
-    // second MMA: high nibbles of the same bytes (x 16), activations / 16;
-    // plus the columns' corrections: d = the exact block sums of columns 2t,
-    // 2t + 1 for rows g (d0, d1) and g + 8 (d2, d3).
-    hmma2(d0, d1, d2, d3, lo_pair(w0), lo_pair(w1), lo_pair(v0), lo_pair(v1), x.b[0], x.b[1], hi_pair(w0),
-          hi_pair(w1), hi_pair(v0), hi_pair(v1), x.b[2], x.b[3]);
-    // acc += (d_w * d_x) * isum; the scale product is exact in fp32
-    fadd2(d0, d1, e.m0, e.m1);
-    fadd2(d2, d3, e.m0, e.m1);
-    const float dwa = half_bits_to_float(dw0), dwb = half_bits_to_float(dw1);
-    float s0, s1, s2, s3;
-    fmul2(s0, s1, dwa, dwa, e.dx0, e.dx1);
-    fmul2(s2, s3, dwb, dwb, e.dx0, e.dx1);
-    ffma2(acc[0], acc[1], s0, s1, d0, d1);
-    ffma2(acc[2], acc[3], s2, s3, d2, d3);
-    isum[0] = d0;
-    isum[1] = d1;
-    isum[2] = d2;
-    isum[3] = d3;
+    const uint8_t* rows[4] = {ra, rb, rc, rd};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t w0 = nibble_word<kB>(rows[2 * h], t);
+        const uint32_t w1 = nibble_word<kB>(rows[2 * h + 1], t);
+        const uint32_t v0 = w0 >> 8, v1 = w1 >> 8;
+        const unsigned short dw0 = *reinterpret_cast<const unsigned short*>(rows[2 * h] + 18 * kB);
+        const unsigned short dw1 = *reinterpret_cast<const unsigned short*>(rows[2 * h + 1] + 18 * kB);
+        float d0, d1, d2, d3;
+        // first MMA: low nibbles of bytes (0, 2) and (1, 3), rows g and g + 8
+        // of the group; second MMA: high nibbles of the same bytes (x 16),
+        // activations / 16; plus the columns' corrections: d = the exact
+        // block sums of columns 2t, 2t + 1 for the two rows
+        hmma2(d0, d1, d2, d3, lo_pair(w0), lo_pair(w1), lo_pair(v0), lo_pair(v1), x.b[0], x.b[1], hi_pair(w0),
+              hi_pair(w1), hi_pair(v0), hi_pair(v1), x.b[2], x.b[3]);
+        // acc += (d_w * d_x) * isum; the scale product is exact in fp32
+        fadd2(d0, d1, e.m0, e.m1);
+        fadd2(d2, d3, e.m0, e.m1);
+        const float dwa = half_bits_to_float(dw0), dwb = half_bits_to_float(dw1);
+        float s0, s1, s2, s3;
+        fmul2(s0, s1, dwa, dwa, e.dx0, e.dx1);
+        fmul2(s2, s3, dwb, dwb, e.dx0, e.dx1);
+        ffma2(acc[4 * h], acc[4 * h + 1], s0, s1, d0, d1);
+        ffma2(acc[4 * h + 2], acc[4 * h + 3], s2, s3, d2, d3);
+        isum[4 * h] = d0;
+        isum[4 * h + 1] = d1;
+        isum[4 * h + 2] = d2;
+        isum[4 * h + 3] = d3;
+    }
 }
 
 // Shared memory: [mbarriers][counters][pad], the per-warp tables, then the
@@ -144,8 +156,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
     uint64_t* xbar = full + kMaxStages - 1;                                  // activation copies (S < kMaxStages)
     XTab* tab = reinterpret_cast<XTab*>(smem + kHeadBytes) + warp * kChunkBlocks * 4;   // [8 blocks][4]
     uint8_t* ring = smem + kHeadBytes + kTabBytes;
-    float* part = reinterpret_cast<float*>(ring + S * stage_bytes);          // [bt][wmax][128]
-    float* loc = part + a.part_floats;                                       // [2][bt * 128], cluster case
+    float* part = reinterpret_cast<float*>(ring + S * stage_bytes);          // [bt][wmax][kPartTile]
+    float* loc = part + a.part_floats;                                       // [2][bt * kPartTile], cluster case
 
     const int csize = kCluster ? a.csize : 1;
     const int rank = kCluster ? static_cast<int>(cluster_rank()) : 0;
@@ -153,7 +165,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
     const int cid = static_cast<int>(blockIdx.x) / csize;
     const int64_t O = a.O;
     // the cluster's row tiles [tile0, tile0 + ntiles); rows past O read as zero
-    const int64_t tiles = (O + kTileRows - 1) / kTileRows;
+    const int64_t tiles = (O + kRows - 1) / kRows;
     const int64_t tile0 = static_cast<int64_t>(cid) * tiles / ncl;
     const int ntiles = static_cast<int>(static_cast<int64_t>(cid + 1) * tiles / ncl - tile0);
     const int nbatch = (ntiles + bt - 1) / bt;
@@ -167,10 +179,10 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
     const int chunk = ch0 + wl;
 
     // Tile tau of the cluster's rows goes to stage s = tau % S; one tensor copy
-    // brings the 16 rows x wmax chunks of the CTA (chunk slabs of 16 x 144 B).
+    // brings the 32 rows x wmax chunks of the CTA (chunk slabs of 32 x 144 B).
     auto issue = [&](int s, int tau) {
         mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(stage_bytes));
-        tma_load_3d(ring + s * stage_bytes, &a.wmap, 0, static_cast<int>((tile0 + tau) * kTileRows), ch0, &full[s]);
+        tma_load_3d(ring + s * stage_bytes, &a.wmap, 0, static_cast<int>((tile0 + tau) * kRows), ch0, &full[s]);
     };
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -251,7 +263,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
             const int tb = j * nslots + slot;          // tile within the batch
             const int tau = beta * bt + tb;            // tile within the cluster's rows
             if (tau >= ntiles) break;
-            float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
             if (worker && ok) {
                 ok = *abort_sh == 0 && __all_sync(0xffffffffu, mbar_wait(&full[s], ph));
                 if (!ok && lane == 0) {
@@ -262,21 +274,23 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
             if (worker && ok) {
                 const uint8_t* ra = ring + s * stage_bytes + wl * kUnitBytes + g * kChunkBytes;
                 const uint8_t* rb = ra + 8 * kChunkBytes;
-                float is[kChunkBlocks][4];
-                block_step<0>(ra, rb, t, xs[0], tab, acc, is[0]);
-                block_step<1>(ra, rb, t, xs[1], tab, acc, is[1]);
-                block_step<2>(ra, rb, t, xs[2], tab, acc, is[2]);
-                block_step<3>(ra, rb, t, xs[3], tab, acc, is[3]);
-                block_step<4>(ra, rb, t, xs[4], tab, acc, is[4]);
-                block_step<5>(ra, rb, t, xs[5], tab, acc, is[5]);
-                block_step<6>(ra, rb, t, xs[6], tab, acc, is[6]);
-                block_step<7>(ra, rb, t, xs[7], tab, acc, is[7]);
+                const uint8_t* rc = ra + 16 * kChunkBytes;
+                const uint8_t* rd = ra + 24 * kChunkBytes;
+                float is[kChunkBlocks][8];
+                block_step<0>(ra, rb, rc, rd, t, xs[0], tab, acc, is[0]);
+                block_step<1>(ra, rb, rc, rd, t, xs[1], tab, acc, is[1]);
+                block_step<2>(ra, rb, rc, rd, t, xs[2], tab, acc, is[2]);
+                block_step<3>(ra, rb, rc, rd, t, xs[3], tab, acc, is[3]);
+                block_step<4>(ra, rb, rc, rd, t, xs[4], tab, acc, is[4]);
+                block_step<5>(ra, rb, rc, rd, t, xs[5], tab, acc, is[5]);
+                block_step<6>(ra, rb, rc, rd, t, xs[6], tab, acc, is[6]);
+                block_step<7>(ra, rb, rc, rd, t, xs[7], tab, acc, is[7]);
                 if (kDebug) {
-                    const int64_t rt = (tile0 + tau) * kTileRows;
+                    const int64_t rt = (tile0 + tau) * kRows;
 #pragma unroll
                     for (int b = 0; b < kChunkBlocks; ++b)
 #pragma unroll
-                        for (int i = 0; i < 4; ++i) {
+                        for (int i = 0; i < 8; ++i) {
                             const int64_t row = rt + g + 8 * (i >> 1);
                             const int col = 2 * t + (i & 1);
                             if (row < O && col < a.N)
@@ -296,9 +310,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
                 }
                 __syncwarp();
             }
-            if (worker)
-                *reinterpret_cast<float4*>(part + (tb * wmax + wl) * 128 + lane * 4) =
-                    make_float4(acc[0], acc[1], acc[2], acc[3]);
+            if (worker) {
+                float4* dst = reinterpret_cast<float4*>(part + (tb * wmax + wl) * kPartTile + lane * 8);
+                dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            }
             s += nslots;
             if (s >= S) {
                 s -= S;
@@ -306,42 +322,42 @@ __global__ void __launch_bounds__(kMaxWarps * 32, 1) small_n_kernel(const __grid
             }
         }
         __syncthreads();
-        // ---- batch reduction.  Index e of a tile's 128 partials = lane * 4 + i
+        // ---- batch reduction.  Index e of a tile's 256 partials = lane * 8 + i
         // of the writing lane: row g + 8 (i >> 1), column 2t + (i & 1).
         const int tiles_here = min(bt, ntiles - beta * bt);
-        const int64_t rbase = (tile0 + static_cast<int64_t>(beta) * bt) * kTileRows;
+        const int64_t rbase = (tile0 + static_cast<int64_t>(beta) * bt) * kRows;
         if (kDebug) {
             __syncthreads();
         } else if (!kCluster) {
-            for (int e = threadIdx.x; e < tiles_here * 128; e += blockDim.x) {
-                const int tb = e >> 7, l = (e >> 2) & 31, i = e & 3;
+            for (int e = threadIdx.x; e < tiles_here * kPartTile; e += blockDim.x) {
+                const int tb = e >> 8, l = (e >> 3) & 31, i = e & 7;
                 const int col = 2 * (l & 3) + (i & 1);
-                const int64_t row = rbase + tb * kTileRows + (l >> 2) + 8 * (i >> 1);
+                const int64_t row = rbase + tb * kRows + (l >> 2) + 8 * (i >> 1);
                 if (col >= a.N || row >= O) continue;
-                const float* src = part + tb * wmax * 128 + (e & 127);
+                const float* src = part + tb * wmax * kPartTile + (e & 255);
                 float v = src[0];
-                for (int w = 1; w < cq; ++w) v = __fadd_rn(v, src[w * 128]);
+                for (int w = 1; w < cq; ++w) v = __fadd_rn(v, src[w * kPartTile]);
                 a.y[col * a.ldy + row] = v;
             }
             __syncthreads();   // partials read before the next batch overwrites them
         } else {
             // clusters imply one slot
-            float* lb = loc + (beta & 1) * bt * 128;
-            for (int e = threadIdx.x; e < tiles_here * 128; e += blockDim.x) {
-                const float* src = part + (e >> 7) * wmax * 128 + (e & 127);
+            float* lb = loc + (beta & 1) * bt * kPartTile;
+            for (int e = threadIdx.x; e < tiles_here * kPartTile; e += blockDim.x) {
+                const float* src = part + (e >> 8) * wmax * kPartTile + (e & 255);
                 float v = src[0];
-                for (int w = 1; w < cq; ++w) v = __fadd_rn(v, src[w * 128]);
+                for (int w = 1; w < cq; ++w) v = __fadd_rn(v, src[w * kPartTile]);
                 lb[e] = v;
             }
             __syncwarp();
             cluster_sync();
-            const int per = (tiles_here * 128 + csize - 1) / csize;
+            const int per = (tiles_here * kPartTile + csize - 1) / csize;
             const int e0 = rank * per;
-            const int e1 = min(tiles_here * 128, e0 + per);
+            const int e1 = min(tiles_here * kPartTile, e0 + per);
             for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += blockDim.x) {
-                const int tb = e >> 7, l = (e >> 2) & 31, i = e & 3;
+                const int tb = e >> 8, l = (e >> 3) & 31, i = e & 7;
                 const int col = 2 * (l & 3) + (i & 1);
-                const int64_t row = rbase + tb * kTileRows + (l >> 2) + 8 * (i >> 1);
+                const int64_t row = rbase + tb * kRows + (l >> 2) + 8 * (i >> 1);
                 if (col >= a.N || row >= O) continue;
                 float v = ld_cluster(lb + e, 0);
                 for (int q = 1; q < csize; ++q) v = __fadd_rn(v, ld_cluster(lb + e, static_cast<uint32_t>(q)));
@@ -367,7 +383,7 @@ std::map<std::tuple<int, bool, int, int, size_t>, int> g_max_clusters;
 size_t smem_bytes(const Args& a) {
     const size_t stage = static_cast<size_t>(a.wmax) * kUnitBytes;
     return kHeadBytes + kTabBytes + a.stages * stage + static_cast<size_t>(a.part_floats) * sizeof(float) +
-           (a.csize > 1 ? 2 * static_cast<size_t>(a.bt) * 128 * sizeof(float) : 0);
+           (a.csize > 1 ? 2 * static_cast<size_t>(a.bt) * kPartTile * sizeof(float) : 0);
 }
 
 template <bool kDebug, bool kCluster>
@@ -404,7 +420,7 @@ template <bool kDebug, bool kCluster>
 cudaError_t launch_small_n(const Args& a, int warps, size_t smem, int sms, int64_t O, cudaStream_t stream) {
     const int maxcl = max_clusters<kDebug, kCluster>(a.csize, warps, smem, sms);
     if (maxcl < 1) return cudaErrorInvalidConfiguration;
-    const int64_t tiles = (O + kTileRows - 1) / kTileRows;
+    const int64_t tiles = (O + kRows - 1) / kRows;
     const int ncl = static_cast<int>(std::min<int64_t>(maxcl, tiles));
     return launch_cluster(small_n_kernel<kDebug, kCluster>, dim3(static_cast<unsigned>(ncl * a.csize)),
                           dim3(static_cast<unsigned>(warps * 32)), smem, stream, !kDebug, kCluster ? a.csize : 1, a);
@@ -417,7 +433,7 @@ int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t
     if (!W || !xq || (!y && !dbg)) return QDG_EINVAL;
     if (O <= 0 || K <= 0 || N < 1 || N > 8) return QDG_EINVAL;
     if (!dbg && ldy < O) return QDG_EINVAL;
-    if (K % 256 != 0 || K > 32768 || O >= (int64_t(1) << 31) - kTileRows) return QDG_ESHAPE;
+    if (K % 256 != 0 || K > 32768 || O >= (int64_t(1) << 31) - kRows) return QDG_ESHAPE;
     if (!aligned(W, 16) || !aligned(xq, 16) || (y && !aligned(y, 4))) return QDG_EALIGN;
     const DeviceInfo dev = device_info();
     if (dev.device < 0) return QDG_ECUDA;
@@ -437,7 +453,7 @@ int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t
     // memory holds as many tile stages as fit (at least two).
     a.bt = kBatchTilesPerSlot * a.nslots;
     // the partial-sum area first receives the activations: N x wmax chunks x 272 bytes
-    a.part_floats = std::max(a.bt * a.wmax * 128, 8 * (a.wmax * kChunkBlocks * 34 + 16) / 4);
+    a.part_floats = std::max(a.bt * a.wmax * kPartTile, 8 * (a.wmax * kChunkBlocks * 34 + 16) / 4);
     if (a.csize > kMaxCluster) return QDG_ECUDA;
     a.stages = 0;
     const size_t fixed = smem_bytes(a);
@@ -446,7 +462,7 @@ int small_n_launch(const void* W, const void* xq, float* y, int64_t ldy, int64_t
     a.stages = static_cast<int>(std::min<size_t>(kMaxStages - 1, (dev.smem_optin - fixed) / stage));
     const int warps = a.wmax * a.nslots;
     const size_t smem = smem_bytes(a);
-    if (!encode_row_segments(&a.wmap, W, static_cast<int64_t>(a.nb) * 18, O, kChunkBytes, kTileRows, a.wmax))
+    if (!encode_row_segments(&a.wmap, W, static_cast<int64_t>(a.nb) * 18, O, kChunkBytes, kRows, a.wmax))
         return QDG_ECUDA;
     cudaError_t e;
     if (dbg)
