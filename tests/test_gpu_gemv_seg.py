@@ -404,3 +404,28 @@ def test_fused_seg_rows_in_two_chunks():
     rows = synth.sample_indices(O, "rows-fc", O, 384)
     _, y64, S = oracle.matvec(Wq, xq_ref, K, rows=rows, threads=8)
     assert_within_tol(to_host(y)[rows][None, :], y64, S)
+
+
+def test_seg_deep_ring_matches_four_deep():
+    """A launch with at least 384 rows per CTA takes the eight-deep ring: one
+    launch over 60000 rows (395 a CTA) against the same rows as two launches
+    of 30000 (197 a CTA, the four-deep ring).  Per-row arithmetic is the same,
+    so the outputs agree bit for bit; sampled rows against the oracle."""
+    torch = torch_cuda()
+    O, K = 60000, 4096
+    Wq = raw_q4_0(O, "Wdeep", O, K)
+    xq = oracle.quantize_q8_0(synth.activations(O, "xdeep", 1, K, outlier_frac=0.01), None)
+    Wr = oracle.repack_q4_0_seg(Wq, K)
+    Wd, xd = to_dev(Wr), to_dev(xq)
+    y = torch.full((O,), float("nan"), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemv(Wd, xd, y, O, K)
+    h = O // 2
+    y2 = torch.full((O,), float("nan"), dtype=torch.float32, device="cuda")
+    qdg.q4_0s_q8_0_gemv(Wd[:h], xd, y2[:h], h, K)          # rows [0, h): 16-byte aligned (h x 2304 bytes)
+    qdg.q4_0s_q8_0_gemv(Wd[h:], xd, y2[h:], O - h, K)
+    torch.cuda.synchronize()
+    assert qdg.qdg_device_status() == qdg.QDG_OK
+    assert np.array_equal(to_host(y).view(np.uint32), to_host(y2).view(np.uint32))
+    rows = synth.sample_indices(O, "rows-deep", O, 256)
+    _, y64, S = oracle.matvec(Wq, xq, K, rows=rows, threads=8)
+    assert_within_tol(to_host(y)[rows][None, :], y64, S)
