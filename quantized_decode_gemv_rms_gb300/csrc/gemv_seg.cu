@@ -22,11 +22,14 @@
 //   * Lane l of a warp owns blocks 64s+l and 64s+32+l of its segment: two
 //     coalesced 16-byte nibble loads (512 contiguous bytes per warp each) and
 //     one 4-byte scale-word load per row-segment, issued four row-segments
-//     ahead of use (74 KB in flight per SM); the matching Q8_0 activations
-//     stay in registers.
+//     ahead of use (74 KB in flight per SM, 96 registers, so that a CTA of
+//     the quantize kernel fits beside it); launches with at least 384 rows
+//     per CTA (a vocabulary head) go eight row-segments ahead at 128
+//     registers; the matching Q8_0 activations stay in registers.
 //   * Exact block sums with dp4a (minus 8 * sum(q_x)), scaled by d_w * d_x;
-//     the four rows of the ring share one warp butterfly; segment partials
-//     combined per row in a fixed order (deterministic).
+//     each four rows of the ring share one warp butterfly; segment partials
+//     combined per row in a fixed order (deterministic, and the same bits for
+//     either ring depth).
 //   * Programmatic dependent launch: the first row-segments of W are
 //     requested before the kernel waits for the preceding grid.
 #include "common.cuh"
