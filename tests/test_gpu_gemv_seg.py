@@ -355,12 +355,14 @@ def raw_q4_0(seed, name, O, K):
     return W.reshape(O, -1)
 
 
-@pytest.mark.parametrize("O,K,N", [(29500, 32768, 1), (14800, 32768, 2), (7500, 16384, 4), (9900, 16384, 3)])
+@pytest.mark.parametrize("O,K,N", [(29500, 32768, 1), (14800, 32768, 2), (118000, 4096, 2), (7500, 16384, 4),
+                                   (9900, 16384, 3)])
 def test_seg_rows_in_two_chunks(O, K, N):
     """More rows per CTA than one chunk of partial sums holds, so each CTA
     fills its ring again at the chunk boundary: the batch-1 GEMV at K = 32768
     (192 rows a chunk, 194-195 rows a CTA), the two-vector kernel at K = 32768
-    (96 rows a chunk, 97-98 rows a CTA) and the three/four-vector dp4a
+    (96 rows a chunk, 97-98 rows a CTA) and at K = 4096 (768 rows a chunk,
+    776-777 rows a CTA), and the three/four-vector dp4a
     kernel at K = 16384 (four vectors: 48 rows a chunk, 49-50 rows a CTA;
     three: 64 rows a chunk, 65-66 rows a CTA).  Exact block sums and outputs
     on sampled rows."""
